@@ -1,0 +1,189 @@
+"""Scheduler references — test infrastructure only.
+
+1. ``Reference`` — the fill / gather / fold loop of "Fat-station continuous
+   batching" ("Components", item 3) with the decode-first, bounded-prefill
+   policy of "DGR-012 — Continuous batching and bounded admission"
+   ("Summary": in-flight decodes run first, prefill per tick is capped but at
+   least one). Readings (the pages leave them open):
+     * fill: at the start of a step each free lane, in lane-index order, takes
+       the next pending job (FIFO by arrival); a lane freed in step t is
+       refilled at the start of step t+1;
+     * gather: a prompt is fed one token per step through the batched step;
+       every lane past its prompt is included; prompt-phase lanes are added
+       oldest-admitted first until max_prefill_tokens_per_tick tokens
+       (at least one);
+     * fold: the step that consumes the last prompt token yields the first
+       generated token; a job retires at max_new_tokens or on its stop id;
+     * sampling of a job's t-th generated token uses (seed, counter = t),
+       so a job's tokens do not depend on its lane, step or neighbours.
+   ``step_fn(lanes, positions, tokens) -> logits[n, V]`` is the engine
+   (the oracle model, or anything with the decode_step_batch contract);
+   ``sample_fn(logits_row, temp, seed, counter) -> token``.
+
+2. ``tick_sweep`` — the model-free tick model of the DGR-012 concurrency sweep
+   ("Concurrency 1/2/4/8 sweep"): a whole-prompt prefill takes one tick and
+   yields the first token, at most one prefill per tick, the active cap is
+   the concurrency level, decode runs before prefill, and a slot retired in
+   tick t is reusable in tick t+1.
+"""
+from __future__ import annotations
+
+from collections import deque
+
+
+class Reference:
+    def __init__(self, n_lanes: int, max_prefill_tokens_per_tick: int,
+                 step_fn, sample_fn, reset_fn=None):
+        self.n_lanes = n_lanes
+        self.budget = max(1, int(max_prefill_tokens_per_tick))
+        self.step_fn = step_fn
+        self.sample_fn = sample_fn
+        self.reset_fn = reset_fn
+        self.pending = deque()
+        self.lanes = [None] * n_lanes
+        self.positions = [0] * n_lanes
+        self.done = {}
+        self.admit_seq = 0
+        self.steps = 0
+        self.occupancy = []
+        self.prefill_tokens = 0
+        self.decode_tokens = 0
+        self.prefill_per_step = []
+
+    def submit(self, job: dict) -> None:
+        """job: id, prompt (len >= 1), max_new (>= 1), temperature, seed,
+        optional stop."""
+        self.pending.append(job)
+
+    def idle(self) -> bool:
+        return not self.pending and all(l is None for l in self.lanes)
+
+    def _fill(self) -> None:
+        for k in range(self.n_lanes):
+            if self.lanes[k] is None and self.pending:
+                job = self.pending.popleft()
+                if self.reset_fn:
+                    self.reset_fn(k)
+                self.positions[k] = 0
+                self.lanes[k] = dict(job=job, feed=0, gen=[], last=None,
+                                     seq=self.admit_seq)
+                self.admit_seq += 1
+
+    def step(self):
+        """One scheduler step; returns the list of job ids retired."""
+        self._fill()
+        decode = [k for k in range(self.n_lanes) if self.lanes[k] is not None
+                  and self.lanes[k]["feed"] >= len(self.lanes[k]["job"]["prompt"])]
+        prompt = [k for k in range(self.n_lanes) if self.lanes[k] is not None
+                  and self.lanes[k]["feed"] < len(self.lanes[k]["job"]["prompt"])]
+        prompt.sort(key=lambda k: self.lanes[k]["seq"])
+        chosen = set(decode) | set(prompt[:self.budget])
+        batch = sorted(chosen)
+        if not batch:
+            return []
+        toks, poss = [], []
+        for k in batch:
+            ln = self.lanes[k]
+            p = ln["job"]["prompt"]
+            toks.append(int(p[ln["feed"]]) if ln["feed"] < len(p) else ln["last"])
+            poss.append(self.positions[k])
+        logits = self.step_fn(batch, poss, toks)
+        self.steps += 1
+        self.occupancy.append(len(batch))
+        retired = []
+        self.prefill_per_step.append(
+            sum(1 for k in batch
+                if self.lanes[k]["feed"] < len(self.lanes[k]["job"]["prompt"])))
+        for i, k in enumerate(batch):
+            ln = self.lanes[k]
+            self.positions[k] += 1
+            job = ln["job"]
+            if ln["feed"] < len(job["prompt"]):
+                self.prefill_tokens += 1
+            else:
+                self.decode_tokens += 1
+            ln["feed"] += 1
+            if ln["feed"] < len(job["prompt"]):
+                continue
+            t = self.sample_fn(logits[i], job["temperature"], job["seed"],
+                               len(ln["gen"]))
+            ln["gen"].append(int(t))
+            ln["last"] = int(t)
+            stop = job.get("stop")
+            if len(ln["gen"]) >= job["max_new"] or (stop is not None
+                                                    and t == stop):
+                self.done[job["id"]] = list(ln["gen"])
+                self.lanes[k] = None
+                retired.append(job["id"])
+        return retired
+
+    def run(self, jobs, max_steps: int = 10**7) -> dict:
+        """Run jobs with ``arrive`` ticks (0 if absent) to completion."""
+        order = sorted(jobs, key=lambda j: (j.get("arrive", 0), j["id"]))
+        i = 0
+        tick = 0
+        while (i < len(order) or not self.idle()) and tick < max_steps:
+            while i < len(order) and order[i].get("arrive", 0) <= tick:
+                self.submit(order[i])
+                i += 1
+            self.step()
+            tick += 1
+        return self.done
+
+
+def serial_job(job: dict, step_fn, sample_fn, reset_fn=None, lane: int = 0):
+    """One job alone on one lane: the per-job reference of the parity gate."""
+    if reset_fn:
+        reset_fn(lane)
+    pos = 0
+    out = []
+    logits = None
+    for t in job["prompt"]:
+        logits = step_fn([lane], [pos], [int(t)])
+        pos += 1
+    while True:
+        tok = int(sample_fn(logits[0], job["temperature"], job["seed"],
+                            len(out)))
+        out.append(tok)
+        stop = job.get("stop")
+        if len(out) >= job["max_new"] or (stop is not None and tok == stop):
+            return out
+        logits = step_fn([lane], [pos], [tok])
+        pos += 1
+
+
+def tick_sweep(concurrency: int, n_sessions: int = 8, prompt_len: int = 4,
+               new_tokens: int = 8, max_prefill_per_tick: int = 1) -> dict:
+    """Model-free tick simulation of the DGR-012 sweep."""
+    pending = deque(range(n_sessions))
+    active = {}  # session -> generated tokens so far
+    ticks = 0
+    occ = []
+    while pending or active:
+        ticks += 1
+        retired = []
+        decoders = sorted(active)
+        if decoders:
+            occ.append(len(decoders))
+        for s in decoders:
+            active[s] += 1
+            if active[s] >= new_tokens:
+                retired.append(s)
+        started = []
+        n_pref = 0
+        while (pending and len(active) + len(started) < concurrency
+               and n_pref < max_prefill_per_tick):
+            s = pending.popleft()
+            started.append(s)
+            n_pref += 1
+        for s in retired:
+            del active[s]  # slot reusable from the next tick on
+        for s in started:
+            active[s] = 1  # the prefill tick yields the first token
+            if new_tokens <= 1:
+                del active[s]
+    total = n_sessions * prompt_len + n_sessions * (new_tokens - 1)
+    return dict(ticks=ticks,
+                avg_occupancy=(sum(occ) / len(occ)) if occ else 0.0,
+                max_occupancy=max(occ) if occ else 0,
+                tokens_per_tick=total / ticks)

@@ -1,0 +1,135 @@
+"""Pins of the scheduler and page-allocator references."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle.core as O
+from oracle import pages as P
+from oracle import sched as S
+from continuous_transformer_decode_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_dgr012_concurrency_sweep_replay():
+    g = json.load(open(os.path.join(GOLDEN, "dgr012_concurrency_sweep.json")))
+    for row in g["rows"]:
+        r = S.tick_sweep(row["concurrency"], g["sessions"], g["prompt_len"],
+                         g["new_tokens"])
+        assert r["ticks"] == row["ticks"]
+        assert round(r["avg_occupancy"], 3) == row["avg_occupancy"]
+        assert r["max_occupancy"] == row["max_occupancy"]
+        assert round(r["tokens_per_tick"], 3) == row["tokens_per_tick"]
+    tot = g["total_tokens"]
+    assert g["sessions"] * (g["new_tokens"] - 1) == tot["decode"]
+    assert g["sessions"] * g["prompt_len"] == tot["prefill"]
+
+
+def test_page_model_lowest_free_and_counts():
+    pm = P.PageModel(n_pages=8, page_size=4, max_lanes=3, max_pages_per_lane=4)
+    assert pm.step([0, 1], [0, 0], [1, 1], 10) == P.OK
+    assert pm.table(0) == [0] and pm.table(1) == [1]
+    for p in range(1, 9):
+        assert pm.step([1], [p], [1], 10) == P.OK
+    assert pm.table(1) == [1, 2, 3]  # lengths 9 -> ceil(9/4) = 3 pages
+    assert pm.reset(0) == P.OK
+    assert pm.step([2], [0], [1], 10) == P.OK
+    assert pm.table(2) == [0]  # lowest free index reused
+    for k in range(3):
+        assert len(pm.table(k)) == -(-pm.length[k] // 4)
+
+
+def test_page_model_errors_are_atomic():
+    pm = P.PageModel(n_pages=2, page_size=2, max_lanes=4, max_pages_per_lane=8)
+    assert pm.step([0, 1], [0, 0], [0, 0], 5) == P.OK
+    snap = ([list(t) for t in pm.tables], list(pm.length), sorted(pm.free))
+    assert pm.step([0, 0], [1, 1], [0, 0], 5) == P.ERR_DUP_LANE
+    assert pm.step([0], [0], [0], 5) == P.ERR_POSITION
+    assert pm.step([0], [1], [5], 5) == P.ERR_TOKEN
+    assert pm.step([4], [0], [0], 5) == P.ERR_LANE
+    assert pm.step([2], [0], [0], 5) == P.ERR_KV_FULL  # pool exhausted
+    assert ([list(t) for t in pm.tables], list(pm.length), sorted(pm.free)) == snap
+
+
+@pytest.fixture(scope="module")
+def tiny_engine():
+    cfg = synth.MODEL_T
+    m = O.Model(cfg, synth.make_weights(cfg, seed=1, fmt="f32"), O.F32)
+    return cfg, m
+
+
+def _engine(m, n_lanes, max_pos=96):
+    lanes = [m.lane(max_pos) for _ in range(n_lanes)]
+
+    def step_fn(ks, poss, toks):
+        for k, p in zip(ks, poss):
+            assert lanes[k].pos == p
+        return m.step_batch([lanes[k] for k in ks], toks)
+
+    def reset_fn(k):
+        lanes[k].reset()
+
+    def sample_fn(row, temp, seed, counter):
+        return O.sample(row, temp, seed, counter)
+    return step_fn, reset_fn, sample_fn
+
+
+def test_scheduler_reference_per_job_equals_serial(tiny_engine):
+    cfg, m = tiny_engine
+    g = np.random.default_rng(4)
+    jobs = []
+    for j in range(10):
+        jobs.append(dict(id=j, arrive=int(g.integers(0, 12)),
+                         prompt=synth.make_prompts(1, int(g.integers(1, 9)),
+                                                   cfg["V"], seed=100 + j)[0],
+                         max_new=int(g.integers(1, 10)),
+                         temperature=0.0 if j % 2 else 0.8, seed=1000 + j))
+    step_fn, reset_fn, sample_fn = _engine(m, 3)
+    ref = S.Reference(3, 2, step_fn, sample_fn, reset_fn)
+    done = ref.run(jobs)
+    assert sorted(done) == list(range(10))
+    s_step, s_reset, s_sample = _engine(m, 1)
+    for job in jobs:
+        solo = S.serial_job(job, s_step, s_sample, s_reset)
+        assert done[job["id"]] == solo, job["id"]
+        assert len(solo) == job["max_new"]
+    assert max(ref.occupancy) <= 3
+    assert ref.prefill_tokens == sum(len(j["prompt"]) for j in jobs)
+    assert ref.decode_tokens == sum(j["max_new"] - 1 for j in jobs)
+
+
+def test_scheduler_reference_decode_first_bounded_prefill(tiny_engine):
+    cfg, m = tiny_engine
+    seen = []
+    step_fn, reset_fn, sample_fn = _engine(m, 4)
+
+    def spy(ks, poss, toks):
+        seen.append(list(ks))
+        return step_fn(ks, poss, toks)
+    ref = S.Reference(4, 1, spy, sample_fn, reset_fn)
+    ref.submit(dict(id=0, prompt=[1], max_new=12, temperature=0.0, seed=0))
+    ref.step()  # lane 0 consumes its one prompt token -> decoding from now on
+    for j in range(1, 4):
+        ref.submit(dict(id=j, prompt=[2, 3, 4, 5], max_new=2,
+                        temperature=0.0, seed=0))
+    for _ in range(6):
+        ref.step()
+    for ks in seen[1:]:
+        assert 0 in ks            # the in-flight decode runs every step
+    assert max(ref.prefill_per_step) == 1  # at most one prompt token per step
+    assert sum(ref.prefill_per_step) == 1 + 6  # budget used on every step
+
+
+def test_scheduler_reference_stop_id_and_lane_reuse(tiny_engine):
+    cfg, m = tiny_engine
+    step_fn, reset_fn, sample_fn = _engine(m, 1)
+    job = dict(id=0, prompt=[7, 8], max_new=20, temperature=0.0, seed=0)
+    full = S.serial_job(job, step_fn, sample_fn, reset_fn)
+    stop = full[3]
+    first = full.index(stop)
+    ref = S.Reference(1, 1, step_fn, sample_fn, reset_fn)
+    done = ref.run([dict(job, stop=stop), dict(job, id=1, arrive=0)])
+    assert done[0] == full[:first + 1]  # retired on the stop id
+    assert done[1] == full              # the freed lane serves the next job
