@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of decode_step_batch: aggregate decode tokens/s and roofline.
+
+One step = one fs_decode_step_batch over B lanes (embed, all layers, final
+norm, LM head) plus the per-lane sampler. Default workload: the
+SmolLM2-135M-shaped model with bf16 random weights N(0, 0.02), B = 256
+lanes, 16-token uniform random prompts ingested before timing, then decode
+steps (the workload of MODEL-BATCHING-RESULTS, "Measured": 16-token
+prompts, 12 decode steps; the B sweep there tops out at 256 for this shape).
+
+  value      device time (CUDA events on the handle's stream) of K steps,
+             inputs resident on the device; tokens/s = B * K / time.
+  e2e        the same K steps through the host API: host arrays in
+             (fs_decode_step_batch), host tokens out (fs_sample), timed with
+             the host clock including every copy.
+  roofline   the weight-streaming GEMM (dominant kernel class): algorithmic
+             bytes per launch / mean launch time, from CUDA events around
+             each launch in a profiled pass of K steps identical to the timed
+             one, against the measured HBM copy bandwidth.
+  cpu_baseline  the C++ f32 oracle (StepBatch) on this host's cores over a
+             bounded sample of the same workload.
+
+Multi-GPU (torchrun): replicas, one per GPU, no collective on the data path;
+value = all ranks' tokens / max over ranks of the time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "smollm2-135m-bf16": dict(model="S", wdtype="bf16", B=256, prompt=16),
+    "smollm2-135m-q8_0": dict(model="S", wdtype="q8_0", B=960, prompt=16),
+    "mistral-7b-bf16": dict(model="M", wdtype="bf16", B=128, ctx=(128, 4096)),
+}
+METRIC = "aggregate decode tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"],
+                    bf16_sus=j.get("bf16_tflops_sustained"), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during timing."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.p = None
+        self.out = os.path.join("/tmp", f"fs_clocks_{os.getpid()}.csv")
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id],
+                stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        rows = []
+        for line in open(self.out):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.out)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[2 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def model_cfg(name):
+    from continuous_transformer_decode_gb300 import synth
+    return {"S": synth.MODEL_S, "M": synth.MODEL_M, "T": synth.MODEL_T}[name]
+
+
+def gpu_weights(cfg, wdtype, seed=1):
+    """Random-init weights. bf16: N(0, 0.02) drawn on the host (seeded);
+    q8_0: the same bf16 values quantised on the device by the library."""
+    import torch
+    from continuous_transformer_decode_gb300 import fs, synth
+    W = synth.make_weights(cfg, seed=seed, fmt="bf16")
+    if wdtype == "bf16":
+        return W, fs.FS_DTYPE_BF16
+
+    def q(a):
+        x = torch.from_numpy(synth.bf16_to_f32(a).reshape(-1)).cuda()
+        out = torch.empty((x.numel() // 32, 34), dtype=torch.uint8, device="cuda")
+        fs.fs_quantize_q8_0(x, out)
+        return out
+    Q = {"embed": q(W["embed"]), "lm_head": None if W["lm_head"] is None else q(W["lm_head"]),
+         "final_norm": W["final_norm"],
+         "layers": [{k: (v if k in ("attn_norm", "ffn_norm") else q(v))
+                     for k, v in ly.items()} for ly in W["layers"]]}
+    return Q, fs.FS_DTYPE_Q8_0
+
+
+def run_ours(args, wl, ws, rank, local):
+    import torch
+    from continuous_transformer_decode_gb300 import build, fs, synth
+    build.build()
+    torch.cuda.set_device(local)
+    cfg = model_cfg(wl["model"])
+    B = args.batch or wl["B"]
+    K, Wm = args.steps, args.warmup
+    prompt = wl.get("prompt", 0)
+    if "ctx" in wl:
+        ctx = synth.make_context_lengths(B, *wl["ctx"], seed=3)
+    else:
+        ctx = np.full(B, prompt, dtype=np.int32)
+    extra = Wm + 3 * K + 8  # warm-up, timed, profiled and end-to-end steps
+    max_pos = int(ctx.max()) + extra
+    ps = 16
+    n_pages = int(sum(-(-(int(c) + extra) // ps) for c in ctx)) + B
+    Wt, wdt = gpu_weights(cfg, wl["wdtype"])
+    desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps)
+    h = fs.fs_create(desc, Wt)
+    del Wt
+    stream = torch.cuda.current_stream()
+    fs.fs_set_stream(h, stream)
+    lanes = np.arange(B, dtype=np.int32)
+    if "ctx" in wl:  # long synthetic contexts: random KV (content irrelevant)
+        for b in range(B):
+            fs.fs_lane_fill_random_kv(h, b, int(ctx[b]), 1000 + b)
+        pos = ctx.astype(np.int32).copy()
+        toks = np.array([p[0] for p in synth.make_prompts(B, 1, cfg["V"], seed=2)], np.int32)
+    else:  # prompt ingestion, one token per lane per step, outside timing
+        prompts = np.stack(synth.make_prompts(B, prompt, cfg["V"], seed=2))
+        pos = np.zeros(B, dtype=np.int32)
+        for t in range(prompt):
+            fs.fs_decode_step_batch(h, lanes, pos, prompts[:, t])
+        toks = prompts[:, -1].astype(np.int32).copy()
+    temps = torch.zeros(B, dtype=torch.float32, device="cuda")
+    seeds = torch.arange(B, dtype=torch.int64, device="cuda")
+    ctrs = torch.zeros(B, dtype=torch.int64, device="cuda")
+    dtok = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def device_step():
+        fs.fs_decode_step_batch(h, lanes, pos, toks)
+        fs.fs_sample_device(h, temps, seeds, ctrs, dtok)
+
+    for _ in range(Wm):
+        device_step()
+    torch.cuda.synchronize()
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid) \
+        if hasattr(torch.cuda.get_device_properties(local), "uuid") else str(local)
+    if gpu_id.startswith("GPU-GPU-"):
+        gpu_id = gpu_id[4:]
+    clocks = Clocks(gpu_id)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    l0 = fs.fs_kernel_launches(h)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        device_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    launches = fs.fs_kernel_launches(h) - l0
+    clk = clocks.stop()
+
+    # profiled pass: identical steps, CUDA events around every launch
+    fs.fs_profile_enable(h, True)
+    for c in range(3):
+        fs.fs_profile_read(h, c)
+    for _ in range(K):
+        device_step()
+    prof = {c: fs.fs_profile_read(h, c) for c in (fs.FS_PROF_GEMM, fs.FS_PROF_ATTN,
+                                                  fs.FS_PROF_OTHER)}
+    fs.fs_profile_enable(h, False)
+
+    # end to end through the host API
+    tk = torch.cuda.current_stream()
+    hsteps = K
+    temps_h = np.zeros(B, np.float32)
+    seeds_h = np.arange(B, dtype=np.uint64)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    htoks = toks.copy()
+    for i in range(hsteps):
+        fs.fs_decode_step_batch(h, lanes, pos, htoks)
+        htoks = fs.fs_sample(h, temps_h, seeds_h, np.full(B, i, np.uint64))
+    tk.synchronize()
+    e2e_s = time.perf_counter() - t0
+    fs.fs_destroy(h)
+
+    # ---- aggregate over ranks (max time)
+    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_s = float(t[0]), float(t[1])
+    total_tokens = B * K * ws
+    value = total_tokens / (ms / 1e3)
+    peaks = _peaks()
+    g_ms, g_n, g_bytes = prof[fs.FS_PROF_GEMM]
+    achieved = (g_bytes / g_n) / (g_ms / g_n / 1e3) / 1e9 if g_n else None
+    roof = {"kernel": "weight-streaming GEMM (" + fs_path_name(cfg, wdt) + ")",
+            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": (achieved / peaks["hbm"]) if achieved else None,
+            "traffic": None, "peak_source": peaks["src"],
+            "launches": g_n, "mean_launch_us": (g_ms / g_n * 1e3) if g_n else None,
+            "algorithmic_bytes_per_launch": (g_bytes / g_n) if g_n else None,
+            "share_of_step": {"gemm": g_ms, "attention": prof[fs.FS_PROF_ATTN][0],
+                              "other": prof[fs.FS_PROF_OTHER][0]}}
+    arg_bytes = (7 * B + 1) * 4
+    e2e = {"value": total_tokens / e2e_s, "unit": "tok/s",
+           "h2d_bytes_per_step": arg_bytes + B * (4 + 8 + 8),
+           "d2h_bytes_per_step": B * 4}
+    return dict(value=value, ms=ms, B=B, launches=launches, clocks=clk, roofline=roof,
+                e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt)
+
+
+def fs_path_name(cfg, wdt):
+    return {0: "f32", 1: "bf16", 2: "q8_0"}[wdt] + " weights"
+
+
+class OracleArm:
+    """The oracle as it stands, on this host's cores: StepBatch over a bounded
+    number of the workload's lanes (up to 32), after seeding each lane with
+    the workload's context as random KV (content does not change the work)."""
+
+    def __init__(self, wl, B, max_steps=64):
+        import oracle.core as O
+        from continuous_transformer_decode_gb300 import synth
+        cfg = model_cfg(wl["model"])
+        self.scale = 1.0
+        if wl["model"] == "M":  # bounded: 2 of 32 layers, scaled by work share
+            full = cfg
+            cfg = synth.with_layers(cfg, 2)
+            per_layer = (cfg["H"] * cfg["hd"] * 2 + cfg["Hkv"] * cfg["hd"] * 2) * cfg["d"] \
+                + 3 * cfg["F"] * cfg["d"]
+            head = cfg["V"] * cfg["d"]
+            self.scale = (2 * per_layer + head) / (full["L"] * per_layer + head)
+        self.cores = os.cpu_count() or 1
+        O.set_threads(self.cores)
+        W = synth.make_weights(cfg, seed=1, fmt="bf16")
+        if wl["wdtype"] == "q8_0":
+            q = lambda a: O.quantize_q8_0(synth.bf16_to_f32(a))
+            W = {"embed": q(W["embed"]),
+                 "lm_head": None if W["lm_head"] is None else q(W["lm_head"]),
+                 "final_norm": W["final_norm"],
+                 "layers": [{k: (v if k in ("attn_norm", "ffn_norm") else q(v))
+                             for k, v in ly.items()} for ly in W["layers"]]}
+            self.m = O.Model(cfg, W, O.Q8_0)
+        else:
+            self.m = O.Model(cfg, W, O.BF16)
+        del W
+        self.nb = min(B, 32)
+        self.B = B
+        self.ctx = wl.get("prompt", 16) if "ctx" not in wl else 1024
+        self.lanes = [self.m.lane(self.ctx + max_steps + 2) for _ in range(self.nb)]
+        for b, ln in enumerate(self.lanes):
+            for l in range(cfg["L"]):
+                K, V = synth.make_kv(self.ctx, cfg["Hkv"], cfg["hd"], seed=9, path=(b, l))
+                ln.import_kv(l, K, V)
+        self.L = cfg["L"]
+        self.steps = 0
+        self.seconds = 0.0
+
+    def step(self) -> float:
+        t0 = time.perf_counter()
+        self.m.step_batch(self.lanes, [1] * self.nb)
+        dt = time.perf_counter() - t0
+        self.steps += 1
+        self.seconds += dt
+        return self.nb / dt * self.scale
+
+    def describe(self, value):
+        return {"value": value, "unit": "tok/s", "cores": self.cores, "kind": "oracle",
+                "sample": f"oracle StepBatch over {self.nb} of {self.B} lanes, "
+                          f"{self.steps} steps after {self.ctx} tokens of context, "
+                          f"{self.L} layers" + (" (scaled to the full depth by weight share)"
+                                                if self.scale != 1.0 else "")}
+
+
+def cpu_baseline(wl, B, seconds=15.0):
+    arm = OracleArm(wl, B)
+    vals = []
+    while not vals or (arm.seconds < seconds and arm.steps < 48):
+        vals.append(arm.step())
+    return arm.describe(arm.nb * arm.steps / arm.seconds * arm.scale)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=12)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="smollm2-135m-bf16", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    ws, rank, local = _dist()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        B = args.batch or wl["B"]
+        arm = OracleArm(wl, B, max_steps=args.warmup + args.steps + 2)
+        for _ in range(args.warmup):
+            arm.step()
+        arm.steps, arm.seconds = 0, 0.0
+        for _ in range(args.steps):
+            arm.step()
+        v = arm.nb * arm.steps / arm.seconds * arm.scale
+        cb = arm.describe(v)
+        print(json.dumps({"metric": METRIC, "value": v, "unit": "tok/s", "impl": "reference",
+                          "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f32", "data": "synthetic",
+                          "config": {"workload": args.workload, "lanes": B},
+                          "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+
+    if ws > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    r = run_ours(args, wl, ws, rank, local)
+    if rank != 0:
+        if ws > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
+    cb = None if args.no_cpu_baseline else cpu_baseline(wl, r["B"])
+    cfg = r["cfg"]
+    wbytes = {"bf16": 2, "q8_0": 34 / 32}[wl["wdtype"]]
+    n_par = cfg["V"] * cfg["d"] * (1 if cfg["tied"] else 2) + cfg["L"] * (
+        (cfg["H"] * cfg["hd"] * 2 + cfg["Hkv"] * cfg["hd"] * 2) * cfg["d"] + 3 * cfg["F"] * cfg["d"])
+    weight_mb = n_par * wbytes / 1e6
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "tok/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl["wdtype"], "data": "synthetic (random N(0,0.02) weights, uniform prompts)",
+        "config": {"workload": args.workload, "model_shape": cfg["name"], "lanes": r["B"],
+                   "layers": cfg["L"], "d": cfg["d"], "vocab": cfg["V"],
+                   "context": (f"16-token prompts, positions 16..{16 + args.warmup + args.steps}"
+                               if "ctx" not in wl else
+                               f"ctx U[{wl['ctx'][0]},{wl['ctx'][1]}] mean {float(np.mean(r['ctx'])):.0f}"),
+                   "l2": f"no flush: inputs larger than L2 ({weight_mb:.0f} MB of weights "
+                         "streamed per step vs 129 MB L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+        "clocks": r["clocks"], "gpu_launches": r["launches"],
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

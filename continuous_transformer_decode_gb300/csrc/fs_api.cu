@@ -1,0 +1,783 @@
+// Host side of the C ABI (include/fs.h): descriptor validation, weight
+// upload and re-layout, the paged KV arena and its page allocator, and the
+// orchestration of one decode_step_batch call as a sequence of kernels on
+// the handle's stream.
+//
+// The step follows "Fat-station continuous batching" ("The capture"): the
+// caller passes, per lane, its position and the token it consumes; the call
+// appends that token's K/V to the lane's cache, returns its logits and
+// advances the position. Validation and page allocation happen before any
+// launch, so an invalid call changes nothing.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "../../include/fs.h"
+#include "fs_internal.h"
+
+using namespace fsk;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct LayerW {
+  Mat qkv, o, gateup, down;
+  float* g_attn = nullptr;
+  float* g_ffn = nullptr;
+};
+
+}  // namespace
+
+struct fs_handle {
+  fs_model_desc d{};
+  int wtype = W_BF16;
+  int xtype = X_BF16;
+  int Kp_d = 0, Kp_q = 0, Kp_f = 0;
+  int Nq = 0, Nkv = 0, Nqkv = 0;
+  int G = 1;
+  int split_len = 256, max_splits = 1;
+  int max_pages_per_lane = 0;
+
+  std::vector<LayerW> layers;
+  Mat embed, head;
+  float* g_final = nullptr;
+  std::vector<void*> allocs;  // every cudaMalloc of the handle
+
+  KV kv;
+  std::vector<std::vector<int32_t>> pt;  // host page tables
+  std::vector<int32_t> len;              // lane lengths
+  std::set<int32_t> free_pages;
+
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+
+  float* x = nullptr;
+  void* hpanel = nullptr;
+  void* opanel = nullptr;
+  void* apanel = nullptr;
+  float* qkv = nullptr;
+  float* q = nullptr;
+  float* logits = nullptr;
+  float* part_ml = nullptr;
+  float* part_acc = nullptr;
+
+  int32_t* d_args = nullptr;  // [7 * max_lanes + 1]
+  int32_t* h_args = nullptr;  // pinned staging
+  StepArgs args{};
+  cudaEvent_t args_done = nullptr;
+
+  float* d_temps = nullptr;
+  uint64_t* d_seeds = nullptr;
+  uint64_t* d_counters = nullptr;
+  int32_t* d_tokens = nullptr;
+  unsigned char* h_samp = nullptr;  // pinned staging for sampler I/O
+
+  cudaStream_t own_stream = nullptr;
+  cudaStream_t stream = nullptr;
+
+  int last_n = -1;
+  const float* last_logits = nullptr;
+  int64_t launches = 0;
+  std::string err;
+
+  // event profiler (fs_profile_enable / fs_profile_read)
+  struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+    double bytes;
+  };
+  bool prof_on = false;
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> prof_pool;
+  double prof_ms[FS_PROF_CLASSES] = {0, 0, 0};
+  double prof_bytes[FS_PROF_CLASSES] = {0, 0, 0};
+  int64_t prof_n[FS_PROF_CLASSES] = {0, 0, 0};
+
+  cudaEvent_t prof_event() {
+    if (!prof_pool.empty()) {
+      cudaEvent_t e = prof_pool.back();
+      prof_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  // Launches through `fn` (returns the kernel count) with optional timing.
+  template <typename Fn>
+  void launch(int cls, double bytes, Fn fn) {
+    if (!prof_on) {
+      launches += fn();
+      return;
+    }
+    cudaEvent_t a = prof_event(), b = prof_event();
+    cudaEventRecord(a, stream);
+    launches += fn();
+    cudaEventRecord(b, stream);
+    prof_pending.push_back({cls, a, b, bytes});
+  }
+
+  int fail(int code, const std::string& msg) {
+    err = msg;
+    return code;
+  }
+  int cuda_fail(cudaError_t e, const char* what) {
+    err = std::string(what) + ": " + cudaGetErrorString(e);
+    return FS_ERR_CUDA;
+  }
+  template <typename T>
+  cudaError_t alloc(T** p, size_t bytes) {
+    void* v = nullptr;
+    cudaError_t e = cudaMalloc(&v, bytes ? bytes : 16);
+    if (e == cudaSuccess) {
+      allocs.push_back(v);
+      *p = static_cast<T*>(v);
+    }
+    return e;
+  }
+};
+
+#define FS_CK(h, call)                                   \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return (h)->cuda_fail(e_, #call); \
+  } while (0)
+
+namespace {
+
+size_t elem_bytes(int wtype) { return wtype == W_F32 ? 4 : (wtype == W_BF16 ? 2 : 1); }
+
+// Allocates a device matrix of N rows in the library layout.
+int alloc_mat(fs_handle* h, Mat* m, int N, int K) {
+  m->N = N;
+  m->K = K;
+  m->Kp = (int)round_up(K, 64);
+  m->wtype = h->wtype;
+  void* w = nullptr;
+  const size_t bytes = (size_t)N * m->Kp * elem_bytes(h->wtype);
+  if (h->alloc(&w, bytes) != cudaSuccess)
+    return h->fail(FS_ERR_OOM, "weight allocation failed");
+  FS_CK(h, cudaMemset(w, 0, bytes));
+  m->w = w;
+  if (h->wtype == W_Q8) {
+    __half* s = nullptr;
+    const size_t sb = (size_t)N * (m->Kp / 32) * sizeof(__half);
+    if (h->alloc(&s, sb) != cudaSuccess)
+      return h->fail(FS_ERR_OOM, "scale allocation failed");
+    FS_CK(h, cudaMemset(s, 0, sb));
+    m->scales = s;
+  }
+  return FS_OK;
+}
+
+// Copies a [rows, cols] source matrix (host or device, caller layout) into
+// rows [row_offset, row_offset + rows) of m.
+int upload_rows(fs_handle* h, Mat* m, const void* src, int rows, int cols,
+                int row_offset, uint8_t* staging) {
+  if (!src) return h->fail(FS_ERR_ARG, "missing weight pointer");
+  if (h->wtype == W_Q8) {
+    const size_t bytes = (size_t)rows * (cols / 32) * 34;
+    FS_CK(h, cudaMemcpy(staging, src, bytes, cudaMemcpyDefault));
+    h->launches += launch_repack_q8(staging, rows, cols, m->Kp,
+                                    (int8_t*)m->w, (__half*)m->scales,
+                                    row_offset, h->stream);
+    FS_CK(h, cudaGetLastError());
+    FS_CK(h, cudaStreamSynchronize(h->stream));
+    return FS_OK;
+  }
+  const size_t es = elem_bytes(h->wtype);
+  char* dst = (char*)m->w + (size_t)row_offset * m->Kp * es;
+  FS_CK(h, cudaMemcpy2D(dst, (size_t)m->Kp * es, src, (size_t)cols * es,
+                        (size_t)cols * es, rows, cudaMemcpyDefault));
+  return FS_OK;
+}
+
+int validate_desc(const fs_model_desc* d, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return FS_ERR_ARG;
+  };
+  if (d->n_layers < 1 || d->d_model < 1 || d->n_heads < 1 ||
+      d->n_kv_heads < 1 || d->head_dim < 2 || d->d_ffn < 1 || d->vocab < 1)
+    return bad("model dimensions must be positive");
+  if (d->n_heads % d->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+  if (d->n_heads / d->n_kv_heads > 8) return bad("at most 8 query heads per KV head");
+  if (d->head_dim % 2 || d->head_dim > 256) return bad("head_dim must be even and <= 256");
+  if (d->weight_dtype < 0 || d->weight_dtype > 2) return bad("unknown weight_dtype");
+  if (d->kv_dtype != FS_DTYPE_F32 && d->kv_dtype != FS_DTYPE_BF16)
+    return bad("kv_dtype must be F32 or BF16");
+  if (d->weight_dtype == FS_DTYPE_Q8_0 &&
+      (d->d_model % 32 || d->d_ffn % 32 || (d->n_heads * d->head_dim) % 32))
+    return bad("Q8_0 needs every input width to be a multiple of 32");
+  if (d->max_lanes < 1 || d->page_size < 1 || d->n_pages < 1 || d->max_pos < 1)
+    return bad("max_lanes, page_size, n_pages and max_pos must be positive");
+  if (!(d->rms_eps >= 0.0f) || !(d->rope_theta > 0.0)) return bad("bad rms_eps or rope_theta");
+  return FS_OK;
+}
+
+int create_impl(fs_handle* h, const fs_weights* W) {
+  const fs_model_desc& d = h->d;
+  h->wtype = d.weight_dtype == FS_DTYPE_F32 ? W_F32
+             : d.weight_dtype == FS_DTYPE_BF16 ? W_BF16 : W_Q8;
+  h->xtype = h->wtype == W_F32 ? X_F32 : X_BF16;
+  h->Nq = d.n_heads * d.head_dim;
+  h->Nkv = d.n_kv_heads * d.head_dim;
+  h->Nqkv = h->Nq + 2 * h->Nkv;
+  h->G = d.n_heads / d.n_kv_heads;
+  h->Kp_d = (int)round_up(d.d_model, 64);
+  h->Kp_q = (int)round_up(h->Nq, 64);
+  h->Kp_f = (int)round_up(d.d_ffn, 64);
+  h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
+  h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;
+
+  FS_CK(h, cudaStreamCreateWithFlags(&h->own_stream, cudaStreamNonBlocking));
+  h->stream = h->own_stream;
+  FS_CK(h, cudaEventCreateWithFlags(&h->args_done, cudaEventDisableTiming));
+
+  // ---- weights
+  size_t stage = 0;
+  if (h->wtype == W_Q8) {
+    auto blk = [](int64_t r, int64_t c) { return (size_t)(r * (c / 32) * 34); };
+    stage = std::max({blk(d.vocab, d.d_model), blk(d.d_ffn, d.d_model),
+                      blk(d.d_model, d.d_ffn), blk(h->Nq, d.d_model),
+                      blk(d.d_model, h->Nq)});
+  }
+  uint8_t* staging = nullptr;
+  if (stage) {
+    if (cudaMalloc(&staging, stage) != cudaSuccess)
+      return h->fail(FS_ERR_OOM, "staging allocation failed");
+  }
+  struct StageFree {
+    uint8_t* p;
+    ~StageFree() { if (p) cudaFree(p); }
+  } sf{staging};
+
+  if (!W || !W->embed || !W->final_norm || !W->layers)
+    return h->fail(FS_ERR_ARG, "missing weights");
+  if (!d.tied_embeddings && !W->lm_head)
+    return h->fail(FS_ERR_ARG, "lm_head is NULL but tied_embeddings == 0");
+  int rc;
+  if ((rc = alloc_mat(h, &h->embed, d.vocab, d.d_model))) return rc;
+  if ((rc = upload_rows(h, &h->embed, W->embed, d.vocab, d.d_model, 0, staging))) return rc;
+  if (d.tied_embeddings) {
+    h->head = h->embed;
+  } else {
+    if ((rc = alloc_mat(h, &h->head, d.vocab, d.d_model))) return rc;
+    if ((rc = upload_rows(h, &h->head, W->lm_head, d.vocab, d.d_model, 0, staging))) return rc;
+  }
+  auto upload_vec = [&](float** dst, const float* src, int n) -> int {
+    if (!src) return h->fail(FS_ERR_ARG, "missing norm gain");
+    if (h->alloc(dst, (size_t)n * 4) != cudaSuccess)
+      return h->fail(FS_ERR_OOM, "norm allocation failed");
+    FS_CK(h, cudaMemcpy(*dst, src, (size_t)n * 4, cudaMemcpyDefault));
+    return FS_OK;
+  };
+  if ((rc = upload_vec(&h->g_final, W->final_norm, d.d_model))) return rc;
+  h->layers.resize(d.n_layers);
+  for (int l = 0; l < d.n_layers; ++l) {
+    const fs_layer_weights& s = W->layers[l];
+    LayerW& L = h->layers[l];
+    if ((rc = alloc_mat(h, &L.qkv, h->Nqkv, d.d_model))) return rc;
+    if ((rc = upload_rows(h, &L.qkv, s.wq, h->Nq, d.d_model, 0, staging))) return rc;
+    if ((rc = upload_rows(h, &L.qkv, s.wk, h->Nkv, d.d_model, h->Nq, staging))) return rc;
+    if ((rc = upload_rows(h, &L.qkv, s.wv, h->Nkv, d.d_model, h->Nq + h->Nkv, staging))) return rc;
+    if ((rc = alloc_mat(h, &L.o, d.d_model, h->Nq))) return rc;
+    if ((rc = upload_rows(h, &L.o, s.wo, d.d_model, h->Nq, 0, staging))) return rc;
+    if ((rc = alloc_mat(h, &L.gateup, 2 * d.d_ffn, d.d_model))) return rc;
+    if ((rc = upload_rows(h, &L.gateup, s.w_gate, d.d_ffn, d.d_model, 0, staging))) return rc;
+    if ((rc = upload_rows(h, &L.gateup, s.w_up, d.d_ffn, d.d_model, d.d_ffn, staging))) return rc;
+    if ((rc = alloc_mat(h, &L.down, d.d_model, d.d_ffn))) return rc;
+    if ((rc = upload_rows(h, &L.down, s.w_down, d.d_model, d.d_ffn, 0, staging))) return rc;
+    if ((rc = upload_vec(&L.g_attn, s.attn_norm, d.d_model))) return rc;
+    if ((rc = upload_vec(&L.g_ffn, s.ffn_norm, d.d_model))) return rc;
+  }
+
+  // ---- KV arena
+  KV& kv = h->kv;
+  kv.kv_f32 = d.kv_dtype == FS_DTYPE_F32;
+  kv.Hkv = d.n_kv_heads;
+  kv.hd = d.head_dim;
+  kv.page_size = d.page_size;
+  kv.max_pages = h->max_pages_per_lane;
+  kv.layer_stride = (int64_t)d.n_pages * kv.Hkv * kv.page_size * kv.hd;
+  const size_t kv_bytes = (size_t)d.n_layers * kv.layer_stride * (kv.kv_f32 ? 4 : 2);
+  if (h->alloc(&kv.k, kv_bytes) != cudaSuccess || h->alloc(&kv.v, kv_bytes) != cudaSuccess)
+    return h->fail(FS_ERR_OOM, "KV arena allocation failed");
+  if (h->alloc(&kv.pt, (size_t)d.max_lanes * kv.max_pages * 4) != cudaSuccess)
+    return h->fail(FS_ERR_OOM, "page table allocation failed");
+  FS_CK(h, cudaMemset(kv.pt, 0, (size_t)d.max_lanes * kv.max_pages * 4));
+  h->pt.assign(d.max_lanes, {});
+  h->len.assign(d.max_lanes, 0);
+  for (int p = 0; p < d.n_pages; ++p) h->free_pages.insert(p);
+
+  // ---- RoPE tables: cos/sin of pos * theta^(-2i/hd), in double, to f32
+  {
+    const int half = d.head_dim / 2;
+    std::vector<float> c((size_t)d.max_pos * half), s((size_t)d.max_pos * half);
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow(d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
+      for (int p = 0; p < d.max_pos; ++p) {
+        const double a = (double)p * inv;
+        c[(size_t)p * half + i] = (float)std::cos(a);
+        s[(size_t)p * half + i] = (float)std::sin(a);
+      }
+    }
+    if (h->alloc(&h->rope_cos, c.size() * 4) != cudaSuccess ||
+        h->alloc(&h->rope_sin, s.size() * 4) != cudaSuccess)
+      return h->fail(FS_ERR_OOM, "rope table allocation failed");
+    FS_CK(h, cudaMemcpy(h->rope_cos, c.data(), c.size() * 4, cudaMemcpyHostToDevice));
+    FS_CK(h, cudaMemcpy(h->rope_sin, s.data(), s.size() * 4, cudaMemcpyHostToDevice));
+  }
+
+  // ---- scratch panels
+  const int B = d.max_lanes;
+  const size_t xs = h->xtype == X_F32 ? 4 : 2;
+  bool ok = h->alloc(&h->x, (size_t)B * d.d_model * 4) == cudaSuccess &&
+            h->alloc(&h->hpanel, (size_t)B * h->Kp_d * xs) == cudaSuccess &&
+            h->alloc(&h->opanel, (size_t)B * h->Kp_q * xs) == cudaSuccess &&
+            h->alloc(&h->apanel, (size_t)B * h->Kp_f * xs) == cudaSuccess &&
+            h->alloc(&h->qkv, (size_t)B * h->Nqkv * 4) == cudaSuccess &&
+            h->alloc(&h->q, (size_t)B * h->Nq * 4) == cudaSuccess &&
+            h->alloc(&h->logits, (size_t)B * d.vocab * 4) == cudaSuccess &&
+            h->alloc(&h->part_ml, (size_t)B * h->max_splits * d.n_heads * 2 * 4) == cudaSuccess &&
+            h->alloc(&h->part_acc, (size_t)B * h->max_splits * h->Nq * 4) == cudaSuccess &&
+            h->alloc(&h->d_args, (size_t)(7 * B + 1) * 4) == cudaSuccess &&
+            h->alloc(&h->d_temps, (size_t)B * 4) == cudaSuccess &&
+            h->alloc(&h->d_seeds, (size_t)B * 8) == cudaSuccess &&
+            h->alloc(&h->d_counters, (size_t)B * 8) == cudaSuccess &&
+            h->alloc(&h->d_tokens, (size_t)B * 4) == cudaSuccess;
+  if (!ok) return h->fail(FS_ERR_OOM, "scratch allocation failed");
+  FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
+  FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
+  FS_CK(h, cudaMemset(h->apanel, 0, (size_t)B * h->Kp_f * xs));
+  FS_CK(h, cudaHostAlloc((void**)&h->h_args, (size_t)(7 * B + 1) * 4, cudaHostAllocDefault));
+  FS_CK(h, cudaHostAlloc((void**)&h->h_samp, (size_t)B * 24, cudaHostAllocDefault));
+  int32_t* a = h->d_args;
+  h->args.lane = a;
+  h->args.pos = a + B;
+  h->args.tok = a + 2 * B;
+  h->args.upd_lane = a + 3 * B;
+  h->args.upd_slot = a + 4 * B;
+  h->args.upd_page = a + 5 * B;
+  h->args.n_upd = a + 7 * B;
+  FS_CK(h, cudaDeviceSynchronize());
+  return FS_OK;
+}
+
+void destroy_impl(fs_handle* h) {
+  if (h->stream) cudaStreamSynchronize(h->stream);
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+  if (h->h_args) cudaFreeHost(h->h_args);
+  if (h->h_samp) cudaFreeHost(h->h_samp);
+  if (h->args_done) cudaEventDestroy(h->args_done);
+  for (auto& r : h->prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
+  if (h->own_stream) cudaStreamDestroy(h->own_stream);
+}
+
+// Allocates pages for `n` more tokens of lane k starting at its current
+// length (lowest free index first). Caller has checked capacity.
+void take_pages(fs_handle* h, int k, int n_tokens_after) {
+  const int ps = h->d.page_size;
+  const int need = (n_tokens_after + ps - 1) / ps;
+  while ((int)h->pt[k].size() < need) {
+    const int p = *h->free_pages.begin();
+    h->free_pages.erase(h->free_pages.begin());
+    h->pt[k].push_back(p);
+  }
+}
+
+int seed_lane_pages(fs_handle* h, int lane, int n) {
+  if (lane < 0 || lane >= h->d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+  if (n < 0) return h->fail(FS_ERR_ARG, "negative token count");
+  if (h->len[lane] != 0) return h->fail(FS_ERR_STATE, "lane is not empty");
+  if (n > h->d.max_pos) return h->fail(FS_ERR_KV_FULL, "n exceeds max_pos");
+  const int need = (n + h->d.page_size - 1) / h->d.page_size;
+  if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  take_pages(h, lane, n);
+  h->len[lane] = n;
+  if (need)
+    FS_CK(h, cudaMemcpyAsync(h->kv.pt + (size_t)lane * h->kv.max_pages, h->pt[lane].data(),
+                             (size_t)need * 4, cudaMemcpyHostToDevice, h->stream));
+  return FS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fs_create(const fs_model_desc* desc, const fs_weights* weights, fs_handle** out) {
+  if (!desc || !out) {
+    g_create_error = "NULL descriptor or output pointer";
+    return FS_ERR_ARG;
+  }
+  *out = nullptr;
+  std::string why;
+  if (validate_desc(desc, &why)) {
+    g_create_error = why;
+    return FS_ERR_ARG;
+  }
+  fs_handle* h = new fs_handle();
+  h->d = *desc;
+  int rc = create_impl(h, weights);
+  if (rc) {
+    g_create_error = h->err;
+    destroy_impl(h);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return FS_OK;
+}
+
+int fs_destroy(fs_handle* h) {
+  if (!h) return FS_OK;
+  destroy_impl(h);
+  delete h;
+  return FS_OK;
+}
+
+const char* fs_last_error(const fs_handle* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int fs_set_stream(fs_handle* h, void* stream) {
+  if (!h) return FS_ERR_ARG;
+  FS_CK(h, cudaStreamSynchronize(h->stream));
+  h->stream = stream ? (cudaStream_t)stream : h->own_stream;
+  return FS_OK;
+}
+
+int fs_lane_reset(fs_handle* h, int32_t lane) {
+  if (!h) return FS_ERR_ARG;
+  if (lane < 0 || lane >= h->d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+  for (int32_t p : h->pt[lane]) h->free_pages.insert(p);
+  h->pt[lane].clear();
+  h->len[lane] = 0;
+  return FS_OK;
+}
+
+int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
+                         const int32_t* tokens, int32_t n, float* logits_out) {
+  if (!h) return FS_ERR_ARG;
+  if (n == 0) return FS_OK;
+  if (n < 0 || n > h->d.max_lanes) return h->fail(FS_ERR_ARG, "n outside [0, max_lanes]");
+  if (!lanes || !positions || !tokens) return h->fail(FS_ERR_ARG, "NULL argument array");
+  const fs_model_desc& d = h->d;
+  // ---- validate (no state change)
+  std::vector<char> seen(d.max_lanes, 0);
+  int need = 0;
+  for (int i = 0; i < n; ++i) {
+    const int k = lanes[i];
+    if (k < 0 || k >= d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+    if (seen[k]) return h->fail(FS_ERR_DUP_LANE, "lane appears twice in one step");
+    seen[k] = 1;
+    if (positions[i] != h->len[k]) return h->fail(FS_ERR_POSITION, "position differs from lane length");
+    if (tokens[i] < 0 || tokens[i] >= d.vocab) return h->fail(FS_ERR_TOKEN, "token outside [0, vocab)");
+    if (h->len[k] >= d.max_pos) return h->fail(FS_ERR_KV_FULL, "lane is at max_pos");
+    if (h->len[k] % d.page_size == 0) ++need;
+  }
+  if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+
+  // ---- commit: page allocation (input order, lowest free index first)
+  FS_CK(h, cudaEventSynchronize(h->args_done));  // staging no longer in use
+  const int B = d.max_lanes;
+  int32_t* A = h->h_args;
+  int n_upd = 0;
+  for (int i = 0; i < n; ++i) {
+    const int k = lanes[i];
+    A[i] = k;
+    A[B + i] = positions[i];
+    A[2 * B + i] = tokens[i];
+    if (h->len[k] % d.page_size == 0) {
+      take_pages(h, k, h->len[k] + 1);
+      A[3 * B + n_upd] = k;
+      A[4 * B + n_upd] = h->len[k] / d.page_size;
+      A[5 * B + n_upd] = h->pt[k].back();
+      ++n_upd;
+    }
+  }
+  A[7 * B] = n_upd;
+  // copy only the used prefix of each section: one copy of the whole block
+  // keeps this to a single H2D transfer per step
+  FS_CK(h, cudaMemcpyAsync(h->d_args, h->h_args, (size_t)(7 * B + 1) * 4,
+                           cudaMemcpyHostToDevice, h->stream));
+  FS_CK(h, cudaEventRecord(h->args_done, h->stream));
+
+  // ---- the step
+  cudaStream_t s = h->stream;
+  const StepArgs& args = h->args;
+  const double xs = h->xtype == X_F32 ? 4.0 : 2.0;
+  const double kvs = h->kv.kv_f32 ? 4.0 : 2.0;
+  auto wbytes = [&](const Mat& m) {
+    double b = (double)m.N * m.K * (m.wtype == W_F32 ? 4 : (m.wtype == W_BF16 ? 2 : 1));
+    if (m.wtype == W_Q8) b += (double)m.N * (m.K / 32) * 2;
+    return b;
+  };
+  // algorithmic bytes: weights once, activations in, outputs out
+  auto gemm = [&](const Mat& W, const void* X, int epi, float* of, void* ox, int ldo,
+                  int n_out) {
+    GemmArgs g{};
+    g.W = W; g.X = X; g.x_type = h->xtype; g.B = n; g.epi = epi;
+    g.out_f32 = of; g.out_x = ox; g.ldo = ldo; g.n_out = n_out;
+    double bytes = wbytes(W) + (double)n * W.K * xs;
+    bytes += epi == EPI_SWIGLU ? (double)n * n_out * xs
+             : (double)n * n_out * 4.0 * (epi == EPI_RESID ? 2 : 1);
+    h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemv(g, s); });
+  };
+  double kv_read = 0.0;  // K and V bytes attention reads per layer
+  for (int i = 0; i < n; ++i)
+    kv_read += (double)(h->len[lanes[i]] + 1) * h->Nkv * 2.0 * kvs;
+  const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
+  h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
+    return launch_embed(h->embed, args, n, n_upd, h->kv, h->x, d.d_model, s);
+  });
+  for (int l = 0; l < d.n_layers; ++l) {
+    const LayerW& W = h->layers[l];
+    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+      return launch_rmsnorm(h->x, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                            h->Kp_d, s);
+    });
+    gemm(W.qkv, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
+    h->launch(FS_PROF_OTHER,
+              (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
+                return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
+                                          h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
+              });
+    h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
+      return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
+                              h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
+                              h->Kp_q, s);
+    });
+    gemm(W.o, h->opanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
+    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+      return launch_rmsnorm(h->x, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                            h->Kp_d, s);
+    });
+    gemm(W.gateup, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f, d.d_ffn);
+    gemm(W.down, h->apanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
+  }
+  h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+    return launch_rmsnorm(h->x, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                          h->Kp_d, s);
+  });
+  float* out = logits_out ? logits_out : h->logits;
+  gemm(h->head, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  FS_CK(h, cudaGetLastError());
+
+  for (int i = 0; i < n; ++i) {
+    h->len[lanes[i]] += 1;
+    positions[i] += 1;
+  }
+  h->last_n = n;
+  h->last_logits = out;
+  return FS_OK;
+}
+
+int fs_sample(fs_handle* h, int32_t n, const float* temps, const uint64_t* seeds,
+              const uint64_t* counters, int32_t* tokens_out) {
+  if (!h) return FS_ERR_ARG;
+  if (h->last_n < 0) return h->fail(FS_ERR_STATE, "no decode step to sample from");
+  if (n != h->last_n) return h->fail(FS_ERR_STATE, "n differs from the last step's n");
+  if (!temps || !seeds || !counters || !tokens_out) return h->fail(FS_ERR_ARG, "NULL argument array");
+  for (int i = 0; i < n; ++i)
+    if (!(temps[i] >= 0.0f)) return h->fail(FS_ERR_ARG, "temperature must be >= 0");
+  const int B = h->d.max_lanes;
+  unsigned char* st = h->h_samp;
+  float* ht = (float*)st;
+  uint64_t* hs = (uint64_t*)(st + (size_t)B * 8);
+  uint64_t* hc = (uint64_t*)(st + (size_t)B * 16);
+  std::memcpy(ht, temps, (size_t)n * 4);
+  std::memcpy(hs, seeds, (size_t)n * 8);
+  std::memcpy(hc, counters, (size_t)n * 8);
+  cudaStream_t s = h->stream;
+  FS_CK(h, cudaMemcpyAsync(h->d_temps, ht, (size_t)n * 4, cudaMemcpyHostToDevice, s));
+  FS_CK(h, cudaMemcpyAsync(h->d_seeds, hs, (size_t)n * 8, cudaMemcpyHostToDevice, s));
+  FS_CK(h, cudaMemcpyAsync(h->d_counters, hc, (size_t)n * 8, cudaMemcpyHostToDevice, s));
+  h->launch(FS_PROF_OTHER, (double)n * h->d.vocab * 4.0, [&] {
+    return launch_sample(h->last_logits, n, h->d.vocab, h->d_temps, h->d_seeds,
+                         h->d_counters, h->d_tokens, s);
+  });
+  FS_CK(h, cudaGetLastError());
+  int32_t* ho = (int32_t*)(st);  // temps are consumed by now: reuse after sync
+  FS_CK(h, cudaStreamSynchronize(s));
+  FS_CK(h, cudaMemcpyAsync(ho, h->d_tokens, (size_t)n * 4, cudaMemcpyDeviceToHost, s));
+  FS_CK(h, cudaStreamSynchronize(s));
+  std::memcpy(tokens_out, ho, (size_t)n * 4);
+  return FS_OK;
+}
+
+int fs_sample_device(fs_handle* h, int32_t n, const float* temps, const uint64_t* seeds,
+                     const uint64_t* counters, int32_t* tokens_out) {
+  if (!h) return FS_ERR_ARG;
+  if (h->last_n < 0) return h->fail(FS_ERR_STATE, "no decode step to sample from");
+  if (n != h->last_n) return h->fail(FS_ERR_STATE, "n differs from the last step's n");
+  if (!temps || !seeds || !counters || !tokens_out) return h->fail(FS_ERR_ARG, "NULL argument array");
+  cudaStream_t s = h->stream;
+  h->launch(FS_PROF_OTHER, (double)n * h->d.vocab * 4.0, [&] {
+    return launch_sample(h->last_logits, n, h->d.vocab, temps, seeds, counters, tokens_out, s);
+  });
+  FS_CK(h, cudaGetLastError());
+  return FS_OK;
+}
+
+int fs_profile_enable(fs_handle* h, int32_t enable) {
+  if (!h) return FS_ERR_ARG;
+  h->prof_on = enable != 0;
+  return FS_OK;
+}
+
+int fs_profile_read(fs_handle* h, int32_t cls, double* ms_out, int64_t* launches_out,
+                    double* bytes_out) {
+  if (!h || cls < 0 || cls >= FS_PROF_CLASSES) return FS_ERR_ARG;
+  FS_CK(h, cudaStreamSynchronize(h->stream));
+  for (auto& r : h->prof_pending) {
+    float ms = 0.0f;
+    FS_CK(h, cudaEventElapsedTime(&ms, r.a, r.b));
+    h->prof_ms[r.cls] += ms;
+    h->prof_n[r.cls] += 1;
+    h->prof_bytes[r.cls] += r.bytes;
+    h->prof_pool.push_back(r.a);
+    h->prof_pool.push_back(r.b);
+  }
+  h->prof_pending.clear();
+  if (ms_out) *ms_out = h->prof_ms[cls];
+  if (launches_out) *launches_out = h->prof_n[cls];
+  if (bytes_out) *bytes_out = h->prof_bytes[cls];
+  h->prof_ms[cls] = 0.0;
+  h->prof_n[cls] = 0;
+  h->prof_bytes[cls] = 0.0;
+  return FS_OK;
+}
+
+int fs_lane_length(const fs_handle* h, int32_t lane, int32_t* length_out) {
+  if (!h || !length_out) return FS_ERR_ARG;
+  if (lane < 0 || lane >= h->d.max_lanes) return FS_ERR_LANE;
+  *length_out = h->len[lane];
+  return FS_OK;
+}
+
+int fs_lane_pages(const fs_handle* h, int32_t lane, int32_t* pages_out, int32_t cap,
+                  int32_t* n_out) {
+  if (!h || !n_out || cap < 0 || (cap > 0 && !pages_out)) return FS_ERR_ARG;
+  if (lane < 0 || lane >= h->d.max_lanes) return FS_ERR_LANE;
+  const auto& t = h->pt[lane];
+  for (int i = 0; i < (int)t.size() && i < cap; ++i) pages_out[i] = t[i];
+  *n_out = (int32_t)t.size();
+  return FS_OK;
+}
+
+int fs_lane_export_kv(fs_handle* h, int32_t lane, int32_t layer, float* k_out, float* v_out) {
+  if (!h || !k_out || !v_out) return FS_ERR_ARG;
+  if (lane < 0 || lane >= h->d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+  if (layer < 0 || layer >= h->d.n_layers) return h->fail(FS_ERR_ARG, "layer out of range");
+  const int n = h->len[lane];
+  if (n == 0) return FS_OK;
+  const size_t cnt = (size_t)n * h->kv.Hkv * h->kv.hd;
+  int32_t* dp = nullptr;
+  float *dk = nullptr, *dv = nullptr;
+  int rc = FS_OK;
+  if (cudaMalloc(&dp, h->pt[lane].size() * 4) != cudaSuccess ||
+      cudaMalloc(&dk, cnt * 4) != cudaSuccess || cudaMalloc(&dv, cnt * 4) != cudaSuccess) {
+    rc = h->fail(FS_ERR_OOM, "export buffers");
+  } else {
+    cudaError_t e = cudaMemcpyAsync(dp, h->pt[lane].data(), h->pt[lane].size() * 4,
+                                    cudaMemcpyHostToDevice, h->stream);
+    if (e == cudaSuccess) {
+      h->launches += launch_export_kv(h->kv, layer, dp, n, dk, dv, h->stream);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(k_out, dk, cnt * 4, cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(v_out, dv, cnt * 4, cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) rc = h->cuda_fail(e, "export_kv");
+  }
+  cudaFree(dp);
+  cudaFree(dk);
+  cudaFree(dv);
+  return rc;
+}
+
+int fs_lane_import_kv(fs_handle* h, int32_t lane, const float* k, const float* v, int32_t n) {
+  if (!h || (n > 0 && (!k || !v))) return FS_ERR_ARG;
+  int rc = seed_lane_pages(h, lane, n);
+  if (rc) return rc;
+  if (n == 0) return FS_OK;
+  const size_t cnt = (size_t)n * h->kv.Hkv * h->kv.hd;
+  int32_t* dp = nullptr;
+  float *dk = nullptr, *dv = nullptr;
+  if (cudaMalloc(&dp, h->pt[lane].size() * 4) != cudaSuccess ||
+      cudaMalloc(&dk, cnt * 4) != cudaSuccess || cudaMalloc(&dv, cnt * 4) != cudaSuccess) {
+    rc = h->fail(FS_ERR_OOM, "import buffers");
+  } else {
+    cudaError_t e = cudaMemcpyAsync(dp, h->pt[lane].data(), h->pt[lane].size() * 4,
+                                    cudaMemcpyHostToDevice, h->stream);
+    for (int l = 0; l < h->d.n_layers && e == cudaSuccess; ++l) {
+      e = cudaMemcpyAsync(dk, k + (size_t)l * cnt, cnt * 4, cudaMemcpyHostToDevice, h->stream);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dv, v + (size_t)l * cnt, cnt * 4, cudaMemcpyHostToDevice, h->stream);
+      if (e == cudaSuccess) {
+        h->launches += launch_import_kv(h->kv, l, dp, n, dk, dv, h->stream);
+        e = cudaGetLastError();
+      }
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) rc = h->cuda_fail(e, "import_kv");
+  }
+  cudaFree(dp);
+  cudaFree(dk);
+  cudaFree(dv);
+  return rc;
+}
+
+int fs_lane_fill_random_kv(fs_handle* h, int32_t lane, int32_t n, uint64_t seed) {
+  if (!h) return FS_ERR_ARG;
+  int rc = seed_lane_pages(h, lane, n);
+  if (rc || n == 0) return rc;
+  int32_t* dp = nullptr;
+  const size_t np = h->pt[lane].size();
+  if (cudaMalloc(&dp, np * 4) != cudaSuccess) return h->fail(FS_ERR_OOM, "fill buffers");
+  cudaError_t e = cudaMemcpyAsync(dp, h->pt[lane].data(), np * 4, cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) {
+    h->launches += launch_fill_random_kv(h->kv, h->d.n_layers, dp, (int)np, seed, h->stream);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+  cudaFree(dp);
+  if (e != cudaSuccess) return h->cuda_fail(e, "fill_random_kv");
+  return FS_OK;
+}
+
+int fs_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks_out, void* stream) {
+  if (!src || !blocks_out || n < 0 || n % 32) return FS_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  launch_quantize_q8_0(src, n, blocks_out, s);
+  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FS_ERR_CUDA;
+  return FS_OK;
+}
+
+int fs_kernel_launches(const fs_handle* h, int64_t* count_out) {
+  if (!h || !count_out) return FS_ERR_ARG;
+  *count_out = h->launches;
+  return FS_OK;
+}
+
+const char* fs_gemm_path(const fs_handle* h) {
+  (void)h;
+  return "warp-gemv";
+}
+
+}  // extern "C"

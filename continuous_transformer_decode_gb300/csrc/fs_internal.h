@@ -1,0 +1,97 @@
+// Internal interfaces between the host orchestrator (fs_api.cu) and the
+// kernel translation units. Not installed; not part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fsk {
+
+enum WType { W_F32 = 0, W_BF16 = 1, W_Q8 = 2 };
+enum XType { X_F32 = 0, X_BF16 = 1 };
+
+// A weight matrix in the library's device layout: rows of Kp elements
+// (K rounded up to 64, zero padded). Q8_0 is split into int8 codes [N][Kp]
+// and fp16 scales [N][Kp/32] so that both are read with aligned vector loads.
+struct Mat {
+  const void* w = nullptr;
+  const __half* scales = nullptr;
+  int N = 0, K = 0, Kp = 0;
+  int wtype = W_BF16;
+};
+
+// Device copy of one step's arguments (written by one H2D copy per step).
+// Arrays have max_lanes entries; row b of every panel belongs to lane[b].
+struct StepArgs {
+  const int32_t* lane;
+  const int32_t* pos;   // position of the token consumed (length before step)
+  const int32_t* tok;
+  const int32_t* upd_lane;  // page-table updates for this step
+  const int32_t* upd_slot;
+  const int32_t* upd_page;
+  const int32_t* n_upd;
+};
+
+struct KV {
+  void* k = nullptr;  // [L][n_pages][Hkv][page_size][hd] in kv dtype
+  void* v = nullptr;
+  int kv_f32 = 0;     // 1: f32, 0: bf16
+  int64_t layer_stride = 0;  // elements per layer
+  int Hkv = 0, hd = 0, page_size = 0;
+  int32_t* pt = nullptr;     // [max_lanes][max_pages_per_lane]
+  int max_pages = 0;
+};
+
+enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+
+// Y = X * W^T over B panel rows with a fused epilogue:
+//   EPI_STORE : out_f32[b * ldo + n] = y
+//   EPI_RESID : out_f32[b * ldo + n] += y       (residual stream)
+//   EPI_SWIGLU: W holds gate rows [0, F) then up rows [F, 2F);
+//               out_x[b * ldo + f] = silu(gate) * up  (x_type panel)
+// X is a panel [B][W.Kp] of x_type (zero padded beyond K).
+struct GemmArgs {
+  Mat W;
+  const void* X;
+  int x_type;
+  int B;
+  int epi;
+  float* out_f32;
+  void* out_x;
+  int ldo;
+  int n_out;  // output rows (W.N, or F for SwiGLU)
+};
+
+// Launchers (each returns the number of kernels launched).
+int launch_gemv(const GemmArgs& a, cudaStream_t s);
+
+int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
+                 const KV& kv, float* x, int d, cudaStream_t s);
+int launch_rmsnorm(const float* x, const float* g, int B, int d, float eps,
+                   void* out, int x_type, int ld_out, cudaStream_t s);
+int launch_rope_append(const float* qkv, int B, int H, int Hkv, int hd,
+                       const float* rope_cos, const float* rope_sin,
+                       const StepArgs& args, const KV& kv, int layer,
+                       float* q_out, cudaStream_t s);
+int launch_attention(const float* q, int B, int H, const StepArgs& args,
+                     const KV& kv, int layer, int max_splits, int split_len,
+                     float* part_ml, float* part_acc, void* o_panel,
+                     int x_type, int ld_o, cudaStream_t s);
+int launch_sample(const float* logits, int B, int V, const float* temps,
+                  const uint64_t* seeds, const uint64_t* counters,
+                  int32_t* out, cudaStream_t s);
+int launch_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks,
+                         cudaStream_t s);
+int launch_repack_q8(const uint8_t* blocks, int N, int K, int Kp,
+                     int8_t* qs, __half* scales, int row_offset,
+                     cudaStream_t s);
+int launch_fill_random_kv(const KV& kv, int L, const int32_t* pages,
+                          int n_pages, uint64_t seed, cudaStream_t s);
+int launch_import_kv(const KV& kv, int layer, const int32_t* pages, int n,
+                     const float* k, const float* v, cudaStream_t s);
+int launch_export_kv(const KV& kv, int layer, const int32_t* pages, int n,
+                     float* k, float* v, cudaStream_t s);
+
+}  // namespace fsk

@@ -1,0 +1,393 @@
+// Embedding gather, RMSNorm, the per-lane sampler, the Q8_0 quantiser and
+// the weight / KV layout helpers.
+
+#include <math_constants.h>
+
+#include "fs_internal.h"
+
+namespace fsk {
+namespace {
+
+__device__ __forceinline__ float load_w(const Mat& E, int64_t row, int i) {
+  if (E.wtype == W_BF16)
+    return __bfloat162float(
+        static_cast<const __nv_bfloat16*>(E.w)[row * E.Kp + i]);
+  if (E.wtype == W_F32) return static_cast<const float*>(E.w)[row * E.Kp + i];
+  const float d = __half2float(E.scales[row * (E.Kp / 32) + i / 32]);
+  return (float)static_cast<const int8_t*>(E.w)[row * E.Kp + i] * d;
+}
+
+// x[b] = E[tok[b]]; block b also applies page-table update b of the step.
+__global__ void k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x,
+                        int d) {
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0 && b < *args.n_upd) {
+    kv.pt[(int64_t)args.upd_lane[b] * kv.max_pages + args.upd_slot[b]] =
+        args.upd_page[b];
+  }
+  const int64_t tok = args.tok[b];
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    x[(int64_t)b * d + i] = load_w(E, tok, i);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < nw; ++i) r += red[i];
+  return r;
+}
+
+// y = x * (1 / sqrt(mean(x^2) + eps)) * g, one block per panel row; the sum
+// of squares is reduced in a fixed order, independent of the batch.
+template <typename OT>
+__global__ void k_rmsnorm(const float* __restrict__ x,
+                          const float* __restrict__ g, int d, float eps,
+                          OT* __restrict__ out, int ld_out) {
+  __shared__ float red[32];
+  const int b = blockIdx.x;
+  const float* xr = x + (int64_t)b * d;
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  ss = block_sum(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = xr[i] * r * g[i];
+    if constexpr (sizeof(OT) == 2)
+      out[(int64_t)b * ld_out + i] = __float2bfloat16_rn(v);
+    else
+      out[(int64_t)b * ld_out + i] = v;
+  }
+}
+
+// ---------------------------------------------------------------- sampler
+// Philox4x32-10 (Salmon et al., SC 2011), written from its definition.
+__device__ __forceinline__ void philox(uint32_t c[4], uint32_t k0,
+                                       uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+    const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
+constexpr int kSampThreads = 1024;
+
+// One block per row. Greedy: argmax with the lowest index on ties.
+// Temperature: contiguous per-thread segments, an ordered exclusive scan of
+// the segment sums, then the owning thread walks its segment.
+__global__ void __launch_bounds__(kSampThreads)
+    k_sample(const float* __restrict__ logits, int V,
+             const float* __restrict__ temps, const uint64_t* __restrict__ seeds,
+             const uint64_t* __restrict__ counters, int32_t* __restrict__ out) {
+  __shared__ double sd[kSampThreads];
+  __shared__ int si[kSampThreads];
+  const int b = blockIdx.x, t = threadIdx.x;
+  const float* lg = logits + (int64_t)b * V;
+  const float temp = temps[b];
+  const int seg = (V + kSampThreads - 1) / kSampThreads;
+  const int lo = min(V, t * seg), hi = min(V, lo + seg);
+  if (temp == 0.0f) {
+    float best = -CUDART_INF_F;
+    int bi = V;  // sentinel: no candidate
+    for (int i = lo; i < hi; ++i)
+      if (bi == V || lg[i] > best) {
+        best = lg[i];
+        bi = i;
+      }
+    sd[t] = best;
+    si[t] = bi;
+    __syncthreads();
+    for (int w = kSampThreads / 2; w > 0; w >>= 1) {
+      if (t < w) {
+        const double ov = sd[t + w];
+        const int oi = si[t + w];
+        if (oi != V && (si[t] == V || ov > sd[t] || (ov == sd[t] && oi < si[t]))) {
+          sd[t] = ov;
+          si[t] = oi;
+        }
+      }
+      __syncthreads();
+    }
+    if (t == 0) out[b] = si[0] == V ? 0 : si[0];
+    return;
+  }
+  // max of z = logit / T
+  double mz = -CUDART_INF;
+  for (int i = lo; i < hi; ++i) mz = fmax(mz, (double)lg[i] / (double)temp);
+  sd[t] = mz;
+  __syncthreads();
+  for (int w = kSampThreads / 2; w > 0; w >>= 1) {
+    if (t < w) sd[t] = fmax(sd[t], sd[t + w]);
+    __syncthreads();
+  }
+  const double m = sd[0];
+  __syncthreads();
+  double part = 0.0;
+  int last_pos = -1;
+  for (int i = lo; i < hi; ++i) {
+    const double e = exp((double)lg[i] / (double)temp - m);
+    part += e;
+    if (e > 0.0) last_pos = i;
+  }
+  sd[t] = part;
+  si[t] = last_pos;
+  __syncthreads();
+  // inclusive scan (Hillis-Steele) of segment sums in thread order
+  for (int w = 1; w < kSampThreads; w <<= 1) {
+    const double v = t >= w ? sd[t - w] : 0.0;
+    __syncthreads();
+    sd[t] += v;
+    __syncthreads();
+  }
+  const double total = sd[kSampThreads - 1];
+  const double before = t > 0 ? sd[t - 1] : 0.0;
+  uint32_t c[4] = {(uint32_t)counters[b], (uint32_t)(counters[b] >> 32), 0u, 0u};
+  philox(c, (uint32_t)seeds[b], (uint32_t)(seeds[b] >> 32));
+  const uint64_t bits = ((uint64_t)c[0] << 32) | c[1];
+  const double u = (double)(bits >> 11) * (1.0 / 9007199254740992.0);
+  const double target = u * total;
+  __shared__ int found;
+  if (t == 0) found = V;
+  __syncthreads();
+  if (before < target || (t == 0 && target <= 0.0)) {
+    double cum = before;
+    for (int i = lo; i < hi; ++i) {
+      const double e = exp((double)lg[i] / (double)temp - m);
+      cum += e;
+      if (cum >= target && e > 0.0) {
+        atomicMin(&found, i);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    int r = found;
+    if (r == V) {  // rounding left the target above the total: last positive
+      r = 0;
+      for (int j = kSampThreads - 1; j >= 0; --j)
+        if (si[j] >= 0) {
+          r = si[j];
+          break;
+        }
+    }
+    out[b] = r;
+  }
+}
+
+// ------------------------------------------------------------- Q8_0 codec
+__global__ void k_quantize_q8_0(const float* __restrict__ x, int64_t nblk,
+                                uint8_t* __restrict__ blocks) {
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int j = threadIdx.x & 31;
+  if (blk >= nblk) return;
+  const float v = x[blk * 32 + j];
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = amax / 127.0f;
+  const float id = d != 0.0f ? 1.0f / d : 0.0f;
+  float q = roundf(v * id);
+  q = fminf(127.0f, fmaxf(-127.0f, q));
+  uint8_t* ob = blocks + blk * 34;
+  if (j == 0) {
+    const __half hd = __float2half_rn(d);
+    const uint16_t bits = __half_as_ushort(hd);
+    ob[0] = (uint8_t)(bits & 0xff);
+    ob[1] = (uint8_t)(bits >> 8);
+  }
+  ob[2 + j] = (uint8_t)(int8_t)q;
+}
+
+// 34-byte blocks of rows [N][K] -> codes [row_offset + n][Kp], scales.
+__global__ void k_repack_q8(const uint8_t* __restrict__ blocks, int N, int K,
+                            int Kp, int8_t* __restrict__ qs,
+                            __half* __restrict__ scales, int row_offset) {
+  const int64_t nb_row = K / 32;
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int j = threadIdx.x & 31;
+  if (blk >= (int64_t)N * nb_row) return;
+  const int64_t n = blk / nb_row, kb = blk - n * nb_row;
+  const uint8_t* ib = blocks + blk * 34;
+  const int64_t r = row_offset + n;
+  qs[r * Kp + kb * 32 + j] = (int8_t)ib[2 + j];
+  if (j == 0)
+    scales[r * (Kp / 32) + kb] =
+        __ushort_as_half((uint16_t)(ib[0] | ((uint16_t)ib[1] << 8)));
+}
+
+// ------------------------------------------------------------- KV helpers
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {  // splitmix64 finaliser
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Fills whole pages (every layer, K and V) with values uniform in
+// [-sqrt(3), sqrt(3)) (unit variance) derived from (seed, element index).
+template <typename KVT>
+__global__ void k_fill_random_kv(KV kv, int L, const int32_t* __restrict__ pages,
+                                 int n_pages, uint64_t seed) {
+  const int64_t per_page = (int64_t)kv.Hkv * kv.page_size * kv.hd;
+  const int64_t total = (int64_t)L * n_pages * per_page;
+  KVT* K = static_cast<KVT*>(kv.k);
+  KVT* V = static_cast<KVT*>(kv.v);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t l = i / ((int64_t)n_pages * per_page);
+    const int64_t rem = i - l * n_pages * per_page;
+    const int64_t p = rem / per_page, e = rem - p * per_page;
+    const int64_t off = l * kv.layer_stride + (int64_t)pages[p] * per_page + e;
+    const uint64_t h1 = mix64(seed ^ (uint64_t)(2 * off));
+    const uint64_t h2 = mix64(seed ^ (uint64_t)(2 * off + 1));
+    const float u1 = (float)(h1 >> 40) * (1.0f / 16777216.0f);
+    const float u2 = (float)(h2 >> 40) * (1.0f / 16777216.0f);
+    const float k = (2.0f * u1 - 1.0f) * 1.7320508f;
+    const float v = (2.0f * u2 - 1.0f) * 1.7320508f;
+    if constexpr (sizeof(KVT) == 2) {
+      K[off] = __float2bfloat16_rn(k);
+      V[off] = __float2bfloat16_rn(v);
+    } else {
+      K[off] = k;
+      V[off] = v;
+    }
+  }
+}
+
+// Copies n tokens of one layer between a lane's pages and dense f32
+// [n][Hkv][hd] arrays (to_pages: dense -> pages).
+template <typename KVT, bool kToPages>
+__global__ void k_copy_kv(KV kv, int layer, const int32_t* __restrict__ pages,
+                          int n, float* k, float* v) {
+  const int64_t row = (int64_t)kv.Hkv * kv.hd;
+  const int64_t total = (int64_t)n * row;
+  KVT* K = static_cast<KVT*>(kv.k);
+  KVT* V = static_cast<KVT*>(kv.v);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / row);
+    const int64_t r = i - (int64_t)t * row;
+    const int g = (int)(r / kv.hd), e = (int)(r - (int64_t)g * kv.hd);
+    const int page = pages[t / kv.page_size], slot = t % kv.page_size;
+    const int64_t off = (int64_t)layer * kv.layer_stride +
+                        (((int64_t)page * kv.Hkv + g) * kv.page_size + slot) * kv.hd + e;
+    if (kToPages) {
+      if constexpr (sizeof(KVT) == 2) {
+        K[off] = __float2bfloat16_rn(k[i]);
+        V[off] = __float2bfloat16_rn(v[i]);
+      } else {
+        K[off] = k[i];
+        V[off] = v[i];
+      }
+    } else {
+      if constexpr (sizeof(KVT) == 2) {
+        k[i] = __bfloat162float(K[off]);
+        v[i] = __bfloat162float(V[off]);
+      } else {
+        k[i] = K[off];
+        v[i] = V[off];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
+                 const KV& kv, float* x, int d, cudaStream_t s) {
+  (void)n_upd_max;
+  if (B <= 0) return 0;
+  k_embed<<<B, 256, 0, s>>>(E, args, kv, x, d);
+  return 1;
+}
+
+int launch_rmsnorm(const float* x, const float* g, int B, int d, float eps,
+                   void* out, int x_type, int ld_out, cudaStream_t s) {
+  if (B <= 0) return 0;
+  if (x_type == X_BF16)
+    k_rmsnorm<__nv_bfloat16><<<B, 256, 0, s>>>(
+        x, g, d, eps, static_cast<__nv_bfloat16*>(out), ld_out);
+  else
+    k_rmsnorm<float><<<B, 256, 0, s>>>(x, g, d, eps, static_cast<float*>(out),
+                                       ld_out);
+  return 1;
+}
+
+int launch_sample(const float* logits, int B, int V, const float* temps,
+                  const uint64_t* seeds, const uint64_t* counters, int32_t* out,
+                  cudaStream_t s) {
+  if (B <= 0) return 0;
+  k_sample<<<B, kSampThreads, 0, s>>>(logits, V, temps, seeds, counters, out);
+  return 1;
+}
+
+int launch_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks,
+                         cudaStream_t s) {
+  const int64_t nblk = n / 32;
+  if (nblk <= 0) return 0;
+  const int per = 8;  // blocks per CTA (one warp each)
+  k_quantize_q8_0<<<(unsigned)((nblk + per - 1) / per), per * 32, 0, s>>>(
+      src, nblk, blocks);
+  return 1;
+}
+
+int launch_repack_q8(const uint8_t* blocks, int N, int K, int Kp, int8_t* qs,
+                     __half* scales, int row_offset, cudaStream_t s) {
+  const int64_t nblk = (int64_t)N * (K / 32);
+  if (nblk <= 0) return 0;
+  const int per = 8;
+  k_repack_q8<<<(unsigned)((nblk + per - 1) / per), per * 32, 0, s>>>(
+      blocks, N, K, Kp, qs, scales, row_offset);
+  return 1;
+}
+
+int launch_fill_random_kv(const KV& kv, int L, const int32_t* pages,
+                          int n_pages, uint64_t seed, cudaStream_t s) {
+  if (n_pages <= 0) return 0;
+  if (kv.kv_f32)
+    k_fill_random_kv<float><<<1216, 256, 0, s>>>(kv, L, pages, n_pages, seed);
+  else
+    k_fill_random_kv<__nv_bfloat16><<<1216, 256, 0, s>>>(kv, L, pages, n_pages,
+                                                          seed);
+  return 1;
+}
+
+int launch_import_kv(const KV& kv, int layer, const int32_t* pages, int n,
+                     const float* k, const float* v, cudaStream_t s) {
+  if (n <= 0) return 0;
+  if (kv.kv_f32)
+    k_copy_kv<float, true><<<304, 256, 0, s>>>(kv, layer, pages, n,
+                                               const_cast<float*>(k),
+                                               const_cast<float*>(v));
+  else
+    k_copy_kv<__nv_bfloat16, true><<<304, 256, 0, s>>>(
+        kv, layer, pages, n, const_cast<float*>(k), const_cast<float*>(v));
+  return 1;
+}
+
+int launch_export_kv(const KV& kv, int layer, const int32_t* pages, int n,
+                     float* k, float* v, cudaStream_t s) {
+  if (n <= 0) return 0;
+  if (kv.kv_f32)
+    k_copy_kv<float, false><<<304, 256, 0, s>>>(kv, layer, pages, n, k, v);
+  else
+    k_copy_kv<__nv_bfloat16, false><<<304, 256, 0, s>>>(kv, layer, pages, n,
+                                                        k, v);
+  return 1;
+}
+
+}  // namespace fsk

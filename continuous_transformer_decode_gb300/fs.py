@@ -1,0 +1,280 @@
+"""Thin Python binding of the C ABI in include/fs.h (argument marshalling only).
+
+Every step of the decode path runs inside ``_build/libfs.so``; this module
+only converts Python/numpy/torch arguments to pointers and sizes. If the
+library is missing the import of any entry point raises: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+FS_OK = 0
+ERRORS = {-1: "FS_ERR_ARG", -2: "FS_ERR_LANE", -3: "FS_ERR_DUP_LANE",
+          -4: "FS_ERR_POSITION", -5: "FS_ERR_TOKEN", -6: "FS_ERR_KV_FULL",
+          -7: "FS_ERR_OOM", -8: "FS_ERR_CUDA", -9: "FS_ERR_STATE",
+          -10: "FS_ERR_DEVICE"}
+CODES = {v: k for k, v in ERRORS.items()}
+FS_DTYPE_F32, FS_DTYPE_BF16, FS_DTYPE_Q8_0 = 0, 1, 2
+
+
+class FsError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+        self.name = ERRORS.get(code, str(code))
+
+
+class fs_model_desc(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32),
+                ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ffn", C.c_int32),
+                ("vocab", C.c_int32), ("rms_eps", C.c_float),
+                ("rope_theta", C.c_double), ("tied_embeddings", C.c_int32),
+                ("weight_dtype", C.c_int32), ("kv_dtype", C.c_int32),
+                ("max_lanes", C.c_int32), ("page_size", C.c_int32),
+                ("n_pages", C.c_int32), ("max_pos", C.c_int32)]
+
+
+class fs_layer_weights(C.Structure):
+    _fields_ = [(k, C.c_void_p) for k in ("wq", "wk", "wv", "wo", "w_gate",
+                                          "w_up", "w_down", "attn_norm",
+                                          "ffn_norm")]
+
+
+class fs_weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p),
+                ("final_norm", C.c_void_p),
+                ("layers", C.POINTER(fs_layer_weights))]
+
+
+LIB_PATH = _build.LIB
+_lib = None
+
+
+def lib():
+    """Loads libfs.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                          "(run __graft_entry__.build())")
+    L = C.CDLL(LIB_PATH)
+    p, i32, i64, u64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64
+    sig = {
+        "fs_create": (C.c_int, [C.POINTER(fs_model_desc),
+                                C.POINTER(fs_weights), C.POINTER(p)]),
+        "fs_destroy": (C.c_int, [p]),
+        "fs_last_error": (C.c_char_p, [p]),
+        "fs_set_stream": (C.c_int, [p, p]),
+        "fs_lane_reset": (C.c_int, [p, i32]),
+        "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
+        "fs_sample": (C.c_int, [p, i32, p, p, p, p]),
+        "fs_lane_length": (C.c_int, [p, i32, p]),
+        "fs_lane_pages": (C.c_int, [p, i32, p, i32, p]),
+        "fs_lane_export_kv": (C.c_int, [p, i32, i32, p, p]),
+        "fs_lane_import_kv": (C.c_int, [p, i32, p, p, i32]),
+        "fs_lane_fill_random_kv": (C.c_int, [p, i32, i32, u64]),
+        "fs_quantize_q8_0": (C.c_int, [p, i64, p, p]),
+        "fs_sample_device": (C.c_int, [p, i32, p, p, p, p]),
+        "fs_profile_enable": (C.c_int, [p, i32]),
+        "fs_profile_read": (C.c_int, [p, i32, p, p, p]),
+        "fs_kernel_launches": (C.c_int, [p, p]),
+        "fs_gemm_path": (C.c_char_p, [p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def exported_symbols() -> list:
+    """Names of the entry points declared in include/fs.h."""
+    return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
+            "fs_lane_reset", "fs_decode_step_batch", "fs_sample",
+            "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
+            "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
+            "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
+            "fs_profile_enable", "fs_profile_read"]
+
+
+def _check(h, rc: int) -> None:
+    if rc != FS_OK:
+        msg = lib().fs_last_error(h)
+        raise FsError(rc, msg.decode() if msg else "")
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _dptr(x):
+    """Address of a host numpy array, a torch tensor (host or device) or None."""
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        assert x.flags["C_CONTIGUOUS"]
+        return x.ctypes.data
+    if hasattr(x, "data_ptr"):
+        assert x.is_contiguous()
+        return x.data_ptr()
+    return int(x)
+
+
+def make_desc(cfg: dict, weight_dtype: int, kv_dtype: int, max_lanes: int,
+              n_pages: int, max_pos: int, page_size: int = 16) -> fs_model_desc:
+    return fs_model_desc(cfg["L"], cfg["d"], cfg["H"], cfg["Hkv"], cfg["hd"],
+                         cfg["F"], cfg["V"], cfg["rms_eps"], cfg["rope_theta"],
+                         1 if cfg["tied"] else 0, weight_dtype, kv_dtype,
+                         max_lanes, page_size, n_pages, max_pos)
+
+
+LAYER_KEYS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down",
+              "attn_norm", "ffn_norm")
+
+
+def fs_create(desc: fs_model_desc, weights: dict):
+    """weights: dict of host numpy arrays or torch tensors (host or device):
+    embed, lm_head (or None), final_norm, layers[list of LAYER_KEYS dicts]."""
+    layers = (fs_layer_weights * len(weights["layers"]))()
+    for i, ly in enumerate(weights["layers"]):
+        for k in LAYER_KEYS:
+            setattr(layers[i], k, _dptr(ly[k]))
+    w = fs_weights(_dptr(weights["embed"]), _dptr(weights.get("lm_head")),
+                   _dptr(weights["final_norm"]), layers)
+    h = C.c_void_p()
+    _check(None, lib().fs_create(C.byref(desc), C.byref(w), C.byref(h)))
+    return h
+
+
+def fs_destroy(h) -> None:
+    lib().fs_destroy(h)
+
+
+def fs_last_error(h) -> str:
+    m = lib().fs_last_error(h)
+    return m.decode() if m else ""
+
+
+def fs_set_stream(h, stream) -> None:
+    """stream: a torch.cuda.Stream, a raw cudaStream_t int, or None."""
+    raw = getattr(stream, "cuda_stream", stream)
+    _check(h, lib().fs_set_stream(h, raw))
+
+
+def fs_lane_reset(h, lane: int) -> None:
+    _check(h, lib().fs_lane_reset(h, int(lane)))
+
+
+def fs_decode_step_batch(h, lanes, positions, tokens, logits_out=None):
+    """Advances lanes by one token. ``positions`` (np.int32) is incremented
+    in place on success and returned. logits_out: torch CUDA f32 [n, V]."""
+    la = _i32(lanes)
+    to = _i32(tokens)
+    if (isinstance(positions, np.ndarray) and positions.dtype == np.int32
+            and positions.flags["C_CONTIGUOUS"]):
+        po = positions
+    else:
+        po = _i32(positions)
+    n = la.size
+    assert po.size == n and to.size == n
+    _check(h, lib().fs_decode_step_batch(h, _ptr(la), _ptr(po), _ptr(to), n,
+                                         _dptr(logits_out)))
+    return po
+
+
+def fs_sample(h, temps, seeds, counters) -> np.ndarray:
+    t = np.ascontiguousarray(np.asarray(temps, dtype=np.float32))
+    s = np.ascontiguousarray(np.asarray(seeds, dtype=np.uint64))
+    c = np.ascontiguousarray(np.asarray(counters, dtype=np.uint64))
+    out = np.empty(t.size, dtype=np.int32)
+    _check(h, lib().fs_sample(h, t.size, _ptr(t), _ptr(s), _ptr(c), _ptr(out)))
+    return out
+
+
+def fs_sample_device(h, temps, seeds, counters, tokens_out) -> None:
+    """All four are torch CUDA tensors (f32, int64/uint64, int64/uint64,
+    int32) of n entries; no synchronisation."""
+    _check(h, lib().fs_sample_device(h, tokens_out.numel(), _dptr(temps),
+                                     _dptr(seeds), _dptr(counters),
+                                     _dptr(tokens_out)))
+
+
+FS_PROF_GEMM, FS_PROF_ATTN, FS_PROF_OTHER = 0, 1, 2
+
+
+def fs_profile_enable(h, enable: bool) -> None:
+    _check(h, lib().fs_profile_enable(h, 1 if enable else 0))
+
+
+def fs_profile_read(h, cls: int):
+    """(ms, launches, algorithmic bytes) of kernel class `cls` since the
+    last read."""
+    ms, n, b = C.c_double(), C.c_int64(), C.c_double()
+    _check(h, lib().fs_profile_read(h, int(cls), C.byref(ms), C.byref(n),
+                                    C.byref(b)))
+    return ms.value, n.value, b.value
+
+
+def fs_lane_length(h, lane: int) -> int:
+    v = C.c_int32()
+    _check(h, lib().fs_lane_length(h, int(lane), C.byref(v)))
+    return v.value
+
+
+def fs_lane_pages(h, lane: int) -> list:
+    n = C.c_int32()
+    _check(h, lib().fs_lane_pages(h, int(lane), None, 0, C.byref(n)))
+    out = np.empty(max(1, n.value), dtype=np.int32)
+    _check(h, lib().fs_lane_pages(h, int(lane), _ptr(out), n.value, C.byref(n)))
+    return out[:n.value].tolist()
+
+
+def fs_lane_export_kv(h, lane: int, layer: int, Hkv: int, hd: int):
+    n = fs_lane_length(h, lane)
+    k = np.empty((n, Hkv, hd), dtype=np.float32)
+    v = np.empty((n, Hkv, hd), dtype=np.float32)
+    _check(h, lib().fs_lane_export_kv(h, int(lane), int(layer), _ptr(k), _ptr(v)))
+    return k, v
+
+
+def fs_lane_import_kv(h, lane: int, k: np.ndarray, v: np.ndarray) -> None:
+    """k, v: f32 [n_layers, n, Hkv, hd] (K already rotated)."""
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    _check(h, lib().fs_lane_import_kv(h, int(lane), _ptr(k), _ptr(v),
+                                      k.shape[1]))
+
+
+def fs_lane_fill_random_kv(h, lane: int, n: int, seed: int) -> None:
+    _check(h, lib().fs_lane_fill_random_kv(h, int(lane), int(n), int(seed)))
+
+
+def fs_quantize_q8_0(src, blocks_out, stream=None) -> None:
+    """src: torch CUDA f32 tensor; blocks_out: torch CUDA uint8 [n/32, 34]."""
+    raw = getattr(stream, "cuda_stream", stream)
+    rc = lib().fs_quantize_q8_0(_dptr(src), src.numel(), _dptr(blocks_out), raw)
+    if rc != FS_OK:
+        raise FsError(rc, "fs_quantize_q8_0 failed")
+
+
+def fs_kernel_launches(h) -> int:
+    v = C.c_int64()
+    _check(h, lib().fs_kernel_launches(h, C.byref(v)))
+    return v.value
+
+
+def fs_gemm_path(h) -> str:
+    return lib().fs_gemm_path(h).decode()

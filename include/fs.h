@@ -1,0 +1,233 @@
+/*
+ * fs.h — C ABI of the continuous-batched decode step (decode_step_batch).
+ *
+ * One handle holds one dense Llama-style model on one GPU, a paged KV arena
+ * shared by up to max_lanes lanes, and the scratch panels of one step. One
+ * call advances up to max_lanes lanes by one token each: every weight byte is
+ * read once for the whole batch, while attention stays per lane over that
+ * lane's own pages.
+ *
+ * Sources of the operations (page title, section):
+ *   - "Fat-station continuous batching — the live-path integration",
+ *     "The capture": decode_step_batch(kv caches, positions, tokens) advances
+ *     K lanes by one token with one weight read for the wave; "Components",
+ *     item 3: fill (reset a free lane, position 0), gather, fold (sample with
+ *     the lane's temperature/seed, retire, free the lane).
+ *   - "MODEL-BATCHING-RESULTS — multi-user batched decode, measured",
+ *     "The lever": the seven projection matmuls and the LM head run as one
+ *     GEMM over a [B, *] panel; attention is per user over its own KV cache;
+ *     "API": StepBatch(ids) is the per-step primitive a continuous-batching
+ *     scheduler calls after admitting/evicting users between steps.
+ *   - mlx-bun "Parallel slots — configurable batched serving", "KV memory",
+ *     rung 3: fixed-size KV blocks in a shared pool with a block manager.
+ *
+ * Conventions
+ *   - Every call returns FS_OK (0) or a negative FS_ERR_* code; the message
+ *     of the last failure is available from fs_last_error(handle) (or
+ *     fs_last_error(NULL) for a failed fs_create). No C++ exception crosses
+ *     this boundary.
+ *   - A handle is used by one host thread at a time.
+ *   - Calls that change lane state are atomic: on any error no lane length,
+ *     position or page changes.
+ *   - Unless stated otherwise, pointers are HOST pointers owned by the caller
+ *     and only read during the call.
+ *   - All kernels run on the handle's stream (fs_set_stream). Calls that
+ *     return host results synchronise that stream; fs_decode_step_batch does
+ *     not (its logits are ready once the stream reaches that point).
+ */
+#ifndef FS_H_
+#define FS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define FS_OK 0
+#define FS_ERR_ARG (-1)       /* bad argument, size or descriptor field      */
+#define FS_ERR_LANE (-2)      /* lane index outside [0, max_lanes)            */
+#define FS_ERR_DUP_LANE (-3)  /* a lane appears twice in one step            */
+#define FS_ERR_POSITION (-4)  /* positions[i] differs from the lane length   */
+#define FS_ERR_TOKEN (-5)     /* token outside [0, vocab)                     */
+#define FS_ERR_KV_FULL (-6)   /* page pool exhausted, or lane at max_pos      */
+#define FS_ERR_OOM (-7)       /* device allocation failed                     */
+#define FS_ERR_CUDA (-8)      /* a CUDA call failed (message has the detail)  */
+#define FS_ERR_STATE (-9)     /* call out of order (e.g. sample before step)  */
+#define FS_ERR_DEVICE (-10)   /* a kernel reported a device-side error flag   */
+
+/* ---- element types ----------------------------------------------------- */
+#define FS_DTYPE_F32 0   /* IEEE binary32                                     */
+#define FS_DTYPE_BF16 1  /* bfloat16 bit patterns (uint16)                    */
+#define FS_DTYPE_Q8_0 2  /* blocks of 32 inputs: fp16 scale d (little endian)
+                            then 32 int8 codes q; value = q * d; 34 bytes.
+                            A [rows, cols] matrix is rows*cols/32 blocks in
+                            row-major order (cols must be a multiple of 32).  */
+
+/* Model and arena description. */
+typedef struct fs_model_desc {
+  int32_t n_layers;        /* L                                              */
+  int32_t d_model;         /* d                                              */
+  int32_t n_heads;         /* H query heads                                  */
+  int32_t n_kv_heads;      /* Hkv; H must be a multiple of Hkv (GQA)         */
+  int32_t head_dim;        /* hd, even; RoPE pairs (i, i + hd/2)             */
+  int32_t d_ffn;           /* F (SwiGLU width)                               */
+  int32_t vocab;           /* V                                              */
+  float rms_eps;           /* RMSNorm epsilon                                */
+  double rope_theta;       /* RoPE base                                      */
+  int32_t tied_embeddings; /* 1: LM head is the embedding matrix             */
+  int32_t weight_dtype;    /* FS_DTYPE_F32 / _BF16 / _Q8_0 for all matrices  */
+  int32_t kv_dtype;        /* FS_DTYPE_F32 or FS_DTYPE_BF16                  */
+  int32_t max_lanes;       /* lanes addressable by fs_decode_step_batch      */
+  int32_t page_size;       /* tokens per KV page (e.g. 16)                   */
+  int32_t n_pages;         /* pages in the shared arena                      */
+  int32_t max_pos;         /* tokens a lane may hold                         */
+} fs_model_desc;
+
+/* Per-layer weights in Hugging Face layout W[out, in], row-major, in
+ * weight_dtype; norm gains are always f32. Pointers may be host or device
+ * memory (the library copies them during fs_create; the caller keeps
+ * ownership). */
+typedef struct fs_layer_weights {
+  const void* wq;        /* [H*hd, d]   */
+  const void* wk;        /* [Hkv*hd, d] */
+  const void* wv;        /* [Hkv*hd, d] */
+  const void* wo;        /* [d, H*hd]   */
+  const void* w_gate;    /* [F, d]      */
+  const void* w_up;      /* [F, d]      */
+  const void* w_down;    /* [d, F]      */
+  const float* attn_norm; /* [d]        */
+  const float* ffn_norm;  /* [d]        */
+} fs_layer_weights;
+
+typedef struct fs_weights {
+  const void* embed;              /* [V, d]                               */
+  const void* lm_head;            /* [V, d]; NULL when tied_embeddings    */
+  const float* final_norm;        /* [d]                                  */
+  const fs_layer_weights* layers; /* n_layers entries                     */
+} fs_weights;
+
+typedef struct fs_handle fs_handle;
+
+/* Creates a handle on the current CUDA device: validates the descriptor,
+ * uploads and re-lays out the weights, allocates the KV arena and scratch.
+ * Errors: FS_ERR_ARG (descriptor), FS_ERR_OOM, FS_ERR_CUDA. */
+int fs_create(const fs_model_desc* desc, const fs_weights* weights,
+              fs_handle** out);
+
+/* Frees every device buffer of the handle. NULL is accepted. */
+int fs_destroy(fs_handle* h);
+
+/* Message of the last failed call on h (or of the last failed fs_create
+ * when h is NULL). Valid until the next call on the same handle. */
+const char* fs_last_error(const fs_handle* h);
+
+/* Kernels of h run on `stream` (a cudaStream_t) from now on. NULL selects
+ * the handle's own stream. */
+int fs_set_stream(fs_handle* h, void* stream);
+
+/* Fill step of the scheduler ("Components", item 3): frees lane k's pages
+ * and sets its length to 0. Errors: FS_ERR_LANE. */
+int fs_lane_reset(fs_handle* h, int32_t lane);
+
+/* decode_step_batch. For each i < n, lane lanes[i], whose length must equal
+ * positions[i], consumes tokens[i]: its K/V at that position are appended to
+ * its pages (a new page, lowest free index first, when the length is a
+ * multiple of page_size) and its next-token logits are produced. On success
+ * positions[i] is incremented. lanes, positions and tokens are host arrays.
+ * logits_out: DEVICE pointer to f32 [n, vocab] in input order, or NULL to
+ * keep the logits inside the handle for fs_sample. n == 0 is a no-op.
+ * Errors (nothing changes): FS_ERR_ARG (n outside [0, max_lanes]),
+ * FS_ERR_LANE, FS_ERR_DUP_LANE, FS_ERR_POSITION, FS_ERR_TOKEN,
+ * FS_ERR_KV_FULL; FS_ERR_CUDA if a launch fails (lane state is then
+ * undefined). */
+int fs_decode_step_batch(fs_handle* h, const int32_t* lanes,
+                         int32_t* positions, const int32_t* tokens, int32_t n,
+                         float* logits_out);
+
+/* Samples one token per row of the last step's logits ("Components", item 3,
+ * fold: the lane's temperature and seed). Row i: temps[i] == 0 selects the
+ * argmax (lowest index on ties); otherwise z = logit / temps[i] in double,
+ * u = (Philox4x32-10(key = seeds[i], counter = counters[i]) >> 11) * 2^-53,
+ * and the first index whose running sum of exp(z - max z) reaches u times
+ * the total. temps/seeds/counters are host arrays of n entries, n must equal
+ * the last step's n; tokens_out is a host array. Synchronises the stream.
+ * Errors: FS_ERR_STATE (no step yet, or n differs), FS_ERR_ARG. */
+int fs_sample(fs_handle* h, int32_t n, const float* temps,
+              const uint64_t* seeds, const uint64_t* counters,
+              int32_t* tokens_out);
+
+/* fs_sample on device buffers, without synchronising: temps (f32), seeds and
+ * counters (uint64) and tokens_out (int32) are DEVICE arrays of n entries.
+ * The tokens are ready once the stream reaches this point. Same rule and
+ * errors as fs_sample. */
+int fs_sample_device(fs_handle* h, int32_t n, const float* temps,
+                     const uint64_t* seeds, const uint64_t* counters,
+                     int32_t* tokens_out);
+
+/* ---- inspection and test hooks ---------------------------------------- */
+
+/* Kernel classes of the profiler. */
+#define FS_PROF_GEMM 0      /* weight-streaming GEMM (all matrices)          */
+#define FS_PROF_ATTN 1      /* attention partial + combine                  */
+#define FS_PROF_OTHER 2     /* embed, norms, RoPE/append, sampler           */
+#define FS_PROF_CLASSES 3
+
+/* Enables (1) or disables (0) CUDA-event timing of every kernel launch of
+ * the handle, on the handle's stream. */
+int fs_profile_enable(fs_handle* h, int32_t enable);
+
+/* Synchronises the stream and returns, for kernel class `cls`, the summed
+ * device time in ms, the number of launches and the algorithmic bytes those
+ * launches move (weights, activations, KV and outputs, each counted once)
+ * since the last read; then clears that class. */
+int fs_profile_read(fs_handle* h, int32_t cls, double* ms_out,
+                    int64_t* launches_out, double* bytes_out);
+
+/* Current length (tokens held) of a lane. */
+int fs_lane_length(const fs_handle* h, int32_t lane, int32_t* length_out);
+
+/* Page table of a lane: writes min(cap, n_pages_of_lane) page indices and
+ * the lane's page count to *n_out. */
+int fs_lane_pages(const fs_handle* h, int32_t lane, int32_t* pages_out,
+                  int32_t cap, int32_t* n_out);
+
+/* Copies a lane's K (after RoPE) and V of one layer to host f32 arrays of
+ * [length, Hkv, hd]. Synchronises the stream. */
+int fs_lane_export_kv(fs_handle* h, int32_t lane, int32_t layer, float* k_out,
+                      float* v_out);
+
+/* Seeds lane `lane` (which must be empty) with n tokens of given K (already
+ * rotated) and V for every layer: k and v are host f32 arrays
+ * [n_layers, n, Hkv, hd]. Pages are allocated as by n decode steps.
+ * Errors: FS_ERR_STATE (lane not empty), FS_ERR_KV_FULL, FS_ERR_ARG. */
+int fs_lane_import_kv(fs_handle* h, int32_t lane, const float* k,
+                      const float* v, int32_t n);
+
+/* Seeds an empty lane with n tokens of pseudo-random K/V (values of unit
+ * scale drawn on the device from `seed`) for timing long contexts, where
+ * the content does not matter. Errors as fs_lane_import_kv. */
+int fs_lane_fill_random_kv(fs_handle* h, int32_t lane, int32_t n,
+                           uint64_t seed);
+
+/* Q8_0 quantiser on the device: src is n f32 values (DEVICE pointer, n a
+ * multiple of 32), blocks_out receives n/32 blocks of 34 bytes (DEVICE
+ * pointer). Per block: d = max|x| / 127, q = round-half-away(x * (1/d))
+ * clamped to [-127, 127], d stored as fp16 (round to nearest even); an
+ * all-zero block stores d = 0 and q = 0. Runs on `stream` (a cudaStream_t,
+ * NULL = default stream) and synchronises it. */
+int fs_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks_out,
+                     void* stream);
+
+/* Number of kernels the library launched on the handle since creation. */
+int fs_kernel_launches(const fs_handle* h, int64_t* count_out);
+
+/* Name of the GEMM path serving the handle's weight matrices. */
+const char* fs_gemm_path(const fs_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FS_H_ */

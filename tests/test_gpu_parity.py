@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA path through the C ABI against the f32 oracle.
+
+Tolerances (float): bf16 paths max-abs 5e-2 and cosine >= 0.9995 per
+(lane, step) logits row; the f32 path max-abs 2e-3. Integers (tokens where
+decisive, positions, page tables) are compared exactly. Batch invariance is
+bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle.core as O
+from oracle import pages as P
+from continuous_transformer_decode_gb300 import fs, synth
+from tests import _gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+T = synth.MODEL_T
+BF16_MAX_ABS, BF16_MIN_COS = 5e-2, 0.9995
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from continuous_transformer_decode_gb300 import build
+    build.build()
+    O.set_threads(8)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    W = synth.make_weights(T, seed=1, fmt="f32")
+    return W, O.Model(T, W, O.F32)
+
+
+def test_tiny_f32_teacher_forced_and_free_running(tiny):
+    W, m = tiny
+    prompts = synth.make_prompts(4, [3, 5, 7, 9], T["V"], seed=2)
+    seqs, ref = U.oracle_runs(m, prompts, 8)
+    h = U.make_gpu(T, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=4)
+    try:
+        got = U.gpu_teacher_forced(h, T, [0, 1, 2, 3], seqs, T["V"])
+        for b in range(4):
+            err, cos = U.compare_logits(got[b], ref[b], 2e-3, 0.99999)
+            # free-running greedy tokens equal the oracle's outright
+            assert np.array_equal(np.argmax(got[b], -1), np.argmax(ref[b], -1))
+        # positions, page tables and KV against the oracle / page model
+        pm = P.PageModel(16, 16, 4, 4)
+        for t in range(max(len(s) for s in seqs)):
+            ls = [b for b in range(4) if t < len(seqs[b])]
+            assert pm.step(ls, [t] * len(ls), [0] * len(ls), T["V"]) == P.OK
+        for b in range(4):
+            assert fs.fs_lane_length(h, b) == len(seqs[b])
+            assert fs.fs_lane_pages(h, b) == pm.table(b)
+        ln = m.lane(64)
+        for tok in seqs[3]:
+            m.step(ln, tok)
+        for l in range(T["L"]):
+            k, v = fs.fs_lane_export_kv(h, 3, l, T["Hkv"], T["hd"])
+            assert np.abs(k - ln.export(l, "K")).max() < 1e-4
+            assert np.abs(v - ln.export(l, "V")).max() < 1e-4
+    finally:
+        fs.fs_destroy(h)
+
+
+def test_tiny_batch_invariance_bitwise(tiny):
+    W, m = tiny
+    h = U.make_gpu(T, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=8)
+    try:
+        seq = [int(t) for t in synth.make_prompts(1, 10, T["V"], seed=3)[0]]
+        others = synth.make_prompts(7, 10, T["V"], seed=4)
+        solo = U.gpu_teacher_forced(h, T, [5], [seq], T["V"])[0]
+        for k in range(8):
+            fs.fs_lane_reset(h, k)
+        mixed = U.gpu_teacher_forced(
+            h, T, [2, 0, 7, 1, 3], [others[0], others[1], seq, others[2], others[3]],
+            T["V"])[2]
+        assert np.array_equal(solo.view(np.uint32), mixed.view(np.uint32))
+    finally:
+        fs.fs_destroy(h)
+
+
+@pytest.fixture(scope="module")
+def smol_l2():
+    cfg = synth.with_layers(synth.MODEL_S, 2)
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    return cfg, Wb, O.Model(cfg, Wb, O.BF16)
+
+
+def test_smollm2_bf16_two_layers_parity(smol_l2):
+    cfg, Wb, m = smol_l2
+    prompts = synth.make_prompts(5, [16, 1, 7, 16, 12], cfg["V"], seed=2)
+    seqs, ref = U.oracle_runs(m, prompts, 12)
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=8)
+    try:
+        got = U.gpu_teacher_forced(h, cfg, [0, 3, 4, 6, 7], seqs, cfg["V"])
+        worst = 0.0
+        for b in range(5):
+            err, _ = U.compare_logits(got[b], ref[b], BF16_MAX_ABS, BF16_MIN_COS)
+            worst = max(worst, err)
+        for b in range(5):
+            U.decisive_token_agreement(got[b], ref[b], worst)
+    finally:
+        fs.fs_destroy(h)
+
+
+def test_smollm2_bf16_batch_invariance(smol_l2):
+    cfg, Wb, m = smol_l2
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=64, max_pos=32)
+    try:
+        seq = [int(t) for t in synth.make_prompts(1, 6, cfg["V"], seed=5)[0]]
+        base = U.gpu_teacher_forced(h, cfg, [9], [seq], cfg["V"])[0]
+        for B in (3, 17, 64):
+            for k in range(64):
+                fs.fs_lane_reset(h, k)
+            others = synth.make_prompts(B - 1, 6, cfg["V"], seed=100 + B)
+            lanes = list(range(B))
+            where = B // 2
+            seqs = others[:where] + [seq] + others[where:]
+            got = U.gpu_teacher_forced(h, cfg, lanes, seqs, cfg["V"])[where]
+            assert np.array_equal(base.view(np.uint32), got.view(np.uint32)), B
+    finally:
+        fs.fs_destroy(h)
+
+
+def test_smollm2_q8_parity_and_gate(smol_l2):
+    cfg, Wb, m_f32 = smol_l2
+    Wq = U.quantize_weights(Wb)
+    mq = O.Model(cfg, Wq, O.Q8_0)
+    prompts = synth.make_prompts(3, 16, cfg["V"], seed=2)
+    seqs, ref_q = U.oracle_runs(mq, prompts, 12)
+    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=4)
+    try:
+        got = U.gpu_teacher_forced(h, cfg, [0, 1, 2], seqs, cfg["V"])
+        for b in range(3):
+            U.compare_logits(got[b], ref_q[b], BF16_MAX_ABS, BF16_MIN_COS)
+        # the pages' Q8 gate against the f32 oracle on the same tokens
+        agree, cos, n = 0, [], 0
+        for b in range(3):
+            ln = m_f32.lane(64)
+            for t, tok in enumerate(seqs[b]):
+                r = m_f32.step(ln, tok)
+                if t == len(prompts[b]) - 1:
+                    srt = np.sort(r)
+                    if srt[-1] - srt[-2] > 0.05:
+                        assert np.argmax(r) == np.argmax(got[b][t])
+                if t >= len(prompts[b]) - 1:
+                    agree += int(np.argmax(r) == np.argmax(got[b][t]))
+                    g = got[b][t]
+                    cos.append(np.dot(r, g) / np.linalg.norm(r) / np.linalg.norm(g))
+                    n += 1
+        assert agree / n >= 0.80 and np.mean(cos) >= 0.99
+    finally:
+        fs.fs_destroy(h)
+
+
+def test_q8_quantiser_matches_oracle_bitwise():
+    import torch
+    g = np.random.default_rng(8)
+    x = (g.standard_normal(32 * 4096) * 0.02).astype(np.float32)
+    x[:32] = 0.0
+    x[32:64] *= 1000
+    ref = O.quantize_q8_0(x)
+    src = torch.from_numpy(x).cuda()
+    out = torch.empty((x.size // 32, 34), dtype=torch.uint8, device="cuda")
+    fs.fs_quantize_q8_0(src, out)
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_sampler_greedy_and_temperature_against_oracle(smol_l2):
+    import torch
+    cfg, Wb, m = smol_l2
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=8)
+    try:
+        n = 8
+        buf = torch.empty((n, cfg["V"]), dtype=torch.float32, device="cuda")
+        toks = synth.make_prompts(1, n, cfg["V"], seed=6)[0]
+        fs.fs_decode_step_batch(h, list(range(n)), np.zeros(n, np.int32), toks,
+                                logits_out=buf)
+        lg = buf.cpu().numpy()
+        greedy = fs.fs_sample(h, np.zeros(n), np.zeros(n), np.zeros(n))
+        assert greedy.tolist() == [O.sample(lg[i]) for i in range(n)]
+        mismatch = 0
+        for c in range(40):
+            temps = np.array([0.8, 1.0, 0.5, 2.0, 0.8, 1.3, 0.7, 1.0], np.float32)
+            seeds = np.arange(n, dtype=np.uint64) * 7919 + 11
+            ctr = np.full(n, c, dtype=np.uint64)
+            got = fs.fs_sample(h, temps, seeds, ctr)
+            for i in range(n):
+                want = O.sample(lg[i], float(temps[i]), int(seeds[i]), c)
+                mismatch += int(got[i] != want)
+        assert mismatch == 0
+    finally:
+        fs.fs_destroy(h)
+
+
+def test_error_paths_are_atomic(tiny):
+    W, m = tiny
+    h = U.make_gpu(T, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=4,
+                   max_pos=32, n_pages=3)
+    try:
+        pos = fs.fs_decode_step_batch(h, [0, 1], np.array([0, 0], np.int32), [1, 2])
+        assert pos.tolist() == [1, 1]
+        before = ([fs.fs_lane_pages(h, k) for k in range(4)],
+                  [fs.fs_lane_length(h, k) for k in range(4)])
+        cases = [([0, 0], [1, 1], [1, 1], "FS_ERR_DUP_LANE"),
+                 ([0], [0], [1], "FS_ERR_POSITION"),
+                 ([0], [1], [T["V"]], "FS_ERR_TOKEN"),
+                 ([4], [0], [1], "FS_ERR_LANE"),
+                 ([2, 3], [0, 0], [1, 1], "FS_ERR_KV_FULL")]  # 1 page left
+        for ls, ps, ts, name in cases:
+            with pytest.raises(fs.FsError) as e:
+                fs.fs_decode_step_batch(h, ls, np.array(ps, np.int32), ts)
+            assert e.value.name == name
+        after = ([fs.fs_lane_pages(h, k) for k in range(4)],
+                 [fs.fs_lane_length(h, k) for k in range(4)])
+        assert before == after
+        # n == 0 is a no-op; sampling with a different n is refused
+        fs.fs_decode_step_batch(h, [], np.zeros(0, np.int32), [])
+        with pytest.raises(fs.FsError):
+            fs.fs_sample(h, [0.0], [0], [0])
+        # reset frees pages; the lane then computes exactly as a fresh one
+        fs.fs_lane_reset(h, 0)
+        assert fs.fs_lane_pages(h, 0) == [] and fs.fs_lane_length(h, 0) == 0
+    finally:
+        fs.fs_destroy(h)
