@@ -156,7 +156,8 @@ def run_ours(args, wl, ws, rank, local):
     desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps)
     h = fs.fs_create(desc, Wt)
     del Wt
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
     fs.fs_set_stream(h, stream)
     lanes = np.arange(B, dtype=np.int32)
     if "ctx" in wl:  # long synthetic contexts: random KV (content irrelevant)

@@ -11,8 +11,10 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <set>
 #include <string>
 #include <vector>
@@ -28,11 +30,30 @@ thread_local std::string g_create_error;
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// tcgen05 operand map and the fixed K split of one weight matrix.
+struct TcW {
+  CUtensorMap tm;
+  int m_tiles = 0, splits = 1;
+};
+
 struct LayerW {
   Mat qkv, o, gateup, down;
+  TcW qkv_tc, o_tc, gateup_tc, down_tc;
   float* g_attn = nullptr;
   float* g_ffn = nullptr;
 };
+
+// K split of a weight matrix: enough (128-row tile, K range) units to cover
+// the SMs, at least two 64-wide K blocks per unit, and fewer splits the more
+// lanes the handle can batch (the split partials grow with the lanes). It
+// depends on the matrix and the handle only, never on a call's lane count.
+int choose_splits(int m_tiles, int kb, int max_lanes) {
+  const int cap = max_lanes <= 64 ? 8 : (max_lanes <= 256 ? 4 : 2);
+  int s = (152 + m_tiles - 1) / m_tiles;
+  s = std::min(s, std::max(1, kb / 2));
+  s = std::min(s, cap);
+  return std::max(1, s);
+}
 
 }  // namespace
 
@@ -48,6 +69,13 @@ struct fs_handle {
 
   std::vector<LayerW> layers;
   Mat embed, head;
+  TcW head_tc;
+  bool use_tc = false;
+  CUtensorMap tm_h, tm_o, tm_a;  // panels (box 16 lanes)
+  float* ws = nullptr;
+  int* counters = nullptr;
+  int* err_flag = nullptr;  // mapped pinned host memory
+  int* d_err_flag = nullptr;
   float* g_final = nullptr;
   std::vector<void*> allocs;  // every cudaMalloc of the handle
 
@@ -85,6 +113,13 @@ struct fs_handle {
 
   int last_n = -1;
   const float* last_logits = nullptr;
+  // one CUDA graph per lane count n (steps whose logits stay internal)
+  struct Graph {
+    cudaGraphExec_t exec = nullptr;
+    int64_t kernels = 0;
+  };
+  std::map<int, Graph> graphs;
+  bool graphs_on = true;
   int64_t launches = 0;
   std::string err;
 
@@ -237,8 +272,15 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   h->Kp_f = (int)round_up(d.d_ffn, 64);
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;
+  {
+    const char* env = getenv("FS_GEMM_PATH");
+    const bool force_gemv = env && std::string(env) == "gemv";
+    h->use_tc = h->wtype == W_BF16 && d.d_ffn % 64 == 0 && !force_gemv && tc_available();
+    const char* genv = getenv("FS_GRAPHS");
+    h->graphs_on = !(genv && std::string(genv) == "0");
+  }
 
-  FS_CK(h, cudaStreamCreateWithFlags(&h->own_stream, cudaStreamNonBlocking));
+  FS_CK(h, cudaStreamCreateWithFlags(&h->own_stream, cudaStreamDefault));
   h->stream = h->own_stream;
   FS_CK(h, cudaEventCreateWithFlags(&h->args_done, cudaEventDisableTiming));
 
@@ -292,8 +334,22 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     if ((rc = alloc_mat(h, &L.o, d.d_model, h->Nq))) return rc;
     if ((rc = upload_rows(h, &L.o, s.wo, d.d_model, h->Nq, 0, staging))) return rc;
     if ((rc = alloc_mat(h, &L.gateup, 2 * d.d_ffn, d.d_model))) return rc;
-    if ((rc = upload_rows(h, &L.gateup, s.w_gate, d.d_ffn, d.d_model, 0, staging))) return rc;
-    if ((rc = upload_rows(h, &L.gateup, s.w_up, d.d_ffn, d.d_model, d.d_ffn, staging))) return rc;
+    if (h->use_tc) {
+      // 128-row tiles of 64 gate rows then the 64 matching up rows
+      const size_t rb = (size_t)d.d_model * 2;
+      for (int t = 0; t < d.d_ffn / 64; ++t) {
+        if ((rc = upload_rows(h, &L.gateup, (const char*)s.w_gate + (size_t)t * 64 * rb, 64,
+                              d.d_model, 128 * t, staging)))
+          return rc;
+        if ((rc = upload_rows(h, &L.gateup, (const char*)s.w_up + (size_t)t * 64 * rb, 64,
+                              d.d_model, 128 * t + 64, staging)))
+          return rc;
+      }
+    } else {
+      if ((rc = upload_rows(h, &L.gateup, s.w_gate, d.d_ffn, d.d_model, 0, staging))) return rc;
+      if ((rc = upload_rows(h, &L.gateup, s.w_up, d.d_ffn, d.d_model, d.d_ffn, staging)))
+        return rc;
+    }
     if ((rc = alloc_mat(h, &L.down, d.d_model, d.d_ffn))) return rc;
     if ((rc = upload_rows(h, &L.down, s.w_down, d.d_model, d.d_ffn, 0, staging))) return rc;
     if ((rc = upload_vec(&L.g_attn, s.attn_norm, d.d_model))) return rc;
@@ -359,6 +415,37 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
   FS_CK(h, cudaMemset(h->apanel, 0, (size_t)B * h->Kp_f * xs));
   FS_CK(h, cudaHostAlloc((void**)&h->h_args, (size_t)(7 * B + 1) * 4, cudaHostAllocDefault));
+  FS_CK(h, cudaHostAlloc((void**)&h->err_flag, 16, cudaHostAllocMapped));
+  *h->err_flag = 0;
+  FS_CK(h, cudaHostGetDevicePointer((void**)&h->d_err_flag, h->err_flag, 0));
+  if (h->use_tc) {
+    const int n_tot_max = (int)round_up(std::min(B, 512), 16);
+    size_t ws_elems = 0;
+    int max_tiles = 1;
+    auto setup = [&](const Mat& m, TcW* t) -> int {
+      t->m_tiles = (m.N + 127) / 128;
+      t->splits = choose_splits(t->m_tiles, m.Kp / 64, B);
+      max_tiles = std::max(max_tiles, t->m_tiles);
+      if (t->splits > 1)
+        ws_elems = std::max(ws_elems, (size_t)t->splits * n_tot_max * t->m_tiles * 128);
+      if (tc_make_map(m.w, m.N, m.Kp, 128, &t->tm)) return h->fail(FS_ERR_CUDA, "tensor map");
+      return FS_OK;
+    };
+    for (auto& L : h->layers) {
+      if ((rc = setup(L.qkv, &L.qkv_tc)) || (rc = setup(L.o, &L.o_tc)) ||
+          (rc = setup(L.gateup, &L.gateup_tc)) || (rc = setup(L.down, &L.down_tc)))
+        return rc;
+    }
+    if ((rc = setup(h->head, &h->head_tc))) return rc;
+    if (tc_make_map(h->hpanel, B, h->Kp_d, 16, &h->tm_h) ||
+        tc_make_map(h->opanel, B, h->Kp_q, 16, &h->tm_o) ||
+        tc_make_map(h->apanel, B, h->Kp_f, 16, &h->tm_a))
+      return h->fail(FS_ERR_CUDA, "panel tensor map");
+    if (h->alloc(&h->ws, std::max<size_t>(ws_elems, 1) * 4) != cudaSuccess ||
+        h->alloc(&h->counters, (size_t)max_tiles * 4) != cudaSuccess)
+      return h->fail(FS_ERR_OOM, "GEMM workspace allocation failed");
+    FS_CK(h, cudaMemset(h->counters, 0, (size_t)max_tiles * 4));
+  }
   FS_CK(h, cudaHostAlloc((void**)&h->h_samp, (size_t)B * 24, cudaHostAllocDefault));
   int32_t* a = h->d_args;
   h->args.lane = a;
@@ -378,12 +465,15 @@ void destroy_impl(fs_handle* h) {
   h->allocs.clear();
   if (h->h_args) cudaFreeHost(h->h_args);
   if (h->h_samp) cudaFreeHost(h->h_samp);
+  if (h->err_flag) cudaFreeHost(h->err_flag);
   if (h->args_done) cudaEventDestroy(h->args_done);
   for (auto& r : h->prof_pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
   }
   for (cudaEvent_t e : h->prof_pool) cudaEventDestroy(e);
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.second.exec);
+  h->graphs.clear();
   if (h->own_stream) cudaStreamDestroy(h->own_stream);
 }
 
@@ -412,6 +502,85 @@ int seed_lane_pages(fs_handle* h, int lane, int n) {
     FS_CK(h, cudaMemcpyAsync(h->kv.pt + (size_t)lane * h->kv.max_pages, h->pt[lane].data(),
                              (size_t)need * 4, cudaMemcpyHostToDevice, h->stream));
   return FS_OK;
+}
+
+// Enqueues every kernel of one step for the n panel rows on h->stream (the
+// per-step arguments are read from device memory, so the sequence can be
+// captured once per n and replayed).
+void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
+  const fs_model_desc& d = h->d;
+  cudaStream_t s = h->stream;
+  const StepArgs& args = h->args;
+  const double xs = h->xtype == X_F32 ? 4.0 : 2.0;
+  const double kvs = h->kv.kv_f32 ? 4.0 : 2.0;
+  auto wbytes = [&](const Mat& m) {
+    double b = (double)m.N * m.K * (m.wtype == W_F32 ? 4 : (m.wtype == W_BF16 ? 2 : 1));
+    if (m.wtype == W_Q8) b += (double)m.N * (m.K / 32) * 2;
+    return b;
+  };
+  // algorithmic bytes: weights once, activations in, outputs out
+  auto gemm = [&](const Mat& W, const TcW& T, const CUtensorMap& tmX, const void* X, int epi,
+                  float* of, void* ox, int ldo, int n_out) {
+    double bytes = wbytes(W) + (double)n * W.K * xs;
+    bytes += epi == EPI_SWIGLU ? (double)n * n_out * xs
+             : (double)n * n_out * 4.0 * (epi == EPI_RESID ? 2 : 1);
+    if (!h->use_tc) {
+      GemmArgs g{};
+      g.W = W; g.X = X; g.x_type = h->xtype; g.B = n; g.epi = epi;
+      g.out_f32 = of; g.out_x = ox; g.ldo = ldo; g.n_out = n_out;
+      h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemv(g, s); });
+      return;
+    }
+    for (int lane0 = 0; lane0 < n; lane0 += 512) {  // passes of up to 512 lanes
+      TcParams p{};
+      p.m_tiles = T.m_tiles; p.splits = T.splits; p.kb_total = W.Kp / 64;
+      p.lanes = std::min(512, n - lane0); p.lane0 = lane0;
+      p.n_tot = (int)round_up(p.lanes, 16);
+      p.tmem_cols = 32;
+      while (p.tmem_cols < p.n_tot) p.tmem_cols *= 2;
+      p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
+      p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
+      const double share = (double)p.lanes / n;
+      h->launch(FS_PROF_GEMM, lane0 == 0 ? bytes * share + wbytes(W) * (1 - share)
+                                         : bytes * share,
+                [&] { return launch_gemm_tc(T.tm, tmX, p, s); });
+    }
+  };
+  const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
+  h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
+    return launch_embed(h->embed, args, n, n, h->kv, h->x, d.d_model, s);
+  });
+  for (int l = 0; l < d.n_layers; ++l) {
+    const LayerW& W = h->layers[l];
+    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+      return launch_rmsnorm(h->x, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                            h->Kp_d, s);
+    });
+    gemm(W.qkv, W.qkv_tc, h->tm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
+    h->launch(FS_PROF_OTHER,
+              (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
+                return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
+                                          h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
+              });
+    h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
+      return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
+                              h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
+                              h->Kp_q, s);
+    });
+    gemm(W.o, W.o_tc, h->tm_o, h->opanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
+    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+      return launch_rmsnorm(h->x, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                            h->Kp_d, s);
+    });
+    gemm(W.gateup, W.gateup_tc, h->tm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
+         d.d_ffn);
+    gemm(W.down, W.down_tc, h->tm_a, h->apanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
+  }
+  h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+    return launch_rmsnorm(h->x, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                          h->Kp_d, s);
+  });
+  gemm(h->head, h->head_tc, h->tm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
 }
 
 }  // namespace
@@ -516,65 +685,33 @@ int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
                            cudaMemcpyHostToDevice, h->stream));
   FS_CK(h, cudaEventRecord(h->args_done, h->stream));
 
-  // ---- the step
-  cudaStream_t s = h->stream;
-  const StepArgs& args = h->args;
-  const double xs = h->xtype == X_F32 ? 4.0 : 2.0;
-  const double kvs = h->kv.kv_f32 ? 4.0 : 2.0;
-  auto wbytes = [&](const Mat& m) {
-    double b = (double)m.N * m.K * (m.wtype == W_F32 ? 4 : (m.wtype == W_BF16 ? 2 : 1));
-    if (m.wtype == W_Q8) b += (double)m.N * (m.K / 32) * 2;
-    return b;
-  };
-  // algorithmic bytes: weights once, activations in, outputs out
-  auto gemm = [&](const Mat& W, const void* X, int epi, float* of, void* ox, int ldo,
-                  int n_out) {
-    GemmArgs g{};
-    g.W = W; g.X = X; g.x_type = h->xtype; g.B = n; g.epi = epi;
-    g.out_f32 = of; g.out_x = ox; g.ldo = ldo; g.n_out = n_out;
-    double bytes = wbytes(W) + (double)n * W.K * xs;
-    bytes += epi == EPI_SWIGLU ? (double)n * n_out * xs
-             : (double)n * n_out * 4.0 * (epi == EPI_RESID ? 2 : 1);
-    h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemv(g, s); });
-  };
+  // ---- the step: one graph replay, or the kernels one by one
   double kv_read = 0.0;  // K and V bytes attention reads per layer
   for (int i = 0; i < n; ++i)
-    kv_read += (double)(h->len[lanes[i]] + 1) * h->Nkv * 2.0 * kvs;
-  const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
-  h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
-    return launch_embed(h->embed, args, n, n_upd, h->kv, h->x, d.d_model, s);
-  });
-  for (int l = 0; l < d.n_layers; ++l) {
-    const LayerW& W = h->layers[l];
-    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-      return launch_rmsnorm(h->x, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                            h->Kp_d, s);
-    });
-    gemm(W.qkv, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
-    h->launch(FS_PROF_OTHER,
-              (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
-                return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
-                                          h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
-              });
-    h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
-      return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
-                              h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
-                              h->Kp_q, s);
-    });
-    gemm(W.o, h->opanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
-    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-      return launch_rmsnorm(h->x, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                            h->Kp_d, s);
-    });
-    gemm(W.gateup, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f, d.d_ffn);
-    gemm(W.down, h->apanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
-  }
-  h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-    return launch_rmsnorm(h->x, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                          h->Kp_d, s);
-  });
+    kv_read += (double)(h->len[lanes[i]] + 1) * h->Nkv * 2.0 * (h->kv.kv_f32 ? 4.0 : 2.0);
   float* out = logits_out ? logits_out : h->logits;
-  gemm(h->head, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  if (!logits_out && !h->prof_on && h->graphs_on) {
+    auto it = h->graphs.find(n);
+    if (it == h->graphs.end()) {
+      const int64_t before = h->launches;
+      cudaGraph_t g = nullptr;
+      FS_CK(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+      enqueue_step(h, n, out, kv_read);
+      cudaError_t e = cudaStreamEndCapture(h->stream, &g);
+      if (e != cudaSuccess) return h->cuda_fail(e, "cudaStreamEndCapture");
+      fs_handle::Graph G;
+      e = cudaGraphInstantiate(&G.exec, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return h->cuda_fail(e, "cudaGraphInstantiate");
+      G.kernels = h->launches - before;
+      h->launches = before;
+      it = h->graphs.emplace(n, G).first;
+    }
+    FS_CK(h, cudaGraphLaunch(it->second.exec, h->stream));
+    h->launches += it->second.kernels;
+  } else {
+    enqueue_step(h, n, out, kv_read);
+  }
   FS_CK(h, cudaGetLastError());
 
   for (int i = 0; i < n; ++i) {
@@ -616,6 +753,9 @@ int fs_sample(fs_handle* h, int32_t n, const float* temps, const uint64_t* seeds
   FS_CK(h, cudaMemcpyAsync(ho, h->d_tokens, (size_t)n * 4, cudaMemcpyDeviceToHost, s));
   FS_CK(h, cudaStreamSynchronize(s));
   std::memcpy(tokens_out, ho, (size_t)n * 4);
+  if (*(volatile int*)h->err_flag)
+    return h->fail(FS_ERR_DEVICE, "a GEMM block timed out waiting on a barrier (code " +
+                                      std::to_string(*(volatile int*)h->err_flag) + ")");
   return FS_OK;
 }
 
@@ -659,6 +799,15 @@ int fs_profile_read(fs_handle* h, int32_t cls, double* ms_out, int64_t* launches
   h->prof_ms[cls] = 0.0;
   h->prof_n[cls] = 0;
   h->prof_bytes[cls] = 0.0;
+  return FS_OK;
+}
+
+int fs_copy_logits(fs_handle* h, float* dst) {
+  if (!h || !dst) return FS_ERR_ARG;
+  if (h->last_n < 0) return h->fail(FS_ERR_STATE, "no decode step yet");
+  FS_CK(h, cudaMemcpyAsync(dst, h->last_logits, (size_t)h->last_n * h->d.vocab * 4,
+                           cudaMemcpyDefault, h->stream));
+  FS_CK(h, cudaStreamSynchronize(h->stream));
   return FS_OK;
 }
 
@@ -776,8 +925,71 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out) {
 }
 
 const char* fs_gemm_path(const fs_handle* h) {
-  (void)h;
-  return "warp-gemv";
+  if (!h) return "";
+  return h->use_tc ? "tcgen05" : "warp-gemv";
+}
+
+int fs_device_error(fs_handle* h, int32_t* code_out) {
+  if (!h || !code_out) return FS_ERR_ARG;
+  FS_CK(h, cudaStreamSynchronize(h->stream));
+  *code_out = *(volatile int*)h->err_flag;
+  *(volatile int*)h->err_flag = 0;
+  return FS_OK;
+}
+
+int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,
+                 float* Y, int32_t splits, int32_t path, void* stream) {
+  using namespace fsk;
+  if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
+      splits > K / 64 || splits > 8 || (path != 0 && path != 1))
+    return FS_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  Mat m;
+  m.w = W; m.N = N; m.K = K; m.Kp = K; m.wtype = W_BF16;
+  if (path == 0) {
+    GemmArgs g{};
+    g.W = m; g.X = X; g.x_type = X_BF16; g.B = B; g.epi = EPI_STORE;
+    g.out_f32 = Y; g.ldo = N; g.n_out = N;
+    launch_gemv(g, s);
+    if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+  }
+  CUtensorMap tw, tx;
+  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx)) return FS_ERR_CUDA;
+  const int m_tiles = (N + 127) / 128;
+  float* ws = nullptr;
+  int *cnt = nullptr, *err = nullptr;
+  const int n_tot0 = (int)round_up(std::min(B, 512), 16);
+  int rc = FS_OK;
+  if (cudaMalloc(&ws, (size_t)splits * n_tot0 * m_tiles * 128 * 4) != cudaSuccess ||
+      cudaMalloc(&cnt, (size_t)m_tiles * 4) != cudaSuccess ||
+      cudaMalloc(&err, 4) != cudaSuccess) {
+    rc = FS_ERR_OOM;
+  } else {
+    cudaMemsetAsync(cnt, 0, (size_t)m_tiles * 4, s);
+    cudaMemsetAsync(err, 0, 4, s);
+    for (int lane0 = 0; lane0 < B; lane0 += 512) {
+      TcParams p{};
+      p.m_tiles = m_tiles; p.splits = splits; p.kb_total = K / 64;
+      p.lanes = std::min(512, B - lane0); p.lane0 = lane0;
+      p.n_tot = (int)round_up(p.lanes, 16);
+      p.tmem_cols = 32;
+      while (p.tmem_cols < p.n_tot) p.tmem_cols *= 2;
+      p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
+      p.ws = ws; p.counters = cnt; p.err = err;
+      launch_gemm_tc(tw, tx, p, s);
+    }
+    int herr = 0;
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      rc = FS_ERR_CUDA;
+    else if (herr)
+      rc = FS_ERR_DEVICE;
+  }
+  cudaFree(ws);
+  cudaFree(cnt);
+  cudaFree(err);
+  return rc;
 }
 
 }  // extern "C"

@@ -2,6 +2,7 @@
 // kernel translation units. Not installed; not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -66,6 +67,29 @@ struct GemmArgs {
 
 // Launchers (each returns the number of kernels launched).
 int launch_gemv(const GemmArgs& a, cudaStream_t s);
+
+// tcgen05 GEMM (bf16 weights and panels). Work unit = (128-row tile,
+// K split); grid = m_tiles * splits.
+struct TcParams {
+  int m_tiles, splits, kb_total;
+  int lanes;     // valid lanes in this pass
+  int lane0;     // first panel row of this pass
+  int n_tot;     // lanes rounded up to 16 (<= 512)
+  int tmem_cols; // power of two >= max(32, n_tot)
+  int stages, stage_bytes;  // set by the launcher
+  int epi;
+  float* out_f32;
+  void* out_x;
+  int ldo;
+  int n_out;     // output rows (W rows, or F for SwiGLU)
+  float* ws;     // split partials [splits][n_tot][m_tiles * 128]
+  int* counters; // [m_tiles], zero between launches
+  int* err;      // device-visible error flag
+};
+bool tc_available();
+int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
+int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
+                   cudaStream_t s);
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
                  const KV& kv, float* x, int d, cudaStream_t s);

@@ -1,0 +1,432 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// Y[b, n] = sum_k X[b, k] * W[n, k] over the B lanes of the step panel: the
+// seven projections and the LM head of every lane run as one GEMM per weight
+// matrix, so each weight byte is read once per step ("MODEL-BATCHING-
+// RESULTS", "The lever").
+//
+// Swap-AB: the weight tile is the M = 128 operand (rows of W), the lanes are
+// the N operand, so one 128-row weight tile serves every lane and small B
+// costs no weight re-reads. Operands are staged by TMA into 128-byte-swizzled
+// shared memory; the f32 accumulator lives in tensor memory (TMEM).
+//
+// Block = 6 warps: warp 4 issues TMA loads, warp 5 owns TMEM and issues the
+// MMAs, warps 0-3 run the epilogue (warp w reads TMEM lanes 32w..32w+31,
+// i.e. weight rows; each thread then holds one output row for every lane).
+// A block owns one (128-row tile, K range) work unit. With a K split > 1 the
+// partial tiles go to a workspace and the last block of the row tile to
+// arrive sums them in split order, so results never depend on timing. The
+// split count depends only on the matrix shape and the handle's lane
+// capacity, never on the number of lanes in a call: a lane's output is then
+// independent of the batch it is computed in.
+//
+// Every wait on an mbarrier is bounded (1 s of %globaltimer); on timeout the
+// block records an error code, stops issuing work, drains the TMA loads it
+// issued (again bounded), frees its TMEM and exits.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fs_internal.h"
+
+namespace fsk {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                 // bf16 elements per 128-byte row
+constexpr int kThreads = 192;
+constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kXBoxRows = 16;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!mbar_test(bar, parity))
+    if (gtimer() - t0 > kWaitNs) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x,
+                                            int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 B
+// apart (stride byte offset), descriptor version 1, layout SWIZZLE_128B (2).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// kind::f16 instruction descriptor: D f32, A and B bf16, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void epi_bar() {  // the 128 epilogue threads
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+// 16 consecutive f32 columns of this thread's TMEM lane; the caller waits
+// (tmem_wait) before reading the registers, so several loads can be in
+// flight together.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+constexpr int kMaxSplits = 8;
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Writes one 16-lane chunk of final values of this thread's row.
+// For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
+// rows; the up half hands its values to the gate half through shared memory.
+__device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int row_local,
+                                           int c0, const float v[16], float* xbuf) {
+  if (p.epi == EPI_SWIGLU) {
+    if (row_local >= 64) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xbuf[(row_local - 64) * 17 + j] = v[j];
+    }
+    epi_bar();
+    if (row_local < 64) {
+      const int f = m_tile * 64 + row_local;
+      if (f < p.n_out) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int b = c0 + j;
+          if (b < p.lanes) {
+            const float a = silu(v[j]) * xbuf[row_local * 17 + j];
+            static_cast<__nv_bfloat16*>(p.out_x)[(int64_t)(p.lane0 + b) * p.ldo + f] =
+                __float2bfloat16_rn(a);
+          }
+        }
+      }
+    }
+    epi_bar();
+    return;
+  }
+  const int row = m_tile * kBM + row_local;
+  if (row >= p.n_out) return;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int b = c0 + j;
+    if (b < p.lanes) {
+      float* o = p.out_f32 + (int64_t)(p.lane0 + b) * p.ldo + row;
+      if (p.epi == EPI_RESID)
+        *o += v[j];
+      else
+        *o = v[j];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x / p.splits, split = blockIdx.x - m_tile * p.splits;
+  const int kb0 = split * p.kb_total / p.splits;
+  const int kb1 = (split + 1) * p.kb_total / p.splits;
+  const int nkb = kb1 - kb0;
+  const int S = p.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S),
+                 accum = smem_u32(bars + 2 * S);
+  const uint32_t ncols = p.tmem_cols;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accum, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_abort = 0;
+    s_last = 0;
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 4) {
+    if (lane == 0) {  // ---- TMA producer
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+          atomicExch(p.err, 1);
+          s_abort = 1;
+          break;
+        }
+        if (*(volatile int*)&s_abort) break;
+        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)p.stage_bytes);
+        const int x = (kb0 + i) * kBK;
+        tma_load_2d(st, &tmW, x, m_tile * kBM, full0 + 8 * s);
+        for (int r = 0; r < p.n_tot; r += kXBoxRows)
+          tma_load_2d(st + kWTileBytes + r * 128, &tmX, x, p.lane0 + r, full0 + 8 * s);
+        issued = i + 1;
+      }
+      // drain: every issued load must have landed before the block exits
+      for (int i = 0; i < issued; ++i) {
+        if (i < issued - S) continue;
+        const int s = i % S;
+        if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) atomicExch(p.err, 2);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // ---- MMA issuer
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        if (!mbar_wait(full0 + 8 * s, ph) || *(volatile int*)&s_abort) {
+          atomicExch(p.err, 3);
+          s_abort = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint32_t b0 = a0 + kWTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = sw128_desc(a0 + kk * 32);
+          for (int c = 0; c * 256 < p.n_tot; ++c) {
+            const int nc = min(256, p.n_tot - c * 256);
+            const uint64_t bd = sw128_desc(b0 + c * 256 * 128 + kk * 32);
+            mma_bf16(tmem + c * 256, ad, bd, idesc_bf16(kBM, nc),
+                     (i > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
+      }
+      mma_commit(accum);  // arrives when every MMA issued above has finished
+    }
+  } else {  // ---- epilogue, warps 0-3
+    const int row_local = warp * 32 + lane;
+    float* xbuf = reinterpret_cast<float*>(smem);  // stages are idle by now
+    if (!mbar_wait(accum, 0)) {
+      atomicExch(p.err, 4);
+      s_abort = 1;
+    }
+    tc_fence_after();
+    epi_bar();  // makes the abort decision uniform over the epilogue warps
+    const bool abort = *(volatile int*)&s_abort != 0;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    if (p.splits == 1) {
+      for (int c0 = 0; c0 < p.n_tot; c0 += 32) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(trow + c0, r0);
+        if (c0 + 16 < p.n_tot) tmem_ld16(trow + c0 + 16, r1);
+        tmem_wait();
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r0[j]);
+        if (!abort) emit_chunk(p, m_tile, row_local, c0, v, xbuf);
+        if (c0 + 16 < p.n_tot) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r1[j]);
+          if (!abort) emit_chunk(p, m_tile, row_local, c0 + 16, v, xbuf);
+        }
+      }
+    } else {
+      const int64_t R = (int64_t)p.m_tiles * kBM;
+      const int64_t row = (int64_t)m_tile * kBM + row_local;
+      for (int c0 = 0; c0 < p.n_tot; c0 += 32) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(trow + c0, r0);
+        if (c0 + 16 < p.n_tot) tmem_ld16(trow + c0 + 16, r1);
+        tmem_wait();
+        float* dst = p.ws + ((int64_t)split * p.n_tot + c0) * R + row;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < p.lanes) dst[(int64_t)j * R] = __uint_as_float(r0[j]);
+        if (c0 + 16 < p.n_tot) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + 16 + j < p.lanes) dst[(int64_t)(16 + j) * R] = __uint_as_float(r1[j]);
+        }
+      }
+      __threadfence();
+      epi_bar();
+      if (threadIdx.x == 0) {
+        const int prev = atomicAdd(p.counters + m_tile, 1);
+        s_last = (prev == p.splits - 1);
+      }
+      epi_bar();
+      if (s_last) {
+        __threadfence();
+        for (int c0 = 0; c0 < p.n_tot; c0 += 16) {
+          // all loads of the chunk first, then the sums in split order
+          float part[kMaxSplits][16];
+#pragma unroll
+          for (int sp = 0; sp < kMaxSplits; ++sp) {
+            if (sp < p.splits) {
+              const float* src = p.ws + ((int64_t)sp * p.n_tot + c0) * R + row;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                part[sp][j] = (c0 + j < p.lanes) ? __ldcg(src + (int64_t)j * R) : 0.0f;
+            }
+          }
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float acc = part[0][j];
+#pragma unroll
+            for (int sp = 1; sp < kMaxSplits; ++sp)
+              if (sp < p.splits) acc += part[sp][j];
+            v[j] = acc;
+          }
+          if (!abort) emit_chunk(p, m_tile, row_local, c0, v, xbuf);
+        }
+        if (threadIdx.x == 0) p.counters[m_tile] = 0;  // ready for the next launch
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(ncols)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
+
+bool tc_available() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                       cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D bf16 map over [rows][Kp] (row stride Kp elements), box [box_rows][64],
+// 128-byte swizzle; reads beyond the rows return zeros.
+int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out) {
+  if (!tc_available()) return -1;
+  cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)Kp * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+// Dynamic shared memory: 1 KB alignment slack, the stages, the barriers.
+// The stage budget leaves room under the 227 KB per-block limit for the
+// kernel's static shared variables.
+constexpr int kSmemAttr = 227 * 1024 - 256;
+int tc_stages_for(int n_tot, int* stage_bytes, int* smem_bytes) {
+  const int sb = kWTileBytes + n_tot * 128;
+  const int budget = kSmemAttr - 1024 - 512;
+  int st = budget / sb;
+  if (st > 8) st = 8;
+  *stage_bytes = sb;
+  *smem_bytes = 1024 + st * sb + 8 * (2 * st + 1);
+  return st;
+}
+
+int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p0,
+                   cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAttr) != cudaSuccess)
+      return 0;  // the launch below then fails and the caller reports it
+    attr_set = true;
+  }
+  TcParams p = p0;
+  int smem = 0;
+  p.stages = tc_stages_for(p.n_tot, &p.stage_bytes, &smem);
+  k_gemm_tc<<<p.m_tiles * p.splits, kThreads, smem, s>>>(tmW, tmX, p);
+  return 1;
+}
+
+}  // namespace fsk

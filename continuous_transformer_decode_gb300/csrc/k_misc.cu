@@ -200,16 +200,23 @@ __global__ void k_quantize_q8_0(const float* __restrict__ x, int64_t nblk,
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float d = amax / 127.0f;
   const float id = d != 0.0f ? 1.0f / d : 0.0f;
-  float q = roundf(v * id);
-  q = fminf(127.0f, fmaxf(-127.0f, q));
+  const float q = fminf(127.0f, fmaxf(-127.0f, roundf(v * id)));
+  const uint32_t code = (uint32_t)(uint8_t)(int8_t)q;
+  const uint32_t dbits = (uint32_t)__half_as_ushort(__float2half_rn(d));
+  // byte t of the 34-byte block: 0-1 scale (little endian), 2+i code i.
+  // Thread j writes byte j, threads 0 and 1 also bytes 32 and 33.
+  const uint32_t code_m2 = __shfl_sync(0xffffffffu, code, (j + 30) & 31);
+  const uint32_t code_30 = __shfl_sync(0xffffffffu, code, 30 + (j & 1));
   uint8_t* ob = blocks + blk * 34;
-  if (j == 0) {
-    const __half hd = __float2half_rn(d);
-    const uint16_t bits = __half_as_ushort(hd);
-    ob[0] = (uint8_t)(bits & 0xff);
-    ob[1] = (uint8_t)(bits >> 8);
-  }
-  ob[2 + j] = (uint8_t)(int8_t)q;
+  uint32_t byte_j;
+  if (j == 0)
+    byte_j = dbits & 0xffu;
+  else if (j == 1)
+    byte_j = (dbits >> 8) & 0xffu;
+  else
+    byte_j = code_m2;
+  ob[j] = (uint8_t)byte_j;
+  if (j < 2) ob[32 + j] = (uint8_t)code_30;
 }
 
 // 34-byte blocks of rows [N][K] -> codes [row_offset + n][Kp], scales.

@@ -87,6 +87,9 @@ def lib():
         "fs_profile_read": (C.c_int, [p, i32, p, p, p]),
         "fs_kernel_launches": (C.c_int, [p, p]),
         "fs_gemm_path": (C.c_char_p, [p]),
+        "fs_device_error": (C.c_int, [p, p]),
+        "fs_copy_logits": (C.c_int, [p, p]),
+        "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -103,7 +106,8 @@ def exported_symbols() -> list:
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
-            "fs_profile_enable", "fs_profile_read"]
+            "fs_profile_enable", "fs_profile_read", "fs_device_error",
+            "fs_gemm_bf16", "fs_copy_logits"]
 
 
 def _check(h, rc: int) -> None:
@@ -278,3 +282,26 @@ def fs_kernel_launches(h) -> int:
 
 def fs_gemm_path(h) -> str:
     return lib().fs_gemm_path(h).decode()
+
+
+def fs_device_error(h) -> int:
+    v = C.c_int32()
+    _check(h, lib().fs_device_error(h, C.byref(v)))
+    return v.value
+
+
+def fs_gemm_bf16(W, X, Y, splits: int = 1, path: int = 1, stream=None) -> None:
+    """Test hook: Y = X @ W^T on the device (torch bf16 W [N, K], X [B, K],
+    f32 Y [B, N])."""
+    raw = getattr(stream, "cuda_stream", stream)
+    N, K = W.shape
+    B = X.shape[0]
+    rc = lib().fs_gemm_bf16(_dptr(W), N, K, _dptr(X), B, _dptr(Y), splits,
+                            path, raw)
+    if rc != FS_OK:
+        raise FsError(rc, "fs_gemm_bf16 failed")
+
+
+def fs_copy_logits(h, dst) -> None:
+    """Copies the last step's logits [n, V] f32 into dst (numpy or torch)."""
+    _check(h, lib().fs_copy_logits(h, _dptr(dst)))

@@ -139,6 +139,9 @@ int fs_lane_reset(fs_handle* h, int32_t lane);
  * positions[i] is incremented. lanes, positions and tokens are host arrays.
  * logits_out: DEVICE pointer to f32 [n, vocab] in input order, or NULL to
  * keep the logits inside the handle for fs_sample. n == 0 is a no-op.
+ * With logits_out == NULL the step's kernels run as one CUDA graph, captured
+ * on the first call with that n and replayed afterwards; the first call
+ * for an n therefore must not happen inside another stream capture.
  * Errors (nothing changes): FS_ERR_ARG (n outside [0, max_lanes]),
  * FS_ERR_LANE, FS_ERR_DUP_LANE, FS_ERR_POSITION, FS_ERR_TOKEN,
  * FS_ERR_KV_FULL; FS_ERR_CUDA if a launch fails (lane state is then
@@ -168,6 +171,11 @@ int fs_sample_device(fs_handle* h, int32_t n, const float* temps,
                      int32_t* tokens_out);
 
 /* ---- inspection and test hooks ---------------------------------------- */
+
+/* Copies the last step's logits (f32 [n, vocab], input order) to `dst`
+ * (host or device memory). Synchronises the stream. Errors: FS_ERR_STATE
+ * (no step yet). */
+int fs_copy_logits(fs_handle* h, float* dst);
 
 /* Kernel classes of the profiler. */
 #define FS_PROF_GEMM 0      /* weight-streaming GEMM (all matrices)          */
@@ -224,8 +232,26 @@ int fs_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks_out,
 /* Number of kernels the library launched on the handle since creation. */
 int fs_kernel_launches(const fs_handle* h, int64_t* count_out);
 
-/* Name of the GEMM path serving the handle's weight matrices. */
+/* Name of the GEMM path serving the handle's weight matrices: "tcgen05"
+ * (bf16 weights on the tensor cores) or "warp-gemv". The environment
+ * variable FS_GEMM_PATH=gemv, read by fs_create, selects the warp-GEMV
+ * path for bf16 weights too (a comparison point). */
 const char* fs_gemm_path(const fs_handle* h);
+
+/* Synchronises the stream, returns the handle's device error code (0: none;
+ * non-zero: a kernel gave up on a bounded wait) and clears it. fs_sample
+ * reports a set code as FS_ERR_DEVICE. */
+int fs_device_error(fs_handle* h, int32_t* code_out);
+
+/* Test hook: Y[b, n] = sum_k X[b, k] * W[n, k] for bf16 W [N, K] and
+ * X [B, K] (K a multiple of 64), f32 Y [B, N]; all DEVICE pointers owned by
+ * the caller. path 1 = tcgen05 kernel with `splits` K splits (1 <= splits
+ * <= min(8, K/64)), path 0 = warp-GEMV kernel. Allocates its own workspace; runs on
+ * `stream` (NULL = default) and synchronises it. Errors: FS_ERR_ARG,
+ * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_DEVICE (a bounded wait timed out). */
+int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
+                 int32_t B, float* Y, int32_t splits, int32_t path,
+                 void* stream);
 
 #ifdef __cplusplus
 }

@@ -64,6 +64,7 @@ def gpu_teacher_forced(h, cfg, lanes, seqs, V):
         ps = np.array([pos[k] for k in ls], dtype=np.int32)
         buf = torch.empty((len(idx), V), dtype=torch.float32, device="cuda")
         fs.fs_decode_step_batch(h, ls, ps, toks, logits_out=buf)
+        torch.cuda.synchronize()
         lg = buf.cpu().numpy()
         for j, i in enumerate(idx):
             out[i][t] = lg[j]

@@ -1,0 +1,62 @@
+"""GPU: the weight-streaming GEMM kernels through the fs_gemm_bf16 test hook.
+
+Reference: the same bf16 operands multiplied in f64 on the host. The bound
+is the f32 accumulation error of a K-term dot product, relative to the sum
+of |terms|. Batch invariance: a lane's outputs are bit-identical whatever
+the number of lanes in the call.
+"""
+import numpy as np
+import pytest
+
+from continuous_transformer_decode_gb300 import fs
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(N, K, B, seed):
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    W = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    X = torch.randn(B, K, generator=g).to(torch.bfloat16)
+    return W, X
+
+
+def _ref(W, X):
+    return X.double() @ W.double().T, X.double().abs() @ W.double().abs().T
+
+
+@pytest.mark.parametrize("N,K,B,splits", [
+    (128, 64, 1, 1), (960, 576, 1, 4), (960, 576, 17, 4), (576, 1536, 64, 4),
+    (3072, 576, 256, 1), (200, 128, 33, 2), (1000, 576, 600, 3),
+    (576, 576, 5, 8)])
+def test_tcgen05_gemm_matches_f64(N, K, B, splits):
+    import torch
+    W, X = _case(N, K, B, N * 7 + K + B)
+    Y = torch.empty(B, N, dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16(W.cuda(), X.cuda(), Y, splits=splits, path=1)
+    ref, mag = _ref(W, X)
+    err = (Y.cpu().double() - ref).abs()
+    bound = 1e-5 * mag + 1e-6
+    assert bool((err <= bound).all()), float((err / mag.clamp_min(1e-9)).max())
+
+
+def test_gemv_matches_f64():
+    import torch
+    W, X = _case(960, 576, 9, 5)
+    Y = torch.empty(9, 960, dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16(W.cuda(), X.cuda(), Y, path=0)
+    ref, mag = _ref(W, X)
+    assert bool(((Y.cpu().double() - ref).abs() <= 1e-5 * mag + 1e-6).all())
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_tcgen05_gemm_batch_invariance_bitwise(splits):
+    import torch
+    W, X = _case(960, 576, 300, 11)
+    Wd, Xd = W.cuda(), X.cuda()
+    full = torch.empty(300, 960, dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16(Wd, Xd, full, splits=splits, path=1)
+    for B in (1, 2, 16, 17, 100, 256):
+        Y = torch.empty(B, 960, dtype=torch.float32, device="cuda")
+        fs.fs_gemm_bf16(Wd, Xd[:B].contiguous(), Y, splits=splits, path=1)
+        assert torch.equal(Y.view(torch.int32), full[:B].view(torch.int32)), B

@@ -223,3 +223,33 @@ def test_error_paths_are_atomic(tiny):
         assert fs.fs_lane_pages(h, 0) == [] and fs.fs_lane_length(h, 0) == 0
     finally:
         fs.fs_destroy(h)
+
+
+def test_graph_replay_equals_direct_launches_bitwise(smol_l2):
+    """Steps replayed from the per-n CUDA graph (logits kept internal) give
+    the same bits as the same steps launched kernel by kernel."""
+    import torch
+    cfg, Wb, m = smol_l2
+    prompts = synth.make_prompts(6, 5, cfg["V"], seed=21)
+    outs = []
+    for direct in (True, False):
+        h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=8)
+        try:
+            pos = np.zeros(6, np.int32)
+            rows = []
+            for t in range(5):
+                toks = [int(p[t]) for p in prompts]
+                if direct:
+                    buf = torch.empty((6, cfg["V"]), dtype=torch.float32, device="cuda")
+                    fs.fs_decode_step_batch(h, list(range(6)), pos, toks, logits_out=buf)
+                    torch.cuda.synchronize()
+                    rows.append(buf.cpu().numpy())
+                else:
+                    fs.fs_decode_step_batch(h, list(range(6)), pos, toks)
+                    lg = np.empty((6, cfg["V"]), np.float32)
+                    fs.fs_copy_logits(h, lg)
+                    rows.append(lg)
+            outs.append(np.stack(rows))
+        finally:
+            fs.fs_destroy(h)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
