@@ -88,6 +88,7 @@ struct fs_handle {
   float* rope_sin = nullptr;
 
   float* x = nullptr;
+  float* y = nullptr;  // projection output added to x by the next norm
   void* hpanel = nullptr;
   void* opanel = nullptr;
   void* apanel = nullptr;
@@ -96,6 +97,8 @@ struct fs_handle {
   float* logits = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
+  int* attn_counters = nullptr;  // [max_lanes * Hkv], zero between steps
+  bool attn_fused = false;
 
   int32_t* d_args = nullptr;  // [7 * max_lanes + 1]
   int32_t* h_args = nullptr;  // pinned staging
@@ -397,6 +400,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   const int B = d.max_lanes;
   const size_t xs = h->xtype == X_F32 ? 4 : 2;
   bool ok = h->alloc(&h->x, (size_t)B * d.d_model * 4) == cudaSuccess &&
+            h->alloc(&h->y, (size_t)B * d.d_model * 4) == cudaSuccess &&
             h->alloc(&h->hpanel, (size_t)B * h->Kp_d * xs) == cudaSuccess &&
             h->alloc(&h->opanel, (size_t)B * h->Kp_q * xs) == cudaSuccess &&
             h->alloc(&h->apanel, (size_t)B * h->Kp_f * xs) == cudaSuccess &&
@@ -405,12 +409,15 @@ int create_impl(fs_handle* h, const fs_weights* W) {
             h->alloc(&h->logits, (size_t)B * d.vocab * 4) == cudaSuccess &&
             h->alloc(&h->part_ml, (size_t)B * h->max_splits * d.n_heads * 2 * 4) == cudaSuccess &&
             h->alloc(&h->part_acc, (size_t)B * h->max_splits * h->Nq * 4) == cudaSuccess &&
+            h->alloc(&h->attn_counters, (size_t)B * d.n_kv_heads * 4) == cudaSuccess &&
             h->alloc(&h->d_args, (size_t)(7 * B + 1) * 4) == cudaSuccess &&
             h->alloc(&h->d_temps, (size_t)B * 4) == cudaSuccess &&
             h->alloc(&h->d_seeds, (size_t)B * 8) == cudaSuccess &&
             h->alloc(&h->d_counters, (size_t)B * 8) == cudaSuccess &&
             h->alloc(&h->d_tokens, (size_t)B * 4) == cudaSuccess;
   if (!ok) return h->fail(FS_ERR_OOM, "scratch allocation failed");
+  FS_CK(h, cudaMemset(h->attn_counters, 0, (size_t)B * d.n_kv_heads * 4));
+  h->attn_fused = attn_fused_supports(d.head_dim, h->G);
   FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
   FS_CK(h, cudaMemset(h->apanel, 0, (size_t)B * h->Kp_f * xs));
@@ -552,32 +559,44 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
   });
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& W = h->layers[l];
-    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-      return launch_rmsnorm(h->x, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                            h->Kp_d, s);
+    h->launch(FS_PROF_OTHER, norm_bytes + (l ? 3.0 * n * d.d_model * 4 : 0.0), [&] {
+      return launch_rmsnorm(h->x, l ? h->y : nullptr, W.g_attn, n, d.d_model, d.rms_eps,
+                            h->hpanel, h->xtype, h->Kp_d, s);
     });
     gemm(W.qkv, W.qkv_tc, h->tm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
-    h->launch(FS_PROF_OTHER,
-              (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
-                return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
-                                          h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
-              });
-    h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
-      return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
-                              h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
-                              h->Kp_q, s);
-    });
-    gemm(W.o, W.o_tc, h->tm_o, h->opanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
-    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-      return launch_rmsnorm(h->x, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+    if (h->attn_fused) {
+      h->launch(FS_PROF_ATTN,
+                kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
+                  return launch_attention_fused(h->qkv, n, d.n_heads, h->rope_cos,
+                                                h->rope_sin, args, h->kv, l, h->max_splits,
+                                                h->split_len, h->part_ml, h->part_acc,
+                                                h->attn_counters, h->opanel, h->xtype,
+                                                h->Kp_q, s);
+                });
+    } else {
+      h->launch(FS_PROF_OTHER,
+                (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
+                  return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
+                                            h->rope_cos, h->rope_sin, args, h->kv, l, h->q,
+                                            s);
+                });
+      h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
+        return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
+                                h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
+                                h->Kp_q, s);
+      });
+    }
+    gemm(W.o, W.o_tc, h->tm_o, h->opanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
+    h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
+      return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
                             h->Kp_d, s);
     });
     gemm(W.gateup, W.gateup_tc, h->tm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
          d.d_ffn);
-    gemm(W.down, W.down_tc, h->tm_a, h->apanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model);
+    gemm(W.down, W.down_tc, h->tm_a, h->apanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
   }
-  h->launch(FS_PROF_OTHER, norm_bytes, [&] {
-    return launch_rmsnorm(h->x, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+  h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
+    return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
                           h->Kp_d, s);
   });
   gemm(h->head, h->head_tc, h->tm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);

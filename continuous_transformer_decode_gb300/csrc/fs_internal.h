@@ -93,7 +93,8 @@ int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParam
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
                  const KV& kv, float* x, int d, cudaStream_t s);
-int launch_rmsnorm(const float* x, const float* g, int B, int d, float eps,
+// x += resid (if resid is given), out = RMSNorm(x) * g.
+int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
                    void* out, int x_type, int ld_out, cudaStream_t s);
 int launch_rope_append(const float* qkv, int B, int H, int Hkv, int hd,
                        const float* rope_cos, const float* rope_sin,
@@ -103,6 +104,13 @@ int launch_attention(const float* q, int B, int H, const StepArgs& args,
                      const KV& kv, int layer, int max_splits, int split_len,
                      float* part_ml, float* part_acc, void* o_panel,
                      int x_type, int ld_o, cudaStream_t s);
+// RoPE + KV append + split-K attention (+ ordered merge) in one kernel.
+bool attn_fused_supports(int hd, int G);
+int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos,
+                           const float* rope_sin, const StepArgs& args, const KV& kv,
+                           int layer, int max_splits, int split_len, float* part_ml,
+                           float* part_acc, int* counters, void* o_panel, int x_type,
+                           int ld_o, cudaStream_t s);
 int launch_sample(const float* logits, int B, int V, const float* temps,
                   const uint64_t* seeds, const uint64_t* counters,
                   int32_t* out, cudaStream_t s);

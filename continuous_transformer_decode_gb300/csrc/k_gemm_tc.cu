@@ -165,15 +165,97 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
   }
   const int row = m_tile * kBM + row_local;
   if (row >= p.n_out) return;
+  float* o = p.out_f32 + (int64_t)(p.lane0 + c0) * p.ldo + row;
+  if (p.epi == EPI_RESID) {
+    float prev[16];  // every load of the chunk before any store
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int b = c0 + j;
-    if (b < p.lanes) {
-      float* o = p.out_f32 + (int64_t)(p.lane0 + b) * p.ldo + row;
-      if (p.epi == EPI_RESID)
-        *o += v[j];
-      else
-        *o = v[j];
+    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < p.lanes) ? o[(int64_t)j * p.ldo] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < p.lanes) o[(int64_t)j * p.ldo] = prev[j] + v[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < p.lanes) o[(int64_t)j * p.ldo] = v[j];
+  }
+}
+
+// Sum of the split partials of 4 consecutive rows of one lane, split order.
+__device__ __forceinline__ float4 sum_splits4(const TcParams& p, int64_t R, int b,
+                                              int64_t row0) {
+  float4 part[kMaxSplits];
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplits; ++sp)
+    if (sp < p.splits)
+      part[sp] = __ldcg(reinterpret_cast<const float4*>(
+          p.ws + ((int64_t)sp * p.n_tot + b) * R + row0));
+  float4 acc = part[0];
+#pragma unroll
+  for (int sp = 1; sp < kMaxSplits; ++sp)
+    if (sp < p.splits) {
+      acc.x += part[sp].x;
+      acc.y += part[sp].y;
+      acc.z += part[sp].z;
+      acc.w += part[sp].w;
+    }
+  return acc;
+}
+
+// Last block of a row tile: reduce the split partials and apply the
+// epilogue with 16-byte accesses (threads map to 4-row groups x lanes).
+__device__ void reduce_tile(const TcParams& p, int m_tile) {
+  const int64_t R = (int64_t)p.m_tiles * kBM;
+  const int t = threadIdx.x;  // 0..127
+  if (p.epi == EPI_SWIGLU) {
+    const int rq = (t & 15) * 4, lsub = t >> 4;  // 16 threads per lane row
+    const int f0 = m_tile * 64 + rq;
+    if (f0 >= p.n_out) return;
+    for (int b0 = lsub; b0 < p.lanes; b0 += 16) {
+      float4 g[2], u[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (b0 + 8 * k < p.lanes) {
+          g[k] = sum_splits4(p, R, b0 + 8 * k, (int64_t)m_tile * kBM + rq);
+          u[k] = sum_splits4(p, R, b0 + 8 * k, (int64_t)m_tile * kBM + 64 + rq);
+        }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int b = b0 + 8 * k;
+        if (b >= p.lanes) break;
+        __nv_bfloat162 lo =
+            __floats2bfloat162_rn(silu(g[k].x) * u[k].x, silu(g[k].y) * u[k].y);
+        __nv_bfloat162 hi =
+            __floats2bfloat162_rn(silu(g[k].z) * u[k].z, silu(g[k].w) * u[k].w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_x) +
+                                  (int64_t)(p.lane0 + b) * p.ldo + f0) = pk;
+      }
+    }
+    return;
+  }
+  const int rq = (t & 31) * 4, lsub = t >> 5;  // 32 threads per lane row
+  const int row0 = m_tile * kBM + rq;
+  if (row0 >= p.n_out) return;
+  const bool vec = (p.ldo & 3) == 0 && row0 + 4 <= p.n_out;
+  constexpr int U = 4;  // lanes in flight per thread: all loads, then stores
+  for (int b0 = lsub; b0 < p.lanes; b0 += 4 * U) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (b0 + 4 * u < p.lanes) v[u] = sum_splits4(p, R, b0 + 4 * u, row0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int b = b0 + 4 * u;
+      if (b >= p.lanes) break;
+      float* o = p.out_f32 + (int64_t)(p.lane0 + b) * p.ldo + row0;
+      if (vec) {
+        *reinterpret_cast<float4*>(o) = v[u];
+      } else {
+        const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int e = 0; e < 4 && row0 + e < p.n_out; ++e) o[e] = vv[e];
+      }
     }
   }
 }
@@ -331,29 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_bar();
       if (s_last) {
         __threadfence();
-        for (int c0 = 0; c0 < p.n_tot; c0 += 16) {
-          // all loads of the chunk first, then the sums in split order
-          float part[kMaxSplits][16];
-#pragma unroll
-          for (int sp = 0; sp < kMaxSplits; ++sp) {
-            if (sp < p.splits) {
-              const float* src = p.ws + ((int64_t)sp * p.n_tot + c0) * R + row;
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                part[sp][j] = (c0 + j < p.lanes) ? __ldcg(src + (int64_t)j * R) : 0.0f;
-            }
-          }
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float acc = part[0][j];
-#pragma unroll
-            for (int sp = 1; sp < kMaxSplits; ++sp)
-              if (sp < p.splits) acc += part[sp][j];
-            v[j] = acc;
-          }
-          if (!abort) emit_chunk(p, m_tile, row_local, c0, v, xbuf);
-        }
+        if (!abort) reduce_tile(p, m_tile);
         if (threadIdx.x == 0) p.counters[m_tile] = 0;  // ready for the next launch
       }
     }

@@ -42,21 +42,32 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return r;
 }
 
-// y = x * (1 / sqrt(mean(x^2) + eps)) * g, one block per panel row; the sum
-// of squares is reduced in a fixed order, independent of the batch.
+// Residual add then RMSNorm, one block per panel row: if r is given,
+// x += r (written back: the residual stream), then
+// out = x * (1 / sqrt(mean(x^2) + eps)) * g. The sum of squares is reduced
+// in a fixed order, independent of the batch.
 template <typename OT>
-__global__ void k_rmsnorm(const float* __restrict__ x,
+__global__ void k_rmsnorm(float* __restrict__ x, const float* __restrict__ r,
                           const float* __restrict__ g, int d, float eps,
                           OT* __restrict__ out, int ld_out) {
   __shared__ float red[32];
   const int b = blockIdx.x;
-  const float* xr = x + (int64_t)b * d;
+  float* xr = x + (int64_t)b * d;
   float ss = 0.0f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  if (r) {
+    const float* rr = r + (int64_t)b * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+      const float v = xr[i] + rr[i];
+      xr[i] = v;
+      ss = fmaf(v, v, ss);
+    }
+  } else {
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  }
   ss = block_sum(ss, red);
-  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+  const float rs = 1.0f / sqrtf(ss / (float)d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = xr[i] * r * g[i];
+    const float v = xr[i] * rs * g[i];
     if constexpr (sizeof(OT) == 2)
       out[(int64_t)b * ld_out + i] = __float2bfloat16_rn(v);
     else
@@ -322,14 +333,14 @@ int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
   return 1;
 }
 
-int launch_rmsnorm(const float* x, const float* g, int B, int d, float eps,
+int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
                    void* out, int x_type, int ld_out, cudaStream_t s) {
   if (B <= 0) return 0;
   if (x_type == X_BF16)
     k_rmsnorm<__nv_bfloat16><<<B, 256, 0, s>>>(
-        x, g, d, eps, static_cast<__nv_bfloat16*>(out), ld_out);
+        x, resid, g, d, eps, static_cast<__nv_bfloat16*>(out), ld_out);
   else
-    k_rmsnorm<float><<<B, 256, 0, s>>>(x, g, d, eps, static_cast<float*>(out),
+    k_rmsnorm<float><<<B, 256, 0, s>>>(x, resid, g, d, eps, static_cast<float*>(out),
                                        ld_out);
   return 1;
 }

