@@ -44,17 +44,34 @@ struct LayerW {
 };
 
 // K split of a weight matrix: enough (128-row tile, K range) units to cover
-// the SMs, at least two 64-wide K blocks per unit, and fewer splits the more
-// lanes the handle can batch (the split partials grow with the lanes). It
-// depends on the matrix and the handle only, never on a call's lane count.
-int choose_splits(int m_tiles, int kb, int max_lanes) {
-  const int cap = max_lanes <= 64 ? 8 : (max_lanes <= 256 ? 4 : 2);
+// the SMs, at least two 64-wide K blocks per unit, at most 8, and only while
+// the split partials (128 rows x the handle's lane capacity, f32) stay small
+// next to the unit's weight bytes (128 rows x K / splits, bf16). It depends
+// on the matrix and the handle only, never on a call's lane count.
+int choose_splits(int m_tiles, int K, int max_lanes) {
+  const int n_cap = std::min(256, (int)round_up(max_lanes, 16));
   int s = (152 + m_tiles - 1) / m_tiles;
-  s = std::min(s, std::max(1, kb / 2));
-  s = std::min(s, cap);
+  s = std::min(s, std::max(1, K / 128));
+  s = std::min(s, K / (8 * n_cap));
+  s = std::min(s, 8);
   return std::max(1, s);
 }
 
+// Lanes per group of a GEMM launch: enough (tile, split, group) units for
+// about two blocks per SM, groups of 32..256 lanes (fewer when n is small).
+// Groups split N only, so this may depend on the call's lane count.
+int choose_lane_group(int n, int units) {
+  const int want = std::max(1, (304 + units - 1) / units);
+  int lg = (int)round_up((n + want - 1) / want, 16);
+  lg = std::max(lg, std::min(32, (int)round_up(n, 16)));
+  return std::min(lg, 256);
+}
+
+int tmem_cols_for(int lg) {
+  int c = 32;
+  while (c < lg) c *= 2;
+  return c;
+}
 }  // namespace
 
 struct fs_handle {
@@ -71,7 +88,8 @@ struct fs_handle {
   Mat embed, head;
   TcW head_tc;
   bool use_tc = false;
-  CUtensorMap tm_h, tm_o, tm_a;  // panels (box 16 lanes)
+  CUtensorMap tm_h, tm_o, tm_a;        // panels, boxes of 16 lanes
+  CUtensorMap tm_h64, tm_o64, tm_a64;  // panels, boxes of 64 lanes
   float* ws = nullptr;
   int* counters = nullptr;
   int* err_flag = nullptr;  // mapped pinned host memory
@@ -426,15 +444,14 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   *h->err_flag = 0;
   FS_CK(h, cudaHostGetDevicePointer((void**)&h->d_err_flag, h->err_flag, 0));
   if (h->use_tc) {
-    const int n_tot_max = (int)round_up(std::min(B, 512), 16);
     size_t ws_elems = 0;
     int max_tiles = 1;
     auto setup = [&](const Mat& m, TcW* t) -> int {
       t->m_tiles = (m.N + 127) / 128;
-      t->splits = choose_splits(t->m_tiles, m.Kp / 64, B);
+      t->splits = choose_splits(t->m_tiles, m.Kp, B);
       max_tiles = std::max(max_tiles, t->m_tiles);
       if (t->splits > 1)
-        ws_elems = std::max(ws_elems, (size_t)t->splits * n_tot_max * t->m_tiles * 128);
+        ws_elems = std::max(ws_elems, (size_t)t->splits * B * t->m_tiles * 128);
       if (tc_make_map(m.w, m.N, m.Kp, 128, &t->tm)) return h->fail(FS_ERR_CUDA, "tensor map");
       return FS_OK;
     };
@@ -446,12 +463,16 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     if ((rc = setup(h->head, &h->head_tc))) return rc;
     if (tc_make_map(h->hpanel, B, h->Kp_d, 16, &h->tm_h) ||
         tc_make_map(h->opanel, B, h->Kp_q, 16, &h->tm_o) ||
-        tc_make_map(h->apanel, B, h->Kp_f, 16, &h->tm_a))
+        tc_make_map(h->apanel, B, h->Kp_f, 16, &h->tm_a) ||
+        tc_make_map(h->hpanel, B, h->Kp_d, 64, &h->tm_h64) ||
+        tc_make_map(h->opanel, B, h->Kp_q, 64, &h->tm_o64) ||
+        tc_make_map(h->apanel, B, h->Kp_f, 64, &h->tm_a64))
       return h->fail(FS_ERR_CUDA, "panel tensor map");
+    const size_t n_counters = (size_t)max_tiles * ((B + 15) / 16);
     if (h->alloc(&h->ws, std::max<size_t>(ws_elems, 1) * 4) != cudaSuccess ||
-        h->alloc(&h->counters, (size_t)max_tiles * 4) != cudaSuccess)
+        h->alloc(&h->counters, n_counters * 4) != cudaSuccess)
       return h->fail(FS_ERR_OOM, "GEMM workspace allocation failed");
-    FS_CK(h, cudaMemset(h->counters, 0, (size_t)max_tiles * 4));
+    FS_CK(h, cudaMemset(h->counters, 0, n_counters * 4));
   }
   FS_CK(h, cudaHostAlloc((void**)&h->h_samp, (size_t)B * 24, cudaHostAllocDefault));
   int32_t* a = h->d_args;
@@ -526,8 +547,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
     return b;
   };
   // algorithmic bytes: weights once, activations in, outputs out
-  auto gemm = [&](const Mat& W, const TcW& T, const CUtensorMap& tmX, const void* X, int epi,
-                  float* of, void* ox, int ldo, int n_out) {
+  auto gemm = [&](const Mat& W, const TcW& T, const CUtensorMap& tmX, const CUtensorMap& tmX64,
+                  const void* X, int epi, float* of, void* ox, int ldo, int n_out) {
     double bytes = wbytes(W) + (double)n * W.K * xs;
     bytes += epi == EPI_SWIGLU ? (double)n * n_out * xs
              : (double)n * n_out * 4.0 * (epi == EPI_RESID ? 2 : 1);
@@ -538,20 +559,15 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
       h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemv(g, s); });
       return;
     }
-    for (int lane0 = 0; lane0 < n; lane0 += 512) {  // passes of up to 512 lanes
-      TcParams p{};
-      p.m_tiles = T.m_tiles; p.splits = T.splits; p.kb_total = W.Kp / 64;
-      p.lanes = std::min(512, n - lane0); p.lane0 = lane0;
-      p.n_tot = (int)round_up(p.lanes, 16);
-      p.tmem_cols = 32;
-      while (p.tmem_cols < p.n_tot) p.tmem_cols *= 2;
-      p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
-      p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
-      const double share = (double)p.lanes / n;
-      h->launch(FS_PROF_GEMM, lane0 == 0 ? bytes * share + wbytes(W) * (1 - share)
-                                         : bytes * share,
-                [&] { return launch_gemm_tc(T.tm, tmX, p, s); });
-    }
+    TcParams p{};
+    p.m_tiles = T.m_tiles; p.splits = T.splits; p.kb_total = W.Kp / 64;
+    p.lanes_total = n;
+    p.lg = choose_lane_group(n, T.m_tiles * T.splits);
+    p.groups = (n + p.lg - 1) / p.lg;
+    p.tmem_cols = tmem_cols_for(p.lg);
+    p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
+    p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
+    h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc(T.tm, tmX64, tmX, p, s); });
   };
   const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
   h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
@@ -563,7 +579,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
       return launch_rmsnorm(h->x, l ? h->y : nullptr, W.g_attn, n, d.d_model, d.rms_eps,
                             h->hpanel, h->xtype, h->Kp_d, s);
     });
-    gemm(W.qkv, W.qkv_tc, h->tm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
+    gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
     if (h->attn_fused) {
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
@@ -586,20 +602,20 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                                 h->Kp_q, s);
       });
     }
-    gemm(W.o, W.o_tc, h->tm_o, h->opanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
+    gemm(W.o, W.o_tc, h->tm_o, h->tm_o64, h->opanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
     h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
       return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
                             h->Kp_d, s);
     });
-    gemm(W.gateup, W.gateup_tc, h->tm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
+    gemm(W.gateup, W.gateup_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
          d.d_ffn);
-    gemm(W.down, W.down_tc, h->tm_a, h->apanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
+    gemm(W.down, W.down_tc, h->tm_a, h->tm_a64, h->apanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
   }
   h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
     return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
                           h->Kp_d, s);
   });
-  gemm(h->head, h->head_tc, h->tm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
 }
 
 }  // namespace
@@ -973,31 +989,31 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
     if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
     return cudaStreamSynchronize(s) == cudaSuccess ? FS_OK : FS_ERR_CUDA;
   }
-  CUtensorMap tw, tx;
-  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx)) return FS_ERR_CUDA;
+  CUtensorMap tw, tx, tx64;
+  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
+      tc_make_map(X, B, K, 64, &tx64))
+    return FS_ERR_CUDA;
   const int m_tiles = (N + 127) / 128;
   float* ws = nullptr;
   int *cnt = nullptr, *err = nullptr;
-  const int n_tot0 = (int)round_up(std::min(B, 512), 16);
+  const int max_groups = (B + 15) / 16;
   int rc = FS_OK;
-  if (cudaMalloc(&ws, (size_t)splits * n_tot0 * m_tiles * 128 * 4) != cudaSuccess ||
-      cudaMalloc(&cnt, (size_t)m_tiles * 4) != cudaSuccess ||
+  if (cudaMalloc(&ws, (size_t)splits * B * m_tiles * 128 * 4) != cudaSuccess ||
+      cudaMalloc(&cnt, (size_t)m_tiles * max_groups * 4) != cudaSuccess ||
       cudaMalloc(&err, 4) != cudaSuccess) {
     rc = FS_ERR_OOM;
   } else {
-    cudaMemsetAsync(cnt, 0, (size_t)m_tiles * 4, s);
+    cudaMemsetAsync(cnt, 0, (size_t)m_tiles * max_groups * 4, s);
     cudaMemsetAsync(err, 0, 4, s);
-    for (int lane0 = 0; lane0 < B; lane0 += 512) {
-      TcParams p{};
-      p.m_tiles = m_tiles; p.splits = splits; p.kb_total = K / 64;
-      p.lanes = std::min(512, B - lane0); p.lane0 = lane0;
-      p.n_tot = (int)round_up(p.lanes, 16);
-      p.tmem_cols = 32;
-      while (p.tmem_cols < p.n_tot) p.tmem_cols *= 2;
-      p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
-      p.ws = ws; p.counters = cnt; p.err = err;
-      launch_gemm_tc(tw, tx, p, s);
-    }
+    TcParams p{};
+    p.m_tiles = m_tiles; p.splits = splits; p.kb_total = K / 64;
+    p.lanes_total = B;
+    p.lg = choose_lane_group(B, m_tiles * splits);
+    p.groups = (B + p.lg - 1) / p.lg;
+    p.tmem_cols = tmem_cols_for(p.lg);
+    p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
+    p.ws = ws; p.counters = cnt; p.err = err;
+    launch_gemm_tc(tw, tx64, tx, p, s);
     int herr = 0;
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
         cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)

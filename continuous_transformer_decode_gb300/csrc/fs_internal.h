@@ -68,28 +68,30 @@ struct GemmArgs {
 // Launchers (each returns the number of kernels launched).
 int launch_gemv(const GemmArgs& a, cudaStream_t s);
 
-// tcgen05 GEMM (bf16 weights and panels). Work unit = (128-row tile,
-// K split); grid = m_tiles * splits.
+// tcgen05 GEMM (bf16 weights and panels). Work unit = (128-row weight tile,
+// K split, lane group); grid = m_tiles * splits * groups, the groups of one
+// (tile, split) adjacent so they share the weight tile through L2.
 struct TcParams {
   int m_tiles, splits, kb_total;
-  int lanes;     // valid lanes in this pass
-  int lane0;     // first panel row of this pass
-  int n_tot;     // lanes rounded up to 16 (<= 512)
-  int tmem_cols; // power of two >= max(32, n_tot)
+  int groups;      // lane groups
+  int lg;          // lanes per group (multiple of 16, <= 256)
+  int lanes_total; // lanes of the step (panel rows 0 .. lanes_total-1)
+  int tmem_cols;   // power of two >= max(32, lg)
   int stages, stage_bytes;  // set by the launcher
   int epi;
   float* out_f32;
   void* out_x;
   int ldo;
-  int n_out;     // output rows (W rows, or F for SwiGLU)
-  float* ws;     // split partials [splits][n_tot][m_tiles * 128]
-  int* counters; // [m_tiles], zero between launches
-  int* err;      // device-visible error flag
+  int n_out;       // output rows (W rows, or F for SwiGLU)
+  float* ws;       // split partials [splits][lanes_total][m_tiles * 128]
+  int* counters;   // [m_tiles * groups], zero between launches
+  int* err;        // device-visible error flag
 };
 bool tc_available();
 int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
-int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p,
-                   cudaStream_t s);
+// tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.
+int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                   const TcParams& p, cudaStream_t s);
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
                  const KV& kv, float* x, int d, cudaStream_t s);

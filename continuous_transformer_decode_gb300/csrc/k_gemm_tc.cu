@@ -13,12 +13,14 @@
 // Block = 6 warps: warp 4 issues TMA loads, warp 5 owns TMEM and issues the
 // MMAs, warps 0-3 run the epilogue (warp w reads TMEM lanes 32w..32w+31,
 // i.e. weight rows; each thread then holds one output row for every lane).
-// A block owns one (128-row tile, K range) work unit. With a K split > 1 the
-// partial tiles go to a workspace and the last block of the row tile to
-// arrive sums them in split order, so results never depend on timing. The
-// split count depends only on the matrix shape and the handle's lane
-// capacity, never on the number of lanes in a call: a lane's output is then
-// independent of the batch it is computed in.
+// A block owns one (128-row tile, K range, lane group) work unit. Lane
+// groups split the N dimension only, which leaves every output element's
+// K order unchanged. With a K split > 1 the partial tiles go to a workspace
+// and the last block of the (row tile, lane group) to arrive sums them in
+// split order, so results never depend on timing. The K split count depends
+// only on the matrix shape and the handle's lane capacity, never on the
+// number of lanes in a call: a lane's output is then independent of the
+// batch it is computed in.
 //
 // Every wait on an mbarrier is bounded (1 s of %globaltimer); on timeout the
 // block records an error code, stops issuing work, drains the TMA loads it
@@ -26,6 +28,8 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "fs_internal.h"
 
@@ -139,7 +143,8 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
 // rows; the up half hands its values to the gate half through shared memory.
 __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int row_local,
-                                           int c0, const float v[16], float* xbuf) {
+                                           int lane0, int lanes, int c0, const float v[16],
+                                           float* xbuf) {
   if (p.epi == EPI_SWIGLU) {
     if (row_local >= 64) {
 #pragma unroll
@@ -152,9 +157,9 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int b = c0 + j;
-          if (b < p.lanes) {
+          if (b < lanes) {
             const float a = silu(v[j]) * xbuf[row_local * 17 + j];
-            static_cast<__nv_bfloat16*>(p.out_x)[(int64_t)(p.lane0 + b) * p.ldo + f] =
+            static_cast<__nv_bfloat16*>(p.out_x)[(int64_t)(lane0 + b) * p.ldo + f] =
                 __float2bfloat16_rn(a);
           }
         }
@@ -165,18 +170,18 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
   }
   const int row = m_tile * kBM + row_local;
   if (row >= p.n_out) return;
-  float* o = p.out_f32 + (int64_t)(p.lane0 + c0) * p.ldo + row;
+  float* o = p.out_f32 + (int64_t)(lane0 + c0) * p.ldo + row;
   if (p.epi == EPI_RESID) {
     float prev[16];  // every load of the chunk before any store
 #pragma unroll
-    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < p.lanes) ? o[(int64_t)j * p.ldo] : 0.0f;
+    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < lanes) ? o[(int64_t)j * p.ldo] : 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < p.lanes) o[(int64_t)j * p.ldo] = prev[j] + v[j];
+      if (c0 + j < lanes) o[(int64_t)j * p.ldo] = prev[j] + v[j];
   } else {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < p.lanes) o[(int64_t)j * p.ldo] = v[j];
+      if (c0 + j < lanes) o[(int64_t)j * p.ldo] = v[j];
   }
 }
 
@@ -188,7 +193,7 @@ __device__ __forceinline__ float4 sum_splits4(const TcParams& p, int64_t R, int 
   for (int sp = 0; sp < kMaxSplits; ++sp)
     if (sp < p.splits)
       part[sp] = __ldcg(reinterpret_cast<const float4*>(
-          p.ws + ((int64_t)sp * p.n_tot + b) * R + row0));
+          p.ws + ((int64_t)sp * p.lanes_total + b) * R + row0));
   float4 acc = part[0];
 #pragma unroll
   for (int sp = 1; sp < kMaxSplits; ++sp)
@@ -203,25 +208,25 @@ __device__ __forceinline__ float4 sum_splits4(const TcParams& p, int64_t R, int 
 
 // Last block of a row tile: reduce the split partials and apply the
 // epilogue with 16-byte accesses (threads map to 4-row groups x lanes).
-__device__ void reduce_tile(const TcParams& p, int m_tile) {
+__device__ void reduce_tile(const TcParams& p, int m_tile, int lane0, int lanes) {
   const int64_t R = (int64_t)p.m_tiles * kBM;
   const int t = threadIdx.x;  // 0..127
   if (p.epi == EPI_SWIGLU) {
     const int rq = (t & 15) * 4, lsub = t >> 4;  // 16 threads per lane row
     const int f0 = m_tile * 64 + rq;
     if (f0 >= p.n_out) return;
-    for (int b0 = lsub; b0 < p.lanes; b0 += 16) {
+    for (int b0 = lsub; b0 < lanes; b0 += 16) {
       float4 g[2], u[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k)
-        if (b0 + 8 * k < p.lanes) {
-          g[k] = sum_splits4(p, R, b0 + 8 * k, (int64_t)m_tile * kBM + rq);
-          u[k] = sum_splits4(p, R, b0 + 8 * k, (int64_t)m_tile * kBM + 64 + rq);
+        if (b0 + 8 * k < lanes) {
+          g[k] = sum_splits4(p, R, lane0 + b0 + 8 * k, (int64_t)m_tile * kBM + rq);
+          u[k] = sum_splits4(p, R, lane0 + b0 + 8 * k, (int64_t)m_tile * kBM + 64 + rq);
         }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int b = b0 + 8 * k;
-        if (b >= p.lanes) break;
+        if (b >= lanes) break;
         __nv_bfloat162 lo =
             __floats2bfloat162_rn(silu(g[k].x) * u[k].x, silu(g[k].y) * u[k].y);
         __nv_bfloat162 hi =
@@ -230,7 +235,7 @@ __device__ void reduce_tile(const TcParams& p, int m_tile) {
         pk.x = *reinterpret_cast<uint32_t*>(&lo);
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
         *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_x) +
-                                  (int64_t)(p.lane0 + b) * p.ldo + f0) = pk;
+                                  (int64_t)(lane0 + b) * p.ldo + f0) = pk;
       }
     }
     return;
@@ -240,16 +245,16 @@ __device__ void reduce_tile(const TcParams& p, int m_tile) {
   if (row0 >= p.n_out) return;
   const bool vec = (p.ldo & 3) == 0 && row0 + 4 <= p.n_out;
   constexpr int U = 4;  // lanes in flight per thread: all loads, then stores
-  for (int b0 = lsub; b0 < p.lanes; b0 += 4 * U) {
+  for (int b0 = lsub; b0 < lanes; b0 += 4 * U) {
     float4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (b0 + 4 * u < p.lanes) v[u] = sum_splits4(p, R, b0 + 4 * u, row0);
+      if (b0 + 4 * u < lanes) v[u] = sum_splits4(p, R, lane0 + b0 + 4 * u, row0);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int b = b0 + 4 * u;
-      if (b >= p.lanes) break;
-      float* o = p.out_f32 + (int64_t)(p.lane0 + b) * p.ldo + row0;
+      if (b >= lanes) break;
+      float* o = p.out_f32 + (int64_t)(lane0 + b) * p.ldo + row0;
       if (vec) {
         *reinterpret_cast<float4*>(o) = v[u];
       } else {
@@ -261,8 +266,8 @@ __device__ void reduce_tile(const TcParams& p, int m_tile) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-              const TcParams p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
+              const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -271,7 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x / p.splits, split = blockIdx.x - m_tile * p.splits;
+  const int group = blockIdx.x % p.groups;
+  const int rest = blockIdx.x / p.groups;
+  const int split = rest % p.splits, m_tile = rest / p.splits;
+  const int lane0 = group * p.lg;
+  const int lanes = min(p.lg, p.lanes_total - lane0);
+  const int n_tot = (lanes + 15) & ~15;
   const int kb0 = split * p.kb_total / p.splits;
   const int kb1 = (split + 1) * p.kb_total / p.splits;
   const int nkb = kb1 - kb0;
@@ -316,11 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*(volatile int*)&s_abort) break;
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)p.stage_bytes);
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
         const int x = (kb0 + i) * kBK;
         tma_load_2d(st, &tmW, x, m_tile * kBM, full0 + 8 * s);
-        for (int r = 0; r < p.n_tot; r += kXBoxRows)
-          tma_load_2d(st + kWTileBytes + r * 128, &tmX, x, p.lane0 + r, full0 + 8 * s);
+        int r = 0;
+        for (; r + 64 <= n_tot; r += 64)
+          tma_load_2d(st + kWTileBytes + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
+        for (; r < n_tot; r += kXBoxRows)
+          tma_load_2d(st + kWTileBytes + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
         issued = i + 1;
       }
       // drain: every issued load must have landed before the block exits
@@ -345,16 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
         const uint32_t b0 = a0 + kWTileBytes;
+        const uint32_t idesc = idesc_bf16(kBM, n_tot);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = sw128_desc(a0 + kk * 32);
-          for (int c = 0; c * 256 < p.n_tot; ++c) {
-            const int nc = min(256, p.n_tot - c * 256);
-            const uint64_t bd = sw128_desc(b0 + c * 256 * 128 + kk * 32);
-            mma_bf16(tmem + c * 256, ad, bd, idesc_bf16(kBM, nc),
-                     (i > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                   (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
       }
       mma_commit(accum);  // arrives when every MMA issued above has finished
@@ -371,50 +379,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool abort = *(volatile int*)&s_abort != 0;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     if (p.splits == 1) {
-      for (int c0 = 0; c0 < p.n_tot; c0 += 32) {
+      for (int c0 = 0; c0 < n_tot; c0 += 32) {
         uint32_t r0[16], r1[16];
         tmem_ld16(trow + c0, r0);
-        if (c0 + 16 < p.n_tot) tmem_ld16(trow + c0 + 16, r1);
+        if (c0 + 16 < n_tot) tmem_ld16(trow + c0 + 16, r1);
         tmem_wait();
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r0[j]);
-        if (!abort) emit_chunk(p, m_tile, row_local, c0, v, xbuf);
-        if (c0 + 16 < p.n_tot) {
+        if (!abort) emit_chunk(p, m_tile, row_local, lane0, lanes, c0, v, xbuf);
+        if (c0 + 16 < n_tot) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r1[j]);
-          if (!abort) emit_chunk(p, m_tile, row_local, c0 + 16, v, xbuf);
+          if (!abort) emit_chunk(p, m_tile, row_local, lane0, lanes, c0 + 16, v, xbuf);
         }
       }
     } else {
       const int64_t R = (int64_t)p.m_tiles * kBM;
       const int64_t row = (int64_t)m_tile * kBM + row_local;
-      for (int c0 = 0; c0 < p.n_tot; c0 += 32) {
+      for (int c0 = 0; c0 < n_tot; c0 += 32) {
         uint32_t r0[16], r1[16];
         tmem_ld16(trow + c0, r0);
-        if (c0 + 16 < p.n_tot) tmem_ld16(trow + c0 + 16, r1);
+        if (c0 + 16 < n_tot) tmem_ld16(trow + c0 + 16, r1);
         tmem_wait();
-        float* dst = p.ws + ((int64_t)split * p.n_tot + c0) * R + row;
+        float* dst = p.ws + ((int64_t)split * p.lanes_total + lane0 + c0) * R + row;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (c0 + j < p.lanes) dst[(int64_t)j * R] = __uint_as_float(r0[j]);
-        if (c0 + 16 < p.n_tot) {
+          if (c0 + j < lanes) dst[(int64_t)j * R] = __uint_as_float(r0[j]);
+        if (c0 + 16 < n_tot) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + 16 + j < p.lanes) dst[(int64_t)(16 + j) * R] = __uint_as_float(r1[j]);
+            if (c0 + 16 + j < lanes) dst[(int64_t)(16 + j) * R] = __uint_as_float(r1[j]);
         }
       }
       __threadfence();
       epi_bar();
+      int* ctr = p.counters + m_tile * p.groups + group;
       if (threadIdx.x == 0) {
-        const int prev = atomicAdd(p.counters + m_tile, 1);
+        const int prev = atomicAdd(ctr, 1);
         s_last = (prev == p.splits - 1);
       }
       epi_bar();
       if (s_last) {
         __threadfence();
-        if (!abort) reduce_tile(p, m_tile);
-        if (threadIdx.x == 0) p.counters[m_tile] = 0;  // ready for the next launch
+        if (!abort) reduce_tile(p, m_tile, lane0, lanes);
+        if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
       }
     }
   }
@@ -460,21 +469,24 @@ int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMa
 }
 
 // Dynamic shared memory: 1 KB alignment slack, the stages, the barriers.
-// The stage budget leaves room under the 227 KB per-block limit for the
-// kernel's static shared variables.
+// Small tiles (<= 24 KB per stage) get a budget that lets two blocks share
+// an SM; large ones use the per-block limit, minus room for the kernel's
+// static shared variables.
 constexpr int kSmemAttr = 227 * 1024 - 256;
 int tc_stages_for(int n_tot, int* stage_bytes, int* smem_bytes) {
   const int sb = kWTileBytes + n_tot * 128;
-  const int budget = kSmemAttr - 1024 - 512;
-  int st = budget / sb;
-  if (st > 8) st = 8;
+  int st;
+  if (sb <= 24 * 1024)
+    st = std::min(5, (110 * 1024 - 1536) / sb);
+  else
+    st = std::min(8, (kSmemAttr - 1536) / sb);
   *stage_bytes = sb;
   *smem_bytes = 1024 + st * sb + 8 * (2 * st + 1);
   return st;
 }
 
-int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParams& p0,
-                   cudaStream_t s) {
+int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                   const TcParams& p0, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -484,8 +496,8 @@ int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcParam
   }
   TcParams p = p0;
   int smem = 0;
-  p.stages = tc_stages_for(p.n_tot, &p.stage_bytes, &smem);
-  k_gemm_tc<<<p.m_tiles * p.splits, kThreads, smem, s>>>(tmW, tmX, p);
+  p.stages = tc_stages_for((p.lg + 15) & ~15, &p.stage_bytes, &smem);
+  k_gemm_tc<<<p.m_tiles * p.splits * p.groups, kThreads, smem, s>>>(tmW, tmX64, tmX16, p);
   return 1;
 }
 
