@@ -1,0 +1,127 @@
+// fs_gemm_bf16_noalloc: the tcgen05 weight-streaming GEMM without any device
+// allocation.
+//
+// Some callers cannot call cudaMalloc or cudaFree. One example is a process
+// whose device memory belongs to another framework's caching allocator, where
+// raw allocations would compete with that pool. Another is a latency-critical
+// loop, where cudaFree synchronises the whole device and allocation time is
+// unbounded. A third is an embedder with a fixed, pre-planned device-memory
+// budget. For them, this entry point runs the same GEMM kernel as
+// fs_gemm_bf16. The K-split workspace of that kernel (partial tiles, arrival
+// counters and the error flag) lives in the file-scope array below instead of
+// memory allocated per call. Every GPU that loads this library keeps the array
+// until the process exits.
+//
+// Set-up: the first call on a device looks up the array's device address with
+// cudaGetSymbolAddress (with that device current) and caches it per device.
+// That first call on a device should come before any stream capture.
+//
+// Sharing: every call on a device uses the same array, which keeps the last
+// call's contents. Each call clears the counters and the error flag before
+// its launch. Calls that overlap on the GPU (on different streams, or from
+// different threads) race on the array and must be serialised by the caller.
+
+#include <mutex>
+
+#include "../../include/fs.h"
+#include "fs_internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = (size_t)8 << 20;  // 8 MiB in all
+constexpr size_t kCtrBytes = (size_t)64 << 10;     // counters + error flag
+constexpr size_t kPartialBytes = kScratchBytes - kCtrBytes;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned char* g_dev_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up once).
+unsigned char* scratch_on_current_device(int* rc) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *rc = FS_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      *rc = FS_ERR_CUDA;
+      return nullptr;
+    }
+    g_dev_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *rc = FS_OK;
+  return g_dev_addr[dev];
+}
+
+int64_t round_up16(int64_t x) { return (x + 15) / 16 * 16; }
+
+// Lanes per group: the same rule as the allocating entry point (about two
+// blocks per SM, groups of 32..256 lanes; fewer when B is small).
+int lane_group(int n, int units) {
+  const int want = (304 + units - 1) / units > 1 ? (304 + units - 1) / units : 1;
+  int lg = (int)round_up16((n + want - 1) / want);
+  const int floor_lg = (int)(round_up16(n) < 32 ? round_up16(n) : 32);
+  if (lg < floor_lg) lg = floor_lg;
+  return lg < 256 ? lg : 256;
+}
+
+}  // namespace
+
+extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
+                                    const uint16_t* X, int32_t B, float* Y,
+                                    int32_t splits, void* stream) {
+  using namespace fsk;
+  if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
+      splits > K / 64 || splits > 8)
+    return FS_ERR_ARG;
+  const int64_t m_tiles = (N + 127) / 128;
+  const int lg = lane_group(B, (int)(m_tiles * splits));
+  const int groups = (B + lg - 1) / lg;
+  const size_t ctr_bytes = (size_t)(m_tiles * groups + 1) * sizeof(int);
+  const size_t part_bytes =
+      splits > 1 ? (size_t)splits * B * m_tiles * 128 * sizeof(float) : 0;
+  if (ctr_bytes > kCtrBytes || part_bytes > kPartialBytes) return FS_ERR_SCRATCH;
+
+  int rc = FS_OK;
+  unsigned char* base = scratch_on_current_device(&rc);
+  if (rc != FS_OK) return rc;
+  int* counters = reinterpret_cast<int*>(base);
+  int* err = counters + m_tiles * groups;
+  float* ws = reinterpret_cast<float*>(base + kCtrBytes);
+
+  CUtensorMap tw, tx, tx64;
+  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
+      tc_make_map(X, B, K, 64, &tx64))
+    return FS_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // what must start at zero: the arrival counters and the error flag
+  if (cudaMemsetAsync(counters, 0, ctr_bytes, s) != cudaSuccess) return FS_ERR_CUDA;
+  TcParams p{};
+  p.m_tiles = (int)m_tiles;
+  p.splits = splits;
+  p.kb_total = K / 64;
+  p.lanes_total = B;
+  p.lg = lg;
+  p.groups = groups;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < lg) p.tmem_cols *= 2;
+  p.epi = EPI_STORE;
+  p.out_f32 = Y;
+  p.ldo = N;
+  p.n_out = N;
+  p.ws = ws;
+  p.counters = counters;
+  p.err = err;
+  launch_gemm_tc(tw, tx64, tx, p, s);
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return FS_ERR_CUDA;
+  int herr = 0;
+  if (cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FS_ERR_CUDA;
+  return herr ? FS_ERR_DEVICE : FS_OK;
+}

@@ -18,7 +18,7 @@ FS_OK = 0
 ERRORS = {-1: "FS_ERR_ARG", -2: "FS_ERR_LANE", -3: "FS_ERR_DUP_LANE",
           -4: "FS_ERR_POSITION", -5: "FS_ERR_TOKEN", -6: "FS_ERR_KV_FULL",
           -7: "FS_ERR_OOM", -8: "FS_ERR_CUDA", -9: "FS_ERR_STATE",
-          -10: "FS_ERR_DEVICE"}
+          -10: "FS_ERR_DEVICE", -11: "FS_ERR_SCRATCH"}
 CODES = {v: k for k, v in ERRORS.items()}
 FS_DTYPE_F32, FS_DTYPE_BF16, FS_DTYPE_Q8_0 = 0, 1, 2
 
@@ -89,6 +89,7 @@ def lib():
         "fs_gemm_path": (C.c_char_p, [p]),
         "fs_device_error": (C.c_int, [p, p]),
         "fs_copy_logits": (C.c_int, [p, p]),
+        "fs_gemm_bf16_noalloc": (C.c_int, [p, i32, i32, p, i32, p, i32, p]),
         "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
     }
     for name, (res, args) in sig.items():
@@ -107,7 +108,7 @@ def exported_symbols() -> list:
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
-            "fs_gemm_bf16", "fs_copy_logits"]
+            "fs_gemm_bf16", "fs_copy_logits", "fs_gemm_bf16_noalloc"]
 
 
 def _check(h, rc: int) -> None:
@@ -305,3 +306,15 @@ def fs_gemm_bf16(W, X, Y, splits: int = 1, path: int = 1, stream=None) -> None:
 def fs_copy_logits(h, dst) -> None:
     """Copies the last step's logits [n, V] f32 into dst (numpy or torch)."""
     _check(h, lib().fs_copy_logits(h, _dptr(dst)))
+
+
+def fs_gemm_bf16_noalloc(W, X, Y, splits: int = 1, stream=None) -> None:
+    """fs_gemm_bf16 (tcgen05 path) with its workspace in the library's static
+    device scratch instead of allocations (see include/fs.h)."""
+    raw = getattr(stream, "cuda_stream", stream)
+    N, K = W.shape
+    B = X.shape[0]
+    rc = lib().fs_gemm_bf16_noalloc(_dptr(W), N, K, _dptr(X), B, _dptr(Y),
+                                    splits, raw)
+    if rc != FS_OK:
+        raise FsError(rc, "fs_gemm_bf16_noalloc failed")

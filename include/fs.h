@@ -57,6 +57,8 @@ extern "C" {
 #define FS_ERR_CUDA (-8)      /* a CUDA call failed (message has the detail)  */
 #define FS_ERR_STATE (-9)     /* call out of order (e.g. sample before step)  */
 #define FS_ERR_DEVICE (-10)   /* a kernel reported a device-side error flag   */
+#define FS_ERR_SCRATCH (-11)  /* request exceeds fs_gemm_bf16_noalloc's static
+                                 scratch                                      */
 
 /* ---- element types ----------------------------------------------------- */
 #define FS_DTYPE_F32 0   /* IEEE binary32                                     */
@@ -252,6 +254,34 @@ int fs_device_error(fs_handle* h, int32_t* code_out);
 int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
                  int32_t B, float* Y, int32_t splits, int32_t path,
                  void* stream);
+
+/* fs_gemm_bf16 without any device allocation. The pages have no counterpart
+ * of this entry point; it exists for callers that cannot call cudaMalloc or
+ * cudaFree: for example a process whose device memory belongs to another
+ * framework's caching allocator, a latency-critical loop in which cudaFree's
+ * device-wide synchronisation or an unbounded allocation time is not
+ * acceptable, or an embedder with a fixed device-memory budget.
+ *
+ * Computes Y[b, n] = sum_k X[b, k] * W[n, k] on the tcgen05 path with
+ * `splits` K splits (1 <= splits <= min(8, K/64)), exactly as
+ * fs_gemm_bf16(..., splits, path = 1, ...): bf16 W [N, K], bf16 X [B, K],
+ * f32 Y [B, N], K a multiple of 64, all DEVICE pointers owned by the caller.
+ * Runs on `stream` (NULL = default) and synchronises it.
+ *
+ * Scratch: a static device array of 8 MiB in this library (every GPU that
+ * loads the library holds it until exit). It holds up to 16384 arrival
+ * counters (ceil(N/128) * lane groups + 1 <= 16384) and, when splits > 1,
+ * splits * B * ceil(N/128) * 128 f32 partials within 8 MiB - 64 KiB (for
+ * example N = 4096, splits = 4, B <= 126). Larger requests return
+ * FS_ERR_SCRATCH and run nothing. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture. Every call shares the
+ * array and clears its counters and error flag first; calls that overlap on
+ * the GPU race and must be serialised by the caller.
+ * Errors: FS_ERR_ARG, FS_ERR_SCRATCH, FS_ERR_CUDA, FS_ERR_DEVICE. */
+int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
+                         const uint16_t* X, int32_t B, float* Y,
+                         int32_t splits, void* stream);
 
 #ifdef __cplusplus
 }
