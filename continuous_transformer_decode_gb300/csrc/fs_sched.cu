@@ -1,0 +1,341 @@
+// Host scheduler around decode_step_batch: fill / gather / step / fold with
+// decode-first, bounded prefill ("Fat-station continuous batching",
+// "Components" item 3; "DGR-012", "Summary"). Policy details are stated in
+// include/fs_sched.h. Host code only.
+
+#include <algorithm>
+#include <cstring>
+#include <deque>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/fs.h"
+#include "../../include/fs_sched.h"
+
+namespace {
+
+// What one batched step needs from a model.
+struct Engine {
+  virtual ~Engine() = default;
+  virtual int capacity() const = 0;
+  virtual int reset(int lane) = 0;
+  // lanes/positions/tokens of n lanes; positions advanced on success
+  virtual int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens,
+                   int n) = 0;
+  virtual int sample(int n, const float* temps, const uint64_t* seeds,
+                     const uint64_t* counters, int32_t* out) = 0;
+  virtual std::string error() const = 0;
+};
+
+struct GpuEngine : Engine {
+  fs_handle* h;
+  int cap;
+  explicit GpuEngine(fs_handle* hh, int c) : h(hh), cap(c) {}
+  int capacity() const override { return cap; }
+  int reset(int lane) override { return fs_lane_reset(h, lane); }
+  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens,
+           int n) override {
+    return fs_decode_step_batch(h, lanes, positions, tokens, n, nullptr);
+  }
+  int sample(int n, const float* temps, const uint64_t* seeds, const uint64_t* counters,
+             int32_t* out) override {
+    return fs_sample(h, n, temps, seeds, counters, out);
+  }
+  std::string error() const override { return fs_last_error(h); }
+};
+
+uint64_t mix64(uint64_t z) {  // splitmix64 finaliser
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Deterministic stand-in for a model: each lane hashes the tokens it consumed.
+struct ModelFreeEngine : Engine {
+  int cap, vocab;
+  std::vector<uint64_t> hash;
+  std::vector<int32_t> len;
+  std::vector<int32_t> last_lanes;
+  ModelFreeEngine(int c, int v) : cap(c), vocab(v), hash(c, 0xCBF29CE484222325ull), len(c, 0) {}
+  int capacity() const override { return cap; }
+  int reset(int lane) override {
+    if (lane < 0 || lane >= cap) return FS_ERR_LANE;
+    hash[lane] = 0xCBF29CE484222325ull;
+    len[lane] = 0;
+    return FS_OK;
+  }
+  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n) override {
+    for (int i = 0; i < n; ++i) {
+      if (lanes[i] < 0 || lanes[i] >= cap) return FS_ERR_LANE;
+      if (positions[i] != len[lanes[i]]) return FS_ERR_POSITION;
+      if (tokens[i] < 0 || tokens[i] >= vocab) return FS_ERR_TOKEN;
+    }
+    last_lanes.assign(lanes, lanes + n);
+    for (int i = 0; i < n; ++i) {
+      uint64_t& hh = hash[lanes[i]];
+      hh = (hh ^ (uint64_t)(uint32_t)tokens[i]) * 0x100000001B3ull;
+      len[lanes[i]] += 1;
+      positions[i] += 1;
+    }
+    return FS_OK;
+  }
+  int sample(int n, const float* temps, const uint64_t* seeds, const uint64_t* counters,
+             int32_t* out) override {
+    if (n != (int)last_lanes.size()) return FS_ERR_STATE;
+    for (int i = 0; i < n; ++i) {
+      const uint64_t hh = hash[last_lanes[i]];
+      uint64_t v = hh;
+      if (temps[i] != 0.0f) v = hh ^ mix64(seeds[i] + 0x9E3779B97F4A7C15ull * (counters[i] + 1));
+      out[i] = (int32_t)(v % (uint64_t)vocab);
+    }
+    return FS_OK;
+  }
+  std::string error() const override { return "model-free engine"; }
+};
+
+struct Job {
+  int64_t id;
+  std::vector<int32_t> prompt;
+  int32_t max_new;
+  float temp;
+  uint64_t seed;
+  int32_t stop;
+};
+
+struct Lane {
+  bool busy = false;
+  Job job;
+  int32_t feed = 0;
+  std::vector<int32_t> gen;
+  int32_t last = 0;
+  int64_t seq = 0;
+  int32_t pos = 0;
+};
+
+}  // namespace
+
+struct fs_sched {
+  std::unique_ptr<Engine> eng;
+  fs_sched_config cfg{};
+  std::deque<Job> pending;
+  std::vector<Lane> lanes;
+  std::map<int64_t, std::vector<int32_t>> done;
+  int64_t next_id = 0, admit_seq = 0;
+  fs_sched_stats st{};
+  double occ_sum = 0.0;
+  std::vector<int32_t> last_batch;
+  std::string err;
+  // per-step buffers
+  std::vector<int32_t> b_lanes, b_pos, b_tok, b_out;
+  std::vector<float> b_temp;
+  std::vector<uint64_t> b_seed, b_ctr;
+
+  int fail(int code, const std::string& m) {
+    err = m;
+    return code;
+  }
+};
+
+namespace {
+
+int make(std::unique_ptr<Engine> eng, const fs_sched_config* cfg, fs_sched** out) {
+  if (!cfg || !out) return FS_ERR_ARG;
+  if (cfg->lanes < 1 || cfg->lanes > eng->capacity() || cfg->max_prefill_tokens_per_tick < 1 ||
+      cfg->max_queue < 0)
+    return FS_ERR_ARG;
+  fs_sched* s = new fs_sched();
+  s->eng = std::move(eng);
+  s->cfg = *cfg;
+  s->lanes.resize(cfg->lanes);
+  *out = s;
+  return FS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fs_sched_create(fs_handle* h, const fs_sched_config* cfg, fs_sched** out) {
+  if (!h || !cfg || cfg->lanes < 1) return FS_ERR_ARG;
+  int32_t len = 0;  // the handle must address lanes 0 .. cfg->lanes - 1
+  if (fs_lane_length(h, cfg->lanes - 1, &len) != FS_OK) return FS_ERR_ARG;
+  return make(std::unique_ptr<Engine>(new GpuEngine(h, cfg->lanes)), cfg, out);
+}
+
+int fs_sched_create_model_free(const fs_sched_config* cfg, int32_t vocab, fs_sched** out) {
+  if (!cfg || vocab < 1) return FS_ERR_ARG;
+  return make(std::unique_ptr<Engine>(new ModelFreeEngine(cfg->lanes, vocab)), cfg, out);
+}
+
+int fs_sched_destroy(fs_sched* s) {
+  delete s;
+  return FS_OK;
+}
+
+int fs_sched_submit(fs_sched* s, const fs_job* j, int64_t* job_id_out) {
+  if (!s || !j) return FS_ERR_ARG;
+  if (!j->prompt || j->prompt_len < 1 || j->max_new_tokens < 1 || !(j->temperature >= 0.0f))
+    return s->fail(FS_ERR_ARG, "job needs a prompt, max_new_tokens >= 1, temperature >= 0");
+  if (s->cfg.max_queue > 0 && (int)s->pending.size() >= s->cfg.max_queue) {
+    s->st.rejected += 1;
+    return s->fail(FS_ERR_QUEUE_FULL, "pending queue is full");
+  }
+  Job job;
+  job.id = s->next_id++;
+  job.prompt.assign(j->prompt, j->prompt + j->prompt_len);
+  job.max_new = j->max_new_tokens;
+  job.temp = j->temperature;
+  job.seed = j->seed;
+  job.stop = j->stop_token;
+  s->pending.push_back(std::move(job));
+  s->st.jobs_submitted += 1;
+  if (job_id_out) *job_id_out = s->next_id - 1;
+  return FS_OK;
+}
+
+int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
+  if (!s) return FS_ERR_ARG;
+  if (n_retired_out) *n_retired_out = 0;
+  const int L = s->cfg.lanes;
+  // ---- fill: free lanes in lane order take the oldest pending jobs
+  for (int k = 0; k < L && !s->pending.empty(); ++k) {
+    Lane& ln = s->lanes[k];
+    if (ln.busy) continue;
+    int rc = s->eng->reset(k);
+    if (rc) return s->fail(rc, "lane reset: " + s->eng->error());
+    ln.busy = true;
+    ln.job = std::move(s->pending.front());
+    s->pending.pop_front();
+    ln.feed = 0;
+    ln.gen.clear();
+    ln.last = 0;
+    ln.pos = 0;
+    ln.seq = s->admit_seq++;
+  }
+  // ---- gather: decode lanes always, prompt lanes oldest first within budget
+  std::vector<int> prompt_lanes;
+  std::vector<char> chosen(L, 0);
+  for (int k = 0; k < L; ++k) {
+    const Lane& ln = s->lanes[k];
+    if (!ln.busy) continue;
+    if (ln.feed >= (int)ln.job.prompt.size())
+      chosen[k] = 1;
+    else
+      prompt_lanes.push_back(k);
+  }
+  std::sort(prompt_lanes.begin(), prompt_lanes.end(),
+            [&](int a, int b) { return s->lanes[a].seq < s->lanes[b].seq; });
+  const int budget = std::max(1, s->cfg.max_prefill_tokens_per_tick);
+  for (int i = 0; i < (int)prompt_lanes.size() && i < budget; ++i) chosen[prompt_lanes[i]] = 1;
+  s->b_lanes.clear();
+  s->b_pos.clear();
+  s->b_tok.clear();
+  for (int k = 0; k < L; ++k) {
+    if (!chosen[k]) continue;
+    const Lane& ln = s->lanes[k];
+    s->b_lanes.push_back(k);
+    s->b_pos.push_back(ln.pos);
+    s->b_tok.push_back(ln.feed < (int)ln.job.prompt.size() ? ln.job.prompt[ln.feed] : ln.last);
+  }
+  const int n = (int)s->b_lanes.size();
+  if (n == 0) return FS_OK;
+  // ---- one batched step, then one sample over the step's lanes
+  int rc = s->eng->step(s->b_lanes.data(), s->b_pos.data(), s->b_tok.data(), n);
+  if (rc) return s->fail(rc, "decode step: " + s->eng->error());
+  s->b_temp.resize(n);
+  s->b_seed.resize(n);
+  s->b_ctr.resize(n);
+  s->b_out.resize(n);
+  for (int i = 0; i < n; ++i) {
+    const Lane& ln = s->lanes[s->b_lanes[i]];
+    s->b_temp[i] = ln.job.temp;
+    s->b_seed[i] = ln.job.seed;
+    s->b_ctr[i] = (uint64_t)ln.gen.size();
+  }
+  rc = s->eng->sample(n, s->b_temp.data(), s->b_seed.data(), s->b_ctr.data(), s->b_out.data());
+  if (rc) return s->fail(rc, "sample: " + s->eng->error());
+  s->last_batch = s->b_lanes;
+  s->st.steps += 1;
+  s->st.occupancy_last = n;
+  s->st.occupancy_max = std::max(s->st.occupancy_max, n);
+  s->occ_sum += n;
+  // ---- fold
+  int retired = 0;
+  for (int i = 0; i < n; ++i) {
+    Lane& ln = s->lanes[s->b_lanes[i]];
+    ln.pos += 1;
+    const bool in_prompt = ln.feed < (int)ln.job.prompt.size();
+    if (in_prompt)
+      s->st.prefill_tokens += 1;
+    else
+      s->st.decode_tokens += 1;
+    ln.feed += 1;
+    if (ln.feed < (int)ln.job.prompt.size()) continue;
+    const int32_t t = s->b_out[i];
+    ln.gen.push_back(t);
+    ln.last = t;
+    if ((int)ln.gen.size() >= ln.job.max_new || (ln.job.stop >= 0 && t == ln.job.stop)) {
+      s->done[ln.job.id] = ln.gen;
+      ln.busy = false;
+      s->st.jobs_done += 1;
+      ++retired;
+    }
+  }
+  if (n_retired_out) *n_retired_out = retired;
+  return FS_OK;
+}
+
+int fs_sched_run(fs_sched* s, int64_t max_steps, int64_t* steps_out) {
+  if (!s) return FS_ERR_ARG;
+  int64_t k = 0;
+  auto busy = [&] {
+    if (!s->pending.empty()) return true;
+    for (const Lane& l : s->lanes)
+      if (l.busy) return true;
+    return false;
+  };
+  while (busy() && k < max_steps) {
+    int rc = fs_sched_step(s, nullptr);
+    if (rc) return rc;
+    ++k;
+  }
+  if (steps_out) *steps_out = k;
+  return FS_OK;
+}
+
+int fs_sched_take(fs_sched* s, int64_t job_id, int32_t* tokens_out, int32_t cap,
+                  int32_t* n_out) {
+  if (!s || !n_out || cap < 0 || (cap > 0 && !tokens_out)) return FS_ERR_ARG;
+  auto it = s->done.find(job_id);
+  if (it == s->done.end()) return s->fail(FS_ERR_STATE, "job unknown or not finished");
+  const int n = (int)it->second.size();
+  std::memcpy(tokens_out, it->second.data(), (size_t)std::min(n, cap) * 4);
+  *n_out = n;
+  s->done.erase(it);
+  return FS_OK;
+}
+
+int fs_sched_get_stats(const fs_sched* s, fs_sched_stats* out) {
+  if (!s || !out) return FS_ERR_ARG;
+  *out = s->st;
+  int active = 0;
+  for (const Lane& l : s->lanes) active += l.busy ? 1 : 0;
+  out->active = active;
+  out->queued = (int32_t)s->pending.size();
+  out->occupancy_avg = s->st.steps ? s->occ_sum / (double)s->st.steps : 0.0;
+  return FS_OK;
+}
+
+int fs_sched_last_batch(const fs_sched* s, int32_t* lanes_out, int32_t cap, int32_t* n_out) {
+  if (!s || !n_out || cap < 0 || (cap > 0 && !lanes_out)) return FS_ERR_ARG;
+  const int n = (int)s->last_batch.size();
+  std::memcpy(lanes_out, s->last_batch.data(), (size_t)std::min(n, cap) * 4);
+  *n_out = n;
+  return FS_OK;
+}
+
+const char* fs_sched_last_error(const fs_sched* s) { return s ? s->err.c_str() : ""; }
+
+}  // extern "C"

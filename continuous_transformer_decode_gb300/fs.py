@@ -18,7 +18,7 @@ FS_OK = 0
 ERRORS = {-1: "FS_ERR_ARG", -2: "FS_ERR_LANE", -3: "FS_ERR_DUP_LANE",
           -4: "FS_ERR_POSITION", -5: "FS_ERR_TOKEN", -6: "FS_ERR_KV_FULL",
           -7: "FS_ERR_OOM", -8: "FS_ERR_CUDA", -9: "FS_ERR_STATE",
-          -10: "FS_ERR_DEVICE", -11: "FS_ERR_SCRATCH"}
+          -10: "FS_ERR_DEVICE", -11: "FS_ERR_SCRATCH", -12: "FS_ERR_QUEUE_FULL"}
 CODES = {v: k for k, v in ERRORS.items()}
 FS_DTYPE_F32, FS_DTYPE_BF16, FS_DTYPE_Q8_0 = 0, 1, 2
 
@@ -51,6 +51,26 @@ class fs_weights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p),
                 ("final_norm", C.c_void_p),
                 ("layers", C.POINTER(fs_layer_weights))]
+
+
+class fs_sched_config(C.Structure):
+    _fields_ = [("lanes", C.c_int32), ("max_prefill_tokens_per_tick", C.c_int32),
+                ("max_queue", C.c_int32)]
+
+
+class fs_job(C.Structure):
+    _fields_ = [("prompt", C.c_void_p), ("prompt_len", C.c_int32),
+                ("max_new_tokens", C.c_int32), ("temperature", C.c_float),
+                ("seed", C.c_uint64), ("stop_token", C.c_int32)]
+
+
+class fs_sched_stats(C.Structure):
+    _fields_ = [("steps", C.c_int64), ("prefill_tokens", C.c_int64),
+                ("decode_tokens", C.c_int64), ("jobs_submitted", C.c_int64),
+                ("jobs_done", C.c_int64), ("rejected", C.c_int64),
+                ("active", C.c_int32), ("queued", C.c_int32),
+                ("occupancy_last", C.c_int32), ("occupancy_max", C.c_int32),
+                ("occupancy_avg", C.c_double)]
 
 
 LIB_PATH = _build.LIB
@@ -90,6 +110,17 @@ def lib():
         "fs_device_error": (C.c_int, [p, p]),
         "fs_copy_logits": (C.c_int, [p, p]),
         "fs_gemm_bf16_noalloc": (C.c_int, [p, i32, i32, p, i32, p, i32, p]),
+        "fs_sched_create": (C.c_int, [p, C.POINTER(fs_sched_config), C.POINTER(p)]),
+        "fs_sched_create_model_free": (C.c_int, [C.POINTER(fs_sched_config), i32,
+                                                 C.POINTER(p)]),
+        "fs_sched_destroy": (C.c_int, [p]),
+        "fs_sched_submit": (C.c_int, [p, C.POINTER(fs_job), p]),
+        "fs_sched_step": (C.c_int, [p, p]),
+        "fs_sched_run": (C.c_int, [p, i64, p]),
+        "fs_sched_take": (C.c_int, [p, i64, p, i32, p]),
+        "fs_sched_get_stats": (C.c_int, [p, C.POINTER(fs_sched_stats)]),
+        "fs_sched_last_batch": (C.c_int, [p, p, i32, p]),
+        "fs_sched_last_error": (C.c_char_p, [p]),
         "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
     }
     for name, (res, args) in sig.items():
@@ -108,7 +139,10 @@ def exported_symbols() -> list:
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
-            "fs_gemm_bf16", "fs_copy_logits", "fs_gemm_bf16_noalloc"]
+            "fs_gemm_bf16", "fs_copy_logits", "fs_gemm_bf16_noalloc",
+            "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
+            "fs_sched_submit", "fs_sched_step", "fs_sched_run", "fs_sched_take",
+            "fs_sched_get_stats", "fs_sched_last_batch", "fs_sched_last_error"]
 
 
 def _check(h, rc: int) -> None:
@@ -318,3 +352,82 @@ def fs_gemm_bf16_noalloc(W, X, Y, splits: int = 1, stream=None) -> None:
                                     splits, raw)
     if rc != FS_OK:
         raise FsError(rc, "fs_gemm_bf16_noalloc failed")
+
+
+# ------------------------------------------------------------------ scheduler
+def _sched_check(s, rc: int) -> None:
+    if rc != FS_OK:
+        msg = lib().fs_sched_last_error(s)
+        raise FsError(rc, msg.decode() if msg else "")
+
+
+def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
+                    max_queue: int = 0):
+    s = C.c_void_p()
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue)
+    rc = lib().fs_sched_create(h, C.byref(cfg), C.byref(s))
+    if rc != FS_OK:
+        raise FsError(rc, "fs_sched_create failed")
+    return s
+
+
+def fs_sched_create_model_free(lanes: int, vocab: int,
+                               max_prefill_tokens_per_tick: int = 1,
+                               max_queue: int = 0):
+    s = C.c_void_p()
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue)
+    rc = lib().fs_sched_create_model_free(C.byref(cfg), vocab, C.byref(s))
+    if rc != FS_OK:
+        raise FsError(rc, "fs_sched_create_model_free failed")
+    return s
+
+
+def fs_sched_destroy(s) -> None:
+    lib().fs_sched_destroy(s)
+
+
+def fs_sched_submit(s, prompt, max_new_tokens: int, temperature: float = 0.0,
+                    seed: int = 0, stop_token: int = -1) -> int:
+    p = _i32(prompt)
+    job = fs_job(p.ctypes.data, p.size, max_new_tokens, temperature,
+                 int(seed) & (2**64 - 1), stop_token)
+    jid = C.c_int64()
+    _sched_check(s, lib().fs_sched_submit(s, C.byref(job), C.byref(jid)))
+    return jid.value
+
+
+def fs_sched_step(s) -> int:
+    n = C.c_int32()
+    _sched_check(s, lib().fs_sched_step(s, C.byref(n)))
+    return n.value
+
+
+def fs_sched_run(s, max_steps: int = 10**9) -> int:
+    n = C.c_int64()
+    _sched_check(s, lib().fs_sched_run(s, max_steps, C.byref(n)))
+    return n.value
+
+
+def fs_sched_take(s, job_id: int) -> list:
+    n = C.c_int32()
+    buf = np.empty(1 << 16, dtype=np.int32)
+    _sched_check(s, lib().fs_sched_take(s, job_id, _ptr(buf), buf.size, C.byref(n)))
+    return buf[:n.value].tolist()
+
+
+def fs_sched_get_stats(s) -> dict:
+    st = fs_sched_stats()
+    _sched_check(s, lib().fs_sched_get_stats(s, C.byref(st)))
+    return {k: getattr(st, k) for k, _ in st._fields_}
+
+
+def fs_sched_last_batch(s) -> list:
+    n = C.c_int32()
+    buf = np.empty(4096, dtype=np.int32)
+    _sched_check(s, lib().fs_sched_last_batch(s, _ptr(buf), buf.size, C.byref(n)))
+    return buf[:n.value].tolist()
+
+
+def fs_sched_last_error(s) -> str:
+    m = lib().fs_sched_last_error(s)
+    return m.decode() if m else ""

@@ -1,0 +1,123 @@
+/*
+ * fs_sched.h — host scheduler around decode_step_batch (continuous batching).
+ *
+ * Sources (page title, section):
+ *   - "Fat-station continuous batching — the live-path integration",
+ *     "Components", item 3: the decode thread loops fill (a free lane takes
+ *     a pending job: lane reset, position 0), gather (one input token per
+ *     live lane: the next prompt token while the prompt lasts, else the last
+ *     sampled token), one batched step, fold (feed count + 1; inside the
+ *     prompt nothing is sampled; otherwise sample with the lane's
+ *     temperature and seed, append, retire on the stop token or
+ *     max_new_tokens and free the lane for the next fill).
+ *   - "DGR-012 — Continuous batching and bounded admission: evidence",
+ *     "Summary": decode first, then bounded prefill — in-flight decodes
+ *     always run; prompt work per tick is capped by
+ *     max_prefill_tokens_per_tick, with at least one so a long prompt still
+ *     progresses; a full queue is refused (backpressure).
+ *
+ * Policy (the readings taken where the pages leave it open):
+ *   - fill: at the start of a step each free lane, in lane order, takes the
+ *     oldest pending job; a lane freed in step t is refilled in step t+1;
+ *   - gather: every lane past its prompt is in the step; lanes still in their
+ *     prompt are added oldest-admitted first, one token each, up to
+ *     max_prefill_tokens_per_tick tokens (at least 1); the batch lists lanes
+ *     in lane order;
+ *   - fold: the step that consumes a prompt's last token yields the job's
+ *     first generated token; the job's t-th generated token is sampled with
+ *     (seed, counter = t), so a job's tokens do not depend on its lane, its
+ *     step or its neighbours.
+ *
+ * Conventions as in fs.h: FS_OK or a negative FS_ERR_* code; a scheduler is
+ * used by one host thread at a time; pointers are host pointers.
+ */
+#ifndef FS_SCHED_H_
+#define FS_SCHED_H_
+
+#include "fs.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FS_ERR_QUEUE_FULL (-12) /* bounded pending queue is full (backpressure) */
+
+typedef struct fs_sched fs_sched;
+
+typedef struct fs_sched_config {
+  int32_t lanes;                       /* lanes used: 1 .. engine capacity   */
+  int32_t max_prefill_tokens_per_tick; /* prompt tokens per step (>= 1)      */
+  int32_t max_queue;                   /* pending jobs allowed, 0 = no bound */
+} fs_sched_config;
+
+typedef struct fs_job {
+  const int32_t* prompt;   /* prompt_len tokens (copied at submit)           */
+  int32_t prompt_len;      /* >= 1                                            */
+  int32_t max_new_tokens;  /* >= 1                                            */
+  float temperature;       /* 0: greedy                                       */
+  uint64_t seed;           /* per-job sampling seed                           */
+  int32_t stop_token;      /* retire after sampling this token; -1: none      */
+} fs_job;
+
+typedef struct fs_sched_stats {
+  int64_t steps;           /* batched steps run                               */
+  int64_t prefill_tokens;  /* prompt tokens consumed                          */
+  int64_t decode_tokens;   /* generated tokens fed back                       */
+  int64_t jobs_submitted;
+  int64_t jobs_done;
+  int64_t rejected;        /* submits refused with FS_ERR_QUEUE_FULL          */
+  int32_t active;          /* lanes holding a job                             */
+  int32_t queued;          /* pending jobs                                    */
+  int32_t occupancy_last;  /* lanes in the last step                          */
+  int32_t occupancy_max;
+  double occupancy_avg;    /* mean lanes per step                             */
+} fs_sched_stats;
+
+/* Scheduler over a decode handle: each step is one fs_decode_step_batch
+ * (logits kept inside the handle) and one fs_sample over the step's lanes.
+ * cfg->lanes must not exceed the handle's max_lanes. The handle must outlive
+ * the scheduler. Errors: FS_ERR_ARG. */
+int fs_sched_create(fs_handle* h, const fs_sched_config* cfg, fs_sched** out);
+
+/* Scheduler over a model-free engine (no GPU): a lane's "model" keeps a
+ * running 64-bit hash of the tokens it consumed; after a step, greedy lanes
+ * draw hash % vocab and sampled lanes (hash ^ mix(seed, counter)) % vocab,
+ * where mix is the splitmix64 finaliser of seed + 0x9E3779B97F4A7C15 *
+ * (counter + 1) and the hash update is h = (h ^ token) * 0x100000001B3 over
+ * an initial 0xCBF29CE484222325 at lane reset. For testing the policy. */
+int fs_sched_create_model_free(const fs_sched_config* cfg, int32_t vocab,
+                               fs_sched** out);
+
+int fs_sched_destroy(fs_sched* s);
+
+/* Queues a job (FIFO). *job_id_out receives its id (0, 1, ... in submit
+ * order). Errors: FS_ERR_ARG, FS_ERR_QUEUE_FULL (nothing queued). */
+int fs_sched_submit(fs_sched* s, const fs_job* job, int64_t* job_id_out);
+
+/* One fill / gather / step / fold. *n_retired_out (optional) receives the
+ * number of jobs that finished in this step. Idle (no lane, no job) is a
+ * no-op. Errors: those of the engine (the scheduler state is then
+ * undefined). */
+int fs_sched_step(fs_sched* s, int32_t* n_retired_out);
+
+/* Steps until no job is queued or running, at most max_steps steps. */
+int fs_sched_run(fs_sched* s, int64_t max_steps, int64_t* steps_out);
+
+/* Copies a finished job's generated tokens (up to cap) and their count, then
+ * forgets the job. Errors: FS_ERR_STATE (unknown or unfinished job). */
+int fs_sched_take(fs_sched* s, int64_t job_id, int32_t* tokens_out,
+                  int32_t cap, int32_t* n_out);
+
+int fs_sched_get_stats(const fs_sched* s, fs_sched_stats* out);
+
+/* Lanes of the last step in batch order (inspection hook). */
+int fs_sched_last_batch(const fs_sched* s, int32_t* lanes_out, int32_t cap,
+                        int32_t* n_out);
+
+/* Message of the last failure on s. */
+const char* fs_sched_last_error(const fs_sched* s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FS_SCHED_H_ */

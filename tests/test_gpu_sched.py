@@ -1,0 +1,101 @@
+"""GPU: continuous batching through fs_sched over the CUDA decode step.
+
+Per-job tokens must equal the same job run alone (the parity gate of "Fat-
+station continuous batching", "Parity"): against the oracle's serial runs on
+the f32 tiny model, and bit for bit against GPU serial runs on the bf16
+SmolLM2 shape (the GPU step is batch-invariant).
+"""
+import numpy as np
+import pytest
+
+import oracle.core as O
+from oracle import sched as S
+from continuous_transformer_decode_gb300 import build, fs, synth
+from tests import _gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _jobs(n, vocab, seed, max_prompt=12, max_new=10):
+    g = np.random.default_rng(seed)
+    return [dict(id=j, arrive=int(g.integers(0, 2 * n)),
+                 prompt=[int(t) for t in g.integers(0, vocab, int(g.integers(1, max_prompt)))],
+                 max_new=int(g.integers(1, max_new)),
+                 temperature=0.0 if j % 2 else 0.8, seed=1000 + 7 * j)
+            for j in range(n)]
+
+
+def _run_sched(h, jobs, lanes, budget):
+    s = fs.fs_sched_create(h, lanes, budget)
+    try:
+        order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
+        ids, i, tick = {}, 0, 0
+        while i < len(order) or fs.fs_sched_get_stats(s)["active"] or \
+                fs.fs_sched_get_stats(s)["queued"]:
+            while i < len(order) and order[i]["arrive"] <= tick:
+                j = order[i]
+                ids[j["id"]] = fs.fs_sched_submit(s, j["prompt"], j["max_new"],
+                                                  j["temperature"], j["seed"])
+                i += 1
+            fs.fs_sched_step(s)
+            tick += 1
+        st = fs.fs_sched_get_stats(s)
+        return {j["id"]: fs.fs_sched_take(s, ids[j["id"]]) for j in jobs}, st
+    finally:
+        fs.fs_sched_destroy(s)
+
+
+def test_scheduler_tiny_f32_per_job_equals_oracle_serial():
+    cfg = synth.MODEL_T
+    W = synth.make_weights(cfg, seed=1, fmt="f32")
+    m = O.Model(cfg, W, O.F32)
+    jobs = _jobs(14, cfg["V"], 3)
+    h = U.make_gpu(cfg, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=4, max_pos=32)
+    try:
+        got, st = _run_sched(h, jobs, 4, 2)
+    finally:
+        fs.fs_destroy(h)
+    assert st["occupancy_max"] >= 3
+    ln = m.lane(32)
+
+    def step_fn(ks, poss, toks):
+        return m.step_batch([ln], toks)
+
+    def reset_fn(k):
+        ln.reset()
+
+    def sample_fn(row, temp, seed, counter):
+        return O.sample(row, temp, seed, counter)
+    for j in jobs:
+        assert got[j["id"]] == S.serial_job(j, step_fn, sample_fn, reset_fn), j["id"]
+
+
+def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise():
+    cfg = synth.with_layers(synth.MODEL_S, 2)
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    jobs = _jobs(12, cfg["V"], 5)
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=6, max_pos=32)
+    try:
+        got, st = _run_sched(h, jobs, 6, 3)
+        for k in range(6):
+            fs.fs_lane_reset(h, k)
+        for j in jobs:  # each job alone on lane 0, one token per step
+            fs.fs_lane_reset(h, 0)
+            pos = np.zeros(1, np.int32)
+            out = []
+            for t in j["prompt"]:
+                fs.fs_decode_step_batch(h, [0], pos, [t])
+            while True:
+                tok = int(fs.fs_sample(h, [j["temperature"]], [j["seed"]], [len(out)])[0])
+                out.append(tok)
+                if len(out) >= j["max_new"]:
+                    break
+                fs.fs_decode_step_batch(h, [0], pos, [tok])
+            assert got[j["id"]] == out, j["id"]
+    finally:
+        fs.fs_destroy(h)

@@ -1,0 +1,158 @@
+"""The product scheduler (C++, fs_sched_*) against the scheduler reference.
+
+CPU: both drive the same model-free stand-in for a model (a per-lane running
+hash of consumed tokens, as fs_sched.h defines it, restated here in Python),
+so every step's batch, every job's tokens and the counters must match.
+"""
+import numpy as np
+import pytest
+
+from oracle import sched as S
+from continuous_transformer_decode_gb300 import build, fs, synth
+
+M64 = (1 << 64) - 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _mix64(z):
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+    return z ^ (z >> 31)
+
+
+class HashModel:
+    """Python restatement of the model-free engine, for the reference."""
+
+    def __init__(self, n_lanes, vocab):
+        self.h = [0xCBF29CE484222325] * n_lanes
+        self.vocab = vocab
+        self.batches = []
+
+    def reset(self, k):
+        self.h[k] = 0xCBF29CE484222325
+
+    def step(self, ks, poss, toks):
+        self.batches.append(list(ks))
+        for k, t in zip(ks, toks):
+            self.h[k] = ((self.h[k] ^ (t & 0xFFFFFFFF)) * 0x100000001B3) & M64
+        return [self.h[k] for k in ks]  # "logits": the lane's state
+
+    def sample(self, state, temp, seed, counter):
+        v = state
+        if temp != 0.0:
+            v = state ^ _mix64((seed + 0x9E3779B97F4A7C15 * (counter + 1)) & M64)
+        return int(v % self.vocab)
+
+
+def _jobs(n, vocab, seed, max_prompt=9, max_new=9):
+    g = np.random.default_rng(seed)
+    jobs = []
+    for j in range(n):
+        jobs.append(dict(id=j, arrive=int(g.integers(0, 3 * n)),
+                         prompt=[int(t) for t in g.integers(0, vocab, int(g.integers(1, max_prompt)))],
+                         max_new=int(g.integers(1, max_new)),
+                         temperature=0.0 if g.uniform() < 0.5 else 0.8,
+                         seed=int(g.integers(0, 2**63)),
+                         stop=int(g.integers(0, vocab)) if g.uniform() < 0.3 else None))
+    return jobs
+
+
+@pytest.mark.parametrize("lanes,budget,seed", [(1, 1, 0), (3, 1, 1), (4, 2, 2),
+                                               (8, 3, 3), (5, 100, 4)])
+def test_product_scheduler_matches_reference(lanes, budget, seed):
+    vocab = 97
+    jobs = _jobs(24, vocab, seed)
+    model = HashModel(lanes, vocab)
+    ref = S.Reference(lanes, budget, model.step, model.sample, model.reset)
+    want = ref.run(jobs)
+
+    s = fs.fs_sched_create_model_free(lanes, vocab, budget)
+    try:
+        order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
+        ids, i, tick, batches = {}, 0, 0, []
+        while i < len(order) or fs.fs_sched_get_stats(s)["active"] or \
+                fs.fs_sched_get_stats(s)["queued"]:
+            while i < len(order) and order[i]["arrive"] <= tick:
+                j = order[i]
+                ids[j["id"]] = fs.fs_sched_submit(
+                    s, j["prompt"], j["max_new"], j["temperature"], j["seed"],
+                    -1 if j["stop"] is None else j["stop"])
+                i += 1
+            before = fs.fs_sched_get_stats(s)["steps"]
+            fs.fs_sched_step(s)
+            if fs.fs_sched_get_stats(s)["steps"] > before:
+                batches.append(fs.fs_sched_last_batch(s))
+            tick += 1
+        assert batches == model.batches
+        for j in jobs:
+            assert fs.fs_sched_take(s, ids[j["id"]]) == want[j["id"]]
+        st = fs.fs_sched_get_stats(s)
+        assert st["steps"] == ref.steps
+        assert st["prefill_tokens"] == ref.prefill_tokens
+        assert st["decode_tokens"] == ref.decode_tokens
+        assert st["occupancy_max"] == max(ref.occupancy)
+        assert abs(st["occupancy_avg"] - np.mean(ref.occupancy)) < 1e-12
+        assert st["jobs_done"] == len(jobs)
+    finally:
+        fs.fs_sched_destroy(s)
+
+
+def test_decode_first_and_prefill_budget():
+    s = fs.fs_sched_create_model_free(4, 50, max_prefill_tokens_per_tick=1)
+    try:
+        a = fs.fs_sched_submit(s, [1], 20)
+        fs.fs_sched_step(s)  # lane 0 consumes its only prompt token
+        for _ in range(3):
+            fs.fs_sched_submit(s, [2, 3, 4, 5], 2)
+        for _ in range(8):
+            fs.fs_sched_step(s)
+            lanes = fs.fs_sched_last_batch(s)
+            assert 0 in lanes  # the in-flight decode runs every step
+        st = fs.fs_sched_get_stats(s)
+        assert st["prefill_tokens"] == 1 + 8  # one prompt token per step
+    finally:
+        fs.fs_sched_destroy(s)
+
+
+def test_backpressure_and_argument_errors():
+    s = fs.fs_sched_create_model_free(1, 50, 1, max_queue=2)
+    try:
+        fs.fs_sched_submit(s, [1], 3)
+        fs.fs_sched_submit(s, [1], 3)
+        with pytest.raises(fs.FsError) as e:
+            fs.fs_sched_submit(s, [1], 3)
+        assert e.value.name == "FS_ERR_QUEUE_FULL"
+        with pytest.raises(fs.FsError):
+            fs.fs_sched_submit(s, [], 3)
+        with pytest.raises(fs.FsError):
+            fs.fs_sched_submit(s, [1], 0)
+        assert fs.fs_sched_get_stats(s)["rejected"] == 1
+        fs.fs_sched_run(s)
+        st = fs.fs_sched_get_stats(s)
+        assert st["jobs_done"] == 2 and st["active"] == 0 and st["queued"] == 0
+        with pytest.raises(fs.FsError):
+            fs.fs_sched_take(s, 99)
+    finally:
+        fs.fs_sched_destroy(s)
+
+
+def test_dgr_sweep_shape_with_the_product_scheduler():
+    """DGR-012 sweep workload (8 sessions, prompt 4, 8 new tokens) through the
+    product scheduler with one prompt token per step: per-session tokens are
+    identical at every concurrency level and occupancy rises with it."""
+    outs, occ = [], []
+    for c in (1, 2, 4, 8):
+        s = fs.fs_sched_create_model_free(c, 1000, max_prefill_tokens_per_tick=1)
+        try:
+            ids = [fs.fs_sched_submit(s, [10 + k, 20, 30, 40], 8) for k in range(8)]
+            fs.fs_sched_run(s)
+            outs.append([fs.fs_sched_take(s, i) for i in ids])
+            occ.append(fs.fs_sched_get_stats(s)["occupancy_avg"])
+        finally:
+            fs.fs_sched_destroy(s)
+    assert all(o == outs[0] for o in outs)
+    assert occ == sorted(occ) and occ[0] == 1.0
