@@ -34,6 +34,8 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct TcW {
   CUtensorMap tm;
   int m_tiles = 0, splits = 1;
+  int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
+  __half* q8_scales = nullptr;
 };
 
 struct LayerW {
@@ -189,6 +191,14 @@ struct fs_handle {
     err = std::string(what) + ": " + cudaGetErrorString(e);
     return FS_ERR_CUDA;
   }
+  void release(void* p) {
+    for (size_t i = 0; i < allocs.size(); ++i)
+      if (allocs[i] == p) {
+        cudaFree(p);
+        allocs.erase(allocs.begin() + i);
+        return;
+      }
+  }
   template <typename T>
   cudaError_t alloc(T** p, size_t bytes) {
     void* v = nullptr;
@@ -296,7 +306,8 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   {
     const char* env = getenv("FS_GEMM_PATH");
     const bool force_gemv = env && std::string(env) == "gemv";
-    h->use_tc = h->wtype == W_BF16 && d.d_ffn % 64 == 0 && !force_gemv && tc_available();
+    h->use_tc = (h->wtype == W_BF16 || h->wtype == W_Q8) && d.d_ffn % 64 == 0 && !force_gemv &&
+                tc_available();
     const char* genv = getenv("FS_GRAPHS");
     h->graphs_on = !(genv && std::string(genv) == "0");
   }
@@ -357,7 +368,8 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     if ((rc = alloc_mat(h, &L.gateup, 2 * d.d_ffn, d.d_model))) return rc;
     if (h->use_tc) {
       // 128-row tiles of 64 gate rows then the 64 matching up rows
-      const size_t rb = (size_t)d.d_model * 2;
+      const size_t rb = h->wtype == W_Q8 ? (size_t)d.d_model / 32 * 34
+                                         : (size_t)d.d_model * elem_bytes(h->wtype);
       for (int t = 0; t < d.d_ffn / 64; ++t) {
         if ((rc = upload_rows(h, &L.gateup, (const char*)s.w_gate + (size_t)t * 64 * rb, 64,
                               d.d_model, 128 * t, staging)))
@@ -452,6 +464,17 @@ int create_impl(fs_handle* h, const fs_weights* W) {
       max_tiles = std::max(max_tiles, t->m_tiles);
       if (t->splits > 1)
         ws_elems = std::max(ws_elems, (size_t)t->splits * B * t->m_tiles * 128);
+      if (h->wtype == W_Q8) {
+        const size_t tiles = (size_t)t->m_tiles * (m.Kp / 64);
+        if (h->alloc(&t->q8_codes, tiles * 8192) != cudaSuccess ||
+            h->alloc(&t->q8_scales, tiles * 512) != cudaSuccess)
+          return h->fail(FS_ERR_OOM, "Q8_0 tile allocation failed");
+        h->launches += launch_tile_q8((const int8_t*)m.w, m.scales, m.N, m.Kp, t->q8_codes,
+                                      t->q8_scales, h->stream);
+        FS_CK(h, cudaGetLastError());
+        FS_CK(h, cudaStreamSynchronize(h->stream));
+        return FS_OK;
+      }
       if (tc_make_map(m.w, m.N, m.Kp, 128, &t->tm)) return h->fail(FS_ERR_CUDA, "tensor map");
       return FS_OK;
     };
@@ -461,6 +484,20 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         return rc;
     }
     if ((rc = setup(h->head, &h->head_tc))) return rc;
+    if (h->wtype == W_Q8) {  // only the embedding gather still reads row-major codes
+      for (auto& L : h->layers) {
+        for (Mat* m : {&L.qkv, &L.o, &L.gateup, &L.down}) {
+          h->release((void*)m->w);
+          h->release((void*)m->scales);
+          m->w = nullptr;
+          m->scales = nullptr;
+        }
+      }
+      if (!d.tied_embeddings) {
+        h->release((void*)h->head.w);
+        h->release((void*)h->head.scales);
+      }
+    }
     if (tc_make_map(h->hpanel, B, h->Kp_d, 16, &h->tm_h) ||
         tc_make_map(h->opanel, B, h->Kp_q, 16, &h->tm_o) ||
         tc_make_map(h->apanel, B, h->Kp_f, 16, &h->tm_a) ||
@@ -567,7 +604,11 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
     p.tmem_cols = tmem_cols_for(p.lg);
     p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
-    h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc(T.tm, tmX64, tmX, p, s); });
+    p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
+    if (h->wtype == W_Q8)
+      h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc_q8(tmX64, tmX, p, s); });
+    else
+      h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc(T.tm, tmX64, tmX, p, s); });
   };
   const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
   h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
@@ -961,7 +1002,8 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out) {
 
 const char* fs_gemm_path(const fs_handle* h) {
   if (!h) return "";
-  return h->use_tc ? "tcgen05" : "warp-gemv";
+  if (!h->use_tc) return "warp-gemv";
+  return h->wtype == W_Q8 ? "tcgen05-q8_0" : "tcgen05";
 }
 
 int fs_device_error(fs_handle* h, int32_t* code_out) {

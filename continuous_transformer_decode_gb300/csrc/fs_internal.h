@@ -86,12 +86,24 @@ struct TcParams {
   float* ws;       // split partials [splits][lanes_total][m_tiles * 128]
   int* counters;   // [m_tiles * groups], zero between launches
   int* err;        // device-visible error flag
+  // Q8_0 weights in tiles: codes [m_tiles][kb][128][64] int8 and scales
+  // [m_tiles][kb][128][2] fp16 (one per 32 inputs)
+  const int8_t* q8_codes;
+  const __half* q8_scales;
 };
 bool tc_available();
 int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
 // tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.
 int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                    const TcParams& p, cudaStream_t s);
+// Same GEMM over Q8_0 tiles (p.q8_codes / p.q8_scales), dequantised to bf16
+// in shared memory inside the kernel.
+int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const TcParams& p,
+                      cudaStream_t s);
+// Row-major Q8_0 codes [N][Kp] / scales [N][Kp/32] -> the tiled layout above
+// (rows beyond N are zero).
+int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,
+                   __half* scales_t, cudaStream_t s);
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
                  const KV& kv, float* x, int d, cudaStream_t s);

@@ -41,6 +41,10 @@ constexpr int kBK = 64;                 // bf16 elements per 128-byte row
 constexpr int kThreads = 192;
 constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kXBoxRows = 16;
+// Q8_0 stage: bf16 A tile | int8 codes (8 KB) | fp16 scales (512 B) | X tile
+constexpr int kQ8Codes = kBM * kBK;        // 8 KB
+constexpr int kQ8Scales = kBM * 2 * 2;     // 512 B
+constexpr int kQ8XOff = 25 * 1024;         // 16 + 8 + 0.5 KB, 1 KB aligned
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -96,6 +100,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"((uint64_t)src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -265,6 +281,36 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, int lane0, int lanes)
   }
 }
 
+// Dequantises one stage's Q8_0 tile (thread r = weight row r) into the
+// 128-byte-swizzled bf16 A tile: 16-byte chunk c of row r lands at
+// r * 128 + ((c ^ (r % 8)) * 16), the layout a SWIZZLE_128B copy produces.
+__device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
+  const uint8_t* raw = stage + kWTileBytes + r * kBK;
+  const __half* sc = reinterpret_cast<const __half*>(stage + kWTileBytes + kQ8Codes) + r * 2;
+  const float d0 = __half2float(sc[0]), d1 = __half2float(sc[1]);
+  uint8_t* arow = stage + r * 128;
+#pragma unroll
+  for (int c16 = 0; c16 < 4; ++c16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(raw + c16 * 16);
+    const int8_t* q = reinterpret_cast<const int8_t*>(&u);
+    const float d = c16 < 2 ? d0 : d1;  // inputs 0-31 / 32-63 of the block
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn((float)q[half * 8 + 2 * e] * d,
+                                                       (float)q[half * 8 + 2 * e + 1] * d);
+        ow[e] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      const int c = c16 * 2 + half;
+      *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) * 16)) = o;
+    }
+  }
+}
+
+template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
               const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
@@ -288,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S),
-                 accum = smem_u32(bars + 2 * S);
+                 accum = smem_u32(bars + 2 * S), conv0 = smem_u32(bars + 2 * S + 1);
+  constexpr int kXOff = kQ8 ? kQ8XOff : kWTileBytes;
   const uint32_t ncols = p.tmem_cols;
 
   if (threadIdx.x == 0) {
@@ -297,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty0 + 8 * s, 1);
     }
     mbar_init(accum, 1);
+    if (kQ8)
+      for (int s = 0; s < S; ++s) mbar_init(conv0 + 8 * s, 128);  // the 128 converters
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_abort = 0;
     s_last = 0;
@@ -326,14 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (*(volatile int*)&s_abort) break;
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
         const int x = (kb0 + i) * kBK;
-        tma_load_2d(st, &tmW, x, m_tile * kBM, full0 + 8 * s);
+        if (kQ8) {
+          mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
+          const int64_t tile = (int64_t)m_tile * p.kb_total + kb0 + i;
+          bulk_load(st + kWTileBytes, p.q8_codes + tile * kQ8Codes, kQ8Codes, full0 + 8 * s);
+          bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + tile * (kQ8Scales / 2), kQ8Scales,
+                    full0 + 8 * s);
+        } else {
+          mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
+          tma_load_2d(st, &tmW, x, m_tile * kBM, full0 + 8 * s);
+        }
         int r = 0;
         for (; r + 64 <= n_tot; r += 64)
-          tma_load_2d(st + kWTileBytes + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
+          tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
         for (; r < n_tot; r += kXBoxRows)
-          tma_load_2d(st + kWTileBytes + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
+          tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
         issued = i + 1;
       }
       // drain: every issued load must have landed before the block exits
@@ -349,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nkb && ok; ++i) {
         const int s = i % S;
         const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(full0 + 8 * s, ph) || *(volatile int*)&s_abort) {
+        if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
+            *(volatile int*)&s_abort) {
           atomicExch(p.err, 3);
           s_abort = 1;
           ok = false;
@@ -357,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const uint32_t b0 = a0 + kWTileBytes;
+        const uint32_t b0 = a0 + kXOff;
         const uint32_t idesc = idesc_bf16(kBM, n_tot);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -367,8 +425,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(accum);  // arrives when every MMA issued above has finished
     }
-  } else {  // ---- epilogue, warps 0-3
+  } else {  // ---- warps 0-3: Q8_0 dequantisation during the mainloop, then epilogue
     const int row_local = warp * 32 + lane;
+    if (kQ8) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) {
+          atomicExch(p.err, 5);
+          s_abort = 1;
+          break;
+        }
+        dequant_q8_tile(smem + (size_t)s * p.stage_bytes, row_local);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+        mbar_arrive(conv0 + 8 * s);
+      }
+    }
     float* xbuf = reinterpret_cast<float*>(smem);  // stages are idle by now
     if (!mbar_wait(accum, 0)) {
       atomicExch(p.err, 4);
@@ -468,36 +539,83 @@ int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMa
   return r == CUDA_SUCCESS ? 0 : -2;
 }
 
+namespace {
+
 // Dynamic shared memory: 1 KB alignment slack, the stages, the barriers.
 // Small tiles (<= 24 KB per stage) get a budget that lets two blocks share
 // an SM; large ones use the per-block limit, minus room for the kernel's
 // static shared variables.
 constexpr int kSmemAttr = 227 * 1024 - 256;
-int tc_stages_for(int n_tot, int* stage_bytes, int* smem_bytes) {
-  const int sb = kWTileBytes + n_tot * 128;
+int tc_stages_for(int n_tot, bool q8, int* stage_bytes, int* smem_bytes) {
+  const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128;
   int st;
   if (sb <= 24 * 1024)
     st = std::min(5, (110 * 1024 - 1536) / sb);
   else
     st = std::min(8, (kSmemAttr - 1536) / sb);
   *stage_bytes = sb;
-  *smem_bytes = 1024 + st * sb + 8 * (2 * st + 1);
+  *smem_bytes = 1024 + st * sb + 8 * (3 * st + 1);
   return st;
 }
 
-int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                   const TcParams& p0, cudaStream_t s) {
+template <bool kQ8>
+int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                const TcParams& p0, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_gemm_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemAttr) != cudaSuccess)
       return 0;  // the launch below then fails and the caller reports it
     attr_set = true;
   }
   TcParams p = p0;
   int smem = 0;
-  p.stages = tc_stages_for((p.lg + 15) & ~15, &p.stage_bytes, &smem);
-  k_gemm_tc<<<p.m_tiles * p.splits * p.groups, kThreads, smem, s>>>(tmW, tmX64, tmX16, p);
+  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, &p.stage_bytes, &smem);
+  k_gemm_tc<kQ8><<<p.m_tiles * p.splits * p.groups, kThreads, smem, s>>>(tmW, tmX64, tmX16, p);
+  return 1;
+}
+
+__global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __restrict__ scales,
+                          int N, int Kp, int8_t* __restrict__ codes_t,
+                          __half* __restrict__ scales_t) {
+  const int kb_total = Kp / kBK;
+  const int64_t tile = blockIdx.x;  // (m_tile, kb)
+  const int m_tile = (int)(tile / kb_total), kb = (int)(tile % kb_total);
+  const int r = threadIdx.x;        // row in the tile (128 threads)
+  const int row = m_tile * kBM + r;
+  int8_t* dst = codes_t + tile * kQ8Codes + r * kBK;
+  __half* sdst = scales_t + tile * (kQ8Scales / 2) + r * 2;
+  if (row < N) {
+    const int8_t* src = codes + (int64_t)row * Kp + kb * kBK;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+    sdst[0] = scales[(int64_t)row * (Kp / 32) + kb * 2];
+    sdst[1] = scales[(int64_t)row * (Kp / 32) + kb * 2 + 1];
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+    sdst[0] = __float2half_rn(0.0f);
+    sdst[1] = __float2half_rn(0.0f);
+  }
+}
+
+}  // namespace
+
+int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                   const TcParams& p, cudaStream_t s) {
+  return launch_impl<false>(tmW, tmX64, tmX16, p, s);
+}
+
+int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const TcParams& p,
+                      cudaStream_t s) {
+  return launch_impl<true>(tmX64, tmX64, tmX16, p, s);  // the W map is unused
+}
+
+int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,
+                   __half* scales_t, cudaStream_t s) {
+  const int m_tiles = (N + kBM - 1) / kBM;
+  k_tile_q8<<<m_tiles * (Kp / kBK), kBM, 0, s>>>(codes, scales, N, Kp, codes_t, scales_t);
   return 1;
 }
 

@@ -309,3 +309,25 @@ def test_mistral_shape_long_ragged_context_parity(mistral_l2):
         assert k2.shape[0] == 2103
     finally:
         fs.fs_destroy(h)
+
+
+def test_smollm2_q8_tensor_core_path_batch_invariance(smol_l2):
+    """Q8_0 weights on the tensor-core path: a lane's logits do not change
+    bits with the batch it runs in (B = 1, 5, 40)."""
+    cfg, Wb, m = smol_l2
+    Wq = U.quantize_weights(Wb)
+    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=40, max_pos=32)
+    try:
+        assert fs.fs_gemm_path(h) == "tcgen05-q8_0"
+        seq = [int(t) for t in synth.make_prompts(1, 6, cfg["V"], seed=15)[0]]
+        base = U.gpu_teacher_forced(h, cfg, [7], [seq], cfg["V"])[0]
+        for B in (5, 40):
+            for k in range(40):
+                fs.fs_lane_reset(h, k)
+            others = synth.make_prompts(B - 1, 6, cfg["V"], seed=200 + B)
+            where = B - 1
+            seqs = others[:where] + [seq]
+            got = U.gpu_teacher_forced(h, cfg, list(range(B)), seqs, cfg["V"])[where]
+            assert np.array_equal(base.view(np.uint32), got.view(np.uint32)), B
+    finally:
+        fs.fs_destroy(h)
