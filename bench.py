@@ -114,11 +114,37 @@ def model_cfg(name):
     return {"S": synth.MODEL_S, "M": synth.MODEL_M, "T": synth.MODEL_T}[name]
 
 
+def device_weights(cfg, seed=1):
+    """Random-init bf16 weights N(0, 0.02) drawn on the device (seeded torch
+    generator): for the 7B shape, where host draws would dominate the run.
+    The timing does not depend on the values."""
+    import torch
+    from continuous_transformer_decode_gb300 import synth
+    g = torch.Generator(device="cuda").manual_seed(seed)
+
+    def mat(rows, cols):
+        return (torch.randn(rows, cols, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    d, V = cfg["d"], cfg["V"]
+    shapes = synth.matrix_shapes(cfg)
+    ones = torch.ones(d, dtype=torch.float32, device="cuda")
+    W = {"embed": mat(V, d), "lm_head": None if cfg["tied"] else mat(V, d),
+         "final_norm": ones, "layers": []}
+    for _ in range(cfg["L"]):
+        ly = {k: mat(*shapes[k]) for k in synth.LAYER_KEYS[:7]}
+        ly["attn_norm"] = ones
+        ly["ffn_norm"] = ones
+        W["layers"].append(ly)
+    return W
+
+
 def gpu_weights(cfg, wdtype, seed=1):
-    """Random-init weights. bf16: N(0, 0.02) drawn on the host (seeded);
-    q8_0: the same bf16 values quantised on the device by the library."""
+    """Random-init weights. bf16: N(0, 0.02) drawn on the host (seeded), or
+    on the device for the 7B shape; q8_0: the same bf16 values quantised on
+    the device by the library."""
     import torch
     from continuous_transformer_decode_gb300 import fs, synth
+    if cfg["d"] >= 4096 and wdtype == "bf16":
+        return device_weights(cfg, seed), fs.FS_DTYPE_BF16
     W = synth.make_weights(cfg, seed=seed, fmt="bf16")
     if wdtype == "bf16":
         return W, fs.FS_DTYPE_BF16
@@ -141,6 +167,8 @@ def run_ours(args, wl, ws, rank, local):
     build.build()
     torch.cuda.set_device(local)
     cfg = model_cfg(wl["model"])
+    if args.layers:
+        cfg = synth.with_layers(cfg, args.layers)
     B = args.batch or wl["B"]
     K, Wm = args.steps, args.warmup
     prompt = wl.get("prompt", 0)
@@ -334,6 +362,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="smollm2-135m-bf16", choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only the first L layers (same per-layer shapes; for "
+                         "small profiling captures, never for a reported number)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
@@ -391,6 +422,7 @@ def main():
                          "streamed per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+        **({"reduced_layers_for_profiling": args.layers} if args.layers else {}),
         "clocks": r["clocks"], "gpu_launches": r["launches"],
     }
     print(json.dumps(line))

@@ -119,6 +119,8 @@ struct fs_handle {
   float* part_acc = nullptr;
   int* attn_counters = nullptr;  // [max_lanes * Hkv], zero between steps
   bool attn_fused = false;
+  bool attn_tiled = false;
+  bool attn_mma = false;
 
   int32_t* d_args = nullptr;  // [7 * max_lanes + 1]
   int32_t* h_args = nullptr;  // pinned staging
@@ -286,6 +288,7 @@ int validate_desc(const fs_model_desc* d, std::string* why) {
   if (d->max_lanes < 1 || d->page_size < 1 || d->n_pages < 1 || d->max_pos < 1)
     return bad("max_lanes, page_size, n_pages and max_pos must be positive");
   if (!(d->rms_eps >= 0.0f) || !(d->rope_theta > 0.0)) return bad("bad rms_eps or rope_theta");
+  if (d->d_model > 8192) return bad("d_model above 8192 is not supported");
   return FS_OK;
 }
 
@@ -301,6 +304,11 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   h->Kp_d = (int)round_up(d.d_model, 64);
   h->Kp_q = (int)round_up(h->Nq, 64);
   h->Kp_f = (int)round_up(d.d_ffn, 64);
+  // attention split length: a handle constant (it fixes the merge order);
+  // handles batching many lanes amortise each block over longer splits
+  h->split_len = attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
+                     ? (d.max_lanes >= 64 ? 512 : 128)
+                     : 256;
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;
   {
@@ -448,6 +456,14 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   if (!ok) return h->fail(FS_ERR_OOM, "scratch allocation failed");
   FS_CK(h, cudaMemset(h->attn_counters, 0, (size_t)B * d.n_kv_heads * 4));
   h->attn_fused = attn_fused_supports(d.head_dim, h->G);
+  {
+    const char* e = getenv("FS_ATTN");
+    const bool force_fused = e && std::string(e) == "fused";
+    const bool force_tiled = e && std::string(e) == "tiled";
+    h->attn_tiled = !force_fused && attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
+    h->attn_mma = !force_fused && !force_tiled &&
+                  attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len);
+  }
   FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
   FS_CK(h, cudaMemset(h->apanel, 0, (size_t)B * h->Kp_f * xs));
@@ -621,7 +637,19 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                             h->hpanel, h->xtype, h->Kp_d, s);
     });
     gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
-    if (h->attn_fused) {
+    if (h->attn_tiled) {
+      AttnParams ap{};
+      ap.qkv = h->qkv; ap.H = d.n_heads; ap.rc = h->rope_cos; ap.rs = h->rope_sin;
+      ap.args = args; ap.kv = h->kv; ap.layer = l; ap.split_len = h->split_len;
+      ap.max_splits = h->max_splits; ap.part_ml = h->part_ml; ap.part_acc = h->part_acc;
+      ap.counters = h->attn_counters; ap.o = h->opanel; ap.ld_o = h->Kp_q; ap.err = h->d_err_flag;
+      h->launch(FS_PROF_ATTN,
+                kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs),
+                [&] {
+                  return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
+                                     : launch_attention_tiled(ap, n, h->xtype, s);
+                });
+    } else if (h->attn_fused) {
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
                   return launch_attention_fused(h->qkv, n, d.n_heads, h->rope_cos,

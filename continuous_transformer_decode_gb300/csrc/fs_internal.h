@@ -8,7 +8,43 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace fsk {
+
+// Programmatic dependent launch: a kernel waits for its predecessor in the
+// stream (griddepcontrol.wait) before touching memory the predecessor may
+// write or read, and immediately allows its successor to be scheduled, so
+// a successor's launch and prologue overlap this kernel's tail. Without the
+// launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() {
+#if defined(__CUDA_ARCH__)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#if defined(__CUDA_ARCH__)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+bool pdl_enabled();  // FS_PDL=0 in the environment turns the attribute off
+
+// Kernel launch with the programmatic-stream-serialization attribute.
+template <typename... K, typename... A>
+inline cudaError_t launch_k(void (*kern)(K...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<K>(args)...);
+}
 
 enum WType { W_F32 = 0, W_BF16 = 1, W_Q8 = 2 };
 enum XType { X_F32 = 0, X_BF16 = 1 };
@@ -118,6 +154,28 @@ int launch_attention(const float* q, int B, int H, const StepArgs& args,
                      const KV& kv, int layer, int max_splits, int split_len,
                      float* part_ml, float* part_acc, void* o_panel,
                      int x_type, int ld_o, cudaStream_t s);
+// Arguments of the tiled attention kernel (k_attn_tiled.cu).
+struct AttnParams {
+  const float* qkv;  // [B][(H + 2 Hkv) hd] projection output
+  int H;
+  const float* rc;   // RoPE cos [max_pos][hd/2]
+  const float* rs;   // RoPE sin
+  StepArgs args;
+  KV kv;
+  int layer;
+  int split_len, max_splits;
+  float* part_ml;    // [B][max_splits][H][2]
+  float* part_acc;   // [B][max_splits][H][hd]
+  int* counters;     // [B][Hkv]
+  void* o;           // output panel
+  int ld_o;
+  int* err;          // device-visible error flag
+};
+bool attn_tiled_supports(int hd, int G, int page_size, int split_len);
+bool attn_mma_supports(int hd, int G, int kv_f32, int split_len);
+int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s);
+int launch_attention_tiled(const AttnParams& a, int B, int x_type, cudaStream_t s);
+
 // RoPE + KV append + split-K attention (+ ordered merge) in one kernel.
 bool attn_fused_supports(int hd, int G);
 int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos,

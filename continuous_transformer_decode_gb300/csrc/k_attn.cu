@@ -50,6 +50,8 @@ __global__ void k_rope_append(const float* __restrict__ qkv, int H, int Hkv,
                               int hd, const float* __restrict__ rc,
                               const float* __restrict__ rs, StepArgs args,
                               KV kv, int layer, float* __restrict__ q_out) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int lane = args.lane[b];
   const int pos = args.pos[b];
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kCh)
     k_attn_partial(const float* __restrict__ q, int H, StepArgs args, KV kv,
                    int layer, int split_len, int max_splits,
                    float* __restrict__ part_ml, float* __restrict__ part_acc) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int len = args.pos[b] + 1;
   const int start = s * split_len;
@@ -200,6 +204,8 @@ __global__ void k_attn_combine(int H, int hd, StepArgs args, int split_len,
                                int max_splits, const float* __restrict__ part_ml,
                                const float* __restrict__ part_acc, OT* o,
                                int ld_o) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int len = args.pos[b] + 1;
   const int ns = (len + split_len - 1) / split_len;
@@ -227,10 +233,10 @@ int launch_rope_append(const float* qkv, int B, int H, int Hkv, int hd,
                        float* q_out, cudaStream_t s) {
   if (B <= 0) return 0;
   if (kv.kv_f32)
-    k_rope_append<float><<<B, 256, 0, s>>>(qkv, H, Hkv, hd, rope_cos, rope_sin,
+    launch_k(k_rope_append<float>, B, 256, 0, s, qkv, H, Hkv, hd, rope_cos, rope_sin,
                                            args, kv, layer, q_out);
   else
-    k_rope_append<__nv_bfloat16><<<B, 256, 0, s>>>(
+    launch_k(k_rope_append<__nv_bfloat16>, B, 256, 0, s, 
         qkv, H, Hkv, hd, rope_cos, rope_sin, args, kv, layer, q_out);
   return 1;
 }
@@ -242,18 +248,18 @@ int launch_attention(const float* q, int B, int H, const StepArgs& args,
   if (B <= 0) return 0;
   dim3 grid(max_splits, kv.Hkv, B);
   if (kv.kv_f32)
-    k_attn_partial<float><<<grid, kCh, 0, s>>>(q, H, args, kv, layer,
+    launch_k(k_attn_partial<float>, grid, kCh, 0, s, q, H, args, kv, layer,
                                                split_len, max_splits, part_ml,
                                                part_acc);
   else
-    k_attn_partial<__nv_bfloat16><<<grid, kCh, 0, s>>>(
+    launch_k(k_attn_partial<__nv_bfloat16>, grid, kCh, 0, s, 
         q, H, args, kv, layer, split_len, max_splits, part_ml, part_acc);
   if (x_type == X_BF16)
-    k_attn_combine<__nv_bfloat16><<<B, 256, 0, s>>>(
+    launch_k(k_attn_combine<__nv_bfloat16>, B, 256, 0, s, 
         H, kv.hd, args, split_len, max_splits, part_ml, part_acc,
         static_cast<__nv_bfloat16*>(o_panel), ld_o);
   else
-    k_attn_combine<float><<<B, 256, 0, s>>>(H, kv.hd, args, split_len,
+    launch_k(k_attn_combine<float>, B, 256, 0, s, H, kv.hd, args, split_len,
                                             max_splits, part_ml, part_acc,
                                             static_cast<float*>(o_panel), ld_o);
   return 2;

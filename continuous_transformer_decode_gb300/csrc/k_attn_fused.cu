@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kT)
                  int split_len, int max_splits, float* __restrict__ part_ml,
                  float* __restrict__ part_acc, int* __restrict__ counters, OT* o_panel,
                  int ld_o) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kHalf = HD / 2;
   constexpr int kVec = KVIO<KVT>::kVec;
   constexpr int kOut = (kG * HD + kT - 1) / kT;  // outputs per thread (max)
@@ -281,7 +283,7 @@ int dispatch_hd(int hd, dim3 grid, cudaStream_t s, const float* qkv, int H, cons
                 int ld_o) {
 #define FS_ATTN_CASE(D)                                                                  \
   case D:                                                                                \
-    k_attn_fused<KVT, OT, D><<<grid, kT, 0, s>>>(qkv, H, rc, rs, args, kv, layer,        \
+    launch_k(k_attn_fused<KVT, OT, D>, grid, kT, 0, s, qkv, H, rc, rs, args, kv, layer,        \
                                                  split_len, max_splits, part_ml,         \
                                                  part_acc, counters, o, ld_o);            \
     return 1;

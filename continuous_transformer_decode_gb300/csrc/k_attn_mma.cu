@@ -1,0 +1,396 @@
+// Per-lane GQA decode attention over paged bf16 KV with warp-level MMA.
+//
+// Computes what k_attn_tiled computes (RoPE of q and k at the lane's own
+// position, append of k and v there, online-softmax attention of the lane's
+// G query heads of one KV head over the lane's own keys 0..pos, split-K with
+// an ordered merge; "MODEL-BATCHING-RESULTS", "The lever"; mlx-bun "Parallel
+// slots", "KV memory" rung 3; "S1b decode: design traps" trap 2), with the
+// two inner products on tensor cores so the kernel is limited by the KV
+// stream rather than by instruction issue:
+//   * a block = (split s, KV head g, panel row b), 4 warps; the split is
+//     walked in tiles of 64 positions, K and V copied by cp.async into
+//     XOR-swizzled shared memory (double-buffered), rows past the lane's
+//     length zero-filled;
+//   * warp w owns positions 16w .. 16w+15 of every tile: S = Q Kᵀ with
+//     mma.m16n8k16 (bf16 in, f32 accumulate; the G heads are rows 0..G-1 of
+//     the 16-row A operand), a per-warp online softmax, then O += P V with
+//     the probabilities re-packed from the S accumulators into A fragments;
+//     q and P are f32 values split as hi + lo bf16 pairs (two MMAs each),
+//     so the products with the exact bf16 K and V keep near-f32 accuracy;
+//   * the 4 warps' (m, l, O) are merged in warp order, then the splits in
+//     split order, so a lane's result does not depend on the batch.
+
+#include <math_constants.h>
+
+#include "fs_internal.h"
+
+namespace fsk {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kT = 32 * kWarps;
+constexpr int kTT = 64;      // positions per tile
+constexpr int kG = 8;        // max query heads per KV head
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D += A(16x16, rows = heads) * B(16x8); A1 = A3 = 0 (rows 8..15 unused).
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// (lo, hi) f32 pair -> bf16 pair "hi" and the bf16 pair of the remainders.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16(x0 - hf.x, x1 - hf.y);
+}
+__device__ __forceinline__ void st_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+// byte offset of (row, 16-byte chunk) in a swizzled [kTT][HD] bf16 tile
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * (HD * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+template <typename OT, int HD>
+__global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kHalf = HD / 2;
+  constexpr int kCh = HD / 8;            // 16-byte chunks per row
+  constexpr int kTileBytes = kTT * HD * 2;
+  constexpr int kKs = HD / 16;           // k-steps of Q Kᵀ
+  constexpr int kNt = HD / 8;            // n-tiles of P V
+  const KV& kv = a.kv;
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int pos = a.args.pos[b];
+  const int len = pos + 1;
+  const int start = s * a.split_len;
+  if (start >= len) return;
+  const int end = min(len, start + a.split_len);
+  const int ns = (len + a.split_len - 1) / a.split_len;
+  const int H = a.H, Hkv = kv.Hkv, G = H / Hkv, ps = kv.page_size;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, cq = lane & 3;  // fragment row (head) and column pair
+  const int32_t* ptrow = kv.pt + (int64_t)a.args.lane[b] * kv.max_pages;
+  __nv_bfloat16* Kg = static_cast<__nv_bfloat16*>(kv.k);
+  __nv_bfloat16* Vg = static_cast<__nv_bfloat16*>(kv.v);
+  const bool owns_pos = (s == ns - 1);
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* Kt = smem;                                       // [2] swizzled tiles
+  uint8_t* Vt = smem + 2 * kTileBytes;
+  float* qs = reinterpret_cast<float*>(smem + 4 * kTileBytes);  // [kG][HD]
+  float* knew = qs + kG * HD;                               // [HD]
+  float* vnew = knew + HD;
+  float* wm = vnew + HD;                                    // [kWarps][kG]
+  float* wl = wm + kWarps * kG;
+  float* wo = reinterpret_cast<float*>(smem);  // [kWarps][kG][HD], reuses the idle tiles
+  __shared__ int s_last;
+
+  const int n_tiles = (end - start + kTT - 1) / kTT;
+  // all threads: copy tile i (valid rows by cp.async, the rest zero) to buffer i % 2
+  auto issue = [&](int i) {
+    const int t0 = start + i * kTT;
+    const int cnt = min(kTT, end - t0);
+    uint8_t* kd = Kt + (i & 1) * kTileBytes;
+    uint8_t* vd = Vt + (i & 1) * kTileBytes;
+    for (int idx = tid; idx < kTT * kCh; idx += kT) {
+      const int r = idx / kCh, ch = idx - r * kCh;
+      const uint32_t o = swz<HD>(r, ch);
+      if (r < cnt) {
+        const int t = t0 + r, pi = t / ps, slot = t - pi * ps;
+        const int64_t off = (int64_t)a.layer * kv.layer_stride +
+                            (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD + ch * 8;
+        cp_async16(smem_u32(kd + o), Kg + off);
+        cp_async16(smem_u32(vd + o), Vg + off);
+      } else {
+        *reinterpret_cast<uint4*>(kd + o) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vd + o) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_commit();
+  };
+  issue(0);  // the KV fetch starts before the query work
+  if (n_tiles > 1) issue(1);
+
+  // ---- rotated queries; the owner of pos also rotates k and appends k, v
+  const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
+  const float* c = a.rc + (int64_t)pos * kHalf;
+  const float* sn = a.rs + (int64_t)pos * kHalf;
+  for (int idx = tid; idx < kG * kHalf; idx += kT) {
+    const int h = idx / kHalf, i = idx - h * kHalf;
+    float q0 = 0.0f, q1 = 0.0f;
+    if (h < G) {
+      const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
+      q0 = x0 * c[i] - x1 * sn[i];
+      q1 = x1 * c[i] + x0 * sn[i];
+    }
+    qs[h * HD + i] = q0;
+    qs[h * HD + i + kHalf] = q1;
+  }
+  if (owns_pos) {
+    const float* kr = row + H * HD + g * HD;
+    const float* vr = row + (H + Hkv) * HD + g * HD;
+    const int pi = pos / ps, slot = pos - pi * ps;
+    const int64_t off = (int64_t)a.layer * kv.layer_stride +
+                        (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
+    for (int i = tid; i < kHalf; i += kT) {
+      const float x0 = kr[i], x1 = kr[i + kHalf];
+      const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
+      Kg[off + i] = __float2bfloat16_rn(k0);
+      Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
+      knew[i] = k0;
+      knew[i + kHalf] = k1;
+    }
+    for (int i = tid; i < HD; i += kT) {
+      Vg[off + i] = __float2bfloat16_rn(vr[i]);
+      vnew[i] = vr[i];
+    }
+  }
+  __syncthreads();
+
+  // Q as bf16 A fragments (rows = heads; rows >= G are zero), hi + lo parts
+  uint32_t qa[kKs][2], ql[kKs][2];
+#pragma unroll
+  for (int ks = 0; ks < kKs; ++ks) {
+    const int c0 = ks * 16 + 2 * cq;
+    const float* q = qs + gq * HD;
+    split_bf16(q[c0], q[c0 + 1], qa[ks][0], ql[ks][0]);
+    split_bf16(q[c0 + 8], q[c0 + 9], qa[ks][1], ql[ks][1]);
+  }
+
+
+  const float scale = 1.0f / sqrtf((float)HD);
+  float m_run = -CUDART_INF_F, l_run = 0.0f;  // head gq, this warp's positions
+  float o_acc[kNt][4];
+#pragma unroll
+  for (int j = 0; j < kNt; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.0f;
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const int t0 = start + i * kTT;
+    const int cnt = min(kTT, end - t0);
+    if (i + 1 < n_tiles)
+      cp_wait<1>();
+    else
+      cp_wait<0>();
+    uint8_t* kb = Kt + (i & 1) * kTileBytes;
+    uint8_t* vb = Vt + (i & 1) * kTileBytes;
+    __syncthreads();
+    if (owns_pos && pos >= t0 && pos < t0 + kTT) {  // the appended token, from registers
+      const int r = pos - t0;
+      for (int ch = tid; ch < kCh; ch += kT) {
+        uint4 kk, vv;
+        uint32_t* kw = reinterpret_cast<uint32_t*>(&kk);
+        uint32_t* vw = reinterpret_cast<uint32_t*>(&vv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kw[e] = pack_bf16(knew[ch * 8 + 2 * e], knew[ch * 8 + 2 * e + 1]);
+          vw[e] = pack_bf16(vnew[ch * 8 + 2 * e], vnew[ch * 8 + 2 * e + 1]);
+        }
+        *reinterpret_cast<uint4*>(kb + swz<HD>(r, ch)) = kk;
+        *reinterpret_cast<uint4*>(vb + swz<HD>(r, ch)) = vv;
+      }
+      __syncthreads();
+    }
+    const int p0 = warp * 16;  // this warp's first position in the tile
+    if (p0 < cnt) {
+      // S = Q Kᵀ for positions p0 .. p0+15 (two n-tiles of 8)
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+      for (int ks = 0; ks < kKs; ++ks) {
+        uint32_t bk[4];
+        const int rr = p0 + (mi >> 1) * 8 + ri, ch = 2 * ks + (mi & 1);
+        ldsm_x4(smem_u32(kb + swz<HD>(rr, ch)), bk);
+        mma16816(sacc[0], qa[ks][0], qa[ks][1], bk[0], bk[1]);
+        mma16816(sacc[1], qa[ks][0], qa[ks][1], bk[2], bk[3]);
+        mma16816(sacc[0], ql[ks][0], ql[ks][1], bk[0], bk[1]);
+        mma16816(sacc[1], ql[ks][0], ql[ks][1], bk[2], bk[3]);
+      }
+      // online softmax over this warp's positions, per head (row gq)
+      float sv[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pp = p0 + nt * 8 + 2 * cq + e;
+          sv[nt * 2 + e] = pp < cnt ? sacc[nt][e] * scale : -CUDART_INF_F;
+        }
+      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mnew = fmaxf(m_run, mx);
+      const float alpha = (m_run == -CUDART_INF_F) ? 0.0f : expf(m_run - mnew);
+      float pv[4], psum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[e] = (sv[e] == -CUDART_INF_F) ? 0.0f : expf(sv[e] - mnew);
+        psum += pv[e];
+      }
+      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+      l_run = l_run * alpha + psum;
+      m_run = mnew;
+#pragma unroll
+      for (int j = 0; j < kNt; ++j) {
+        o_acc[j][0] *= alpha;
+        o_acc[j][1] *= alpha;
+      }
+      // O += P V; P's A fragment: positions 2cq..2cq+1 (n-tile 0) and +8
+      uint32_t pa0, pa2, pl0, pl2;
+      split_bf16(pv[0], pv[1], pa0, pl0);
+      split_bf16(pv[2], pv[3], pa2, pl2);
+#pragma unroll
+      for (int j = 0; j < kNt; j += 2) {
+        uint32_t bv[4];
+        const int rr = p0 + (mi & 1) * 8 + ri, ch = j + (mi >> 1);
+        ldsm_x4_t(smem_u32(vb + swz<HD>(rr, ch)), bv);
+        mma16816(o_acc[j], pa0, pa2, bv[0], bv[1]);
+        mma16816(o_acc[j + 1], pa0, pa2, bv[2], bv[3]);
+        mma16816(o_acc[j], pl0, pl2, bv[0], bv[1]);
+        mma16816(o_acc[j + 1], pl0, pl2, bv[2], bv[3]);
+      }
+    }
+    __syncthreads();  // buffer i % 2 is free
+    if (i + 2 < n_tiles) issue(i + 2);
+  }
+
+  // ---- merge the warps in warp order
+  if (cq == 0 && gq < kG) {
+    wm[warp * kG + gq] = m_run;
+    wl[warp * kG + gq] = l_run;
+  }
+  if (gq < G) {
+#pragma unroll
+    for (int j = 0; j < kNt; ++j) {
+      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq] = o_acc[j][0];
+      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq + 1] = o_acc[j][1];
+    }
+  }
+  __syncthreads();
+  OT* orow = static_cast<OT*>(a.o) + (int64_t)b * a.ld_o + g * G * HD;
+  const int64_t base = ((int64_t)b * a.max_splits + s) * H + g * G;
+  for (int o = tid; o < G * HD; o += kT) {
+    const int h = o / HD, d = o - h * HD;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kG + h]);
+    float L = 0.0f, A = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = wm[w * kG + h];
+      const float sc = (mw == -CUDART_INF_F) ? 0.0f : expf(mw - M);
+      L = fmaf(wl[w * kG + h], sc, L);
+      A = fmaf(wo[(w * kG + h) * HD + d], sc, A);
+    }
+    if (ns == 1) {
+      st_out(orow + o, A / L);
+    } else {
+      if (d == 0) {
+        a.part_ml[2 * (base + h)] = M;
+        a.part_ml[2 * (base + h) + 1] = L;
+      }
+      a.part_acc[base * HD + o] = A;
+    }
+  }
+  if (ns == 1) return;
+  // several splits: the last block of (b, g) merges them in split order
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int* ctr = a.counters + (int64_t)b * Hkv + g;
+    s_last = atomicAdd(ctr, 1) == ns - 1;
+    if (s_last) *ctr = 0;  // every split has arrived: ready for the next step
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int o = tid; o < G * HD; o += kT) {
+    const int h = o / HD;
+    float mx = -CUDART_INF_F;
+    for (int q = 0; q < ns; ++q)
+      mx = fmaxf(mx, __ldcg(a.part_ml + 2 * (((int64_t)b * a.max_splits + q) * H + g * G + h)));
+    float L = 0.0f, A = 0.0f;
+    for (int q = 0; q < ns; ++q) {
+      const int64_t bq = ((int64_t)b * a.max_splits + q) * H + g * G + h;
+      const float w = expf(__ldcg(a.part_ml + 2 * bq) - mx);
+      L = fmaf(__ldcg(a.part_ml + 2 * bq + 1), w, L);
+      A = fmaf(__ldcg(a.part_acc + bq * HD + (o - h * HD)), w, A);
+    }
+    st_out(orow + o, A / L);
+  }
+}
+
+template <typename OT, int HD>
+int launch_hd(const AttnParams& a, int B, cudaStream_t s) {
+  static_assert(kWarps * kG * HD * sizeof(float) <= 4 * (size_t)kTT * HD * 2,
+                "the warp-merge buffer must fit in the tile buffers");
+  const size_t smem =
+      4 * (size_t)kTT * HD * 2 + sizeof(float) * ((size_t)kG * HD + 2 * HD + 2 * kWarps * kG);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(k_attn_mma<OT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    attr = true;
+  }
+  dim3 grid(a.max_splits, a.kv.Hkv, B);
+  launch_k(k_attn_mma<OT, HD>, grid, kT, smem, s, a);
+  return 1;
+}
+
+template <typename OT>
+int dispatch(const AttnParams& a, int B, cudaStream_t s) {
+  switch (a.kv.hd) {
+    case 64: return launch_hd<OT, 64>(a, B, s);
+    case 128: return launch_hd<OT, 128>(a, B, s);
+    case 256: return launch_hd<OT, 256>(a, B, s);
+    default: return 0;
+  }
+}
+
+}  // namespace
+
+bool attn_mma_supports(int hd, int G, int kv_f32, int split_len) {
+  return !kv_f32 && (hd == 64 || hd == 128 || hd == 256) && G >= 1 && G <= kG &&
+         split_len % kTT == 0;
+}
+
+int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s) {
+  if (B <= 0) return 0;
+  return x_type == X_BF16 ? dispatch<__nv_bfloat16>(a, B, s) : dispatch<float>(a, B, s);
+}
+
+}  // namespace fsk

@@ -361,6 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_wait();     // the predecessor's outputs (our panel) are complete
+  pdl_trigger();  // let the successor launch and run its prologue meanwhile
 
   if (warp == 4) {
     if (lane == 0) {  // ---- TMA producer
@@ -571,7 +573,7 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
   TcParams p = p0;
   int smem = 0;
   p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, &p.stage_bytes, &smem);
-  k_gemm_tc<kQ8><<<p.m_tiles * p.splits * p.groups, kThreads, smem, s>>>(tmW, tmX64, tmX16, p);
+  launch_k(k_gemm_tc<kQ8>, p.m_tiles * p.splits * p.groups, kThreads, smem, s, tmW, tmX64, tmX16, p);
   return 1;
 }
 

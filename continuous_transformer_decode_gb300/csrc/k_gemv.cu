@@ -79,6 +79,8 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, t = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + warp;
   if (row >= a.n_out) return;
@@ -134,9 +136,9 @@ int launch_gemv(const GemmArgs& a, cudaStream_t s) {
   if (a.B <= 0) return 0;
   dim3 grid((a.n_out + kWarps - 1) / kWarps);
   if (a.epi == EPI_SWIGLU)
-    k_gemv<true><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_k(k_gemv<true>, grid, kWarps * 32, 0, s, a);
   else
-    k_gemv<false><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_k(k_gemv<false>, grid, kWarps * 32, 0, s, a);
   return 1;
 }
 
