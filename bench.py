@@ -109,6 +109,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(vals, world_size: int, device: str = "cpu"):
+    """Element-wise max of per-rank timings over the process group (the
+    slowest replica bounds the job); identity for a single process."""
+    if world_size <= 1:
+        return [float(v) for v in vals]
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_throughput(tokens_per_rank: int, ms_per_rank: float, world_size: int,
+                         device: str = "cpu") -> float:
+    """Whole-job tokens/s of replicas: all ranks' tokens over the slowest
+    rank's time."""
+    (ms,) = max_over_ranks([ms_per_rank], world_size, device)
+    return tokens_per_rank * world_size / (ms / 1e3)
+
+
 def model_cfg(name):
     from continuous_transformer_decode_gb300 import synth
     return {"S": synth.MODEL_S, "M": synth.MODEL_M, "T": synth.MODEL_T}[name]
@@ -255,13 +274,37 @@ def run_ours(args, wl, ws, rank, local):
         htoks = fs.fs_sample(h, temps_h, seeds_h, np.full(B, i, np.uint64))
     tk.synchronize()
     e2e_s = time.perf_counter() - t0
+
+    # ---- B sweep on the same handle (device-timed, like `value`)
+    sweep = []
+    if not args.no_sweep and "ctx" not in wl:
+        for Bs in [b for b in (1, 4, 16, 64, 256, 512, 960) if b <= B]:
+            for k in range(B):
+                fs.fs_lane_reset(h, k)
+            ls = np.arange(Bs, dtype=np.int32)
+            ps_ = np.zeros(Bs, dtype=np.int32)
+            for t in range(prompt):
+                fs.fs_decode_step_batch(h, ls, ps_, prompts[:Bs, t])
+            tk_ = prompts[:Bs, -1].astype(np.int32).copy()
+            for _ in range(2):
+                fs.fs_decode_step_batch(h, ls, ps_, tk_)
+                fs.fs_sample_device(h, temps[:Bs], seeds[:Bs], ctrs[:Bs], dtok[:Bs])
+            torch.cuda.synchronize()
+            k_sw = 6
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(k_sw):
+                fs.fs_decode_step_batch(h, ls, ps_, tk_)
+                fs.fs_sample_device(h, temps[:Bs], seeds[:Bs], ctrs[:Bs], dtok[:Bs])
+            a1.record(stream)
+            torch.cuda.synchronize()
+            ms_sw = a0.elapsed_time(a1) / k_sw
+            sweep.append({"lanes": Bs, "ms_per_step": ms_sw, "tok_s": Bs / (ms_sw / 1e3),
+                          "positions": f"{prompt + 2}..{prompt + 2 + k_sw}"})
     fs.fs_destroy(h)
 
     # ---- aggregate over ranks (max time)
-    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms, e2e_s = float(t[0]), float(t[1])
+    ms, e2e_s = max_over_ranks([ms, e2e_s], ws, "cuda")
     total_tokens = B * K * ws
     value = total_tokens / (ms / 1e3)
     peaks = _peaks()
@@ -280,7 +323,39 @@ def run_ours(args, wl, ws, rank, local):
            "h2d_bytes_per_step": arg_bytes + B * (4 + 8 + 8),
            "d2h_bytes_per_step": B * 4}
     return dict(value=value, ms=ms, B=B, launches=launches, clocks=clk, roofline=roof,
-                e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt)
+                e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt, sweep=sweep)
+
+
+def step_roofline(cfg, wbytes_per_param, lanes, ctx_mean, peaks):
+    """Whole-step ceiling min(B*BW/bytes_step, P_tc/flops_token): weights
+    once per step, each lane's KV read plus its append (logits stay on the
+    device and are not counted); flops = 2 * streamed params + attention."""
+    L, Hkv, hd, H = cfg["L"], cfg["Hkv"], cfg["hd"], cfg["H"]
+    n_par = cfg["V"] * cfg["d"] * (1 if cfg["tied"] else 2) + L * (
+        (H * hd * 2 + Hkv * hd * 2) * cfg["d"] + 3 * cfg["F"] * cfg["d"])
+    w_bytes = n_par * wbytes_per_param
+    kv_tok = 2 * L * Hkv * hd * 2
+    bytes_step = w_bytes + lanes * (ctx_mean + 1) * kv_tok
+    flops_tok = 2 * n_par + 4 * H * hd * (ctx_mean + 1) * L
+    hbm = lanes * peaks["hbm"] * 1e9 / bytes_step
+    tc = (peaks["bf16_sus"] or peaks["bf16"]) * 1e12 / flops_tok
+    return {"tok_s_ceiling": min(hbm, tc), "bound": "hbm" if hbm < tc else "tensor",
+            "bytes_per_step": bytes_step, "flops_per_token": flops_tok}
+
+
+def traffic_for(kernel_src: str, workload: str, lanes: int):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(f"{workload}@{lanes}")
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "continuous_transformer_decode_gb300", "csrc", kernel_src)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec["dram_bytes_per_launch"] if rec.get("source_sha256") == digest else None
 
 
 def fs_path_name(cfg, wdt):
@@ -366,6 +441,7 @@ def main():
                     help="use only the first L layers (same per-layer shapes; for "
                          "small profiling captures, never for a reported number)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
     ws, rank, local = _dist()
@@ -408,6 +484,9 @@ def main():
     n_par = cfg["V"] * cfg["d"] * (1 if cfg["tied"] else 2) + cfg["L"] * (
         (cfg["H"] * cfg["hd"] * 2 + cfg["Hkv"] * cfg["hd"] * 2) * cfg["d"] + 3 * cfg["F"] * cfg["d"])
     weight_mb = n_par * wbytes / 1e6
+    peaks = _peaks()
+    ctx_mean = float(np.mean(r["ctx"])) + args.warmup + args.steps / 2.0
+    sr = step_roofline(cfg, wbytes, r["B"], ctx_mean, peaks)
     line = {
         "metric": METRIC, "value": r["value"], "unit": "tok/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
@@ -421,7 +500,11 @@ def main():
                    "l2": f"no flush: inputs larger than L2 ({weight_mb:.0f} MB of weights "
                          "streamed per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": r["roofline"], "cpu_baseline": cb, "e2e": r["e2e"],
+        "roofline": dict(r["roofline"], traffic=traffic_for("k_gemm_tc.cu", args.workload, r["B"])),
+        "step_roofline": dict(sr, frac=r["value"] / ws / sr["tok_s_ceiling"], peak_source=peaks["src"]),
+        "sweep": [dict(p, frac_of_step_roofline=p["tok_s"] / step_roofline(
+            cfg, wbytes, p["lanes"], 17 + 3, peaks)["tok_s_ceiling"]) for p in r["sweep"]],
+        "cpu_baseline": cb, "e2e": r["e2e"],
         **({"reduced_layers_for_profiling": args.layers} if args.layers else {}),
         "clocks": r["clocks"], "gpu_launches": r["launches"],
     }
