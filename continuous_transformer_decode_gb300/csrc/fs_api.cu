@@ -288,7 +288,7 @@ int validate_desc(const fs_model_desc* d, std::string* why) {
   if (d->max_lanes < 1 || d->page_size < 1 || d->n_pages < 1 || d->max_pos < 1)
     return bad("max_lanes, page_size, n_pages and max_pos must be positive");
   if (!(d->rms_eps >= 0.0f) || !(d->rope_theta > 0.0)) return bad("bad rms_eps or rope_theta");
-  if (d->d_model > 8192) return bad("d_model above 8192 is not supported");
+  if (d->d_model > 8192 || d->d_model % 4) return bad("d_model must be a multiple of 4, <= 8192");
   return FS_OK;
 }
 
@@ -526,6 +526,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         h->alloc(&h->counters, n_counters * 4) != cudaSuccess)
       return h->fail(FS_ERR_OOM, "GEMM workspace allocation failed");
     FS_CK(h, cudaMemset(h->counters, 0, n_counters * 4));
+
   }
   FS_CK(h, cudaHostAlloc((void**)&h->h_samp, (size_t)B * 24, cudaHostAllocDefault));
   int32_t* a = h->d_args;
@@ -626,16 +627,19 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
     else
       h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc(T.tm, tmX64, tmX, p, s); });
   };
-  const double norm_bytes = (double)n * d.d_model * (4.0 + xs);
-  h->launch(FS_PROF_OTHER, (double)n * d.d_model * 4.0 * 2, [&] {
-    return launch_embed(h->embed, args, n, n, h->kv, h->x, d.d_model, s);
+  const double norm_bytes = (double)n * d.d_model * (4.0 * 3 + xs);
+  // embedding gather + the first layer's input norm
+  h->launch(FS_PROF_OTHER, (double)n * d.d_model * (4.0 * 2 + xs), [&] {
+    return launch_embed(h->embed, args, n, h->kv, h->x, d.d_model, h->layers[0].g_attn,
+                        d.rms_eps, h->hpanel, h->xtype, h->Kp_d, s);
   });
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& W = h->layers[l];
-    h->launch(FS_PROF_OTHER, norm_bytes + (l ? 3.0 * n * d.d_model * 4 : 0.0), [&] {
-      return launch_rmsnorm(h->x, l ? h->y : nullptr, W.g_attn, n, d.d_model, d.rms_eps,
-                            h->hpanel, h->xtype, h->Kp_d, s);
-    });
+    if (l > 0)
+      h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+        return launch_rmsnorm(h->x, h->y, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel,
+                              h->xtype, h->Kp_d, s);
+      });
     gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
     if (h->attn_tiled) {
       AttnParams ap{};
@@ -671,19 +675,21 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                                 h->Kp_q, s);
       });
     }
-    gemm(W.o, W.o_tc, h->tm_o, h->tm_o64, h->opanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
-    h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
-      return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                            h->Kp_d, s);
-    });
+    gemm(W.o, W.o_tc, h->tm_o, h->tm_o64, h->opanel, EPI_STORE, h->y, nullptr, d.d_model,
+         d.d_model);
+    h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+        return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel,
+                              h->xtype, h->Kp_d, s);
+      });
     gemm(W.gateup, W.gateup_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
          d.d_ffn);
-    gemm(W.down, W.down_tc, h->tm_a, h->tm_a64, h->apanel, EPI_STORE, h->y, nullptr, d.d_model, d.d_model);
+    gemm(W.down, W.down_tc, h->tm_a, h->tm_a64, h->apanel, EPI_STORE, h->y, nullptr, d.d_model,
+         d.d_model);
   }
-  h->launch(FS_PROF_OTHER, norm_bytes + 3.0 * n * d.d_model * 4, [&] {
-    return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                          h->Kp_d, s);
-  });
+  h->launch(FS_PROF_OTHER, norm_bytes, [&] {
+      return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
+                            h->Kp_d, s);
+    });
   gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
 }
 

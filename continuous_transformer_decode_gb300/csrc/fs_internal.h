@@ -141,8 +141,9 @@ int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const 
 int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,
                    __half* scales_t, cudaStream_t s);
 
-int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
-                 const KV& kv, float* x, int d, cudaStream_t s);
+// x = E[tok]; if g is given also h = RMSNorm(x) * g (x_type panel).
+int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
+                 const float* g, float eps, void* h, int x_type, int ld_h, cudaStream_t s);
 // x += resid (if resid is given), out = RMSNorm(x) * g.
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
                    void* out, int x_type, int ld_out, cudaStream_t s);

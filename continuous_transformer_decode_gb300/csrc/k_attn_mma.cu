@@ -86,8 +86,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <typename OT, int HD>
 __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
-  pdl_wait();
-  pdl_trigger();
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
   constexpr int kTileBytes = kTT * HD * 2;
@@ -143,8 +141,14 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
     }
     cp_commit();
   };
-  issue(0);  // the KV fetch starts before the query work
+  // Programmatic dependent launch: the KV of earlier positions, the page
+  // table and the step arguments were written by kernels that finished before
+  // the predecessor started, so the first tiles are fetched before waiting
+  // for the predecessor (the QKV projection read below).
+  issue(0);
   if (n_tiles > 1) issue(1);
+  pdl_wait();
+  pdl_trigger();
 
   // ---- rotated queries; the owner of pos also rotates k and appends k, v
   const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;

@@ -361,23 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  pdl_wait();     // the predecessor's outputs (our panel) are complete
-  pdl_trigger();  // let the successor launch and run its prologue meanwhile
+  // Programmatic dependent launch: the weight tiles do not depend on the
+  // predecessor kernel, so the producer starts them before waiting for it;
+  // the panel loads and every other global access come after the wait.
+  if (!(warp == 4 && lane == 0)) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 4) {
     if (lane == 0) {  // ---- TMA producer
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
+      auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
         const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
-          atomicExch(p.err, 1);
-          s_abort = 1;
-          break;
-        }
-        if (*(volatile int*)&s_abort) break;
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const int x = (kb0 + i) * kBK;
         if (kQ8) {
           mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
           const int64_t tile = (int64_t)m_tile * p.kb_total + kb0 + i;
@@ -386,13 +383,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     full0 + 8 * s);
         } else {
           mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
-          tma_load_2d(st, &tmW, x, m_tile * kBM, full0 + 8 * s);
+          tma_load_2d(st, &tmW, (kb0 + i) * kBK, m_tile * kBM, full0 + 8 * s);
         }
+      };
+      auto load_x = [&](int i) {  // panel part of stage i
+        const int s = i % S;
+        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const int x = (kb0 + i) * kBK;
         int r = 0;
         for (; r + 64 <= n_tot; r += 64)
           tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
         for (; r < n_tot; r += kXBoxRows)
           tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
+      };
+      const int pre = min(S, nkb);  // stages are empty at start: no wait needed
+      for (int i = 0; i < pre; ++i) load_w(i);
+      pdl_wait();  // the panel is the predecessor's output
+      pdl_trigger();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      issued = pre;
+      for (int i = pre; i < nkb; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+          atomicExch(p.err, 1);
+          s_abort = 1;
+          break;
+        }
+        if (*(volatile int*)&s_abort) break;
+        load_w(i);
+        load_x(i);
         issued = i + 1;
       }
       // drain: every issued load must have landed before the block exits

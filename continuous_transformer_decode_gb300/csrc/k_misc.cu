@@ -6,6 +6,7 @@
 #include <cstdlib>
 
 #include "fs_internal.h"
+#include "norm_row.cuh"
 
 namespace fsk {
 namespace {
@@ -19,116 +20,47 @@ __device__ __forceinline__ float load_w(const Mat& E, int64_t row, int i) {
   return (float)static_cast<const int8_t*>(E.w)[row * E.Kp + i] * d;
 }
 
-// x[b] = E[tok[b]]; block b also applies page-table update b of the step.
-__global__ void k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x,
-                        int d) {
+// x[b] = E[tok[b]] and, when g is given, h[b] = RMSNorm(x[b]) * g (the first
+// layer's input norm); block b also applies page-table update b of the step.
+template <typename OT>
+__global__ void __launch_bounds__(kNormRowThreads)
+    k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x, int d, const float* g,
+            float eps, OT* __restrict__ h, int ld_h) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x;
-  if (threadIdx.x == 0 && b < *args.n_upd) {
+  __shared__ float red[4];
+  const int b = blockIdx.x, t = threadIdx.x;
+  if (t == 0 && b < *args.n_upd) {
     kv.pt[(int64_t)args.upd_lane[b] * kv.max_pages + args.upd_slot[b]] =
         args.upd_page[b];
   }
   const int64_t tok = args.tok[b];
-  for (int i = threadIdx.x; i < d; i += blockDim.x)
-    x[(int64_t)b * d + i] = load_w(E, tok, i);
+  float* xr = x + (int64_t)b * d;
+  // the same float4 chunks the norm routine gives this thread
+  for (int c = t; c < d / 4; c += kNormRowThreads) {
+    float4 v;
+    v.x = load_w(E, tok, 4 * c);
+    v.y = load_w(E, tok, 4 * c + 1);
+    v.z = load_w(E, tok, 4 * c + 2);
+    v.w = load_w(E, tok, 4 * c + 3);
+    *reinterpret_cast<float4*>(xr + 4 * c) = v;
+  }
+  if (g) norm_row_128<OT, 16>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red);
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  __syncthreads();
-  float r = red[0];
-  for (int i = 1; i < nw; ++i) r += red[i];
-  return r;
-}
 
-// Residual add then RMSNorm, one block per panel row: if r is given,
-// x += r (written back: the residual stream), then
-// out = x * (1 / sqrt(mean(x^2) + eps)) * g. Each thread first loads all of
-// its elements (up to kNormPer, 16-byte loads when d allows), so the loads
-// of a row are in flight together; the sum of squares is reduced in a fixed
-// order, independent of the batch.
-constexpr int kNormThreads = 256;
-constexpr int kNormPer = 32;  // elements per thread: d <= 8192
-
-template <typename OT, bool kVec>
-__global__ void __launch_bounds__(kNormThreads)
+// Residual add then RMSNorm, one block of 128 threads per panel row (see
+// norm_row.cuh for the arithmetic and its fixed reduction order).
+template <typename OT>
+__global__ void __launch_bounds__(kNormRowThreads)
     k_rmsnorm(float* __restrict__ x, const float* __restrict__ r,
               const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[32];
-  const int b = blockIdx.x, t = threadIdx.x;
-  float* xr = x + (int64_t)b * d;
-  const float* rr = r ? r + (int64_t)b * d : nullptr;
-  float v[kNormPer];
-  float ss = 0.0f;
-  if constexpr (kVec) {  // d % 4 == 0: element i of thread t is 4*(t + kNormThreads*(i/4)) + i%4
-#pragma unroll
-    for (int j = 0; j < kNormPer / 4; ++j) {
-      const int i0 = 4 * (t + kNormThreads * j);
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i0 < d) {
-        a = *reinterpret_cast<const float4*>(xr + i0);
-        if (rr) {
-          const float4 c = *reinterpret_cast<const float4*>(rr + i0);
-          a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
-        }
-      }
-      v[4 * j] = a.x; v[4 * j + 1] = a.y; v[4 * j + 2] = a.z; v[4 * j + 3] = a.w;
-    }
-#pragma unroll
-    for (int i = 0; i < kNormPer; ++i) ss = fmaf(v[i], v[i], ss);
-    ss = block_sum(ss, red);
-    const float rs = 1.0f / sqrtf(ss / (float)d + eps);
-#pragma unroll
-    for (int j = 0; j < kNormPer / 4; ++j) {
-      const int i0 = 4 * (t + kNormThreads * j);
-      if (i0 < d) {
-        if (rr) *reinterpret_cast<float4*>(xr + i0) =
-            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        const float4 gg = *reinterpret_cast<const float4*>(g + i0);
-        const float o0 = v[4 * j] * rs * gg.x, o1 = v[4 * j + 1] * rs * gg.y;
-        const float o2 = v[4 * j + 2] * rs * gg.z, o3 = v[4 * j + 3] * rs * gg.w;
-        if constexpr (sizeof(OT) == 2) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(out + (int64_t)b * ld_out + i0) = pk;
-        } else {
-          *reinterpret_cast<float4*>(out + (int64_t)b * ld_out + i0) = make_float4(o0, o1, o2, o3);
-        }
-      }
-    }
-  } else {
-  // scalar path (d % 4 != 0): element i of thread t is t + kNormThreads*i
-#pragma unroll
-  for (int i = 0; i < kNormPer; ++i) {
-    const int k = t + kNormThreads * i;
-    v[i] = k < d ? xr[k] + (rr ? rr[k] : 0.0f) : 0.0f;
-  }
-#pragma unroll
-  for (int i = 0; i < kNormPer; ++i) ss = fmaf(v[i], v[i], ss);
-  ss = block_sum(ss, red);
-  const float rs = 1.0f / sqrtf(ss / (float)d + eps);
-#pragma unroll
-  for (int i = 0; i < kNormPer; ++i) {
-    const int k = t + kNormThreads * i;
-    if (k < d) {
-      if (rr) xr[k] = v[i];
-      const float o = v[i] * rs * g[k];
-      if constexpr (sizeof(OT) == 2)
-        out[(int64_t)b * ld_out + k] = __float2bfloat16_rn(o);
-      else
-        out[(int64_t)b * ld_out + k] = o;
-    }
-  }
-  }
+  __shared__ float red[4];
+  const int b = blockIdx.x;
+  norm_row_128<OT, 16>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, g, d, eps,
+                       out + (int64_t)b * ld_out, threadIdx.x, 1, red);
 }
 
 // ---------------------------------------------------------------- sampler
@@ -391,34 +323,27 @@ bool pdl_enabled() {
   return on;
 }
 
-int launch_embed(const Mat& E, const StepArgs& args, int B, int n_upd_max,
-                 const KV& kv, float* x, int d, cudaStream_t s) {
-  (void)n_upd_max;
+int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
+                 const float* g, float eps, void* h, int x_type, int ld_h, cudaStream_t s) {
   if (B <= 0) return 0;
-  launch_k(k_embed, B, 256, 0, s, E, args, kv, x, d);
+  if (x_type == X_BF16)
+    launch_k(k_embed<__nv_bfloat16>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
+             static_cast<__nv_bfloat16*>(h), ld_h);
+  else
+    launch_k(k_embed<float>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
+             static_cast<float*>(h), ld_h);
   return 1;
 }
 
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
                    void* out, int x_type, int ld_out, cudaStream_t s) {
   if (B <= 0) return 0;
-  if (d > kNormThreads * kNormPer) return 0;  // rejected at fs_create
-  const bool vec = d % 4 == 0 && ld_out % 4 == 0;
-  if (x_type == X_BF16) {
-    auto* o = static_cast<__nv_bfloat16*>(out);
-    if (vec)
-      launch_k(k_rmsnorm<__nv_bfloat16, true>, B, kNormThreads, 0, s, x, resid, g, d, eps, o,
-               ld_out);
-    else
-      launch_k(k_rmsnorm<__nv_bfloat16, false>, B, kNormThreads, 0, s, x, resid, g, d, eps, o,
-               ld_out);
-  } else {
-    auto* o = static_cast<float*>(out);
-    if (vec)
-      launch_k(k_rmsnorm<float, true>, B, kNormThreads, 0, s, x, resid, g, d, eps, o, ld_out);
-    else
-      launch_k(k_rmsnorm<float, false>, B, kNormThreads, 0, s, x, resid, g, d, eps, o, ld_out);
-  }
+  if (x_type == X_BF16)
+    launch_k(k_rmsnorm<__nv_bfloat16>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
+             static_cast<__nv_bfloat16*>(out), ld_out);
+  else
+    launch_k(k_rmsnorm<float>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
+             static_cast<float*>(out), ld_out);
   return 1;
 }
 
