@@ -462,7 +462,8 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     const bool force_tiled = e && std::string(e) == "tiled";
     h->attn_tiled = !force_fused && attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
     h->attn_mma = !force_fused && !force_tiled &&
-                  attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len);
+                  attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len,
+                                    h->max_splits);
   }
   FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));

@@ -173,7 +173,7 @@ struct AttnParams {
   int* err;          // device-visible error flag
 };
 bool attn_tiled_supports(int hd, int G, int page_size, int split_len);
-bool attn_mma_supports(int hd, int G, int kv_f32, int split_len);
+bool attn_mma_supports(int hd, int G, int kv_f32, int split_len, int max_splits);
 int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s);
 int launch_attention_tiled(const AttnParams& a, int B, int x_type, cudaStream_t s);
 

@@ -15,8 +15,10 @@
 //     mma.m16n8k16 (bf16 in, f32 accumulate; the G heads are rows 0..G-1 of
 //     the 16-row A operand), a per-warp online softmax, then O += P V with
 //     the probabilities re-packed from the S accumulators into A fragments;
-//     q and P are f32 values split as hi + lo bf16 pairs (two MMAs each),
-//     so the products with the exact bf16 K and V keep near-f32 accuracy;
+//     q and P are f32 values split as hi + lo bf16 parts placed in rows g and
+//     g + 8 of the A operand, so one MMA yields both partial products (summed
+//     afterwards) and the products with the exact bf16 K and V keep
+//     near-f32 accuracy;
 //   * the 4 warps' (m, l, O) are merged in warp order, then the splits in
 //     split order, so a lane's result does not depend on the batch.
 
@@ -53,14 +55,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t r[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-// D += A(16x16, rows = heads) * B(16x8); A1 = A3 = 0 (rows 8..15 unused).
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a2, uint32_t b0,
+// D += A(16x16) * B(16x8): rows 0..7 of A hold the hi parts of the heads,
+// rows 8..15 the lo parts; D rows follow (d0, d1: hi; d2, d3: lo).
+__device__ __forceinline__ void mma16816(float d[4], const uint32_t a[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -85,7 +88,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 }
 
 template <typename OT, int HD>
-__global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
+__global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
   constexpr int kTileBytes = kTT * HD * 2;
@@ -186,14 +189,15 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
   }
   __syncthreads();
 
-  // Q as bf16 A fragments (rows = heads; rows >= G are zero), hi + lo parts
-  uint32_t qa[kKs][2], ql[kKs][2];
+  // Q as bf16 A fragments: row gq = hi part of head gq, row gq + 8 = its lo
+  // part (heads >= G are zero)
+  uint32_t qa[kKs][4];
 #pragma unroll
   for (int ks = 0; ks < kKs; ++ks) {
     const int c0 = ks * 16 + 2 * cq;
     const float* q = qs + gq * HD;
-    split_bf16(q[c0], q[c0 + 1], qa[ks][0], ql[ks][0]);
-    split_bf16(q[c0 + 8], q[c0 + 9], qa[ks][1], ql[ks][1]);
+    split_bf16(q[c0], q[c0 + 1], qa[ks][0], qa[ks][1]);
+    split_bf16(q[c0 + 8], q[c0 + 9], qa[ks][2], qa[ks][3]);
   }
 
 
@@ -239,10 +243,8 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
         uint32_t bk[4];
         const int rr = p0 + (mi >> 1) * 8 + ri, ch = 2 * ks + (mi & 1);
         ldsm_x4(smem_u32(kb + swz<HD>(rr, ch)), bk);
-        mma16816(sacc[0], qa[ks][0], qa[ks][1], bk[0], bk[1]);
-        mma16816(sacc[1], qa[ks][0], qa[ks][1], bk[2], bk[3]);
-        mma16816(sacc[0], ql[ks][0], ql[ks][1], bk[0], bk[1]);
-        mma16816(sacc[1], ql[ks][0], ql[ks][1], bk[2], bk[3]);
+        mma16816(sacc[0], qa[ks], bk[0], bk[1]);
+        mma16816(sacc[1], qa[ks], bk[2], bk[3]);
       }
       // online softmax over this warp's positions, per head (row gq)
       float sv[4];
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int pp = p0 + nt * 8 + 2 * cq + e;
-          sv[nt * 2 + e] = pp < cnt ? sacc[nt][e] * scale : -CUDART_INF_F;
+          sv[nt * 2 + e] = pp < cnt ? (sacc[nt][e] + sacc[nt][2 + e]) * scale : -CUDART_INF_F;
         }
       float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -269,23 +271,24 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
       l_run = l_run * alpha + psum;
       m_run = mnew;
 #pragma unroll
-      for (int j = 0; j < kNt; ++j) {
+      for (int j = 0; j < kNt; ++j) {  // both the hi and the lo accumulators
         o_acc[j][0] *= alpha;
         o_acc[j][1] *= alpha;
+        o_acc[j][2] *= alpha;
+        o_acc[j][3] *= alpha;
       }
-      // O += P V; P's A fragment: positions 2cq..2cq+1 (n-tile 0) and +8
-      uint32_t pa0, pa2, pl0, pl2;
-      split_bf16(pv[0], pv[1], pa0, pl0);
-      split_bf16(pv[2], pv[3], pa2, pl2);
+      // O += P V; P's A fragment: positions 2cq..2cq+1 (n-tile 0) and +8,
+      // hi parts in row gq, lo parts in row gq + 8
+      uint32_t pa[4];
+      split_bf16(pv[0], pv[1], pa[0], pa[1]);
+      split_bf16(pv[2], pv[3], pa[2], pa[3]);
 #pragma unroll
       for (int j = 0; j < kNt; j += 2) {
         uint32_t bv[4];
         const int rr = p0 + (mi & 1) * 8 + ri, ch = j + (mi >> 1);
         ldsm_x4_t(smem_u32(vb + swz<HD>(rr, ch)), bv);
-        mma16816(o_acc[j], pa0, pa2, bv[0], bv[1]);
-        mma16816(o_acc[j + 1], pa0, pa2, bv[2], bv[3]);
-        mma16816(o_acc[j], pl0, pl2, bv[0], bv[1]);
-        mma16816(o_acc[j + 1], pl0, pl2, bv[2], bv[3]);
+        mma16816(o_acc[j], pa, bv[0], bv[1]);
+        mma16816(o_acc[j + 1], pa, bv[2], bv[3]);
       }
     }
     __syncthreads();  // buffer i % 2 is free
@@ -300,8 +303,8 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
   if (gq < G) {
 #pragma unroll
     for (int j = 0; j < kNt; ++j) {
-      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq] = o_acc[j][0];
-      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq + 1] = o_acc[j][1];
+      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq] = o_acc[j][0] + o_acc[j][2];
+      wo[(warp * kG + gq) * HD + 8 * j + 2 * cq + 1] = o_acc[j][1] + o_acc[j][3];
     }
   }
   __syncthreads();
@@ -342,19 +345,48 @@ __global__ void __launch_bounds__(kT, 3) k_attn_mma(AttnParams a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int o = tid; o < G * HD; o += kT) {
-    const int h = o / HD;
+  // merge: every split's (m, l) into shared memory at once, the weights once
+  // per (split, head), then the outputs with independent loads; all sums in
+  // ascending split order
+  float* sm = reinterpret_cast<float*>(smem);     // [ns][kG] m, then weights
+  float* sl = sm + (size_t)ns * kG;               // [ns][kG] l
+  float* sL = sl + (size_t)ns * kG;               // [kG] merged l
+  for (int idx = tid; idx < ns * G; idx += kT) {
+    const int q = idx / G, h = idx - q * G;
+    const int64_t bq = ((int64_t)b * a.max_splits + q) * H + g * G + h;
+    sm[q * kG + h] = __ldcg(a.part_ml + 2 * bq);
+    sl[q * kG + h] = __ldcg(a.part_ml + 2 * bq + 1);
+  }
+  __syncthreads();
+  if (tid < G) {
+    const int h = tid;
     float mx = -CUDART_INF_F;
-    for (int q = 0; q < ns; ++q)
-      mx = fmaxf(mx, __ldcg(a.part_ml + 2 * (((int64_t)b * a.max_splits + q) * H + g * G + h)));
-    float L = 0.0f, A = 0.0f;
+    for (int q = 0; q < ns; ++q) mx = fmaxf(mx, sm[q * kG + h]);
+    float L = 0.0f;
     for (int q = 0; q < ns; ++q) {
-      const int64_t bq = ((int64_t)b * a.max_splits + q) * H + g * G + h;
-      const float w = expf(__ldcg(a.part_ml + 2 * bq) - mx);
-      L = fmaf(__ldcg(a.part_ml + 2 * bq + 1), w, L);
-      A = fmaf(__ldcg(a.part_acc + bq * HD + (o - h * HD)), w, A);
+      const float w = expf(sm[q * kG + h] - mx);
+      sm[q * kG + h] = w;
+      L = fmaf(sl[q * kG + h], w, L);
     }
-    st_out(orow + o, A / L);
+    sL[h] = L;
+  }
+  __syncthreads();
+  for (int o = tid; o < G * HD; o += kT) {
+    const int h = o / HD, d = o - h * HD;
+    const float* src = a.part_acc + (((int64_t)b * a.max_splits) * H + g * G + h) * HD + d;
+    const int64_t qstride = (int64_t)H * HD;
+    float A = 0.0f;
+    int q = 0;
+    for (; q + 4 <= ns; q += 4) {  // four independent loads in flight
+      const float a0 = __ldcg(src + (q + 0) * qstride), a1 = __ldcg(src + (q + 1) * qstride);
+      const float a2 = __ldcg(src + (q + 2) * qstride), a3 = __ldcg(src + (q + 3) * qstride);
+      A = fmaf(a0, sm[(q + 0) * kG + h], A);
+      A = fmaf(a1, sm[(q + 1) * kG + h], A);
+      A = fmaf(a2, sm[(q + 2) * kG + h], A);
+      A = fmaf(a3, sm[(q + 3) * kG + h], A);
+    }
+    for (; q < ns; ++q) A = fmaf(__ldcg(src + q * qstride), sm[q * kG + h], A);
+    st_out(orow + o, A / sL[h]);
   }
 }
 
@@ -387,9 +419,11 @@ int dispatch(const AttnParams& a, int B, cudaStream_t s) {
 
 }  // namespace
 
-bool attn_mma_supports(int hd, int G, int kv_f32, int split_len) {
+bool attn_mma_supports(int hd, int G, int kv_f32, int split_len, int max_splits) {
+  // the split merge stages 2 * kG floats per split in the tile buffers
+  const size_t merge_bytes = (size_t)(2 * kG * max_splits + kG) * sizeof(float);
   return !kv_f32 && (hd == 64 || hd == 128 || hd == 256) && G >= 1 && G <= kG &&
-         split_len % kTT == 0;
+         split_len % kTT == 0 && merge_bytes <= 4 * (size_t)kTT * hd * 2;
 }
 
 int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s) {
