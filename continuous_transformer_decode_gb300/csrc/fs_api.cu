@@ -33,7 +33,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 // tcgen05 operand map and the fixed K split of one weight matrix.
 struct TcW {
   CUtensorMap tm;
-  int m_tiles = 0, splits = 1;
+  int m_tiles = 0, P = 1;  // row tiles, stream-K width
   int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
   __half* q8_scales = nullptr;
 };
@@ -45,34 +45,24 @@ struct LayerW {
   float* g_ffn = nullptr;
 };
 
-// K split of a weight matrix: enough (128-row tile, K range) units to cover
-// the SMs, at least two 64-wide K blocks per unit, at most 8, and only while
-// the split partials (128 rows x the handle's lane capacity, f32) stay small
-// next to the unit's weight bytes (128 rows x K / splits, bf16). It depends
-// on the matrix and the handle only, never on a call's lane count.
-int choose_splits(int m_tiles, int K, int max_lanes) {
-  const int n_cap = std::min(256, (int)round_up(max_lanes, 16));
-  int s = (152 + m_tiles - 1) / m_tiles;
-  s = std::min(s, std::max(1, K / 128));
-  s = std::min(s, K / (8 * n_cap));
-  s = std::min(s, 8);
-  return std::max(1, s);
-}
-
-// Lanes per group of a GEMM launch: enough (tile, split, group) units for
-// about two blocks per SM, groups of 32..256 lanes (fewer when n is small).
-// Groups split N only, so this may depend on the call's lane count.
-int choose_lane_group(int n, int units) {
-  const int want = std::max(1, (304 + units - 1) / units);
-  int lg = (int)round_up((n + want - 1) / want, 16);
-  lg = std::max(lg, std::min(32, (int)round_up(n, 16)));
-  return std::min(lg, 256);
-}
-
-int tmem_cols_for(int lg) {
-  int c = 32;
-  while (c < lg) c *= 2;
-  return c;
+// Stream-K width P of a weight matrix (blocks per lane group), from timings
+// of this kernel on the decode step's matrix shapes:
+//  * at least as many 128-row tiles as SMs: one whole tile per block
+//    (P = m_tiles), no partial sums;
+//  * lane capacity <= 32 and at least 4 k-blocks per block at P = 2 x SMs:
+//    P = 2 x SMs, ranges crossing tile boundaries (partials are small);
+//  * otherwise equal K splits of every tile, P = m_tiles * s with
+//    m_tiles * s <= 0.85 x SMs, at least 16 k-blocks per split and s <= 8;
+//    lane groups then bring the launch to about two blocks per SM.
+// P depends on the matrix, the handle's lane capacity and the device only,
+// never on a call's lane count.
+int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
+  const int64_t T = (int64_t)m_tiles * kb_total;
+  if (m_tiles >= sms) return m_tiles;
+  if (max_lanes <= 32 && T >= (int64_t)8 * sms) return 2 * sms;
+  int s = (85 * sms) / (100 * m_tiles);
+  s = std::min(s, std::min(8, kb_total / 16));
+  return m_tiles * std::max(1, s);
 }
 }  // namespace
 
@@ -83,6 +73,7 @@ struct fs_handle {
   int Kp_d = 0, Kp_q = 0, Kp_f = 0;
   int Nq = 0, Nkv = 0, Nqkv = 0;
   int G = 1;
+  int sms = 1;  // SMs of the handle's device
   int split_len = 256, max_splits = 1;
   int max_pages_per_lane = 0;
 
@@ -473,14 +464,20 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   *h->err_flag = 0;
   FS_CK(h, cudaHostGetDevicePointer((void**)&h->d_err_flag, h->err_flag, 0));
   if (h->use_tc) {
+    {
+      int dev = 0;
+      FS_CK(h, cudaGetDevice(&dev));
+      FS_CK(h, cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev));
+    }
     size_t ws_elems = 0;
     int max_tiles = 1;
     auto setup = [&](const Mat& m, TcW* t) -> int {
       t->m_tiles = (m.N + 127) / 128;
-      t->splits = choose_splits(t->m_tiles, m.Kp, B);
+      t->P = choose_width(t->m_tiles, m.Kp / 64, B, h->sms);
+      if (!tc_width_ok(t->m_tiles, m.Kp / 64, t->P))
+        return h->fail(FS_ERR_ARG, "weight matrix too large for the tcgen05 GEMM");
       max_tiles = std::max(max_tiles, t->m_tiles);
-      if (t->splits > 1)
-        ws_elems = std::max(ws_elems, (size_t)t->splits * B * t->m_tiles * 128);
+      ws_elems = std::max(ws_elems, tc_ws_floats(t->P, B));
       if (h->wtype == W_Q8) {
         const size_t tiles = (size_t)t->m_tiles * (m.Kp / 64);
         if (h->alloc(&t->q8_codes, tiles * 8192) != cudaSuccess ||
@@ -615,11 +612,10 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
       return;
     }
     TcParams p{};
-    p.m_tiles = T.m_tiles; p.splits = T.splits; p.kb_total = W.Kp / 64;
-    p.lanes_total = n;
-    p.lg = choose_lane_group(n, T.m_tiles * T.splits);
-    p.groups = (n + p.lg - 1) / p.lg;
-    p.tmem_cols = tmem_cols_for(p.lg);
+    p.m_tiles = T.m_tiles; p.P = T.P; p.kb_total = W.Kp / 64;
+    p.lanes_total = n; p.sms = h->sms;
+    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups);
+    p.tmem_cols = tc_tmem_cols(p.lg);
     p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
     p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
@@ -1049,33 +1045,28 @@ int fs_device_error(fs_handle* h, int32_t* code_out) {
   return FS_OK;
 }
 
-int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,
-                 float* Y, int32_t splits, int32_t path, void* stream) {
+}  // extern "C"
+
+namespace {
+// tcgen05 GEMM of the test hooks with stream-K width P and its own workspace.
+int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, float* Y, int P,
+                 int reps, double* ms_out, cudaStream_t s) {
   using namespace fsk;
-  if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
-      splits > K / 64 || splits > 8 || (path != 0 && path != 1))
-    return FS_ERR_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  Mat m;
-  m.w = W; m.N = N; m.K = K; m.Kp = K; m.wtype = W_BF16;
-  if (path == 0) {
-    GemmArgs g{};
-    g.W = m; g.X = X; g.x_type = X_BF16; g.B = B; g.epi = EPI_STORE;
-    g.out_f32 = Y; g.ldo = N; g.n_out = N;
-    launch_gemv(g, s);
-    if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
-    return cudaStreamSynchronize(s) == cudaSuccess ? FS_OK : FS_ERR_CUDA;
-  }
   CUtensorMap tw, tx, tx64;
   if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
       tc_make_map(X, B, K, 64, &tx64))
     return FS_ERR_CUDA;
   const int m_tiles = (N + 127) / 128;
+  if (!tc_width_ok(m_tiles, K / 64, P)) return FS_ERR_ARG;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FS_ERR_CUDA;
   float* ws = nullptr;
   int *cnt = nullptr, *err = nullptr;
   const int max_groups = (B + 15) / 16;
   int rc = FS_OK;
-  if (cudaMalloc(&ws, (size_t)splits * B * m_tiles * 128 * 4) != cudaSuccess ||
+  if (cudaMalloc(&ws, tc_ws_floats(P, B) * 4) != cudaSuccess ||
       cudaMalloc(&cnt, (size_t)m_tiles * max_groups * 4) != cudaSuccess ||
       cudaMalloc(&err, 4) != cudaSuccess) {
     rc = FS_ERR_OOM;
@@ -1083,14 +1074,39 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
     cudaMemsetAsync(cnt, 0, (size_t)m_tiles * max_groups * 4, s);
     cudaMemsetAsync(err, 0, 4, s);
     TcParams p{};
-    p.m_tiles = m_tiles; p.splits = splits; p.kb_total = K / 64;
-    p.lanes_total = B;
-    p.lg = choose_lane_group(B, m_tiles * splits);
-    p.groups = (B + p.lg - 1) / p.lg;
-    p.tmem_cols = tmem_cols_for(p.lg);
+    p.m_tiles = m_tiles; p.P = P; p.kb_total = K / 64;
+    p.lanes_total = B; p.sms = sms;
+    tc_lane_groups(B, P, sms, &p.lg, &p.groups);
+    p.tmem_cols = tc_tmem_cols(p.lg);
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
     launch_gemm_tc(tw, tx64, tx, p, s);
+    if (reps > 0 && ms_out) {
+      // each launch between two events, after a 256 MiB memset that evicts
+      // the operands from L2 and keeps the GPU busy (clocks up)
+      const size_t flush_bytes = (size_t)256 << 20;
+      void* flush = nullptr;
+      std::vector<cudaEvent_t> ev(2 * (size_t)reps);
+      for (auto& e : ev) cudaEventCreate(&e);
+      if (cudaMalloc(&flush, flush_bytes) == cudaSuccess) {
+        for (int r = 0; r < reps; ++r) {
+          cudaMemsetAsync(flush, r & 0xff, flush_bytes, s);
+          cudaEventRecord(ev[2 * r], s);
+          launch_gemm_tc(tw, tx64, tx, p, s);
+          cudaEventRecord(ev[2 * r + 1], s);
+        }
+        double sum = 0.0;
+        bool ok = cudaEventSynchronize(ev.back()) == cudaSuccess;
+        for (int r = 0; ok && r < reps; ++r) {
+          float ms = 0.0f;
+          ok = cudaEventElapsedTime(&ms, ev[2 * r], ev[2 * r + 1]) == cudaSuccess;
+          sum += ms;
+        }
+        if (ok) *ms_out = sum / reps;
+        cudaFree(flush);
+      }
+      for (auto& e : ev) cudaEventDestroy(e);
+    }
     int herr = 0;
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
         cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -1102,6 +1118,48 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
   cudaFree(cnt);
   cudaFree(err);
   return rc;
+}
+}  // namespace
+
+extern "C" {
+
+int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,
+                 float* Y, int32_t splits, int32_t path, void* stream) {
+  using namespace fsk;
+  if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
+      splits > K / 64 || splits > 8 || (path != 0 && path != 1))
+    return FS_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (path == 0) {
+    Mat m;
+    m.w = W; m.N = N; m.K = K; m.Kp = K; m.wtype = W_BF16;
+    GemmArgs g{};
+    g.W = m; g.X = X; g.x_type = X_BF16; g.B = B; g.epi = EPI_STORE;
+    g.out_f32 = Y; g.ldo = N; g.n_out = N;
+    launch_gemv(g, s);
+    if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+  }
+  // stream-K width m_tiles * splits: every block's range is the K split of
+  // one tile, so the pieces are exactly the `splits` K splits
+  return gemm_tc_hook(W, N, K, X, B, Y, ((N + 127) / 128) * splits, 0, nullptr, s);
+}
+
+int fs_gemm_bf16_width(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,
+                       float* Y, int32_t width, void* stream) {
+  if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || width < 1 ||
+      (int64_t)width > (int64_t)((N + 127) / 128) * (K / 64))
+    return FS_ERR_ARG;
+  return gemm_tc_hook(W, N, K, X, B, Y, width, 0, nullptr, (cudaStream_t)stream);
+}
+
+int fs_gemm_bf16_time(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,
+                      float* Y, int32_t width, int32_t reps, double* ms_out, void* stream) {
+  if (!W || !X || !Y || !ms_out || N < 1 || K < 64 || K % 64 || B < 1 || width < 1 ||
+      (int64_t)width > (int64_t)((N + 127) / 128) * (K / 64) || reps < 1)
+    return FS_ERR_ARG;
+  *ms_out = 0.0;
+  return gemm_tc_hook(W, N, K, X, B, Y, width, reps, ms_out, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <utility>
 
 namespace fsk {
@@ -104,22 +105,24 @@ struct GemmArgs {
 // Launchers (each returns the number of kernels launched).
 int launch_gemv(const GemmArgs& a, cudaStream_t s);
 
-// tcgen05 GEMM (bf16 weights and panels). Work unit = (128-row weight tile,
-// K split, lane group); grid = m_tiles * splits * groups, the groups of one
-// (tile, split) adjacent so they share the weight tile through L2.
+// tcgen05 GEMM (bf16 weights and panels). Stream-K: the m_tiles * kb_total
+// k-blocks are cut into P equal ranges; grid = P * groups, the lane groups
+// of one range adjacent so they share its weight tiles through L2.
 struct TcParams {
-  int m_tiles, splits, kb_total;
+  int m_tiles, kb_total;
+  int P;           // stream-K blocks per lane group (1 <= P <= m_tiles * kb_total)
   int groups;      // lane groups
   int lg;          // lanes per group (multiple of 16, <= 256)
   int lanes_total; // lanes of the step (panel rows 0 .. lanes_total-1)
   int tmem_cols;   // power of two >= max(32, lg)
+  int sms;         // SMs of the device (stage budget: one or two blocks per SM)
   int stages, stage_bytes;  // set by the launcher
   int epi;
   float* out_f32;
   void* out_x;
   int ldo;
   int n_out;       // output rows (W rows, or F for SwiGLU)
-  float* ws;       // split partials [splits][lanes_total][m_tiles * 128]
+  float* ws;       // partial pieces [2][P][lanes_total][128] f32
   int* counters;   // [m_tiles * groups], zero between launches
   int* err;        // device-visible error flag
   // Q8_0 weights in tiles: codes [m_tiles][kb][128][64] int8 and scales
@@ -127,6 +130,34 @@ struct TcParams {
   const int8_t* q8_codes;
   const __half* q8_scales;
 };
+// Lanes per group of one tcgen05 GEMM call: at most 256 (the MMA's N
+// limit); a matrix with fewer stream-K blocks than SMs is spread over more
+// groups of at least 32 lanes to fill about two blocks per SM. Groups split
+// N only, so this may depend on the call's lane count.
+inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups) {
+  int g = (n + 255) / 256;
+  if (P < sms) {
+    const int fill = std::max(1, 2 * sms / P);
+    g = std::max(g, std::min(fill, std::max(1, (n + 31) / 32)));
+  }
+  const int l = ((n + g - 1) / g + 15) / 16 * 16;
+  *lg = l;
+  *groups = (n + l - 1) / l;
+}
+// The kernel's stream-K index arithmetic is 32-bit: (P + 1) * T < 2^31 with
+// T = m_tiles * kb_total.
+inline bool tc_width_ok(int m_tiles, int kb_total, int P) {
+  const int64_t T = (int64_t)m_tiles * kb_total;
+  return P >= 1 && P <= T && (int64_t)(P + 1) * T < ((int64_t)1 << 31);
+}
+// Workspace floats of a launch: two slots per block and lane, 128 rows each.
+inline size_t tc_ws_floats(int P, int lanes) { return (size_t)2 * P * lanes * 128; }
+// TMEM columns of a block: a power of two >= max(32, lg).
+inline int tc_tmem_cols(int lg) {
+  int c = 32;
+  while (c < lg) c *= 2;
+  return c;
+}
 bool tc_available();
 int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
 // tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.

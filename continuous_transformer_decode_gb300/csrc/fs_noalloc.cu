@@ -58,18 +58,6 @@ unsigned char* scratch_on_current_device(int* rc) {
   return g_dev_addr[dev];
 }
 
-int64_t round_up16(int64_t x) { return (x + 15) / 16 * 16; }
-
-// Lanes per group: the same rule as the allocating entry point (about two
-// blocks per SM, groups of 32..256 lanes; fewer when B is small).
-int lane_group(int n, int units) {
-  const int want = (304 + units - 1) / units > 1 ? (304 + units - 1) / units : 1;
-  int lg = (int)round_up16((n + want - 1) / want);
-  const int floor_lg = (int)(round_up16(n) < 32 ? round_up16(n) : 32);
-  if (lg < floor_lg) lg = floor_lg;
-  return lg < 256 ? lg : 256;
-}
-
 }  // namespace
 
 extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
@@ -80,8 +68,16 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
       splits > K / 64 || splits > 8)
     return FS_ERR_ARG;
   const int64_t m_tiles = (N + 127) / 128;
-  const int lg = lane_group(B, (int)(m_tiles * splits));
-  const int groups = (B + lg - 1) / lg;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FS_ERR_CUDA;
+  // stream-K width m_tiles * splits: each block's range is the K split of one
+  // tile, so only the first workspace slot of each block is ever written
+  const int P = (int)(m_tiles * splits);
+  if (!tc_width_ok((int)m_tiles, K / 64, P)) return FS_ERR_ARG;
+  int lg = 0, groups = 0;
+  tc_lane_groups(B, P, sms, &lg, &groups);
   const size_t ctr_bytes = (size_t)(m_tiles * groups + 1) * sizeof(int);
   const size_t part_bytes =
       splits > 1 ? (size_t)splits * B * m_tiles * 128 * sizeof(float) : 0;
@@ -103,13 +99,13 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
   if (cudaMemsetAsync(counters, 0, ctr_bytes, s) != cudaSuccess) return FS_ERR_CUDA;
   TcParams p{};
   p.m_tiles = (int)m_tiles;
-  p.splits = splits;
+  p.P = P;
   p.kb_total = K / 64;
   p.lanes_total = B;
+  p.sms = sms;
   p.lg = lg;
   p.groups = groups;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < lg) p.tmem_cols *= 2;
+  p.tmem_cols = tc_tmem_cols(lg);
   p.epi = EPI_STORE;
   p.out_f32 = Y;
   p.ldo = N;

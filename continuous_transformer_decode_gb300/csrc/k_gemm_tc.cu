@@ -13,14 +13,17 @@
 // Block = 6 warps: warp 4 issues TMA loads, warp 5 owns TMEM and issues the
 // MMAs, warps 0-3 run the epilogue (warp w reads TMEM lanes 32w..32w+31,
 // i.e. weight rows; each thread then holds one output row for every lane).
-// A block owns one (128-row tile, K range, lane group) work unit. Lane
-// groups split the N dimension only, which leaves every output element's
-// K order unchanged. With a K split > 1 the partial tiles go to a workspace
-// and the last block of the (row tile, lane group) to arrive sums them in
-// split order, so results never depend on timing. The K split count depends
-// only on the matrix shape and the handle's lane capacity, never on the
-// number of lanes in a call: a lane's output is then independent of the
-// batch it is computed in.
+// Work split (stream-K): the matrix's k-blocks, row tile after row tile, are
+// cut into P equal contiguous ranges, and block c of each lane group streams
+// range c through one ring of stages, so every block moves the same number
+// of weight bytes and no launch ends in a partial wave. The part of a range
+// inside one row tile is a piece, accumulated in TMEM; a piece covering the
+// whole tile goes straight to the epilogue, a partial one to a workspace,
+// and the last piece of a tile to arrive sums the tile's pieces in block
+// order, so results never depend on timing. P depends only on the matrix
+// shape, the handle's lane capacity and the SM count, never on the number of
+// lanes in a call; lane groups split the N dimension only. A lane's output
+// is therefore independent of the batch it is computed in.
 //
 // Every wait on an mbarrier is bounded (1 s of %globaltimer); on timeout the
 // block records an error code, stops issuing work, drains the TMA loads it
@@ -30,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "fs_internal.h"
 
@@ -45,6 +49,7 @@ constexpr int kXBoxRows = 16;
 constexpr int kQ8Codes = kBM * kBK;        // 8 KB
 constexpr int kQ8Scales = kBM * 2 * 2;     // 512 B
 constexpr int kQ8XOff = 25 * 1024;         // 16 + 8 + 0.5 KB, 1 KB aligned
+constexpr int kXbufBytes = 64 * 17 * 4 + 256;  // SwiGLU gate/up exchange, 8-byte aligned end
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -151,9 +156,38 @@ __device__ __forceinline__ void tmem_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-constexpr int kMaxSplits = 8;
-
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Stream-K bookkeeping. The T = m_tiles * kb_total k-blocks of the matrix,
+// taken tile by tile, are cut into P contiguous ranges; block c of a lane
+// group owns k-blocks [c T / P, (c + 1) T / P). The part of a range that
+// falls in one row tile is a piece: a whole tile goes straight to the
+// epilogue, a partial one to the workspace, and the last piece of a tile to
+// arrive sums that tile's pieces in block order.
+// (32-bit: the host keeps (P + 1) * T below 2^31.)
+__device__ __forceinline__ int sk_lo(int c, int T, int P) { return c * T / P; }
+// The block whose range holds k-block g.
+__device__ __forceinline__ int sk_owner(int g, int T, int P) {
+  return ((g + 1) * P - 1) / T;
+}
+// Workspace piece of block c (slot 0: the first tile of its range, slot 1:
+// the last) for one lane of the call: 128 f32, one per row of the tile.
+__device__ __forceinline__ float* piece_ptr(const TcParams& p, int slot, int c, int lane) {
+  return p.ws + (((int64_t)slot * p.P + c) * p.lanes_total + lane) * kBM;
+}
+struct TilePieces {
+  int cA, cB;  // first and last block contributing to the tile
+  int slotA;   // slot of block cA's piece (1 when its range starts in an earlier tile)
+};
+__device__ __forceinline__ TilePieces tile_pieces(const TcParams& p, int t) {
+  const int T = p.m_tiles * p.kb_total;
+  const int tb = t * p.kb_total;
+  TilePieces r;
+  r.cA = sk_owner(tb, T, p.P);
+  r.cB = sk_owner(tb + p.kb_total - 1, T, p.P);
+  r.slotA = sk_lo(r.cA, T, p.P) < tb ? 1 : 0;
+  return r;
+}
 
 // Writes one 16-lane chunk of final values of this thread's row.
 // For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
@@ -201,31 +235,38 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
   }
 }
 
-// Sum of the split partials of 4 consecutive rows of one lane, split order.
-__device__ __forceinline__ float4 sum_splits4(const TcParams& p, int64_t R, int b,
-                                              int64_t row0) {
-  float4 part[kMaxSplits];
-#pragma unroll
-  for (int sp = 0; sp < kMaxSplits; ++sp)
-    if (sp < p.splits)
-      part[sp] = __ldcg(reinterpret_cast<const float4*>(
-          p.ws + ((int64_t)sp * p.lanes_total + b) * R + row0));
-  float4 acc = part[0];
-#pragma unroll
-  for (int sp = 1; sp < kMaxSplits; ++sp)
-    if (sp < p.splits) {
-      acc.x += part[sp].x;
-      acc.y += part[sp].y;
-      acc.z += part[sp].z;
-      acc.w += part[sp].w;
-    }
+__device__ __forceinline__ float4 ld4(const float* q) {
+  return __ldcg(reinterpret_cast<const float4*>(q));
+}
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+// Sum, in block order, of a tile's pieces at rows r0 .. r0+3 of one lane.
+__device__ __forceinline__ float4 sum_pieces4(const TcParams& p, const TilePieces& tp,
+                                              int lane, int r0) {
+  float4 acc = ld4(piece_ptr(p, tp.slotA, tp.cA, lane) + r0);
+  int c = tp.cA + 1;
+  for (; c + 3 <= tp.cB; c += 4) {  // four independent loads, added in block order
+    const float4 v0 = ld4(piece_ptr(p, 0, c, lane) + r0);
+    const float4 v1 = ld4(piece_ptr(p, 0, c + 1, lane) + r0);
+    const float4 v2 = ld4(piece_ptr(p, 0, c + 2, lane) + r0);
+    const float4 v3 = ld4(piece_ptr(p, 0, c + 3, lane) + r0);
+    add4(acc, v0);
+    add4(acc, v1);
+    add4(acc, v2);
+    add4(acc, v3);
+  }
+  for (; c <= tp.cB; ++c) add4(acc, ld4(piece_ptr(p, 0, c, lane) + r0));
   return acc;
 }
 
-// Last block of a row tile: reduce the split partials and apply the
+// Last piece of a row tile to arrive: sum the tile's pieces and apply the
 // epilogue with 16-byte accesses (threads map to 4-row groups x lanes).
-__device__ void reduce_tile(const TcParams& p, int m_tile, int lane0, int lanes) {
-  const int64_t R = (int64_t)p.m_tiles * kBM;
+__device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp, int lane0,
+                            int lanes) {
   const int t = threadIdx.x;  // 0..127
   if (p.epi == EPI_SWIGLU) {
     const int rq = (t & 15) * 4, lsub = t >> 4;  // 16 threads per lane row
@@ -236,8 +277,8 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, int lane0, int lanes)
 #pragma unroll
       for (int k = 0; k < 2; ++k)
         if (b0 + 8 * k < lanes) {
-          g[k] = sum_splits4(p, R, lane0 + b0 + 8 * k, (int64_t)m_tile * kBM + rq);
-          u[k] = sum_splits4(p, R, lane0 + b0 + 8 * k, (int64_t)m_tile * kBM + 64 + rq);
+          g[k] = sum_pieces4(p, tp, lane0 + b0 + 8 * k, rq);
+          u[k] = sum_pieces4(p, tp, lane0 + b0 + 8 * k, 64 + rq);
         }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -265,7 +306,7 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, int lane0, int lanes)
     float4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (b0 + 4 * u < lanes) v[u] = sum_splits4(p, R, lane0 + b0 + 4 * u, row0);
+      if (b0 + 4 * u < lanes) v[u] = sum_pieces4(p, tp, lane0 + b0 + 4 * u, rq);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int b = b0 + 4 * u;
@@ -311,7 +352,7 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
 }
 
 template <bool kQ8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
               const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -320,21 +361,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_last;
+  __shared__ int s_stop[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = blockIdx.x % p.groups;
-  const int rest = blockIdx.x / p.groups;
-  const int split = rest % p.splits, m_tile = rest / p.splits;
+  const int cblk = blockIdx.x / p.groups;  // stream-K block within the lane group
   const int lane0 = group * p.lg;
   const int lanes = min(p.lg, p.lanes_total - lane0);
   const int n_tot = (lanes + 15) & ~15;
-  const int kb0 = split * p.kb_total / p.splits;
-  const int kb1 = (split + 1) * p.kb_total / p.splits;
-  const int nkb = kb1 - kb0;
+  const int kbt = p.kb_total;
+  const int T = p.m_tiles * kbt;
+  const int g0 = sk_lo(cblk, T, p.P), g1 = sk_lo(cblk + 1, T, p.P);
+  const int n_it = g1 - g0;  // >= 1 because P <= T
+  const int t_first = g0 / kbt;
+  const int n_pieces = (g1 - 1) / kbt - t_first + 1;
   const int S = p.stages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+  float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * p.stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S),
-                 accum = smem_u32(bars + 2 * S), conv0 = smem_u32(bars + 2 * S + 1);
+                 conv0 = smem_u32(bars + 2 * S), tfull = smem_u32(bars + 3 * S),
+                 tempty = smem_u32(bars + 3 * S + 1);
   constexpr int kXOff = kQ8 ? kQ8XOff : kWTileBytes;
   const uint32_t ncols = p.tmem_cols;
 
@@ -342,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
+      if (kQ8) mbar_init(conv0 + 8 * s, 128);  // the 128 converters
     }
-    mbar_init(accum, 1);
-    if (kQ8)
-      for (int s = 0; s < S; ++s) mbar_init(conv0 + 8 * s, 128);  // the 128 converters
+    mbar_init(tfull, 1);     // the MMA issuer's commit at the end of a piece
+    mbar_init(tempty, 128);  // every epilogue thread, after reading TMEM
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_abort = 0;
     s_last = 0;
@@ -370,39 +416,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == 4) {
-    if (lane == 0) {  // ---- TMA producer
+    if (lane == 0) {  // ---- TMA producer: the block's k-blocks in order
       int issued = 0;
       auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
         const int s = i % S;
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const int g = g0 + i;  // = m_tile * kb_total + kb
         if (kQ8) {
           mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
-          const int64_t tile = (int64_t)m_tile * p.kb_total + kb0 + i;
-          bulk_load(st + kWTileBytes, p.q8_codes + tile * kQ8Codes, kQ8Codes, full0 + 8 * s);
-          bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + tile * (kQ8Scales / 2), kQ8Scales,
+          bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
                     full0 + 8 * s);
+          bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + (int64_t)g * (kQ8Scales / 2),
+                    kQ8Scales, full0 + 8 * s);
         } else {
+          const int tile = g / kbt;
           mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
-          tma_load_2d(st, &tmW, (kb0 + i) * kBK, m_tile * kBM, full0 + 8 * s);
+          tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
         }
       };
       auto load_x = [&](int i) {  // panel part of stage i
         const int s = i % S;
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const int x = (kb0 + i) * kBK;
+        const int x = ((g0 + i) % kbt) * kBK;
         int r = 0;
         for (; r + 64 <= n_tot; r += 64)
           tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
         for (; r < n_tot; r += kXBoxRows)
           tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
       };
-      const int pre = min(S, nkb);  // stages are empty at start: no wait needed
+      const int pre = min(S, n_it);  // stages are empty at start: no wait needed
       for (int i = 0; i < pre; ++i) load_w(i);
       pdl_wait();  // the panel is the predecessor's output
       pdl_trigger();
       for (int i = 0; i < pre; ++i) load_x(i);
       issued = pre;
-      for (int i = pre; i < nkb; ++i) {
+      for (int i = pre; i < n_it; ++i) {
         const int s = i % S;
         const uint32_t ph = (uint32_t)(i / S) & 1u;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
@@ -416,107 +464,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = i + 1;
       }
       // drain: every issued load must have landed before the block exits
-      for (int i = 0; i < issued; ++i) {
-        if (i < issued - S) continue;
+      for (int i = max(0, issued - S); i < issued; ++i) {
         const int s = i % S;
         if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) atomicExch(p.err, 2);
       }
     }
   } else if (warp == 5) {
-    if (lane == 0) {  // ---- MMA issuer
+    if (lane == 0) {  // ---- MMA issuer: one TMEM accumulation per piece
       bool ok = true;
-      for (int i = 0; i < nkb && ok; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
-            *(volatile int*)&s_abort) {
-          atomicExch(p.err, 3);
-          s_abort = 1;
-          ok = false;
-          break;
+      int i = 0;
+      const uint32_t idesc = idesc_bf16(kBM, n_tot);
+      for (int q = 0; q < n_pieces && ok; ++q) {
+        const int pe = min(g1, (t_first + q + 1) * kbt);
+        if (q > 0) {  // the epilogue has read the previous piece out of TMEM
+          if (!mbar_wait(tempty, (uint32_t)(q - 1) & 1u) || *(volatile int*)&s_abort) {
+            atomicExch(p.err, 6);
+            s_abort = 1;
+            ok = false;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const uint32_t b0 = a0 + kXOff;
-        const uint32_t idesc = idesc_bf16(kBM, n_tot);
+        bool acc = false;
+        for (; ok && g0 + i < pe; ++i) {
+          const int s = i % S;
+          const uint32_t ph = (uint32_t)(i / S) & 1u;
+          if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
+              *(volatile int*)&s_abort) {
+            atomicExch(p.err, 3);
+            s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
+          const uint32_t b0 = a0 + kXOff;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                     (acc || kk > 0) ? 1u : 0u);
+          acc = true;
+          mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
+        }
+        mma_commit(tfull);  // arrives when every MMA issued above has finished
       }
-      mma_commit(accum);  // arrives when every MMA issued above has finished
     }
-  } else {  // ---- warps 0-3: Q8_0 dequantisation during the mainloop, then epilogue
+  } else {  // ---- warps 0-3: Q8_0 dequantisation of each piece, then its epilogue
     const int row_local = warp * 32 + lane;
-    if (kQ8) {
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) {
-          atomicExch(p.err, 5);
-          s_abort = 1;
-          break;
-        }
-        dequant_q8_tile(smem + (size_t)s * p.stage_bytes, row_local);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
-        mbar_arrive(conv0 + 8 * s);
-      }
-    }
-    float* xbuf = reinterpret_cast<float*>(smem);  // stages are idle by now
-    if (!mbar_wait(accum, 0)) {
-      atomicExch(p.err, 4);
-      s_abort = 1;
-    }
-    tc_fence_after();
-    epi_bar();  // makes the abort decision uniform over the epilogue warps
-    const bool abort = *(volatile int*)&s_abort != 0;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    if (p.splits == 1) {
-      for (int c0 = 0; c0 < n_tot; c0 += 32) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(trow + c0, r0);
-        if (c0 + 16 < n_tot) tmem_ld16(trow + c0 + 16, r1);
-        tmem_wait();
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r0[j]);
-        if (!abort) emit_chunk(p, m_tile, row_local, lane0, lanes, c0, v, xbuf);
-        if (c0 + 16 < n_tot) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r1[j]);
-          if (!abort) emit_chunk(p, m_tile, row_local, lane0, lanes, c0 + 16, v, xbuf);
+    int i = 0;
+    for (int q = 0; q < n_pieces; ++q) {
+      const int t = t_first + q;
+      const int tb = t * kbt;
+      const int pb = max(g0, tb), pe = min(g1, tb + kbt);
+      if (kQ8) {
+        for (; g0 + i < pe; ++i) {
+          const int s = i % S;
+          if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) {
+            atomicExch(p.err, 5);
+            s_abort = 1;
+            break;
+          }
+          dequant_q8_tile(smem + (size_t)s * p.stage_bytes, row_local);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+          mbar_arrive(conv0 + 8 * s);
         }
       }
-    } else {
-      const int64_t R = (int64_t)p.m_tiles * kBM;
-      const int64_t row = (int64_t)m_tile * kBM + row_local;
-      for (int c0 = 0; c0 < n_tot; c0 += 32) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(trow + c0, r0);
-        if (c0 + 16 < n_tot) tmem_ld16(trow + c0 + 16, r1);
+      if (!mbar_wait(tfull, (uint32_t)q & 1u)) {
+        atomicExch(p.err, 4);
+        s_abort = 1;
+      }
+      tc_fence_after();
+      // one thread samples the abort flag so that all 128 take the same
+      // branch (the slot alternates: a slot is rewritten only two pieces
+      // later, after a barrier every thread has passed)
+      if (threadIdx.x == 0) s_stop[q & 1] = *(volatile int*)&s_abort;
+      epi_bar();
+      if (s_stop[q & 1]) break;
+      const bool whole = pb == tb && pe == tb + kbt;
+      const int slot = q == 0 ? 0 : 1;
+      for (int c0 = 0; c0 < n_tot; c0 += 32) {  // two 16-lane loads in flight
+        uint32_t r[2][16];
+        tmem_ld16(trow + (uint32_t)c0, r[0]);
+        if (c0 + 16 < n_tot) tmem_ld16(trow + (uint32_t)(c0 + 16), r[1]);
         tmem_wait();
-        float* dst = p.ws + ((int64_t)split * p.lanes_total + lane0 + c0) * R + row;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < lanes) dst[(int64_t)j * R] = __uint_as_float(r0[j]);
-        if (c0 + 16 < n_tot) {
+        for (int h = 0; h < 2; ++h) {
+          const int cc = c0 + 16 * h;
+          if (cc >= n_tot) break;
+          float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + 16 + j < lanes) dst[(int64_t)(16 + j) * R] = __uint_as_float(r1[j]);
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
+          if (whole) {
+            emit_chunk(p, t, row_local, lane0, lanes, cc, v, xbuf);
+          } else {
+            float* dst = piece_ptr(p, slot, cblk, lane0 + cc) + row_local;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (cc + j < lanes) dst[j * kBM] = v[j];
+          }
         }
       }
-      __threadfence();
-      epi_bar();
-      int* ctr = p.counters + m_tile * p.groups + group;
-      if (threadIdx.x == 0) {
-        const int prev = atomicAdd(ctr, 1);
-        s_last = (prev == p.splits - 1);
-      }
-      epi_bar();
-      if (s_last) {
+      tc_fence_before();
+      mbar_arrive(tempty);  // the accumulator may be overwritten by the next piece
+      if (!whole) {
         __threadfence();
-        if (!abort) reduce_tile(p, m_tile, lane0, lanes);
-        if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
+        epi_bar();
+        const TilePieces tp = tile_pieces(p, t);
+        int* ctr = p.counters + t * p.groups + group;
+        if (threadIdx.x == 0) s_last = atomicAdd(ctr, 1) == tp.cB - tp.cA;
+        epi_bar();
+        if (s_last) {
+          __threadfence();
+          reduce_tile(p, t, tp, lane0, lanes);
+          if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
+        }
       }
     }
   }
@@ -563,20 +624,29 @@ int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMa
 
 namespace {
 
-// Dynamic shared memory: 1 KB alignment slack, the stages, the barriers.
-// Small tiles (<= 24 KB per stage) get a budget that lets two blocks share
-// an SM; large ones use the per-block limit, minus room for the kernel's
-// static shared variables.
+// Dynamic shared memory: 1 KB alignment slack, the stages, the SwiGLU
+// exchange buffer, the barriers. The budget lets two blocks share an SM
+// (and leaves room for the next kernel's blocks to start under
+// programmatic dependent launch); beyond 3-4 stages a block's stream is
+// limited by its SM's outstanding-load capacity rather than by the ring.
 constexpr int kSmemAttr = 227 * 1024 - 256;
+constexpr int kMaxStages = 12;
+// FS_TC_MAX_STAGES (2..12) lowers the stage cap, a tuning knob read once.
+int max_stages() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_MAX_STAGES");
+    const int x = e ? atoi(e) : kMaxStages;
+    return std::max(2, std::min(kMaxStages, x));
+  }();
+  return v;
+}
 int tc_stages_for(int n_tot, bool q8, int* stage_bytes, int* smem_bytes) {
   const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128;
-  int st;
-  if (sb <= 24 * 1024)
-    st = std::min(5, (110 * 1024 - 1536) / sb);
-  else
-    st = std::min(8, (kSmemAttr - 1536) / sb);
+  const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 2);
+  const int budget = 112 * 1024 - fixed;
+  const int st = std::max(2, std::min(max_stages(), budget / sb));
   *stage_bytes = sb;
-  *smem_bytes = 1024 + st * sb + 8 * (3 * st + 1);
+  *smem_bytes = 1024 + st * sb + kXbufBytes + 8 * (3 * st + 2);
   return st;
 }
 
@@ -592,8 +662,9 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
   }
   TcParams p = p0;
   int smem = 0;
+  const int grid = p.P * p.groups;
   p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, &p.stage_bytes, &smem);
-  launch_k(k_gemm_tc<kQ8>, p.m_tiles * p.splits * p.groups, kThreads, smem, s, tmW, tmX64, tmX16, p);
+  launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
   return 1;
 }
 

@@ -122,6 +122,8 @@ def lib():
         "fs_sched_last_batch": (C.c_int, [p, p, i32, p]),
         "fs_sched_last_error": (C.c_char_p, [p]),
         "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
+        "fs_gemm_bf16_width": (C.c_int, [p, i32, i32, p, i32, p, i32, p]),
+        "fs_gemm_bf16_time": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -139,7 +141,7 @@ def exported_symbols() -> list:
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
-            "fs_gemm_bf16", "fs_copy_logits", "fs_gemm_bf16_noalloc",
+            "fs_gemm_bf16", "fs_gemm_bf16_width", "fs_gemm_bf16_time", "fs_copy_logits", "fs_gemm_bf16_noalloc",
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
             "fs_sched_submit", "fs_sched_step", "fs_sched_run", "fs_sched_take",
             "fs_sched_get_stats", "fs_sched_last_batch", "fs_sched_last_error"]
@@ -335,6 +337,30 @@ def fs_gemm_bf16(W, X, Y, splits: int = 1, path: int = 1, stream=None) -> None:
                             path, raw)
     if rc != FS_OK:
         raise FsError(rc, "fs_gemm_bf16 failed")
+
+
+def fs_gemm_bf16_width(W, X, Y, width: int, stream=None) -> None:
+    """Test hook: the tcgen05 GEMM with the stream-K width given directly."""
+    raw = getattr(stream, "cuda_stream", stream)
+    N, K = W.shape
+    B = X.shape[0]
+    rc = lib().fs_gemm_bf16_width(_dptr(W), N, K, _dptr(X), B, _dptr(Y), width, raw)
+    if rc != FS_OK:
+        raise FsError(rc, "fs_gemm_bf16_width failed")
+
+
+def fs_gemm_bf16_time(W, X, Y, width: int, reps: int = 10, stream=None) -> float:
+    """Tuning hook: mean device ms of one tcgen05 GEMM launch with the given
+    stream-K width, over `reps` launches each after an L2-evicting memset."""
+    raw = getattr(stream, "cuda_stream", stream)
+    N, K = W.shape
+    B = X.shape[0]
+    ms = C.c_double()
+    rc = lib().fs_gemm_bf16_time(_dptr(W), N, K, _dptr(X), B, _dptr(Y), width, reps,
+                                 C.byref(ms), raw)
+    if rc != FS_OK:
+        raise FsError(rc, "fs_gemm_bf16_time failed")
+    return ms.value
 
 
 def fs_copy_logits(h, dst) -> None:

@@ -247,13 +247,32 @@ int fs_device_error(fs_handle* h, int32_t* code_out);
 
 /* Test hook: Y[b, n] = sum_k X[b, k] * W[n, k] for bf16 W [N, K] and
  * X [B, K] (K a multiple of 64), f32 Y [B, N]; all DEVICE pointers owned by
- * the caller. path 1 = tcgen05 kernel with `splits` K splits (1 <= splits
- * <= min(8, K/64)), path 0 = warp-GEMV kernel. Allocates its own workspace; runs on
+ * the caller. path 1 = tcgen05 kernel with `splits` equal K splits per
+ * 128-row tile (1 <= splits <= min(8, K/64)), path 0 = warp-GEMV kernel. Allocates its own workspace; runs on
  * `stream` (NULL = default) and synchronises it. Errors: FS_ERR_ARG,
  * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_DEVICE (a bounded wait timed out). */
 int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
                  int32_t B, float* Y, int32_t splits, int32_t path,
                  void* stream);
+
+/* Test hook: the tcgen05 path of fs_gemm_bf16 with the stream-K width given
+ * directly: the ceil(N/128) * K/64 k-blocks (row tile after row tile) are
+ * cut into `width` equal ranges, one block per range and lane group, so a
+ * range may end inside a row tile and cover parts of several
+ * (1 <= width <= ceil(N/128) * K/64). Same operands, ownership, stream and
+ * errors as fs_gemm_bf16. The pages have no counterpart; it exists to test
+ * the work split that the decode step uses. */
+int fs_gemm_bf16_width(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
+                       int32_t B, float* Y, int32_t width, void* stream);
+
+/* Tuning hook: fs_gemm_bf16_width launched once and then `reps` times, each
+ * launch between two CUDA events and after a 256 MiB memset that evicts the
+ * operands from L2; *ms_out receives the mean device time of one launch in
+ * ms. Same operands, ownership and errors as fs_gemm_bf16. The pages have
+ * no counterpart. */
+int fs_gemm_bf16_time(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
+                      int32_t B, float* Y, int32_t width, int32_t reps,
+                      double* ms_out, void* stream);
 
 /* fs_gemm_bf16 without any device allocation. The pages have no counterpart
  * of this entry point; it exists for callers that cannot call cudaMalloc or

@@ -60,3 +60,30 @@ def test_tcgen05_gemm_batch_invariance_bitwise(splits):
         Y = torch.empty(B, 960, dtype=torch.float32, device="cuda")
         fs.fs_gemm_bf16(Wd, Xd[:B].contiguous(), Y, splits=splits, path=1)
         assert torch.equal(Y.view(torch.int32), full[:B].view(torch.int32)), B
+
+
+@pytest.mark.parametrize("N,K,B,width", [
+    (960, 576, 1, 5), (960, 576, 17, 13), (960, 576, 130, 72), (1000, 576, 33, 50),
+    (3072, 576, 256, 7), (576, 1536, 64, 113), (4096, 1024, 9, 152), (200, 128, 300, 3)])
+def test_tcgen05_stream_k_widths_match_f64(N, K, B, width):
+    """Widths whose ranges end inside row tiles: partial pieces, two slots
+    per block and multi-piece reductions."""
+    import torch
+    W, X = _case(N, K, B, N + 3 * K + B + width)
+    Y = torch.empty(B, N, dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16_width(W.cuda(), X.cuda(), Y, width)
+    ref, mag = _ref(W, X)
+    err = (Y.cpu().double() - ref).abs()
+    assert bool((err <= 1e-5 * mag + 1e-6).all()), float((err / mag.clamp_min(1e-9)).max())
+
+
+def test_tcgen05_stream_k_batch_invariance_bitwise():
+    import torch
+    W, X = _case(1000, 576, 300, 12)
+    Wd, Xd = W.cuda(), X.cuda()
+    full = torch.empty(300, 1000, dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16_width(Wd, Xd, full, 23)
+    for B in (1, 16, 33, 257):
+        Y = torch.empty(B, 1000, dtype=torch.float32, device="cuda")
+        fs.fs_gemm_bf16_width(Wd, Xd[:B].contiguous(), Y, 23)
+        assert torch.equal(Y.view(torch.int32), full[:B].view(torch.int32)), B
