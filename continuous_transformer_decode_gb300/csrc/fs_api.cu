@@ -112,6 +112,8 @@ struct fs_handle {
   bool attn_fused = false;
   bool attn_tiled = false;
   bool attn_mma = false;
+  bool attn_tma = false;         // KV tiles by TMA (k_attn_tma.cu)
+  CUtensorMap tm_kv_k, tm_kv_v;  // KV arenas as [rows][hd] bf16 for that kernel
 
   int32_t* d_args = nullptr;  // [7 * max_lanes + 1]
   int32_t* h_args = nullptr;  // pinned staging
@@ -295,11 +297,23 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   h->Kp_d = (int)round_up(d.d_model, 64);
   h->Kp_q = (int)round_up(h->Nq, 64);
   h->Kp_f = (int)round_up(d.d_ffn, 64);
-  // attention split length: a handle constant (it fixes the merge order);
-  // handles batching many lanes amortise each block over longer splits
-  h->split_len = attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
-                     ? (d.max_lanes >= 64 ? 512 : 128)
-                     : 256;
+  {
+    int dev = 0;
+    FS_CK(h, cudaGetDevice(&dev));
+    FS_CK(h, cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev));
+  }
+  // attention split length: a handle constant (it fixes the merge order).
+  // Long splits amortise each block's fixed cost once a full handle has
+  // enough (lane, KV head, split) blocks to fill the GPU several times over;
+  // otherwise short splits give the parallelism.
+  {
+    const int64_t blocks512 =
+        (int64_t)d.max_lanes * d.n_kv_heads * ((d.max_pos + 511) / 512);
+    h->split_len =
+        attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
+            ? (blocks512 >= 4 * (int64_t)h->sms ? 512 : 128)
+            : 256;
+  }
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;
   {
@@ -452,9 +466,22 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     const bool force_fused = e && std::string(e) == "fused";
     const bool force_tiled = e && std::string(e) == "tiled";
     h->attn_tiled = !force_fused && attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
+    const bool force_mma = e && std::string(e) == "mma";
     h->attn_mma = !force_fused && !force_tiled &&
                   attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len,
                                     h->max_splits);
+    // the TMA kernel's producer warp and barrier set-up pay off on long
+    // contexts; a handle whose lanes stay short keeps the cp.async kernel
+    // (both give the same bits)
+    h->attn_tma = !force_fused && !force_tiled && !force_mma && d.max_pos > 256 &&
+                  attn_tma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, d.page_size,
+                                    h->split_len, h->max_splits);
+    if (h->attn_tma) {
+      const int64_t rows = (int64_t)d.n_layers * (h->kv.layer_stride / d.head_dim);
+      if (attn_tma_make_map(h->kv.k, rows, d.head_dim, d.page_size, &h->tm_kv_k) ||
+          attn_tma_make_map(h->kv.v, rows, d.head_dim, d.page_size, &h->tm_kv_v))
+        h->attn_tma = false;  // arena too large for 32-bit rows: the cp.async kernel serves
+    }
   }
   FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
@@ -464,11 +491,6 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   *h->err_flag = 0;
   FS_CK(h, cudaHostGetDevicePointer((void**)&h->d_err_flag, h->err_flag, 0));
   if (h->use_tc) {
-    {
-      int dev = 0;
-      FS_CK(h, cudaGetDevice(&dev));
-      FS_CK(h, cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev));
-    }
     size_t ws_elems = 0;
     int max_tiles = 1;
     auto setup = [&](const Mat& m, TcW* t) -> int {
@@ -638,7 +660,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                               h->xtype, h->Kp_d, s);
       });
     gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
-    if (h->attn_tiled) {
+    if (h->attn_tma || h->attn_mma || h->attn_tiled) {
       AttnParams ap{};
       ap.qkv = h->qkv; ap.H = d.n_heads; ap.rc = h->rope_cos; ap.rs = h->rope_sin;
       ap.args = args; ap.kv = h->kv; ap.layer = l; ap.split_len = h->split_len;
@@ -647,6 +669,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs),
                 [&] {
+                  if (h->attn_tma)
+                    return launch_attention_tma(h->tm_kv_k, h->tm_kv_v, ap, n, h->xtype, s);
                   return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
                                      : launch_attention_tiled(ap, n, h->xtype, s);
                 });
@@ -1035,6 +1059,15 @@ const char* fs_gemm_path(const fs_handle* h) {
   if (!h) return "";
   if (!h->use_tc) return "warp-gemv";
   return h->wtype == W_Q8 ? "tcgen05-q8_0" : "tcgen05";
+}
+
+const char* fs_attention_path(const fs_handle* h) {
+  if (!h) return "";
+  if (h->attn_tma) return "tma-mma";
+  if (h->attn_mma) return "cp.async-mma";
+  if (h->attn_tiled) return "tiled";
+  if (h->attn_fused) return "fused";
+  return "three-kernel";
 }
 
 int fs_device_error(fs_handle* h, int32_t* code_out) {

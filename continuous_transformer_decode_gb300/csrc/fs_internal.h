@@ -205,6 +205,13 @@ struct AttnParams {
 };
 bool attn_tiled_supports(int hd, int G, int page_size, int split_len);
 bool attn_mma_supports(int hd, int G, int kv_f32, int split_len, int max_splits);
+// Same attention with the KV tiles fetched by TMA (k_attn_tma.cu): bf16 KV,
+// page_size a multiple of 8 that divides or is a multiple of 64.
+bool attn_tma_supports(int hd, int G, int kv_f32, int page_size, int split_len,
+                       int max_splits);
+int attn_tma_make_map(const void* arena, int64_t rows, int hd, int page_size, CUtensorMap* out);
+int launch_attention_tma(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& a,
+                         int B, int x_type, cudaStream_t s);
 int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s);
 int launch_attention_tiled(const AttnParams& a, int B, int x_type, cudaStream_t s);
 

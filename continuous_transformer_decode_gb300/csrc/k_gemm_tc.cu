@@ -36,9 +36,12 @@
 #include <cstdlib>
 
 #include "fs_internal.h"
+#include "tma_mbar.cuh"
 
 namespace fsk {
 namespace {
+
+using namespace tma;
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                 // bf16 elements per 128-byte row
@@ -50,50 +53,9 @@ constexpr int kQ8Codes = kBM * kBK;        // 8 KB
 constexpr int kQ8Scales = kBM * 2 * 2;     // 512 B
 constexpr int kQ8XOff = 25 * 1024;         // 16 + 8 + 0.5 KB, 1 KB aligned
 constexpr int kXbufBytes = 64 * 17 * 4 + 256;  // SwiGLU gate/up exchange, 8-byte aligned end
-constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
-  while (!mbar_test(bar, parity))
-    if (gtimer() - t0 > kWaitNs) return false;
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x,
-                                            int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
-      : "memory");
 }
 // K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 B
 // apart (stride byte offset), descriptor version 1, layout SWIZZLE_128B (2).
@@ -114,9 +76,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           dst),
       "l"((uint64_t)src), "r"(bytes), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -392,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mbar_init(tfull, 1);     // the MMA issuer's commit at the end of a piece
     mbar_init(tempty, 128);  // every epilogue thread, after reading TMEM
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
     s_abort = 0;
     s_last = 0;
   }
@@ -525,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
           }
           dequant_q8_tile(smem + (size_t)s * p.stage_bytes, row_local);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+          fence_proxy_async_smem();  // visible to the MMA
           mbar_arrive(conv0 + 8 * s);
         }
       }

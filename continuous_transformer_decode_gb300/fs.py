@@ -107,6 +107,7 @@ def lib():
         "fs_profile_read": (C.c_int, [p, i32, p, p, p]),
         "fs_kernel_launches": (C.c_int, [p, p]),
         "fs_gemm_path": (C.c_char_p, [p]),
+        "fs_attention_path": (C.c_char_p, [p]),
         "fs_device_error": (C.c_int, [p, p]),
         "fs_copy_logits": (C.c_int, [p, p]),
         "fs_gemm_bf16_noalloc": (C.c_int, [p, i32, i32, p, i32, p, i32, p]),
@@ -139,7 +140,7 @@ def exported_symbols() -> list:
             "fs_lane_reset", "fs_decode_step_batch", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
-            "fs_kernel_launches", "fs_gemm_path", "fs_sample_device",
+            "fs_kernel_launches", "fs_gemm_path", "fs_attention_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
             "fs_gemm_bf16", "fs_gemm_bf16_width", "fs_gemm_bf16_time", "fs_copy_logits", "fs_gemm_bf16_noalloc",
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
@@ -319,6 +320,10 @@ def fs_kernel_launches(h) -> int:
 
 def fs_gemm_path(h) -> str:
     return lib().fs_gemm_path(h).decode()
+
+
+def fs_attention_path(h) -> str:
+    return lib().fs_attention_path(h).decode()
 
 
 def fs_device_error(h) -> int:

@@ -240,6 +240,14 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out);
  * path for bf16 weights too (a comparison point). */
 const char* fs_gemm_path(const fs_handle* h);
 
+/* Name of the decode-attention kernel serving the handle: "tma-mma" (KV
+ * tiles by TMA, warp MMAs; bf16 KV, page_size a multiple of 8 that divides
+ * or is a multiple of 64), "cp.async-mma" (KV tiles by cp.async, warp MMAs;
+ * bf16 KV), "tiled", "fused" or "three-kernel" (the f32-KV and odd-shape
+ * paths). The environment variable FS_ATTN=mma|tiled|fused, read by
+ * fs_create, selects a slower kernel (a comparison point). */
+const char* fs_attention_path(const fs_handle* h);
+
 /* Synchronises the stream, returns the handle's device error code (0: none;
  * non-zero: a kernel gave up on a bounded wait) and clears it. fs_sample
  * reports a set code as FS_ERR_DEVICE. */
