@@ -5,24 +5,25 @@
 // G query heads of one KV head over the lane's own keys 0..pos, split-K with
 // an ordered merge; "MODEL-BATCHING-RESULTS", "The lever"; mlx-bun "Parallel
 // slots", "KV memory" rung 3; "S1b decode: design traps" trap 2), with the
-// same warp-level MMA arithmetic, but the key and value tiles reach shared
+// same warp-level MMA arithmetic, but the key and value rows reach shared
 // memory through the tensor memory accelerator:
 //   * the KV arena [layer][page][Hkv][page_size][hd] is a 2-D tensor of
 //     rows (layer, page, head, slot) x hd columns, so the rows of one
-//     lane's page for one KV head are one contiguous run; a tile of 64
-//     positions is a few box copies (one per page run and 64-column block)
-//     with 128-byte swizzle, instead of thousands of 16-byte copies;
-//   * warp 4 issues the copies (the split's page indices are read into
-//     shared memory once), kStages tiles in flight on full/empty mbarrier
-//     rings; warps 0-3 consume, each zeroing the value rows of its own 16
-//     positions past the lane's length (a page's unused rows hold stale
-//     data) and writing the token appended at pos into the tile from
-//     registers, so the loop needs no block-wide barrier;
-//   * per tile, warp w owns positions 16w..16w+15: S = Q K^T and O += P V
-//     on mma.m16n8k16 with q and P split into hi + lo bf16 parts (rows g and
-//     g + 8 of the A operand), a per-warp online softmax; the warps' and then
-//     the splits' (m, l, O) are merged in a fixed order, so a lane's result
-//     does not depend on the batch.
+//     lane's page for one KV head are one contiguous run, copied as boxes of
+//     16 rows x 64 columns with 128-byte swizzle (the split's page indices
+//     are read into shared memory once);
+//   * each of the 4 warps owns rows 16w..16w+15 of every 64-position tile
+//     and runs its own ring of 3 slices on its own mbarriers: its lanes issue
+//     the slice's copies together (a thread's copies are served one after
+//     another, so independent issuers are what keeps several in flight), it
+//     zeroes its value rows past the lane's length (a page's unused rows
+//     hold stale data), writes the token appended at pos from registers,
+//     and refills the slot when done, with no block-wide barrier in the
+//     loop;
+//   * per slice: S = Q K^T and O += P V on mma.m16n8k16 with q and P split
+//     into hi + lo bf16 parts (rows g and g + 8 of the A operand), a per-warp
+//     online softmax; the warps' and then the splits' (m, l, O) are merged in
+//     a fixed order, so a lane's result does not depend on the batch.
 
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -38,28 +39,34 @@ namespace {
 using namespace attn;
 using namespace tma;
 
-constexpr int kWarps = 4;             // consumer warps; warp 4 is the producer
-constexpr int kT = 32 * (kWarps + 1);
-constexpr int kMaxRuns = 64;          // page runs per split (split_len / min(page_size, 64))
-constexpr int kTT = 64;      // positions per tile
-constexpr int kG = 8;        // max query heads per KV head
-constexpr int kStages = 3;   // tiles in flight per block
+constexpr int kWarps = 4;
+constexpr int kT = 32 * kWarps;
+constexpr int kTT = 64;       // positions per tile; warp w owns rows 16w..16w+15
+constexpr int kG = 8;         // max query heads per KV head
+constexpr int kMaxRuns = 64;  // page runs per split (split_len / min(page_size, 16))
 
-// Byte offset of (row, 16-byte chunk) in a tile laid out as [HD / 64]
-// column blocks of [kTT rows][128 bytes], each written by TMA with 128-byte
-// swizzle (chunk c of row r at (c ^ (r % 8)) * 16 within the row).
-__device__ __forceinline__ uint32_t swt(int row, int chunk) {
-  return (uint32_t)((chunk >> 3) * (kTT * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+template <int HD>
+struct Ring {
+  static constexpr int kBlocks = HD / 64;          // 128-byte column blocks
+  static constexpr int kSlice = 16 * HD * 2;       // one of K or V for 16 rows
+  static constexpr int kStages = 3;                // slices in flight per warp
+  static constexpr int kWarpBytes = kStages * 2 * kSlice;
+};
+
+// Byte offset of (row r < 16, 16-byte chunk) in a 16-row slice laid out as
+// [HD / 64] column blocks of [16 rows][128 bytes], each written by TMA with
+// 128-byte swizzle (chunk c of row r at (c ^ (r % 8)) * 16 within the row).
+__device__ __forceinline__ uint32_t sws(int r, int chunk) {
+  return (uint32_t)((chunk >> 3) * 2048 + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
 }
 
 template <typename OT, int HD>
-__global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2) k_attn_tma(const __grid_constant__ CUtensorMap tmK,
-                                                 const __grid_constant__ CUtensorMap tmV,
-                                                 AttnParams a) {
+__global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
+    k_attn_tma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               AttnParams a) {
+  using R = Ring<HD>;
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
-  constexpr int kBlocks = HD / 64;       // 128-byte column blocks
-  constexpr int kTileBytes = kTT * HD * 2;
   constexpr int kKs = HD / 16;           // k-steps of Q K^T
   constexpr int kNt = HD / 8;            // n-tiles of P V
   const KV& kv = a.kv;
@@ -78,23 +85,22 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2) k_attn_tma(const __grid
   __nv_bfloat16* Vg = static_cast<__nv_bfloat16*>(kv.v);
   const bool owns_pos = (s == ns - 1);
   const int64_t layer_row0 = (int64_t)a.layer * (kv.layer_stride / HD);
-  const int box = min(ps, kTT);  // rows per copy: one page, or 64 rows of one
+  const int box = min(ps, 16);  // rows per copy: one page, or 16 rows of one
 
   extern __shared__ uint8_t smem_raw[];
-  // tiles 1 KB aligned: the 128-byte swizzle pattern repeats every 8 rows
+  // rings 1 KB aligned: the 128-byte swizzle pattern repeats every 8 rows
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* Kt = smem;                               // [kStages] tiles
-  uint8_t* Vt = smem + kStages * kTileBytes;
-  float* qs = reinterpret_cast<float*>(smem + 2 * kStages * kTileBytes);  // [kG][HD]
+  uint8_t* ring = smem + warp * R::kWarpBytes;      // this warp's [kStages][K | V] slices
+  float* qs = reinterpret_cast<float*>(smem + kWarps * R::kWarpBytes);  // [kG][HD]
   float* knew = qs + kG * HD;                       // [HD]
   float* vnew = knew + HD;
   float* wm = vnew + HD;                            // [kWarps][kG]
   float* wl = wm + kWarps * kG;
-  uint64_t* full = reinterpret_cast<uint64_t*>(wl + kWarps * kG);  // [kStages]
-  uint64_t* empty = full + kStages;                                 // [kStages]
-  int* srow = reinterpret_cast<int*>(empty + kStages);              // [kMaxRuns]
-  float* wo = reinterpret_cast<float*>(smem);       // [kWarps][kG][HD], reuses the idle tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(wl + kWarps * kG);  // [kWarps][kStages]
+  int* srow = reinterpret_cast<int*>(full + kWarps * R::kStages);  // [kMaxRuns]
+  float* wo = reinterpret_cast<float*>(smem);       // [kWarps][kG][HD], reuses the idle rings
+  uint64_t* my_full = full + warp * R::kStages;
   __shared__ int s_last;
 
   const int n_tiles = (end - start + kTT - 1) / kTT;
@@ -105,205 +111,192 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2) k_attn_tma(const __grid
     srow[r] = (int)(layer_row0 + ((int64_t)ptrow[pi] * Hkv + g) * ps + slot);
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(full + i), 1);
-      mbar_init(smem_u32(empty + i), kWarps);  // one arrival per consumer warp
-    }
+    for (int i = 0; i < kWarps * R::kStages; ++i) mbar_init(smem_u32(full + i), 1);
     mbar_init_fence();
   }
   __syncthreads();
-  if (warp == kWarps) {  // ---- producer
-    if (lane == 0) {
-      // Programmatic dependent launch: the KV of earlier positions and the
-      // page table were written by kernels that finished before the
-      // predecessor started, so copies start before waiting for it.
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages &&
-            !mbar_wait(smem_u32(empty + st), (uint32_t)((i / kStages) - 1) & 1u)) {
-          atomicExch(a.err, 8);
-          break;  // the consumers time out on this tile's full barrier
-        }
-        const int cnt = min(kTT, end - (start + i * kTT));
-        const int runs = (cnt + box - 1) / box;
-        const uint32_t bar = smem_u32(full + st);
-        mbar_expect_tx(bar, (uint32_t)(2 * runs * box * HD * 2));
-        const uint32_t kd = smem_u32(Kt + st * kTileBytes), vd = smem_u32(Vt + st * kTileBytes);
-        const int r0 = i * (kTT / box);
-        for (int r = 0; r < runs; ++r) {
-#pragma unroll
-          for (int cb = 0; cb < kBlocks; ++cb) {
-            const uint32_t off = (uint32_t)(cb * kTT * 128 + r * box * 128);
-            tma_load_2d(kd + off, &tmK, cb * 64, srow[r0 + r], bar);
-            tma_load_2d(vd + off, &tmV, cb * 64, srow[r0 + r], bar);
-          }
-        }
-      }
+  const int p0 = warp * 16;  // this warp's rows in every tile
+  // this warp's slice of tile i: `cnt` valid rows (0 when past the end)
+  auto slice_rows = [&](int i) { return max(0, min(16, end - (start + i * kTT + p0))); };
+  // lanes 0..: copy the runs of this warp's slice of tile i into stage i % kStages
+  auto issue = [&](int i) {
+    const int st = i % R::kStages;
+    const int cnt = slice_rows(i);
+    if (cnt == 0) return;
+    const int runs = (cnt + box - 1) / box;
+    const uint32_t bar = smem_u32(my_full + st);
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(2 * runs * box * HD * 2));
+    __syncwarp();
+    const int n_copies = 2 * runs * R::kBlocks;   // <= 16
+    if (lane < n_copies) {
+      const int kvsel = lane & 1, rest = lane >> 1;
+      const int cb = rest % R::kBlocks, r = rest / R::kBlocks;
+      const uint32_t dst = smem_u32(ring + st * 2 * R::kSlice + kvsel * R::kSlice) +
+                           (uint32_t)(cb * 2048 + r * box * 128);
+      const int run = (i * kTT + p0) / box + r;
+      tma_load_2d(dst, kvsel ? &tmV : &tmK, cb * 64, srow[run], bar);
     }
-    // the producer reads nothing the predecessor writes: no dependency wait
+  };
+  // Programmatic dependent launch: the KV of earlier positions and the page
+  // table were written by kernels that finished before the predecessor
+  // started, so each warp's first copies start before waiting for it.
+  for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
+  pdl_wait();  // the QKV projection's output is read below
+  pdl_trigger();
+
+  // ---- rotated queries; the owner of pos also rotates k and appends k, v
+  const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
+  const float* c = a.rc + (int64_t)pos * kHalf;
+  const float* sn = a.rs + (int64_t)pos * kHalf;
+  for (int idx = tid; idx < kG * kHalf; idx += kT) {
+    const int h = idx / kHalf, i = idx - h * kHalf;
+    float q0 = 0.0f, q1 = 0.0f;
+    if (h < G) {
+      const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
+      q0 = x0 * c[i] - x1 * sn[i];
+      q1 = x1 * c[i] + x0 * sn[i];
+    }
+    qs[h * HD + i] = q0;
+    qs[h * HD + i + kHalf] = q1;
+  }
+  if (owns_pos) {
+    const float* kr = row + H * HD + g * HD;
+    const float* vr = row + (H + Hkv) * HD + g * HD;
+    const int pi = pos / ps, slot = pos - pi * ps;
+    const int64_t off = (int64_t)a.layer * kv.layer_stride +
+                        (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
+    for (int i = tid; i < kHalf; i += kT) {
+      const float x0 = kr[i], x1 = kr[i + kHalf];
+      const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
+      Kg[off + i] = __float2bfloat16_rn(k0);
+      Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
+      knew[i] = k0;
+      knew[i + kHalf] = k1;
+    }
+    for (int i = tid; i < HD; i += kT) {
+      Vg[off + i] = __float2bfloat16_rn(vr[i]);
+      vnew[i] = vr[i];
+    }
+  }
+  __syncthreads();
+
+  // Q as bf16 A fragments: row gq = hi part of head gq, row gq + 8 = its lo
+  // part (heads >= G are zero)
+  uint32_t qa[kKs][4];
+#pragma unroll
+  for (int ks = 0; ks < kKs; ++ks) {
+    const int c0 = ks * 16 + 2 * cq;
+    const float* q = qs + gq * HD;
+    split_bf16(q[c0], q[c0 + 1], qa[ks][0], qa[ks][1]);
+    split_bf16(q[c0 + 8], q[c0 + 9], qa[ks][2], qa[ks][3]);
   }
 
-  constexpr int kC = 32 * kWarps;  // consumer threads
   const float scale = 1.0f / sqrtf((float)HD);
   float m_run = -CUDART_INF_F, l_run = 0.0f;  // head gq, this warp's positions
   float o_acc[kNt][4];
 #pragma unroll
   for (int j = 0; j < kNt; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.0f;
-  uint32_t qa[kKs][4];
-  if (warp < kWarps) {
-    pdl_wait();  // the QKV projection's output is read below
-    pdl_trigger();
-    // ---- rotated queries; the owner of pos also rotates k and appends k, v
-    const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
-    const float* c = a.rc + (int64_t)pos * kHalf;
-    const float* sn = a.rs + (int64_t)pos * kHalf;
-    for (int idx = tid; idx < kG * kHalf; idx += kC) {
-      const int h = idx / kHalf, i = idx - h * kHalf;
-      float q0 = 0.0f, q1 = 0.0f;
-      if (h < G) {
-        const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
-        q0 = x0 * c[i] - x1 * sn[i];
-        q1 = x1 * c[i] + x0 * sn[i];
-      }
-      qs[h * HD + i] = q0;
-      qs[h * HD + i + kHalf] = q1;
-    }
-    if (owns_pos) {
-      const float* kr = row + H * HD + g * HD;
-      const float* vr = row + (H + Hkv) * HD + g * HD;
-      const int pi = pos / ps, slot = pos - pi * ps;
-      const int64_t off = (int64_t)a.layer * kv.layer_stride +
-                          (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
-      for (int i = tid; i < kHalf; i += kC) {
-        const float x0 = kr[i], x1 = kr[i + kHalf];
-        const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
-        Kg[off + i] = __float2bfloat16_rn(k0);
-        Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
-        knew[i] = k0;
-        knew[i + kHalf] = k1;
-      }
-      for (int i = tid; i < HD; i += kC) {
-        Vg[off + i] = __float2bfloat16_rn(vr[i]);
-        vnew[i] = vr[i];
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kC) : "memory");  // the consumer warps only
-    // Q as bf16 A fragments: row gq = hi part of head gq, row gq + 8 = its
-    // lo part (heads >= G are zero)
-#pragma unroll
-    for (int ks = 0; ks < kKs; ++ks) {
-      const int c0 = ks * 16 + 2 * cq;
-      const float* q = qs + gq * HD;
-      split_bf16(q[c0], q[c0 + 1], qa[ks][0], qa[ks][1]);
-      split_bf16(q[c0 + 8], q[c0 + 9], qa[ks][2], qa[ks][3]);
-    }
-  }
 
+  const int mi = lane >> 3, ri = lane & 7;
   bool failed = false;
-  if (warp < kWarps) {
-    const int p0 = warp * 16;  // this warp's positions in every tile
-    const int mi = lane >> 3, ri = lane & 7;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kStages;
-      const int t0 = start + i * kTT;
-      const int cnt = min(kTT, end - t0);
-      uint8_t* kb = Kt + st * kTileBytes;
-      uint8_t* vb = Vt + st * kTileBytes;
-      if (!mbar_wait(smem_u32(full + st), (uint32_t)(i / kStages) & 1u)) {
-        atomicExch(a.err, 7);
-        failed = true;
-        break;
-      }
-      if (p0 < cnt) {
-        // value rows of this warp's positions past the lane's length: zeros
-        if (p0 + 16 > cnt)
-          for (int idx = lane; idx < (p0 + 16 - cnt) * kCh; idx += 32) {
-            const int r = cnt + idx / kCh, ch = idx % kCh;
-            *reinterpret_cast<uint4*>(vb + swt(r, ch)) = make_uint4(0, 0, 0, 0);
-          }
-        if (owns_pos && pos >= t0 + p0 && pos < t0 + p0 + 16) {  // the appended token
-          const int r = pos - t0;
-          for (int ch = lane; ch < kCh; ch += 32) {
-            uint4 kk, vv;
-            uint32_t* kw = reinterpret_cast<uint32_t*>(&kk);
-            uint32_t* vw = reinterpret_cast<uint32_t*>(&vv);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              kw[e] = pack_bf16(knew[ch * 8 + 2 * e], knew[ch * 8 + 2 * e + 1]);
-              vw[e] = pack_bf16(vnew[ch * 8 + 2 * e], vnew[ch * 8 + 2 * e + 1]);
-            }
-            *reinterpret_cast<uint4*>(kb + swt(r, ch)) = kk;
-            *reinterpret_cast<uint4*>(vb + swt(r, ch)) = vv;
-          }
-        }
-        __syncwarp();
-        // S = Q K^T for positions p0 .. p0+15 (two n-tiles of 8)
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int ks = 0; ks < kKs; ++ks) {
-          uint32_t bk[4];
-          const int rr = p0 + (mi >> 1) * 8 + ri, ch = 2 * ks + (mi & 1);
-          ldsm_x4(smem_u32(kb + swt(rr, ch)), bk);
-          mma16816(sacc[0], qa[ks], bk[0], bk[1]);
-          mma16816(sacc[1], qa[ks], bk[2], bk[3]);
-        }
-        // online softmax over this warp's positions, per head (row gq)
-        float sv[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int pp = p0 + nt * 8 + 2 * cq + e;
-            sv[nt * 2 + e] = pp < cnt ? (sacc[nt][e] + sacc[nt][2 + e]) * scale : -CUDART_INF_F;
-          }
-        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(m_run, mx);
-        const float alpha = (m_run == -CUDART_INF_F) ? 0.0f : expf(m_run - mnew);
-        float pv[4], psum = 0.0f;
+  for (int i = 0; i < n_tiles; ++i) {
+    const int cnt = slice_rows(i);
+    if (cnt == 0) break;  // past the end: so are all later slices of this warp
+    const int st = i % R::kStages;
+    uint8_t* kb = ring + st * 2 * R::kSlice;
+    uint8_t* vb = kb + R::kSlice;
+    const bool ok = mbar_wait(smem_u32(my_full + st), (uint32_t)(i / R::kStages) & 1u);
+    if (!__all_sync(0xffffffffu, ok)) {  // uniform over the warp
+      if (lane == 0) atomicExch(a.err, 7);
+      failed = true;
+      break;
+    }
+    // value rows past the lane's length: zeros (stale page rows)
+    for (int idx = lane; idx < (16 - cnt) * kCh; idx += 32) {
+      const int r = cnt + idx / kCh, ch = idx % kCh;
+      *reinterpret_cast<uint4*>(vb + sws(r, ch)) = make_uint4(0, 0, 0, 0);
+    }
+    const int t0 = start + i * kTT + p0;
+    if (owns_pos && pos >= t0 && pos < t0 + 16) {  // the appended token, from registers
+      const int r = pos - t0;
+      for (int ch = lane; ch < kCh; ch += 32) {
+        uint4 kk, vv;
+        uint32_t* kw = reinterpret_cast<uint32_t*>(&kk);
+        uint32_t* vw = reinterpret_cast<uint32_t*>(&vv);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pv[e] = (sv[e] == -CUDART_INF_F) ? 0.0f : expf(sv[e] - mnew);
-          psum += pv[e];
+          kw[e] = pack_bf16(knew[ch * 8 + 2 * e], knew[ch * 8 + 2 * e + 1]);
+          vw[e] = pack_bf16(vnew[ch * 8 + 2 * e], vnew[ch * 8 + 2 * e + 1]);
         }
-        psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-        l_run = l_run * alpha + psum;
-        m_run = mnew;
-#pragma unroll
-        for (int j = 0; j < kNt; ++j) {  // both the hi and the lo accumulators
-          o_acc[j][0] *= alpha;
-          o_acc[j][1] *= alpha;
-          o_acc[j][2] *= alpha;
-          o_acc[j][3] *= alpha;
-        }
-        // O += P V; P's A fragment: positions 2cq..2cq+1 (n-tile 0) and +8,
-        // hi parts in row gq, lo parts in row gq + 8
-        uint32_t pa[4];
-        split_bf16(pv[0], pv[1], pa[0], pa[1]);
-        split_bf16(pv[2], pv[3], pa[2], pa[3]);
-#pragma unroll
-        for (int j = 0; j < kNt; j += 2) {
-          uint32_t bv[4];
-          const int rr = p0 + (mi & 1) * 8 + ri, ch = j + (mi >> 1);
-          ldsm_x4_t(smem_u32(vb + swt(rr, ch)), bv);
-          mma16816(o_acc[j], pa, bv[0], bv[1]);
-          mma16816(o_acc[j + 1], pa, bv[2], bv[3]);
-        }
+        *reinterpret_cast<uint4*>(kb + sws(r, ch)) = kk;
+        *reinterpret_cast<uint4*>(vb + sws(r, ch)) = vv;
       }
-      // this warp is done with stage st: its generic stores come before the
-      // producer's next copy into it
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + st));
     }
+    __syncwarp();
+    // S = Q K^T for the slice's 16 positions (two n-tiles of 8)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < kKs; ++ks) {
+      uint32_t bk[4];
+      ldsm_x4(smem_u32(kb + sws((mi >> 1) * 8 + ri, 2 * ks + (mi & 1))), bk);
+      mma16816(sacc[0], qa[ks], bk[0], bk[1]);
+      mma16816(sacc[1], qa[ks], bk[2], bk[3]);
+    }
+    // online softmax over this warp's positions, per head (row gq)
+    float sv[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int pp = nt * 8 + 2 * cq + e;
+        sv[nt * 2 + e] = pp < cnt ? (sacc[nt][e] + sacc[nt][2 + e]) * scale : -CUDART_INF_F;
+      }
+    float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mnew = fmaxf(m_run, mx);
+    const float alpha = (m_run == -CUDART_INF_F) ? 0.0f : expf(m_run - mnew);
+    float pv[4], psum = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pv[e] = (sv[e] == -CUDART_INF_F) ? 0.0f : expf(sv[e] - mnew);
+      psum += pv[e];
+    }
+    psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+    psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+    l_run = l_run * alpha + psum;
+    m_run = mnew;
+#pragma unroll
+    for (int j = 0; j < kNt; ++j) {  // both the hi and the lo accumulators
+      o_acc[j][0] *= alpha;
+      o_acc[j][1] *= alpha;
+      o_acc[j][2] *= alpha;
+      o_acc[j][3] *= alpha;
+    }
+    // O += P V; P's A fragment: positions 2cq..2cq+1 (n-tile 0) and +8,
+    // hi parts in row gq, lo parts in row gq + 8
+    uint32_t pa[4];
+    split_bf16(pv[0], pv[1], pa[0], pa[1]);
+    split_bf16(pv[2], pv[3], pa[2], pa[3]);
+#pragma unroll
+    for (int j = 0; j < kNt; j += 2) {
+      uint32_t bv[4];
+      ldsm_x4_t(smem_u32(vb + sws((mi & 1) * 8 + ri, j + (mi >> 1))), bv);
+      mma16816(o_acc[j], pa, bv[0], bv[1]);
+      mma16816(o_acc[j + 1], pa, bv[2], bv[3]);
+    }
+    // refill this stage with slice i + kStages: the stores and shared-memory
+    // reads above come before the copy's writes
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (i + R::kStages < n_tiles) issue(i + R::kStages);
   }
   if (__syncthreads_or(failed)) {
-    // a consumer gave up: let the copies in flight land (bounded), then exit
-    if (tid == 0)
-      for (int i = max(0, n_tiles - kStages); i < n_tiles; ++i)
-        mbar_wait(smem_u32(full + i % kStages), (uint32_t)(i / kStages) & 1u);
+    // a warp gave up: let every copy in flight land (bounded), then exit
+    if (lane == 0)
+      for (int i = 0; i < n_tiles; ++i)
+        if (slice_rows(i) > 0)
+          mbar_wait(smem_u32(my_full + i % R::kStages), (uint32_t)(i / R::kStages) & 1u);
     __syncthreads();
     return;
   }
@@ -405,16 +398,16 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2) k_attn_tma(const __grid
 
 template <int HD>
 constexpr size_t smem_bytes() {
-  return 1024 + 2 * (size_t)kStages * kTT * HD * 2 +
-         sizeof(float) * ((size_t)kG * HD + 2 * HD + 2 * kWarps * kG) + 16 * kStages +
-         sizeof(int) * kMaxRuns;
+  return 1024 + (size_t)kWarps * Ring<HD>::kWarpBytes +
+         sizeof(float) * ((size_t)kG * HD + 2 * HD + 2 * kWarps * kG) +
+         8 * (size_t)kWarps * Ring<HD>::kStages + sizeof(int) * kMaxRuns;
 }
 
 template <typename OT, int HD>
 int launch_hd(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& a, int B,
               cudaStream_t s) {
-  static_assert(kWarps * kG * HD * sizeof(float) <= 2 * (size_t)kStages * kTT * HD * 2,
-                "the warp-merge buffer must fit in the tile buffers");
+  static_assert(kWarps * kG * HD * sizeof(float) <= (size_t)kWarps * Ring<HD>::kWarpBytes,
+                "the warp-merge buffer must fit in the rings");
   constexpr size_t smem = smem_bytes<HD>();
   static bool attr = false;
   if (!attr) {
@@ -443,16 +436,19 @@ int dispatch(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& a
 bool attn_tma_supports(int hd, int G, int kv_f32, int page_size, int split_len,
                        int max_splits) {
   if (kv_f32 || !(hd == 64 || hd == 128 || hd == 256) || G < 1 || G > kG) return false;
-  // a copy is one page (page_size | 64) or 64 rows of one (64 | page_size),
+  // a copy is one page (page_size | 16) or 16 rows of one (16 | page_size),
   // a whole number of 8-row swizzle atoms
-  const bool runs = (page_size % 8 == 0) && (kTT % page_size == 0 || page_size % kTT == 0);
+  const bool runs = (page_size % 8 == 0) && (16 % page_size == 0 || page_size % 16 == 0);
+  const size_t ring_bytes = hd == 64 ? (size_t)kWarps * Ring<64>::kWarpBytes
+                            : hd == 128 ? (size_t)kWarps * Ring<128>::kWarpBytes
+                                        : (size_t)kWarps * Ring<256>::kWarpBytes;
   const size_t merge_bytes = (size_t)(2 * kG * max_splits + kG) * sizeof(float);
-  return runs && split_len % kTT == 0 && split_len / std::min(page_size, kTT) <= kMaxRuns &&
-         merge_bytes <= 2 * (size_t)kStages * kTT * hd * 2;
+  return runs && split_len % kTT == 0 && split_len / std::min(page_size, 16) <= kMaxRuns &&
+         merge_bytes <= ring_bytes;
 }
 
 // 2-D map over a KV arena [rows][hd] bf16 (rows = layers * pages * Hkv *
-// page_size), box [min(page_size, 64) rows][64 columns], 128-byte swizzle.
+// page_size), box [min(page_size, 16) rows][64 columns], 128-byte swizzle.
 int attn_tma_make_map(const void* arena, int64_t rows, int hd, int page_size, CUtensorMap* out) {
   if (!tc_available() || rows >= ((int64_t)1 << 31)) return -1;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -467,7 +463,7 @@ int attn_tma_make_map(const void* arena, int64_t rows, int hd, int page_size, CU
   }
   cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)std::min(page_size, kTT)};
+  cuuint32_t box[2] = {64, (cuuint32_t)std::min(page_size, 16)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(arena), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
