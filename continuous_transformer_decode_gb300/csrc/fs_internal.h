@@ -117,6 +117,7 @@ struct TcParams {
   int tmem_cols;   // power of two >= max(32, lg)
   int sms;         // SMs of the device (stage budget: one or two blocks per SM)
   int stages, stage_bytes;  // set by the launcher
+  int prod_warps;  // TMA-issuing warps of single-piece blocks (set by the launcher)
   int epi;
   float* out_f32;
   void* out_x;

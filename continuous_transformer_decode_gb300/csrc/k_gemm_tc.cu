@@ -366,68 +366,86 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  // Programmatic dependent launch: the weight tiles do not depend on the
-  // predecessor kernel, so the producer starts them before waiting for it;
-  // the panel loads and every other global access come after the wait.
-  if (!(warp == 4 && lane == 0)) {
+  // TMA producers. A thread's copies are served one after another, so a block
+  // holding a single piece (whole tile, or one K split of one) lets its 4
+  // epilogue warps, idle until the accumulator is ready, issue the stages
+  // congruent to their index; otherwise warp 4 issues every stage (the
+  // epilogue warps then drain pieces while it keeps the ring full).
+  const int npw = p.prod_warps;  // divides S
+  const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
+  // warp-collective: lane 0 issues iterations first, first + step, ...
+  auto produce = [&](int first, int step) {
+    int issued = -1;  // last iteration issued
+    auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
+      const int s = i % S;
+      const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+      const int g = g0 + i;  // = m_tile * kb_total + kb
+      if (kQ8) {
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
+        bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
+                  full0 + 8 * s);
+        bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + (int64_t)g * (kQ8Scales / 2),
+                  kQ8Scales, full0 + 8 * s);
+      } else {
+        const int tile = g / kbt;
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
+        tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
+      }
+    };
+    auto load_x = [&](int i) {  // panel part of stage i
+      const int s = i % S;
+      const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+      const int x = ((g0 + i) % kbt) * kBK;
+      int r = 0;
+      for (; r + 64 <= n_tot; r += 64)
+        tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
+      for (; r < n_tot; r += kXBoxRows)
+        tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
+    };
+    // Programmatic dependent launch: the weight tiles do not depend on the
+    // predecessor kernel, so they start before waiting for it; the panel is
+    // the predecessor's output.
+    const int pre = min(S, n_it);  // stages are empty at start: no wait needed
+    if (lane == 0)
+      for (int i = first; i < pre; i += step) load_w(i);
+    pdl_wait();
+    pdl_trigger();
+    for (int i = first; i < pre; i += step) {
+      if (lane == 0) load_x(i);
+      issued = i;
+    }
+    for (int i = first + ((pre - first + step - 1) / step) * step; i < n_it; i += step) {
+      const int s = i % S;
+      const uint32_t ph = (uint32_t)(i / S) & 1u;
+      const bool ok = mbar_wait(empty0 + 8 * s, ph ^ 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          atomicExch(p.err, 1);
+          s_abort = 1;
+        }
+        break;
+      }
+      if (__shfl_sync(0xffffffffu, *(volatile int*)&s_abort, 0)) break;
+      if (lane == 0) {
+        load_w(i);
+        load_x(i);
+      }
+      issued = i;
+    }
+    // drain: every copy issued here must have landed before the block exits
+    for (int i = issued; i >= 0 && i > issued - S; i -= step) {
+      const int s = i % S;
+      if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u) && lane == 0) atomicExch(p.err, 2);
+    }
+  };
+  const bool early = warp_prod ? warp < npw : warp == 4;  // producers wait inside produce
+  if (!early) {
     pdl_wait();
     pdl_trigger();
   }
 
   if (warp == 4) {
-    if (lane == 0) {  // ---- TMA producer: the block's k-blocks in order
-      int issued = 0;
-      auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
-        const int s = i % S;
-        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const int g = g0 + i;  // = m_tile * kb_total + kb
-        if (kQ8) {
-          mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
-          bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
-                    full0 + 8 * s);
-          bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + (int64_t)g * (kQ8Scales / 2),
-                    kQ8Scales, full0 + 8 * s);
-        } else {
-          const int tile = g / kbt;
-          mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
-          tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
-        }
-      };
-      auto load_x = [&](int i) {  // panel part of stage i
-        const int s = i % S;
-        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const int x = ((g0 + i) % kbt) * kBK;
-        int r = 0;
-        for (; r + 64 <= n_tot; r += 64)
-          tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
-        for (; r < n_tot; r += kXBoxRows)
-          tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
-      };
-      const int pre = min(S, n_it);  // stages are empty at start: no wait needed
-      for (int i = 0; i < pre; ++i) load_w(i);
-      pdl_wait();  // the panel is the predecessor's output
-      pdl_trigger();
-      for (int i = 0; i < pre; ++i) load_x(i);
-      issued = pre;
-      for (int i = pre; i < n_it; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
-          atomicExch(p.err, 1);
-          s_abort = 1;
-          break;
-        }
-        if (*(volatile int*)&s_abort) break;
-        load_w(i);
-        load_x(i);
-        issued = i + 1;
-      }
-      // drain: every issued load must have landed before the block exits
-      for (int i = max(0, issued - S); i < issued; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u)) atomicExch(p.err, 2);
-      }
-    }
+    if (!warp_prod) produce(0, 1);
   } else if (warp == 5) {
     if (lane == 0) {  // ---- MMA issuer: one TMEM accumulation per piece
       bool ok = true;
@@ -468,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else {  // ---- warps 0-3: Q8_0 dequantisation of each piece, then its epilogue
+    if (warp_prod && warp < npw) produce(warp, npw);
     const int row_local = warp * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     int i = 0;
@@ -623,6 +642,15 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
   int smem = 0;
   const int grid = p.P * p.groups;
   p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, &p.stage_bytes, &smem);
+  // producer warps of single-piece blocks: up to 4, dividing the stage count
+  p.prod_warps = 1;
+  if (!kQ8) {
+    p.prod_warps = p.stages >= 4 ? 4 : p.stages;
+    if (p.stages % p.prod_warps) {
+      p.stages -= p.stages % p.prod_warps;
+      smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 2);
+    }
+  }
   launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
   return 1;
 }
