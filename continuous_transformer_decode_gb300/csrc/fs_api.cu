@@ -45,23 +45,26 @@ struct LayerW {
   float* g_ffn = nullptr;
 };
 
-// Stream-K width P of a weight matrix (blocks per lane group), from timings
-// of this kernel on the decode step's matrix shapes:
+// Stream-K width P of a weight matrix (blocks per lane group), from event
+// timings of this kernel on the decode step's matrix shapes at 1, 32 and 128
+// lanes:
 //  * at least as many 128-row tiles as SMs: one whole tile per block
 //    (P = m_tiles), no partial sums;
-//  * lane capacity <= 32 and at least 4 k-blocks per block at P = 2 x SMs:
-//    P = 2 x SMs, ranges crossing tile boundaries (partials are small);
-//  * otherwise equal K splits of every tile, P = m_tiles * s with
-//    m_tiles * s <= 0.85 x SMs, at least 16 k-blocks per split and s <= 8;
-//    lane groups then bring the launch to about two blocks per SM.
+//  * lane capacity <= 8 and at least 4 k-blocks per block at P = 2 x SMs:
+//    P = 2 x SMs, ranges crossing tile boundaries (partials are tiny);
+//  * otherwise s equal K splits of every tile, P = m_tiles * s: about
+//    1.3 x SMs blocks with splits of >= 8 k-blocks up to 32 lanes, about
+//    0.85 x SMs blocks with splits of >= 32 k-blocks beyond (lane groups then
+//    bring the launch to about two blocks per SM), s <= 8.
 // P depends on the matrix, the handle's lane capacity and the device only,
 // never on a call's lane count.
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
   if (m_tiles >= sms) return m_tiles;
-  if (max_lanes <= 32 && T >= (int64_t)8 * sms) return 2 * sms;
-  int s = (85 * sms) / (100 * m_tiles);
-  s = std::min(s, std::min(8, kb_total / 16));
+  if (max_lanes <= 8 && T >= (int64_t)8 * sms) return 2 * sms;
+  const bool narrow = max_lanes <= 32;
+  int s = narrow ? (13 * sms + 5 * m_tiles) / (10 * m_tiles) : (85 * sms) / (100 * m_tiles);
+  s = std::min(s, std::min(8, kb_total / (narrow ? 8 : 32)));
   return m_tiles * std::max(1, s);
 }
 }  // namespace
