@@ -306,16 +306,20 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     FS_CK(h, cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev));
   }
   // attention split length: a handle constant (it fixes the merge order).
-  // Long splits amortise each block's fixed cost once a full handle has
-  // enough (lane, KV head, split) blocks to fill the GPU several times over;
-  // otherwise short splits give the parallelism.
+  // Long splits amortise each block's fixed cost (page indices, q rotation,
+  // merges) once a full handle has enough (lane, KV head, split) blocks to
+  // fill the GPU several times over; otherwise short splits give the
+  // parallelism.
   {
-    const int64_t blocks512 =
-        (int64_t)d.max_lanes * d.n_kv_heads * ((d.max_pos + 511) / 512);
-    h->split_len =
-        attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
-            ? (blocks512 >= 4 * (int64_t)h->sms ? 512 : 128)
-            : 256;
+    auto blocks = [&](int len) {
+      return (int64_t)d.max_lanes * d.n_kv_heads * ((d.max_pos + len - 1) / len);
+    };
+    const int64_t sms = h->sms;
+    h->split_len = !attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
+                       ? 256
+                   : blocks(1024) >= 8 * sms ? 1024
+                   : blocks(512) >= 4 * sms  ? 512
+                                             : 128;
   }
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;

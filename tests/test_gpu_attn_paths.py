@@ -30,14 +30,14 @@ def _built():
     O.set_threads(8)
 
 
-def _handle(cfg, Wb, page_size, max_pos, force=None):
+def _handle(cfg, Wb, page_size, max_pos, force=None, max_lanes=4):
     old = os.environ.get("FS_ATTN")
     try:
         if force:
             os.environ["FS_ATTN"] = force
         else:
             os.environ.pop("FS_ATTN", None)
-        return U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=4, max_pos=max_pos,
+        return U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=max_lanes, max_pos=max_pos,
                           page_size=page_size)
     finally:
         if old is None:
@@ -84,13 +84,13 @@ def _run_oracle(cfg, Wb, ctx, kv, toks, max_pos):
     return np.stack([m.step_batch(lanes, t) for t in toks])
 
 
-def _check(cfg, Wb, page_size, ctx, with_oracle):
-    max_pos = max(ctx) + 8
+def _check(cfg, Wb, page_size, ctx, with_oracle, max_lanes=4, max_pos=None):
+    max_pos = max_pos or max(ctx) + 8
     kv = _kv(cfg, ctx, seed=41)
     rng = np.random.default_rng(page_size)
     toks = [[int(x) for x in rng.integers(0, cfg["V"], len(ctx))] for _ in range(3)]
-    h_t = _handle(cfg, Wb, page_size, max_pos)
-    h_m = _handle(cfg, Wb, page_size, max_pos, force="mma")
+    h_t = _handle(cfg, Wb, page_size, max_pos, max_lanes=max_lanes)
+    h_m = _handle(cfg, Wb, page_size, max_pos, force="mma", max_lanes=max_lanes)
     try:
         assert fs.fs_attention_path(h_t) == "tma-mma"
         assert fs.fs_attention_path(h_m) == "cp.async-mma"
@@ -128,3 +128,11 @@ def test_tma_attention_hd128_mistral_shape():
 def test_tma_attention_hd256(page_size):
     Wb = synth.make_weights(HD256, seed=3, fmt="bf16")
     _check(HD256, Wb, page_size, [5, 130, 700], with_oracle=True)
+
+
+def test_tma_attention_long_splits(smol_l2):
+    """A handle large enough (128 lanes x 3 KV heads x 4 chunks of 1024) to
+    take 1024-position attention splits: contexts of 300 / 1100 / 2100 tokens
+    are 1, 2 and 3 splits."""
+    cfg, Wb = smol_l2
+    _check(cfg, Wb, 16, [300, 1100, 2100], with_oracle=True, max_lanes=128, max_pos=3100)
