@@ -616,7 +616,7 @@ int seed_lane_pages(fs_handle* h, int lane, int n) {
 // Enqueues every kernel of one step for the n panel rows on h->stream (the
 // per-step arguments are read from device memory, so the sequence can be
 // captured once per n and replayed).
-void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
+void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked) {
   const fs_model_desc& d = h->d;
   cudaStream_t s = h->stream;
   const StepArgs& args = h->args;
@@ -667,8 +667,20 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                               h->xtype, h->Kp_d, s);
       });
     gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
-    if (h->attn_tma || h->attn_mma || h->attn_tiled) {
+    // a chunked step first appends every row's k, v (rows of one lane at
+    // consecutive positions see each other's keys); the MMA attention kernels
+    // then only read, the other kernels give way to the three-kernel path
+    const bool fused_append = !chunked || h->attn_tma || h->attn_mma || h->attn_tiled ||
+                              h->attn_fused;
+    if (chunked && fused_append)
+      h->launch(FS_PROF_OTHER, (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs),
+                [&] {
+                  return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
+                                            h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
+                });
+    if (fused_append && (h->attn_tma || h->attn_mma || h->attn_tiled)) {
       AttnParams ap{};
+      ap.kv_written = chunked ? 1 : 0;
       ap.qkv = h->qkv; ap.H = d.n_heads; ap.rc = h->rope_cos; ap.rs = h->rope_sin;
       ap.args = args; ap.kv = h->kv; ap.layer = l; ap.split_len = h->split_len;
       ap.max_splits = h->max_splits; ap.part_ml = h->part_ml; ap.part_acc = h->part_acc;
@@ -681,14 +693,14 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read) {
                   return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
                                      : launch_attention_tiled(ap, n, h->xtype, s);
                 });
-    } else if (h->attn_fused) {
+    } else if (fused_append && h->attn_fused) {
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
                   return launch_attention_fused(h->qkv, n, d.n_heads, h->rope_cos,
                                                 h->rope_sin, args, h->kv, l, h->max_splits,
                                                 h->split_len, h->part_ml, h->part_acc,
                                                 h->attn_counters, h->opanel, h->xtype,
-                                                h->Kp_q, s);
+                                                h->Kp_q, chunked ? 1 : 0, s);
                 });
     } else {
       h->launch(FS_PROF_OTHER,
@@ -776,6 +788,89 @@ int fs_lane_reset(fs_handle* h, int32_t lane) {
   return FS_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// Commit and launch of a validated step: page allocation (per lane in
+// position order, lowest free index first), the argument block, then the
+// kernels (one graph replay per (n, mode)).
+int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
+             int n, float* logits_out, bool chunked) {
+  const fs_model_desc& d = h->d;
+  FS_CK(h, cudaEventSynchronize(h->args_done));  // staging no longer in use
+  const int B = d.max_lanes;
+  int32_t* A = h->h_args;
+  int n_upd = 0;
+  // lanes in order of first appearance; a lane's positions (its length on
+  // up, one per row of this step) in ascending order
+  std::vector<int32_t> rows(d.max_lanes, 0);
+  for (int i = 0; i < n; ++i) {
+    A[i] = lanes[i];
+    A[B + i] = positions[i];
+    A[2 * B + i] = tokens[i];
+    rows[lanes[i]] += 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int k = lanes[i];
+    if (rows[k] == 0) continue;  // this lane's pages are already taken
+    for (int p = h->len[k]; p < h->len[k] + rows[k]; ++p) {
+      if (p % d.page_size) continue;
+      take_pages(h, k, p + 1);
+      A[3 * B + n_upd] = k;
+      A[4 * B + n_upd] = p / d.page_size;
+      A[5 * B + n_upd] = h->pt[k].back();
+      ++n_upd;
+    }
+    rows[k] = 0;
+  }
+  A[7 * B] = n_upd;
+  // one copy of the whole block keeps this to a single H2D transfer per step
+  FS_CK(h, cudaMemcpyAsync(h->d_args, h->h_args, (size_t)(7 * B + 1) * 4,
+                           cudaMemcpyHostToDevice, h->stream));
+  FS_CK(h, cudaEventRecord(h->args_done, h->stream));
+
+  // ---- the step: one graph replay, or the kernels one by one
+  double kv_read = 0.0;  // K and V bytes attention reads per layer
+  for (int i = 0; i < n; ++i)
+    kv_read += (double)(positions[i] + 1) * h->Nkv * 2.0 * (h->kv.kv_f32 ? 4.0 : 2.0);
+  float* out = logits_out ? logits_out : h->logits;
+  if (!logits_out && !h->prof_on && h->graphs_on) {
+    const int key = chunked ? n + (1 << 20) : n;
+    auto it = h->graphs.find(key);
+    if (it == h->graphs.end()) {
+      const int64_t before = h->launches;
+      cudaGraph_t g = nullptr;
+      FS_CK(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+      enqueue_step(h, n, out, kv_read, chunked);
+      cudaError_t e = cudaStreamEndCapture(h->stream, &g);
+      if (e != cudaSuccess) return h->cuda_fail(e, "cudaStreamEndCapture");
+      fs_handle::Graph G;
+      e = cudaGraphInstantiate(&G.exec, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return h->cuda_fail(e, "cudaGraphInstantiate");
+      G.kernels = h->launches - before;
+      h->launches = before;
+      it = h->graphs.emplace(key, G).first;
+    }
+    FS_CK(h, cudaGraphLaunch(it->second.exec, h->stream));
+    h->launches += it->second.kernels;
+  } else {
+    enqueue_step(h, n, out, kv_read, chunked);
+  }
+  FS_CK(h, cudaGetLastError());
+
+  for (int i = 0; i < n; ++i) {
+    h->len[lanes[i]] += 1;
+    positions[i] += 1;
+  }
+  h->last_n = n;
+  h->last_logits = out;
+  return FS_OK;
+}
+}  // namespace
+
+extern "C" {
+
 int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
                          const int32_t* tokens, int32_t n, float* logits_out) {
   if (!h) return FS_ERR_ARG;
@@ -797,68 +892,43 @@ int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
     if (h->len[k] % d.page_size == 0) ++need;
   }
   if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  return run_step(h, lanes, positions, tokens, n, logits_out, false);
+}
 
-  // ---- commit: page allocation (input order, lowest free index first)
-  FS_CK(h, cudaEventSynchronize(h->args_done));  // staging no longer in use
-  const int B = d.max_lanes;
-  int32_t* A = h->h_args;
-  int n_upd = 0;
+int fs_step_batch_chunked(fs_handle* h, const int32_t* lanes, int32_t* positions,
+                          const int32_t* tokens, int32_t n, float* logits_out) {
+  if (!h) return FS_ERR_ARG;
+  if (n == 0) return FS_OK;
+  if (n < 0 || n > h->d.max_lanes) return h->fail(FS_ERR_ARG, "n outside [0, max_lanes]");
+  if (!lanes || !positions || !tokens) return h->fail(FS_ERR_ARG, "NULL argument array");
+  const fs_model_desc& d = h->d;
+  // ---- validate (no state change): per lane, its rows' positions are
+  // exactly len, len + 1, ..., len + rows - 1 (in any order)
+  std::vector<int32_t> rows(d.max_lanes, 0);
   for (int i = 0; i < n; ++i) {
     const int k = lanes[i];
-    A[i] = k;
-    A[B + i] = positions[i];
-    A[2 * B + i] = tokens[i];
-    if (h->len[k] % d.page_size == 0) {
-      take_pages(h, k, h->len[k] + 1);
-      A[3 * B + n_upd] = k;
-      A[4 * B + n_upd] = h->len[k] / d.page_size;
-      A[5 * B + n_upd] = h->pt[k].back();
-      ++n_upd;
-    }
+    if (k < 0 || k >= d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+    if (tokens[i] < 0 || tokens[i] >= d.vocab) return h->fail(FS_ERR_TOKEN, "token outside [0, vocab)");
+    rows[k] += 1;
   }
-  A[7 * B] = n_upd;
-  // copy only the used prefix of each section: one copy of the whole block
-  // keeps this to a single H2D transfer per step
-  FS_CK(h, cudaMemcpyAsync(h->d_args, h->h_args, (size_t)(7 * B + 1) * 4,
-                           cudaMemcpyHostToDevice, h->stream));
-  FS_CK(h, cudaEventRecord(h->args_done, h->stream));
-
-  // ---- the step: one graph replay, or the kernels one by one
-  double kv_read = 0.0;  // K and V bytes attention reads per layer
-  for (int i = 0; i < n; ++i)
-    kv_read += (double)(h->len[lanes[i]] + 1) * h->Nkv * 2.0 * (h->kv.kv_f32 ? 4.0 : 2.0);
-  float* out = logits_out ? logits_out : h->logits;
-  if (!logits_out && !h->prof_on && h->graphs_on) {
-    auto it = h->graphs.find(n);
-    if (it == h->graphs.end()) {
-      const int64_t before = h->launches;
-      cudaGraph_t g = nullptr;
-      FS_CK(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
-      enqueue_step(h, n, out, kv_read);
-      cudaError_t e = cudaStreamEndCapture(h->stream, &g);
-      if (e != cudaSuccess) return h->cuda_fail(e, "cudaStreamEndCapture");
-      fs_handle::Graph G;
-      e = cudaGraphInstantiate(&G.exec, g, 0);
-      cudaGraphDestroy(g);
-      if (e != cudaSuccess) return h->cuda_fail(e, "cudaGraphInstantiate");
-      G.kernels = h->launches - before;
-      h->launches = before;
-      it = h->graphs.emplace(n, G).first;
-    }
-    FS_CK(h, cudaGraphLaunch(it->second.exec, h->stream));
-    h->launches += it->second.kernels;
-  } else {
-    enqueue_step(h, n, out, kv_read);
-  }
-  FS_CK(h, cudaGetLastError());
-
+  std::vector<std::vector<char>> hit;  // per lane with rows: which offsets are present
+  std::vector<int> idx(d.max_lanes, -1);
+  int need = 0;
   for (int i = 0; i < n; ++i) {
-    h->len[lanes[i]] += 1;
-    positions[i] += 1;
+    const int k = lanes[i];
+    const int64_t off = (int64_t)positions[i] - h->len[k];
+    if (off < 0 || off >= rows[k]) return h->fail(FS_ERR_POSITION, "positions of a lane must be its next consecutive ones");
+    if (idx[k] < 0) {
+      if ((int64_t)h->len[k] + rows[k] > d.max_pos) return h->fail(FS_ERR_KV_FULL, "lane would pass max_pos");
+      idx[k] = (int)hit.size();
+      hit.emplace_back(rows[k], 0);
+    }
+    if (hit[idx[k]][off]) return h->fail(FS_ERR_POSITION, "a position appears twice");
+    hit[idx[k]][off] = 1;
+    if (positions[i] % d.page_size == 0) ++need;
   }
-  h->last_n = n;
-  h->last_logits = out;
-  return FS_OK;
+  if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  return run_step(h, lanes, positions, tokens, n, logits_out, true);
 }
 
 int fs_sample(fs_handle* h, int32_t n, const float* temps, const uint64_t* seeds,

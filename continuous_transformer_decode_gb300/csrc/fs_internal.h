@@ -82,6 +82,17 @@ struct KV {
   int max_pages = 0;
 };
 
+// RoPE of one rotate-half pair (x0 = element i, x1 = element i + hd/2) with
+// cos c and sin s: (x0 c - x1 s, x1 c + x0 s), every product and sum rounded
+// on its own (no contraction into fused multiply-adds). Every kernel that
+// rotates q or k calls this, so a key written by one kernel has the same bits
+// as the key another kernel would write.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0,
+                                          float& y1) {
+  y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+  y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
+}
+
 enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
 
 // Y = X * W^T over B panel rows with a fused epilogue:
@@ -203,6 +214,11 @@ struct AttnParams {
   void* o;           // output panel
   int ld_o;
   int* err;          // device-visible error flag
+  // 0: the block holding a row's position rotates k and appends k, v there;
+  // 1: every row's k, v were appended by a preceding kernel of the step (rows
+  //    of one lane at consecutive positions, chunked prefill), so the kernel
+  //    appends nothing and reads no KV before its predecessor has finished
+  int kv_written;
 };
 bool attn_tiled_supports(int hd, int G, int page_size, int split_len);
 bool attn_mma_supports(int hd, int G, int kv_f32, int split_len, int max_splits);
@@ -222,7 +238,7 @@ int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos
                            const float* rope_sin, const StepArgs& args, const KV& kv,
                            int layer, int max_splits, int split_len, float* part_ml,
                            float* part_acc, int* counters, void* o_panel, int x_type,
-                           int ld_o, cudaStream_t s);
+                           int ld_o, int kv_written, cudaStream_t s);
 int launch_sample(const float* logits, int B, int V, const float* temps,
                   const uint64_t* seeds, const uint64_t* counters,
                   int32_t* out, cudaStream_t s);

@@ -67,15 +67,16 @@ __global__ void k_rope_append(const float* __restrict__ qkv, int H, int Hkv,
     const int h = idx / half, i = idx - h * half;
     const float a = row[h * hd + i], e = row[h * hd + i + half];
     float* qo = q_out + (int64_t)b * nq + h * hd;
-    qo[i] = a * c[i] - e * s[i];
-    qo[i + half] = e * c[i] + a * s[i];
+    rope_pair(a, e, c[i], s[i], qo[i], qo[i + half]);
   }
   for (int idx = threadIdx.x; idx < Hkv * half; idx += blockDim.x) {
     const int g = idx / half, i = idx - g * half;
     const float a = row[nq + g * hd + i], e = row[nq + g * hd + i + half];
     const int64_t off = kv_off(kv, ptrow, layer, g, pos);
-    st_f(K, off + i, a * c[i] - e * s[i]);
-    st_f(K, off + i + half, e * c[i] + a * s[i]);
+    float k0, k1;
+    rope_pair(a, e, c[i], s[i], k0, k1);
+    st_f(K, off + i, k0);
+    st_f(K, off + i + half, k1);
   }
   for (int idx = threadIdx.x; idx < Hkv * hd; idx += blockDim.x) {
     const int g = idx / hd, i = idx - g * hd;

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kT)
                  const float* __restrict__ rs, StepArgs args, KV kv, int layer,
                  int split_len, int max_splits, float* __restrict__ part_ml,
                  float* __restrict__ part_acc, int* __restrict__ counters, OT* o_panel,
-                 int ld_o) {
+                 int ld_o, int kv_written) {
   pdl_wait();
   pdl_trigger();
   constexpr int kHalf = HD / 2;
@@ -107,17 +107,18 @@ __global__ void __launch_bounds__(kT)
   for (int idx = tid; idx < G * kHalf; idx += kT) {
     const int h = idx / kHalf, i = idx - h * kHalf;
     const float a = row[(g * G + h) * HD + i], e = row[(g * G + h) * HD + i + kHalf];
-    qs[h * HD + i] = a * c[i] - e * sn[i];
-    qs[h * HD + i + kHalf] = e * c[i] + a * sn[i];
+    rope_pair(a, e, c[i], sn[i], qs[h * HD + i], qs[h * HD + i + kHalf]);
   }
-  if (s == ns - 1) {  // this split holds position pos: append k and v
+  if (s == ns - 1 && !kv_written) {  // this split holds position pos: append k and v
     const int64_t off = kv_base(kv, ptrow, layer, g, pos);
     const float* kr = row + H * HD + g * HD;
     const float* vr = row + (H + Hkv) * HD + g * HD;
     for (int i = tid; i < kHalf; i += kT) {
       const float a = kr[i], e = kr[i + kHalf];
-      KVIO<KVT>::st(K + off + i, a * c[i] - e * sn[i]);
-      KVIO<KVT>::st(K + off + i + kHalf, e * c[i] + a * sn[i]);
+      float k0, k1;
+      rope_pair(a, e, c[i], sn[i], k0, k1);
+      KVIO<KVT>::st(K + off + i, k0);
+      KVIO<KVT>::st(K + off + i + kHalf, k1);
     }
     for (int i = tid; i < HD; i += kT) KVIO<KVT>::st(V + off + i, vr[i]);
   }
@@ -280,12 +281,12 @@ template <typename KVT, typename OT>
 int dispatch_hd(int hd, dim3 grid, cudaStream_t s, const float* qkv, int H, const float* rc,
                 const float* rs, const StepArgs& args, const KV& kv, int layer, int split_len,
                 int max_splits, float* part_ml, float* part_acc, int* counters, OT* o,
-                int ld_o) {
+                int ld_o, int kv_written) {
 #define FS_ATTN_CASE(D)                                                                  \
   case D:                                                                                \
     launch_k(k_attn_fused<KVT, OT, D>, grid, kT, 0, s, qkv, H, rc, rs, args, kv, layer,        \
                                                  split_len, max_splits, part_ml,         \
-                                                 part_acc, counters, o, ld_o);            \
+                                                 part_acc, counters, o, ld_o, kv_written); \
     return 1;
   switch (hd) {
     FS_ATTN_CASE(16)
@@ -309,7 +310,7 @@ int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos
                            const float* rope_sin, const StepArgs& args, const KV& kv,
                            int layer, int max_splits, int split_len, float* part_ml,
                            float* part_acc, int* counters, void* o_panel, int x_type,
-                           int ld_o, cudaStream_t s) {
+                           int ld_o, int kv_written, cudaStream_t s) {
   if (B <= 0) return 0;
   dim3 grid(max_splits, kv.Hkv, B);
   if (kv.kv_f32) {
@@ -317,19 +318,20 @@ int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos
       return dispatch_hd<float, __nv_bfloat16>(kv.hd, grid, s, qkv, H, rope_cos, rope_sin,
                                                args, kv, layer, split_len, max_splits,
                                                part_ml, part_acc, counters,
-                                               static_cast<__nv_bfloat16*>(o_panel), ld_o);
+                                               static_cast<__nv_bfloat16*>(o_panel), ld_o,
+                                               kv_written);
     return dispatch_hd<float, float>(kv.hd, grid, s, qkv, H, rope_cos, rope_sin, args, kv,
                                      layer, split_len, max_splits, part_ml, part_acc,
-                                     counters, static_cast<float*>(o_panel), ld_o);
+                                     counters, static_cast<float*>(o_panel), ld_o, kv_written);
   }
   if (x_type == X_BF16)
     return dispatch_hd<__nv_bfloat16, __nv_bfloat16>(
         kv.hd, grid, s, qkv, H, rope_cos, rope_sin, args, kv, layer, split_len, max_splits,
-        part_ml, part_acc, counters, static_cast<__nv_bfloat16*>(o_panel), ld_o);
+        part_ml, part_acc, counters, static_cast<__nv_bfloat16*>(o_panel), ld_o, kv_written);
   return dispatch_hd<__nv_bfloat16, float>(kv.hd, grid, s, qkv, H, rope_cos, rope_sin, args,
                                            kv, layer, split_len, max_splits, part_ml,
                                            part_acc, counters, static_cast<float*>(o_panel),
-                                           ld_o);
+                                           ld_o, kv_written);
 }
 
 }  // namespace fsk

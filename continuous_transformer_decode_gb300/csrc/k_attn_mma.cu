@@ -111,10 +111,17 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
   // table and the step arguments were written by kernels that finished before
   // the predecessor started, so the first tiles are fetched before waiting
   // for the predecessor (the QKV projection read below).
-  issue(0);
-  if (n_tiles > 1) issue(1);
+  const bool prefetch = !a.kv_written;  // else this step's rows come from the predecessor
+  if (prefetch) {
+    issue(0);
+    if (n_tiles > 1) issue(1);
+  }
   pdl_wait();
   pdl_trigger();
+  if (!prefetch) {
+    issue(0);
+    if (n_tiles > 1) issue(1);
+  }
 
   // ---- rotated queries; the owner of pos also rotates k and appends k, v
   const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
@@ -125,13 +132,13 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
     float q0 = 0.0f, q1 = 0.0f;
     if (h < G) {
       const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
-      q0 = x0 * c[i] - x1 * sn[i];
-      q1 = x1 * c[i] + x0 * sn[i];
+      rope_pair(x0, x1, c[i], sn[i], q0, q1);
     }
     qs[h * HD + i] = q0;
     qs[h * HD + i + kHalf] = q1;
   }
-  if (owns_pos) {
+  const bool append = owns_pos && !a.kv_written;
+  if (append) {
     const float* kr = row + H * HD + g * HD;
     const float* vr = row + (H + Hkv) * HD + g * HD;
     const int pi = pos / ps, slot = pos - pi * ps;
@@ -139,7 +146,8 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
                         (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
     for (int i = tid; i < kHalf; i += kT) {
       const float x0 = kr[i], x1 = kr[i + kHalf];
-      const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
+      float k0, k1;
+      rope_pair(x0, x1, c[i], sn[i], k0, k1);
       Kg[off + i] = __float2bfloat16_rn(k0);
       Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
       knew[i] = k0;
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
     uint8_t* kb = Kt + (i & 1) * kTileBytes;
     uint8_t* vb = Vt + (i & 1) * kTileBytes;
     __syncthreads();
-    if (owns_pos && pos >= t0 && pos < t0 + kTT) {  // the appended token, from registers
+    if (append && pos >= t0 && pos < t0 + kTT) {  // the appended token, from registers
       const int r = pos - t0;
       for (int ch = tid; ch < kCh; ch += kT) {
         uint4 kk, vv;

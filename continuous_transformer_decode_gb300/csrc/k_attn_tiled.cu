@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
   for (int idx = tid; idx < G * kHalf; idx += kT) {
     const int h = idx / kHalf, i = idx - h * kHalf;
     const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
-    qs[h * HD + i] = x0 * c[i] - x1 * sn[i];
-    qs[h * HD + i + kHalf] = x1 * c[i] + x0 * sn[i];
+    rope_pair(x0, x1, c[i], sn[i], qs[h * HD + i], qs[h * HD + i + kHalf]);
   }
-  if (owns_pos) {
+  const bool append = owns_pos && !a.kv_written;
+  if (append) {
     const float* kr = row + H * HD + g * HD;
     const float* vr = row + (H + Hkv) * HD + g * HD;
     const int pi = pos / ps, slot = pos - pi * ps;
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
                         (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
     for (int i = tid; i < kHalf; i += kT) {
       const float x0 = kr[i], x1 = kr[i + kHalf];
-      const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
+      float k0, k1;
+      rope_pair(x0, x1, c[i], sn[i], k0, k1);
       Elem<KVT>::st(Kg + off + i, k0);
       Elem<KVT>::st(Kg + off + i + kHalf, k1);
       knew[i] = k0;
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
     }
     KVT* Kb = Kt + (i & 1) * kTT * HD;
     KVT* Vb = Vt + (i & 1) * kTT * HD;
-    if (owns_pos && pos >= t0 && pos < t0 + kTT) {  // the appended token, from registers
+    if (append && pos >= t0 && pos < t0 + kTT) {  // the appended token, from registers
       const int r = pos - t0;
       for (int e = tid; e < HD; e += kT) {
         Elem<KVT>::st(Kb + r * HD + e, knew[e]);

@@ -140,9 +140,13 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
   // Programmatic dependent launch: the KV of earlier positions and the page
   // table were written by kernels that finished before the predecessor
   // started, so each warp's first copies start before waiting for it.
-  for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
+  const bool prefetch = !a.kv_written;  // else this step's rows come from the predecessor
+  if (prefetch)
+    for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
   pdl_wait();  // the QKV projection's output is read below
   pdl_trigger();
+  if (!prefetch)
+    for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
 
   // ---- rotated queries; the owner of pos also rotates k and appends k, v
   const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
@@ -153,13 +157,13 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
     float q0 = 0.0f, q1 = 0.0f;
     if (h < G) {
       const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
-      q0 = x0 * c[i] - x1 * sn[i];
-      q1 = x1 * c[i] + x0 * sn[i];
+      rope_pair(x0, x1, c[i], sn[i], q0, q1);
     }
     qs[h * HD + i] = q0;
     qs[h * HD + i + kHalf] = q1;
   }
-  if (owns_pos) {
+  const bool append = owns_pos && !a.kv_written;
+  if (append) {
     const float* kr = row + H * HD + g * HD;
     const float* vr = row + (H + Hkv) * HD + g * HD;
     const int pi = pos / ps, slot = pos - pi * ps;
@@ -167,7 +171,8 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
                         (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
     for (int i = tid; i < kHalf; i += kT) {
       const float x0 = kr[i], x1 = kr[i + kHalf];
-      const float k0 = x0 * c[i] - x1 * sn[i], k1 = x1 * c[i] + x0 * sn[i];
+      float k0, k1;
+      rope_pair(x0, x1, c[i], sn[i], k0, k1);
       Kg[off + i] = __float2bfloat16_rn(k0);
       Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
       knew[i] = k0;
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
       *reinterpret_cast<uint4*>(vb + sws(r, ch)) = make_uint4(0, 0, 0, 0);
     }
     const int t0 = start + i * kTT + p0;
-    if (owns_pos && pos >= t0 && pos < t0 + 16) {  // the appended token, from registers
+    if (append && pos >= t0 && pos < t0 + 16) {  // the appended token, from registers
       const int r = pos - t0;
       for (int ch = lane; ch < kCh; ch += 32) {
         uint4 kk, vv;

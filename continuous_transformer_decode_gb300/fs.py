@@ -95,6 +95,7 @@ def lib():
         "fs_set_stream": (C.c_int, [p, p]),
         "fs_lane_reset": (C.c_int, [p, i32]),
         "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
+        "fs_step_batch_chunked": (C.c_int, [p, p, p, p, i32, p]),
         "fs_sample": (C.c_int, [p, i32, p, p, p, p]),
         "fs_lane_length": (C.c_int, [p, i32, p]),
         "fs_lane_pages": (C.c_int, [p, i32, p, i32, p]),
@@ -137,7 +138,7 @@ def lib():
 def exported_symbols() -> list:
     """Names of the entry points declared in include/fs.h."""
     return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
-            "fs_lane_reset", "fs_decode_step_batch", "fs_sample",
+            "fs_lane_reset", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_attention_path", "fs_sample_device",
@@ -234,6 +235,24 @@ def fs_decode_step_batch(h, lanes, positions, tokens, logits_out=None):
     assert po.size == n and to.size == n
     _check(h, lib().fs_decode_step_batch(h, _ptr(la), _ptr(po), _ptr(to), n,
                                          _dptr(logits_out)))
+    return po
+
+
+def fs_step_batch_chunked(h, lanes, positions, tokens, logits_out=None):
+    """Chunked prefill step: a lane may appear on several rows at its next
+    consecutive positions. ``positions`` (np.int32) is incremented in place
+    on success and returned. logits_out: torch CUDA f32 [n, V]."""
+    la = _i32(lanes)
+    to = _i32(tokens)
+    if (isinstance(positions, np.ndarray) and positions.dtype == np.int32
+            and positions.flags["C_CONTIGUOUS"]):
+        po = positions
+    else:
+        po = _i32(positions)
+    n = la.size
+    assert po.size == n and to.size == n
+    _check(h, lib().fs_step_batch_chunked(h, _ptr(la), _ptr(po), _ptr(to), n,
+                                          _dptr(logits_out)))
     return po
 
 

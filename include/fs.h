@@ -152,6 +152,27 @@ int fs_decode_step_batch(fs_handle* h, const int32_t* lanes,
                          int32_t* positions, const int32_t* tokens, int32_t n,
                          float* logits_out);
 
+/* decode_step_batch with chunked prefill: the prompt of a lane is consumed in
+ * chunks ("Fat-station continuous batching", "What /generate does today":
+ * the prompt is prefilled in chunks) within one batched step, next to the
+ * decoding lanes ("DGR-012", "Prefill does not starve decode": prefill per
+ * tick is capped in tokens). Rows i < n: lane lanes[i] consumes tokens[i] at
+ * positions[i]; a lane may appear on several rows, and its rows' positions
+ * must be exactly its length, length + 1, ..., length + rows - 1, in any
+ * order. Every row's K/V are appended before attention, so a row attends to
+ * its lane's keys 0..positions[i], including the other rows of this step
+ * at earlier positions; a row's logits equal, bit for bit, those of feeding
+ * the same tokens one per call through fs_decode_step_batch. Pages are taken
+ * per lane in position order, lanes in order of first appearance. n counts
+ * rows (at most max_lanes). On success every positions[i] is incremented
+ * and each lane's length grows by its row count. logits_out, graphs and
+ * errors as fs_decode_step_batch, except that FS_ERR_POSITION also reports
+ * positions that are not the lane's next consecutive ones (repeated lanes
+ * are not FS_ERR_DUP_LANE here). */
+int fs_step_batch_chunked(fs_handle* h, const int32_t* lanes,
+                          int32_t* positions, const int32_t* tokens, int32_t n,
+                          float* logits_out);
+
 /* Samples one token per row of the last step's logits ("Components", item 3,
  * fold: the lane's temperature and seed). Row i: temps[i] == 0 selects the
  * argmax (lowest index on ties); otherwise z = logit / temps[i] in double,
