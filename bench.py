@@ -434,8 +434,8 @@ def cpu_baseline(wl, B, seconds=15.0):
 
 def run_trace(args, wl, ws, rank):
     """The continuous-batching trace: jobs with Poisson arrivals on the
-    scheduler's step clock, log-uniform prompts of 8..2048 tokens fed one per
-    step, U[16, 512] new tokens, temperature 0 or 0.8 with per-job seeds,
+    scheduler's step clock, log-uniform prompts of 8..2048 tokens (consumed in
+    chunks, decode first), U[16, 512] new tokens, temperature 0 or 0.8 with per-job seeds,
     through fs_sched over the decode step. Returns the JSON line's fields.
     Gate: a few jobs re-run alone on the same handle give the same tokens."""
     import torch
@@ -451,10 +451,11 @@ def run_trace(args, wl, ws, rank):
     n_pages = lanes * ((max_pos + ps - 1) // ps)
     W, wdt = gpu_weights(cfg, wl["wdtype"])
     h = fs.fs_create(fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, lanes, n_pages, max_pos, ps), W)
-    budget = max(1, lanes // 4)
+    budget = args.prefill_budget or max(1, lanes // 2)
+    chunk = args.prefill_chunk or budget
 
     def run(sched_lanes, js):
-        s = fs.fs_sched_create(h, sched_lanes, budget)
+        s = fs.fs_sched_create(h, sched_lanes, budget, prefill_chunk=chunk)
         try:
             order = sorted(js, key=lambda j: (j["arrive"], j["id"]))
             ids, i, tick = {}, 0, 0
@@ -497,7 +498,7 @@ def run_trace(args, wl, ws, rank):
                 tok_s=total * ws / dt, decode_tok_s=st["decode_tokens"] * ws / dt,
                 prefill_tokens=st["prefill_tokens"], decode_tokens=st["decode_tokens"],
                 occupancy_avg=st["occupancy_avg"], occupancy_max=st["occupancy_max"],
-                budget=budget, alone_ok=alone_ok, max_pos=max_pos)
+                budget=budget, chunk=chunk, alone_ok=alone_ok, max_pos=max_pos)
 
 
 def main():
@@ -515,6 +516,11 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--jobs", type=int, default=0,
                     help="trace workload: number of jobs (default min(512, 4 x lanes))")
+    ap.add_argument("--prefill-budget", type=int, default=0,
+                    help="trace workload: prompt tokens per step (default lanes / 2)")
+    ap.add_argument("--prefill-chunk", type=int, default=0,
+                    help="trace workload: prompt tokens per lane per step (default the "
+                         "budget; 1 = no chunking)")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
     ws, rank, local = _dist()
@@ -541,7 +547,8 @@ def main():
                 "dtype": wl["wdtype"], "data": "synthetic job trace (random N(0,0.02) weights)",
                 "config": {"workload": args.workload, "model_shape": cfg["name"],
                            "layers": cfg["L"], "lanes": r["lanes"], "jobs": r["jobs"],
-                           "max_prefill_tokens_per_tick": r["budget"], "max_pos": r["max_pos"],
+                           "max_prefill_tokens_per_tick": r["budget"],
+                           "prefill_chunk": r["chunk"], "max_pos": r["max_pos"],
                            "parallelism": f"replicas x{ws}"},
                 "decode_tok_s": r["decode_tok_s"], "prefill_tokens": r["prefill_tokens"],
                 "decode_tokens": r["decode_tokens"], "occupancy_avg": r["occupancy_avg"],

@@ -21,9 +21,10 @@ struct Engine {
   virtual ~Engine() = default;
   virtual int capacity() const = 0;
   virtual int reset(int lane) = 0;
-  // lanes/positions/tokens of n lanes; positions advanced on success
-  virtual int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens,
-                   int n) = 0;
+  // n rows (lane, position, token); a lane on several rows has them at its
+  // next consecutive positions (chunked); positions advanced on success
+  virtual int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
+                   bool chunked) = 0;
   virtual int sample(int n, const float* temps, const uint64_t* seeds,
                      const uint64_t* counters, int32_t* out) = 0;
   virtual std::string error() const = 0;
@@ -35,9 +36,10 @@ struct GpuEngine : Engine {
   explicit GpuEngine(fs_handle* hh, int c) : h(hh), cap(c) {}
   int capacity() const override { return cap; }
   int reset(int lane) override { return fs_lane_reset(h, lane); }
-  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens,
-           int n) override {
-    return fs_decode_step_batch(h, lanes, positions, tokens, n, nullptr);
+  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
+           bool chunked) override {
+    return chunked ? fs_step_batch_chunked(h, lanes, positions, tokens, n, nullptr)
+                   : fs_decode_step_batch(h, lanes, positions, tokens, n, nullptr);
   }
   int sample(int n, const float* temps, const uint64_t* seeds, const uint64_t* counters,
              int32_t* out) override {
@@ -66,11 +68,15 @@ struct ModelFreeEngine : Engine {
     len[lane] = 0;
     return FS_OK;
   }
-  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n) override {
+  int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
+           bool) override {
+    // rows in order; a lane's rows at its next consecutive positions
+    std::vector<int32_t> at(len);
     for (int i = 0; i < n; ++i) {
       if (lanes[i] < 0 || lanes[i] >= cap) return FS_ERR_LANE;
-      if (positions[i] != len[lanes[i]]) return FS_ERR_POSITION;
+      if (positions[i] != at[lanes[i]]) return FS_ERR_POSITION;
       if (tokens[i] < 0 || tokens[i] >= vocab) return FS_ERR_TOKEN;
+      at[lanes[i]] += 1;
     }
     last_lanes.assign(lanes, lanes + n);
     for (int i = 0; i < n; ++i) {
@@ -143,7 +149,7 @@ namespace {
 int make(std::unique_ptr<Engine> eng, const fs_sched_config* cfg, fs_sched** out) {
   if (!cfg || !out) return FS_ERR_ARG;
   if (cfg->lanes < 1 || cfg->lanes > eng->capacity() || cfg->max_prefill_tokens_per_tick < 1 ||
-      cfg->max_queue < 0)
+      cfg->max_queue < 0 || cfg->prefill_chunk < 0)
     return FS_ERR_ARG;
   fs_sched* s = new fs_sched();
   s->eng = std::move(eng);
@@ -214,35 +220,53 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
     ln.pos = 0;
     ln.seq = s->admit_seq++;
   }
-  // ---- gather: decode lanes always, prompt lanes oldest first within budget
+  // ---- gather: decode lanes always (one row each); prompt lanes oldest
+  // first, each up to prefill_chunk tokens, within the prompt-token budget
+  // and within L rows in all
   std::vector<int> prompt_lanes;
-  std::vector<char> chosen(L, 0);
+  std::vector<int32_t> take(L, 0);
+  int rows_left = L;
   for (int k = 0; k < L; ++k) {
     const Lane& ln = s->lanes[k];
     if (!ln.busy) continue;
-    if (ln.feed >= (int)ln.job.prompt.size())
-      chosen[k] = 1;
-    else
+    if (ln.feed >= (int)ln.job.prompt.size()) {
+      take[k] = 1;
+      --rows_left;
+    } else {
       prompt_lanes.push_back(k);
+    }
   }
   std::sort(prompt_lanes.begin(), prompt_lanes.end(),
             [&](int a, int b) { return s->lanes[a].seq < s->lanes[b].seq; });
-  const int budget = std::max(1, s->cfg.max_prefill_tokens_per_tick);
-  for (int i = 0; i < (int)prompt_lanes.size() && i < budget; ++i) chosen[prompt_lanes[i]] = 1;
+  int left = std::max(1, s->cfg.max_prefill_tokens_per_tick);
+  const int chunk = std::max(1, s->cfg.prefill_chunk);
+  for (int k : prompt_lanes) {
+    const Lane& ln = s->lanes[k];
+    const int t = std::min(std::min((int)ln.job.prompt.size() - ln.feed, chunk),
+                           std::min(left, rows_left));
+    if (t <= 0) break;
+    take[k] = t;
+    left -= t;
+    rows_left -= t;
+  }
   s->b_lanes.clear();
   s->b_pos.clear();
   s->b_tok.clear();
+  bool chunked = false;
   for (int k = 0; k < L; ++k) {
-    if (!chosen[k]) continue;
     const Lane& ln = s->lanes[k];
-    s->b_lanes.push_back(k);
-    s->b_pos.push_back(ln.pos);
-    s->b_tok.push_back(ln.feed < (int)ln.job.prompt.size() ? ln.job.prompt[ln.feed] : ln.last);
+    chunked = chunked || take[k] > 1;
+    for (int r = 0; r < take[k]; ++r) {
+      const int f = ln.feed + r;
+      s->b_lanes.push_back(k);
+      s->b_pos.push_back(ln.pos + r);
+      s->b_tok.push_back(f < (int)ln.job.prompt.size() ? ln.job.prompt[f] : ln.last);
+    }
   }
   const int n = (int)s->b_lanes.size();
   if (n == 0) return FS_OK;
-  // ---- one batched step, then one sample over the step's lanes
-  int rc = s->eng->step(s->b_lanes.data(), s->b_pos.data(), s->b_tok.data(), n);
+  // ---- one batched step, then one sample over the step's rows
+  int rc = s->eng->step(s->b_lanes.data(), s->b_pos.data(), s->b_tok.data(), n, chunked);
   if (rc) return s->fail(rc, "decode step: " + s->eng->error());
   s->b_temp.resize(n);
   s->b_seed.resize(n);
@@ -261,19 +285,23 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
   s->st.occupancy_last = n;
   s->st.occupancy_max = std::max(s->st.occupancy_max, n);
   s->occ_sum += n;
-  // ---- fold
+  // ---- fold: a lane's rows advance its feed; its last row's token counts
+  // once the prompt is consumed
   int retired = 0;
-  for (int i = 0; i < n; ++i) {
-    Lane& ln = s->lanes[s->b_lanes[i]];
-    ln.pos += 1;
-    const bool in_prompt = ln.feed < (int)ln.job.prompt.size();
-    if (in_prompt)
-      s->st.prefill_tokens += 1;
-    else
-      s->st.decode_tokens += 1;
-    ln.feed += 1;
+  for (int i = 0; i < n;) {
+    const int k = s->b_lanes[i];
+    Lane& ln = s->lanes[k];
+    const int last = i + take[k] - 1;
+    for (; i <= last; ++i) {
+      ln.pos += 1;
+      if (ln.feed < (int)ln.job.prompt.size())
+        s->st.prefill_tokens += 1;
+      else
+        s->st.decode_tokens += 1;
+      ln.feed += 1;
+    }
     if (ln.feed < (int)ln.job.prompt.size()) continue;
-    const int32_t t = s->b_out[i];
+    const int32_t t = s->b_out[last];
     ln.gen.push_back(t);
     ln.last = t;
     if ((int)ln.gen.size() >= ln.job.max_new || (ln.job.stop >= 0 && t == ln.job.stop)) {

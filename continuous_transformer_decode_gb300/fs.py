@@ -55,7 +55,7 @@ class fs_weights(C.Structure):
 
 class fs_sched_config(C.Structure):
     _fields_ = [("lanes", C.c_int32), ("max_prefill_tokens_per_tick", C.c_int32),
-                ("max_queue", C.c_int32)]
+                ("max_queue", C.c_int32), ("prefill_chunk", C.c_int32)]
 
 
 class fs_job(C.Structure):
@@ -412,9 +412,9 @@ def _sched_check(s, rc: int) -> None:
 
 
 def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
-                    max_queue: int = 0):
+                    max_queue: int = 0, prefill_chunk: int = 1):
     s = C.c_void_p()
-    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue)
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk)
     rc = lib().fs_sched_create(h, C.byref(cfg), C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create failed")
@@ -423,9 +423,9 @@ def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
 
 def fs_sched_create_model_free(lanes: int, vocab: int,
                                max_prefill_tokens_per_tick: int = 1,
-                               max_queue: int = 0):
+                               max_queue: int = 0, prefill_chunk: int = 1):
     s = C.c_void_p()
-    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue)
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk)
     rc = lib().fs_sched_create_model_free(C.byref(cfg), vocab, C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create_model_free failed")

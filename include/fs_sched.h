@@ -19,12 +19,16 @@
  * Policy (the readings taken where the pages leave it open):
  *   - fill: at the start of a step each free lane, in lane order, takes the
  *     oldest pending job; a lane freed in step t is refilled in step t+1;
- *   - gather: every lane past its prompt is in the step; lanes still in their
- *     prompt are added oldest-admitted first, one token each, up to
- *     max_prefill_tokens_per_tick tokens (at least 1); the batch lists lanes
- *     in lane order;
+ *   - gather: every lane past its prompt is in the step (one row each);
+ *     lanes still in their prompt are added oldest-admitted first, each with
+ *     up to prefill_chunk of its next prompt tokens (chunked prefill,
+ *     "Fat-station continuous batching", "What /generate does today"), until
+ *     max_prefill_tokens_per_tick prompt tokens (at least 1) or `lanes` rows
+ *     in all; the rows list lanes in lane order and a lane's positions in
+ *     ascending order; a step with a lane on several rows runs through
+ *     fs_step_batch_chunked, any other through fs_decode_step_batch;
  *   - fold: the step that consumes a prompt's last token yields the job's
- *     first generated token; the job's t-th generated token is sampled with
+ *     first generated token (from that lane's last row); the job's t-th generated token is sampled with
  *     (seed, counter = t), so a job's tokens do not depend on its lane, its
  *     step or its neighbours.
  *
@@ -48,6 +52,8 @@ typedef struct fs_sched_config {
   int32_t lanes;                       /* lanes used: 1 .. engine capacity   */
   int32_t max_prefill_tokens_per_tick; /* prompt tokens per step (>= 1)      */
   int32_t max_queue;                   /* pending jobs allowed, 0 = no bound */
+  int32_t prefill_chunk;               /* prompt tokens per lane per step;
+                                          0 or 1: one (no chunking)         */
 } fs_sched_config;
 
 typedef struct fs_job {

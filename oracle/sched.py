@@ -33,9 +33,12 @@ from collections import deque
 
 class Reference:
     def __init__(self, n_lanes: int, max_prefill_tokens_per_tick: int,
-                 step_fn, sample_fn, reset_fn=None):
+                 step_fn, sample_fn, reset_fn=None, prefill_chunk: int = 1):
         self.n_lanes = n_lanes
         self.budget = max(1, int(max_prefill_tokens_per_tick))
+        # prompt tokens one lane may consume in one step (chunked prefill,
+        # "Fat-station continuous batching", "What /generate does today")
+        self.chunk = max(1, int(prefill_chunk))
         self.step_fn = step_fn
         self.sample_fn = sample_fn
         self.reset_fn = reset_fn
@@ -77,35 +80,54 @@ class Reference:
         prompt = [k for k in range(self.n_lanes) if self.lanes[k] is not None
                   and self.lanes[k]["feed"] < len(self.lanes[k]["job"]["prompt"])]
         prompt.sort(key=lambda k: self.lanes[k]["seq"])
-        chosen = set(decode) | set(prompt[:self.budget])
-        batch = sorted(chosen)
-        if not batch:
+        # decode first; then prompt lanes oldest first, each up to `chunk`
+        # tokens, within the step's prompt-token budget and within n_lanes
+        # rows in all ("DGR-012", "Prefill does not starve decode")
+        take = {k: 1 for k in decode}
+        left, rows_left = self.budget, self.n_lanes - len(decode)
+        for k in prompt:
+            ln = self.lanes[k]
+            t = min(len(ln["job"]["prompt"]) - ln["feed"], self.chunk, left, rows_left)
+            if t <= 0:
+                break
+            take[k] = t
+            left -= t
+            rows_left -= t
+        if not take:
             return []
-        toks, poss = [], []
-        for k in batch:
+        # rows: lanes ascending, a lane's positions ascending
+        rows, toks, poss = [], [], []
+        for k in sorted(take):
             ln = self.lanes[k]
             p = ln["job"]["prompt"]
-            toks.append(int(p[ln["feed"]]) if ln["feed"] < len(p) else ln["last"])
-            poss.append(self.positions[k])
-        logits = self.step_fn(batch, poss, toks)
+            for r in range(take[k]):
+                f = ln["feed"] + r
+                rows.append(k)
+                toks.append(int(p[f]) if f < len(p) else ln["last"])
+                poss.append(self.positions[k] + r)
+        logits = self.step_fn(rows, poss, toks)
         self.steps += 1
-        self.occupancy.append(len(batch))
+        self.occupancy.append(len(rows))
         retired = []
         self.prefill_per_step.append(
-            sum(1 for k in batch
-                if self.lanes[k]["feed"] < len(self.lanes[k]["job"]["prompt"])))
-        for i, k in enumerate(batch):
+            sum(1 for k, f in zip(rows, poss)
+                if f < len(self.lanes[k]["job"]["prompt"])))
+        i = 0
+        for k in sorted(take):
             ln = self.lanes[k]
-            self.positions[k] += 1
             job = ln["job"]
-            if ln["feed"] < len(job["prompt"]):
-                self.prefill_tokens += 1
-            else:
-                self.decode_tokens += 1
-            ln["feed"] += 1
+            for r in range(take[k]):
+                if ln["feed"] < len(job["prompt"]):
+                    self.prefill_tokens += 1
+                else:
+                    self.decode_tokens += 1
+                ln["feed"] += 1
+                self.positions[k] += 1
+            last = i + take[k] - 1  # the lane's last row of this step
+            i += take[k]
             if ln["feed"] < len(job["prompt"]):
                 continue
-            t = self.sample_fn(logits[i], job["temperature"], job["seed"],
+            t = self.sample_fn(logits[last], job["temperature"], job["seed"],
                                len(ln["gen"]))
             ln["gen"].append(int(t))
             ln["last"] = int(t)

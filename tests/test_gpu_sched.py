@@ -30,8 +30,8 @@ def _jobs(n, vocab, seed, max_prompt=12, max_new=10):
             for j in range(n)]
 
 
-def _run_sched(h, jobs, lanes, budget):
-    s = fs.fs_sched_create(h, lanes, budget)
+def _run_sched(h, jobs, lanes, budget, chunk=1):
+    s = fs.fs_sched_create(h, lanes, budget, prefill_chunk=chunk)
     try:
         order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
         ids, i, tick = {}, 0, 0
@@ -75,13 +75,18 @@ def test_scheduler_tiny_f32_per_job_equals_oracle_serial():
         assert got[j["id"]] == S.serial_job(j, step_fn, sample_fn, reset_fn), j["id"]
 
 
-def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise():
+@pytest.mark.parametrize("budget,chunk,max_prompt", [(3, 1, 12), (10, 6, 40)])
+def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise(budget, chunk, max_prompt):
+    """One token per lane per step, and chunked prefill (several prompt tokens
+    of a lane per step through fs_step_batch_chunked)."""
     cfg = synth.with_layers(synth.MODEL_S, 2)
     Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
-    jobs = _jobs(12, cfg["V"], 5)
-    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=6, max_pos=32)
+    jobs = _jobs(12, cfg["V"], 5, max_prompt=max_prompt)
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=6, max_pos=64)
     try:
-        got, st = _run_sched(h, jobs, 6, 3)
+        got, st = _run_sched(h, jobs, 6, budget, chunk)
+        if chunk > 1:
+            assert st["occupancy_max"] > 1
         for k in range(6):
             fs.fs_lane_reset(h, k)
         for j in jobs:  # each job alone on lane 0, one token per step

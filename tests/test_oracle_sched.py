@@ -76,6 +76,44 @@ def _engine(m, n_lanes, max_pos=96):
     return step_fn, reset_fn, sample_fn
 
 
+def _engine_rows(m, n_lanes, max_pos=96):
+    """Rows in order through serial Step: a lane on several rows (chunked
+    prefill) consumes them one after another."""
+    lanes = [m.lane(max_pos) for _ in range(n_lanes)]
+
+    def step_fn(ks, poss, toks):
+        out = []
+        for k, p, t in zip(ks, poss, toks):
+            assert lanes[k].pos == p
+            out.append(m.step(lanes[k], t))
+        return out
+
+    def reset_fn(k):
+        lanes[k].reset()
+
+    def sample_fn(row, temp, seed, counter):
+        return O.sample(row, temp, seed, counter)
+    return step_fn, reset_fn, sample_fn
+
+
+def test_scheduler_reference_chunked_prefill_per_job_equals_serial(tiny_engine):
+    cfg, m = tiny_engine
+    g = np.random.default_rng(5)
+    jobs = [dict(id=j, arrive=int(g.integers(0, 12)),
+                 prompt=synth.make_prompts(1, int(g.integers(1, 25)), cfg["V"],
+                                           seed=200 + j)[0],
+                 max_new=int(g.integers(1, 8)),
+                 temperature=0.0 if j % 2 else 0.8, seed=2000 + j) for j in range(8)]
+    step_fn, reset_fn, sample_fn = _engine_rows(m, 3)
+    ref = S.Reference(3, 7, step_fn, sample_fn, reset_fn, prefill_chunk=5)
+    done = ref.run(jobs)
+    s_step, s_reset, s_sample = _engine(m, 1)
+    for job in jobs:
+        assert done[job["id"]] == S.serial_job(job, s_step, s_sample, s_reset), job["id"]
+    assert max(ref.prefill_per_step) <= 7 and max(ref.occupancy) <= 3
+    assert ref.prefill_tokens == sum(len(j["prompt"]) for j in jobs)
+
+
 def test_scheduler_reference_per_job_equals_serial(tiny_engine):
     cfg, m = tiny_engine
     g = np.random.default_rng(4)

@@ -61,16 +61,19 @@ def _jobs(n, vocab, seed, max_prompt=9, max_new=9):
     return jobs
 
 
-@pytest.mark.parametrize("lanes,budget,seed", [(1, 1, 0), (3, 1, 1), (4, 2, 2),
-                                               (8, 3, 3), (5, 100, 4)])
-def test_product_scheduler_matches_reference(lanes, budget, seed):
+@pytest.mark.parametrize("lanes,budget,chunk,seed", [
+    (1, 1, 1, 0), (3, 1, 1, 1), (4, 2, 1, 2), (8, 3, 1, 3), (5, 100, 1, 4),
+    # chunked prefill: several prompt tokens of a lane in one step
+    (4, 6, 3, 5), (3, 20, 8, 6), (8, 5, 2, 7), (2, 1, 4, 8), (6, 100, 100, 9)])
+def test_product_scheduler_matches_reference(lanes, budget, chunk, seed):
     vocab = 97
-    jobs = _jobs(24, vocab, seed)
+    jobs = _jobs(24, vocab, seed, max_prompt=9 if chunk == 1 else 30)
     model = HashModel(lanes, vocab)
-    ref = S.Reference(lanes, budget, model.step, model.sample, model.reset)
+    ref = S.Reference(lanes, budget, model.step, model.sample, model.reset,
+                      prefill_chunk=chunk)
     want = ref.run(jobs)
 
-    s = fs.fs_sched_create_model_free(lanes, vocab, budget)
+    s = fs.fs_sched_create_model_free(lanes, vocab, budget, prefill_chunk=chunk)
     try:
         order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
         ids, i, tick, batches = {}, 0, 0, []
