@@ -1147,6 +1147,12 @@ const char* fs_attention_path(const fs_handle* h) {
   return "three-kernel";
 }
 
+int fs_lane_capacity(const fs_handle* h, int32_t* tokens_out) {
+  if (!h || !tokens_out) return FS_ERR_ARG;
+  *tokens_out = h->d.max_pos;
+  return FS_OK;
+}
+
 int fs_device_error(fs_handle* h, int32_t* code_out) {
   if (!h || !code_out) return FS_ERR_ARG;
   FS_CK(h, cudaStreamSynchronize(h->stream));

@@ -4,6 +4,7 @@
 // include/fs_sched.h. Host code only.
 
 #include <algorithm>
+#include <chrono>
 #include <cstring>
 #include <deque>
 #include <map>
@@ -20,6 +21,7 @@ namespace {
 struct Engine {
   virtual ~Engine() = default;
   virtual int capacity() const = 0;
+  virtual int64_t lane_tokens() const = 0;  // KV tokens one lane can hold; 0 = no bound
   virtual int reset(int lane) = 0;
   // n rows (lane, position, token); a lane on several rows has them at its
   // next consecutive positions (chunked); positions advanced on success
@@ -35,6 +37,10 @@ struct GpuEngine : Engine {
   int cap;
   explicit GpuEngine(fs_handle* hh, int c) : h(hh), cap(c) {}
   int capacity() const override { return cap; }
+  int64_t lane_tokens() const override {
+    int32_t t = 0;
+    return fs_lane_capacity(h, &t) == FS_OK ? t : 0;
+  }
   int reset(int lane) override { return fs_lane_reset(h, lane); }
   int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
            bool chunked) override {
@@ -62,6 +68,7 @@ struct ModelFreeEngine : Engine {
   std::vector<int32_t> last_lanes;
   ModelFreeEngine(int c, int v) : cap(c), vocab(v), hash(c, 0xCBF29CE484222325ull), len(c, 0) {}
   int capacity() const override { return cap; }
+  int64_t lane_tokens() const override { return 0; }
   int reset(int lane) override {
     if (lane < 0 || lane >= cap) return FS_ERR_LANE;
     hash[lane] = 0xCBF29CE484222325ull;
@@ -103,6 +110,7 @@ struct ModelFreeEngine : Engine {
 
 struct Job {
   int64_t id;
+  int64_t need;  // KV tokens reserved: prompt + max_new
   std::vector<int32_t> prompt;
   int32_t max_new;
   float temp;
@@ -129,6 +137,9 @@ struct fs_sched {
   std::vector<Lane> lanes;
   std::map<int64_t, std::vector<int32_t>> done;
   int64_t next_id = 0, admit_seq = 0;
+  int64_t reserved = 0;  // KV tokens reserved by the lanes' jobs
+  bool clock_started = false;
+  std::chrono::steady_clock::time_point t_first, t_last;
   fs_sched_stats st{};
   double occ_sum = 0.0;
   std::vector<int32_t> last_batch;
@@ -149,11 +160,12 @@ namespace {
 int make(std::unique_ptr<Engine> eng, const fs_sched_config* cfg, fs_sched** out) {
   if (!cfg || !out) return FS_ERR_ARG;
   if (cfg->lanes < 1 || cfg->lanes > eng->capacity() || cfg->max_prefill_tokens_per_tick < 1 ||
-      cfg->max_queue < 0 || cfg->prefill_chunk < 0)
+      cfg->max_queue < 0 || cfg->prefill_chunk < 0 || cfg->kv_budget_tokens < 0)
     return FS_ERR_ARG;
   fs_sched* s = new fs_sched();
   s->eng = std::move(eng);
   s->cfg = *cfg;
+  s->st.kv_budget_tokens = cfg->kv_budget_tokens;
   s->lanes.resize(cfg->lanes);
   *out = s;
   return FS_OK;
@@ -184,12 +196,22 @@ int fs_sched_submit(fs_sched* s, const fs_job* j, int64_t* job_id_out) {
   if (!s || !j) return FS_ERR_ARG;
   if (!j->prompt || j->prompt_len < 1 || j->max_new_tokens < 1 || !(j->temperature >= 0.0f))
     return s->fail(FS_ERR_ARG, "job needs a prompt, max_new_tokens >= 1, temperature >= 0");
+  const int64_t need = (int64_t)j->prompt_len + j->max_new_tokens;
+  const int64_t lane_cap = s->eng->lane_tokens();
+  if ((s->cfg.kv_budget_tokens > 0 && need > s->cfg.kv_budget_tokens) ||
+      (lane_cap > 0 && need > lane_cap)) {
+    s->st.rejected += 1;
+    s->st.rejected_kv_budget += 1;
+    return s->fail(FS_ERR_KV_BUDGET, "prompt + new tokens exceed the KV budget");
+  }
   if (s->cfg.max_queue > 0 && (int)s->pending.size() >= s->cfg.max_queue) {
     s->st.rejected += 1;
+    s->st.rejected_queue_full += 1;
     return s->fail(FS_ERR_QUEUE_FULL, "pending queue is full");
   }
   Job job;
   job.id = s->next_id++;
+  job.need = need;
   job.prompt.assign(j->prompt, j->prompt + j->prompt_len);
   job.max_new = j->max_new_tokens;
   job.temp = j->temperature;
@@ -205,10 +227,18 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
   if (!s) return FS_ERR_ARG;
   if (n_retired_out) *n_retired_out = 0;
   const int L = s->cfg.lanes;
-  // ---- fill: free lanes in lane order take the oldest pending jobs
+  // ---- fill: free lanes in lane order take the oldest pending jobs while
+  // their KV reservations fit the budget (no overtaking)
+  const int64_t budget_kv = s->cfg.kv_budget_tokens;
   for (int k = 0; k < L && !s->pending.empty(); ++k) {
     Lane& ln = s->lanes[k];
     if (ln.busy) continue;
+    if (budget_kv > 0 && s->reserved + s->pending.front().need > budget_kv) {
+      s->st.kv_wait_steps += 1;
+      break;
+    }
+    s->reserved += s->pending.front().need;
+    s->st.kv_reserved_max = std::max(s->st.kv_reserved_max, s->reserved);
     int rc = s->eng->reset(k);
     if (rc) return s->fail(rc, "lane reset: " + s->eng->error());
     ln.busy = true;
@@ -265,6 +295,10 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
   }
   const int n = (int)s->b_lanes.size();
   if (n == 0) return FS_OK;
+  if (!s->clock_started) {
+    s->clock_started = true;
+    s->t_first = std::chrono::steady_clock::now();
+  }
   // ---- one batched step, then one sample over the step's rows
   int rc = s->eng->step(s->b_lanes.data(), s->b_pos.data(), s->b_tok.data(), n, chunked);
   if (rc) return s->fail(rc, "decode step: " + s->eng->error());
@@ -281,6 +315,7 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
   rc = s->eng->sample(n, s->b_temp.data(), s->b_seed.data(), s->b_ctr.data(), s->b_out.data());
   if (rc) return s->fail(rc, "sample: " + s->eng->error());
   s->last_batch = s->b_lanes;
+  s->t_last = std::chrono::steady_clock::now();
   s->st.steps += 1;
   s->st.occupancy_last = n;
   s->st.occupancy_max = std::max(s->st.occupancy_max, n);
@@ -306,6 +341,7 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
     ln.last = t;
     if ((int)ln.gen.size() >= ln.job.max_new || (ln.job.stop >= 0 && t == ln.job.stop)) {
       s->done[ln.job.id] = ln.gen;
+      s->reserved -= ln.job.need;
       ln.busy = false;
       s->st.jobs_done += 1;
       ++retired;
@@ -353,6 +389,12 @@ int fs_sched_get_stats(const fs_sched* s, fs_sched_stats* out) {
   out->active = active;
   out->queued = (int32_t)s->pending.size();
   out->occupancy_avg = s->st.steps ? s->occ_sum / (double)s->st.steps : 0.0;
+  out->kv_reserved_tokens = s->reserved;
+  out->seconds = s->clock_started
+                     ? std::chrono::duration<double>(s->t_last - s->t_first).count()
+                     : 0.0;
+  out->prefill_tok_s = out->seconds > 0 ? (double)s->st.prefill_tokens / out->seconds : 0.0;
+  out->decode_tok_s = out->seconds > 0 ? (double)s->st.decode_tokens / out->seconds : 0.0;
   return FS_OK;
 }
 

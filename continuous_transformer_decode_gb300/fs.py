@@ -18,7 +18,8 @@ FS_OK = 0
 ERRORS = {-1: "FS_ERR_ARG", -2: "FS_ERR_LANE", -3: "FS_ERR_DUP_LANE",
           -4: "FS_ERR_POSITION", -5: "FS_ERR_TOKEN", -6: "FS_ERR_KV_FULL",
           -7: "FS_ERR_OOM", -8: "FS_ERR_CUDA", -9: "FS_ERR_STATE",
-          -10: "FS_ERR_DEVICE", -11: "FS_ERR_SCRATCH", -12: "FS_ERR_QUEUE_FULL"}
+          -10: "FS_ERR_DEVICE", -11: "FS_ERR_SCRATCH", -12: "FS_ERR_QUEUE_FULL",
+          -13: "FS_ERR_KV_BUDGET"}
 CODES = {v: k for k, v in ERRORS.items()}
 FS_DTYPE_F32, FS_DTYPE_BF16, FS_DTYPE_Q8_0 = 0, 1, 2
 
@@ -55,7 +56,8 @@ class fs_weights(C.Structure):
 
 class fs_sched_config(C.Structure):
     _fields_ = [("lanes", C.c_int32), ("max_prefill_tokens_per_tick", C.c_int32),
-                ("max_queue", C.c_int32), ("prefill_chunk", C.c_int32)]
+                ("max_queue", C.c_int32), ("prefill_chunk", C.c_int32),
+                ("kv_budget_tokens", C.c_int64)]
 
 
 class fs_job(C.Structure):
@@ -70,7 +72,12 @@ class fs_sched_stats(C.Structure):
                 ("jobs_done", C.c_int64), ("rejected", C.c_int64),
                 ("active", C.c_int32), ("queued", C.c_int32),
                 ("occupancy_last", C.c_int32), ("occupancy_max", C.c_int32),
-                ("occupancy_avg", C.c_double)]
+                ("occupancy_avg", C.c_double),
+                ("rejected_queue_full", C.c_int64), ("rejected_kv_budget", C.c_int64),
+                ("kv_reserved_tokens", C.c_int64), ("kv_reserved_max", C.c_int64),
+                ("kv_budget_tokens", C.c_int64), ("kv_wait_steps", C.c_int64),
+                ("seconds", C.c_double), ("prefill_tok_s", C.c_double),
+                ("decode_tok_s", C.c_double)]
 
 
 LIB_PATH = _build.LIB
@@ -108,6 +115,7 @@ def lib():
         "fs_profile_read": (C.c_int, [p, i32, p, p, p]),
         "fs_kernel_launches": (C.c_int, [p, p]),
         "fs_gemm_path": (C.c_char_p, [p]),
+        "fs_lane_capacity": (C.c_int, [p, p]),
         "fs_attention_path": (C.c_char_p, [p]),
         "fs_device_error": (C.c_int, [p, p]),
         "fs_copy_logits": (C.c_int, [p, p]),
@@ -141,7 +149,7 @@ def exported_symbols() -> list:
             "fs_lane_reset", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
-            "fs_kernel_launches", "fs_gemm_path", "fs_attention_path", "fs_sample_device",
+            "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
             "fs_gemm_bf16", "fs_gemm_bf16_width", "fs_gemm_bf16_time", "fs_copy_logits", "fs_gemm_bf16_noalloc",
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
@@ -412,9 +420,10 @@ def _sched_check(s, rc: int) -> None:
 
 
 def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
-                    max_queue: int = 0, prefill_chunk: int = 1):
+                    max_queue: int = 0, prefill_chunk: int = 1, kv_budget_tokens: int = 0):
     s = C.c_void_p()
-    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk)
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk,
+                          kv_budget_tokens)
     rc = lib().fs_sched_create(h, C.byref(cfg), C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create failed")
@@ -423,9 +432,11 @@ def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
 
 def fs_sched_create_model_free(lanes: int, vocab: int,
                                max_prefill_tokens_per_tick: int = 1,
-                               max_queue: int = 0, prefill_chunk: int = 1):
+                               max_queue: int = 0, prefill_chunk: int = 1,
+                               kv_budget_tokens: int = 0):
     s = C.c_void_p()
-    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk)
+    cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk,
+                          kv_budget_tokens)
     rc = lib().fs_sched_create_model_free(C.byref(cfg), vocab, C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create_model_free failed")

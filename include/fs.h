@@ -217,6 +217,9 @@ int fs_profile_enable(fs_handle* h, int32_t enable);
 int fs_profile_read(fs_handle* h, int32_t cls, double* ms_out,
                     int64_t* launches_out, double* bytes_out);
 
+/* Tokens one lane can hold (the descriptor's max_pos). */
+int fs_lane_capacity(const fs_handle* h, int32_t* tokens_out);
+
 /* Current length (tokens held) of a lane. */
 int fs_lane_length(const fs_handle* h, int32_t lane, int32_t* length_out);
 

@@ -14,7 +14,14 @@
  *     "Summary": decode first, then bounded prefill — in-flight decodes
  *     always run; prompt work per tick is capped by
  *     max_prefill_tokens_per_tick, with at least one so a long prompt still
- *     progresses; a full queue is refused (backpressure).
+ *     progresses; a full queue is refused (backpressure). "Summary",
+ *     bounded admission: a session is admitted only if it fits the KV budget
+ *     (it must be able to hold its whole generation, prompt + new tokens, on
+ *     its own); what cannot fit is rejected up front with its reason; what
+ *     fits but finds no room waits in the bounded queue; KV growth stays
+ *     within the budget and returns to zero as sessions complete. Telemetry:
+ *     active sessions, queue depth, occupancy (last/avg/max), KV pressure,
+ *     prefill/decode totals and rates, rejections by reason.
  *
  * Policy (the readings taken where the pages leave it open):
  *   - fill: at the start of a step each free lane, in lane order, takes the
@@ -27,6 +34,15 @@
  *     in all; the rows list lanes in lane order and a lane's positions in
  *     ascending order; a step with a lane on several rows runs through
  *     fs_step_batch_chunked, any other through fs_decode_step_batch;
+ *   - admission: a job reserves prompt_len + max_new_tokens tokens of KV.
+ *     Submit refuses it (FS_ERR_KV_BUDGET) when that exceeds kv_budget_tokens
+ *     or the engine's tokens per lane; fill admits the oldest pending job
+ *     into a free lane only while the reservations of the lanes' jobs plus
+ *     its own stay within kv_budget_tokens, else the queue waits (oldest
+ *     first, no overtaking); a retired job releases its reservation. A
+ *     session has no external key here, so there is no duplicate check, and
+ *     activation scratch is preallocated per lane, so `lanes` is the scratch
+ *     bound;
  *   - fold: the step that consumes a prompt's last token yields the job's
  *     first generated token (from that lane's last row); the job's t-th generated token is sampled with
  *     (seed, counter = t), so a job's tokens do not depend on its lane, its
@@ -45,6 +61,7 @@ extern "C" {
 #endif
 
 #define FS_ERR_QUEUE_FULL (-12) /* bounded pending queue is full (backpressure) */
+#define FS_ERR_KV_BUDGET (-13)  /* a job's prompt + new tokens can never fit   */
 
 typedef struct fs_sched fs_sched;
 
@@ -54,6 +71,8 @@ typedef struct fs_sched_config {
   int32_t max_queue;                   /* pending jobs allowed, 0 = no bound */
   int32_t prefill_chunk;               /* prompt tokens per lane per step;
                                           0 or 1: one (no chunking)         */
+  int64_t kv_budget_tokens;            /* KV tokens reserved by the lanes'
+                                          jobs at most; 0 = no bound        */
 } fs_sched_config;
 
 typedef struct fs_job {
@@ -71,12 +90,22 @@ typedef struct fs_sched_stats {
   int64_t decode_tokens;   /* generated tokens fed back                       */
   int64_t jobs_submitted;
   int64_t jobs_done;
-  int64_t rejected;        /* submits refused with FS_ERR_QUEUE_FULL          */
+  int64_t rejected;        /* submits refused (all reasons)                   */
   int32_t active;          /* lanes holding a job                             */
   int32_t queued;          /* pending jobs                                    */
   int32_t occupancy_last;  /* lanes in the last step                          */
   int32_t occupancy_max;
-  double occupancy_avg;    /* mean lanes per step                             */
+  double occupancy_avg;    /* mean rows per step                              */
+  int64_t rejected_queue_full;  /* refused: pending queue full               */
+  int64_t rejected_kv_budget;   /* refused: prompt + new tokens cannot fit   */
+  int64_t kv_reserved_tokens;   /* KV tokens reserved by the lanes' jobs     */
+  int64_t kv_reserved_max;      /* the largest reservation so far            */
+  int64_t kv_budget_tokens;     /* the configured budget (0 = no bound)      */
+  int64_t kv_wait_steps;        /* steps where a free lane waited on the KV
+                                   budget                                    */
+  double seconds;               /* host time from the first step to the last */
+  double prefill_tok_s;         /* prefill_tokens / seconds                  */
+  double decode_tok_s;          /* decode_tokens / seconds                   */
 } fs_sched_stats;
 
 /* Scheduler over a decode handle: each step is one fs_decode_step_batch

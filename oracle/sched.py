@@ -33,12 +33,23 @@ from collections import deque
 
 class Reference:
     def __init__(self, n_lanes: int, max_prefill_tokens_per_tick: int,
-                 step_fn, sample_fn, reset_fn=None, prefill_chunk: int = 1):
+                 step_fn, sample_fn, reset_fn=None, prefill_chunk: int = 1,
+                 kv_budget_tokens: int = 0, lane_tokens: int = 0):
         self.n_lanes = n_lanes
         self.budget = max(1, int(max_prefill_tokens_per_tick))
         # prompt tokens one lane may consume in one step (chunked prefill,
         # "Fat-station continuous batching", "What /generate does today")
         self.chunk = max(1, int(prefill_chunk))
+        # bounded admission ("DGR-012", "Summary"): a job reserves its whole
+        # generation (prompt + new tokens) of KV; one that can never fit is
+        # rejected at submit, one that fits waits until the reservations of
+        # the running jobs leave room (oldest first)
+        self.kv_budget = int(kv_budget_tokens)
+        self.lane_tokens = int(lane_tokens)
+        self.reserved = 0
+        self.reserved_max = 0
+        self.rejected = []
+        self.kv_wait_steps = 0
         self.step_fn = step_fn
         self.sample_fn = sample_fn
         self.reset_fn = reset_fn
@@ -53,10 +64,17 @@ class Reference:
         self.decode_tokens = 0
         self.prefill_per_step = []
 
-    def submit(self, job: dict) -> None:
+    def submit(self, job: dict) -> bool:
         """job: id, prompt (len >= 1), max_new (>= 1), temperature, seed,
-        optional stop."""
+        optional stop. False: rejected (its prompt + new tokens exceed the
+        KV budget or the tokens one lane holds)."""
+        need = len(job["prompt"]) + job["max_new"]
+        if (self.kv_budget and need > self.kv_budget) or \
+                (self.lane_tokens and need > self.lane_tokens):
+            self.rejected.append(job["id"])
+            return False
         self.pending.append(job)
+        return True
 
     def idle(self) -> bool:
         return not self.pending and all(l is None for l in self.lanes)
@@ -64,6 +82,12 @@ class Reference:
     def _fill(self) -> None:
         for k in range(self.n_lanes):
             if self.lanes[k] is None and self.pending:
+                need = len(self.pending[0]["prompt"]) + self.pending[0]["max_new"]
+                if self.kv_budget and self.reserved + need > self.kv_budget:
+                    self.kv_wait_steps += 1
+                    break
+                self.reserved += need
+                self.reserved_max = max(self.reserved_max, self.reserved)
                 job = self.pending.popleft()
                 if self.reset_fn:
                     self.reset_fn(k)
@@ -135,6 +159,7 @@ class Reference:
             if len(ln["gen"]) >= job["max_new"] or (stop is not None
                                                     and t == stop):
                 self.done[job["id"]] = list(ln["gen"])
+                self.reserved -= len(job["prompt"]) + job["max_new"]
                 self.lanes[k] = None
                 retired.append(job["id"])
         return retired

@@ -104,3 +104,26 @@ def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise(budget, chunk,
             assert got[j["id"]] == out, j["id"]
     finally:
         fs.fs_destroy(h)
+
+
+def test_scheduler_refuses_a_job_longer_than_a_lane():
+    """The GPU engine's lane holds max_pos tokens: a job needing more is
+    refused at submit (FS_ERR_KV_BUDGET) and counted in the telemetry."""
+    cfg = synth.MODEL_T
+    W = synth.make_weights(cfg, seed=1, fmt="f32")
+    h = U.make_gpu(cfg, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=2, max_pos=32)
+    s = fs.fs_sched_create(h, 2, 4, prefill_chunk=4)
+    try:
+        with pytest.raises(fs.FsError) as e:
+            fs.fs_sched_submit(s, list(range(30)), 5)
+        assert e.value.name == "FS_ERR_KV_BUDGET"
+        jid = fs.fs_sched_submit(s, list(range(20)), 5)
+        fs.fs_sched_run(s)
+        assert len(fs.fs_sched_take(s, jid)) == 5
+        st = fs.fs_sched_get_stats(s)
+        assert st["rejected_kv_budget"] == 1 and st["rejected"] == 1
+        assert st["kv_reserved_tokens"] == 0 and st["kv_reserved_max"] == 25
+        assert st["decode_tok_s"] > 0 and st["seconds"] > 0
+    finally:
+        fs.fs_sched_destroy(s)
+        fs.fs_destroy(h)

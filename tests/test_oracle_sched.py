@@ -171,3 +171,30 @@ def test_scheduler_reference_stop_id_and_lane_reuse(tiny_engine):
     done = ref.run([dict(job, stop=stop), dict(job, id=1, arrive=0)])
     assert done[0] == full[:first + 1]  # retired on the stop id
     assert done[1] == full              # the freed lane serves the next job
+
+
+def test_scheduler_reference_kv_budget_admission(tiny_engine):
+    """Bounded admission ("DGR-012", "Summary"): a job whose prompt + new
+    tokens exceed the budget is rejected up front; the others wait until the
+    running jobs' reservations leave room, never exceed the budget, release
+    it as they retire, and still get their serial tokens."""
+    cfg, m = tiny_engine
+    g = np.random.default_rng(6)
+    jobs = [dict(id=j, arrive=int(g.integers(0, 6)),
+                 prompt=synth.make_prompts(1, int(g.integers(1, 20)), cfg["V"],
+                                           seed=300 + j)[0],
+                 max_new=int(g.integers(1, 10)),
+                 temperature=0.0 if j % 2 else 0.8, seed=3000 + j) for j in range(10)]
+    budget = 22
+    step_fn, reset_fn, sample_fn = _engine_rows(m, 4)
+    ref = S.Reference(4, 8, step_fn, sample_fn, reset_fn, prefill_chunk=4,
+                      kv_budget_tokens=budget)
+    done = ref.run(jobs)
+    too_big = [j["id"] for j in jobs if len(j["prompt"]) + j["max_new"] > budget]
+    assert ref.rejected == too_big and too_big
+    assert sorted(done) == sorted(j["id"] for j in jobs if j["id"] not in too_big)
+    assert ref.reserved == 0 and ref.reserved_max <= budget and ref.kv_wait_steps > 0
+    s_step, s_reset, s_sample = _engine(m, 1)
+    for job in jobs:
+        if job["id"] in done:
+            assert done[job["id"]] == S.serial_job(job, s_step, s_sample, s_reset), job["id"]

@@ -61,45 +61,63 @@ def _jobs(n, vocab, seed, max_prompt=9, max_new=9):
     return jobs
 
 
-@pytest.mark.parametrize("lanes,budget,chunk,seed", [
-    (1, 1, 1, 0), (3, 1, 1, 1), (4, 2, 1, 2), (8, 3, 1, 3), (5, 100, 1, 4),
+@pytest.mark.parametrize("lanes,budget,chunk,kv,seed", [
+    (1, 1, 1, 0, 0), (3, 1, 1, 0, 1), (4, 2, 1, 0, 2), (8, 3, 1, 0, 3), (5, 100, 1, 0, 4),
     # chunked prefill: several prompt tokens of a lane in one step
-    (4, 6, 3, 5), (3, 20, 8, 6), (8, 5, 2, 7), (2, 1, 4, 8), (6, 100, 100, 9)])
-def test_product_scheduler_matches_reference(lanes, budget, chunk, seed):
+    (4, 6, 3, 0, 5), (3, 20, 8, 0, 6), (8, 5, 2, 0, 7), (2, 1, 4, 0, 8), (6, 100, 100, 0, 9),
+    # bounded admission: a KV budget (tokens) smaller than the lanes could hold
+    (4, 2, 1, 14, 10), (6, 8, 4, 35, 11), (3, 100, 100, 25, 12)])
+def test_product_scheduler_matches_reference(lanes, budget, chunk, kv, seed):
     vocab = 97
     jobs = _jobs(24, vocab, seed, max_prompt=9 if chunk == 1 else 30)
     model = HashModel(lanes, vocab)
     ref = S.Reference(lanes, budget, model.step, model.sample, model.reset,
-                      prefill_chunk=chunk)
+                      prefill_chunk=chunk, kv_budget_tokens=kv)
     want = ref.run(jobs)
 
-    s = fs.fs_sched_create_model_free(lanes, vocab, budget, prefill_chunk=chunk)
+    s = fs.fs_sched_create_model_free(lanes, vocab, budget, prefill_chunk=chunk,
+                                      kv_budget_tokens=kv)
     try:
         order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
-        ids, i, tick, batches = {}, 0, 0, []
+        ids, i, tick, batches, rejected = {}, 0, 0, [], []
         while i < len(order) or fs.fs_sched_get_stats(s)["active"] or \
                 fs.fs_sched_get_stats(s)["queued"]:
             while i < len(order) and order[i]["arrive"] <= tick:
                 j = order[i]
-                ids[j["id"]] = fs.fs_sched_submit(
-                    s, j["prompt"], j["max_new"], j["temperature"], j["seed"],
-                    -1 if j["stop"] is None else j["stop"])
+                try:
+                    ids[j["id"]] = fs.fs_sched_submit(
+                        s, j["prompt"], j["max_new"], j["temperature"], j["seed"],
+                        -1 if j["stop"] is None else j["stop"])
+                except fs.FsError as e:
+                    assert e.code == -13, e  # FS_ERR_KV_BUDGET
+                    rejected.append(j["id"])
                 i += 1
             before = fs.fs_sched_get_stats(s)["steps"]
             fs.fs_sched_step(s)
-            if fs.fs_sched_get_stats(s)["steps"] > before:
+            st = fs.fs_sched_get_stats(s)
+            if kv:
+                assert st["kv_reserved_tokens"] <= kv
+            if st["steps"] > before:
                 batches.append(fs.fs_sched_last_batch(s))
             tick += 1
         assert batches == model.batches
+        assert rejected == ref.rejected
         for j in jobs:
-            assert fs.fs_sched_take(s, ids[j["id"]]) == want[j["id"]]
+            if j["id"] not in rejected:
+                assert fs.fs_sched_take(s, ids[j["id"]]) == want[j["id"]]
         st = fs.fs_sched_get_stats(s)
+        assert st["rejected_kv_budget"] == len(ref.rejected) == st["rejected"]
+        assert st["kv_reserved_tokens"] == 0 and st["kv_budget_tokens"] == kv
+        assert st["kv_reserved_max"] == ref.reserved_max
+        assert st["kv_wait_steps"] == ref.kv_wait_steps
+        if kv:
+            assert ref.kv_wait_steps > 0 or len(ref.rejected) > 0
         assert st["steps"] == ref.steps
         assert st["prefill_tokens"] == ref.prefill_tokens
         assert st["decode_tokens"] == ref.decode_tokens
         assert st["occupancy_max"] == max(ref.occupancy)
         assert abs(st["occupancy_avg"] - np.mean(ref.occupancy)) < 1e-12
-        assert st["jobs_done"] == len(jobs)
+        assert st["jobs_done"] == len(jobs) - len(rejected)
     finally:
         fs.fs_sched_destroy(s)
 
