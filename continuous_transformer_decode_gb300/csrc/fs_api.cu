@@ -127,6 +127,14 @@ struct fs_handle {
   uint64_t* d_seeds = nullptr;
   uint64_t* d_counters = nullptr;
   int32_t* d_tokens = nullptr;
+  // greedy steps: tile maxima of the LM head's argmax epilogue, the step's
+  // tokens, and zero temperatures / seeds / counters for the sampler fallback
+  bool greedy_fused = false;
+  float* am_val = nullptr;
+  int* am_idx = nullptr;
+  int32_t* d_greedy = nullptr;
+  float* d_zero_temps = nullptr;
+  uint64_t* d_zero_u64 = nullptr;
   unsigned char* h_samp = nullptr;  // pinned staging for sampler I/O
 
   cudaStream_t own_stream = nullptr;
@@ -464,9 +472,14 @@ int create_impl(fs_handle* h, const fs_weights* W) {
             h->alloc(&h->d_temps, (size_t)B * 4) == cudaSuccess &&
             h->alloc(&h->d_seeds, (size_t)B * 8) == cudaSuccess &&
             h->alloc(&h->d_counters, (size_t)B * 8) == cudaSuccess &&
-            h->alloc(&h->d_tokens, (size_t)B * 4) == cudaSuccess;
+            h->alloc(&h->d_tokens, (size_t)B * 4) == cudaSuccess &&
+            h->alloc(&h->d_greedy, (size_t)B * 4) == cudaSuccess &&
+            h->alloc(&h->d_zero_temps, (size_t)B * 4) == cudaSuccess &&
+            h->alloc(&h->d_zero_u64, (size_t)B * 8) == cudaSuccess;
   if (!ok) return h->fail(FS_ERR_OOM, "scratch allocation failed");
   FS_CK(h, cudaMemset(h->attn_counters, 0, (size_t)B * d.n_kv_heads * 4));
+  FS_CK(h, cudaMemset(h->d_zero_temps, 0, (size_t)B * 4));
+  FS_CK(h, cudaMemset(h->d_zero_u64, 0, (size_t)B * 8));
   h->attn_fused = attn_fused_supports(d.head_dim, h->G);
   {
     const char* e = getenv("FS_ATTN");
@@ -527,6 +540,12 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         return rc;
     }
     if ((rc = setup(h->head, &h->head_tc))) return rc;
+    // the argmax epilogue needs every head tile whole in one block
+    h->greedy_fused = h->head_tc.P == h->head_tc.m_tiles;
+    if (h->greedy_fused &&
+        (h->alloc(&h->am_val, (size_t)B * h->head_tc.m_tiles * 4) != cudaSuccess ||
+         h->alloc(&h->am_idx, (size_t)B * h->head_tc.m_tiles * 4) != cudaSuccess))
+      return h->fail(FS_ERR_OOM, "argmax buffer allocation failed");
     if (h->wtype == W_Q8) {  // only the embedding gather still reads row-major codes
       for (auto& L : h->layers) {
         for (Mat* m : {&L.qkv, &L.o, &L.gateup, &L.down}) {
@@ -616,7 +635,8 @@ int seed_lane_pages(fs_handle* h, int lane, int n) {
 // Enqueues every kernel of one step for the n panel rows on h->stream (the
 // per-step arguments are read from device memory, so the sequence can be
 // captured once per n and replayed).
-void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked) {
+void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
+                  int32_t* greedy) {
   const fs_model_desc& d = h->d;
   cudaStream_t s = h->stream;
   const StepArgs& args = h->args;
@@ -631,7 +651,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked)
   auto gemm = [&](const Mat& W, const TcW& T, const CUtensorMap& tmX, const CUtensorMap& tmX64,
                   const void* X, int epi, float* of, void* ox, int ldo, int n_out) {
     double bytes = wbytes(W) + (double)n * W.K * xs;
-    bytes += epi == EPI_SWIGLU ? (double)n * n_out * xs
+    bytes += epi == EPI_ARGMAX ? (double)n * T.m_tiles * 8.0
+             : epi == EPI_SWIGLU ? (double)n * n_out * xs
              : (double)n * n_out * 4.0 * (epi == EPI_RESID ? 2 : 1);
     if (!h->use_tc) {
       GemmArgs g{};
@@ -648,6 +669,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked)
     p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
     p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
+    p.am_val = h->am_val; p.am_idx = h->am_idx;
     if (h->wtype == W_Q8)
       h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc_q8(tmX64, tmX, p, s); });
     else
@@ -730,7 +752,20 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked)
       return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
                             h->Kp_d, s);
     });
+  if (greedy && h->greedy_fused) {  // greedy tokens straight from the head's epilogue
+    gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_ARGMAX, nullptr, nullptr,
+         d.vocab, d.vocab);
+    h->launch(FS_PROF_OTHER, (double)n * (h->head_tc.m_tiles * 8.0 + 4.0), [&] {
+      return launch_argmax_tiles(h->am_val, h->am_idx, n, h->head_tc.m_tiles, greedy, s);
+    });
+    return;
+  }
   gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  if (greedy)
+    h->launch(FS_PROF_OTHER, (double)n * d.vocab * 4.0, [&] {
+      return launch_sample(out, n, d.vocab, h->d_zero_temps, h->d_zero_u64, h->d_zero_u64,
+                           greedy, s);
+    });
 }
 
 }  // namespace
@@ -794,8 +829,11 @@ namespace {
 // Commit and launch of a validated step: page allocation (per lane in
 // position order, lowest free index first), the argument block, then the
 // kernels (one graph replay per (n, mode)).
+int decode_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
+                int32_t n, float* logits_out, int32_t* greedy_out);
+
 int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
-             int n, float* logits_out, bool chunked) {
+             int n, float* logits_out, bool chunked, int32_t* greedy_out = nullptr) {
   const fs_model_desc& d = h->d;
   FS_CK(h, cudaEventSynchronize(h->args_done));  // staging no longer in use
   const int B = d.max_lanes;
@@ -834,14 +872,15 @@ int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32
   for (int i = 0; i < n; ++i)
     kv_read += (double)(positions[i] + 1) * h->Nkv * 2.0 * (h->kv.kv_f32 ? 4.0 : 2.0);
   float* out = logits_out ? logits_out : h->logits;
+  int32_t* greedy = greedy_out ? h->d_greedy : nullptr;
   if (!logits_out && !h->prof_on && h->graphs_on) {
-    const int key = chunked ? n + (1 << 20) : n;
+    const int key = n + (chunked ? (1 << 20) : 0) + (greedy ? (2 << 20) : 0);
     auto it = h->graphs.find(key);
     if (it == h->graphs.end()) {
       const int64_t before = h->launches;
       cudaGraph_t g = nullptr;
       FS_CK(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
-      enqueue_step(h, n, out, kv_read, chunked);
+      enqueue_step(h, n, out, kv_read, chunked, greedy);
       cudaError_t e = cudaStreamEndCapture(h->stream, &g);
       if (e != cudaSuccess) return h->cuda_fail(e, "cudaStreamEndCapture");
       fs_handle::Graph G;
@@ -855,24 +894,49 @@ int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32
     FS_CK(h, cudaGraphLaunch(it->second.exec, h->stream));
     h->launches += it->second.kernels;
   } else {
-    enqueue_step(h, n, out, kv_read, chunked);
+    enqueue_step(h, n, out, kv_read, chunked, greedy);
   }
   FS_CK(h, cudaGetLastError());
+  if (greedy_out)
+    FS_CK(h, cudaMemcpyAsync(greedy_out, h->d_greedy, (size_t)n * 4, cudaMemcpyDefault,
+                             h->stream));
 
   for (int i = 0; i < n; ++i) {
     h->len[lanes[i]] += 1;
     positions[i] += 1;
   }
-  h->last_n = n;
-  h->last_logits = out;
+  h->last_n = greedy_out ? -1 : n;  // a greedy step leaves no logits to sample
+  h->last_logits = greedy_out ? nullptr : out;
   return FS_OK;
 }
 }  // namespace
 
 extern "C" {
 
+int fs_decode_step_greedy(fs_handle* h, const int32_t* lanes, int32_t* positions,
+                          const int32_t* tokens, int32_t n, int32_t* tokens_out) {
+  if (!h) return FS_ERR_ARG;
+  if (n > 0 && !tokens_out) return h->fail(FS_ERR_ARG, "NULL tokens_out");
+  const int rc = decode_step(h, lanes, positions, tokens, n, nullptr, tokens_out);
+  if (rc != FS_OK || n == 0) return rc;
+  cudaPointerAttributes at{};
+  const bool dev = cudaPointerGetAttributes(&at, tokens_out) == cudaSuccess &&
+                   (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged);
+  cudaGetLastError();  // a plain host pointer may leave an error behind
+  if (!dev) FS_CK(h, cudaStreamSynchronize(h->stream));  // host tokens written on return
+  return FS_OK;
+}
+
 int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
                          const int32_t* tokens, int32_t n, float* logits_out) {
+  return decode_step(h, lanes, positions, tokens, n, logits_out, nullptr);
+}
+
+}  // extern "C"
+
+namespace {
+int decode_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
+                int32_t n, float* logits_out, int32_t* greedy_out) {
   if (!h) return FS_ERR_ARG;
   if (n == 0) return FS_OK;
   if (n < 0 || n > h->d.max_lanes) return h->fail(FS_ERR_ARG, "n outside [0, max_lanes]");
@@ -892,8 +956,11 @@ int fs_decode_step_batch(fs_handle* h, const int32_t* lanes, int32_t* positions,
     if (h->len[k] % d.page_size == 0) ++need;
   }
   if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
-  return run_step(h, lanes, positions, tokens, n, logits_out, false);
+  return run_step(h, lanes, positions, tokens, n, logits_out, false, greedy_out);
 }
+}  // namespace
+
+extern "C" {
 
 int fs_step_batch_chunked(fs_handle* h, const int32_t* lanes, int32_t* positions,
                           const int32_t* tokens, int32_t n, float* logits_out) {

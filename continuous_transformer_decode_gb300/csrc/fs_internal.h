@@ -93,7 +93,14 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, 
   y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
 }
 
-enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+enum Epi {
+  EPI_STORE = 0,
+  EPI_RESID = 1,
+  EPI_SWIGLU = 2,
+  // per (lane, 128-row tile): the largest output and its lowest row index
+  // (greedy sampling without writing the outputs; whole-tile pieces only)
+  EPI_ARGMAX = 3
+};
 
 // Y = X * W^T over B panel rows with a fused epilogue:
 //   EPI_STORE : out_f32[b * ldo + n] = y
@@ -141,7 +148,13 @@ struct TcParams {
   // [m_tiles][kb][128][2] fp16 (one per 32 inputs)
   const int8_t* q8_codes;
   const __half* q8_scales;
+  float* am_val;   // EPI_ARGMAX: [lanes_total][m_tiles] tile maxima
+  int* am_idx;     //             and their row indices
 };
+// Per lane, the argmax over the tiles' (max, index) pairs of an EPI_ARGMAX
+// launch (lowest index on ties): tokens_out[b] for b < B.
+int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_tiles,
+                        int32_t* tokens_out, cudaStream_t s);
 // Lanes per group of one tcgen05 GEMM call: at most 256 (the MMA's N
 // limit); a matrix with fewer stream-K blocks than SMs is spread over more
 // groups of at least 32 lanes to fill about two blocks per SM. Groups split

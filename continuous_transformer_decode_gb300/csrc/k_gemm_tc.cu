@@ -31,8 +31,10 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <math_constants.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdlib>
 
 #include "fs_internal.h"
@@ -175,6 +177,64 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
       }
     }
     epi_bar();
+    return;
+  }
+  if (p.epi == EPI_ARGMAX) {
+    // per lane: (max, lowest row) over the tile's 128 rows. Eight lanes at a
+    // time: rows x lanes through shared memory, a thread scans 8 rows of one
+    // lane, then the 16 row groups combine (2 shuffles inside a warp, the 4
+    // warps in row order)
+    const int t = row_local;
+    const int j8 = t & 7, grp = t >> 3;  // lane within the half, group of 8 rows
+    float* sv = xbuf;                                      // [128][8]
+    float* wv = xbuf + 128 * 8;                            // [4][8]
+    int* wi = reinterpret_cast<int*>(wv + 4 * 8);          // [4][8]
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sv[t * 8 + j] = v[half * 8 + j];
+      epi_bar();
+      float bv = -CUDART_INF_F;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int rl = grp * 8 + r, row = m_tile * kBM + rl;
+        const float x = sv[rl * 8 + j8];
+        if (row < p.n_out && (x > bv || bi == INT_MAX)) {
+          bv = x;
+          bi = row;
+        }
+      }
+#pragma unroll
+      for (int o = 8; o < 32; o <<= 1) {  // the 4 row groups of this warp
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((t & 31) < 8) {
+        wv[(t >> 5) * 8 + j8] = bv;
+        wi[(t >> 5) * 8 + j8] = bi;
+      }
+      epi_bar();
+      const int lane_c = c0 + half * 8 + t;  // the lane this thread stores
+      if (t < 8 && lane_c < lanes) {
+        float mv = wv[t];
+        int mi = wi[t];
+#pragma unroll
+        for (int w = 1; w < 4; ++w)
+          if (wv[w * 8 + t] > mv) {  // later warps hold larger rows
+            mv = wv[w * 8 + t];
+            mi = wi[w * 8 + t];
+          }
+        const int64_t at = (int64_t)(lane0 + lane_c) * p.m_tiles + m_tile;
+        p.am_val[at] = mv;
+        p.am_idx[at] = mi;
+      }
+      epi_bar();
+    }
     return;
   }
   const int row = m_tile * kBM + row_local;
@@ -690,6 +750,46 @@ int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUten
 int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const TcParams& p,
                       cudaStream_t s) {
   return launch_impl<true>(tmX64, tmX64, tmX16, p, s);  // the W map is unused
+}
+
+namespace {
+// One warp per lane: the argmax over the lane's tile maxima, lowest index on
+// ties (each lane of the warp scans tiles t = lane, lane + 32, ... upward).
+__global__ void k_argmax_tiles(const float* __restrict__ am_val, const int* __restrict__ am_idx,
+                               int B, int m_tiles, int32_t* __restrict__ tokens_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int ln = threadIdx.x & 31;
+  if (b >= B) return;
+  float bv = -CUDART_INF_F;
+  int bi = INT_MAX;
+  for (int t = ln; t < m_tiles; t += 32) {
+    const float v = am_val[(int64_t)b * m_tiles + t];
+    const int i = am_idx[(int64_t)b * m_tiles + t];
+    if (v > bv || (v == bv && i < bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  if (ln == 0) tokens_out[b] = bi;
+}
+}  // namespace
+
+int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_tiles,
+                        int32_t* tokens_out, cudaStream_t s) {
+  if (B <= 0) return 0;
+  launch_k(k_argmax_tiles, (B + 3) / 4, 128, 0, s, am_val, am_idx, B, m_tiles, tokens_out);
+  return 1;
 }
 
 int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,

@@ -103,6 +103,7 @@ def lib():
         "fs_lane_reset": (C.c_int, [p, i32]),
         "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
         "fs_step_batch_chunked": (C.c_int, [p, p, p, p, i32, p]),
+        "fs_decode_step_greedy": (C.c_int, [p, p, p, p, i32, p]),
         "fs_sample": (C.c_int, [p, i32, p, p, p, p]),
         "fs_lane_length": (C.c_int, [p, i32, p]),
         "fs_lane_pages": (C.c_int, [p, i32, p, i32, p]),
@@ -146,7 +147,7 @@ def lib():
 def exported_symbols() -> list:
     """Names of the entry points declared in include/fs.h."""
     return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
-            "fs_lane_reset", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_sample",
+            "fs_lane_reset", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
@@ -244,6 +245,26 @@ def fs_decode_step_batch(h, lanes, positions, tokens, logits_out=None):
     _check(h, lib().fs_decode_step_batch(h, _ptr(la), _ptr(po), _ptr(to), n,
                                          _dptr(logits_out)))
     return po
+
+
+def fs_decode_step_greedy(h, lanes, positions, tokens, tokens_out=None):
+    """Decode step + greedy token per lane without materialising logits.
+    tokens_out: torch CUDA int32 [n] (no synchronisation) or None for a host
+    numpy array. ``positions`` (np.int32) is incremented in place."""
+    la = _i32(lanes)
+    to = _i32(tokens)
+    if (isinstance(positions, np.ndarray) and positions.dtype == np.int32
+            and positions.flags["C_CONTIGUOUS"]):
+        po = positions
+    else:
+        po = _i32(positions)
+    n = la.size
+    assert po.size == n and to.size == n
+    host = tokens_out is None
+    out = np.empty(n, dtype=np.int32) if host else tokens_out
+    _check(h, lib().fs_decode_step_greedy(h, _ptr(la), _ptr(po), _ptr(to), n,
+                                          _ptr(out) if host else _dptr(out)))
+    return out
 
 
 def fs_step_batch_chunked(h, lanes, positions, tokens, logits_out=None):

@@ -152,6 +152,23 @@ int fs_decode_step_batch(fs_handle* h, const int32_t* lanes,
                          int32_t* positions, const int32_t* tokens, int32_t n,
                          float* logits_out);
 
+/* decode_step_batch followed by greedy sampling, without materialising the
+ * logits: the LM head's GEMM epilogue keeps, per lane and 128-row vocab
+ * tile, the largest logit and its lowest index, and a small kernel takes each
+ * lane's argmax over its tiles (lowest index on ties), the token fs_sample
+ * returns with temperature 0 for the same step. Lanes, positions, tokens and
+ * errors as fs_decode_step_batch. tokens_out: int32 [n] in DEVICE memory
+ * (ready once the stream reaches this point; the call does not synchronise)
+ * or host memory (written before the call returns). When the handle's LM head
+ * is split across blocks the logits are written and argmaxed by the sampler
+ * kernel instead (same tokens). After this call fs_sample refuses
+ * (FS_ERR_STATE): the step left no logits. The pages have this as "fused
+ * sampling" in their cost notes (the LM head's [B, V] output dominates the
+ * small model at large B). */
+int fs_decode_step_greedy(fs_handle* h, const int32_t* lanes,
+                          int32_t* positions, const int32_t* tokens, int32_t n,
+                          int32_t* tokens_out);
+
 /* decode_step_batch with chunked prefill: the prompt of a lane is consumed in
  * chunks ("Fat-station continuous batching", "What /generate does today":
  * the prompt is prefilled in chunks) within one batched step, next to the
