@@ -97,6 +97,8 @@ struct fs_handle {
   std::vector<std::vector<int32_t>> pt;  // host page tables
   std::vector<int32_t> len;              // lane lengths
   std::set<int32_t> free_pages;
+  std::vector<int32_t> page_ref;     // lanes holding each page (0: free)
+  int32_t* d_reloc_pt = nullptr;     // [max_pages_per_lane]: a table before a move
 
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
@@ -434,6 +436,9 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   h->pt.assign(d.max_lanes, {});
   h->len.assign(d.max_lanes, 0);
   for (int p = 0; p < d.n_pages; ++p) h->free_pages.insert(p);
+  h->page_ref.assign(d.n_pages, 0);
+  if (h->alloc(&h->d_reloc_pt, (size_t)kv.max_pages * 4) != cudaSuccess)
+    return h->fail(FS_ERR_OOM, "page table scratch allocation failed");
 
   // ---- RoPE tables: cos/sin of pos * theta^(-2i/hd), in double, to f32
   {
@@ -605,15 +610,26 @@ void destroy_impl(fs_handle* h) {
   if (h->own_stream) cudaStreamDestroy(h->own_stream);
 }
 
+// The lowest free page, now held by one lane.
+int32_t take_page(fs_handle* h) {
+  const int32_t p = *h->free_pages.begin();
+  h->free_pages.erase(h->free_pages.begin());
+  h->page_ref[p] = 1;
+  return p;
+}
+
+// One lane lets go of page p; the page is free once no lane holds it.
+void release_page(fs_handle* h, int32_t p) {
+  if (--h->page_ref[p] == 0) h->free_pages.insert(p);
+}
+
 // Allocates pages for `n` more tokens of lane k starting at its current
 // length (lowest free index first). Caller has checked capacity.
 void take_pages(fs_handle* h, int k, int n_tokens_after) {
   const int ps = h->d.page_size;
   const int need = (n_tokens_after + ps - 1) / ps;
   while ((int)h->pt[k].size() < need) {
-    const int p = *h->free_pages.begin();
-    h->free_pages.erase(h->free_pages.begin());
-    h->pt[k].push_back(p);
+    h->pt[k].push_back(take_page(h));
   }
 }
 
@@ -817,9 +833,78 @@ int fs_set_stream(fs_handle* h, void* stream) {
 int fs_lane_reset(fs_handle* h, int32_t lane) {
   if (!h) return FS_ERR_ARG;
   if (lane < 0 || lane >= h->d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
-  for (int32_t p : h->pt[lane]) h->free_pages.insert(p);
+  for (int32_t p : h->pt[lane]) release_page(h, p);
   h->pt[lane].clear();
   h->len[lane] = 0;
+  return FS_OK;
+}
+
+int fs_lane_clone(fs_handle* h, int32_t src, int32_t dst) {
+  if (!h) return FS_ERR_ARG;
+  const int B = h->d.max_lanes, ps = h->d.page_size;
+  if (src < 0 || src >= B || dst < 0 || dst >= B) return h->fail(FS_ERR_LANE, "lane out of range");
+  if (src == dst) return h->fail(FS_ERR_ARG, "src and dst are the same lane");
+  if (h->len[dst] != 0 || !h->pt[dst].empty()) return h->fail(FS_ERR_STATE, "dst lane is not empty");
+  const int n = h->len[src], full = n / ps;
+  const bool partial = n % ps != 0;
+  if (partial && h->free_pages.empty()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  // full pages are shared (never written again: later tokens go to later
+  // pages); the partial last page, which both lanes go on writing, is copied
+  std::vector<int32_t> t(h->pt[src].begin(), h->pt[src].begin() + full);
+  for (int32_t p : t) ++h->page_ref[p];
+  if (partial) t.push_back(take_page(h));
+  h->pt[dst] = std::move(t);
+  h->len[dst] = n;
+  if (h->pt[dst].empty()) return FS_OK;
+  int32_t* dst_row = h->kv.pt + (size_t)dst * h->kv.max_pages;
+  FS_CK(h, cudaMemcpyAsync(dst_row, h->pt[dst].data(), h->pt[dst].size() * 4,
+                           cudaMemcpyHostToDevice, h->stream));
+  if (partial) {
+    h->launches += launch_kv_relocate(h->kv, h->d.n_layers, h->kv.pt + (size_t)src * h->kv.max_pages,
+                                      dst_row, full * ps, n, n, 0, h->rope_cos, h->rope_sin,
+                                      h->stream);
+    FS_CK(h, cudaGetLastError());
+  }
+  return FS_OK;
+}
+
+int fs_lane_evict(fs_handle* h, int32_t lane, int32_t start, int32_t end) {
+  if (!h) return FS_ERR_ARG;
+  if (lane < 0 || lane >= h->d.max_lanes) return h->fail(FS_ERR_LANE, "lane out of range");
+  const int n = h->len[lane], ps = h->d.page_size;
+  if (start < 0 || start > end || end > n) return h->fail(FS_ERR_ARG, "span outside [0, length]");
+  if (start == end) return FS_OK;
+  const int delta = end - start, nl = n - delta;
+  const int keep = (nl + ps - 1) / ps, first = start / ps;
+  const std::vector<int32_t> old = h->pt[lane];
+  // pages [first, keep) are written (moved rows now, the next token later):
+  // a page another lane still holds is replaced by a private copy
+  int need = 0;
+  for (int x = first; x < keep; ++x) need += h->page_ref[old[x]] > 1;
+  if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  std::vector<int32_t> t(old.begin(), old.begin() + keep);
+  for (int x = first; x < keep; ++x)
+    if (h->page_ref[old[x]] > 1) {
+      --h->page_ref[old[x]];
+      t[x] = take_page(h);
+    }
+  // rows [start, nl) move down by delta; a replaced first page also takes
+  // its rows below start
+  const int q_begin = (first < keep && t[first] != old[first]) ? first * ps : start;
+  if (q_begin < nl) {
+    int32_t* row = h->kv.pt + (size_t)lane * h->kv.max_pages;
+    FS_CK(h, cudaMemcpyAsync(h->d_reloc_pt, row, old.size() * 4, cudaMemcpyDeviceToDevice,
+                             h->stream));
+    FS_CK(h, cudaMemcpyAsync(row, t.data(), t.size() * 4, cudaMemcpyHostToDevice, h->stream));
+    h->launches += launch_kv_relocate(h->kv, h->d.n_layers, h->d_reloc_pt, row, q_begin, nl,
+                                      start, delta, h->rope_cos, h->rope_sin, h->stream);
+    FS_CK(h, cudaGetLastError());
+  }
+  // pages past the new end are let go (stream order keeps them unwritten
+  // until the move above has read them)
+  for (int x = keep; x < (int)old.size(); ++x) release_page(h, old[x]);
+  h->pt[lane] = std::move(t);
+  h->len[lane] = nl;
   return FS_OK;
 }
 

@@ -266,5 +266,11 @@ int launch_import_kv(const KV& kv, int layer, const int32_t* pages, int n,
                      const float* k, const float* v, cudaStream_t s);
 int launch_export_kv(const KV& kv, int layer, const int32_t* pages, int n,
                      float* k, float* v, cudaStream_t s);
+// Rows [q_begin, q_end) of one lane into the pages of dst_pt: row q from row
+// q (q < a) or q + delta (q >= a) of src_pt's pages, keys moved down by delta
+// turned back delta positions (k_misc.cu). Every layer, K and V.
+int launch_kv_relocate(const KV& kv, int L, const int32_t* src_pt, const int32_t* dst_pt,
+                       int q_begin, int q_end, int a, int delta, const float* rc,
+                       const float* rs, cudaStream_t s);
 
 }  // namespace fsk

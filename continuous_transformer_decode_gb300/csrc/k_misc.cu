@@ -375,6 +375,90 @@ int launch_repack_q8(const uint8_t* blocks, int N, int K, int Kp, int8_t* qs,
   return 1;
 }
 
+// Rewrites rows [q_begin, q_end) of one lane's history, in every layer, into
+// the pages of dst_pt: row q comes from row q (q < a) or from row q + delta
+// (q >= a) of the pages of src_pt, and a key that moves down by delta
+// positions is turned back by delta positions, R(-delta) R(p) k = R(p - delta) k
+// (the rotate-half pairs of the RoPE, with the tables' cos/sin at position
+// delta). One block per (layer, kv head, K|V) walks its rows in ascending
+// batches; a batch is read whole before any of it is written, and a
+// destination row q lies below every source row not yet read (q < q + delta),
+// so compaction within a shared page table is safe without a second buffer.
+constexpr int kRelocThreads = 256;
+constexpr int kRelocPairs = 4;  // rotate-half pairs per thread per batch
+
+template <typename KVT>
+__global__ void __launch_bounds__(kRelocThreads)
+k_kv_relocate(KV kv, const int32_t* __restrict__ src_pt, const int32_t* __restrict__ dst_pt,
+              int q_begin, int q_end, int a, int delta, const float* __restrict__ rc,
+              const float* __restrict__ rs) {
+  const int half = kv.hd / 2;
+  const int which = blockIdx.x & 1;  // 0: K, 1: V
+  const int g = (blockIdx.x >> 1) % kv.Hkv;
+  const int layer = (blockIdx.x >> 1) / kv.Hkv;
+  KVT* base = static_cast<KVT*>(which ? kv.v : kv.k) + (int64_t)layer * kv.layer_stride;
+  auto at = [&](int page, int slot) {
+    return base + (((int64_t)page * kv.Hkv + g) * kv.page_size + slot) * kv.hd;
+  };
+  const int rows_per_batch = kRelocThreads * kRelocPairs / half;  // half <= 128
+  for (int r0 = q_begin; r0 < q_end; r0 += rows_per_batch) {
+    float y0[kRelocPairs], y1[kRelocPairs];
+#pragma unroll
+    for (int u = 0; u < kRelocPairs; ++u) {
+      const int unit = threadIdx.x + u * kRelocThreads;
+      const int q = r0 + unit / half, i = unit % half;
+      if (unit >= rows_per_batch * half || q >= q_end) continue;
+      const int p = q < a ? q : q + delta;
+      const KVT* row = at(src_pt[p / kv.page_size], p % kv.page_size);
+      float x0, x1;
+      if constexpr (sizeof(KVT) == 2) {
+        x0 = __bfloat162float(row[i]);
+        x1 = __bfloat162float(row[i + half]);
+      } else {
+        x0 = row[i];
+        x1 = row[i + half];
+      }
+      if (which == 0 && q >= a && delta > 0) {
+        const float c = rc[(int64_t)delta * half + i], sn = rs[(int64_t)delta * half + i];
+        rope_pair(x0, x1, c, -sn, y0[u], y1[u]);
+      } else {
+        y0[u] = x0;
+        y1[u] = x1;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kRelocPairs; ++u) {
+      const int unit = threadIdx.x + u * kRelocThreads;
+      const int q = r0 + unit / half, i = unit % half;
+      if (unit >= rows_per_batch * half || q >= q_end) continue;
+      KVT* row = at(dst_pt[q / kv.page_size], q % kv.page_size);
+      if constexpr (sizeof(KVT) == 2) {
+        row[i] = __float2bfloat16_rn(y0[u]);
+        row[i + half] = __float2bfloat16_rn(y1[u]);
+      } else {
+        row[i] = y0[u];
+        row[i + half] = y1[u];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+int launch_kv_relocate(const KV& kv, int L, const int32_t* src_pt, const int32_t* dst_pt,
+                       int q_begin, int q_end, int a, int delta, const float* rc,
+                       const float* rs, cudaStream_t s) {
+  if (q_end <= q_begin || kv.hd > 2 * kRelocThreads * kRelocPairs) return 0;
+  const unsigned grid = (unsigned)L * kv.Hkv * 2;
+  if (kv.kv_f32)
+    k_kv_relocate<float><<<grid, kRelocThreads, 0, s>>>(kv, src_pt, dst_pt, q_begin, q_end, a,
+                                                        delta, rc, rs);
+  else
+    k_kv_relocate<__nv_bfloat16><<<grid, kRelocThreads, 0, s>>>(kv, src_pt, dst_pt, q_begin,
+                                                                q_end, a, delta, rc, rs);
+  return 1;
+}
+
 int launch_fill_random_kv(const KV& kv, int L, const int32_t* pages,
                           int n_pages, uint64_t seed, cudaStream_t s) {
   if (n_pages <= 0) return 0;

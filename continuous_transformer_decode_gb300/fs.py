@@ -101,6 +101,8 @@ def lib():
         "fs_last_error": (C.c_char_p, [p]),
         "fs_set_stream": (C.c_int, [p, p]),
         "fs_lane_reset": (C.c_int, [p, i32]),
+        "fs_lane_clone": (C.c_int, [p, i32, i32]),
+        "fs_lane_evict": (C.c_int, [p, i32, i32, i32]),
         "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
         "fs_step_batch_chunked": (C.c_int, [p, p, p, p, i32, p]),
         "fs_decode_step_greedy": (C.c_int, [p, p, p, p, i32, p]),
@@ -147,7 +149,7 @@ def lib():
 def exported_symbols() -> list:
     """Names of the entry points declared in include/fs.h."""
     return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
-            "fs_lane_reset", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
+            "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
@@ -228,6 +230,18 @@ def fs_set_stream(h, stream) -> None:
 
 def fs_lane_reset(h, lane: int) -> None:
     _check(h, lib().fs_lane_reset(h, int(lane)))
+
+
+def fs_lane_clone(h, src: int, dst: int) -> None:
+    """Empty lane ``dst`` takes lane ``src``'s history (full pages shared,
+    the partial last page copied)."""
+    _check(h, lib().fs_lane_clone(h, int(src), int(dst)))
+
+
+def fs_lane_evict(h, lane: int, start: int, end: int) -> None:
+    """Positions [start, end) leave the lane; later entries move down, their
+    keys rotated back by end - start positions."""
+    _check(h, lib().fs_lane_evict(h, int(lane), int(start), int(end)))
 
 
 def fs_decode_step_batch(h, lanes, positions, tokens, logits_out=None):

@@ -130,9 +130,38 @@ const char* fs_last_error(const fs_handle* h);
  * the handle's own stream. */
 int fs_set_stream(fs_handle* h, void* stream);
 
-/* Fill step of the scheduler ("Components", item 3): frees lane k's pages
- * and sets its length to 0. Errors: FS_ERR_LANE. */
+/* Fill step of the scheduler ("Components", item 3): lane k lets go of its
+ * pages (a page returns to the pool once no lane holds it) and its length
+ * becomes 0. Errors: FS_ERR_LANE. */
 int fs_lane_reset(fs_handle* h, int32_t lane);
+
+/* Clone, per-user prefix reuse kept under batching ("MODEL-BATCHING-RESULTS",
+ * "Why in-kernel batching, not vLLM"): empty lane dst takes lane src's
+ * history. dst shares src's full pages (a page holds a count of the lanes
+ * that hold it; a full page is never written again), and src's partial last
+ * page, which both lanes go on writing, is copied to a new page (lowest free
+ * index) in every layer. Both lanes then have src's length, and a token fed
+ * to either gives the logits the other gives for the same token. Enqueued
+ * on the handle's stream; no synchronisation.
+ * Errors: FS_ERR_LANE, FS_ERR_ARG (src == dst), FS_ERR_STATE (dst not
+ * empty), FS_ERR_KV_FULL (a partial page and no free page); nothing changes
+ * on error. */
+int fs_lane_clone(fs_handle* h, int32_t src, int32_t dst);
+
+/* Evict, quarantine of a span of one user's history (same passage as
+ * fs_lane_clone): positions [start, end) leave the lane's cache. Entries at
+ * positions p >= end move down to p - (end - start) and their keys are
+ * rotated back by end - start positions, so the lane holds length - (end -
+ * start) consecutive positions and the next token goes at that length.
+ * K/V of the kept entries are not recomputed (they were computed while the
+ * span was present). end == length drops a suffix and moves nothing. Pages
+ * the lane writes (from the one holding `start` on) that another lane still
+ * holds are first replaced by private copies (lowest free index); pages
+ * past the new end are let go. Enqueued on the handle's stream.
+ * Errors: FS_ERR_LANE, FS_ERR_ARG (not 0 <= start <= end <= length),
+ * FS_ERR_KV_FULL (too few free pages for the copies); nothing changes on
+ * error. */
+int fs_lane_evict(fs_handle* h, int32_t lane, int32_t start, int32_t end);
 
 /* decode_step_batch. For each i < n, lane lanes[i], whose length must equal
  * positions[i], consumes tokens[i]: its K/V at that position are appended to

@@ -79,6 +79,8 @@ def lib():
             "or_lane_pos": (i, [p]),
             "or_lane_export": (None, [p, p, i, i, p]),
             "or_lane_import": (None, [p, p, i, p, p, i]),
+            "or_lane_clone": (C.c_int, [p, p]),
+            "or_lane_evict": (C.c_int, [p, p, i, i]),
             "or_step": (i, [p, p, i, p]),
             "or_step_batch": (i, [p, p, p, i, p]),
             "or_prefill": (i, [p, p, p, i, p]),
@@ -330,6 +332,17 @@ class Lane:
         out = np.empty((self.pos, c["Hkv"], c["hd"]), dtype=np.float32)
         lib().or_lane_export(self.model._h, self._h, layer, w, _ptr(out))
         return out
+
+    def clone_from(self, src: "Lane") -> None:
+        """This lane becomes a copy of ``src``'s history (Clone)."""
+        if lib().or_lane_clone(src._h, self._h):
+            raise ValueError("lanes of different max_pos")
+
+    def evict(self, start: int, end: int) -> None:
+        """Positions [start, end) leave the cache; later entries move down,
+        keys re-roped at their new positions (Evict)."""
+        if lib().or_lane_evict(self.model._h, self._h, int(start), int(end)):
+            raise ValueError("span outside [0, length]")
 
     def import_kv(self, layer: int, K: np.ndarray, V: np.ndarray) -> None:
         K = np.ascontiguousarray(K, dtype=np.float32)

@@ -465,6 +465,47 @@ void or_lane_import(void* mp, void* lp, int layer, const float* K,
   ln->pos = n;
 }
 
+// Clone ("MODEL-BATCHING-RESULTS", "Why in-kernel batching, not vLLM":
+// per-user prefix reuse): lane dst becomes a copy of lane src's history
+// (K, un-roped K, V of every layer and the length). Both lanes must have
+// the same max_pos.
+int or_lane_clone(void* srcp, void* dstp) {
+  OrLane* src = (OrLane*)srcp;
+  OrLane* dst = (OrLane*)dstp;
+  if (src->max_pos != dst->max_pos) return -1;
+  dst->K = src->K;
+  dst->Kraw = src->Kraw;
+  dst->V = src->V;
+  dst->pos = src->pos;
+  return 0;
+}
+
+// Evict (same passage: quarantine of a span of one user's history): the
+// entries at positions [start, end) leave the cache; the entry at p >= end
+// becomes the entry at p - (end - start), its V and un-roped K as they
+// were and its K the un-roped K rotated at the new position. K/V are not
+// recomputed. Returns -1 unless 0 <= start <= end <= length.
+int or_lane_evict(void* mp, void* lp, int start, int end) {
+  OrModel* m = (OrModel*)mp;
+  OrLane* ln = (OrLane*)lp;
+  if (start < 0 || start > end || end > ln->pos) return -1;
+  const or_desc& c = m->c;
+  const int delta = end - start;
+  const size_t row = (size_t)c.Hkv * c.hd;
+  for (int l = 0; l < c.L; ++l) {
+    for (int p = end; p < ln->pos; ++p) {
+      const int q = p - delta;
+      std::memcpy(ln->Kraw[l].data() + q * row, ln->Kraw[l].data() + p * row, row * 4);
+      std::memcpy(ln->V[l].data() + q * row, ln->V[l].data() + p * row, row * 4);
+      float* k = ln->K[l].data() + q * row;
+      std::memcpy(k, ln->Kraw[l].data() + q * row, row * 4);
+      or_rope(k, c.Hkv, c.hd, q, c.rope_theta);
+    }
+  }
+  ln->pos -= delta;
+  return 0;
+}
+
 // Attention sub-step for one lane after its K/V at `pos` are appended:
 // every query head h reads KV head h / (H / Hkv) over keys 0..pos.
 static void lane_attention(const OrModel* m, const OrLane* ln, int layer,
