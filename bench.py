@@ -198,7 +198,7 @@ def run_ours(args, wl, ws, rank, local):
         ctx = synth.make_context_lengths(B, *wl["ctx"], seed=3)
     else:
         ctx = np.full(B, prompt, dtype=np.int32)
-    extra = Wm + 3 * K + 8  # warm-up, timed, profiled and end-to-end steps
+    extra = Wm + 3 * K + 8 + args.trace  # warm-up, timed, profiled, end-to-end, traced steps
     max_pos = int(ctx.max()) + extra
     ps = 16
     n_pages = int(sum(-(-(int(c) + extra) // ps) for c in ctx)) + B
@@ -274,6 +274,19 @@ def run_ours(args, wl, ws, rank, local):
     tk.synchronize()
     e2e_s = time.perf_counter() - t0
 
+    # kernel timeline of a few more identical steps (outside every timed region)
+    timeline = None
+    if args.trace:
+        from continuous_transformer_decode_gb300 import trace as tr
+        fs.fs_trace_enable(h, 400000 * args.trace)
+        for _ in range(args.trace):
+            device_step()
+        recs, appended = fs.fs_trace_read(h)
+        fs.fs_trace_enable(h, 0)
+        timeline = tr.summarize(recs, args.trace)
+        timeline["records"] = int(appended)
+        print(tr.table(timeline), file=sys.stderr)
+
     # ---- B sweep on the same handle (device-timed, like `value`)
     sweep = []
     if not args.no_sweep and "ctx" not in wl:
@@ -320,7 +333,7 @@ def run_ours(args, wl, ws, rank, local):
            "h2d_bytes_per_step": arg_bytes + B * (4 + 8 + 8),
            "d2h_bytes_per_step": B * 4}
     return dict(value=value, ms=ms, B=B, launches=launches, clocks=clk, roofline=roof,
-                e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt, sweep=sweep)
+                e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt, sweep=sweep, timeline=timeline)
 
 
 def step_roofline(cfg, wbytes_per_param, lanes, ctx_mean, peaks):
@@ -508,6 +521,9 @@ def main():
                          "small profiling captures, never for a reported number)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--trace", type=int, default=0,
+                    help="after the timed steps, trace N more steps' kernel timeline "
+                         "(%%globaltimer per block) and add its summary to the line")
     ap.add_argument("--jobs", type=int, default=0,
                     help="trace workload: number of jobs (default min(512, 4 x lanes))")
     ap.add_argument("--prefill-budget", type=int, default=0,
@@ -617,6 +633,7 @@ def main():
         "cpu_baseline": cb, "e2e": r["e2e"],
         **({"reduced_layers_for_profiling": args.layers} if args.layers else {}),
         "clocks": r["clocks"], "gpu_launches": r["launches"],
+        **({"kernel_timeline": r["timeline"]} if r["timeline"] else {}),
     }
     print(json.dumps(line))
     if ws > 1:

@@ -58,6 +58,30 @@ struct LayerW {
 //    bring the launch to about two blocks per SM), s <= 8.
 // P depends on the matrix, the handle's lane capacity and the device only,
 // never on a call's lane count.
+// Kernel timeline tracing is process-wide (a device pointer in every kernel
+// translation unit); one handle at a time owns the buffer.
+TraceBuf* g_trace_buf = nullptr;
+int64_t g_trace_cap = 0;
+const fs_handle* g_trace_owner = nullptr;
+
+bool trace_install_all(TraceBuf* b) {
+  return trace_install_misc(b) && trace_install_gemm(b) && trace_install_gemv(b) &&
+         trace_install_attn(b) && trace_install_attn_mma(b) && trace_install_attn_tma(b) &&
+         trace_install_attn_tiled(b) && trace_install_attn_fused(b);
+}
+
+// Uninstalls and frees the trace buffer if h owns it (the stream has been
+// synchronised by the caller).
+int trace_release(const fs_handle* h) {
+  if (g_trace_owner != h) return FS_OK;
+  const bool ok = trace_install_all(nullptr);
+  cudaFree(g_trace_buf);
+  g_trace_buf = nullptr;
+  g_trace_cap = 0;
+  g_trace_owner = nullptr;
+  return ok ? FS_OK : FS_ERR_CUDA;
+}
+
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
   if (m_tiles >= sms) return m_tiles;
@@ -594,6 +618,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
 
 void destroy_impl(fs_handle* h) {
   if (h->stream) cudaStreamSynchronize(h->stream);
+  trace_release(h);
   for (void* p : h->allocs) cudaFree(p);
   h->allocs.clear();
   if (h->h_args) cudaFreeHost(h->h_args);
@@ -1275,6 +1300,45 @@ int fs_quantize_q8_0(const float* src, int64_t n, uint8_t* blocks_out, void* str
   launch_quantize_q8_0(src, n, blocks_out, s);
   if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FS_ERR_CUDA;
+  return FS_OK;
+}
+
+int fs_trace_enable(fs_handle* h, int64_t capacity) {
+  if (!h || capacity < 0) return FS_ERR_ARG;
+  if (capacity > 0 && g_trace_owner && g_trace_owner != h)
+    return h->fail(FS_ERR_STATE, "another handle is tracing");
+  FS_CK(h, cudaStreamSynchronize(h->stream));
+  const int rc = trace_release(h);
+  if (rc != FS_OK || capacity == 0) return rc;
+  TraceBuf* b = nullptr;
+  const size_t bytes = 16 + (size_t)capacity * sizeof(TraceRec);
+  if (cudaMalloc(&b, bytes) != cudaSuccess) return h->fail(FS_ERR_OOM, "trace buffer");
+  const unsigned long long head[2] = {0ull, (unsigned long long)capacity};
+  cudaError_t e = cudaMemcpy(b, head, sizeof head, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess || !trace_install_all(b)) {
+    cudaFree(b);
+    trace_install_all(nullptr);
+    return e != cudaSuccess ? h->cuda_fail(e, "trace buffer") : h->fail(FS_ERR_CUDA, "trace install");
+  }
+  g_trace_buf = b;
+  g_trace_cap = capacity;
+  g_trace_owner = h;
+  return FS_OK;
+}
+
+int fs_trace_read(fs_handle* h, uint64_t* records_out, int64_t cap, int64_t* appended_out,
+                  int reset) {
+  if (!h || !appended_out || cap < 0 || (cap > 0 && !records_out)) return FS_ERR_ARG;
+  if (g_trace_owner != h || !g_trace_buf) return h->fail(FS_ERR_STATE, "tracing is not enabled on this handle");
+  FS_CK(h, cudaStreamSynchronize(h->stream));
+  unsigned long long n = 0;
+  FS_CK(h, cudaMemcpy(&n, g_trace_buf, 8, cudaMemcpyDeviceToHost));
+  const int64_t m = std::min<int64_t>(std::min<int64_t>((int64_t)n, g_trace_cap), cap);
+  if (m > 0)
+    FS_CK(h, cudaMemcpy(records_out, g_trace_buf->rec, (size_t)m * sizeof(TraceRec),
+                        cudaMemcpyDeviceToHost));
+  *appended_out = (int64_t)n;
+  if (reset) FS_CK(h, cudaMemset(g_trace_buf, 0, 8));
   return FS_OK;
 }
 

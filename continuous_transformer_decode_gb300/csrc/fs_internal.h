@@ -30,6 +30,124 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 bool pdl_enabled();  // FS_PDL=0 in the environment turns the attribute off
 
+// ---- kernel timeline tracing. Off unless a buffer is installed: thread 0
+// of every block of a traced kernel then appends one record with the
+// %globaltimer time at entry, after its dependency wait, and at its end.
+// The buffer pointer is a device global of each translation unit (the
+// library is built without relocatable device code); fs_trace_enable
+// installs it in all of them.
+struct TraceRec {
+  // tag << 40 | waited << 39 | smid << 24 | linear block index; waited: the
+  // block passed its wait for the preceding kernel (a block that leaves
+  // early, e.g. an attention split past the lane's length, does not wait)
+  unsigned long long tag_sm_block;
+  unsigned long long t_entry, t_ready, t_exit;  // ns
+};
+struct TraceBuf {
+  unsigned long long count, cap;  // records appended (may exceed cap), capacity
+  TraceRec rec[1];
+};
+// record tags
+enum TraceTag {
+  TR_EMBED = 1, TR_RMSNORM = 2, TR_SAMPLE = 3, TR_ARGMAX = 4,
+  TR_ATTN_MMA = 5, TR_ATTN_TMA = 6, TR_ATTN_TILED = 7, TR_ATTN_FUSED = 8,
+  TR_ROPE_APPEND = 9, TR_GEMV = 10, TR_ATTN_PARTIAL = 11, TR_ATTN_COMBINE = 12,
+  TR_GEMV_SWIGLU = 13,
+  TR_GEMM = 16  // + the epilogue kind (Epi)
+};
+
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void trace_write(TraceBuf* b, unsigned tag, bool waited,
+                                            unsigned long long t0, unsigned long long t1) {
+  const unsigned long long i = atomicAdd(&b->count, 1ull);
+  if (i >= b->cap) return;
+  unsigned sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  const unsigned long long blk =
+      ((unsigned long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  TraceRec r;
+  r.tag_sm_block = ((unsigned long long)tag << 40) | ((unsigned long long)waited << 39) |
+                   ((unsigned long long)(sm & 0x7fff) << 24) | (blk & 0xffffff);
+  r.t_entry = t0;
+  r.t_ready = t1;
+  r.t_exit = gtime();
+  b->rec[i] = r;
+}
+
+// Thread 0's marks kept in registers.
+struct TraceMark {
+  TraceBuf* b = nullptr;
+  unsigned long long t0 = 0, t1 = 0;
+  bool waited = false;
+  __device__ __forceinline__ void begin(TraceBuf* buf) {
+    if (threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0 && buf) {
+      b = buf;
+      t0 = t1 = gtime();
+    }
+  }
+  __device__ __forceinline__ void ready() {
+    if (b) {
+      t1 = gtime();
+      waited = true;
+    }
+  }
+  __device__ __forceinline__ void end(unsigned tag) {
+    if (!b) return;
+    trace_write(b, tag, waited, t0, t1);
+    b = nullptr;
+  }
+};
+
+// Thread 0's marks kept in a __shared__ unsigned long long[4] (buffer, entry,
+// ready, waited), for kernels that have no registers to spare.
+struct TraceSmem {
+  static __device__ __forceinline__ void begin(unsigned long long* sm, TraceBuf* buf) {
+    if (threadIdx.x == 0) {
+      sm[0] = reinterpret_cast<unsigned long long>(buf);
+      sm[3] = 0;
+      if (buf) sm[1] = sm[2] = gtime();
+    }
+  }
+  static __device__ __forceinline__ void ready(unsigned long long* sm) {
+    if (threadIdx.x == 0 && sm[0]) {
+      sm[2] = gtime();
+      sm[3] = 1;
+    }
+  }
+  static __device__ __forceinline__ void end(unsigned long long* sm, unsigned tag) {
+    if (threadIdx.x == 0 && sm[0])
+      trace_write(reinterpret_cast<TraceBuf*>(sm[0]), tag, sm[3] != 0, sm[1], sm[2]);
+  }
+};
+
+// A TraceMark that writes its record when the kernel leaves its scope (for
+// kernels with several exits).
+struct TraceScope : TraceMark {
+  unsigned tag;
+  __device__ __forceinline__ TraceScope(TraceBuf* buf, unsigned t) : tag(t) { begin(buf); }
+  __device__ __forceinline__ ~TraceScope() { end(tag); }
+};
+
+// Defines this translation unit's trace pointer and its host installer.
+#define FS_TRACE_TU(name)                                                     \
+  static __device__ TraceBuf* g_trace = nullptr;                              \
+  int trace_install_##name(TraceBuf* p) {                                     \
+    return cudaMemcpyToSymbol(g_trace, &p, sizeof(p)) == cudaSuccess ? 1 : 0; \
+  }
+int trace_install_misc(TraceBuf* p);
+int trace_install_gemm(TraceBuf* p);
+int trace_install_gemv(TraceBuf* p);
+int trace_install_attn(TraceBuf* p);
+int trace_install_attn_mma(TraceBuf* p);
+int trace_install_attn_tma(TraceBuf* p);
+int trace_install_attn_tiled(TraceBuf* p);
+int trace_install_attn_fused(TraceBuf* p);
+
 // Kernel launch with the programmatic-stream-serialization attribute.
 template <typename... K, typename... A>
 inline cudaError_t launch_k(void (*kern)(K...), dim3 grid, dim3 block, size_t smem,

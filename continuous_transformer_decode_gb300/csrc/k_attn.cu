@@ -17,6 +17,7 @@
 #include "fs_internal.h"
 
 namespace fsk {
+FS_TRACE_TU(attn)
 namespace {
 
 template <typename T>
@@ -50,7 +51,9 @@ __global__ void k_rope_append(const float* __restrict__ qkv, int H, int Hkv,
                               int hd, const float* __restrict__ rc,
                               const float* __restrict__ rs, StepArgs args,
                               KV kv, int layer, float* __restrict__ q_out) {
+  TraceScope tr(g_trace, TR_ROPE_APPEND);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   const int b = blockIdx.x;
   const int lane = args.lane[b];
@@ -111,7 +114,9 @@ __global__ void __launch_bounds__(kCh)
     k_attn_partial(const float* __restrict__ q, int H, StepArgs args, KV kv,
                    int layer, int split_len, int max_splits,
                    float* __restrict__ part_ml, float* __restrict__ part_acc) {
+  TraceScope tr(g_trace, TR_ATTN_PARTIAL);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int len = args.pos[b] + 1;
@@ -205,7 +210,9 @@ __global__ void k_attn_combine(int H, int hd, StepArgs args, int split_len,
                                int max_splits, const float* __restrict__ part_ml,
                                const float* __restrict__ part_acc, OT* o,
                                int ld_o) {
+  TraceScope tr(g_trace, TR_ATTN_COMBINE);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   const int b = blockIdx.x;
   const int len = args.pos[b] + 1;

@@ -20,6 +20,7 @@
 #include "fs_internal.h"
 
 namespace fsk {
+FS_TRACE_TU(attn_fused)
 namespace {
 
 constexpr int kT = 128;   // threads = keys per chunk
@@ -74,7 +75,9 @@ __global__ void __launch_bounds__(kT)
                  int split_len, int max_splits, float* __restrict__ part_ml,
                  float* __restrict__ part_acc, int* __restrict__ counters, OT* o_panel,
                  int ld_o, int kv_written) {
+  TraceScope tr(g_trace, TR_ATTN_FUSED);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   constexpr int kHalf = HD / 2;
   constexpr int kVec = KVIO<KVT>::kVec;

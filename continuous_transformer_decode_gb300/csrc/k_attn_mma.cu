@@ -27,6 +27,7 @@
 #include "attn_mma.cuh"
 
 namespace fsk {
+FS_TRACE_TU(attn_mma)
 namespace {
 
 using namespace attn;
@@ -52,6 +53,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <typename OT, int HD>
 __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
+  TraceScope tr(g_trace, TR_ATTN_MMA);
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
   constexpr int kTileBytes = kTT * HD * 2;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
     if (n_tiles > 1) issue(1);
   }
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   if (!prefetch) {
     issue(0);

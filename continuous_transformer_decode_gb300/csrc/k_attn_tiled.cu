@@ -23,6 +23,7 @@
 #include "fs_internal.h"
 
 namespace fsk {
+FS_TRACE_TU(attn_tiled)
 namespace {
 
 constexpr int kT = 128;   // threads
@@ -101,7 +102,9 @@ __device__ __forceinline__ void st_out(__nv_bfloat16* p, float v) {
 
 template <typename KVT, typename OT, int HD>
 __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
+  TraceScope tr(g_trace, TR_ATTN_TILED);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   constexpr int kHalf = HD / 2;
   constexpr int kVec = Elem<KVT>::kVec;

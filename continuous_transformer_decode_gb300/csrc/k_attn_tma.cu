@@ -34,6 +34,7 @@
 #include "tma_mbar.cuh"
 
 namespace fsk {
+FS_TRACE_TU(attn_tma)
 namespace {
 
 using namespace attn;
@@ -64,6 +65,7 @@ template <typename OT, int HD>
 __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
     k_attn_tma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                AttnParams a) {
+  TraceScope tr(g_trace, TR_ATTN_TMA);
   using R = Ring<HD>;
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
@@ -111,6 +113,8 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
     srow[r] = (int)(layer_row0 + ((int64_t)ptrow[pi] * Hkv + g) * ps + slot);
   }
   if (tid == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
     for (int i = 0; i < kWarps * R::kStages; ++i) mbar_init(smem_u32(full + i), 1);
     mbar_init_fence();
   }
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
   if (prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
   pdl_wait();  // the QKV projection's output is read below
+  tr.ready();
   pdl_trigger();
   if (!prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);

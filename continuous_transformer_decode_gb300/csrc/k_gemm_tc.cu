@@ -41,6 +41,7 @@
 #include "tma_mbar.cuh"
 
 namespace fsk {
+FS_TRACE_TU(gemm)
 namespace {
 
 using namespace tma;
@@ -381,6 +382,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_abort;
   __shared__ int s_last;
   __shared__ int s_stop[2];
+  __shared__ unsigned long long s_tr[4];
+  TraceSmem::begin(s_tr, g_trace);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = blockIdx.x % p.groups;
@@ -404,6 +407,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t ncols = p.tmem_cols;
 
   if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmX64);
+    prefetch_tensormap(&tmX16);
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -426,14 +432,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  // TMA producers. A thread's copies are served one after another, so a block
-  // holding a single piece (whole tile, or one K split of one) lets its 4
-  // epilogue warps, idle until the accumulator is ready, issue the stages
-  // congruent to their index; otherwise warp 4 issues every stage (the
-  // epilogue warps then drain pieces while it keeps the ring full).
+  // TMA producers. The copies one thread issues complete one after another
+  // (about half a microsecond each, whatever their size), so copies are
+  // spread over lanes: before the wait for the predecessor, one lane per
+  // stage issues that stage's weight tile; after it, one lane per panel box
+  // (lanes that issued no weight tile first); in the steady state lane 0
+  // issues the weight tile and lanes 1.. the panel boxes. A block holding a
+  // single piece (whole tile, or one K split of one) also lets its 4 epilogue
+  // warps, idle until the accumulator is ready, take the stages congruent to
+  // their index; otherwise warp 4 issues every stage (the epilogue warps then
+  // drain pieces while it keeps the ring full).
   const int npw = p.prod_warps;  // divides S
   const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
-  // warp-collective: lane 0 issues iterations first, first + step, ...
+  const int nb64 = n_tot / 64;
+  const int nbox = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // panel boxes per stage
+  // warp-collective: iterations first, first + step, ...
   auto produce = [&](int first, int step) {
     int issued = -1;  // last iteration issued
     auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
@@ -452,29 +465,28 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
       }
     };
-    auto load_x = [&](int i) {  // panel part of stage i
+    auto load_x_box = [&](int i, int b) {  // panel box b of stage i
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       const int x = ((g0 + i) % kbt) * kBK;
-      int r = 0;
-      for (; r + 64 <= n_tot; r += 64)
-        tma_load_2d(st + kXOff + r * 128, &tmX64, x, lane0 + r, full0 + 8 * s);
-      for (; r < n_tot; r += kXBoxRows)
-        tma_load_2d(st + kXOff + r * 128, &tmX16, x, lane0 + r, full0 + 8 * s);
+      const int r = b < nb64 ? b * 64 : nb64 * 64 + (b - nb64) * kXBoxRows;
+      tma_load_2d(st + kXOff + r * 128, b < nb64 ? &tmX64 : &tmX16, x, lane0 + r,
+                  full0 + 8 * s);
     };
     // Programmatic dependent launch: the weight tiles do not depend on the
     // predecessor kernel, so they start before waiting for it; the panel is
     // the predecessor's output.
     const int pre = min(S, n_it);  // stages are empty at start: no wait needed
-    if (lane == 0)
-      for (int i = first; i < pre; i += step) load_w(i);
+    const int n_pre = pre > first ? (pre - first + step - 1) / step : 0;  // this warp's
+    for (int j = lane; j < n_pre; j += 32) load_w(first + j * step);
+    __syncwarp();
     pdl_wait();
+    TraceSmem::ready(s_tr);
     pdl_trigger();
-    for (int i = first; i < pre; i += step) {
-      if (lane == 0) load_x(i);
-      issued = i;
-    }
-    for (int i = first + ((pre - first + step - 1) / step) * step; i < n_it; i += step) {
+    for (int c = (lane + 32 - n_pre % 32) % 32; c < n_pre * nbox; c += 32)
+      load_x_box(first + (c / nbox) * step, c % nbox);
+    if (n_pre > 0) issued = first + (n_pre - 1) * step;
+    for (int i = first + n_pre * step; i < n_it; i += step) {
       const int s = i % S;
       const uint32_t ph = (uint32_t)(i / S) & 1u;
       const bool ok = mbar_wait(empty0 + 8 * s, ph ^ 1u);
@@ -486,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       if (__shfl_sync(0xffffffffu, *(volatile int*)&s_abort, 0)) break;
-      if (lane == 0) {
-        load_w(i);
-        load_x(i);
-      }
+      if (lane == 0) load_w(i);  // the expect_tx comes before any panel copy
+      __syncwarp();
+      if (lane >= 1)
+        for (int c = lane - 1; c < nbox; c += 31) load_x_box(i, c);
       issued = i;
     }
     // drain: every copy issued here must have landed before the block exits
@@ -501,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool early = warp_prod ? warp < npw : warp == 4;  // producers wait inside produce
   if (!early) {
     pdl_wait();
+    TraceSmem::ready(s_tr);
     pdl_trigger();
   }
 
@@ -627,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                  "r"(ncols)
                  : "memory");
   }
+  TraceSmem::end(s_tr, TR_GEMM + p.epi);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -757,11 +771,14 @@ namespace {
 // ties (each lane of the warp scans tiles t = lane, lane + 32, ... upward).
 __global__ void k_argmax_tiles(const float* __restrict__ am_val, const int* __restrict__ am_idx,
                                int B, int m_tiles, int32_t* __restrict__ tokens_out) {
+  TraceMark tr;
+  tr.begin(g_trace);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int ln = threadIdx.x & 31;
-  if (b >= B) return;
+  if (b >= B) return;  // never thread 0: the grid has ceil(B / warps) blocks
   float bv = -CUDART_INF_F;
   int bi = INT_MAX;
   for (int t = ln; t < m_tiles; t += 32) {
@@ -782,6 +799,7 @@ __global__ void k_argmax_tiles(const float* __restrict__ am_val, const int* __re
     }
   }
   if (ln == 0) tokens_out[b] = bi;
+  tr.end(TR_ARGMAX);
 }
 }  // namespace
 

@@ -15,6 +15,7 @@
 #include "fs_internal.h"
 
 namespace fsk {
+FS_TRACE_TU(gemv)
 namespace {
 
 constexpr int kWarps = 8;
@@ -79,7 +80,9 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 template <bool kSwiglu>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemmArgs a) {
+  TraceScope tr(g_trace, kSwiglu ? TR_GEMV_SWIGLU : TR_GEMV);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, t = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + warp;

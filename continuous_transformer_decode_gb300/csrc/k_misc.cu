@@ -9,6 +9,7 @@
 #include "norm_row.cuh"
 
 namespace fsk {
+FS_TRACE_TU(misc)
 namespace {
 
 __device__ __forceinline__ float load_w(const Mat& E, int64_t row, int i) {
@@ -26,7 +27,10 @@ template <typename OT>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x, int d, const float* g,
             float eps, OT* __restrict__ h, int ld_h) {
+  TraceMark tr;
+  tr.begin(g_trace);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   __shared__ float red[4];
   const int b = blockIdx.x, t = threadIdx.x;
@@ -46,6 +50,7 @@ __global__ void __launch_bounds__(kNormRowThreads)
     *reinterpret_cast<float4*>(xr + 4 * c) = v;
   }
   if (g) norm_row_128<OT, 16>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red);
+  tr.end(TR_EMBED);
 }
 
 
@@ -55,12 +60,16 @@ template <typename OT>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_rmsnorm(float* __restrict__ x, const float* __restrict__ r,
               const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out) {
+  TraceMark tr;
+  tr.begin(g_trace);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   __shared__ float red[4];
   const int b = blockIdx.x;
   norm_row_128<OT, 16>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, g, d, eps,
                        out + (int64_t)b * ld_out, threadIdx.x, 1, red);
+  tr.end(TR_RMSNORM);
 }
 
 // ---------------------------------------------------------------- sampler
@@ -90,7 +99,10 @@ __global__ void __launch_bounds__(kSampThreads)
     k_sample(const float* __restrict__ logits, int V,
              const float* __restrict__ temps, const uint64_t* __restrict__ seeds,
              const uint64_t* __restrict__ counters, int32_t* __restrict__ out) {
+  TraceMark tr;
+  tr.begin(g_trace);
   pdl_wait();
+  tr.ready();
   pdl_trigger();
   __shared__ double sd[kSampThreads];
   __shared__ int si[kSampThreads];
@@ -122,6 +134,7 @@ __global__ void __launch_bounds__(kSampThreads)
       __syncthreads();
     }
     if (t == 0) out[b] = si[0] == V ? 0 : si[0];
+    tr.end(TR_SAMPLE);
     return;
   }
   // max of z = logit / T
@@ -186,6 +199,7 @@ __global__ void __launch_bounds__(kSampThreads)
     }
     out[b] = r;
   }
+  tr.end(TR_SAMPLE);
 }
 
 // ------------------------------------------------------------- Q8_0 codec

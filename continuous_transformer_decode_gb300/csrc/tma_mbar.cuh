@@ -64,6 +64,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Brings a tensor map (a __grid_constant__ parameter) into the TMA unit's
+// descriptor cache ahead of the first copy that uses it.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
+}
 // Orders this thread's earlier generic-proxy accesses to shared memory
 // before later async-proxy (TMA) writes to it.
 __device__ __forceinline__ void fence_proxy_async_smem() {

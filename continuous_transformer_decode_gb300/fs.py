@@ -102,6 +102,8 @@ def lib():
         "fs_set_stream": (C.c_int, [p, p]),
         "fs_lane_reset": (C.c_int, [p, i32]),
         "fs_lane_clone": (C.c_int, [p, i32, i32]),
+        "fs_trace_enable": (C.c_int, [p, i64]),
+        "fs_trace_read": (C.c_int, [p, p, i64, p, C.c_int]),
         "fs_lane_evict": (C.c_int, [p, i32, i32, i32]),
         "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
         "fs_step_batch_chunked": (C.c_int, [p, p, p, p, i32, p]),
@@ -149,7 +151,7 @@ def lib():
 def exported_symbols() -> list:
     """Names of the entry points declared in include/fs.h."""
     return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
-            "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
+            "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_trace_enable", "fs_trace_read", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
@@ -230,6 +232,29 @@ def fs_set_stream(h, stream) -> None:
 
 def fs_lane_reset(h, lane: int) -> None:
     _check(h, lib().fs_lane_reset(h, int(lane)))
+
+
+TRACE_TAGS = {1: "embed", 2: "rmsnorm", 3: "sample", 4: "argmax_tiles",
+              5: "attn_mma", 6: "attn_tma", 7: "attn_tiled", 8: "attn_fused",
+              9: "rope_append", 10: "gemv", 11: "attn_partial", 12: "attn_combine",
+              13: "gemv_swiglu",
+              16: "gemm_store", 17: "gemm_resid",
+              18: "gemm_swiglu", 19: "gemm_argmax"}
+
+
+def fs_trace_enable(h, capacity: int) -> None:
+    """Kernel timeline tracing into a device buffer of ``capacity`` records
+    (0 turns it off)."""
+    _check(h, lib().fs_trace_enable(h, int(capacity)))
+
+
+def fs_trace_read(h, reset: bool = True):
+    """Returns (records [n, 4] uint64, appended count)."""
+    n = C.c_int64()
+    _check(h, lib().fs_trace_read(h, None, 0, C.byref(n), 0))
+    out = np.zeros((max(1, n.value), 4), dtype=np.uint64)
+    _check(h, lib().fs_trace_read(h, _ptr(out), n.value, C.byref(n), int(bool(reset))))
+    return out[:min(n.value, out.shape[0])], n.value
 
 
 def fs_lane_clone(h, src: int, dst: int) -> None:

@@ -266,6 +266,31 @@ int fs_profile_read(fs_handle* h, int32_t cls, double* ms_out,
 /* Tokens one lane can hold (the descriptor's max_pos). */
 int fs_lane_capacity(const fs_handle* h, int32_t* tokens_out);
 
+/* Kernel timeline tracing (a diagnostic; no counterpart on the pages).
+ * With capacity > 0, thread 0 of every block of the library's step kernels
+ * appends one record of four uint64 to a device buffer of `capacity`
+ * records: word 0 = tag << 40 | waited << 39 | SM id << 24 | linear block
+ * index (waited: the block passed its wait for the preceding kernel; tag: 1
+ * embed, 2 RMSNorm, 3 sampler, 4 tile argmax, 5 attention (cp.async), 6
+ * attention (TMA), 7 attention (tiled), 8 attention (fused), 9 RoPE +
+ * KV append, 10 GEMV, 11 / 12 split attention partials / combine (the
+ * three-kernel path), 13 GEMV with the SwiGLU epilogue, 16 + epilogue
+ * kind for the tensor-core GEMM: 16
+ * store, 17 residual, 18 SwiGLU, 19 argmax); words 1-3 = %globaltimer ns
+ * at the block's entry, after its wait for the preceding kernel, and at its
+ * end. Records past the capacity are counted, not stored. The buffer is
+ * process-wide: one handle at a time may trace (FS_ERR_STATE otherwise);
+ * capacity 0 turns tracing off and frees the buffer (also done by
+ * fs_destroy). Synchronises the stream. */
+int fs_trace_enable(fs_handle* h, int64_t capacity);
+
+/* Copies min(appended, capacity, cap) records (4 uint64 each, in the order
+ * they were appended) to host memory and the count appended so far to
+ * *appended_out; reset != 0 then empties the buffer. Synchronises the
+ * stream. Errors: FS_ERR_STATE (h is not tracing), FS_ERR_ARG. */
+int fs_trace_read(fs_handle* h, uint64_t* records_out, int64_t cap, int64_t* appended_out,
+                  int reset);
+
 /* Current length (tokens held) of a lane. */
 int fs_lane_length(const fs_handle* h, int32_t lane, int32_t* length_out);
 
