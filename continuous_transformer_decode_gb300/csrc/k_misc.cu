@@ -62,13 +62,19 @@ __global__ void __launch_bounds__(kNormRowThreads)
               const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out) {
   TraceMark tr;
   tr.begin(g_trace);
+  __shared__ float red[4];
+  const int b = blockIdx.x;
+  // x was last written two or more kernels back (complete once this kernel
+  // runs: every kernel waits for its predecessor before letting its
+  // successor start), the gains never: both are read before the wait; r is
+  // the predecessor's output.
+  NormRow<16> n;
+  n.load(x + (int64_t)b * d, g, d, threadIdx.x);
   pdl_wait();
   tr.ready();
   pdl_trigger();
-  __shared__ float red[4];
-  const int b = blockIdx.x;
-  norm_row_128<OT, 16>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, g, d, eps,
-                       out + (int64_t)b * ld_out, threadIdx.x, 1, red);
+  n.finish<OT>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, d, eps,
+               out + (int64_t)b * ld_out, threadIdx.x, 1, red);
   tr.end(TR_RMSNORM);
 }
 
