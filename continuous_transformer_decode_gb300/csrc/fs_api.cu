@@ -341,19 +341,26 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   }
   // attention split length: a handle constant (it fixes the merge order).
   // Long splits amortise each block's fixed cost (page indices, q rotation,
-  // merges) once a full handle has enough (lane, KV head, split) blocks to
-  // fill the GPU several times over; otherwise short splits give the
-  // parallelism.
+  // the first copies' latency, merges); the longest of 1024 / 512 / 256 whose
+  // (lane, KV head, split) blocks of a full handle still number three per SM
+  // is taken, else 128 for the parallelism (measured on the Mistral-7B shape,
+  // contexts U[128, 4096]: B = 8 is fastest at 512, B = 32 and up at 1024,
+  // B = 1 at 128).
   {
     auto blocks = [&](int len) {
       return (int64_t)d.max_lanes * d.n_kv_heads * ((d.max_pos + len - 1) / len);
     };
-    const int64_t sms = h->sms;
+    const int64_t want = 3 * (int64_t)h->sms;
     h->split_len = !attn_tiled_supports(d.head_dim, d.n_heads / d.n_kv_heads, d.page_size, 128)
                        ? 256
-                   : blocks(1024) >= 8 * sms ? 1024
-                   : blocks(512) >= 4 * sms  ? 512
-                                             : 128;
+                   : blocks(1024) >= want ? 1024
+                   : blocks(512) >= want  ? 512
+                   : blocks(256) >= want  ? 256
+                                          : 128;
+    // FS_SPLIT_LEN=128|256|512|1024 overrides the rule (a tuning knob)
+    const char* e = getenv("FS_SPLIT_LEN");
+    const int v = e ? atoi(e) : 0;
+    if ((v == 128 || v == 256 || v == 512 || v == 1024) && h->split_len != 256) h->split_len = v;
   }
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;

@@ -37,14 +37,6 @@ constexpr int kT = 32 * kWarps;
 constexpr int kTT = 64;      // positions per tile
 constexpr int kG = 8;        // max query heads per KV head
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 // byte offset of (row, 16-byte chunk) in a swizzled [kTT][HD] bf16 tile
 template <int HD>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {

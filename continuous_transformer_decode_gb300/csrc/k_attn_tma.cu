@@ -361,18 +361,38 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // merge: every split's (m, l) into shared memory at once, the weights once
-  // per (split, head), then the outputs with independent loads; all sums in
-  // ascending split order
+  // merge: every split's (m, l) into shared memory with plain loads and the
+  // splits' outputs by asynchronous copies into the idle rings, all in flight
+  // together (`chunk` splits at a time, every split when they fit); the
+  // weights once per (split, head); then the outputs from shared memory. All
+  // sums in ascending split order.
+  constexpr int kOut = (kG * HD + kT - 1) / kT;   // outputs per thread (at most)
   float* sm = reinterpret_cast<float*>(smem);     // [ns][kG] m, then weights
   float* sl = sm + (size_t)ns * kG;               // [ns][kG] l
   float* sL = sl + (size_t)ns * kG;               // [kG] merged l
+  const int ml_bytes = ((2 * ns * kG + kG) * (int)sizeof(float) + 15) & ~15;
+  float* sp = reinterpret_cast<float*>(smem + ml_bytes);  // [chunk][G * HD]
+  const int gh = G * HD;                                  // floats of one split
+  const int chunk = (kWarps * R::kWarpBytes - ml_bytes) / (gh * (int)sizeof(float));
+  const float* src = a.part_acc + (((int64_t)b * a.max_splits) * H + g * G) * HD;
+  const int64_t qstride = (int64_t)H * HD;
+  auto stage = [&](int q0) {  // splits q0 .. q0 + chunk - 1 into sp
+    const int per = gh / 4;   // 16-byte pieces of one split
+    const int n16 = min(chunk, ns - q0) * per;
+    for (int c = tid; c < n16; c += kT) {
+      const int q = c / per, r = c - q * per;
+      cp_async16(smem_u32(sp + q * gh + 4 * r), src + (q0 + q) * qstride + 4 * r);
+    }
+    cp_commit();
+  };
+  stage(0);
   for (int idx = tid; idx < ns * G; idx += kT) {
     const int q = idx / G, h = idx - q * G;
     const int64_t bq = ((int64_t)b * a.max_splits + q) * H + g * G + h;
     sm[q * kG + h] = __ldcg(a.part_ml + 2 * bq);
     sl[q * kG + h] = __ldcg(a.part_ml + 2 * bq + 1);
   }
+  cp_wait<0>();
   __syncthreads();
   if (tid < G) {
     const int h = tid;
@@ -387,22 +407,31 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
     sL[h] = L;
   }
   __syncthreads();
-  for (int o = tid; o < G * HD; o += kT) {
-    const int h = o / HD, d = o - h * HD;
-    const float* src = a.part_acc + (((int64_t)b * a.max_splits) * H + g * G + h) * HD + d;
-    const int64_t qstride = (int64_t)H * HD;
-    float A = 0.0f;
-    int q = 0;
-    for (; q + 4 <= ns; q += 4) {  // four independent loads in flight
-      const float a0 = __ldcg(src + (q + 0) * qstride), a1 = __ldcg(src + (q + 1) * qstride);
-      const float a2 = __ldcg(src + (q + 2) * qstride), a3 = __ldcg(src + (q + 3) * qstride);
-      A = fmaf(a0, sm[(q + 0) * kG + h], A);
-      A = fmaf(a1, sm[(q + 1) * kG + h], A);
-      A = fmaf(a2, sm[(q + 2) * kG + h], A);
-      A = fmaf(a3, sm[(q + 3) * kG + h], A);
+  float acc[kOut];
+#pragma unroll
+  for (int j = 0; j < kOut; ++j) acc[j] = 0.0f;
+  for (int q0 = 0; q0 < ns; q0 += chunk) {
+    if (q0 > 0) {  // every thread is done with the previous chunk
+      __syncthreads();
+      stage(q0);
+      cp_wait<0>();
+      __syncthreads();
     }
-    for (; q < ns; ++q) A = fmaf(__ldcg(src + q * qstride), sm[q * kG + h], A);
-    st_out(orow + o, A / sL[h]);
+    const int nq = min(chunk, ns - q0);
+    for (int qq = 0; qq < nq; ++qq) {
+      const float* pq = sp + qq * gh;
+      const float* wq = sm + (q0 + qq) * kG;
+#pragma unroll
+      for (int j = 0; j < kOut; ++j) {
+        const int o = tid + j * kT;
+        if (o < gh) acc[j] = fmaf(pq[o], wq[o / HD], acc[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kOut; ++j) {
+    const int o = tid + j * kT;
+    if (o < gh) st_out(orow + o, acc[j] / sL[o / HD]);
   }
 }
 
@@ -452,7 +481,9 @@ bool attn_tma_supports(int hd, int G, int kv_f32, int page_size, int split_len,
   const size_t ring_bytes = hd == 64 ? (size_t)kWarps * Ring<64>::kWarpBytes
                             : hd == 128 ? (size_t)kWarps * Ring<128>::kWarpBytes
                                         : (size_t)kWarps * Ring<256>::kWarpBytes;
-  const size_t merge_bytes = (size_t)(2 * kG * max_splits + kG) * sizeof(float);
+  // the merge's (m, l) arrays and at least one split's outputs in the rings
+  const size_t merge_bytes = (((size_t)(2 * kG * max_splits + kG) * sizeof(float) + 15) & ~15) +
+                             (size_t)G * hd * sizeof(float);
   return runs && split_len % kTT == 0 && split_len / std::min(page_size, 16) <= kMaxRuns &&
          merge_bytes <= ring_bytes;
 }
