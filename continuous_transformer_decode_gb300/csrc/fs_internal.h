@@ -33,9 +33,10 @@ bool pdl_enabled();  // FS_PDL=0 in the environment turns the attribute off
 // ---- kernel timeline tracing. Off unless a buffer is installed: thread 0
 // of every block of a traced kernel then appends one record with the
 // %globaltimer time at entry, after its dependency wait, and at its end.
-// The buffer pointer is a device global of each translation unit (the
-// library is built without relocatable device code); fs_trace_enable
-// installs it in all of them.
+// The buffer pointer is a __constant__ of each translation unit (the
+// library is built without relocatable device code; a constant-cache read
+// keeps the untraced path free of a memory round trip at every block's
+// start); fs_trace_enable installs it in all of them.
 struct TraceRec {
   // tag << 40 | waited << 39 | smid << 24 | linear block index; waited: the
   // block passed its wait for the preceding kernel (a block that leaves
@@ -135,7 +136,7 @@ struct TraceScope : TraceMark {
 
 // Defines this translation unit's trace pointer and its host installer.
 #define FS_TRACE_TU(name)                                                     \
-  static __device__ TraceBuf* g_trace = nullptr;                              \
+  static __constant__ TraceBuf* g_trace = nullptr;                            \
   int trace_install_##name(TraceBuf* p) {                                     \
     return cudaMemcpyToSymbol(g_trace, &p, sizeof(p)) == cudaSuccess ? 1 : 0; \
   }

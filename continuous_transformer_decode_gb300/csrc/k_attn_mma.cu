@@ -43,9 +43,10 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * (HD * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
+// The kernel's body; thread 0's trace marks stay in shared memory (s_tr) so
+// that tracing costs the body no registers.
 template <typename OT, int HD>
-__global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
-  TraceScope tr(g_trace, TR_ATTN_MMA);
+__device__ __forceinline__ void attn_mma_body(const AttnParams& a, unsigned long long* s_tr) {
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
   constexpr int kTileBytes = kTT * HD * 2;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
     if (n_tiles > 1) issue(1);
   }
   pdl_wait();
-  tr.ready();
+  TraceSmem::ready(s_tr);
   pdl_trigger();
   if (!prefetch) {
     issue(0);
@@ -354,6 +355,16 @@ __global__ void __launch_bounds__(kT) k_attn_mma(AttnParams a) {
     for (; q < ns; ++q) A = fmaf(__ldcg(src + q * qstride), sm[q * kG + h], A);
     st_out(orow + o, A / sL[h]);
   }
+}
+
+// hd 64 keeps to 80 registers: six blocks of an SM (a 256-lane, 3-head
+// step is then a single wave)
+template <typename OT, int HD>
+__global__ void __launch_bounds__(kT, HD == 64 ? 6 : 1) k_attn_mma(AttnParams a) {
+  __shared__ unsigned long long s_tr[4];
+  TraceSmem::begin(s_tr, g_trace);
+  attn_mma_body<OT, HD>(a, s_tr);
+  TraceSmem::end(s_tr, TR_ATTN_MMA);
 }
 
 template <typename OT, int HD>

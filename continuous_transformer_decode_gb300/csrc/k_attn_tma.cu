@@ -62,10 +62,8 @@ __device__ __forceinline__ uint32_t sws(int r, int chunk) {
 }
 
 template <typename OT, int HD>
-__global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
-    k_attn_tma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-               AttnParams a) {
-  TraceScope tr(g_trace, TR_ATTN_TMA);
+__device__ __forceinline__ void attn_tma_body(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                              const AttnParams& a, unsigned long long* s_tr) {
   using R = Ring<HD>;
   constexpr int kHalf = HD / 2;
   constexpr int kCh = HD / 8;            // 16-byte chunks per row
@@ -148,7 +146,7 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
   if (prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
   pdl_wait();  // the QKV projection's output is read below
-  tr.ready();
+  TraceSmem::ready(s_tr);
   pdl_trigger();
   if (!prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
@@ -433,6 +431,18 @@ __global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
     const int o = tid + j * kT;
     if (o < gh) st_out(orow + o, acc[j] / sL[o / HD]);
   }
+}
+
+// Thread 0's trace marks stay in shared memory (s_tr): tracing costs the
+// body no registers.
+template <typename OT, int HD>
+__global__ void __launch_bounds__(kT, HD == 256 ? 1 : 2)
+    k_attn_tma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               AttnParams a) {
+  __shared__ unsigned long long s_tr[4];
+  TraceSmem::begin(s_tr, g_trace);
+  attn_tma_body<OT, HD>(tmK, tmV, a, s_tr);
+  TraceSmem::end(s_tr, TR_ATTN_TMA);
 }
 
 template <int HD>

@@ -23,7 +23,7 @@ __device__ __forceinline__ float load_w(const Mat& E, int64_t row, int i) {
 
 // x[b] = E[tok[b]] and, when g is given, h[b] = RMSNorm(x[b]) * g (the first
 // layer's input norm); block b also applies page-table update b of the step.
-template <typename OT>
+template <typename OT, int MV>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x, int d, const float* g,
             float eps, OT* __restrict__ h, int ld_h) {
@@ -49,14 +49,14 @@ __global__ void __launch_bounds__(kNormRowThreads)
     v.w = load_w(E, tok, 4 * c + 3);
     *reinterpret_cast<float4*>(xr + 4 * c) = v;
   }
-  if (g) norm_row_128<OT, 16>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red);
+  if (g) norm_row_128<OT, MV>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red);
   tr.end(TR_EMBED);
 }
 
 
 // Residual add then RMSNorm, one block of 128 threads per panel row (see
 // norm_row.cuh for the arithmetic and its fixed reduction order).
-template <typename OT>
+template <typename OT, int MV>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_rmsnorm(float* __restrict__ x, const float* __restrict__ r,
               const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out) {
@@ -68,12 +68,12 @@ __global__ void __launch_bounds__(kNormRowThreads)
   // runs: every kernel waits for its predecessor before letting its
   // successor start), the gains never: both are read before the wait; r is
   // the predecessor's output.
-  NormRow<16> n;
+  NormRow<MV> n;
   n.load(x + (int64_t)b * d, g, d, threadIdx.x);
   pdl_wait();
   tr.ready();
   pdl_trigger();
-  n.finish<OT>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, d, eps,
+  n.template finish<OT>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, d, eps,
                out + (int64_t)b * ld_out, threadIdx.x, 1, red);
   tr.end(TR_RMSNORM);
 }
@@ -343,27 +343,66 @@ bool pdl_enabled() {
   return on;
 }
 
+// float4 chunks a thread of a row holds: the smallest of 2, 4, 8, 16 that
+// covers d (chunks past d add exact zeros, so the bits do not depend on it)
+int norm_chunks(int d) {
+  const int per = (d / 4 + kNormRowThreads - 1) / kNormRowThreads;
+  return per <= 2 ? 2 : per <= 4 ? 4 : per <= 8 ? 8 : 16;
+}
+
+template <typename OT, int MV>
+void embed_mv(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
+              const float* g, float eps, void* h, int ld_h, cudaStream_t s) {
+  launch_k(k_embed<OT, MV>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
+           static_cast<OT*>(h), ld_h);
+}
+
+template <typename OT>
+void embed_ot(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
+              const float* g, float eps, void* h, int ld_h, cudaStream_t s) {
+  switch (norm_chunks(d)) {
+    case 2: embed_mv<OT, 2>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
+    case 4: embed_mv<OT, 4>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
+    case 8: embed_mv<OT, 8>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
+    default: embed_mv<OT, 16>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
+  }
+}
+
 int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
                  const float* g, float eps, void* h, int x_type, int ld_h, cudaStream_t s) {
   if (B <= 0) return 0;
   if (x_type == X_BF16)
-    launch_k(k_embed<__nv_bfloat16>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
-             static_cast<__nv_bfloat16*>(h), ld_h);
+    embed_ot<__nv_bfloat16>(E, args, B, kv, x, d, g, eps, h, ld_h, s);
   else
-    launch_k(k_embed<float>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
-             static_cast<float*>(h), ld_h);
+    embed_ot<float>(E, args, B, kv, x, d, g, eps, h, ld_h, s);
   return 1;
+}
+
+template <typename OT, int MV>
+void rmsnorm_mv(float* x, const float* resid, const float* g, int B, int d, float eps, void* out,
+                int ld_out, cudaStream_t s) {
+  launch_k(k_rmsnorm<OT, MV>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
+           static_cast<OT*>(out), ld_out);
+}
+
+template <typename OT>
+void rmsnorm_ot(float* x, const float* resid, const float* g, int B, int d, float eps, void* out,
+                int ld_out, cudaStream_t s) {
+  switch (norm_chunks(d)) {
+    case 2: rmsnorm_mv<OT, 2>(x, resid, g, B, d, eps, out, ld_out, s); break;
+    case 4: rmsnorm_mv<OT, 4>(x, resid, g, B, d, eps, out, ld_out, s); break;
+    case 8: rmsnorm_mv<OT, 8>(x, resid, g, B, d, eps, out, ld_out, s); break;
+    default: rmsnorm_mv<OT, 16>(x, resid, g, B, d, eps, out, ld_out, s); break;
+  }
 }
 
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
                    void* out, int x_type, int ld_out, cudaStream_t s) {
   if (B <= 0) return 0;
   if (x_type == X_BF16)
-    launch_k(k_rmsnorm<__nv_bfloat16>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
-             static_cast<__nv_bfloat16*>(out), ld_out);
+    rmsnorm_ot<__nv_bfloat16>(x, resid, g, B, d, eps, out, ld_out, s);
   else
-    launch_k(k_rmsnorm<float>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
-             static_cast<float*>(out), ld_out);
+    rmsnorm_ot<float>(x, resid, g, B, d, eps, out, ld_out, s);
   return 1;
 }
 
