@@ -23,6 +23,8 @@ struct Engine {
   virtual int capacity() const = 0;
   virtual int64_t lane_tokens() const = 0;  // KV tokens one lane can hold; 0 = no bound
   virtual int reset(int lane) = 0;
+  virtual int clone(int src, int dst) = 0;            // dst (empty) takes src's history
+  virtual int evict(int lane, int start, int end) = 0;  // positions [start, end) leave
   // n rows (lane, position, token); a lane on several rows has them at its
   // next consecutive positions (chunked); positions advanced on success
   virtual int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
@@ -42,6 +44,8 @@ struct GpuEngine : Engine {
     return fs_lane_capacity(h, &t) == FS_OK ? t : 0;
   }
   int reset(int lane) override { return fs_lane_reset(h, lane); }
+  int clone(int src, int dst) override { return fs_lane_clone(h, src, dst); }
+  int evict(int lane, int start, int end) override { return fs_lane_evict(h, lane, start, end); }
   int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
            bool chunked) override {
     return chunked ? fs_step_batch_chunked(h, lanes, positions, tokens, n, nullptr)
@@ -60,25 +64,39 @@ uint64_t mix64(uint64_t z) {  // splitmix64 finaliser
   return z ^ (z >> 31);
 }
 
-// Deterministic stand-in for a model: each lane hashes the tokens it consumed.
+// Deterministic stand-in for a model: each lane hashes the tokens it consumed
+// (the running hash after every token is kept, so a suffix can be evicted).
 struct ModelFreeEngine : Engine {
+  static constexpr uint64_t kInit = 0xCBF29CE484222325ull;
   int cap, vocab;
-  std::vector<uint64_t> hash;
-  std::vector<int32_t> len;
+  std::vector<std::vector<uint64_t>> hist;  // per lane: the hash after each token
   std::vector<int32_t> last_lanes;
-  ModelFreeEngine(int c, int v) : cap(c), vocab(v), hash(c, 0xCBF29CE484222325ull), len(c, 0) {}
+  ModelFreeEngine(int c, int v) : cap(c), vocab(v), hist(c) {}
   int capacity() const override { return cap; }
   int64_t lane_tokens() const override { return 0; }
+  uint64_t hash(int lane) const { return hist[lane].empty() ? kInit : hist[lane].back(); }
   int reset(int lane) override {
     if (lane < 0 || lane >= cap) return FS_ERR_LANE;
-    hash[lane] = 0xCBF29CE484222325ull;
-    len[lane] = 0;
+    hist[lane].clear();
+    return FS_OK;
+  }
+  int clone(int src, int dst) override {
+    if (src < 0 || src >= cap || dst < 0 || dst >= cap) return FS_ERR_LANE;
+    if (src == dst || !hist[dst].empty()) return FS_ERR_STATE;
+    hist[dst] = hist[src];
+    return FS_OK;
+  }
+  int evict(int lane, int start, int end) override {
+    if (lane < 0 || lane >= cap) return FS_ERR_LANE;
+    if (start < 0 || start > end || end != (int)hist[lane].size()) return FS_ERR_ARG;
+    hist[lane].resize(start);
     return FS_OK;
   }
   int step(const int32_t* lanes, int32_t* positions, const int32_t* tokens, int n,
            bool) override {
     // rows in order; a lane's rows at its next consecutive positions
-    std::vector<int32_t> at(len);
+    std::vector<int32_t> at(cap);
+    for (int k = 0; k < cap; ++k) at[k] = (int32_t)hist[k].size();
     for (int i = 0; i < n; ++i) {
       if (lanes[i] < 0 || lanes[i] >= cap) return FS_ERR_LANE;
       if (positions[i] != at[lanes[i]]) return FS_ERR_POSITION;
@@ -87,9 +105,8 @@ struct ModelFreeEngine : Engine {
     }
     last_lanes.assign(lanes, lanes + n);
     for (int i = 0; i < n; ++i) {
-      uint64_t& hh = hash[lanes[i]];
-      hh = (hh ^ (uint64_t)(uint32_t)tokens[i]) * 0x100000001B3ull;
-      len[lanes[i]] += 1;
+      const uint64_t hh = (hash(lanes[i]) ^ (uint64_t)(uint32_t)tokens[i]) * 0x100000001B3ull;
+      hist[lanes[i]].push_back(hh);
       positions[i] += 1;
     }
     return FS_OK;
@@ -98,7 +115,7 @@ struct ModelFreeEngine : Engine {
              int32_t* out) override {
     if (n != (int)last_lanes.size()) return FS_ERR_STATE;
     for (int i = 0; i < n; ++i) {
-      const uint64_t hh = hash[last_lanes[i]];
+      const uint64_t hh = hash(last_lanes[i]);
       uint64_t v = hh;
       if (temps[i] != 0.0f) v = hh ^ mix64(seeds[i] + 0x9E3779B97F4A7C15ull * (counters[i] + 1));
       out[i] = (int32_t)(v % (uint64_t)vocab);
@@ -160,7 +177,8 @@ namespace {
 int make(std::unique_ptr<Engine> eng, const fs_sched_config* cfg, fs_sched** out) {
   if (!cfg || !out) return FS_ERR_ARG;
   if (cfg->lanes < 1 || cfg->lanes > eng->capacity() || cfg->max_prefill_tokens_per_tick < 1 ||
-      cfg->max_queue < 0 || cfg->prefill_chunk < 0 || cfg->kv_budget_tokens < 0)
+      cfg->max_queue < 0 || cfg->prefill_chunk < 0 || cfg->kv_budget_tokens < 0 ||
+      cfg->prefix_reuse_min < 0)
     return FS_ERR_ARG;
   fs_sched* s = new fs_sched();
   s->eng = std::move(eng);
@@ -171,6 +189,43 @@ int make(std::unique_ptr<Engine> eng, const fs_sched_config* cfg, fs_sched** out
   return FS_OK;
 }
 
+}  // namespace
+
+namespace {
+// Token a lane fed at position p (p < its position): its prompt, then its
+// generated tokens fed back.
+int32_t fed_token(const Lane& l, int p) {
+  const int P = (int)l.job.prompt.size();
+  return p < P ? l.job.prompt[p] : l.gen[p - P];
+}
+
+// Prefix reuse for the job just admitted into lane k (see fs_sched.h).
+int reuse_prefix(fs_sched* s, int k) {
+  Lane& ln = s->lanes[k];
+  const int cap = (int)ln.job.prompt.size() - 1;
+  int best = 0, src = -1;
+  for (int j = 0; j < s->cfg.lanes; ++j) {
+    const Lane& o = s->lanes[j];
+    if (j == k || !o.busy) continue;
+    const int lim = std::min(cap, o.pos);
+    int c = 0;
+    while (c < lim && fed_token(o, c) == ln.job.prompt[c]) ++c;
+    if (c > best) {
+      best = c;
+      src = j;
+    }
+  }
+  if (src < 0 || best < s->cfg.prefix_reuse_min) return FS_OK;
+  int rc = s->eng->clone(src, k);
+  if (rc) return s->fail(rc, "prefix clone: " + s->eng->error());
+  rc = s->eng->evict(k, best, s->lanes[src].pos);
+  if (rc) return s->fail(rc, "prefix evict: " + s->eng->error());
+  ln.pos = best;
+  ln.feed = best;
+  s->st.prefix_hits += 1;
+  s->st.prefix_tokens += best;
+  return FS_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -249,6 +304,10 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
     ln.last = 0;
     ln.pos = 0;
     ln.seq = s->admit_seq++;
+    if (s->cfg.prefix_reuse_min > 0) {
+      rc = reuse_prefix(s, k);
+      if (rc) return rc;
+    }
   }
   // ---- gather: decode lanes always (one row each); prompt lanes oldest
   // first, each up to prefill_chunk tokens, within the prompt-token budget

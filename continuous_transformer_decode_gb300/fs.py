@@ -57,7 +57,7 @@ class fs_weights(C.Structure):
 class fs_sched_config(C.Structure):
     _fields_ = [("lanes", C.c_int32), ("max_prefill_tokens_per_tick", C.c_int32),
                 ("max_queue", C.c_int32), ("prefill_chunk", C.c_int32),
-                ("kv_budget_tokens", C.c_int64)]
+                ("kv_budget_tokens", C.c_int64), ("prefix_reuse_min", C.c_int32)]
 
 
 class fs_job(C.Structure):
@@ -77,7 +77,8 @@ class fs_sched_stats(C.Structure):
                 ("kv_reserved_tokens", C.c_int64), ("kv_reserved_max", C.c_int64),
                 ("kv_budget_tokens", C.c_int64), ("kv_wait_steps", C.c_int64),
                 ("seconds", C.c_double), ("prefill_tok_s", C.c_double),
-                ("decode_tok_s", C.c_double)]
+                ("decode_tok_s", C.c_double),
+                ("prefix_hits", C.c_int64), ("prefix_tokens", C.c_int64)]
 
 
 LIB_PATH = _build.LIB
@@ -480,10 +481,11 @@ def _sched_check(s, rc: int) -> None:
 
 
 def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
-                    max_queue: int = 0, prefill_chunk: int = 1, kv_budget_tokens: int = 0):
+                    max_queue: int = 0, prefill_chunk: int = 1, kv_budget_tokens: int = 0,
+                    prefix_reuse_min: int = 0):
     s = C.c_void_p()
     cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk,
-                          kv_budget_tokens)
+                          kv_budget_tokens, prefix_reuse_min)
     rc = lib().fs_sched_create(h, C.byref(cfg), C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create failed")
@@ -493,10 +495,10 @@ def fs_sched_create(h, lanes: int, max_prefill_tokens_per_tick: int = 1,
 def fs_sched_create_model_free(lanes: int, vocab: int,
                                max_prefill_tokens_per_tick: int = 1,
                                max_queue: int = 0, prefill_chunk: int = 1,
-                               kv_budget_tokens: int = 0):
+                               kv_budget_tokens: int = 0, prefix_reuse_min: int = 0):
     s = C.c_void_p()
     cfg = fs_sched_config(lanes, max_prefill_tokens_per_tick, max_queue, prefill_chunk,
-                          kv_budget_tokens)
+                          kv_budget_tokens, prefix_reuse_min)
     rc = lib().fs_sched_create_model_free(C.byref(cfg), vocab, C.byref(s))
     if rc != FS_OK:
         raise FsError(rc, "fs_sched_create_model_free failed")

@@ -43,6 +43,17 @@
  *     session has no external key here, so there is no duplicate check, and
  *     activation scratch is preallocated per lane, so `lanes` is the scratch
  *     bound;
+ *   - prefix reuse (prefix_reuse_min > 0; "MODEL-BATCHING-RESULTS", "Why
+ *     in-kernel batching, not vLLM": Clone for prefix reuse): when fill
+ *     admits a job into lane k, the busy lane whose fed history shares the
+ *     longest prefix with the job's prompt (ties: the lowest lane), capped
+ *     at prompt_len - 1 tokens, is cloned into k and the clone's history
+ *     past that prefix is evicted (fs_lane_clone, fs_lane_evict), provided
+ *     the prefix has at least prefix_reuse_min tokens; the job then feeds
+ *     only the rest of its prompt. A lane's history is the tokens its job
+ *     fed (prompt, then generated tokens fed back). The job's tokens are
+ *     those it gives alone: a position's K and V depend only on the tokens
+ *     up to it. Its KV reservation is unchanged;
  *   - fold: the step that consumes a prompt's last token yields the job's
  *     first generated token (from that lane's last row); the job's t-th generated token is sampled with
  *     (seed, counter = t), so a job's tokens do not depend on its lane, its
@@ -73,6 +84,8 @@ typedef struct fs_sched_config {
                                           0 or 1: one (no chunking)         */
   int64_t kv_budget_tokens;            /* KV tokens reserved by the lanes'
                                           jobs at most; 0 = no bound        */
+  int32_t prefix_reuse_min;            /* shortest prompt prefix taken from
+                                          a running lane; 0 = no reuse      */
 } fs_sched_config;
 
 typedef struct fs_job {
@@ -106,6 +119,8 @@ typedef struct fs_sched_stats {
   double seconds;               /* host time from the first step to the last */
   double prefill_tok_s;         /* prefill_tokens / seconds                  */
   double decode_tok_s;          /* decode_tokens / seconds                   */
+  int64_t prefix_hits;          /* admissions that cloned a running lane     */
+  int64_t prefix_tokens;        /* prompt tokens taken from clones, not fed  */
 } fs_sched_stats;
 
 /* Scheduler over a decode handle: each step is one fs_decode_step_batch
@@ -119,7 +134,9 @@ int fs_sched_create(fs_handle* h, const fs_sched_config* cfg, fs_sched** out);
  * draw hash % vocab and sampled lanes (hash ^ mix(seed, counter)) % vocab,
  * where mix is the splitmix64 finaliser of seed + 0x9E3779B97F4A7C15 *
  * (counter + 1) and the hash update is h = (h ^ token) * 0x100000001B3 over
- * an initial 0xCBF29CE484222325 at lane reset. For testing the policy. */
+ * an initial 0xCBF29CE484222325 at lane reset. A clone copies a lane's
+ * hashes; an evict of a suffix returns to the hash after the kept tokens
+ * (only suffixes can be evicted). For testing the policy. */
 int fs_sched_create_model_free(const fs_sched_config* cfg, int32_t vocab,
                                fs_sched** out);
 

@@ -15,7 +15,15 @@
      * fold: the step that consumes the last prompt token yields the first
        generated token; a job retires at max_new_tokens or on its stop id;
      * sampling of a job's t-th generated token uses (seed, counter = t),
-       so a job's tokens do not depend on its lane, step or neighbours.
+       so a job's tokens do not depend on its lane, step or neighbours;
+     * prefix reuse ("MODEL-BATCHING-RESULTS", "Why in-kernel batching,
+       not vLLM": Clone for prefix reuse), when prefix_reuse_min > 0: a job
+       admitted into lane k takes the history of the busy lane whose fed
+       tokens (prompt, then generated tokens fed back) share the longest
+       prefix with its prompt (ties: lowest lane), capped at its prompt
+       length - 1, by a clone and an evict of the clone's suffix, if that
+       prefix has at least prefix_reuse_min tokens; it then feeds only the
+       rest of its prompt.
    ``step_fn(lanes, positions, tokens) -> logits[n, V]`` is the engine
    (the oracle model, or anything with the decode_step_batch contract);
    ``sample_fn(logits_row, temp, seed, counter) -> token``.
@@ -34,7 +42,8 @@ from collections import deque
 class Reference:
     def __init__(self, n_lanes: int, max_prefill_tokens_per_tick: int,
                  step_fn, sample_fn, reset_fn=None, prefill_chunk: int = 1,
-                 kv_budget_tokens: int = 0, lane_tokens: int = 0):
+                 kv_budget_tokens: int = 0, lane_tokens: int = 0,
+                 prefix_reuse_min: int = 0, clone_fn=None, evict_fn=None):
         self.n_lanes = n_lanes
         self.budget = max(1, int(max_prefill_tokens_per_tick))
         # prompt tokens one lane may consume in one step (chunked prefill,
@@ -53,6 +62,11 @@ class Reference:
         self.step_fn = step_fn
         self.sample_fn = sample_fn
         self.reset_fn = reset_fn
+        self.prefix_min = int(prefix_reuse_min)
+        self.clone_fn = clone_fn
+        self.evict_fn = evict_fn
+        self.prefix_hits = 0
+        self.prefix_tokens = 0
         self.pending = deque()
         self.lanes = [None] * n_lanes
         self.positions = [0] * n_lanes
@@ -95,6 +109,34 @@ class Reference:
                 self.lanes[k] = dict(job=job, feed=0, gen=[], last=None,
                                      seq=self.admit_seq)
                 self.admit_seq += 1
+                if self.prefix_min > 0:
+                    self._reuse_prefix(k)
+
+    def _fed(self, j: int) -> list:
+        """Tokens lane j fed so far: its prompt, then its generated tokens."""
+        ln = self.lanes[j]
+        return (list(ln["job"]["prompt"]) + ln["gen"])[:self.positions[j]]
+
+    def _reuse_prefix(self, k: int) -> None:
+        prompt = [int(t) for t in self.lanes[k]["job"]["prompt"]]
+        best, src = 0, None
+        for j in range(self.n_lanes):
+            if j == k or self.lanes[j] is None:
+                continue
+            fed = self._fed(j)
+            c = 0
+            while c < min(len(prompt) - 1, len(fed)) and int(fed[c]) == prompt[c]:
+                c += 1
+            if c > best:
+                best, src = c, j
+        if src is None or best < self.prefix_min:
+            return
+        self.clone_fn(src, k)
+        self.evict_fn(k, best, self.positions[src])
+        self.positions[k] = best
+        self.lanes[k]["feed"] = best
+        self.prefix_hits += 1
+        self.prefix_tokens += best
 
     def step(self):
         """One scheduler step; returns the list of job ids retired."""

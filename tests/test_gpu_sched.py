@@ -21,17 +21,24 @@ def _built():
     build.build()
 
 
-def _jobs(n, vocab, seed, max_prompt=12, max_new=10):
+def _jobs(n, vocab, seed, max_prompt=12, max_new=10, shared=0):
+    """Random jobs; with shared > 0 their prompts start with one of two common
+    prefixes of up to `shared` tokens (prefix reuse)."""
     g = np.random.default_rng(seed)
-    return [dict(id=j, arrive=int(g.integers(0, 2 * n)),
-                 prompt=[int(t) for t in g.integers(0, vocab, int(g.integers(1, max_prompt)))],
-                 max_new=int(g.integers(1, max_new)),
-                 temperature=0.0 if j % 2 else 0.8, seed=1000 + 7 * j)
-            for j in range(n)]
+    heads = [[int(t) for t in g.integers(0, vocab, shared)] for _ in range(2)] if shared else []
+    jobs = []
+    for j in range(n):
+        head = heads[j % 2][:int(g.integers(1, shared + 1))] if shared else []
+        jobs.append(dict(id=j, arrive=int(g.integers(0, 2 * n)),
+                         prompt=head + [int(t) for t in
+                                        g.integers(0, vocab, int(g.integers(1, max_prompt)))],
+                         max_new=int(g.integers(1, max_new)),
+                         temperature=0.0 if j % 2 else 0.8, seed=1000 + 7 * j))
+    return jobs
 
 
-def _run_sched(h, jobs, lanes, budget, chunk=1):
-    s = fs.fs_sched_create(h, lanes, budget, prefill_chunk=chunk)
+def _run_sched(h, jobs, lanes, budget, chunk=1, reuse=0):
+    s = fs.fs_sched_create(h, lanes, budget, prefill_chunk=chunk, prefix_reuse_min=reuse)
     try:
         order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
         ids, i, tick = {}, 0, 0
@@ -75,18 +82,25 @@ def test_scheduler_tiny_f32_per_job_equals_oracle_serial():
         assert got[j["id"]] == S.serial_job(j, step_fn, sample_fn, reset_fn), j["id"]
 
 
-@pytest.mark.parametrize("budget,chunk,max_prompt", [(3, 1, 12), (10, 6, 40)])
-def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise(budget, chunk, max_prompt):
-    """One token per lane per step, and chunked prefill (several prompt tokens
-    of a lane per step through fs_step_batch_chunked)."""
+@pytest.mark.parametrize("budget,chunk,max_prompt,reuse", [
+    (3, 1, 12, 0), (10, 6, 40, 0),
+    # prefix reuse: admitted jobs clone a running lane's shared prefix
+    (3, 1, 12, 1), (10, 6, 20, 4)])
+def test_scheduler_smollm2_bf16_per_job_equals_gpu_serial_bitwise(budget, chunk, max_prompt,
+                                                                 reuse):
+    """One token per lane per step, chunked prefill (several prompt tokens of
+    a lane per step through fs_step_batch_chunked), and prefix reuse (Clone of
+    a running lane, Evict of the clone's suffix)."""
     cfg = synth.with_layers(synth.MODEL_S, 2)
     Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
-    jobs = _jobs(12, cfg["V"], 5, max_prompt=max_prompt)
+    jobs = _jobs(12, cfg["V"], 5, max_prompt=max_prompt, shared=16 if reuse else 0)
     h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=6, max_pos=64)
     try:
-        got, st = _run_sched(h, jobs, 6, budget, chunk)
+        got, st = _run_sched(h, jobs, 6, budget, chunk, reuse)
         if chunk > 1:
             assert st["occupancy_max"] > 1
+        if reuse:
+            assert st["prefix_hits"] > 0
         for k in range(6):
             fs.fs_lane_reset(h, k)
         for j in jobs:  # each job alone on lane 0, one token per step

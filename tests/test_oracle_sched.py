@@ -198,3 +198,44 @@ def test_scheduler_reference_kv_budget_admission(tiny_engine):
     for job in jobs:
         if job["id"] in done:
             assert done[job["id"]] == S.serial_job(job, s_step, s_sample, s_reset), job["id"]
+
+
+def test_scheduler_reference_prefix_reuse_per_job_equals_serial(tiny_engine):
+    """Prefix reuse (Clone of a running lane, then Evict of the clone's
+    suffix): every job's tokens equal its serial run bit for bit, because a
+    position's K/V depend only on the tokens up to it; jobs share prompt
+    prefixes so that clones happen, and the reused tokens are not fed."""
+    cfg, m = tiny_engine
+    g = np.random.default_rng(9)
+    heads = [synth.make_prompts(1, 10, cfg["V"], seed=300 + i)[0] for i in range(2)]
+    jobs = []
+    for j in range(10):
+        head = [int(t) for t in heads[j % 2][:int(g.integers(3, 11))]]
+        tail = [int(t) for t in synth.make_prompts(1, int(g.integers(1, 6)), cfg["V"],
+                                                   seed=400 + j)[0]]
+        jobs.append(dict(id=j, arrive=int(g.integers(0, 10)), prompt=head + tail,
+                         max_new=int(g.integers(1, 8)),
+                         temperature=0.0 if j % 2 else 0.8, seed=3000 + j))
+    lanes = [m.lane(96) for _ in range(3)]
+
+    def step_fn(ks, poss, toks):
+        out = []
+        for k, p, t in zip(ks, poss, toks):
+            assert lanes[k].pos == p
+            out.append(m.step(lanes[k], t))
+        return out
+
+    def clone_fn(src, dst):
+        assert lanes[dst].pos == 0
+        lanes[dst].clone_from(lanes[src])
+
+    ref = S.Reference(3, 4, step_fn, lambda r, t, s, c: O.sample(r, t, s, c),
+                      lambda k: lanes[k].reset(), prefill_chunk=3, prefix_reuse_min=2,
+                      clone_fn=clone_fn, evict_fn=lambda k, a, b: lanes[k].evict(a, b))
+    done = ref.run(jobs)
+    assert ref.prefix_hits > 0
+    assert ref.prefill_tokens + ref.prefix_tokens == sum(len(j["prompt"]) for j in jobs)
+    s_step, s_reset, s_sample = _engine(m, 1)
+    for job in jobs:
+        assert done[job["id"]] == S.serial_job(job, s_step, s_sample, s_reset), job["id"]
+

@@ -25,21 +25,39 @@ def _mix64(z):
 
 
 class HashModel:
-    """Python restatement of the model-free engine, for the reference."""
+    """Python restatement of the model-free engine, for the reference (the
+    running hash after every consumed token, so that a clone copies a lane
+    and an evict of a suffix returns to an earlier hash)."""
+
+    INIT = 0xCBF29CE484222325
 
     def __init__(self, n_lanes, vocab):
-        self.h = [0xCBF29CE484222325] * n_lanes
+        self.hist = [[] for _ in range(n_lanes)]
         self.vocab = vocab
         self.batches = []
 
+    def h(self, k):
+        return self.hist[k][-1] if self.hist[k] else self.INIT
+
     def reset(self, k):
-        self.h[k] = 0xCBF29CE484222325
+        self.hist[k] = []
+
+    def clone(self, src, dst):
+        assert not self.hist[dst]
+        self.hist[dst] = list(self.hist[src])
+
+    def evict(self, k, start, end):
+        assert end == len(self.hist[k])  # suffixes only
+        del self.hist[k][start:]
 
     def step(self, ks, poss, toks):
         self.batches.append(list(ks))
-        for k, t in zip(ks, toks):
-            self.h[k] = ((self.h[k] ^ (t & 0xFFFFFFFF)) * 0x100000001B3) & M64
-        return [self.h[k] for k in ks]  # "logits": the lane's state
+        out = []
+        for k, p, t in zip(ks, poss, toks):
+            assert p == len(self.hist[k])
+            self.hist[k].append(((self.h(k) ^ (t & 0xFFFFFFFF)) * 0x100000001B3) & M64)
+            out.append(self.hist[k][-1])
+        return out  # "logits": each row's state
 
     def sample(self, state, temp, seed, counter):
         v = state
@@ -48,12 +66,18 @@ class HashModel:
         return int(v % self.vocab)
 
 
-def _jobs(n, vocab, seed, max_prompt=9, max_new=9):
+def _jobs(n, vocab, seed, max_prompt=9, max_new=9, shared=0):
+    """Random jobs; with shared > 0, prompts start with one of three common
+    prefixes of up to `shared` tokens (prefix reuse)."""
     g = np.random.default_rng(seed)
+    heads = [[int(t) for t in g.integers(0, vocab, int(g.integers(2, shared + 1)))]
+             for _ in range(3)] if shared else []
     jobs = []
     for j in range(n):
+        tail = [int(t) for t in g.integers(0, vocab, int(g.integers(1, max_prompt)))]
+        head = heads[int(g.integers(0, 3))][:int(g.integers(1, shared + 1))] if shared else []
         jobs.append(dict(id=j, arrive=int(g.integers(0, 3 * n)),
-                         prompt=[int(t) for t in g.integers(0, vocab, int(g.integers(1, max_prompt)))],
+                         prompt=head + tail,
                          max_new=int(g.integers(1, max_new)),
                          temperature=0.0 if g.uniform() < 0.5 else 0.8,
                          seed=int(g.integers(0, 2**63)),
@@ -61,22 +85,28 @@ def _jobs(n, vocab, seed, max_prompt=9, max_new=9):
     return jobs
 
 
-@pytest.mark.parametrize("lanes,budget,chunk,kv,seed", [
-    (1, 1, 1, 0, 0), (3, 1, 1, 0, 1), (4, 2, 1, 0, 2), (8, 3, 1, 0, 3), (5, 100, 1, 0, 4),
+@pytest.mark.parametrize("lanes,budget,chunk,kv,seed,reuse", [
+    (1, 1, 1, 0, 0, 0), (3, 1, 1, 0, 1, 0), (4, 2, 1, 0, 2, 0), (8, 3, 1, 0, 3, 0),
+    (5, 100, 1, 0, 4, 0),
     # chunked prefill: several prompt tokens of a lane in one step
-    (4, 6, 3, 0, 5), (3, 20, 8, 0, 6), (8, 5, 2, 0, 7), (2, 1, 4, 0, 8), (6, 100, 100, 0, 9),
+    (4, 6, 3, 0, 5, 0), (3, 20, 8, 0, 6, 0), (8, 5, 2, 0, 7, 0), (2, 1, 4, 0, 8, 0),
+    (6, 100, 100, 0, 9, 0),
     # bounded admission: a KV budget (tokens) smaller than the lanes could hold
-    (4, 2, 1, 14, 10), (6, 8, 4, 35, 11), (3, 100, 100, 25, 12)])
-def test_product_scheduler_matches_reference(lanes, budget, chunk, kv, seed):
+    (4, 2, 1, 14, 10, 0), (6, 8, 4, 35, 11, 0), (3, 100, 100, 25, 12, 0),
+    # prefix reuse: jobs sharing prompt prefixes clone a running lane
+    (4, 2, 1, 0, 13, 1), (6, 8, 4, 0, 14, 2), (8, 100, 100, 0, 15, 3), (3, 3, 2, 60, 16, 1)])
+def test_product_scheduler_matches_reference(lanes, budget, chunk, kv, seed, reuse):
     vocab = 97
-    jobs = _jobs(24, vocab, seed, max_prompt=9 if chunk == 1 else 30)
+    jobs = _jobs(24, vocab, seed, max_prompt=9 if chunk == 1 else 30,
+                 shared=12 if reuse else 0)
     model = HashModel(lanes, vocab)
     ref = S.Reference(lanes, budget, model.step, model.sample, model.reset,
-                      prefill_chunk=chunk, kv_budget_tokens=kv)
+                      prefill_chunk=chunk, kv_budget_tokens=kv, prefix_reuse_min=reuse,
+                      clone_fn=model.clone, evict_fn=model.evict)
     want = ref.run(jobs)
 
     s = fs.fs_sched_create_model_free(lanes, vocab, budget, prefill_chunk=chunk,
-                                      kv_budget_tokens=kv)
+                                      kv_budget_tokens=kv, prefix_reuse_min=reuse)
     try:
         order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
         ids, i, tick, batches, rejected = {}, 0, 0, [], []
@@ -118,6 +148,12 @@ def test_product_scheduler_matches_reference(lanes, budget, chunk, kv, seed):
         assert st["occupancy_max"] == max(ref.occupancy)
         assert abs(st["occupancy_avg"] - np.mean(ref.occupancy)) < 1e-12
         assert st["jobs_done"] == len(jobs) - len(rejected)
+        assert st["prefix_hits"] == ref.prefix_hits
+        assert st["prefix_tokens"] == ref.prefix_tokens
+        if reuse:
+            assert ref.prefix_hits > 0
+            assert st["prefill_tokens"] + st["prefix_tokens"] == sum(
+                len(j["prompt"]) for j in jobs if j["id"] not in rejected)
     finally:
         fs.fs_sched_destroy(s)
 
