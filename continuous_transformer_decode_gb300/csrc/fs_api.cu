@@ -19,6 +19,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fs.h"
 #include "fs_internal.h"
 
@@ -949,8 +951,17 @@ namespace {
 int decode_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
                 int32_t n, float* logits_out, int32_t* greedy_out);
 
+// An NVTX range around each step (no cost unless a tool is attached; a
+// profiler can then select a step's kernels by range).
+struct StepRange {
+  explicit StepRange(const char* name) { nvtxRangePushA(name); }
+  ~StepRange() { nvtxRangePop(); }
+};
+
 int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32_t* tokens,
              int n, float* logits_out, bool chunked, int32_t* greedy_out = nullptr) {
+  const StepRange range(chunked ? "fs_step_batch_chunked"
+                                : greedy_out ? "fs_decode_step_greedy" : "fs_decode_step_batch");
   const fs_model_desc& d = h->d;
   FS_CK(h, cudaEventSynchronize(h->args_done));  // staging no longer in use
   const int B = d.max_lanes;
@@ -1374,6 +1385,13 @@ int fs_lane_capacity(const fs_handle* h, int32_t* tokens_out) {
   if (!h || !tokens_out) return FS_ERR_ARG;
   *tokens_out = h->d.max_pos;
   return FS_OK;
+}
+
+int fs_selftest_bounded_wait(fs_handle* h, int32_t timeout_us, int32_t* code_out) {
+  if (!h || !code_out || timeout_us < 1 || timeout_us > 1000000) return FS_ERR_ARG;
+  h->launches += launch_wait_selftest((uint64_t)timeout_us * 1000ull, h->d_err_flag, h->stream);
+  FS_CK(h, cudaGetLastError());
+  return fs_device_error(h, code_out);
 }
 
 int fs_device_error(fs_handle* h, int32_t* code_out) {

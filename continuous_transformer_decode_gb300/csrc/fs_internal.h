@@ -385,6 +385,10 @@ int launch_import_kv(const KV& kv, int layer, const int32_t* pages, int n,
                      const float* k, const float* v, cudaStream_t s);
 int launch_export_kv(const KV& kv, int layer, const int32_t* pages, int n,
                      float* k, float* v, cudaStream_t s);
+// The failure-detection check's kernel (k_misc.cu): a bounded wait on a
+// barrier nothing arrives on; sets *err to kErrSelftest when it gives up.
+constexpr int kErrSelftest = 99;
+int launch_wait_selftest(uint64_t timeout_ns, int* err, cudaStream_t s);
 // Rows [q_begin, q_end) of one lane into the pages of dst_pt: row q from row
 // q (q < a) or q + delta (q >= a) of src_pt's pages, keys moved down by delta
 // turned back delta positions (k_misc.cu). Every layer, K and V.

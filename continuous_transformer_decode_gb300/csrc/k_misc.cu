@@ -518,6 +518,41 @@ int launch_kv_relocate(const KV& kv, int L, const int32_t* src_pt, const int32_t
   return 1;
 }
 
+// Failure-detection check: one thread waits on a barrier that nothing
+// arrives on, in the same bounded way as the step kernels' waits (try_wait
+// polled against %globaltimer), and on giving up sets the error flag and
+// returns, leaving the context usable.
+__global__ void k_wait_selftest(uint64_t timeout_ns, int* err) {
+  __shared__ uint64_t bar;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(&bar);
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const unsigned long long t0 = gtime();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(a)
+        : "memory");
+    if (ok) return;  // an arrival (none is made): no error
+    if (gtime() - t0 > timeout_ns) {
+      atomicExch(err, kErrSelftest);
+      return;
+    }
+  }
+}
+
+int launch_wait_selftest(uint64_t timeout_ns, int* err, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(timeout_ns, err);
+  return 1;
+}
+
 int launch_fill_random_kv(const KV& kv, int L, const int32_t* pages,
                           int n_pages, uint64_t seed, cudaStream_t s) {
   if (n_pages <= 0) return 0;

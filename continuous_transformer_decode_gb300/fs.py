@@ -104,6 +104,7 @@ def lib():
         "fs_lane_reset": (C.c_int, [p, i32]),
         "fs_lane_clone": (C.c_int, [p, i32, i32]),
         "fs_trace_enable": (C.c_int, [p, i64]),
+        "fs_selftest_bounded_wait": (C.c_int, [p, i32, p]),
         "fs_trace_read": (C.c_int, [p, p, i64, p, C.c_int]),
         "fs_lane_evict": (C.c_int, [p, i32, i32, i32]),
         "fs_decode_step_batch": (C.c_int, [p, p, p, p, i32, p]),
@@ -152,7 +153,7 @@ def lib():
 def exported_symbols() -> list:
     """Names of the entry points declared in include/fs.h."""
     return ["fs_create", "fs_destroy", "fs_last_error", "fs_set_stream",
-            "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_trace_enable", "fs_trace_read", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
+            "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_trace_enable", "fs_trace_read", "fs_selftest_bounded_wait", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
             "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
@@ -417,6 +418,15 @@ def fs_attention_path(h) -> str:
 def fs_device_error(h) -> int:
     v = C.c_int32()
     _check(h, lib().fs_device_error(h, C.byref(v)))
+    return v.value
+
+
+def fs_selftest_bounded_wait(h, timeout_us: int = 2000) -> int:
+    """Failure-detection check: a kernel's bounded wait on a barrier nothing
+    arrives on gives up after timeout_us; returns the device error code it
+    set (99), which is then cleared."""
+    v = C.c_int32()
+    _check(h, lib().fs_selftest_bounded_wait(h, int(timeout_us), C.byref(v)))
     return v.value
 
 

@@ -348,6 +348,15 @@ const char* fs_attention_path(const fs_handle* h);
  * reports a set code as FS_ERR_DEVICE. */
 int fs_device_error(fs_handle* h, int32_t* code_out);
 
+/* Failure-detection check (no counterpart on the pages): launches on the
+ * handle's stream a kernel that waits, bounded by timeout_us microseconds
+ * (1 .. 1e6), on a barrier nothing arrives on, the way every wait of the
+ * step kernels is bounded; on giving up it sets the handle's device error
+ * code to 99 and returns. Then as fs_device_error: synchronises, writes the
+ * code (99 when the check worked) and clears it. The handle stays usable.
+ * Errors: FS_ERR_ARG, FS_ERR_CUDA. */
+int fs_selftest_bounded_wait(fs_handle* h, int32_t timeout_us, int32_t* code_out);
+
 /* Test hook: Y[b, n] = sum_k X[b, k] * W[n, k] for bf16 W [N, K] and
  * X [B, K] (K a multiple of 64), f32 Y [B, N]; all DEVICE pointers owned by
  * the caller. path 1 = tcgen05 kernel with `splits` equal K splits per
