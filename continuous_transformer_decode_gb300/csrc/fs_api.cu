@@ -884,21 +884,25 @@ int fs_lane_clone(fs_handle* h, int32_t src, int32_t dst) {
   if (partial && h->free_pages.empty()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
   // full pages are shared (never written again: later tokens go to later
   // pages); the partial last page, which both lanes go on writing, is copied
+  // to the lowest free page. Device work first, host state after it, so a
+  // failed call leaves the lanes as they were (dst's row is unused while
+  // dst is empty).
   std::vector<int32_t> t(h->pt[src].begin(), h->pt[src].begin() + full);
-  for (int32_t p : t) ++h->page_ref[p];
-  if (partial) t.push_back(take_page(h));
+  if (partial) t.push_back(*h->free_pages.begin());
+  if (!t.empty()) {
+    int32_t* dst_row = h->kv.pt + (size_t)dst * h->kv.max_pages;
+    FS_CK(h, cudaMemcpyAsync(dst_row, t.data(), t.size() * 4, cudaMemcpyHostToDevice, h->stream));
+    if (partial) {
+      h->launches += launch_kv_relocate(h->kv, h->d.n_layers,
+                                        h->kv.pt + (size_t)src * h->kv.max_pages, dst_row,
+                                        full * ps, n, n, 0, h->rope_cos, h->rope_sin, h->stream);
+      FS_CK(h, cudaGetLastError());
+    }
+  }
+  for (int x = 0; x < full; ++x) ++h->page_ref[t[x]];
+  if (partial) take_page(h);  // the page chosen above: the lowest free one
   h->pt[dst] = std::move(t);
   h->len[dst] = n;
-  if (h->pt[dst].empty()) return FS_OK;
-  int32_t* dst_row = h->kv.pt + (size_t)dst * h->kv.max_pages;
-  FS_CK(h, cudaMemcpyAsync(dst_row, h->pt[dst].data(), h->pt[dst].size() * 4,
-                           cudaMemcpyHostToDevice, h->stream));
-  if (partial) {
-    h->launches += launch_kv_relocate(h->kv, h->d.n_layers, h->kv.pt + (size_t)src * h->kv.max_pages,
-                                      dst_row, full * ps, n, n, 0, h->rope_cos, h->rope_sin,
-                                      h->stream);
-    FS_CK(h, cudaGetLastError());
-  }
   return FS_OK;
 }
 
@@ -910,30 +914,40 @@ int fs_lane_evict(fs_handle* h, int32_t lane, int32_t start, int32_t end) {
   if (start == end) return FS_OK;
   const int delta = end - start, nl = n - delta;
   const int keep = (nl + ps - 1) / ps, first = start / ps;
-  const std::vector<int32_t> old = h->pt[lane];
+  const std::vector<int32_t>& old = h->pt[lane];
   // pages [first, keep) are written (moved rows now, the next token later):
-  // a page another lane still holds is replaced by a private copy
-  int need = 0;
-  for (int x = first; x < keep; ++x) need += h->page_ref[old[x]] > 1;
-  if (need > (int)h->free_pages.size()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+  // a page another lane still holds is replaced by a private copy, the
+  // lowest free pages in ascending index order
   std::vector<int32_t> t(old.begin(), old.begin() + keep);
+  auto fresh = h->free_pages.begin();
   for (int x = first; x < keep; ++x)
     if (h->page_ref[old[x]] > 1) {
-      --h->page_ref[old[x]];
-      t[x] = take_page(h);
+      if (fresh == h->free_pages.end()) return h->fail(FS_ERR_KV_FULL, "page pool exhausted");
+      t[x] = *fresh++;
     }
   // rows [start, nl) move down by delta; a replaced first page also takes
-  // its rows below start
+  // its rows below start. Device work first, host state after it.
   const int q_begin = (first < keep && t[first] != old[first]) ? first * ps : start;
   if (q_begin < nl) {
     int32_t* row = h->kv.pt + (size_t)lane * h->kv.max_pages;
     FS_CK(h, cudaMemcpyAsync(h->d_reloc_pt, row, old.size() * 4, cudaMemcpyDeviceToDevice,
                              h->stream));
-    FS_CK(h, cudaMemcpyAsync(row, t.data(), t.size() * 4, cudaMemcpyHostToDevice, h->stream));
-    h->launches += launch_kv_relocate(h->kv, h->d.n_layers, h->d_reloc_pt, row, q_begin, nl,
-                                      start, delta, h->rope_cos, h->rope_sin, h->stream);
-    FS_CK(h, cudaGetLastError());
+    cudaError_t e = cudaMemcpyAsync(row, t.data(), t.size() * 4, cudaMemcpyHostToDevice, h->stream);
+    if (e == cudaSuccess) {
+      h->launches += launch_kv_relocate(h->kv, h->d.n_layers, h->d_reloc_pt, row, q_begin, nl,
+                                        start, delta, h->rope_cos, h->rope_sin, h->stream);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {  // put the lane's device row back (best effort)
+      cudaMemcpyAsync(row, old.data(), old.size() * 4, cudaMemcpyHostToDevice, h->stream);
+      return h->cuda_fail(e, "evict");
+    }
   }
+  for (int x = first; x < keep; ++x)
+    if (t[x] != old[x]) {
+      --h->page_ref[old[x]];
+      take_page(h);  // == t[x]: the same lowest-first order
+    }
   // pages past the new end are let go (stream order keeps them unwritten
   // until the move above has read them)
   for (int x = keep; x < (int)old.size(); ++x) release_page(h, old[x]);
