@@ -453,6 +453,9 @@ def run_trace(args, wl, ws, rank):
     lanes = args.batch or wl["B"]
     n_jobs = args.jobs or min(512, 4 * lanes)
     jobs = synth.make_trace(n_jobs, cfg["V"], seed=5 + rank, lanes=lanes)
+    if args.shared_prefix:  # one system prompt ahead of every job's own prompt
+        head = [int(t) for t in synth.make_prompts(1, args.shared_prefix, cfg["V"], seed=77)[0]]
+        jobs = [dict(j, prompt=head + [int(t) for t in j["prompt"]]) for j in jobs]
     max_pos = max(len(j["prompt"]) + j["max_new"] for j in jobs) + 1
     ps = 16
     n_pages = lanes * ((max_pos + ps - 1) // ps)
@@ -462,7 +465,8 @@ def run_trace(args, wl, ws, rank):
     chunk = args.prefill_chunk or budget
 
     def run(sched_lanes, js):
-        s = fs.fs_sched_create(h, sched_lanes, budget, prefill_chunk=chunk)
+        s = fs.fs_sched_create(h, sched_lanes, budget, prefill_chunk=chunk,
+                               prefix_reuse_min=args.prefix_reuse)
         try:
             order = sorted(js, key=lambda j: (j["arrive"], j["id"]))
             ids, i, tick = {}, 0, 0
@@ -501,8 +505,13 @@ def run_trace(args, wl, ws, rank):
         alone_ok.append(got[j["id"]] == tokens[j["id"]])
     fs.fs_destroy(h)
     total = st["prefill_tokens"] + st["decode_tokens"]
+    # served: every job's prompt and generated tokens, whether fed or taken
+    # from a clone (prefix reuse)
+    served = sum(len(j["prompt"]) for j in jobs) + sum(len(t) for t in tokens.values())
     return dict(cfg=cfg, lanes=lanes, jobs=n_jobs, seconds=dt, steps=st["steps"],
                 tok_s=total * ws / dt, decode_tok_s=st["decode_tokens"] * ws / dt,
+                served_tok_s=served * ws / dt, prefix_hits=st["prefix_hits"],
+                prefix_tokens=st["prefix_tokens"],
                 prefill_tokens=st["prefill_tokens"], decode_tokens=st["decode_tokens"],
                 occupancy_avg=st["occupancy_avg"], occupancy_max=st["occupancy_max"],
                 budget=budget, chunk=chunk, alone_ok=alone_ok, max_pos=max_pos)
@@ -521,6 +530,11 @@ def main():
                          "small profiling captures, never for a reported number)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--shared-prefix", type=int, default=0,
+                    help="trace workload: a common system prompt of N tokens ahead of "
+                         "every job's prompt")
+    ap.add_argument("--prefix-reuse", type=int, default=0,
+                    help="trace workload: the scheduler's prefix_reuse_min (0: off)")
     ap.add_argument("--trace", type=int, default=0,
                     help="after the timed steps, trace N more steps' kernel timeline "
                          "(%%globaltimer per block) and add its summary to the line")
@@ -559,7 +573,11 @@ def main():
                            "layers": cfg["L"], "lanes": r["lanes"], "jobs": r["jobs"],
                            "max_prefill_tokens_per_tick": r["budget"],
                            "prefill_chunk": r["chunk"], "max_pos": r["max_pos"],
+                           "shared_prefix": args.shared_prefix,
+                           "prefix_reuse_min": args.prefix_reuse,
                            "parallelism": f"replicas x{ws}"},
+                "served_tok_s": r["served_tok_s"], "prefix_hits": r["prefix_hits"],
+                "prefix_tokens": r["prefix_tokens"],
                 "decode_tok_s": r["decode_tok_s"], "prefill_tokens": r["prefill_tokens"],
                 "decode_tokens": r["decode_tokens"], "occupancy_avg": r["occupancy_avg"],
                 "occupancy_max": r["occupancy_max"],
