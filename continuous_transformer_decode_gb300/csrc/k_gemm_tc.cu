@@ -181,60 +181,41 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
     return;
   }
   if (p.epi == EPI_ARGMAX) {
-    // per lane: (max, lowest row) over the tile's 128 rows. Eight lanes at a
-    // time: rows x lanes through shared memory, a thread scans 8 rows of one
-    // lane, then the 16 row groups combine (2 shuffles inside a warp, the 4
-    // warps in row order)
-    const int t = row_local;
-    const int j8 = t & 7, grp = t >> 3;  // lane within the half, group of 8 rows
-    float* sv = xbuf;                                      // [128][8]
-    float* wv = xbuf + 128 * 8;                            // [4][8]
-    int* wi = reinterpret_cast<int*>(wv + 4 * 8);          // [4][8]
+    // per lane: (max, lowest row) over the tile's 128 rows. In each warp, one
+    // integer max reduction over an order-preserving key of the value, then
+    // one min reduction over the rows that hold it; the 4 warps (rows in
+    // warp order) combine through shared memory, one barrier per chunk (two
+    // exchange buffers alternate between chunks)
+    const int t = row_local, w = t >> 5, l = t & 31;
+    const int row = m_tile * kBM + t;
+    const bool valid = row < p.n_out;
+    uint32_t* ek = reinterpret_cast<uint32_t*>(xbuf) + ((c0 >> 4) & 1) * 128;  // [4][16]
+    uint32_t* ei = ek + 64;                                                     // [4][16]
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t u = __float_as_uint(v[j] + 0.0f);  // -0 as +0
+      const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t imin =
+          __reduce_min_sync(0xffffffffu, (valid && key == kmax) ? (uint32_t)row : 0xffffffffu);
+      if (l == j) {
+        ek[w * 16 + j] = kmax;
+        ei[w * 16 + j] = imin;
+      }
+    }
+    epi_bar();
+    if (t < 16 && c0 + t < lanes) {
+      uint32_t km = ek[t], im = ei[t];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sv[t * 8 + j] = v[half * 8 + j];
-      epi_bar();
-      float bv = -CUDART_INF_F;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int rl = grp * 8 + r, row = m_tile * kBM + rl;
-        const float x = sv[rl * 8 + j8];
-        if (row < p.n_out && (x > bv || bi == INT_MAX)) {
-          bv = x;
-          bi = row;
+      for (int ww = 1; ww < 4; ++ww)
+        if (ek[ww * 16 + t] > km) {  // later warps hold larger rows
+          km = ek[ww * 16 + t];
+          im = ei[ww * 16 + t];
         }
-      }
-#pragma unroll
-      for (int o = 8; o < 32; o <<= 1) {  // the 4 row groups of this warp
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((t & 31) < 8) {
-        wv[(t >> 5) * 8 + j8] = bv;
-        wi[(t >> 5) * 8 + j8] = bi;
-      }
-      epi_bar();
-      const int lane_c = c0 + half * 8 + t;  // the lane this thread stores
-      if (t < 8 && lane_c < lanes) {
-        float mv = wv[t];
-        int mi = wi[t];
-#pragma unroll
-        for (int w = 1; w < 4; ++w)
-          if (wv[w * 8 + t] > mv) {  // later warps hold larger rows
-            mv = wv[w * 8 + t];
-            mi = wi[w * 8 + t];
-          }
-        const int64_t at = (int64_t)(lane0 + lane_c) * p.m_tiles + m_tile;
-        p.am_val[at] = mv;
-        p.am_idx[at] = mi;
-      }
-      epi_bar();
+      const uint32_t u = (km & 0x80000000u) ? (km & 0x7fffffffu) : ~km;
+      const int64_t at = (int64_t)(lane0 + c0 + t) * p.m_tiles + m_tile;
+      p.am_val[at] = __uint_as_float(u);
+      p.am_idx[at] = (int)im;
     }
     return;
   }
