@@ -20,7 +20,7 @@
 // layer (Q, K, V, O, gate, up, down) plus the LM head over a [B, d] panel, with
 // attention per user over that user's own KV cache.
 //
-// Readings taken where the pages are silent (each listed in the design doc):
+// Readings taken where the pages are silent:
 //   * RMSNorm: y = x * (1/sqrtf(sum(x^2)/d + eps)) * g, sum ascending.
 //   * RoPE: rotate-half pairing (i, i + hd/2), theta_i = theta^(-2i/hd), the
 //     angle and its cos/sin taken in double and rounded to f32; the position
