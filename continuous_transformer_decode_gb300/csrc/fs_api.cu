@@ -87,7 +87,10 @@ int trace_release(const fs_handle* h) {
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
   if (m_tiles >= sms) return m_tiles;
-  if (max_lanes <= 8 && T >= (int64_t)8 * sms) return 2 * sms;
+  // small handles, large matrices: about two blocks per SM, a whole number
+  // of splits per row tile so that no block's range crosses a tile
+  if (max_lanes <= 8 && T >= (int64_t)8 * sms)
+    return m_tiles * std::max(1, std::min(kb_total, 2 * sms / m_tiles));
   const bool narrow = max_lanes <= 32;
   int s = narrow ? (13 * sms + 5 * m_tiles) / (10 * m_tiles) : (85 * sms) / (100 * m_tiles);
   s = std::min(s, std::min(8, kb_total / (narrow ? 8 : 32)));
