@@ -153,6 +153,7 @@ struct fs_sched {
   std::deque<Job> pending;
   std::vector<Lane> lanes;
   std::map<int64_t, std::vector<int32_t>> done;
+  std::map<int64_t, int32_t> done_state;  // FS_JOB_DONE_* or FS_JOB_CANCELLED
   int64_t next_id = 0, admit_seq = 0;
   int64_t reserved = 0;  // KV tokens reserved by the lanes' jobs
   bool clock_started = false;
@@ -400,6 +401,8 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
     ln.last = t;
     if ((int)ln.gen.size() >= ln.job.max_new || (ln.job.stop >= 0 && t == ln.job.stop)) {
       s->done[ln.job.id] = ln.gen;
+      s->done_state[ln.job.id] =
+          (ln.job.stop >= 0 && t == ln.job.stop) ? FS_JOB_DONE_STOP : FS_JOB_DONE_LENGTH;
       s->reserved -= ln.job.need;
       ln.busy = false;
       s->st.jobs_done += 1;
@@ -437,7 +440,45 @@ int fs_sched_take(fs_sched* s, int64_t job_id, int32_t* tokens_out, int32_t cap,
   std::memcpy(tokens_out, it->second.data(), (size_t)std::min(n, cap) * 4);
   *n_out = n;
   s->done.erase(it);
+  s->done_state.erase(job_id);
   return FS_OK;
+}
+
+int fs_sched_status(const fs_sched* s, int64_t job_id, int32_t* state_out) {
+  if (!s || !state_out) return FS_ERR_ARG;
+  *state_out = FS_JOB_UNKNOWN;
+  for (const Job& j : s->pending)
+    if (j.id == job_id) *state_out = FS_JOB_QUEUED;
+  for (const Lane& l : s->lanes)
+    if (l.busy && l.job.id == job_id) *state_out = FS_JOB_RUNNING;
+  auto it = s->done_state.find(job_id);
+  if (it != s->done_state.end()) *state_out = it->second;
+  return FS_OK;
+}
+
+int fs_sched_cancel(fs_sched* s, int64_t job_id) {
+  if (!s) return FS_ERR_ARG;
+  for (auto it = s->pending.begin(); it != s->pending.end(); ++it)
+    if (it->id == job_id) {
+      s->pending.erase(it);
+      s->done[job_id] = {};
+      s->done_state[job_id] = FS_JOB_CANCELLED;
+      s->st.jobs_cancelled += 1;
+      return FS_OK;
+    }
+  for (int k = 0; k < s->cfg.lanes; ++k) {
+    Lane& ln = s->lanes[k];
+    if (!ln.busy || ln.job.id != job_id) continue;
+    const int rc = s->eng->reset(k);
+    if (rc) return s->fail(rc, "lane reset: " + s->eng->error());
+    s->done[job_id] = ln.gen;
+    s->done_state[job_id] = FS_JOB_CANCELLED;
+    s->reserved -= ln.job.need;
+    ln.busy = false;
+    s->st.jobs_cancelled += 1;
+    return FS_OK;
+  }
+  return s->fail(FS_ERR_STATE, "job unknown or already finished");
 }
 
 int fs_sched_get_stats(const fs_sched* s, fs_sched_stats* out) {

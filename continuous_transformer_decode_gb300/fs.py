@@ -78,7 +78,8 @@ class fs_sched_stats(C.Structure):
                 ("kv_budget_tokens", C.c_int64), ("kv_wait_steps", C.c_int64),
                 ("seconds", C.c_double), ("prefill_tok_s", C.c_double),
                 ("decode_tok_s", C.c_double),
-                ("prefix_hits", C.c_int64), ("prefix_tokens", C.c_int64)]
+                ("prefix_hits", C.c_int64), ("prefix_tokens", C.c_int64),
+                ("jobs_cancelled", C.c_int64)]
 
 
 LIB_PATH = _build.LIB
@@ -136,6 +137,8 @@ def lib():
         "fs_sched_run": (C.c_int, [p, i64, p]),
         "fs_sched_take": (C.c_int, [p, i64, p, i32, p]),
         "fs_sched_get_stats": (C.c_int, [p, C.POINTER(fs_sched_stats)]),
+        "fs_sched_status": (C.c_int, [p, i64, p]),
+        "fs_sched_cancel": (C.c_int, [p, i64]),
         "fs_sched_last_batch": (C.c_int, [p, p, i32, p]),
         "fs_sched_last_error": (C.c_char_p, [p]),
         "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
@@ -161,7 +164,8 @@ def exported_symbols() -> list:
             "fs_gemm_bf16", "fs_gemm_bf16_width", "fs_gemm_bf16_time", "fs_copy_logits", "fs_gemm_bf16_noalloc",
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
             "fs_sched_submit", "fs_sched_step", "fs_sched_run", "fs_sched_take",
-            "fs_sched_get_stats", "fs_sched_last_batch", "fs_sched_last_error"]
+            "fs_sched_get_stats", "fs_sched_status", "fs_sched_cancel", "fs_sched_last_batch",
+            "fs_sched_last_error"]
 
 
 def _check(h, rc: int) -> None:
@@ -552,6 +556,21 @@ def fs_sched_get_stats(s) -> dict:
     st = fs_sched_stats()
     _sched_check(s, lib().fs_sched_get_stats(s, C.byref(st)))
     return {k: getattr(st, k) for k, _ in st._fields_}
+
+
+JOB_UNKNOWN, JOB_QUEUED, JOB_RUNNING, JOB_DONE_LENGTH, JOB_DONE_STOP, JOB_CANCELLED = (
+    -1, 0, 1, 2, 3, 4)
+
+
+def fs_sched_status(s, job_id: int) -> int:
+    """One of the JOB_* states."""
+    v = C.c_int32()
+    _sched_check(s, lib().fs_sched_status(s, int(job_id), C.byref(v)))
+    return v.value
+
+
+def fs_sched_cancel(s, job_id: int) -> None:
+    _sched_check(s, lib().fs_sched_cancel(s, int(job_id)))
 
 
 def fs_sched_last_batch(s) -> list:

@@ -74,6 +74,14 @@ extern "C" {
 #define FS_ERR_QUEUE_FULL (-12) /* bounded pending queue is full (backpressure) */
 #define FS_ERR_KV_BUDGET (-13)  /* a job's prompt + new tokens can never fit   */
 
+/* Job states (fs_sched_status). */
+#define FS_JOB_UNKNOWN (-1)     /* never submitted, or already taken          */
+#define FS_JOB_QUEUED 0         /* waiting for a lane                         */
+#define FS_JOB_RUNNING 1        /* on a lane                                  */
+#define FS_JOB_DONE_LENGTH 2    /* finished: max_new_tokens generated         */
+#define FS_JOB_DONE_STOP 3      /* finished: sampled its stop token           */
+#define FS_JOB_CANCELLED 4      /* cancelled (fs_sched_cancel)                */
+
 typedef struct fs_sched fs_sched;
 
 typedef struct fs_sched_config {
@@ -121,6 +129,7 @@ typedef struct fs_sched_stats {
   double decode_tok_s;          /* decode_tokens / seconds                   */
   int64_t prefix_hits;          /* admissions that cloned a running lane     */
   int64_t prefix_tokens;        /* prompt tokens taken from clones, not fed  */
+  int64_t jobs_cancelled;
 } fs_sched_stats;
 
 /* Scheduler over a decode handle: each step is one fs_decode_step_batch
@@ -155,12 +164,25 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out);
 /* Steps until no job is queued or running, at most max_steps steps. */
 int fs_sched_run(fs_sched* s, int64_t max_steps, int64_t* steps_out);
 
-/* Copies a finished job's generated tokens (up to cap) and their count, then
- * forgets the job. Errors: FS_ERR_STATE (unknown or unfinished job). */
+/* Copies a finished or cancelled job's generated tokens (up to cap) and
+ * their count, then forgets the job. Errors: FS_ERR_STATE (unknown job, or
+ * one still queued or running). */
 int fs_sched_take(fs_sched* s, int64_t job_id, int32_t* tokens_out,
                   int32_t cap, int32_t* n_out);
 
 int fs_sched_get_stats(const fs_sched* s, fs_sched_stats* out);
+
+/* State of a job: one of FS_JOB_* (a taken job is unknown again). */
+int fs_sched_status(const fs_sched* s, int64_t job_id, int32_t* state_out);
+
+/* Cancels a queued or running job between steps (failure and cancellation
+ * handling of "DGR-012", "Summary": the KV is released when a session ends):
+ * a queued job leaves the queue; a running job's lane is reset (its pages go
+ * back to the pool), its KV reservation is released and the lane is free for
+ * the next fill. The tokens generated so far stay for fs_sched_take; the
+ * job's state becomes FS_JOB_CANCELLED. Errors: FS_ERR_STATE (unknown or
+ * already finished job), the engine's (lane reset). */
+int fs_sched_cancel(fs_sched* s, int64_t job_id);
 
 /* Lanes of the last step in batch order (inspection hook). */
 int fs_sched_last_batch(const fs_sched* s, int32_t* lanes_out, int32_t cap,

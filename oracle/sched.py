@@ -23,7 +23,12 @@
        prefix with its prompt (ties: lowest lane), capped at its prompt
        length - 1, by a clone and an evict of the clone's suffix, if that
        prefix has at least prefix_reuse_min tokens; it then feeds only the
-       rest of its prompt.
+       rest of its prompt;
+     * cancellation ("DGR-012", "Summary": KV released when a session ends),
+       between steps: a queued job leaves the queue, a running job's lane is
+       reset and freed with its KV reservation; the tokens generated so far
+       are kept. States: queued, running, done by length, done by stop id,
+       cancelled.
    ``step_fn(lanes, positions, tokens) -> logits[n, V]`` is the engine
    (the oracle model, or anything with the decode_step_batch contract);
    ``sample_fn(logits_row, temp, seed, counter) -> token``.
@@ -67,6 +72,8 @@ class Reference:
         self.evict_fn = evict_fn
         self.prefix_hits = 0
         self.prefix_tokens = 0
+        self.state = {}  # job id -> "done_length" | "done_stop" | "cancelled"
+        self.cancelled = 0
         self.pending = deque()
         self.lanes = [None] * n_lanes
         self.positions = [0] * n_lanes
@@ -201,10 +208,41 @@ class Reference:
             if len(ln["gen"]) >= job["max_new"] or (stop is not None
                                                     and t == stop):
                 self.done[job["id"]] = list(ln["gen"])
+                self.state[job["id"]] = ("done_stop" if stop is not None and t == stop
+                                         else "done_length")
                 self.reserved -= len(job["prompt"]) + job["max_new"]
                 self.lanes[k] = None
                 retired.append(job["id"])
         return retired
+
+    def status(self, job_id) -> str:
+        if any(j["id"] == job_id for j in self.pending):
+            return "queued"
+        if any(l is not None and l["job"]["id"] == job_id for l in self.lanes):
+            return "running"
+        return self.state.get(job_id, "unknown")
+
+    def cancel(self, job_id) -> bool:
+        """Between steps; False when the job is unknown or already finished."""
+        for j in list(self.pending):
+            if j["id"] == job_id:
+                self.pending.remove(j)
+                self.done[job_id] = []
+                self.state[job_id] = "cancelled"
+                self.cancelled += 1
+                return True
+        for k, ln in enumerate(self.lanes):
+            if ln is not None and ln["job"]["id"] == job_id:
+                if self.reset_fn:
+                    self.reset_fn(k)
+                self.positions[k] = 0
+                self.done[job_id] = list(ln["gen"])
+                self.state[job_id] = "cancelled"
+                self.reserved -= len(ln["job"]["prompt"]) + ln["job"]["max_new"]
+                self.lanes[k] = None
+                self.cancelled += 1
+                return True
+        return False
 
     def run(self, jobs, max_steps: int = 10**7) -> dict:
         """Run jobs with ``arrive`` ticks (0 if absent) to completion."""

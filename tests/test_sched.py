@@ -213,3 +213,64 @@ def test_dgr_sweep_shape_with_the_product_scheduler():
             fs.fs_sched_destroy(s)
     assert all(o == outs[0] for o in outs)
     assert occ == sorted(occ) and occ[0] == 1.0
+
+
+_STATE = {fs.JOB_UNKNOWN: "unknown", fs.JOB_QUEUED: "queued", fs.JOB_RUNNING: "running",
+          fs.JOB_DONE_LENGTH: "done_length", fs.JOB_DONE_STOP: "done_stop",
+          fs.JOB_CANCELLED: "cancelled"}
+
+
+@pytest.mark.parametrize("lanes,budget,chunk,kv,seed", [
+    (3, 2, 1, 0, 20), (5, 6, 3, 0, 21), (4, 3, 2, 40, 22)])
+def test_cancellation_matches_reference(lanes, budget, chunk, kv, seed):
+    """Cancellations between steps (queued and running jobs, and refused ones
+    for finished jobs): the same batches, tokens, states and counters as the
+    reference; a cancelled running job's lane and KV reservation are freed."""
+    vocab = 97
+    jobs = _jobs(20, vocab, seed, max_prompt=12, max_new=14)
+    g = np.random.default_rng(seed + 100)
+    model = HashModel(lanes, vocab)
+    ref = S.Reference(lanes, budget, model.step, model.sample, model.reset,
+                      prefill_chunk=chunk, kv_budget_tokens=kv)
+    s = fs.fs_sched_create_model_free(lanes, vocab, budget, prefill_chunk=chunk,
+                                      kv_budget_tokens=kv)
+    try:
+        order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
+        ids, i, tick, batches, n_refused = {}, 0, 0, [], 0
+        while i < len(order) or not ref.idle():
+            while i < len(order) and order[i]["arrive"] <= tick:
+                j = order[i]
+                assert ref.submit(j)
+                ids[j["id"]] = fs.fs_sched_submit(
+                    s, j["prompt"], j["max_new"], j["temperature"], j["seed"],
+                    -1 if j["stop"] is None else j["stop"])
+                i += 1
+            if ids and g.uniform() < 0.25:  # cancel a submitted job, maybe finished
+                jid = int(g.choice(sorted(ids)))
+                assert _STATE[fs.fs_sched_status(s, ids[jid])] == ref.status(jid)
+                ok = ref.cancel(jid)
+                if ok:
+                    fs.fs_sched_cancel(s, ids[jid])
+                else:
+                    n_refused += 1
+                    with pytest.raises(fs.FsError) as e:
+                        fs.fs_sched_cancel(s, ids[jid])
+                    assert e.value.name == "FS_ERR_STATE"
+            before = len(model.batches)
+            ref.step()
+            fs.fs_sched_step(s)
+            if len(model.batches) > before:
+                batches.append(fs.fs_sched_last_batch(s))
+            tick += 1
+        assert batches == model.batches
+        st = fs.fs_sched_get_stats(s)
+        assert st["jobs_cancelled"] == ref.cancelled > 0
+        assert st["jobs_done"] == len(jobs) - ref.cancelled
+        assert st["kv_reserved_tokens"] == 0 and ref.reserved == 0
+        for j in jobs:
+            assert _STATE[fs.fs_sched_status(s, ids[j["id"]])] == ref.status(j["id"])
+            assert fs.fs_sched_take(s, ids[j["id"]]) == ref.done[j["id"]]
+            assert fs.fs_sched_status(s, ids[j["id"]]) == fs.JOB_UNKNOWN
+        assert st["steps"] == ref.steps
+    finally:
+        fs.fs_sched_destroy(s)
