@@ -239,3 +239,42 @@ def test_scheduler_reference_prefix_reuse_per_job_equals_serial(tiny_engine):
     for job in jobs:
         assert done[job["id"]] == S.serial_job(job, s_step, s_sample, s_reset), job["id"]
 
+
+
+def test_scheduler_reference_cancellation_keeps_the_others_serial(tiny_engine):
+    """Cancelling queued and running jobs between steps frees their lanes for
+    others; every job not cancelled still gives its serial tokens, and a
+    cancelled running job keeps the tokens it had (a prefix of its serial
+    run)."""
+    cfg, m = tiny_engine
+    g = np.random.default_rng(12)
+    jobs = [dict(id=j, arrive=int(g.integers(0, 8)),
+                 prompt=synth.make_prompts(1, int(g.integers(1, 7)), cfg["V"],
+                                           seed=500 + j)[0],
+                 max_new=int(g.integers(2, 9)),
+                 temperature=0.0 if j % 2 else 0.8, seed=4000 + j) for j in range(10)]
+    step_fn, reset_fn, sample_fn = _engine(m, 3)
+    ref = S.Reference(3, 2, step_fn, sample_fn, reset_fn)
+    order = sorted(jobs, key=lambda j: (j["arrive"], j["id"]))
+    i, tick, cancelled = 0, 0, set()
+    while i < len(order) or not ref.idle():
+        while i < len(order) and order[i]["arrive"] <= tick:
+            ref.submit(order[i])
+            i += 1
+        if tick in (3, 6, 9):  # a running job, then whatever is oldest queued
+            running = [l["job"]["id"] for l in ref.lanes if l is not None]
+            target = running[0] if tick != 6 or not ref.pending else ref.pending[0]["id"]
+            if running or ref.pending:
+                assert ref.cancel(target)
+                cancelled.add(target)
+        ref.step()
+        tick += 1
+    assert ref.cancelled == len(cancelled) > 0 and ref.reserved == 0
+    s_step, s_reset, s_sample = _engine(m, 1)
+    for job in jobs:
+        solo = S.serial_job(job, s_step, s_sample, s_reset)
+        if job["id"] in cancelled:
+            assert ref.status(job["id"]) == "cancelled"
+            assert ref.done[job["id"]] == solo[:len(ref.done[job["id"]])]
+        else:
+            assert ref.done[job["id"]] == solo, job["id"]
