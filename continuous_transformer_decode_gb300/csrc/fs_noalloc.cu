@@ -12,16 +12,15 @@
 // memory allocated per call. Every GPU that loads this library keeps the array
 // until the process exits.
 //
-// Set-up: the first call on a device looks up the array's device address with
-// cudaGetSymbolAddress (with that device current) and caches it per device.
-// That first call on a device should come before any stream capture.
+// Set-up: every call looks up the array's device address on the current
+// device with cudaGetSymbolAddress (the lookup allocates nothing), so no
+// address outlives a device reset or a re-created context. The call then synchronises its stream and copies the kernel's
+// error flag to the host before it returns.
 //
 // Sharing: every call on a device uses the same array, which keeps the last
 // call's contents. Each call clears the counters and the error flag before
 // its launch. Calls that overlap on the GPU (on different streams, or from
 // different threads) race on the array and must be serialised by the caller.
-
-#include <mutex>
 
 #include "../../include/fs.h"
 #include "fs_internal.h"
@@ -34,28 +33,15 @@ constexpr size_t kPartialBytes = kScratchBytes - kCtrBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-unsigned char* g_dev_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array on the current device.
 unsigned char* scratch_on_current_device(int* rc) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     *rc = FS_ERR_CUDA;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_dev_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      *rc = FS_ERR_CUDA;
-      return nullptr;
-    }
-    g_dev_addr[dev] = static_cast<unsigned char*>(p);
-  }
   *rc = FS_OK;
-  return g_dev_addr[dev];
+  return static_cast<unsigned char*>(p);
 }
 
 }  // namespace

@@ -75,8 +75,13 @@ struct ModelFreeEngine : Engine {
   int capacity() const override { return cap; }
   int64_t lane_tokens() const override { return 0; }
   uint64_t hash(int lane) const { return hist[lane].empty() ? kInit : hist[lane].back(); }
+  int fail_resets = 0;  // host-side fault injection: the next n resets fail
   int reset(int lane) override {
     if (lane < 0 || lane >= cap) return FS_ERR_LANE;
+    if (fail_resets > 0) {
+      --fail_resets;
+      return FS_ERR_CUDA;
+    }
     hist[lane].clear();
     return FS_OK;
   }
@@ -243,6 +248,14 @@ int fs_sched_create_model_free(const fs_sched_config* cfg, int32_t vocab, fs_sch
   return make(std::unique_ptr<Engine>(new ModelFreeEngine(cfg->lanes, vocab)), cfg, out);
 }
 
+int fs_sched_model_free_fail_resets(fs_sched* s, int32_t n) {
+  if (!s || n < 0) return FS_ERR_ARG;
+  ModelFreeEngine* e = dynamic_cast<ModelFreeEngine*>(s->eng.get());
+  if (!e) return s->fail(FS_ERR_STATE, "not a model-free scheduler");
+  e->fail_resets = n;
+  return FS_OK;
+}
+
 int fs_sched_destroy(fs_sched* s) {
   delete s;
   return FS_OK;
@@ -293,10 +306,12 @@ int fs_sched_step(fs_sched* s, int32_t* n_retired_out) {
       s->st.kv_wait_steps += 1;
       break;
     }
-    s->reserved += s->pending.front().need;
-    s->st.kv_reserved_max = std::max(s->st.kv_reserved_max, s->reserved);
+    // the reservation is taken only once the lane is reset: a failed reset
+    // leaves the job pending and the reserved count unchanged
     int rc = s->eng->reset(k);
     if (rc) return s->fail(rc, "lane reset: " + s->eng->error());
+    s->reserved += s->pending.front().need;
+    s->st.kv_reserved_max = std::max(s->st.kv_reserved_max, s->reserved);
     ln.busy = true;
     ln.job = std::move(s->pending.front());
     s->pending.pop_front();

@@ -141,6 +141,7 @@ def lib():
         "fs_sched_cancel": (C.c_int, [p, i64]),
         "fs_sched_last_batch": (C.c_int, [p, p, i32, p]),
         "fs_sched_last_error": (C.c_char_p, [p]),
+        "fs_sched_model_free_fail_resets": (C.c_int, [p, i32]),
         "fs_gemm_bf16": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p]),
         "fs_gemm_bf16_width": (C.c_int, [p, i32, i32, p, i32, p, i32, p]),
         "fs_gemm_bf16_time": (C.c_int, [p, i32, i32, p, i32, p, i32, i32, p, p]),
@@ -165,7 +166,7 @@ def exported_symbols() -> list:
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
             "fs_sched_submit", "fs_sched_step", "fs_sched_run", "fs_sched_take",
             "fs_sched_get_stats", "fs_sched_status", "fs_sched_cancel", "fs_sched_last_batch",
-            "fs_sched_last_error"]
+            "fs_sched_last_error", "fs_sched_model_free_fail_resets"]
 
 
 def _check(h, rc: int) -> None:
@@ -578,6 +579,11 @@ def fs_sched_last_batch(s) -> list:
     buf = np.empty(4096, dtype=np.int32)
     _sched_check(s, lib().fs_sched_last_batch(s, _ptr(buf), buf.size, C.byref(n)))
     return buf[:n.value].tolist()
+
+
+def fs_sched_model_free_fail_resets(s, n: int) -> None:
+    """Test hook: the model-free engine fails its next n lane resets."""
+    _sched_check(s, lib().fs_sched_model_free_fail_resets(s, int(n)))
 
 
 def fs_sched_last_error(s) -> str:

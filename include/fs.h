@@ -403,12 +403,13 @@ int fs_gemm_bf16_time(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X
  * loads the library holds it until exit). It holds up to 16384 arrival
  * counters (ceil(N/128) * lane groups + 1 <= 16384) and, when splits > 1,
  * splits * B * ceil(N/128) * 128 f32 partials within 8 MiB - 64 KiB (for
- * example N = 4096, splits = 4, B <= 126). Larger requests return
- * FS_ERR_SCRATCH and run nothing. The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture. Every call shares the
- * array and clears its counters and error flag first; calls that overlap on
- * the GPU race and must be serialised by the caller.
+ * example N = 4096, splits = 4, B <= 127). Larger requests return
+ * FS_ERR_SCRATCH and run nothing. Every call looks up the array's device
+ * address on the current device (cudaGetSymbolAddress), synchronises
+ * `stream` after the launch and copies the kernel's error flag to the host
+ * before returning. Every call shares the array and clears its counters and
+ * error flag first; calls that overlap on the GPU race and must be
+ * serialised by the caller.
  * Errors: FS_ERR_ARG, FS_ERR_SCRATCH, FS_ERR_CUDA, FS_ERR_DEVICE. */
 int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
                          const uint16_t* X, int32_t B, float* Y,

@@ -149,6 +149,14 @@ int fs_sched_create(fs_handle* h, const fs_sched_config* cfg, fs_sched** out);
 int fs_sched_create_model_free(const fs_sched_config* cfg, int32_t vocab,
                                fs_sched** out);
 
+/* Host-side fault injection for tests of the policy (the pages have no
+ * counterpart): the model-free engine of s fails its next n lane resets with
+ * FS_ERR_CUDA, as a GPU engine would on a failed CUDA call. A step whose fill
+ * meets such a failure returns that error with the job still pending and
+ * the KV reservation not taken. Errors: FS_ERR_ARG (n < 0), FS_ERR_STATE (s
+ * is not over the model-free engine). */
+int fs_sched_model_free_fail_resets(fs_sched* s, int32_t n);
+
 int fs_sched_destroy(fs_sched* s);
 
 /* Queues a job (FIFO). *job_id_out receives its id (0, 1, ... in submit

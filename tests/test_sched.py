@@ -197,6 +197,30 @@ def test_backpressure_and_argument_errors():
         fs.fs_sched_destroy(s)
 
 
+def test_failed_lane_reset_takes_no_kv_reservation():
+    """Host-side fault injection: a lane reset that fails during fill leaves
+    the job pending and the KV reservation untaken; once resets succeed the
+    job runs and every reservation is released at the end."""
+    s = fs.fs_sched_create_model_free(2, 50, 1, kv_budget_tokens=40)
+    try:
+        fs.fs_sched_submit(s, [1, 2, 3], 5)       # needs 8 tokens of KV
+        fs.fs_sched_model_free_fail_resets(s, 1)
+        with pytest.raises(fs.FsError) as e:
+            fs.fs_sched_step(s)
+        assert e.value.name == "FS_ERR_CUDA"
+        st = fs.fs_sched_get_stats(s)
+        assert st["kv_reserved_tokens"] == 0
+        assert st["queued"] == 1 and st["active"] == 0
+        fs.fs_sched_run(s)
+        st = fs.fs_sched_get_stats(s)
+        assert st["jobs_done"] == 1 and st["kv_reserved_tokens"] == 0
+        assert st["kv_reserved_max"] == 8
+        with pytest.raises(fs.FsError):
+            fs.fs_sched_model_free_fail_resets(s, -1)
+    finally:
+        fs.fs_sched_destroy(s)
+
+
 def test_dgr_sweep_shape_with_the_product_scheduler():
     """DGR-012 sweep workload (8 sessions, prompt 4, 8 new tokens) through the
     product scheduler with one prompt token per step: per-session tokens are

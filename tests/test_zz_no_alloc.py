@@ -48,3 +48,21 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     with pytest.raises(fs.FsError) as e:
         fs.fs_gemm_bf16_noalloc(W, X, Y, splits=8)
     assert e.value.name == "FS_ERR_SCRATCH"
+
+
+def test_noalloc_scratch_limit_boundary():
+    """N = 4096 with 4 K splits needs 64 KiB of partials per lane: 127 lanes
+    fit the 8 MiB - 64 KiB partial area, 128 do not."""
+    import torch
+    N, K = 4096, 256
+    W = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+    for B, ok in ((127, True), (128, False)):
+        X = torch.zeros(B, K, dtype=torch.bfloat16, device="cuda")
+        Y = torch.full((B, N), 1.0, dtype=torch.float32, device="cuda")
+        if ok:
+            fs.fs_gemm_bf16_noalloc(W, X, Y, splits=4)
+            assert float(Y.abs().max()) == 0.0
+        else:
+            with pytest.raises(fs.FsError) as e:
+                fs.fs_gemm_bf16_noalloc(W, X, Y, splits=4)
+            assert e.value.name == "FS_ERR_SCRATCH"
