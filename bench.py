@@ -13,10 +13,17 @@ prompts, 12 decode steps; the B sweep there tops out at 256 for this shape).
   e2e        the same K steps through the host API: host arrays in
              (fs_decode_step_batch), host tokens out (fs_sample), timed with
              the host clock including every copy.
-  roofline   the weight-streaming GEMM (dominant kernel class): algorithmic
-             bytes per launch / mean launch time, from CUDA events around
-             each launch in a profiled pass of K steps identical to the timed
-             one, against the measured HBM copy bandwidth.
+  roofline   the weight-streaming GEMM (dominant kernel class): its
+             algorithmic bytes per step / its time per step, where its time
+             per step = the CUDA-event step time x the GEMM launches' share
+             of a traced step (the library's per-block %globaltimer tracer
+             over graph replays identical to the timed ones; a launch's share
+             is its dependency gap plus its body, so the shares partition the
+             step), against the measured HBM copy bandwidth.
+  workloads  the other measured configurations, each on its own handle
+             (SmolLM2-135M Q8_0 at 960 lanes, Mistral-7B bf16 at 1 and 128
+             lanes with contexts U[128, 4096]): device ms per step, tokens/s,
+             the step roofline fraction and the clocks of its timed region.
   cpu_baseline  the C++ f32 oracle (StepBatch) on this host's cores over a
              bounded sample of the same workload.
 
@@ -183,6 +190,56 @@ def gpu_weights(cfg, wdtype, seed=1):
     return Q, fs.FS_DTYPE_Q8_0
 
 
+def make_handle(cfg, wl, B, extra, W=None):
+    """A handle for B lanes of workload `wl`, its lanes filled the way the
+    pages' runs start: 16-token prompts ingested one token per lane per step,
+    or (long contexts) per-lane random KV of U[lo, hi] tokens. Returns the
+    handle and the step inputs (lanes, positions, next tokens, prompts,
+    contexts, weight dtype)."""
+    from continuous_transformer_decode_gb300 import fs, synth
+    prompt = wl.get("prompt", 0)
+    if "ctx" in wl:
+        ctx = synth.make_context_lengths(B, *wl["ctx"], seed=3)
+    else:
+        ctx = np.full(B, prompt, dtype=np.int32)
+    max_pos = int(ctx.max()) + extra
+    ps = 16
+    n_pages = int(sum(-(-(int(c) + extra) // ps) for c in ctx)) + B
+    if W is None:
+        W, wdt = gpu_weights(cfg, wl["wdtype"])
+    else:
+        W, wdt = W
+    desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps)
+    h = fs.fs_create(desc, W)
+    del W
+    return h, ctx, wdt
+
+
+def fill_lanes(h, cfg, wl, B, ctx):
+    from continuous_transformer_decode_gb300 import fs, synth
+    lanes = np.arange(B, dtype=np.int32)
+    prompts = None
+    if "ctx" in wl:  # long synthetic contexts: random KV (content irrelevant)
+        for b in range(B):
+            fs.fs_lane_fill_random_kv(h, b, int(ctx[b]), 1000 + b)
+        pos = ctx.astype(np.int32).copy()
+        toks = np.array([p[0] for p in synth.make_prompts(B, 1, cfg["V"], seed=2)], np.int32)
+    else:  # prompt ingestion, one token per lane per step, outside timing
+        prompts = np.stack(synth.make_prompts(B, wl["prompt"], cfg["V"], seed=2))
+        pos = np.zeros(B, dtype=np.int32)
+        for t in range(wl["prompt"]):
+            fs.fs_decode_step_batch(h, lanes, pos, prompts[:, t])
+        toks = prompts[:, -1].astype(np.int32).copy()
+    return lanes, pos, toks, prompts
+
+
+def gpu_id_of(local):
+    import torch
+    props = torch.cuda.get_device_properties(local)
+    gpu_id = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local)
+    return gpu_id[4:] if gpu_id.startswith("GPU-GPU-") else gpu_id
+
+
 def run_ours(args, wl, ws, rank, local):
     import torch
     from continuous_transformer_decode_gb300 import build, fs, synth
@@ -193,37 +250,13 @@ def run_ours(args, wl, ws, rank, local):
         cfg = synth.with_layers(cfg, args.layers)
     B = args.batch or wl["B"]
     K, Wm = args.steps, args.warmup
-    prompt = wl.get("prompt", 0)
-    if "ctx" in wl:
-        ctx = synth.make_context_lengths(B, *wl["ctx"], seed=3)
-    else:
-        ctx = np.full(B, prompt, dtype=np.int32)
-    extra = Wm + 3 * K + 8 + args.trace  # warm-up, timed, profiled, end-to-end, traced steps
-    max_pos = int(ctx.max()) + extra
-    ps = 16
-    n_pages = int(sum(-(-(int(c) + extra) // ps) for c in ctx)) + B
-    Wt, wdt = gpu_weights(cfg, wl["wdtype"])
-    desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps)
-    h = fs.fs_create(desc, Wt)
-    del Wt
+    extra = Wm + 2 * K + 8 + args.trace  # warm-up, timed, end-to-end, traced steps
+    h, ctx, wdt = make_handle(cfg, wl, B, extra)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     fs.fs_set_stream(h, stream)
-    lanes = np.arange(B, dtype=np.int32)
-    if "ctx" in wl:  # long synthetic contexts: random KV (content irrelevant)
-        for b in range(B):
-            fs.fs_lane_fill_random_kv(h, b, int(ctx[b]), 1000 + b)
-        pos = ctx.astype(np.int32).copy()
-        toks = np.array([p[0] for p in synth.make_prompts(B, 1, cfg["V"], seed=2)], np.int32)
-    else:  # prompt ingestion, one token per lane per step, outside timing
-        prompts = np.stack(synth.make_prompts(B, prompt, cfg["V"], seed=2))
-        pos = np.zeros(B, dtype=np.int32)
-        for t in range(prompt):
-            fs.fs_decode_step_batch(h, lanes, pos, prompts[:, t])
-        toks = prompts[:, -1].astype(np.int32).copy()
-    temps = torch.zeros(B, dtype=torch.float32, device="cuda")
-    seeds = torch.arange(B, dtype=torch.int64, device="cuda")
-    ctrs = torch.zeros(B, dtype=torch.int64, device="cuda")
+    lanes, pos, toks, prompts = fill_lanes(h, cfg, wl, B, ctx)
+    prompt = wl.get("prompt", 0)
     dtok = torch.empty(B, dtype=torch.int32, device="cuda")
 
     def device_step():  # greedy decode: tokens straight from the LM head's epilogue
@@ -232,11 +265,7 @@ def run_ours(args, wl, ws, rank, local):
     for _ in range(Wm):
         device_step()
     torch.cuda.synchronize()
-    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid) \
-        if hasattr(torch.cuda.get_device_properties(local), "uuid") else str(local)
-    if gpu_id.startswith("GPU-GPU-"):
-        gpu_id = gpu_id[4:]
-    clocks = Clocks(gpu_id)
+    clocks = Clocks(gpu_id_of(local))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -253,28 +282,19 @@ def run_ours(args, wl, ws, rank, local):
     launches = fs.fs_kernel_launches(h) - l0
     clk = clocks.stop()
 
-    # profiled pass: identical steps, CUDA events around every launch
-    fs.fs_profile_enable(h, True)
-    for c in range(3):
-        fs.fs_profile_read(h, c)
-    for _ in range(K):
-        device_step()
-    prof = {c: fs.fs_profile_read(h, c) for c in (fs.FS_PROF_GEMM, fs.FS_PROF_ATTN,
-                                                  fs.FS_PROF_OTHER)}
-    fs.fs_profile_enable(h, False)
-
     # end to end through the host API
     tk = torch.cuda.current_stream()
-    hsteps = K
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     htoks = toks.copy()
-    for i in range(hsteps):
+    for i in range(K):
         htoks = fs.fs_decode_step_greedy(h, lanes, pos, htoks)
     tk.synchronize()
     e2e_s = time.perf_counter() - t0
 
-    # kernel timeline of a few more identical steps (outside every timed region)
+    # kernel timeline of a few more identical steps (outside every timed
+    # region): per-launch gap + body, whose GEMM share times the timed step
+    # gives the GEMMs' time per step
     timeline = None
     if args.trace:
         from continuous_transformer_decode_gb300 import trace as tr
@@ -318,22 +338,90 @@ def run_ours(args, wl, ws, rank, local):
     total_tokens = B * K * ws
     value = total_tokens / (ms / 1e3)
     peaks = _peaks()
-    g_ms, g_n, g_bytes = prof[fs.FS_PROF_GEMM]
-    achieved = (g_bytes / g_n) / (g_ms / g_n / 1e3) / 1e9 if g_n else None
+    wb = {0: 4.0, 1: 2.0, 2: 34 / 32}[wdt]
+    g_bytes, g_launches = gemm_bytes_per_step(cfg, wb, B, greedy=True)
+    ms_step = ms / K
     roof = {"kernel": "weight-streaming GEMM (" + fs_path_name(cfg, wdt) + ")",
-            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-            "frac": (achieved / peaks["hbm"]) if achieved else None,
-            "traffic": None, "peak_source": peaks["src"],
-            "launches": g_n, "mean_launch_us": (g_ms / g_n * 1e3) if g_n else None,
-            "algorithmic_bytes_per_launch": (g_bytes / g_n) if g_n else None,
-            "share_of_step": {"gemm": g_ms, "attention": prof[fs.FS_PROF_ATTN][0],
-                              "other": prof[fs.FS_PROF_OTHER][0]}}
+            "bound": "hbm", "achieved": None, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": None, "traffic": None, "peak_source": peaks["src"],
+            "launches_per_step": g_launches,
+            "algorithmic_bytes_per_launch": g_bytes / g_launches}
+    if timeline:
+        share = sum(k["share"] or 0.0 for n, k in timeline["kernels"].items()
+                    if n.startswith("gemm"))
+        g_ms = share * ms_step
+        # the GEMMs' time cannot exceed the step: the shares partition it
+        assert 0.0 < g_ms <= ms_step, (g_ms, ms_step)
+        achieved = g_bytes / (g_ms / 1e3) / 1e9
+        roof.update(achieved=achieved, frac=achieved / peaks["hbm"],
+                    ms_per_step_of_kernel=g_ms, share_of_step=share,
+                    mean_launch_us=g_ms / g_launches * 1e3,
+                    method="CUDA-event step time x GEMM share of the traced step "
+                           "(gap + body per launch, %globaltimer per block)")
     arg_bytes = (7 * B + 1) * 4
     e2e = {"value": total_tokens / e2e_s, "unit": "tok/s",
-           "h2d_bytes_per_step": arg_bytes + B * (4 + 8 + 8),
+           "h2d_bytes_per_step": arg_bytes,
            "d2h_bytes_per_step": B * 4}
     return dict(value=value, ms=ms, B=B, launches=launches, clocks=clk, roofline=roof,
                 e2e=e2e, ctx=ctx, cfg=cfg, wdt=wdt, sweep=sweep, timeline=timeline)
+
+
+def time_steps(h, lanes, pos, toks, dtok, steps, warmup, local):
+    """Device time per greedy step (CUDA events on the handle's stream) and
+    the clocks sampled meanwhile."""
+    import torch
+    from continuous_transformer_decode_gb300 import fs
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fs.fs_decode_step_greedy(h, lanes, pos, toks, dtok)
+    torch.cuda.synchronize()
+    clocks = Clocks(gpu_id_of(local))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fs.fs_decode_step_greedy(h, lanes, pos, toks, dtok)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, clocks.stop()
+
+
+def run_workloads(args, local):
+    """The other configurations of the pages' measurements, each briefly on
+    its own handle: SmolLM2-135M Q8_0 at 960 lanes (MODEL-BATCHING-RESULTS,
+    "Measured": B = 512 -> 960) and Mistral-7B bf16 at 1 and 128 lanes with
+    contexts U[128, 4096]."""
+    import torch
+    from continuous_transformer_decode_gb300 import fs
+    peaks = _peaks()
+    out = []
+    steps, warm = 10, 3
+    plan = [("smollm2-135m-q8_0", [960]), ("mistral-7b-bf16", [1, 128])]
+    for name, Bs in plan:
+        wl = WORKLOADS[name]
+        cfg = model_cfg(wl["model"])
+        Wshared = gpu_weights(cfg, wl["wdtype"]) if len(Bs) > 1 else None
+        for B in Bs:
+            t0 = time.perf_counter()
+            h, ctx, wdt = make_handle(cfg, wl, B, warm + steps + 4, W=Wshared)
+            try:
+                fs.fs_set_stream(h, torch.cuda.current_stream())
+                lanes, pos, toks, _ = fill_lanes(h, cfg, wl, B, ctx)
+                dtok = torch.empty(B, dtype=torch.int32, device="cuda")
+                ms, clk = time_steps(h, lanes, pos, toks, dtok, steps, warm, local)
+            finally:
+                fs.fs_destroy(h)
+            wb = {0: 4.0, 1: 2.0, 2: 34 / 32}[wdt]
+            ctx_mean = float(np.mean(ctx)) + warm + steps / 2.0
+            sr = step_roofline(cfg, wb, B, ctx_mean, peaks)
+            tok_s = B / (ms / 1e3)
+            out.append({"workload": name, "lanes": B, "ms_per_step": ms, "tok_s": tok_s,
+                        "context": (f"16-token prompts" if "ctx" not in wl else
+                                    f"U[{wl['ctx'][0]},{wl['ctx'][1]}] mean {np.mean(ctx):.0f}"),
+                        "step_roofline": dict(sr, frac=tok_s / sr["tok_s_ceiling"]),
+                        "clocks": clk, "wall_s": time.perf_counter() - t0})
+        del Wshared
+        torch.cuda.empty_cache()
+    return out
 
 
 def step_roofline(cfg, wbytes_per_param, lanes, ctx_mean, peaks):
@@ -351,6 +439,21 @@ def step_roofline(cfg, wbytes_per_param, lanes, ctx_mean, peaks):
     tc = (peaks["bf16_sus"] or peaks["bf16"]) * 1e12 / flops_tok
     return {"tok_s_ceiling": min(hbm, tc), "bound": "hbm" if hbm < tc else "tensor",
             "bytes_per_step": bytes_step, "flops_per_token": flops_tok}
+
+
+def gemm_bytes_per_step(cfg, wbytes_per_param, lanes, greedy=True):
+    """Algorithmic bytes of every weight GEMM of one step: each weight once,
+    the bf16 input panel, the output (f32 rows; bf16 for the SwiGLU product;
+    per-tile (max, index) pairs for the greedy LM head)."""
+    d, F, V = cfg["d"], cfg["F"], cfg["V"]
+    nq, nkv = cfg["H"] * cfg["hd"], cfg["Hkv"] * cfg["hd"]
+    B = lanes
+    per_layer = ((nq + 2 * nkv) * d * wbytes_per_param + B * d * 2 + B * (nq + 2 * nkv) * 4
+                 + d * nq * wbytes_per_param + B * nq * 2 + B * d * 4
+                 + 2 * F * d * wbytes_per_param + B * d * 2 + B * F * 2
+                 + d * F * wbytes_per_param + B * F * 2 + B * d * 4)
+    head = V * d * wbytes_per_param + B * d * 2 + (B * -(-V // 128) * 8 if greedy else B * V * 4)
+    return cfg["L"] * per_layer + head, cfg["L"] * 4 + 1
 
 
 def traffic_for(kernel_src: str, workload: str, lanes: int):
@@ -535,9 +638,13 @@ def main():
                          "every job's prompt")
     ap.add_argument("--prefix-reuse", type=int, default=0,
                     help="trace workload: the scheduler's prefix_reuse_min (0: off)")
-    ap.add_argument("--trace", type=int, default=0,
+    ap.add_argument("--trace", type=int, default=2,
                     help="after the timed steps, trace N more steps' kernel timeline "
-                         "(%%globaltimer per block) and add its summary to the line")
+                         "(%%globaltimer per block): the GEMM roofline's time share "
+                         "and the line's kernel_timeline (0: off, no roofline)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations' record (Q8_0 at 960 lanes, "
+                         "Mistral-7B at 1 and 128 lanes)")
     ap.add_argument("--jobs", type=int, default=0,
                     help="trace workload: number of jobs (default min(512, 4 x lanes))")
     ap.add_argument("--prefill-budget", type=int, default=0,
@@ -622,6 +729,10 @@ def main():
             import torch
             torch.distributed.destroy_process_group()
         return
+    workloads = None
+    if (ws == 1 and not args.no_workloads and not args.layers and not args.batch
+            and args.workload == "smollm2-135m-bf16"):
+        workloads = run_workloads(args, local)
     cb = None if args.no_cpu_baseline else cpu_baseline(wl, r["B"])
     cfg = r["cfg"]
     wbytes = {"bf16": 2, "q8_0": 34 / 32}[wl["wdtype"]]
@@ -652,6 +763,7 @@ def main():
         **({"reduced_layers_for_profiling": args.layers} if args.layers else {}),
         "clocks": r["clocks"], "gpu_launches": r["launches"],
         **({"kernel_timeline": r["timeline"]} if r["timeline"] else {}),
+        **({"workloads": workloads} if workloads else {}),
     }
     print(json.dumps(line))
     if ws > 1:

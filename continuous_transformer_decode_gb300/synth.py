@@ -12,6 +12,8 @@ is a Mistral). No real weights or datasets are used anywhere.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 # name: L layers, d width, H/Hkv heads, hd head dim, F ffn, V vocab
@@ -64,24 +66,38 @@ def _normal(seed: int, path, shape) -> np.ndarray:
             * np.float32(WEIGHT_STD)).astype(np.float32)
 
 
-def make_weights(cfg: dict, seed: int = 1, fmt: str = "bf16") -> dict:
+def make_weights(cfg: dict, seed: int = 1, fmt: str = "bf16",
+                 workers: int = 0) -> dict:
     """Random-init weights N(0, 0.02), norm gains 1.
 
     fmt "f32": float32 matrices; "bf16": uint16 bf16 bits of the same draws.
     Returns the dict layout of the library's and the oracle's weight inputs.
+    Every matrix draws from its own seeded stream, so `workers` threads
+    (0: one per core) give the same values as one.
     """
     assert fmt in ("f32", "bf16")
     enc = (lambda a: a) if fmt == "f32" else bf16_bits
     d, V = cfg["d"], cfg["V"]
-    w = {"embed": enc(_normal(seed, (0, 0), (V, d))),
-         "lm_head": None if cfg["tied"] else enc(_normal(seed, (0, 1), (V, d))),
-         "final_norm": np.ones(d, dtype=np.float32),
-         "layers": []}
     shapes = matrix_shapes(cfg)
+    jobs = [("embed", (0, 0), (V, d))]
+    if not cfg["tied"]:
+        jobs.append(("lm_head", (0, 1), (V, d)))
     for l in range(cfg["L"]):
-        ly = {}
         for j, k in enumerate(LAYER_KEYS[:7]):
-            ly[k] = enc(_normal(seed, (1, l, j), shapes[k]))
+            jobs.append(((l, k), (1, l, j), shapes[k]))
+    n_workers = workers or os.cpu_count() or 1
+    draw = lambda job: enc(_normal(seed, job[1], job[2]))
+    if n_workers > 1 and len(jobs) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(min(n_workers, len(jobs))) as ex:
+            mats = list(ex.map(draw, jobs))
+    else:
+        mats = [draw(j) for j in jobs]
+    got = {job[0]: m for job, m in zip(jobs, mats)}
+    w = {"embed": got["embed"], "lm_head": got.get("lm_head"),
+         "final_norm": np.ones(d, dtype=np.float32), "layers": []}
+    for l in range(cfg["L"]):
+        ly = {k: got[(l, k)] for k in LAYER_KEYS[:7]}
         ly["attn_norm"] = np.ones(d, dtype=np.float32)
         ly["ffn_norm"] = np.ones(d, dtype=np.float32)
         w["layers"].append(ly)

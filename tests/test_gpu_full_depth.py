@@ -1,0 +1,339 @@
+"""GPU parity at full depth, on handles of the sizes the benchmark runs.
+
+The GEMM work split depends on the handle's lane capacity and the lane
+grouping on a call's lane count, so these tests use the benchmark's handles
+and call shapes: every lane of the handle steps in every call, and the
+oracle follows a sample of the lanes (one by one would give the same bits:
+its StepBatch equals its serial Step). Lanes in between feed their own
+prompts.
+
+- SmolLM2-135M shape, all 30 layers, bf16 weights: a 256-lane handle, all
+  256 lanes per call, 16-token prompts and 4 teacher-forced decode steps,
+  then one greedy step through the fused LM-head argmax.
+- The same shape with Q8_0 weights on a 960-lane handle, all 960 lanes per
+  call, against the oracle's Q8_0 model (bf16 tolerance) and the pages'
+  Q8 gate against the unquantised model.
+- Chunked prefill on the 30-layer model against the oracle's per-token
+  logits (both attention kernels).
+- Mistral-7B shape, all 32 layers, bf16: a 1-lane handle and a 128-lane
+  handle with ragged long contexts (bf16-exact synthetic KV on both sides).
+
+Tolerances ("MODEL-BATCHING-RESULTS", "Correctness — proven, not asserted",
+read with bf16 weights): per (lane, step) logits row max-abs <= 5e-2 and
+cosine >= 0.9995; greedy tokens equal wherever the oracle's top-1 - top-2
+margin exceeds twice the measured max-abs error. Q8_0 gate: decisive first
+token exact, teacher-forced top-1 >= 80%, mean cosine >= 0.99.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle.core as O
+from continuous_transformer_decode_gb300 import fs, synth
+from tests import _gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MIN_COS = 5e-2, 0.9995
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from continuous_transformer_decode_gb300 import build
+    build.build()
+    O.set_threads(os.cpu_count() or 8)
+
+
+def _margin(r):
+    s = np.sort(r, axis=-1)
+    return s[..., -1] - s[..., -2]
+
+
+def oracle_lockstep(model, prompts, n_steps, max_pos):
+    """Oracle StepBatch over the sampled lanes in lockstep (equal prompt
+    lengths): prompt tokens, then n_steps greedy tokens. Returns the fed
+    sequences [n][T], the logits [n, T, V] and the oracle lanes."""
+    lanes = [model.lane(max_pos) for _ in prompts]
+    P = len(prompts[0])
+    seqs = [list(map(int, p)) for p in prompts]
+    rows = []
+    for t in range(P + n_steps):
+        if t >= P:
+            for i in range(len(seqs)):
+                seqs[i].append(int(np.argmax(rows[-1][i])))
+        rows.append(model.step_batch(lanes, [s[t] for s in seqs]))
+    return seqs, np.stack(rows, axis=1), lanes
+
+
+def gpu_lockstep(h, feed, sample, V):
+    """Every lane of `feed` steps in every call (one token per lane); returns
+    the sampled lanes' logits [n_sample, T, V]."""
+    import torch
+    B, T = len(feed), len(feed[0])
+    lanes = np.arange(B, dtype=np.int32)
+    pos = np.array([fs.fs_lane_length(h, k) for k in range(B)], np.int32)
+    idx = torch.tensor(sample, device="cuda", dtype=torch.long)
+    buf = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    out = np.zeros((len(sample), T, V), np.float32)
+    for t in range(T):
+        fs.fs_decode_step_batch(h, lanes, pos, [feed[b][t] for b in range(B)], logits_out=buf)
+        out[:, t] = buf.index_select(0, idx).cpu().numpy()
+    return out, pos
+
+
+def check_rows(got, ref):
+    """Per-row tolerance over [n, T, V]; returns the worst max-abs error."""
+    worst = 0.0
+    for i in range(got.shape[0]):
+        err, _ = U.compare_logits(got[i], ref[i], MAX_ABS, MIN_COS)
+        worst = max(worst, err)
+    return worst
+
+
+def greedy_step_vs_oracle(h, model, o_lanes, sample, feed_next, B, V, pos, worst):
+    """One fused-greedy step of all B lanes (no logits written) against the
+    oracle's argmax for the sampled lanes where decisive."""
+    lanes = np.arange(B, dtype=np.int32)
+    toks = fs.fs_decode_step_greedy(h, lanes, pos, feed_next)
+    ref = model.step_batch(o_lanes, [feed_next[b] for b in sample])
+    dec = _margin(ref) > 2 * max(worst, 1e-3)
+    want = np.argmax(ref, -1)
+    got = toks[sample]
+    assert np.array_equal(got[dec], want[dec]), (got, want, dec)
+    return int(dec.sum())
+
+
+# ------------------------------------------------------------ SmolLM2 bf16
+@pytest.fixture(scope="module")
+def smol():
+    cfg = synth.MODEL_S
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    return cfg, Wb, O.Model(cfg, Wb, O.BF16)
+
+
+# lanes spread over the handle (first, last, both sides of every 64-lane
+# boundary)
+SAMPLE_256 = [0, 9, 31, 63, 64, 100, 127, 128, 129, 170, 191, 192, 222, 253, 254, 255]
+
+
+def test_smollm2_bf16_full_depth_256_lane_handle(smol):
+    cfg, Wb, m = smol
+    V, B, P, n_steps = cfg["V"], 256, 16, 4
+    prompts = synth.make_prompts(B, P, V, seed=2)
+    seqs, ref, o_lanes = oracle_lockstep(m, [prompts[b] for b in SAMPLE_256], n_steps, 48)
+    feed = [list(map(int, p)) + [int(p[i]) for i in range(n_steps)] for p in prompts]
+    for i, b in enumerate(SAMPLE_256):
+        feed[b] = seqs[i]
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=B, max_pos=48)
+    try:
+        assert fs.fs_gemm_path(h) == "tcgen05"
+        got, pos = gpu_lockstep(h, feed, SAMPLE_256, V)
+        assert pos.tolist() == [P + n_steps] * B
+        worst = check_rows(got, ref)
+        for i in range(len(SAMPLE_256)):
+            U.decisive_token_agreement(got[i], ref[i], worst)
+        nxt = [int(feed[b][-1]) for b in range(B)]
+        for i, b in enumerate(SAMPLE_256):
+            nxt[b] = int(np.argmax(ref[i, -1]))
+        n_dec = greedy_step_vs_oracle(h, m, o_lanes, SAMPLE_256, nxt, B, V, pos, worst)
+        assert n_dec >= len(SAMPLE_256) // 2
+    finally:
+        fs.fs_destroy(h)
+
+
+def _chunk_plan(prompts, chunk):
+    """Steps of (lane, position, token) rows: each lane feeds up to `chunk`
+    prompt tokens per step, lanes in order, rows of a lane reversed."""
+    done = [0] * len(prompts)
+    steps = []
+    while any(d < len(p) for d, p in zip(done, prompts)):
+        rows = []
+        for k, p in enumerate(prompts):
+            c = min(chunk + k % 3, len(p) - done[k])
+            if c <= 0:
+                continue
+            rows += [(k, q, int(p[q])) for q in range(done[k] + c - 1, done[k] - 1, -1)]
+            done[k] += c
+        steps.append(rows)
+    return steps
+
+
+CHUNK_LENS = [41, 23, 9, 64, 30]
+
+
+@pytest.fixture(scope="module")
+def chunk_ref(smol):
+    """Oracle logits of every (lane, position) of the chunked prompts (serial
+    Step per token) and the lanes after them."""
+    cfg, Wb, m = smol
+    prompts = synth.make_prompts(len(CHUNK_LENS), CHUNK_LENS, cfg["V"], seed=44)
+    ref, o_lanes = {}, []
+    for k, p in enumerate(prompts):
+        ln = m.lane(600)
+        for q, tok in enumerate(p):
+            ref[(k, q)] = m.step(ln, int(tok))
+        o_lanes.append(ln)
+    return prompts, ref, o_lanes
+
+
+@pytest.mark.parametrize("max_pos,path", [(128, "cp.async-mma"), (600, "tma-mma")])
+def test_smollm2_bf16_full_depth_chunked_prefill_vs_oracle(smol, chunk_ref, max_pos, path):
+    """fs_step_batch_chunked at full depth: every row's logits against the
+    oracle's logits for that (lane, position); then a decode step."""
+    import torch
+    cfg, Wb, m = smol
+    V = cfg["V"]
+    lens = CHUNK_LENS
+    prompts, ref, src_lanes = chunk_ref
+    o_lanes = []
+    for src in src_lanes:  # copies: the decode step below advances them
+        ln = m.lane(600)
+        ln.clone_from(src)
+        o_lanes.append(ln)
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=32, max_pos=max_pos)
+    try:
+        assert fs.fs_attention_path(h) == path
+        worst = 0.0
+        for rows in _chunk_plan(prompts, 4):
+            la = [r[0] for r in rows]
+            po = np.array([r[1] for r in rows], np.int32)
+            buf = torch.empty((len(rows), V), dtype=torch.float32, device="cuda")
+            fs.fs_step_batch_chunked(h, la, po, [r[2] for r in rows], logits_out=buf)
+            got = buf.cpu().numpy()
+            want = np.stack([ref[(r[0], r[1])] for r in rows])
+            err, _ = U.compare_logits(got, want, MAX_ABS, MIN_COS)
+            worst = max(worst, err)
+            U.decisive_token_agreement(got, want, max(worst, 1e-3))
+        assert [fs.fs_lane_length(h, k) for k in range(len(lens))] == lens
+        # one decode step of every lane on the chunk-built caches
+        nxt = [int(np.argmax(ref[(k, n - 1)])) for k, n in enumerate(lens)]
+        want = m.step_batch(o_lanes, nxt)
+        buf = torch.empty((len(lens), V), dtype=torch.float32, device="cuda")
+        fs.fs_decode_step_batch(h, list(range(len(lens))), np.array(lens, np.int32), nxt,
+                                logits_out=buf)
+        got = buf.cpu().numpy()
+        err, _ = U.compare_logits(got, want, MAX_ABS, MIN_COS)
+        U.decisive_token_agreement(got, want, max(worst, err, 1e-3))
+    finally:
+        fs.fs_destroy(h)
+
+
+# ------------------------------------------------------------ SmolLM2 Q8_0
+SAMPLE_960 = [0, 63, 64, 255, 256, 511, 640, 900, 958, 959]
+
+
+def test_smollm2_q8_full_depth_960_lane_handle(smol):
+    cfg, Wb, m_f32 = smol
+    V, B, P, n_steps = cfg["V"], 960, 16, 2
+    Wq = U.quantize_weights(Wb)
+    mq = O.Model(cfg, Wq, O.Q8_0)
+    prompts = synth.make_prompts(B, P, V, seed=2)
+    seqs, ref, o_lanes = oracle_lockstep(mq, [prompts[b] for b in SAMPLE_960], n_steps, 32)
+    feed = [list(map(int, p)) + [int(p[i]) for i in range(n_steps)] for p in prompts]
+    for i, b in enumerate(SAMPLE_960):
+        feed[b] = seqs[i]
+    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=B, max_pos=32)
+    try:
+        assert fs.fs_gemm_path(h) == "tcgen05-q8_0"
+        got, pos = gpu_lockstep(h, feed, SAMPLE_960, V)
+        worst = check_rows(got, ref)
+        for i in range(len(SAMPLE_960)):
+            U.decisive_token_agreement(got[i], ref[i], worst)
+        # the pages' Q8 gate: GPU Q8_0 against the unquantised model on the
+        # same (teacher-forced) tokens, over the decode rows
+        f_lanes = [m_f32.lane(32) for _ in SAMPLE_960]
+        rows_f = np.stack([m_f32.step_batch(f_lanes, [s[t] for s in seqs])
+                           for t in range(P + n_steps)], axis=1)
+        dec_rows = slice(P - 1, P + n_steps)
+        first = rows_f[:, P - 1]
+        decisive = _margin(first) > 0.05
+        assert np.array_equal(np.argmax(first, -1)[decisive],
+                              np.argmax(got[:, P - 1], -1)[decisive])
+        gf, gq = rows_f[:, dec_rows].reshape(-1, V), got[:, dec_rows].reshape(-1, V)
+        top1 = np.mean(np.argmax(gf, -1) == np.argmax(gq, -1))
+        cos = np.mean((gf * gq).sum(-1) / (np.linalg.norm(gf, axis=-1) *
+                                            np.linalg.norm(gq, axis=-1)))
+        assert top1 >= 0.80 and cos >= 0.99, (top1, cos)
+        nxt = [int(feed[b][-1]) for b in range(B)]
+        for i, b in enumerate(SAMPLE_960):
+            nxt[b] = int(np.argmax(ref[i, -1]))
+        greedy_step_vs_oracle(h, mq, o_lanes, SAMPLE_960, nxt, B, V, pos, worst)
+    finally:
+        fs.fs_destroy(h)
+
+
+# ------------------------------------------------------------ Mistral-7B
+def _mem_available_gb():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) / 2**20
+    except OSError:
+        pass
+    return 0.0
+
+
+def _bf16_exact_kv(n, cfg, seed, lane):
+    Ks, Vs = [], []
+    for l in range(cfg["L"]):
+        K, V = synth.make_kv(n, cfg["Hkv"], cfg["hd"], seed=seed, path=(lane, l))
+        Ks.append(synth.bf16_to_f32(synth.bf16_bits(K)))
+        Vs.append(synth.bf16_to_f32(synth.bf16_bits(V)))
+    return np.stack(Ks), np.stack(Vs)
+
+
+def test_mistral_full_depth_b1_and_128_lane_handles():
+    """All 32 layers of the Mistral-7B shape: a 1-lane handle (context 2500)
+    and a 128-lane handle whose other lanes hold ragged random contexts
+    U[128, 4096], with two sampled lanes (contexts 3001 and 640) followed by
+    the oracle; two teacher-forced steps, then a fused-greedy step."""
+    import torch
+    if _mem_available_gb() < 80:
+        pytest.skip("needs about 80 GB of host memory for the f32 7B oracle")
+    cfg = synth.MODEL_M
+    V, L, Hkv, hd = cfg["V"], cfg["L"], cfg["Hkv"], cfg["hd"]
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    m = O.Model(cfg, Wb, O.BF16)
+    cases = [(1, {0: 2500}), (128, {3: 3001, 77: 640})]
+    for B, sampled in cases:
+        ctx = synth.make_context_lengths(B, seed=3)
+        for k, n in sampled.items():
+            ctx[k] = n
+        max_pos = int(ctx.max()) + 8
+        n_pages = int(sum(-(-(int(c) + 8) // 16) for c in ctx)) + B
+        h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=B, max_pos=max_pos,
+                       n_pages=n_pages)
+        try:
+            o_lanes, sample = [], sorted(sampled)
+            for k in range(B):
+                if k in sampled:
+                    K, Vv = _bf16_exact_kv(int(ctx[k]), cfg, 31, k)
+                    fs.fs_lane_import_kv(h, k, K, Vv)
+                    ln = m.lane(max_pos)
+                    for l in range(L):
+                        ln.import_kv(l, K[l], Vv[l])
+                    o_lanes.append(ln)
+                    del K, Vv
+                else:
+                    fs.fs_lane_fill_random_kv(h, k, int(ctx[k]), 1000 + k)
+            pos = ctx.astype(np.int32).copy()
+            toks = [int(t) for t in synth.make_prompts(1, B, V, seed=9)[0]]
+            idx = torch.tensor(sample, device="cuda", dtype=torch.long)
+            buf = torch.empty((B, V), dtype=torch.float32, device="cuda")
+            worst = 0.0
+            for step in range(2):
+                ref = m.step_batch(o_lanes, [toks[k] for k in sample])
+                fs.fs_decode_step_batch(h, np.arange(B, dtype=np.int32), pos, toks,
+                                        logits_out=buf)
+                got = buf.index_select(0, idx).cpu().numpy()
+                err, _ = U.compare_logits(got, ref, MAX_ABS, MIN_COS)
+                worst = max(worst, err)
+                U.decisive_token_agreement(got, ref, max(worst, 1e-3))
+                for i, k in enumerate(sample):
+                    toks[k] = int(np.argmax(ref[i]))
+            assert pos.tolist() == [int(c) + 2 for c in ctx]
+            greedy_step_vs_oracle(h, m, o_lanes, sample, toks, B, V, pos, worst)
+            del o_lanes
+        finally:
+            fs.fs_destroy(h)

@@ -193,6 +193,52 @@ def test_sampler_greedy_and_temperature_against_oracle(smol_l2):
         fs.fs_destroy(h)
 
 
+def test_temperature_sampler_equal_outside_rounding_band(smol_l2):
+    """The GPU sampler sums exp(z - max z) in per-thread segments and an
+    ordered scan, the oracle in one ascending pass, each with its own exp: the
+    running sums may differ by rounding. A draw is decided by where
+    target = u * total falls among the running sums, so the two samplers must
+    agree whenever the target lies farther than the rounding band from every
+    running sum. Band: 4 * V * 2^-52 * total (V exp results each within an
+    ulp, plus any order of V additions). 2000 draws over 8 lanes and
+    temperatures 0.3 .. 2.0; every draw outside the band must match, and the
+    count inside it is reported (a draw inside may go either way)."""
+    import torch
+    cfg, Wb, m = smol_l2
+    V = cfg["V"]
+    h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=8)
+    try:
+        n = 8
+        buf = torch.empty((n, V), dtype=torch.float32, device="cuda")
+        toks = synth.make_prompts(1, n, V, seed=16)[0]
+        fs.fs_decode_step_batch(h, list(range(n)), np.zeros(n, np.int32), toks,
+                                logits_out=buf)
+        lg = buf.cpu().numpy().astype(np.float64)
+        temps = np.array([0.3, 0.5, 0.8, 1.0, 1.3, 2.0, 0.7, 1.0], np.float32)
+        seeds = np.arange(n, dtype=np.uint64) * 104729 + 5
+        cums = []
+        for i in range(n):
+            z = lg[i] / np.float64(temps[i])
+            cums.append(np.cumsum(np.exp(z - z.max())))
+        outside = inside = 0
+        for c in range(250):
+            got = fs.fs_sample(h, temps, seeds, np.full(n, c, dtype=np.uint64))
+            for i in range(n):
+                cum = cums[i]
+                total = cum[-1]
+                target = O.uniform(int(seeds[i]), c) * total
+                band = 4.0 * V * 2.0 ** -52 * total
+                if np.min(np.abs(cum - target)) <= band:
+                    inside += 1
+                    continue
+                outside += 1
+                want = O.sample(lg[i].astype(np.float32), float(temps[i]), int(seeds[i]), c)
+                assert got[i] == want, (i, c, got[i], want)
+        assert outside + inside == 2000 and outside >= 1990, inside
+    finally:
+        fs.fs_destroy(h)
+
+
 def test_error_paths_are_atomic(tiny):
     W, m = tiny
     h = U.make_gpu(T, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=4,
@@ -287,6 +333,7 @@ def test_mistral_shape_long_ragged_context_parity(mistral_l2):
             lanes_o.append(ln)
         toks = [11, 222, 3333]
         pos = np.array(ctx, np.int32)
+        lane2_rows, lane2_toks = [], []
         for step in range(3):
             ref = m.step_batch(lanes_o, toks)
             buf = torch.empty((3, cfg["V"]), dtype=torch.float32, device="cuda")
@@ -294,19 +341,31 @@ def test_mistral_shape_long_ragged_context_parity(mistral_l2):
             torch.cuda.synchronize()
             got = buf.cpu().numpy()
             U.compare_logits(got, ref, BF16_MAX_ABS, BF16_MIN_COS)
+            lane2_rows.append(got[2].copy())
+            lane2_toks.append(toks[2])
             toks = [int(np.argmax(r)) for r in ref]
         assert pos.tolist() == [c + 3 for c in ctx]
-        # lane 2 alone reproduces its batched bits: re-seed lane 3 the same way
-        Ks = [synth.bf16_to_f32(synth.bf16_bits(synth.make_kv(2100, Hkv, hd, seed=31,
-                                                              path=(2, l))[0]))
-              for l in range(L)]
-        Vs = [synth.bf16_to_f32(synth.bf16_bits(synth.make_kv(2100, Hkv, hd, seed=31,
-                                                              path=(2, l))[1]))
-              for l in range(L)]
+        # lane 2 alone reproduces its batched bits: lane 3 gets lane 2's
+        # starting cache and replays its three tokens in steps of its own
+        Ks, Vs = [], []
+        for l in range(L):
+            K, V = synth.make_kv(2100, Hkv, hd, seed=31, path=(2, l))
+            Ks.append(synth.bf16_to_f32(synth.bf16_bits(K)))
+            Vs.append(synth.bf16_to_f32(synth.bf16_bits(V)))
         fs.fs_lane_import_kv(h, 3, np.stack(Ks), np.stack(Vs))
-        # replay lane 2's three steps on lane 3, alone
-        k2, v2 = fs.fs_lane_export_kv(h, 2, 0, Hkv, hd)
-        assert k2.shape[0] == 2103
+        p3 = np.array([2100], np.int32)
+        for step in range(3):
+            buf = torch.empty((1, cfg["V"]), dtype=torch.float32, device="cuda")
+            fs.fs_decode_step_batch(h, [3], p3, [lane2_toks[step]], logits_out=buf)
+            torch.cuda.synchronize()
+            alone = buf.cpu().numpy()[0]
+            assert np.array_equal(alone.view(np.uint32), lane2_rows[step].view(np.uint32)), step
+        for l in range(L):  # and the same cache bits
+            k2, v2 = fs.fs_lane_export_kv(h, 2, l, Hkv, hd)
+            k3, v3 = fs.fs_lane_export_kv(h, 3, l, Hkv, hd)
+            assert k2.shape[0] == k3.shape[0] == 2103
+            assert np.array_equal(k2.view(np.uint32), k3.view(np.uint32))
+            assert np.array_equal(v2.view(np.uint32), v3.view(np.uint32))
     finally:
         fs.fs_destroy(h)
 
