@@ -69,7 +69,7 @@ const fs_handle* g_trace_owner = nullptr;
 bool trace_install_all(TraceBuf* b) {
   return trace_install_misc(b) && trace_install_gemm(b) && trace_install_gemv(b) &&
          trace_install_attn(b) && trace_install_attn_mma(b) && trace_install_attn_tma(b) &&
-         trace_install_attn_tiled(b) && trace_install_attn_fused(b);
+         trace_install_attn_tiled(b);
 }
 
 // Uninstalls and frees the trace buffer if h owns it (the stream has been
@@ -87,6 +87,13 @@ int trace_release(const fs_handle* h) {
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
   if (m_tiles >= sms) return m_tiles;
+  // FS_TC_SPLIT_KB=r (a tuning knob, read once): matrices with fewer row
+  // tiles than SMs take ceil(kb_total / r) equal K splits of every tile
+  static const int split_kb = [] {
+    const char* e = getenv("FS_TC_SPLIT_KB");
+    return e ? std::max(0, atoi(e)) : 0;
+  }();
+  if (split_kb > 0) return m_tiles * std::min(kb_total, (kb_total + split_kb - 1) / split_kb);
   // small handles, large matrices: about two blocks per SM, a whole number
   // of splits per row tile so that no block's range crosses a tile
   if (max_lanes <= 8 && T >= (int64_t)8 * sms)
@@ -143,7 +150,6 @@ struct fs_handle {
   float* part_ml = nullptr;
   float* part_acc = nullptr;
   int* attn_counters = nullptr;  // [max_lanes * Hkv], zero between steps
-  bool attn_fused = false;
   bool attn_tiled = false;
   bool attn_mma = false;
   bool attn_tma = false;         // KV tiles by TMA (k_attn_tma.cu)
@@ -370,9 +376,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   h->max_splits = (d.max_pos + h->split_len - 1) / h->split_len;
   h->max_pages_per_lane = (d.max_pos + d.page_size - 1) / d.page_size;
   {
-    const char* env = getenv("FS_GEMM_PATH");
-    const bool force_gemv = env && std::string(env) == "gemv";
-    h->use_tc = (h->wtype == W_BF16 || h->wtype == W_Q8) && d.d_ffn % 64 == 0 && !force_gemv &&
+    h->use_tc = (h->wtype == W_BF16 || h->wtype == W_Q8) && d.d_ffn % 64 == 0 &&
                 tc_available();
     const char* genv = getenv("FS_GRAPHS");
     h->graphs_on = !(genv && std::string(genv) == "0");
@@ -521,20 +525,16 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   FS_CK(h, cudaMemset(h->attn_counters, 0, (size_t)B * d.n_kv_heads * 4));
   FS_CK(h, cudaMemset(h->d_zero_temps, 0, (size_t)B * 4));
   FS_CK(h, cudaMemset(h->d_zero_u64, 0, (size_t)B * 8));
-  h->attn_fused = attn_fused_supports(d.head_dim, h->G);
   {
+    // FS_ATTN=mma (a comparison knob read at create) keeps the cp.async
+    // kernel on long-context handles; the two give the same bits
     const char* e = getenv("FS_ATTN");
-    const bool force_fused = e && std::string(e) == "fused";
-    const bool force_tiled = e && std::string(e) == "tiled";
-    h->attn_tiled = !force_fused && attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
     const bool force_mma = e && std::string(e) == "mma";
-    h->attn_mma = !force_fused && !force_tiled &&
-                  attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len,
+    h->attn_mma = attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len,
                                     h->max_splits);
     // the TMA kernel's producer warp and barrier set-up pay off on long
     // contexts; a handle whose lanes stay short keeps the cp.async kernel
-    // (both give the same bits)
-    h->attn_tma = !force_fused && !force_tiled && !force_mma && d.max_pos > 256 &&
+    h->attn_tma = !force_mma && d.max_pos > 256 &&
                   attn_tma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, d.page_size,
                                     h->split_len, h->max_splits);
     if (h->attn_tma) {
@@ -543,6 +543,13 @@ int create_impl(fs_handle* h, const fs_weights* W) {
           attn_tma_make_map(h->kv.v, rows, d.head_dim, d.page_size, &h->tm_kv_v))
         h->attn_tma = false;  // arena too large for 32-bit rows: the cp.async kernel serves
     }
+    // f32 KV and head dims below 64: the tiled kernel
+    h->attn_tiled = !h->attn_tma && !h->attn_mma &&
+                    attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
+    if (!h->attn_tma && !h->attn_mma && !h->attn_tiled)
+      return h->fail(FS_ERR_ARG,
+                     "no attention kernel for this shape: head_dim must be 16, 32, 64, 128 or "
+                     "256, and page_size 16, 32 or 64 for f32 KV or head_dim < 64");
   }
   FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
   FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
@@ -745,15 +752,13 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     // a chunked step first appends every row's k, v (rows of one lane at
     // consecutive positions see each other's keys); the MMA attention kernels
     // then only read, the other kernels give way to the three-kernel path
-    const bool fused_append = !chunked || h->attn_tma || h->attn_mma || h->attn_tiled ||
-                              h->attn_fused;
-    if (chunked && fused_append)
+    if (chunked)
       h->launch(FS_PROF_OTHER, (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs),
                 [&] {
                   return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
                                             h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
                 });
-    if (fused_append && (h->attn_tma || h->attn_mma || h->attn_tiled)) {
+    {
       AttnParams ap{};
       ap.kv_written = chunked ? 1 : 0;
       ap.qkv = h->qkv; ap.H = d.n_heads; ap.rc = h->rope_cos; ap.rs = h->rope_sin;
@@ -768,27 +773,6 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
                   return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
                                      : launch_attention_tiled(ap, n, h->xtype, s);
                 });
-    } else if (fused_append && h->attn_fused) {
-      h->launch(FS_PROF_ATTN,
-                kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
-                  return launch_attention_fused(h->qkv, n, d.n_heads, h->rope_cos,
-                                                h->rope_sin, args, h->kv, l, h->max_splits,
-                                                h->split_len, h->part_ml, h->part_acc,
-                                                h->attn_counters, h->opanel, h->xtype,
-                                                h->Kp_q, chunked ? 1 : 0, s);
-                });
-    } else {
-      h->launch(FS_PROF_OTHER,
-                (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs), [&] {
-                  return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
-                                            h->rope_cos, h->rope_sin, args, h->kv, l, h->q,
-                                            s);
-                });
-      h->launch(FS_PROF_ATTN, kv_read + (double)n * h->Nq * (4.0 + xs), [&] {
-        return launch_attention(h->q, n, d.n_heads, args, h->kv, l, h->max_splits,
-                                h->split_len, h->part_ml, h->part_acc, h->opanel, h->xtype,
-                                h->Kp_q, s);
-      });
     }
     gemm(W.o, W.o_tc, h->tm_o, h->tm_o64, h->opanel, EPI_STORE, h->y, nullptr, d.d_model,
          d.d_model);
@@ -1394,7 +1378,6 @@ const char* fs_attention_path(const fs_handle* h) {
   if (h->attn_tma) return "tma-mma";
   if (h->attn_mma) return "cp.async-mma";
   if (h->attn_tiled) return "tiled";
-  if (h->attn_fused) return "fused";
   return "three-kernel";
 }
 

@@ -147,7 +147,6 @@ int trace_install_attn(TraceBuf* p);
 int trace_install_attn_mma(TraceBuf* p);
 int trace_install_attn_tma(TraceBuf* p);
 int trace_install_attn_tiled(TraceBuf* p);
-int trace_install_attn_fused(TraceBuf* p);
 
 // Kernel launch with the programmatic-stream-serialization attribute.
 template <typename... K, typename... A>
@@ -326,10 +325,6 @@ int launch_rope_append(const float* qkv, int B, int H, int Hkv, int hd,
                        const float* rope_cos, const float* rope_sin,
                        const StepArgs& args, const KV& kv, int layer,
                        float* q_out, cudaStream_t s);
-int launch_attention(const float* q, int B, int H, const StepArgs& args,
-                     const KV& kv, int layer, int max_splits, int split_len,
-                     float* part_ml, float* part_acc, void* o_panel,
-                     int x_type, int ld_o, cudaStream_t s);
 // Arguments of the tiled attention kernel (k_attn_tiled.cu).
 struct AttnParams {
   const float* qkv;  // [B][(H + 2 Hkv) hd] projection output
@@ -364,13 +359,6 @@ int launch_attention_tma(const CUtensorMap& tmK, const CUtensorMap& tmV, const A
 int launch_attention_mma(const AttnParams& a, int B, int x_type, cudaStream_t s);
 int launch_attention_tiled(const AttnParams& a, int B, int x_type, cudaStream_t s);
 
-// RoPE + KV append + split-K attention (+ ordered merge) in one kernel.
-bool attn_fused_supports(int hd, int G);
-int launch_attention_fused(const float* qkv, int B, int H, const float* rope_cos,
-                           const float* rope_sin, const StepArgs& args, const KV& kv,
-                           int layer, int max_splits, int split_len, float* part_ml,
-                           float* part_acc, int* counters, void* o_panel, int x_type,
-                           int ld_o, int kv_written, cudaStream_t s);
 int launch_sample(const float* logits, int B, int V, const float* temps,
                   const uint64_t* seeds, const uint64_t* counters,
                   int32_t* out, cudaStream_t s);

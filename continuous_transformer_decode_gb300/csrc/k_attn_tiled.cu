@@ -1,7 +1,7 @@
 // Per-lane GQA decode attention over paged KV, streamed through shared memory.
 //
-// Same computation as k_attn_fused (RoPE of q and k at the lane's own
-// position, append of k and v at that position, online-softmax attention of
+// The attention of f32-KV handles and head dims below 64 (RoPE of q and k at
+// the lane's own position, append of k and v at that position, online-softmax attention of
 // the lane's query heads over its own keys 0..pos, split-K with an ordered
 // merge; "MODEL-BATCHING-RESULTS", "The lever"; mlx-bun "Parallel slots",
 // "KV memory" rung 3; "S1b decode: design traps" trap 2), organised for

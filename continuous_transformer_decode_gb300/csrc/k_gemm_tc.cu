@@ -673,10 +673,20 @@ int max_stages() {
   }();
   return v;
 }
+// FS_TC_SMEM_KB (64..224, a tuning knob read once) sets the per-block shared
+// memory budget of the ring (default 112 KB: two blocks per SM).
+int smem_budget() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_SMEM_KB");
+    const int x = e ? atoi(e) : 112;
+    return std::max(64, std::min(224, x)) * 1024;
+  }();
+  return v;
+}
 int tc_stages_for(int n_tot, bool q8, int* stage_bytes, int* smem_bytes) {
   const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128;
   const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 2);
-  const int budget = 112 * 1024 - fixed;
+  const int budget = smem_budget() - fixed;
   const int st = std::max(2, std::min(max_stages(), budget / sb));
   *stage_bytes = sb;
   *smem_bytes = 1024 + st * sb + kXbufBytes + 8 * (3 * st + 2);

@@ -4,8 +4,8 @@ A lane's prompt consumed in chunks, next to other lanes decoding in the same
 steps, must give bit for bit the logits and KV of feeding the same tokens one
 per call (every row's K/V are appended before attention, with the same
 rounding as the one-token path). Covered: the TMA attention (long-context
-handle), the cp.async attention (short-context handle) and the f32 three-
-kernel path; rows of a lane in any order; atomic refusals.
+handle), the cp.async attention (short-context handle) and the tiled
+attention of f32-KV handles; rows of a lane in any order; atomic refusals.
 """
 import numpy as np
 import pytest
@@ -100,7 +100,7 @@ def test_chunked_equals_one_token_steps_cp_async(smol_l2):
     _compare(cfg, W, fs.FS_DTYPE_BF16, fs.FS_DTYPE_BF16, 200, "cp.async-mma")
 
 
-def test_chunked_equals_one_token_steps_f32_three_kernel():
+def test_chunked_equals_one_token_steps_f32_tiled():
     cfg = synth.MODEL_T
     W = synth.make_weights(cfg, seed=1, fmt="f32")
     _compare(cfg, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, 128, None)
