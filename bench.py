@@ -48,10 +48,12 @@ sys.path.insert(0, ROOT)
 WORKLOADS = {
     "smollm2-135m-bf16": dict(model="S", wdtype="bf16", B=256, prompt=16),
     "smollm2-135m-q8_0": dict(model="S", wdtype="q8_0", B=960, prompt=16),
-    "mistral-7b-bf16": dict(model="M", wdtype="bf16", B=128, ctx=(128, 4096)),
+    # split activations: the configuration whose full-depth logits meet the
+    # 5e-2 bound against the oracle (bf16 panels alone drift by ~0.15)
+    "mistral-7b-bf16": dict(model="M", wdtype="bf16", B=128, ctx=(128, 4096), act_split=1),
     # continuous batching through the native scheduler (fill / gather / fold,
     # decode-first, bounded prefill) over a synthetic Poisson job trace
-    "mistral-7b-trace": dict(model="M", wdtype="bf16", B=128, trace=True),
+    "mistral-7b-trace": dict(model="M", wdtype="bf16", B=128, trace=True, act_split=1),
 }
 METRIC = "aggregate decode tokens/s"
 
@@ -209,7 +211,8 @@ def make_handle(cfg, wl, B, extra, W=None):
         W, wdt = gpu_weights(cfg, wl["wdtype"])
     else:
         W, wdt = W
-    desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps)
+    desc = fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, B, n_pages, max_pos, ps,
+                        wl.get("act_split", 0))
     h = fs.fs_create(desc, W)
     del W
     return h, ctx, wdt
@@ -415,6 +418,8 @@ def run_workloads(args, local):
             sr = step_roofline(cfg, wb, B, ctx_mean, peaks)
             tok_s = B / (ms / 1e3)
             out.append({"workload": name, "lanes": B, "ms_per_step": ms, "tok_s": tok_s,
+                        "activations": ("bf16 + bf16 remainder (act_split)"
+                                        if wl.get("act_split") else "bf16"),
                         "context": (f"16-token prompts" if "ctx" not in wl else
                                     f"U[{wl['ctx'][0]},{wl['ctx'][1]}] mean {np.mean(ctx):.0f}"),
                         "step_roofline": dict(sr, frac=tok_s / sr["tok_s_ceiling"]),
@@ -563,7 +568,8 @@ def run_trace(args, wl, ws, rank):
     ps = 16
     n_pages = lanes * ((max_pos + ps - 1) // ps)
     W, wdt = gpu_weights(cfg, wl["wdtype"])
-    h = fs.fs_create(fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, lanes, n_pages, max_pos, ps), W)
+    h = fs.fs_create(fs.make_desc(cfg, wdt, fs.FS_DTYPE_BF16, lanes, n_pages, max_pos, ps,
+                                  wl.get("act_split", 0)), W)
     budget = args.prefill_budget or max(1, lanes // 2)
     chunk = args.prefill_chunk or budget
 

@@ -54,9 +54,13 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = pack_bf16(x0 - hf.x, x1 - hf.y);
 }
-__device__ __forceinline__ void st_out(float* p, float v) { *p = v; }
-__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v) {
-  *p = __float2bfloat16_rn(v);
+// An output element; a bf16 panel with a remainder part (lo > 0) also gets
+// bf16(v - hi) lo elements further on.
+__device__ __forceinline__ void st_out(float* p, float v, int64_t) { *p = v; }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v, int64_t lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *p = h;
+  if (lo > 0) p[lo] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
 }  // namespace attn

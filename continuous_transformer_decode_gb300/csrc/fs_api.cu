@@ -120,8 +120,14 @@ struct fs_handle {
   Mat embed, head;
   TcW head_tc;
   bool use_tc = false;
-  CUtensorMap tm_h, tm_o, tm_a;        // panels, boxes of 16 lanes
-  CUtensorMap tm_h64, tm_o64, tm_a64;  // panels, boxes of 64 lanes
+  // tensor maps of one activation panel (boxes of 16 and 64 lanes) and of
+  // its remainder part (act_split)
+  struct PanelMaps {
+    CUtensorMap m16, m64, lo16, lo64;
+  };
+  PanelMaps pm_h, pm_o, pm_a;
+  int act_split = 0;
+  int64_t lo_h = 0, lo_o = 0, lo_a = 0;  // remainder offsets (elements; 0: none)
   float* ws = nullptr;
   int* counters = nullptr;
   int* err_flag = nullptr;  // mapped pinned host memory
@@ -378,6 +384,11 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   {
     h->use_tc = (h->wtype == W_BF16 || h->wtype == W_Q8) && d.d_ffn % 64 == 0 &&
                 tc_available();
+    if (d.act_split != 0 && d.act_split != 1) return h->fail(FS_ERR_ARG, "act_split must be 0 or 1");
+    if (d.act_split && !h->use_tc)
+      return h->fail(FS_ERR_ARG, "act_split needs the tensor-core path (bf16 or Q8_0 weights, "
+                                 "d_ffn a multiple of 64)");
+    h->act_split = d.act_split;
     const char* genv = getenv("FS_GRAPHS");
     h->graphs_on = !(genv && std::string(genv) == "0");
   }
@@ -504,9 +515,9 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   const size_t xs = h->xtype == X_F32 ? 4 : 2;
   bool ok = h->alloc(&h->x, (size_t)B * d.d_model * 4) == cudaSuccess &&
             h->alloc(&h->y, (size_t)B * d.d_model * 4) == cudaSuccess &&
-            h->alloc(&h->hpanel, (size_t)B * h->Kp_d * xs) == cudaSuccess &&
-            h->alloc(&h->opanel, (size_t)B * h->Kp_q * xs) == cudaSuccess &&
-            h->alloc(&h->apanel, (size_t)B * h->Kp_f * xs) == cudaSuccess &&
+            h->alloc(&h->hpanel, (size_t)(1 + h->act_split) * B * h->Kp_d * xs) == cudaSuccess &&
+            h->alloc(&h->opanel, (size_t)(1 + h->act_split) * B * h->Kp_q * xs) == cudaSuccess &&
+            h->alloc(&h->apanel, (size_t)(1 + h->act_split) * B * h->Kp_f * xs) == cudaSuccess &&
             h->alloc(&h->qkv, (size_t)B * h->Nqkv * 4) == cudaSuccess &&
             h->alloc(&h->q, (size_t)B * h->Nq * 4) == cudaSuccess &&
             h->alloc(&h->logits, (size_t)B * d.vocab * 4) == cudaSuccess &&
@@ -551,9 +562,15 @@ int create_impl(fs_handle* h, const fs_weights* W) {
                      "no attention kernel for this shape: head_dim must be 16, 32, 64, 128 or "
                      "256, and page_size 16, 32 or 64 for f32 KV or head_dim < 64");
   }
-  FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)B * h->Kp_d * xs));
-  FS_CK(h, cudaMemset(h->opanel, 0, (size_t)B * h->Kp_q * xs));
-  FS_CK(h, cudaMemset(h->apanel, 0, (size_t)B * h->Kp_f * xs));
+  FS_CK(h, cudaMemset(h->hpanel, 0, (size_t)(1 + h->act_split) * B * h->Kp_d * xs));
+  FS_CK(h, cudaMemset(h->opanel, 0, (size_t)(1 + h->act_split) * B * h->Kp_q * xs));
+  FS_CK(h, cudaMemset(h->apanel, 0, (size_t)(1 + h->act_split) * B * h->Kp_f * xs));
+  // remainder parts follow their panels (act_split)
+  if (h->act_split) {
+    h->lo_h = (int64_t)B * h->Kp_d;
+    h->lo_o = (int64_t)B * h->Kp_q;
+    h->lo_a = (int64_t)B * h->Kp_f;
+  }
   FS_CK(h, cudaHostAlloc((void**)&h->h_args, (size_t)(7 * B + 1) * 4, cudaHostAllocDefault));
   FS_CK(h, cudaHostAlloc((void**)&h->err_flag, 16, cudaHostAllocMapped));
   *h->err_flag = 0;
@@ -608,12 +625,19 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         h->release((void*)h->head.scales);
       }
     }
-    if (tc_make_map(h->hpanel, B, h->Kp_d, 16, &h->tm_h) ||
-        tc_make_map(h->opanel, B, h->Kp_q, 16, &h->tm_o) ||
-        tc_make_map(h->apanel, B, h->Kp_f, 16, &h->tm_a) ||
-        tc_make_map(h->hpanel, B, h->Kp_d, 64, &h->tm_h64) ||
-        tc_make_map(h->opanel, B, h->Kp_q, 64, &h->tm_o64) ||
-        tc_make_map(h->apanel, B, h->Kp_f, 64, &h->tm_a64))
+    auto maps = [&](void* panel, int Kp, fs_handle::PanelMaps* m) {
+      const __nv_bfloat16* lo = static_cast<const __nv_bfloat16*>(panel) + (int64_t)B * Kp;
+      if (tc_make_map(panel, B, Kp, 16, &m->m16) || tc_make_map(panel, B, Kp, 64, &m->m64))
+        return 1;
+      if (!h->act_split) {
+        m->lo16 = m->m16;
+        m->lo64 = m->m64;
+        return 0;
+      }
+      return tc_make_map(lo, B, Kp, 16, &m->lo16) || tc_make_map(lo, B, Kp, 64, &m->lo64) ? 1 : 0;
+    };
+    if (maps(h->hpanel, h->Kp_d, &h->pm_h) || maps(h->opanel, h->Kp_q, &h->pm_o) ||
+        maps(h->apanel, h->Kp_f, &h->pm_a))
       return h->fail(FS_ERR_CUDA, "panel tensor map");
     const size_t n_counters = (size_t)max_tiles * ((B + 15) / 16);
     if (h->alloc(&h->ws, std::max<size_t>(ws_elems, 1) * 4) != cudaSuccess ||
@@ -708,8 +732,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     return b;
   };
   // algorithmic bytes: weights once, activations in, outputs out
-  auto gemm = [&](const Mat& W, const TcW& T, const CUtensorMap& tmX, const CUtensorMap& tmX64,
-                  const void* X, int epi, float* of, void* ox, int ldo, int n_out) {
+  auto gemm = [&](const Mat& W, const TcW& T, const fs_handle::PanelMaps& pm, const void* X,
+                  int epi, float* of, void* ox, int ldo, int n_out) {
     double bytes = wbytes(W) + (double)n * W.K * xs;
     bytes += epi == EPI_ARGMAX ? (double)n * T.m_tiles * 8.0
              : epi == EPI_SWIGLU ? (double)n * n_out * xs
@@ -730,25 +754,31 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
     p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
     p.am_val = h->am_val; p.am_idx = h->am_idx;
+    p.split = h->act_split;
+    p.lo_off = epi == EPI_SWIGLU ? h->lo_a : 0;
     if (h->wtype == W_Q8)
-      h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc_q8(tmX64, tmX, p, s); });
+      h->launch(FS_PROF_GEMM, bytes, [&] {
+        return launch_gemm_tc_q8(pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
+      });
     else
-      h->launch(FS_PROF_GEMM, bytes, [&] { return launch_gemm_tc(T.tm, tmX64, tmX, p, s); });
+      h->launch(FS_PROF_GEMM, bytes, [&] {
+        return launch_gemm_tc(T.tm, pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
+      });
   };
   const double norm_bytes = (double)n * d.d_model * (4.0 * 3 + xs);
   // embedding gather + the first layer's input norm
   h->launch(FS_PROF_OTHER, (double)n * d.d_model * (4.0 * 2 + xs), [&] {
     return launch_embed(h->embed, args, n, h->kv, h->x, d.d_model, h->layers[0].g_attn,
-                        d.rms_eps, h->hpanel, h->xtype, h->Kp_d, s);
+                        d.rms_eps, h->hpanel, h->xtype, h->Kp_d, h->lo_h, s);
   });
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerW& W = h->layers[l];
     if (l > 0)
       h->launch(FS_PROF_OTHER, norm_bytes, [&] {
         return launch_rmsnorm(h->x, h->y, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel,
-                              h->xtype, h->Kp_d, s);
+                              h->xtype, h->Kp_d, h->lo_h, s);
       });
-    gemm(W.qkv, W.qkv_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
+    gemm(W.qkv, W.qkv_tc, h->pm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
     // a chunked step first appends every row's k, v (rows of one lane at
     // consecutive positions see each other's keys); the MMA attention kernels
     // then only read, the other kernels give way to the three-kernel path
@@ -765,6 +795,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
       ap.args = args; ap.kv = h->kv; ap.layer = l; ap.split_len = h->split_len;
       ap.max_splits = h->max_splits; ap.part_ml = h->part_ml; ap.part_acc = h->part_acc;
       ap.counters = h->attn_counters; ap.o = h->opanel; ap.ld_o = h->Kp_q; ap.err = h->d_err_flag;
+      ap.o_lo = h->lo_o;
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs),
                 [&] {
@@ -774,30 +805,30 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
                                      : launch_attention_tiled(ap, n, h->xtype, s);
                 });
     }
-    gemm(W.o, W.o_tc, h->tm_o, h->tm_o64, h->opanel, EPI_STORE, h->y, nullptr, d.d_model,
+    gemm(W.o, W.o_tc, h->pm_o, h->opanel, EPI_STORE, h->y, nullptr, d.d_model,
          d.d_model);
     h->launch(FS_PROF_OTHER, norm_bytes, [&] {
         return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel,
-                              h->xtype, h->Kp_d, s);
+                              h->xtype, h->Kp_d, h->lo_h, s);
       });
-    gemm(W.gateup, W.gateup_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
+    gemm(W.gateup, W.gateup_tc, h->pm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
          d.d_ffn);
-    gemm(W.down, W.down_tc, h->tm_a, h->tm_a64, h->apanel, EPI_STORE, h->y, nullptr, d.d_model,
+    gemm(W.down, W.down_tc, h->pm_a, h->apanel, EPI_STORE, h->y, nullptr, d.d_model,
          d.d_model);
   }
   h->launch(FS_PROF_OTHER, norm_bytes, [&] {
       return launch_rmsnorm(h->x, h->y, h->g_final, n, d.d_model, d.rms_eps, h->hpanel, h->xtype,
-                            h->Kp_d, s);
+                            h->Kp_d, h->lo_h, s);
     });
   if (greedy && h->greedy_fused) {  // greedy tokens straight from the head's epilogue
-    gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_ARGMAX, nullptr, nullptr,
+    gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_ARGMAX, nullptr, nullptr,
          d.vocab, d.vocab);
     h->launch(FS_PROF_OTHER, (double)n * (h->head_tc.m_tiles * 8.0 + 4.0), [&] {
       return launch_argmax_tiles(h->am_val, h->am_idx, n, h->head_tc.m_tiles, greedy, s);
     });
     return;
   }
-  gemm(h->head, h->head_tc, h->tm_h, h->tm_h64, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
   if (greedy)
     h->launch(FS_PROF_OTHER, (double)n * d.vocab * 4.0, [&] {
       return launch_sample(out, n, d.vocab, h->d_zero_temps, h->d_zero_u64, h->d_zero_u64,
@@ -1437,7 +1468,7 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
     p.tmem_cols = tc_tmem_cols(p.lg);
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
-    launch_gemm_tc(tw, tx64, tx, p, s);
+    launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
     if (reps > 0 && ms_out) {
       // each launch between two events, after a 256 MiB memset that evicts
       // the operands from L2 and keeps the GPU busy (clocks up)
@@ -1449,7 +1480,7 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
         for (int r = 0; r < reps; ++r) {
           cudaMemsetAsync(flush, r & 0xff, flush_bytes, s);
           cudaEventRecord(ev[2 * r], s);
-          launch_gemm_tc(tw, tx64, tx, p, s);
+          launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
           cudaEventRecord(ev[2 * r + 1], s);
         }
         double sum = 0.0;

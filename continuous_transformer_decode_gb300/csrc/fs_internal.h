@@ -268,6 +268,10 @@ struct TcParams {
   const __half* q8_scales;
   float* am_val;   // EPI_ARGMAX: [lanes_total][m_tiles] tile maxima
   int* am_idx;     //             and their row indices
+  // 1: the panel has a remainder part (map tmX*lo): two MMAs per k-step,
+  // W x hi then W x lo, into the one accumulator
+  int split;
+  int64_t lo_off;  // EPI_SWIGLU with split: remainders at out_x + lo_off
 };
 // Per lane, the argmax over the tiles' (max, index) pairs of an EPI_ARGMAX
 // launch (lowest index on ties): tokens_out[b] for b < B.
@@ -304,11 +308,15 @@ inline int tc_tmem_cols(int lg) {
 bool tc_available();
 int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
 // tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.
+// tmX64lo / tmX16lo: the same boxes of the remainder panel (p.split = 1;
+// ignored otherwise).
 int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                   const TcParams& p, cudaStream_t s);
+                   const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
+                   cudaStream_t s);
 // Same GEMM over Q8_0 tiles (p.q8_codes / p.q8_scales), dequantised to bf16
 // in shared memory inside the kernel.
-int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const TcParams& p,
+int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                      const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                       cudaStream_t s);
 // Row-major Q8_0 codes [N][Kp] / scales [N][Kp/32] -> the tiled layout above
 // (rows beyond N are zero).
@@ -316,11 +324,15 @@ int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int
                    __half* scales_t, cudaStream_t s);
 
 // x = E[tok]; if g is given also h = RMSNorm(x) * g (x_type panel).
+// lo_off (elements, bf16 panels only; 0: none): the row's rounding
+// remainders bf16(v - hi) are stored lo_off elements after its bf16 values.
 int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-                 const float* g, float eps, void* h, int x_type, int ld_h, cudaStream_t s);
-// x += resid (if resid is given), out = RMSNorm(x) * g.
+                 const float* g, float eps, void* h, int x_type, int ld_h, int64_t lo_off,
+                 cudaStream_t s);
+// x += resid (if resid is given), out = RMSNorm(x) * g (and its remainders
+// at out + lo_off when lo_off > 0).
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
-                   void* out, int x_type, int ld_out, cudaStream_t s);
+                   void* out, int x_type, int ld_out, int64_t lo_off, cudaStream_t s);
 int launch_rope_append(const float* qkv, int B, int H, int Hkv, int hd,
                        const float* rope_cos, const float* rope_sin,
                        const StepArgs& args, const KV& kv, int layer,
@@ -340,6 +352,7 @@ struct AttnParams {
   int* counters;     // [B][Hkv]
   void* o;           // output panel
   int ld_o;
+  int64_t o_lo;      // bf16 panel: remainders bf16(v - hi) at o + o_lo (0: none)
   int* err;          // device-visible error flag
   // 0: the block holding a row's position rotates k and appends k, v there;
   // 1: every row's k, v were appended by a preceding kernel of the step (rows

@@ -99,7 +99,7 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
   p.ws = ws;
   p.counters = counters;
   p.err = err;
-  launch_gemm_tc(tw, tx64, tx, p, s);
+  launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
     return FS_ERR_CUDA;
   int herr = 0;

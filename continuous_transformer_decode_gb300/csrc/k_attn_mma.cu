@@ -291,7 +291,7 @@ __device__ __forceinline__ void attn_mma_body(const AttnParams& a, unsigned long
       A = fmaf(wo[(w * kG + h) * HD + d], sc, A);
     }
     if (ns == 1) {
-      st_out(orow + o, A / L);
+      st_out(orow + o, A / L, a.o_lo);
     } else {
       if (d == 0) {
         a.part_ml[2 * (base + h)] = M;
@@ -353,7 +353,7 @@ __device__ __forceinline__ void attn_mma_body(const AttnParams& a, unsigned long
       A = fmaf(a3, sm[(q + 3) * kG + h], A);
     }
     for (; q < ns; ++q) A = fmaf(__ldcg(src + q * qstride), sm[q * kG + h], A);
-    st_out(orow + o, A / sL[h]);
+    st_out(orow + o, A / sL[h], a.o_lo);
   }
 }
 

@@ -95,9 +95,13 @@ struct Elem<__nv_bfloat16> {
   __device__ static void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
-__device__ __forceinline__ void st_out(float* p, float v) { *p = v; }
-__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v) {
-  *p = __float2bfloat16_rn(v);
+// An output element; a bf16 panel with a remainder part (lo > 0) also gets
+// bf16(v - hi) lo elements further on.
+__device__ __forceinline__ void st_out(float* p, float v, int64_t) { *p = v; }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, float v, int64_t lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *p = h;
+  if (lo > 0) p[lo] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
 template <typename KVT, typename OT, int HD>
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
 #pragma unroll
     for (int j = 0; j < kOut; ++j) {
       const int o = tid + j * kT;
-      if (o < G * HD) st_out(orow + o, acc[j] / s_l[o / HD]);
+      if (o < G * HD) st_out(orow + o, acc[j] / s_l[o / HD], a.o_lo);
     }
     return;
   }
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kT) k_attn_tiled(AttnParams a) {
         L = fmaf(__ldcg(a.part_ml + 2 * bq + 1), w, L);
         A = fmaf(__ldcg(a.part_acc + bq * HD + (o - h * HD)), w, A);
       }
-      st_out(orow + o, A / L);
+      st_out(orow + o, A / L, a.o_lo);
     }
   }
 }

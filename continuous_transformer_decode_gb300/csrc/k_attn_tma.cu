@@ -338,7 +338,7 @@ __device__ __forceinline__ void attn_tma_body(const CUtensorMap& tmK, const CUte
       A = fmaf(wo[(w * kG + h) * HD + d], sc, A);
     }
     if (ns == 1) {
-      st_out(orow + o, A / L);
+      st_out(orow + o, A / L, a.o_lo);
     } else {
       if (d == 0) {
         a.part_ml[2 * (base + h)] = M;
@@ -429,7 +429,7 @@ __device__ __forceinline__ void attn_tma_body(const CUtensorMap& tmK, const CUte
 #pragma unroll
   for (int j = 0; j < kOut; ++j) {
     const int o = tid + j * kT;
-    if (o < gh) st_out(orow + o, acc[j] / sL[o / HD]);
+    if (o < gh) st_out(orow + o, acc[j] / sL[o / HD], a.o_lo);
   }
 }
 

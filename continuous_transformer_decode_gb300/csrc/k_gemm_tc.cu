@@ -171,8 +171,10 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
           const int b = c0 + j;
           if (b < lanes) {
             const float a = silu(v[j]) * xbuf[row_local * 17 + j];
-            static_cast<__nv_bfloat16*>(p.out_x)[(int64_t)(lane0 + b) * p.ldo + f] =
-                __float2bfloat16_rn(a);
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + b) * p.ldo + f;
+            const __nv_bfloat16 ah = __float2bfloat16_rn(a);
+            *o = ah;
+            if (p.lo_off > 0) o[p.lo_off] = __float2bfloat16_rn(a - __bfloat162float(ah));
           }
         }
       }
@@ -285,15 +287,23 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp,
       for (int k = 0; k < 2; ++k) {
         const int b = b0 + 8 * k;
         if (b >= lanes) break;
-        __nv_bfloat162 lo =
-            __floats2bfloat162_rn(silu(g[k].x) * u[k].x, silu(g[k].y) * u[k].y);
-        __nv_bfloat162 hi =
-            __floats2bfloat162_rn(silu(g[k].z) * u[k].z, silu(g[k].w) * u[k].w);
+        const float a0 = silu(g[k].x) * u[k].x, a1 = silu(g[k].y) * u[k].y;
+        const float a2 = silu(g[k].z) * u[k].z, a3 = silu(g[k].w) * u[k].w;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a0, a1);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a2, a3);
         uint2 pk;
         pk.x = *reinterpret_cast<uint32_t*>(&lo);
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_x) +
-                                  (int64_t)(lane0 + b) * p.ldo + f0) = pk;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + b) * p.ldo + f0;
+        *reinterpret_cast<uint2*>(o) = pk;
+        if (p.lo_off > 0) {
+          const float2 fl = __bfloat1622float2(lo), fh = __bfloat1622float2(hi);
+          __nv_bfloat162 rl = __floats2bfloat162_rn(a0 - fl.x, a1 - fl.y);
+          __nv_bfloat162 rh = __floats2bfloat162_rn(a2 - fh.x, a3 - fh.y);
+          pk.x = *reinterpret_cast<uint32_t*>(&rl);
+          pk.y = *reinterpret_cast<uint32_t*>(&rh);
+          *reinterpret_cast<uint2*>(o + p.lo_off) = pk;
+        }
       }
     }
     return;
@@ -355,7 +365,9 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
 template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
-              const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
+              const __grid_constant__ CUtensorMap tmX16,
+              const __grid_constant__ CUtensorMap tmX64lo,
+              const __grid_constant__ CUtensorMap tmX16lo, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -391,6 +403,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmX64);
     prefetch_tensormap(&tmX16);
+    if (p.split) {
+      prefetch_tensormap(&tmX64lo);
+      prefetch_tensormap(&tmX16lo);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -426,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int npw = p.prod_warps;  // divides S
   const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
   const int nb64 = n_tot / 64;
-  const int nbox = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // panel boxes per stage
+  const int nbox1 = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // boxes of one panel part
+  const int nbox = nbox1 * (p.split ? 2 : 1);                 // panel boxes per stage
+  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (p.split ? 2 : 1);
   // warp-collective: iterations first, first + step, ...
   auto produce = [&](int first, int step) {
     int issued = -1;  // last iteration issued
@@ -435,14 +453,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       const int g = g0 + i;  // = m_tile * kb_total + kb
       if (kQ8) {
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales + n_tot * 128));
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales) + x_bytes);
         bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
                   full0 + 8 * s);
         bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + (int64_t)g * (kQ8Scales / 2),
                   kQ8Scales, full0 + 8 * s);
       } else {
         const int tile = g / kbt;
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kWTileBytes + n_tot * 128));
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)kWTileBytes + x_bytes);
         tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
       }
     };
@@ -450,9 +468,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       const int x = ((g0 + i) % kbt) * kBK;
-      const int r = b < nb64 ? b * 64 : nb64 * 64 + (b - nb64) * kXBoxRows;
-      tma_load_2d(st + kXOff + r * 128, b < nb64 ? &tmX64 : &tmX16, x, lane0 + r,
-                  full0 + 8 * s);
+      const int part = b >= nbox1 ? 1 : 0;  // 1: the remainder panel
+      const int bb = b - part * nbox1;
+      const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
+      const CUtensorMap* m = part ? (bb < nb64 ? &tmX64lo : &tmX16lo)
+                                  : (bb < nb64 ? &tmX64 : &tmX16);
+      tma_load_2d(st + kXOff + part * n_tot * 128 + r * 128, m, x, lane0 + r, full0 + 8 * s);
     };
     // Programmatic dependent launch: the weight tiles do not depend on the
     // predecessor kernel, so they start before waiting for it; the panel is
@@ -529,10 +550,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
           const uint32_t b0 = a0 + kXOff;
+          const uint32_t b1 = b0 + (uint32_t)n_tot * 128;  // remainder panel
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
+          for (int kk = 0; kk < kBK / 16; ++kk) {
             mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (acc || kk > 0) ? 1u : 0u);
+            if (p.split) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+          }
           acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
         }
@@ -683,8 +707,8 @@ int smem_budget() {
   }();
   return v;
 }
-int tc_stages_for(int n_tot, bool q8, int* stage_bytes, int* smem_bytes) {
-  const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128;
+int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_bytes) {
+  const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128 * (split ? 2 : 1);
   const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 2);
   const int budget = smem_budget() - fixed;
   const int st = std::max(2, std::min(max_stages(), budget / sb));
@@ -695,7 +719,8 @@ int tc_stages_for(int n_tot, bool q8, int* stage_bytes, int* smem_bytes) {
 
 template <bool kQ8>
 int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                const TcParams& p0, cudaStream_t s) {
+                const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p0,
+                cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(k_gemm_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -706,7 +731,7 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
   TcParams p = p0;
   int smem = 0;
   const int grid = p.P * p.groups;
-  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, &p.stage_bytes, &smem);
+  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, p.split, &p.stage_bytes, &smem);
   // producer warps of single-piece blocks: up to 4, dividing the stage count
   p.prod_warps = 1;
   if (!kQ8) {
@@ -716,7 +741,7 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
       smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 2);
     }
   }
-  launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
+  launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
   return 1;
 }
 
@@ -748,13 +773,16 @@ __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __rest
 }  // namespace
 
 int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                   const TcParams& p, cudaStream_t s) {
-  return launch_impl<false>(tmW, tmX64, tmX16, p, s);
+                   const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
+                   cudaStream_t s) {
+  return launch_impl<false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
-int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16, const TcParams& p,
+int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
+                      const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                       cudaStream_t s) {
-  return launch_impl<true>(tmX64, tmX64, tmX16, p, s);  // the W map is unused
+  // the W map is unused
+  return launch_impl<true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
 namespace {

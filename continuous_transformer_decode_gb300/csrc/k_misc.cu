@@ -26,7 +26,7 @@ __device__ __forceinline__ float load_w(const Mat& E, int64_t row, int i) {
 template <typename OT, int MV>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_embed(Mat E, StepArgs args, KV kv, float* __restrict__ x, int d, const float* g,
-            float eps, OT* __restrict__ h, int ld_h) {
+            float eps, OT* __restrict__ h, int ld_h, int64_t lo_off) {
   TraceMark tr;
   tr.begin(g_trace);
   pdl_wait();
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kNormRowThreads)
     v.w = load_w(E, tok, 4 * c + 3);
     *reinterpret_cast<float4*>(xr + 4 * c) = v;
   }
-  if (g) norm_row_128<OT, MV>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red);
+  if (g) norm_row_128<OT, MV>(xr, nullptr, g, d, eps, h + (int64_t)b * ld_h, t, 1, red, lo_off);
   tr.end(TR_EMBED);
 }
 
@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kNormRowThreads)
 template <typename OT, int MV>
 __global__ void __launch_bounds__(kNormRowThreads)
     k_rmsnorm(float* __restrict__ x, const float* __restrict__ r,
-              const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out) {
+              const float* __restrict__ g, int d, float eps, OT* __restrict__ out, int ld_out,
+              int64_t lo_off) {
   TraceMark tr;
   tr.begin(g_trace);
   __shared__ float red[4];
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kNormRowThreads)
   tr.ready();
   pdl_trigger();
   n.template finish<OT>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, d, eps,
-               out + (int64_t)b * ld_out, threadIdx.x, 1, red);
+               out + (int64_t)b * ld_out, threadIdx.x, 1, red, lo_off);
   tr.end(TR_RMSNORM);
 }
 
@@ -352,57 +353,58 @@ int norm_chunks(int d) {
 
 template <typename OT, int MV>
 void embed_mv(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-              const float* g, float eps, void* h, int ld_h, cudaStream_t s) {
+              const float* g, float eps, void* h, int ld_h, int64_t lo, cudaStream_t s) {
   launch_k(k_embed<OT, MV>, B, kNormRowThreads, 0, s, E, args, kv, x, d, g, eps,
-           static_cast<OT*>(h), ld_h);
+           static_cast<OT*>(h), ld_h, lo);
 }
 
 template <typename OT>
 void embed_ot(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-              const float* g, float eps, void* h, int ld_h, cudaStream_t s) {
+              const float* g, float eps, void* h, int ld_h, int64_t lo, cudaStream_t s) {
   switch (norm_chunks(d)) {
-    case 2: embed_mv<OT, 2>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
-    case 4: embed_mv<OT, 4>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
-    case 8: embed_mv<OT, 8>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
-    default: embed_mv<OT, 16>(E, args, B, kv, x, d, g, eps, h, ld_h, s); break;
+    case 2: embed_mv<OT, 2>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
+    case 4: embed_mv<OT, 4>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
+    case 8: embed_mv<OT, 8>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
+    default: embed_mv<OT, 16>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
   }
 }
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-                 const float* g, float eps, void* h, int x_type, int ld_h, cudaStream_t s) {
+                 const float* g, float eps, void* h, int x_type, int ld_h, int64_t lo_off,
+                 cudaStream_t s) {
   if (B <= 0) return 0;
   if (x_type == X_BF16)
-    embed_ot<__nv_bfloat16>(E, args, B, kv, x, d, g, eps, h, ld_h, s);
+    embed_ot<__nv_bfloat16>(E, args, B, kv, x, d, g, eps, h, ld_h, lo_off, s);
   else
-    embed_ot<float>(E, args, B, kv, x, d, g, eps, h, ld_h, s);
+    embed_ot<float>(E, args, B, kv, x, d, g, eps, h, ld_h, 0, s);
   return 1;
 }
 
 template <typename OT, int MV>
 void rmsnorm_mv(float* x, const float* resid, const float* g, int B, int d, float eps, void* out,
-                int ld_out, cudaStream_t s) {
+                int ld_out, int64_t lo, cudaStream_t s) {
   launch_k(k_rmsnorm<OT, MV>, B, kNormRowThreads, 0, s, x, resid, g, d, eps,
-           static_cast<OT*>(out), ld_out);
+           static_cast<OT*>(out), ld_out, lo);
 }
 
 template <typename OT>
 void rmsnorm_ot(float* x, const float* resid, const float* g, int B, int d, float eps, void* out,
-                int ld_out, cudaStream_t s) {
+                int ld_out, int64_t lo, cudaStream_t s) {
   switch (norm_chunks(d)) {
-    case 2: rmsnorm_mv<OT, 2>(x, resid, g, B, d, eps, out, ld_out, s); break;
-    case 4: rmsnorm_mv<OT, 4>(x, resid, g, B, d, eps, out, ld_out, s); break;
-    case 8: rmsnorm_mv<OT, 8>(x, resid, g, B, d, eps, out, ld_out, s); break;
-    default: rmsnorm_mv<OT, 16>(x, resid, g, B, d, eps, out, ld_out, s); break;
+    case 2: rmsnorm_mv<OT, 2>(x, resid, g, B, d, eps, out, ld_out, lo, s); break;
+    case 4: rmsnorm_mv<OT, 4>(x, resid, g, B, d, eps, out, ld_out, lo, s); break;
+    case 8: rmsnorm_mv<OT, 8>(x, resid, g, B, d, eps, out, ld_out, lo, s); break;
+    default: rmsnorm_mv<OT, 16>(x, resid, g, B, d, eps, out, ld_out, lo, s); break;
   }
 }
 
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,
-                   void* out, int x_type, int ld_out, cudaStream_t s) {
+                   void* out, int x_type, int ld_out, int64_t lo_off, cudaStream_t s) {
   if (B <= 0) return 0;
   if (x_type == X_BF16)
-    rmsnorm_ot<__nv_bfloat16>(x, resid, g, B, d, eps, out, ld_out, s);
+    rmsnorm_ot<__nv_bfloat16>(x, resid, g, B, d, eps, out, ld_out, lo_off, s);
   else
-    rmsnorm_ot<float>(x, resid, g, B, d, eps, out, ld_out, s);
+    rmsnorm_ot<float>(x, resid, g, B, d, eps, out, ld_out, 0, s);
   return 1;
 }
 

@@ -40,9 +40,12 @@ struct NormRow {
   }
   // `bar` is a named barrier id used by exactly the 128 participating
   // threads; `red` is 4 floats of shared memory.
+  // lo_off > 0 (bf16 out only): the remainders bf16(v - hi) go to
+  // out + lo_off.
   template <typename OT>
   __device__ __forceinline__ void finish(float* __restrict__ x, const float* y, int d, float eps,
-                                         OT* __restrict__ out, int t, int bar, float* red) {
+                                         OT* __restrict__ out, int t, int bar, float* red,
+                                         int64_t lo_off = 0) {
     const int nvec = d >> 2;
     if (y) {
 #pragma unroll
@@ -87,6 +90,14 @@ struct NormRow {
           pk.x = *reinterpret_cast<const uint32_t*>(&lo);
           pk.y = *reinterpret_cast<const uint32_t*>(&hi);
           *reinterpret_cast<uint2*>(out + 4 * c) = pk;
+          if (lo_off > 0) {
+            const float2 fl = __bfloat1622float2(lo), fh = __bfloat1622float2(hi);
+            const __nv_bfloat162 rl = __floats2bfloat162_rn(o0 - fl.x, o1 - fl.y);
+            const __nv_bfloat162 rh = __floats2bfloat162_rn(o2 - fh.x, o3 - fh.y);
+            pk.x = *reinterpret_cast<const uint32_t*>(&rl);
+            pk.y = *reinterpret_cast<const uint32_t*>(&rh);
+            *reinterpret_cast<uint2*>(out + lo_off + 4 * c) = pk;
+          }
         } else {
           *reinterpret_cast<float4*>(out + 4 * c) = make_float4(o0, o1, o2, o3);
         }
@@ -99,10 +110,11 @@ struct NormRow {
 template <typename OT, int MaxVec>
 __device__ __forceinline__ void norm_row_128(float* __restrict__ x, const float* y,
                                              const float* __restrict__ g, int d, float eps,
-                                             OT* __restrict__ out, int t, int bar, float* red) {
+                                             OT* __restrict__ out, int t, int bar, float* red,
+                                             int64_t lo_off = 0) {
   NormRow<MaxVec> n;
   n.load(x, g, d, t);
-  n.template finish<OT>(x, y, d, eps, out, t, bar, red);
+  n.template finish<OT>(x, y, d, eps, out, t, bar, red, lo_off);
 }
 
 }  // namespace fsk

@@ -39,7 +39,8 @@ class fs_model_desc(C.Structure):
                 ("rope_theta", C.c_double), ("tied_embeddings", C.c_int32),
                 ("weight_dtype", C.c_int32), ("kv_dtype", C.c_int32),
                 ("max_lanes", C.c_int32), ("page_size", C.c_int32),
-                ("n_pages", C.c_int32), ("max_pos", C.c_int32)]
+                ("n_pages", C.c_int32), ("max_pos", C.c_int32),
+                ("act_split", C.c_int32)]
 
 
 class fs_layer_weights(C.Structure):
@@ -197,11 +198,12 @@ def _dptr(x):
 
 
 def make_desc(cfg: dict, weight_dtype: int, kv_dtype: int, max_lanes: int,
-              n_pages: int, max_pos: int, page_size: int = 16) -> fs_model_desc:
+              n_pages: int, max_pos: int, page_size: int = 16,
+              act_split: int = 0) -> fs_model_desc:
     return fs_model_desc(cfg["L"], cfg["d"], cfg["H"], cfg["Hkv"], cfg["hd"],
                          cfg["F"], cfg["V"], cfg["rms_eps"], cfg["rope_theta"],
                          1 if cfg["tied"] else 0, weight_dtype, kv_dtype,
-                         max_lanes, page_size, n_pages, max_pos)
+                         max_lanes, page_size, n_pages, max_pos, act_split)
 
 
 LAYER_KEYS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down",

@@ -86,6 +86,15 @@ typedef struct fs_model_desc {
   int32_t page_size;       /* tokens per KV page (e.g. 16)                   */
   int32_t n_pages;         /* pages in the shared arena                      */
   int32_t max_pos;         /* tokens a lane may hold                         */
+  int32_t act_split;       /* 0: the bf16 activation panels (normed x,
+                              attention output, SwiGLU product) feed the
+                              tensor-core GEMMs as they are; 1: each panel
+                              also carries its rounding remainder
+                              lo = bf16(v - hi), and every tcgen05 GEMM
+                              multiplies W by hi and by lo into one f32
+                              accumulator (two MMAs per k-step), which keeps
+                              the products near f32 accuracy at depth (bf16
+                              and Q8_0 weights only)                         */
 } fs_model_desc;
 
 /* Per-layer weights in Hugging Face layout W[out, in], row-major, in

@@ -22,11 +22,11 @@ def quantize_weights(W: dict) -> dict:
 
 
 def make_gpu(cfg, W, wdtype, kvdtype=fs.FS_DTYPE_BF16, max_lanes=8,
-             max_pos=64, n_pages=None, page_size=16):
+             max_pos=64, n_pages=None, page_size=16, act_split=0):
     if n_pages is None:
         n_pages = max_lanes * (-(-max_pos // page_size))
     desc = fs.make_desc(cfg, wdtype, kvdtype, max_lanes, n_pages, max_pos,
-                        page_size)
+                        page_size, act_split)
     return fs.fs_create(desc, W)
 
 

@@ -287,7 +287,13 @@ def test_mistral_full_depth_b1_and_128_lane_handles():
     """All 32 layers of the Mistral-7B shape: a 1-lane handle (context 2500)
     and a 128-lane handle whose other lanes hold ragged random contexts
     U[128, 4096], with two sampled lanes (contexts 3001 and 640) followed by
-    the oracle; two teacher-forced steps, then a fused-greedy step."""
+    the oracle; two teacher-forced steps, then a fused-greedy step.
+
+    The handles carry split activations (act_split = 1): at this depth and
+    width, rounding the activation panels to bf16 alone moves the logits by
+    up to ~0.15 (an f32 emulation of the same model with only that rounding
+    gives max-abs 0.147, cosine 0.99969), beyond the 5e-2 bound; with the
+    remainders multiplied too the same emulation gives 0.005."""
     import torch
     if _mem_available_gb() < 80:
         pytest.skip("needs about 80 GB of host memory for the f32 7B oracle")
@@ -303,7 +309,7 @@ def test_mistral_full_depth_b1_and_128_lane_handles():
         max_pos = int(ctx.max()) + 8
         n_pages = int(sum(-(-(int(c) + 8) // 16) for c in ctx)) + B
         h = U.make_gpu(cfg, Wb, fs.FS_DTYPE_BF16, max_lanes=B, max_pos=max_pos,
-                       n_pages=n_pages)
+                       n_pages=n_pages, act_split=1)
         try:
             o_lanes, sample = [], sorted(sampled)
             for k in range(B):

@@ -122,6 +122,44 @@ def test_smollm2_bf16_batch_invariance(smol_l2):
         fs.fs_destroy(h)
 
 
+@pytest.mark.parametrize("wdt", [fs.FS_DTYPE_BF16, fs.FS_DTYPE_Q8_0])
+def test_split_activations_tighten_parity_and_keep_batch_invariance(smol_l2, wdt):
+    """act_split = 1: every activation panel carries its bf16 rounding
+    remainder and the GEMMs multiply both parts, so the logits come within
+    a tenth of the bf16 bound of the oracle (both Q8_0 sides use the same
+    quantised weights); a lane's bits still do not depend on the batch."""
+    cfg, Wb, m = smol_l2
+    W = Wb if wdt == fs.FS_DTYPE_BF16 else U.quantize_weights(Wb)
+    mo = m if wdt == fs.FS_DTYPE_BF16 else O.Model(cfg, W, O.Q8_0)
+    prompts = synth.make_prompts(4, [16, 5, 9, 12], cfg["V"], seed=61)
+    seqs, ref = U.oracle_runs(mo, prompts, 6)
+    errs = {}
+    for split in (0, 1):
+        h = U.make_gpu(cfg, W, wdt, max_lanes=40, act_split=split)
+        try:
+            got = U.gpu_teacher_forced(h, cfg, [0, 7, 20, 39], seqs, cfg["V"])
+            errs[split] = max(U.compare_logits(got[b], ref[b], BF16_MAX_ABS, BF16_MIN_COS)[0]
+                              for b in range(4))
+            if split:
+                for b in range(4):
+                    U.compare_logits(got[b], ref[b], BF16_MAX_ABS / 10, 0.99999)
+                # batch invariance with split panels: lane 7's rows alone
+                for k in range(40):
+                    fs.fs_lane_reset(h, k)
+                alone = U.gpu_teacher_forced(h, cfg, [3], [seqs[1]], cfg["V"])[0]
+                assert np.array_equal(alone.view(np.uint32), got[1].view(np.uint32))
+        finally:
+            fs.fs_destroy(h)
+    assert errs[1] < errs[0] / 4, errs
+
+
+def test_act_split_needs_the_tensor_core_path(tiny):
+    W, m = tiny
+    with pytest.raises(fs.FsError) as e:
+        U.make_gpu(T, W, fs.FS_DTYPE_F32, fs.FS_DTYPE_F32, max_lanes=4, act_split=1)
+    assert e.value.name == "FS_ERR_ARG"
+
+
 def test_smollm2_q8_parity_and_gate(smol_l2):
     cfg, Wb, m_f32 = smol_l2
     Wq = U.quantize_weights(Wb)
