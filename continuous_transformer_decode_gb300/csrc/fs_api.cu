@@ -100,7 +100,12 @@ int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
     return m_tiles * std::max(1, std::min(kb_total, 2 * sms / m_tiles));
   const bool narrow = max_lanes <= 32;
   int s = narrow ? (13 * sms + 5 * m_tiles) / (10 * m_tiles) : (85 * sms) / (100 * m_tiles);
-  s = std::min(s, std::min(8, kb_total / (narrow ? 8 : 32)));
+  // short K (fewer than 32 k-blocks, e.g. a 576- or 1536-wide input): splits
+  // of at least 3 k-blocks, whose partial tiles sum inside a thread-block
+  // cluster; longer K: the splits the workspace reduction was timed with
+  const int cap = kb_total < 32 && tc_cluster_reduce() ? kb_total / 3
+                                                       : kb_total / (narrow ? 8 : 32);
+  s = std::min(s, std::min(8, cap));
   return m_tiles * std::max(1, s);
 }
 }  // namespace
@@ -1438,7 +1443,7 @@ int fs_device_error(fs_handle* h, int32_t* code_out) {
 namespace {
 // tcgen05 GEMM of the test hooks with stream-K width P and its own workspace.
 int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, float* Y, int P,
-                 int reps, double* ms_out, cudaStream_t s) {
+                 int reps, double* ms_out, cudaStream_t s, int cs_off = 0) {
   using namespace fsk;
   CUtensorMap tw, tx, tx64;
   if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
@@ -1468,6 +1473,7 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
     p.tmem_cols = tc_tmem_cols(p.lg);
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
+    p.cs_off = cs_off;
     launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
     if (reps > 0 && ms_out) {
       // each launch between two events, after a 256 MiB memset that evicts
@@ -1515,7 +1521,7 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
                  float* Y, int32_t splits, int32_t path, void* stream) {
   using namespace fsk;
   if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
-      splits > K / 64 || splits > 8 || (path != 0 && path != 1))
+      splits > K / 64 || splits > 8 || path < 0 || path > 2)
     return FS_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == 0) {
@@ -1530,7 +1536,8 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
   }
   // stream-K width m_tiles * splits: every block's range is the K split of
   // one tile, so the pieces are exactly the `splits` K splits
-  return gemm_tc_hook(W, N, K, X, B, Y, ((N + 127) / 128) * splits, 0, nullptr, s);
+  return gemm_tc_hook(W, N, K, X, B, Y, ((N + 127) / 128) * splits, 0, nullptr, s,
+                      path == 2 ? 1 : 0);
 }
 
 int fs_gemm_bf16_width(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,

@@ -164,6 +164,27 @@ inline cudaError_t launch_k(void (*kern)(K...), dim3 grid, dim3 block, size_t sm
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<K>(args)...);
 }
+// The same with thread-block clusters of cluster_x blocks along x (grid.x a
+// multiple of cluster_x).
+template <typename... K, typename... A>
+inline cudaError_t launch_k_cluster(void (*kern)(K...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, int cluster_x, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<K>(args)...);
+}
 
 enum WType { W_F32 = 0, W_BF16 = 1, W_Q8 = 2 };
 enum XType { X_F32 = 0, X_BF16 = 1 };
@@ -272,6 +293,13 @@ struct TcParams {
   // W x hi then W x lo, into the one accumulator
   int split;
   int64_t lo_off;  // EPI_SWIGLU with split: remainders at out_x + lo_off
+  // cluster reduction (set by the launcher): 0, or the number of K splits
+  // of every row tile (P = m_tiles * cs, 2 <= cs <= 8) when the splits of
+  // one (row tile, lane group) run as one thread-block cluster and sum their
+  // partial tiles through distributed shared memory, in split order (the
+  // order of the workspace reduction, so the bits are the same)
+  int cs;
+  int cs_off;      // 1: never the cluster reduction (the caller's workspace serves)
 };
 // Per lane, the argmax over the tiles' (max, index) pairs of an EPI_ARGMAX
 // launch (lowest index on ties): tokens_out[b] for b < B.
@@ -306,6 +334,10 @@ inline int tc_tmem_cols(int lg) {
   return c;
 }
 bool tc_available();
+// K splits of a row tile may sum through a thread-block cluster (see
+// TcParams::cs); FS_TC_CLUSTER=0, a comparison knob read once, keeps the
+// workspace reduction everywhere.
+bool tc_cluster_reduce();
 int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
 // tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.
 // tmX64lo / tmX16lo: the same boxes of the remainder panel (p.split = 1;

@@ -99,6 +99,7 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
   p.ws = ws;
   p.counters = counters;
   p.err = err;
+  p.cs_off = 1;  // K splits sum through the static workspace
   launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
     return FS_ERR_CUDA;

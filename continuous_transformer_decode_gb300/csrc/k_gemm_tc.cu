@@ -118,6 +118,31 @@ __device__ __forceinline__ void tmem_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Thread-block cluster barrier (every thread of every block of the cluster
+// arrives; release / acquire order shared-memory accesses across blocks).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Stream-K bookkeeping. The T = m_tiles * kb_total k-blocks of the matrix,
@@ -379,8 +404,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   TraceSmem::begin(s_tr, g_trace);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int group = blockIdx.x % p.groups;
-  const int cblk = blockIdx.x / p.groups;  // stream-K block within the lane group
+  // cluster reduction: the cs K splits of one (row tile, lane group) are
+  // consecutive blocks, one cluster; otherwise the lane groups of one
+  // stream-K range are consecutive (they share its weight tiles in L2)
+  const int cs_rank = p.cs ? (int)(blockIdx.x % p.cs) : 0;
+  const int cs_unit = p.cs ? (int)(blockIdx.x / p.cs) : 0;  // tile * groups + group
+  const int group = p.cs ? cs_unit % p.groups : (int)(blockIdx.x % p.groups);
+  const int cblk = p.cs ? (cs_unit / p.groups) * p.cs + cs_rank  // stream-K block
+                        : (int)(blockIdx.x / p.groups);
   const int lane0 = group * p.lg;
   const int lanes = min(p.lg, p.lanes_total - lane0);
   const int n_tot = (lanes + 15) & ~15;
@@ -612,6 +643,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
           if (whole) {
             emit_chunk(p, t, row_local, lane0, lanes, cc, v, xbuf);
+          } else if (p.cs) {  // the partial tile stays in this block's ring
+            float4* dst = reinterpret_cast<float4*>(
+                reinterpret_cast<float*>(smem) + row_local * (n_tot + 4) + cc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           } else {
             float* dst = piece_ptr(p, slot, cblk, lane0 + cc) + row_local;
 #pragma unroll
@@ -622,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_fence_before();
       mbar_arrive(tempty);  // the accumulator may be overwritten by the next piece
-      if (!whole) {
+      if (!whole && !p.cs) {
         __threadfence();
         epi_bar();
         const TilePieces tp = tile_pieces(p, t);
@@ -639,6 +676,47 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cs) {
+    // Every thread of every block of the cluster passes both barriers,
+    // whatever happened before (an aborted block still arrives), so no
+    // block waits on another forever. After the first, every block's
+    // partial tile is in its shared memory; block r then sums lane chunks
+    // r, r + cs, ... of the tile over the cs blocks in split order and
+    // applies the epilogue. The second keeps every block's shared memory
+    // alive until the others have read it.
+    cluster_sync();
+    if (warp < 4) {
+      int bad = 0;
+      for (int r = 0; r < p.cs; ++r) bad |= ld_dsmem_s32(dsmem_addr(smem_u32(&s_abort), r));
+      if (!bad) {
+        const int row_local = warp * 32 + lane;
+        const uint32_t mine = smem_u32(smem) + (uint32_t)(row_local * (n_tot + 4)) * 4u;
+        for (int c0 = cs_rank * 16; c0 < n_tot; c0 += p.cs * 16) {
+          float v[16];
+          for (int r = 0; r < p.cs; ++r) {
+            const uint32_t src = dsmem_addr(mine + (uint32_t)c0 * 4u, r);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 q = ld_dsmem4(src + 16u * j);
+              if (r == 0) {
+                v[4 * j] = q.x;
+                v[4 * j + 1] = q.y;
+                v[4 * j + 2] = q.z;
+                v[4 * j + 3] = q.w;
+              } else {
+                v[4 * j] += q.x;
+                v[4 * j + 1] += q.y;
+                v[4 * j + 2] += q.z;
+                v[4 * j + 3] += q.w;
+              }
+            }
+          }
+          emit_chunk(p, t_first, row_local, lane0, lanes, c0, v, xbuf);
+        }
+      }
+    }
+    cluster_sync();
+  }
   if (warp == 5) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -651,6 +729,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 }  // namespace
+
+bool tc_cluster_reduce() {
+  static const bool v = [] {
+    const char* e = getenv("FS_TC_CLUSTER");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
 
 bool tc_available() {
   if (g_encode) return true;
@@ -741,7 +827,23 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
       smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 2);
     }
   }
-  launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
+  // cluster reduction when every stream-K range is one of cs <= 8 equal K
+  // splits of a row tile and the partial tile (128 rows x (lanes + 4) f32)
+  // fits in the ring; the argmax epilogue needs whole tiles anyway
+  p.cs = 0;
+  {
+    const int n_tot = (p.lg + 15) & ~15;
+    const int cs = p.P / p.m_tiles;
+    if (tc_cluster_reduce() && !p.cs_off && p.epi != EPI_ARGMAX && p.P % p.m_tiles == 0 &&
+        cs >= 2 &&
+        cs <= 8 && (size_t)kBM * (n_tot + 4) * 4 <= (size_t)p.stages * p.stage_bytes)
+      p.cs = cs;
+  }
+  if (p.cs)
+    launch_k_cluster(k_gemm_tc<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16, tmX64lo,
+                     tmX16lo, p);
+  else
+    launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
   return 1;
 }
 

@@ -369,7 +369,10 @@ int fs_selftest_bounded_wait(fs_handle* h, int32_t timeout_us, int32_t* code_out
 /* Test hook: Y[b, n] = sum_k X[b, k] * W[n, k] for bf16 W [N, K] and
  * X [B, K] (K a multiple of 64), f32 Y [B, N]; all DEVICE pointers owned by
  * the caller. path 1 = tcgen05 kernel with `splits` equal K splits per
- * 128-row tile (1 <= splits <= min(8, K/64)), path 0 = warp-GEMV kernel. Allocates its own workspace; runs on
+ * 128-row tile (1 <= splits <= min(8, K/64)); the splits of a tile sum
+ * through a thread-block cluster where the partial tile fits in shared
+ * memory, else through the workspace; path 2 = the same with the workspace
+ * reduction always; path 0 = warp-GEMV kernel. Allocates its own workspace; runs on
  * `stream` (NULL = default) and synchronises it. Errors: FS_ERR_ARG,
  * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_DEVICE (a bounded wait timed out). */
 int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,

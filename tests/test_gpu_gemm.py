@@ -87,3 +87,22 @@ def test_tcgen05_stream_k_batch_invariance_bitwise():
         Y = torch.empty(B, 1000, dtype=torch.float32, device="cuda")
         fs.fs_gemm_bf16_width(Wd, Xd[:B].contiguous(), Y, 23)
         assert torch.equal(Y.view(torch.int32), full[:B].view(torch.int32)), B
+
+
+@pytest.mark.parametrize("N,K,B,splits", [
+    (960, 576, 1, 3), (960, 576, 256, 3), (576, 1536, 64, 8), (3072, 576, 200, 3),
+    (576, 576, 17, 2), (6144, 4096, 128, 2), (4096, 14336, 3, 4)])
+def test_cluster_and_workspace_reductions_give_the_same_bits(N, K, B, splits):
+    """The K splits of a row tile summed inside a thread-block cluster
+    (distributed shared memory) and through the global workspace: the same
+    partial tiles added in the same split order, so the same bits."""
+    import torch
+    W, X = _case(N, K, B, N + K + B + splits)
+    Wd, Xd = W.cuda(), X.cuda()
+    a = torch.empty(B, N, dtype=torch.float32, device="cuda")
+    b = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    fs.fs_gemm_bf16(Wd, Xd, a, splits=splits, path=1)
+    fs.fs_gemm_bf16(Wd, Xd, b, splits=splits, path=2)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ref, mag = _ref(W, X)
+    assert bool(((a.cpu().double() - ref).abs() <= 1e-5 * mag + 1e-6).all())
