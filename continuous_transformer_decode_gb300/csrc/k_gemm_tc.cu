@@ -841,7 +841,9 @@ namespace {
 // (and leaves room for the next kernel's blocks to start under
 // programmatic dependent launch); beyond 3-4 stages a block's stream is
 // limited by its SM's outstanding-load capacity rather than by the ring.
-constexpr int kSmemAttr = 227 * 1024 - 256;
+// the largest dynamic allocation: 227 KB less room for the kernel's static
+// shared memory (about 1.6 KB)
+constexpr int kSmemAttr = 227 * 1024 - 4096;
 constexpr int kMaxStages = 12;
 // FS_TC_MAX_STAGES (2..12) lowers the stage cap, a tuning knob read once.
 int max_stages() {
@@ -852,13 +854,13 @@ int max_stages() {
   }();
   return v;
 }
-// FS_TC_SMEM_KB (64..224, a tuning knob read once) sets the per-block shared
+// FS_TC_SMEM_KB (64..208, a tuning knob read once) sets the per-block shared
 // memory budget of the ring (default 112 KB: two blocks per SM).
 int smem_budget() {
   static const int v = [] {
     const char* e = getenv("FS_TC_SMEM_KB");
     const int x = e ? atoi(e) : 112;
-    return std::max(64, std::min(224, x)) * 1024;
+    return std::max(64, std::min(208, x)) * 1024;
   }();
   return v;
 }
