@@ -73,6 +73,7 @@ def lib():
             "or_silu": (C.c_float, [C.c_float]),
             "or_model_create": (p, [C.POINTER(or_desc), i, p, p, p, p]),
             "or_model_free": (None, [p]),
+            "or_model_set_kv_bf16": (None, [p, i]),
             "or_lane_create": (p, [p, i]),
             "or_lane_free": (None, [p]),
             "or_lane_reset": (None, [p]),
@@ -227,7 +228,7 @@ class Model:
     [rows*cols/32, 34], matching ``dtype`` (F32, BF16 or Q8_0).
     """
 
-    def __init__(self, cfg: dict, weights: dict, dtype: int):
+    def __init__(self, cfg: dict, weights: dict, dtype: int, kv_bf16: bool = False):
         self.cfg = dict(cfg)
         d = or_desc(cfg["L"], cfg["d"], cfg["H"], cfg["Hkv"], cfg["hd"],
                     cfg["F"], cfg["V"], cfg["rms_eps"], cfg["rope_theta"],
@@ -251,6 +252,9 @@ class Model:
             p(weights.get("lm_head")), p(weights["final_norm"]), arr)
         self._keep = []  # the oracle keeps its own f32 copies
         self.V = cfg["V"]
+        # KV storage of a bf16 arena: keys (roped) and values enter the
+        # cache rounded to bf16
+        lib().or_model_set_kv_bf16(self._h, 1 if kv_bf16 else 0)
 
     def __del__(self):
         if getattr(self, "_h", None):

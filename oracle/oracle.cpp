@@ -367,6 +367,10 @@ struct OrLayer {
 
 struct OrModel {
   or_desc c;
+  // KV storage: 0 = f32; 1 = bf16 values (a roped key and a value are
+  // rounded to bf16, nearest-even, when they enter the cache; the un-roped
+  // keys stay f32), the storage of a bf16 KV arena
+  int kv_bf16 = 0;
   std::vector<float> embed, head, g_final;
   std::vector<OrLayer> layers;
   const float* head_ptr() const { return c.tied ? embed.data() : head.data(); }
@@ -461,6 +465,11 @@ void or_lane_import(void* mp, void* lp, int layer, const float* K,
   size_t cnt = (size_t)n * m->c.Hkv * m->c.hd;
   std::memcpy(ln->K[layer].data(), K, cnt * 4);
   std::memcpy(ln->V[layer].data(), V, cnt * 4);
+  if (m->kv_bf16)  // stored as the cache stores it
+    for (size_t i = 0; i < cnt; ++i) {
+      ln->K[layer][i] = or_bf16_to_f32(or_f32_to_bf16(ln->K[layer][i]));
+      ln->V[layer][i] = or_bf16_to_f32(or_f32_to_bf16(ln->V[layer][i]));
+    }
   std::fill(ln->Kraw[layer].begin(), ln->Kraw[layer].begin() + cnt, 0.0f);
   ln->pos = n;
 }
@@ -500,6 +509,8 @@ int or_lane_evict(void* mp, void* lp, int start, int end) {
       float* k = ln->K[l].data() + q * row;
       std::memcpy(k, ln->Kraw[l].data() + q * row, row * 4);
       or_rope(k, c.Hkv, c.hd, q, c.rope_theta);
+      if (m->kv_bf16)  // stored as the cache stores it
+        for (size_t i = 0; i < row; ++i) k[i] = or_bf16_to_f32(or_f32_to_bf16(k[i]));
     }
   }
   ln->pos -= delta;
@@ -521,6 +532,11 @@ static void lane_attention(const OrModel* m, const OrLane* ln, int layer,
   }
 }
 
+// A value as the cache stores it.
+static float kv_store(const OrModel* m, float x) {
+  return m->kv_bf16 ? or_bf16_to_f32(or_f32_to_bf16(x)) : x;
+}
+
 static void append_kv(const OrModel* m, OrLane* ln, int layer, int pos,
                       const float* k_raw, const float* k_roped,
                       const float* v) {
@@ -528,9 +544,13 @@ static void append_kv(const OrModel* m, OrLane* ln, int layer, int pos,
   size_t n = (size_t)c.Hkv * c.hd;
   size_t off = (size_t)pos * n;
   std::memcpy(ln->Kraw[layer].data() + off, k_raw, n * 4);
-  std::memcpy(ln->K[layer].data() + off, k_roped, n * 4);
-  std::memcpy(ln->V[layer].data() + off, v, n * 4);
+  for (size_t i = 0; i < n; ++i) {
+    ln->K[layer][off + i] = kv_store(m, k_roped[i]);
+    ln->V[layer][off + i] = kv_store(m, v[i]);
+  }
 }
+
+void or_model_set_kv_bf16(void* mp, int on) { ((OrModel*)mp)->kv_bf16 = on ? 1 : 0; }
 
 // The batched step over n lanes; with n == 1 it is the serial Step. Every
 // per-lane quantity is computed with the same scalar arithmetic either way.

@@ -22,8 +22,18 @@ def _rope(x, pos, theta):
     return np.concatenate([z.real, z.imag], axis=-1)
 
 
-def forward_logits(cfg, W, tokens):
-    """Logits [T, V] for every position of one sequence (causal)."""
+def _bf16_round(a):
+    """Nearest-even bf16 rounding of the values' float32 images (a bf16 KV
+    arena's storage), written with integer bit arithmetic."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def forward_logits(cfg, W, tokens, kv_bf16=False):
+    """Logits [T, V] for every position of one sequence (causal). kv_bf16:
+    the roped keys and the values are stored rounded to bf16 before any
+    query reads them (the storage of a bf16 KV arena)."""
     f = lambda a: np.asarray(a, dtype=np.float64)
     d, H, Hkv, hd = cfg["d"], cfg["H"], cfg["Hkv"], cfg["hd"]
     T = len(tokens)
@@ -37,6 +47,8 @@ def forward_logits(cfg, W, tokens):
         v = (h @ f(ly["wv"]).T).reshape(T, Hkv, hd)
         q = _rope(q, pos, cfg["rope_theta"])
         k = _rope(k, pos, cfg["rope_theta"])
+        if kv_bf16:
+            k, v = _bf16_round(k), _bf16_round(v)
         rep = H // Hkv
         k = np.repeat(k, rep, axis=1)  # head h uses kv head h // rep
         v = np.repeat(v, rep, axis=1)

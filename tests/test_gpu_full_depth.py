@@ -289,18 +289,24 @@ def test_mistral_full_depth_b1_and_128_lane_handles():
     U[128, 4096], with two sampled lanes (contexts 3001 and 640) followed by
     the oracle; two teacher-forced steps, then a fused-greedy step.
 
-    The handles carry split activations (act_split = 1): at this depth and
-    width, rounding the activation panels to bf16 alone moves the logits by
-    up to ~0.15 (an f32 emulation of the same model with only that rounding
-    gives max-abs 0.147, cosine 0.99969), beyond the 5e-2 bound; with the
-    remainders multiplied too the same emulation gives 0.005."""
+    Two readings at this depth and width (32 layers, d = 4096):
+    * the handles carry split activations (act_split = 1): rounding the
+      activation panels to bf16 alone moves the logits by up to ~0.15 (an
+      f32 emulation of the same model with only that rounding gives max-abs
+      0.147, cosine 0.99969), beyond the 5e-2 bound; with the remainders
+      multiplied too the same emulation gives 0.005;
+    * the oracle stores its KV cache as the handle does (kv_bf16: keys and
+      values enter the cache rounded to bf16): a generated token's key that
+      later queries align with carries its bf16 rounding into their softmax,
+      which moves the next step's logits by up to ~0.09 against an f32 cache
+      even with split activations."""
     import torch
     if _mem_available_gb() < 80:
         pytest.skip("needs about 80 GB of host memory for the f32 7B oracle")
     cfg = synth.MODEL_M
     V, L, Hkv, hd = cfg["V"], cfg["L"], cfg["Hkv"], cfg["hd"]
     Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
-    m = O.Model(cfg, Wb, O.BF16)
+    m = O.Model(cfg, Wb, O.BF16, kv_bf16=True)
     cases = [(1, {0: 2500}), (128, {3: 3001, 77: 640})]
     for B, sampled in cases:
         ctx = synth.make_context_lengths(B, seed=3)

@@ -33,6 +33,43 @@ def test_f64_brute_force_whole_model(tiny):
     assert ln.pos == len(toks)
 
 
+def test_f64_brute_force_with_bf16_kv_storage(tiny):
+    """kv_bf16: keys and values enter the cache rounded to bf16. Pinned by
+    the f64 brute force with the same storage rounding, which the f32-KV
+    oracle misses by far more than the tolerance (so the rounding is really
+    applied, to both keys and values); every stored value is bf16-exact."""
+    W, m = tiny
+    mb = O.Model(T, W, O.F32, kv_bf16=True)
+    toks = synth.make_prompts(1, 12, T["V"], seed=2)[0]
+    ref_b = forward_logits(T, W, toks, kv_bf16=True)
+    ref_f = forward_logits(T, W, toks)
+    lb, lf = mb.lane(64), m.lane(64)
+    worst_f = 0.0
+    for t, tok in enumerate(toks):
+        gb, gf = mb.step(lb, tok), m.step(lf, tok)
+        scale = max(1.0, np.abs(ref_b[t]).max())
+        assert np.abs(gb - ref_b[t]).max() < 2e-5 * scale, t
+        worst_f = max(worst_f, np.abs(gf - ref_b[t]).max() / scale)
+    assert worst_f > 1e-4  # the f32-KV oracle is not the bf16-storage model
+    for l in range(T["L"]):
+        for which in ("K", "V"):
+            a = lb.export(l, which)
+            assert np.array_equal(synth.bf16_to_f32(synth.bf16_bits(a)), a)
+    # batched == serial holds in this storage too
+    prompts = synth.make_prompts(3, [4, 6, 5], T["V"], seed=8)
+    ser = [mb.lane(64) for _ in range(3)]
+    bat = [mb.lane(64) for _ in range(3)]
+    for b in range(3):
+        mb.prefill(ser[b], prompts[b])
+        mb.prefill(bat[b], prompts[b])
+    tk = [int(p[-1]) for p in prompts]
+    for _ in range(4):
+        out = mb.step_batch(bat, tk)
+        for b in range(3):
+            assert np.array_equal(mb.step(ser[b], tk[b]).view(np.uint32), out[b].view(np.uint32))
+        tk = [int(np.argmax(r)) for r in out]
+
+
 def test_batched_equals_serial_bitwise_logits_and_kv(tiny):
     """StepBatch == serial Step per lane: logits and the full K/Kraw/V/pos."""
     W, m = tiny
