@@ -648,8 +648,6 @@ def main():
                     help="after the timed steps, trace N more steps' kernel timeline "
                          "(%%globaltimer per block): the GEMM roofline's time share "
                          "and the line's kernel_timeline (0: off, no roofline)")
-    ap.add_argument("--act-split", type=int, default=-1, choices=[-1, 0, 1],
-                    help="override the workload's activation split (-1: the workload's)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other configurations' record (Q8_0 at 960 lanes, "
                          "Mistral-7B at 1 and 128 lanes)")
@@ -661,9 +659,7 @@ def main():
                     help="trace workload: prompt tokens per lane per step (default the "
                          "budget; 1 = no chunking)")
     args = ap.parse_args()
-    wl = dict(WORKLOADS[args.workload])
-    if args.act_split >= 0:
-        wl["act_split"] = args.act_split
+    wl = WORKLOADS[args.workload]
     ws, rank, local = _dist()
 
     if wl.get("trace"):

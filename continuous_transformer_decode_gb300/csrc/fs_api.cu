@@ -133,8 +133,6 @@ struct fs_handle {
   PanelMaps pm_h, pm_o, pm_a;
   int act_split = 0;
   int64_t lo_h = 0, lo_o = 0, lo_a = 0;  // remainder offsets (elements; 0: none)
-  float* ss = nullptr;  // folded norm: sums of squares [max_lanes][ss_ld]
-  int ss_ld = 1;        // 128-column tiles of d
   float* ws = nullptr;
   int* counters = nullptr;
   int* err_flag = nullptr;  // mapped pinned host memory
@@ -519,7 +517,6 @@ int create_impl(fs_handle* h, const fs_weights* W) {
 
   // ---- scratch panels
   const int B = d.max_lanes;
-  h->ss_ld = (d.d_model + 127) / 128;
   const size_t xs = h->xtype == X_F32 ? 4 : 2;
   bool ok = h->alloc(&h->x, (size_t)B * d.d_model * 4) == cudaSuccess &&
             h->alloc(&h->y, (size_t)B * d.d_model * 4) == cudaSuccess &&
@@ -527,7 +524,6 @@ int create_impl(fs_handle* h, const fs_weights* W) {
             h->alloc(&h->opanel, (size_t)(1 + h->act_split) * B * h->Kp_q * xs) == cudaSuccess &&
             h->alloc(&h->apanel, (size_t)(1 + h->act_split) * B * h->Kp_f * xs) == cudaSuccess &&
             h->alloc(&h->qkv, (size_t)B * h->Nqkv * 4) == cudaSuccess &&
-            h->alloc(&h->ss, (size_t)B * ((d.d_model + 127) / 128) * 4) == cudaSuccess &&
             h->alloc(&h->q, (size_t)B * h->Nq * 4) == cudaSuccess &&
             h->alloc(&h->logits, (size_t)B * d.vocab * 4) == cudaSuccess &&
             h->alloc(&h->part_ml, (size_t)B * h->max_splits * d.n_heads * 2 * 4) == cudaSuccess &&
@@ -741,12 +737,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     return b;
   };
   // algorithmic bytes: weights once, activations in, outputs out
-  // folded norm (tensor-core path): `consume` scales the outputs by each
-  // lane's r from ss; `g_next` (with EPI_RESID) writes the next norm's panel
-  // and sums of squares
   auto gemm = [&](const Mat& W, const TcW& T, const fs_handle::PanelMaps& pm, const void* X,
-                  int epi, float* of, void* ox, int ldo, int n_out, bool consume = false,
-                  const float* g_next = nullptr) {
+                  int epi, float* of, void* ox, int ldo, int n_out) {
     double bytes = wbytes(W) + (double)n * W.K * xs;
     bytes += epi == EPI_ARGMAX ? (double)n * T.m_tiles * 8.0
              : epi == EPI_SWIGLU ? (double)n * n_out * xs
@@ -769,12 +761,6 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.am_val = h->am_val; p.am_idx = h->am_idx;
     p.split = h->act_split;
     p.lo_off = epi == EPI_SWIGLU ? h->lo_a : 0;
-    p.ss_ld = h->ss_ld; p.ss_n = h->ss_ld; p.norm_d = d.d_model; p.norm_eps = d.rms_eps;
-    if (consume) p.ss_in = h->ss;
-    if (g_next) {
-      p.g_next = g_next; p.ss_out = h->ss;
-      p.u_out = static_cast<__nv_bfloat16*>(h->hpanel); p.ld_u = h->Kp_d; p.u_lo = h->lo_h;
-    }
     if (h->wtype == W_Q8)
       h->launch(FS_PROF_GEMM, bytes, [&] {
         return launch_gemm_tc_q8(pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
@@ -784,64 +770,6 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
         return launch_gemm_tc(T.tm, pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
       });
   };
-  if (h->use_tc) {
-    // RMSNorm folded into the GEMMs: the embedding and the residual GEMMs
-    // (O, down) write x, the next norm's u = bf16(x g) panel and the sums of
-    // squares; the GEMMs reading that panel (QKV, gate/up, head) scale their
-    // outputs by each lane's r
-    h->launch(FS_PROF_OTHER, (double)n * d.d_model * (4.0 + 4.0 + xs), [&] {
-      return launch_embed_tc(h->embed, args, n, h->kv, h->x, d.d_model, h->layers[0].g_attn,
-                             static_cast<__nv_bfloat16*>(h->hpanel), h->Kp_d, h->lo_h, h->ss,
-                             h->ss_ld, s);
-    });
-    for (int l = 0; l < d.n_layers; ++l) {
-      const LayerW& W = h->layers[l];
-      gemm(W.qkv, W.qkv_tc, h->pm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv,
-           true);
-      if (chunked)
-        h->launch(FS_PROF_OTHER, (double)n * (h->Nqkv * 4.0 + h->Nq * 4.0 + 2.0 * h->Nkv * kvs),
-                  [&] {
-                    return launch_rope_append(h->qkv, n, d.n_heads, d.n_kv_heads, d.head_dim,
-                                              h->rope_cos, h->rope_sin, args, h->kv, l, h->q, s);
-                  });
-      AttnParams ap{};
-      ap.kv_written = chunked ? 1 : 0;
-      ap.qkv = h->qkv; ap.H = d.n_heads; ap.rc = h->rope_cos; ap.rs = h->rope_sin;
-      ap.args = args; ap.kv = h->kv; ap.layer = l; ap.split_len = h->split_len;
-      ap.max_splits = h->max_splits; ap.part_ml = h->part_ml; ap.part_acc = h->part_acc;
-      ap.counters = h->attn_counters; ap.o = h->opanel; ap.ld_o = h->Kp_q; ap.err = h->d_err_flag;
-      ap.o_lo = h->lo_o;
-      h->launch(FS_PROF_ATTN,
-                kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs), [&] {
-                  if (h->attn_tma)
-                    return launch_attention_tma(h->tm_kv_k, h->tm_kv_v, ap, n, h->xtype, s);
-                  return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
-                                     : launch_attention_tiled(ap, n, h->xtype, s);
-                });
-      gemm(W.o, W.o_tc, h->pm_o, h->opanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model,
-           false, W.g_ffn);
-      gemm(W.gateup, W.gateup_tc, h->pm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
-           d.d_ffn, true);
-      gemm(W.down, W.down_tc, h->pm_a, h->apanel, EPI_RESID, h->x, nullptr, d.d_model, d.d_model,
-           false, l + 1 < d.n_layers ? h->layers[l + 1].g_attn : h->g_final);
-    }
-    if (greedy && h->greedy_fused) {
-      gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_ARGMAX, nullptr, nullptr, d.vocab,
-           d.vocab, true);
-      h->launch(FS_PROF_OTHER, (double)n * (h->head_tc.m_tiles * 8.0 + 4.0), [&] {
-        return launch_argmax_tiles(h->am_val, h->am_idx, n, h->head_tc.m_tiles, greedy, s);
-      });
-      return;
-    }
-    gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab,
-         true);
-    if (greedy)
-      h->launch(FS_PROF_OTHER, (double)n * d.vocab * 4.0, [&] {
-        return launch_sample(out, n, d.vocab, h->d_zero_temps, h->d_zero_u64, h->d_zero_u64,
-                             greedy, s);
-      });
-    return;
-  }
   const double norm_bytes = (double)n * d.d_model * (4.0 * 3 + xs);
   // embedding gather + the first layer's input norm
   h->launch(FS_PROF_OTHER, (double)n * d.d_model * (4.0 * 2 + xs), [&] {

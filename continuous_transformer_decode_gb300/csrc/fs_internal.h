@@ -300,25 +300,6 @@ struct TcParams {
   // order of the workspace reduction, so the bits are the same)
   int cs;
   int cs_off;      // 1: never the cluster reduction (the caller's workspace serves)
-  // RMSNorm folded into the GEMMs (tensor-core path). A norm y = x r g with
-  // r = 1 / sqrt(mean(x^2) + eps) is split in two:
-  //  * the GEMM that updates x (EPI_RESID) also writes u = bf16(x * g_next)
-  //    (and its remainder at u + u_lo when u_lo > 0) into the next GEMM's
-  //    panel and, per lane and 128-row tile, the sum of squares of the new
-  //    x over the tile's rows (a fixed tree: each warp's 32 rows by an xor
-  //    butterfly, then the 4 warps in order) into ss_out[lane * ss_ld + tile];
-  //  * the next GEMM multiplies W by u and scales each lane's outputs by its
-  //    r = 1 / sqrtf(sum_t ss_in[lane * ss_ld + t] / norm_d + eps), the
-  //    partials added in tile order (ss_in == nullptr: no scaling).
-  const float* g_next;
-  __nv_bfloat16* u_out;
-  int ld_u;
-  int64_t u_lo;
-  float* ss_out;
-  const float* ss_in;
-  int ss_ld, ss_n;  // partials per lane row (stride) and in use (tiles of d)
-  int norm_d;
-  float norm_eps;
 };
 // Per lane, the argmax over the tiles' (max, index) pairs of an EPI_ARGMAX
 // launch (lowest index on ties): tokens_out[b] for b < B.
@@ -380,12 +361,6 @@ int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int
 int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
                  const float* g, float eps, void* h, int x_type, int ld_h, int64_t lo_off,
                  cudaStream_t s);
-// Tensor-core path: x = E[tok], u = bf16(x * g) (remainders at u + u_lo when
-// u_lo > 0) and the per-128-column-tile sums of squares of x (the tree of
-// TcParams::ss_out) into ss[b * ss_ld + t].
-int launch_embed_tc(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-                    const float* g, __nv_bfloat16* u, int ld_u, int64_t u_lo, float* ss,
-                    int ss_ld, cudaStream_t s);
 // x += resid (if resid is given), out = RMSNorm(x) * g (and its remainders
 // at out + lo_off when lo_off > 0).
 int launch_rmsnorm(float* x, const float* resid, const float* g, int B, int d, float eps,

@@ -176,18 +176,12 @@ __device__ __forceinline__ TilePieces tile_pieces(const TcParams& p, int t) {
   return r;
 }
 
-// Writes one 16-lane chunk of final values of this thread's row (all 128
-// epilogue threads call it together: some paths exchange through shared
-// memory). With a folded norm on the input (p.ss_in) the values are first
-// scaled by their lanes' r (s_r, per lane of the group).
+// Writes one 16-lane chunk of final values of this thread's row.
 // For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
 // rows; the up half hands its values to the gate half through shared memory.
 __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int row_local,
-                                           int lane0, int lanes, int c0, const float vin[16],
-                                           float* xbuf, const float* s_r, float* s_ssx) {
-  float v[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = p.ss_in ? vin[j] * s_r[c0 + j] : vin[j];
+                                           int lane0, int lanes, int c0, const float v[16],
+                                           float* xbuf) {
   if (p.epi == EPI_SWIGLU) {
     if (row_local >= 64) {
 #pragma unroll
@@ -253,51 +247,20 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
     return;
   }
   const int row = m_tile * kBM + row_local;
-  const bool valid = row < p.n_out;
+  if (row >= p.n_out) return;
   float* o = p.out_f32 + (int64_t)(lane0 + c0) * p.ldo + row;
   if (p.epi == EPI_RESID) {
-    float nx[16];  // every load of the chunk before any store
+    float prev[16];  // every load of the chunk before any store
+#pragma unroll
+    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < lanes) ? o[(int64_t)j * p.ldo] : 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      nx[j] = (valid && c0 + j < lanes) ? o[(int64_t)j * p.ldo] + v[j] : 0.0f;
-    if (valid) {
+      if (c0 + j < lanes) o[(int64_t)j * p.ldo] = prev[j] + v[j];
+  } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c0 + j < lanes) o[(int64_t)j * p.ldo] = nx[j];
-    }
-    if (p.ss_out) {  // the next norm's input panel and sums of squares
-      if (valid) {
-        const float g = p.g_next[row];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < lanes) {
-            __nv_bfloat16* u = p.u_out + (int64_t)(lane0 + c0 + j) * p.ld_u + row;
-            const float y = nx[j] * g;
-            const __nv_bfloat16 yh = __float2bfloat16_rn(y);
-            *u = yh;
-            if (p.u_lo > 0) u[p.u_lo] = __float2bfloat16_rn(y - __bfloat162float(yh));
-          }
-      }
-      const int w = row_local >> 5, l = row_local & 31;
-      float* sx = s_ssx + ((c0 >> 4) & 1) * 64;  // [4 warps][16 lanes]
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float q = nx[j] * nx[j];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-        if (l == j) sx[w * 16 + j] = q;
-      }
-      epi_bar();
-      if (row_local < 16 && c0 + row_local < lanes)
-        p.ss_out[(int64_t)(lane0 + c0 + row_local) * p.ss_ld + m_tile] =
-            ((sx[row_local] + sx[16 + row_local]) + sx[32 + row_local]) + sx[48 + row_local];
-    }
-    return;
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < lanes) o[(int64_t)j * p.ldo] = v[j];
   }
-  if (!valid) return;
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (c0 + j < lanes) o[(int64_t)j * p.ldo] = v[j];
 }
 
 __device__ __forceinline__ float4 ld4(const float* q) {
@@ -331,24 +294,8 @@ __device__ __forceinline__ float4 sum_pieces4(const TcParams& p, const TilePiece
 // Last piece of a row tile to arrive: sum the tile's pieces and apply the
 // epilogue with 16-byte accesses (threads map to 4-row groups x lanes).
 __device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp, int lane0,
-                            int lanes, float* xbuf, const float* s_r, float* s_ssx) {
+                            int lanes) {
   const int t = threadIdx.x;  // 0..127
-  if (p.epi == EPI_RESID || p.ss_in) {
-    // thread = row, 16-lane chunks through the whole-tile epilogue (the same
-    // per-row arithmetic and sum-of-squares tree as a tile that never split)
-    for (int c0 = 0; c0 < lanes; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int b = c0 + j < lanes ? lane0 + c0 + j : lane0;  // unused past lanes
-        float acc = __ldcg(piece_ptr(p, tp.slotA, tp.cA, b) + t);
-        for (int c = tp.cA + 1; c <= tp.cB; ++c) acc += __ldcg(piece_ptr(p, 0, c, b) + t);
-        v[j] = acc;
-      }
-      emit_chunk(p, m_tile, t, lane0, lanes, c0, v, xbuf, s_r, s_ssx);
-    }
-    return;
-  }
   if (p.epi == EPI_SWIGLU) {
     const int rq = (t & 15) * 4, lsub = t >> 4;  // 16 threads per lane row
     const int f0 = m_tile * 64 + rq;
@@ -440,9 +387,7 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
   }
 }
 
-// kSplit: the panel has a remainder part (TcParams::split), two MMAs per
-// k-step; a compile-time switch so that the plain kernel carries none of it.
-template <bool kQ8, bool kSplit>
+template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
               const __grid_constant__ CUtensorMap tmX16,
@@ -456,8 +401,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_last;
   __shared__ int s_stop[2];
   __shared__ unsigned long long s_tr[4];
-  __shared__ float s_r[256];       // folded norm: each lane's r
-  __shared__ float s_ssx[2 * 64];  // folded norm: warp sums of squares
   TraceSmem::begin(s_tr, g_trace);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -491,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmX64);
     prefetch_tensormap(&tmX16);
-    if (kSplit) {
+    if (p.split) {
       prefetch_tensormap(&tmX64lo);
       prefetch_tensormap(&tmX16lo);
     }
@@ -531,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
   const int nb64 = n_tot / 64;
   const int nbox1 = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // boxes of one panel part
-  const int nbox = nbox1 * (kSplit ? 2 : 1);                  // panel boxes per stage
-  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (kSplit ? 2 : 1);
+  const int nbox = nbox1 * (p.split ? 2 : 1);                 // panel boxes per stage
+  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (p.split ? 2 : 1);
   // warp-collective: iterations first, first + step, ...
   auto produce = [&](int first, int step) {
     int issued = -1;  // last iteration issued
@@ -556,15 +499,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       const int x = ((g0 + i) % kbt) * kBK;
-      if (kSplit && b >= nbox1) {  // the remainder panel
-        const int bb = b - nbox1;
-        const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
-        tma_load_2d(st + kXOff + n_tot * 128 + r * 128, bb < nb64 ? &tmX64lo : &tmX16lo, x,
-                    lane0 + r, full0 + 8 * s);
-        return;
-      }
-      const int r = b < nb64 ? b * 64 : nb64 * 64 + (b - nb64) * kXBoxRows;
-      tma_load_2d(st + kXOff + r * 128, b < nb64 ? &tmX64 : &tmX16, x, lane0 + r, full0 + 8 * s);
+      const int part = b >= nbox1 ? 1 : 0;  // 1: the remainder panel
+      const int bb = b - part * nbox1;
+      const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
+      const CUtensorMap* m = part ? (bb < nb64 ? &tmX64lo : &tmX16lo)
+                                  : (bb < nb64 ? &tmX64 : &tmX16);
+      tma_load_2d(st + kXOff + part * n_tot * 128 + r * 128, m, x, lane0 + r, full0 + 8 * s);
     };
     // Programmatic dependent launch: the weight tiles do not depend on the
     // predecessor kernel, so they start before waiting for it; the panel is
@@ -646,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (acc || kk > 0) ? 1u : 0u);
-            if (kSplit) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+            if (p.split) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
           }
           acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
@@ -657,15 +597,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {  // ---- warps 0-3: Q8_0 dequantisation of each piece, then its epilogue
     if (warp_prod && warp < npw) produce(warp, npw);
     const int row_local = warp * 32 + lane;
-    if (p.ss_in) {  // the folded norm's r of every lane of the group
-      for (int b = row_local; b < lanes; b += 128) {
-        const float* q = p.ss_in + (int64_t)(lane0 + b) * p.ss_ld;
-        float ss = q[0];
-        for (int t2 = 1; t2 < p.ss_n; ++t2) ss += q[t2];
-        s_r[b] = 1.0f / sqrtf(ss / (float)p.norm_d + p.norm_eps);
-      }
-      epi_bar();
-    }
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     int i = 0;
     for (int q = 0; q < n_pieces; ++q) {
@@ -711,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
           if (whole) {
-            emit_chunk(p, t, row_local, lane0, lanes, cc, v, xbuf, s_r, s_ssx);
+            emit_chunk(p, t, row_local, lane0, lanes, cc, v, xbuf);
           } else if (p.cs) {  // the partial tile stays in this block's ring
             float4* dst = reinterpret_cast<float4*>(
                 reinterpret_cast<float*>(smem) + row_local * (n_tot + 4) + cc);
@@ -737,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         epi_bar();
         if (s_last) {
           __threadfence();
-          reduce_tile(p, t, tp, lane0, lanes, xbuf, s_r, s_ssx);
+          reduce_tile(p, t, tp, lane0, lanes);
           if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
         }
       }
@@ -780,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               }
             }
           }
-          emit_chunk(p, t_first, row_local, lane0, lanes, c0, v, xbuf, s_r, s_ssx);
+          emit_chunk(p, t_first, row_local, lane0, lanes, c0, v, xbuf);
         }
       }
     }
@@ -874,13 +805,13 @@ int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_byt
   return st;
 }
 
-template <bool kQ8, bool kSplit>
+template <bool kQ8>
 int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                 const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p0,
                 cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_gemm_tc<kQ8, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_gemm_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemAttr) != cudaSuccess)
       return 0;  // the launch below then fails and the caller reports it
     attr_set = true;
@@ -888,7 +819,7 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
   TcParams p = p0;
   int smem = 0;
   const int grid = p.P * p.groups;
-  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, kSplit, &p.stage_bytes, &smem);
+  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, p.split, &p.stage_bytes, &smem);
   // producer warps of single-piece blocks: up to 4, dividing the stage count
   p.prod_warps = 1;
   if (!kQ8) {
@@ -911,11 +842,10 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
       p.cs = cs;
   }
   if (p.cs)
-    launch_k_cluster(k_gemm_tc<kQ8, kSplit>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16,
-                     tmX64lo, tmX16lo, p);
+    launch_k_cluster(k_gemm_tc<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16, tmX64lo,
+                     tmX16lo, p);
   else
-    launch_k(k_gemm_tc<kQ8, kSplit>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo,
-             p);
+    launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
   return 1;
 }
 
@@ -949,16 +879,14 @@ __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __rest
 int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                    const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                    cudaStream_t s) {
-  return p.split ? launch_impl<false, true>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
-                 : launch_impl<false, false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+  return launch_impl<false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
 int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                       const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                       cudaStream_t s) {
   // the W map is unused
-  return p.split ? launch_impl<true, true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
-                 : launch_impl<true, false>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+  return launch_impl<true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
 namespace {

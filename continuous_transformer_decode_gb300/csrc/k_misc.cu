@@ -54,49 +54,6 @@ __global__ void __launch_bounds__(kNormRowThreads)
 }
 
 
-// Tensor-core path: x[b] = E[tok[b]], u[b] = bf16(x[b] * g) (remainders at
-// u + u_lo) and, per 128-column tile t, ss[b][t] = the sum of x^2 over the
-// tile by the tree the GEMM epilogues use (thread c holds column 128 t + c;
-// an xor butterfly over each warp, then the 4 warps in order); block b also
-// applies page-table update b of the step.
-__global__ void __launch_bounds__(128)
-    k_embed_tc(Mat E, StepArgs args, KV kv, float* __restrict__ x, int d,
-               const float* __restrict__ g, __nv_bfloat16* __restrict__ u, int ld_u,
-               int64_t u_lo, float* __restrict__ ss, int ss_ld) {
-  TraceMark tr;
-  tr.begin(g_trace);
-  pdl_wait();
-  tr.ready();
-  pdl_trigger();
-  __shared__ float red[2][4];
-  const int b = blockIdx.x, t = threadIdx.x, w = t >> 5, l = t & 31;
-  if (t == 0 && b < *args.n_upd) {
-    kv.pt[(int64_t)args.upd_lane[b] * kv.max_pages + args.upd_slot[b]] =
-        args.upd_page[b];
-  }
-  const int64_t tok = args.tok[b];
-  for (int t0 = 0; t0 * 128 < d; ++t0) {
-    const int col = t0 * 128 + t;
-    float v = 0.0f;
-    if (col < d) {
-      v = load_w(E, tok, col);
-      x[(int64_t)b * d + col] = v;
-      const float y = v * g[col];
-      const __nv_bfloat16 yh = __float2bfloat16_rn(y);
-      u[(int64_t)b * ld_u + col] = yh;
-      if (u_lo > 0) u[(int64_t)b * ld_u + col + u_lo] = __float2bfloat16_rn(y - __bfloat162float(yh));
-    }
-    float q = v * v;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-    if (l == 0) red[t0 & 1][w] = q;
-    __syncthreads();
-    if (t == 0) ss[(int64_t)b * ss_ld + t0] = ((red[t0 & 1][0] + red[t0 & 1][1]) + red[t0 & 1][2]) +
-                                              red[t0 & 1][3];
-  }
-  tr.end(TR_EMBED);
-}
-
 // Residual add then RMSNorm, one block of 128 threads per panel row (see
 // norm_row.cuh for the arithmetic and its fixed reduction order).
 template <typename OT, int MV>
@@ -410,14 +367,6 @@ void embed_ot(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x,
     case 8: embed_mv<OT, 8>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
     default: embed_mv<OT, 16>(E, args, B, kv, x, d, g, eps, h, ld_h, lo, s); break;
   }
-}
-
-int launch_embed_tc(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
-                    const float* g, __nv_bfloat16* u, int ld_u, int64_t u_lo, float* ss,
-                    int ss_ld, cudaStream_t s) {
-  if (B <= 0) return 0;
-  launch_k(k_embed_tc, B, 128, 0, s, E, args, kv, x, d, g, u, ld_u, u_lo, ss, ss_ld);
-  return 1;
 }
 
 int launch_embed(const Mat& E, const StepArgs& args, int B, const KV& kv, float* x, int d,
