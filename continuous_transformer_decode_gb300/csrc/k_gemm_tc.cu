@@ -179,6 +179,7 @@ __device__ __forceinline__ TilePieces tile_pieces(const TcParams& p, int t) {
 // Writes one 16-lane chunk of final values of this thread's row.
 // For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
 // rows; the up half hands its values to the gate half through shared memory.
+template <bool kSplit>
 __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int row_local,
                                            int lane0, int lanes, int c0, const float v[16],
                                            float* xbuf) {
@@ -199,7 +200,7 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + b) * p.ldo + f;
             const __nv_bfloat16 ah = __float2bfloat16_rn(a);
             *o = ah;
-            if (p.lo_off > 0) o[p.lo_off] = __float2bfloat16_rn(a - __bfloat162float(ah));
+            if (kSplit && p.lo_off > 0) o[p.lo_off] = __float2bfloat16_rn(a - __bfloat162float(ah));
           }
         }
       }
@@ -293,6 +294,7 @@ __device__ __forceinline__ float4 sum_pieces4(const TcParams& p, const TilePiece
 
 // Last piece of a row tile to arrive: sum the tile's pieces and apply the
 // epilogue with 16-byte accesses (threads map to 4-row groups x lanes).
+template <bool kSplit>
 __device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp, int lane0,
                             int lanes) {
   const int t = threadIdx.x;  // 0..127
@@ -321,7 +323,7 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp,
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + b) * p.ldo + f0;
         *reinterpret_cast<uint2*>(o) = pk;
-        if (p.lo_off > 0) {
+        if (kSplit && p.lo_off > 0) {
           const float2 fl = __bfloat1622float2(lo), fh = __bfloat1622float2(hi);
           __nv_bfloat162 rl = __floats2bfloat162_rn(a0 - fl.x, a1 - fl.y);
           __nv_bfloat162 rh = __floats2bfloat162_rn(a2 - fh.x, a3 - fh.y);
@@ -387,12 +389,13 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
   }
 }
 
-template <bool kQ8>
-__global__ void __launch_bounds__(kThreads, 2)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
-              const __grid_constant__ CUtensorMap tmX16,
-              const __grid_constant__ CUtensorMap tmX64lo,
-              const __grid_constant__ CUtensorMap tmX16lo, const TcParams p) {
+// kSplit: the panel has a remainder part (TcParams::split), two MMAs per
+// k-step; a compile-time switch so that the plain kernel carries none of it.
+template <bool kQ8, bool kSplit>
+__device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX64,
+                                             const CUtensorMap& tmX16,
+                                             const CUtensorMap& tmX64lo,
+                                             const CUtensorMap& tmX16lo, const TcParams& p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmX64);
     prefetch_tensormap(&tmX16);
-    if (p.split) {
+    if (kSplit) {
       prefetch_tensormap(&tmX64lo);
       prefetch_tensormap(&tmX16lo);
     }
@@ -474,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
   const int nb64 = n_tot / 64;
   const int nbox1 = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // boxes of one panel part
-  const int nbox = nbox1 * (p.split ? 2 : 1);                 // panel boxes per stage
-  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (p.split ? 2 : 1);
+  const int nbox = nbox1 * (kSplit ? 2 : 1);                  // panel boxes per stage
+  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (kSplit ? 2 : 1);
   // warp-collective: iterations first, first + step, ...
   auto produce = [&](int first, int step) {
     int issued = -1;  // last iteration issued
@@ -499,12 +502,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       const int x = ((g0 + i) % kbt) * kBK;
-      const int part = b >= nbox1 ? 1 : 0;  // 1: the remainder panel
-      const int bb = b - part * nbox1;
-      const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
-      const CUtensorMap* m = part ? (bb < nb64 ? &tmX64lo : &tmX16lo)
-                                  : (bb < nb64 ? &tmX64 : &tmX16);
-      tma_load_2d(st + kXOff + part * n_tot * 128 + r * 128, m, x, lane0 + r, full0 + 8 * s);
+      if (kSplit && b >= nbox1) {  // the remainder panel
+        const int bb = b - nbox1;
+        const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
+        tma_load_2d(st + kXOff + n_tot * 128 + r * 128, bb < nb64 ? &tmX64lo : &tmX16lo, x,
+                    lane0 + r, full0 + 8 * s);
+        return;
+      }
+      const int r = b < nb64 ? b * 64 : nb64 * 64 + (b - nb64) * kXBoxRows;
+      tma_load_2d(st + kXOff + r * 128, b < nb64 ? &tmX64 : &tmX16, x, lane0 + r, full0 + 8 * s);
     };
     // Programmatic dependent launch: the weight tiles do not depend on the
     // predecessor kernel, so they start before waiting for it; the panel is
@@ -586,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (acc || kk > 0) ? 1u : 0u);
-            if (p.split) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+            if (kSplit) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
           }
           acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
@@ -642,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
           if (whole) {
-            emit_chunk(p, t, row_local, lane0, lanes, cc, v, xbuf);
+            emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
           } else if (p.cs) {  // the partial tile stays in this block's ring
             float4* dst = reinterpret_cast<float4*>(
                 reinterpret_cast<float*>(smem) + row_local * (n_tot + 4) + cc);
@@ -668,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         epi_bar();
         if (s_last) {
           __threadfence();
-          reduce_tile(p, t, tp, lane0, lanes);
+          reduce_tile<kSplit>(p, t, tp, lane0, lanes);
           if (threadIdx.x == 0) *ctr = 0;  // ready for the next launch
         }
       }
@@ -711,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               }
             }
           }
-          emit_chunk(p, t_first, row_local, lane0, lanes, c0, v, xbuf);
+          emit_chunk<kSplit>(p, t_first, row_local, lane0, lanes, c0, v, xbuf);
         }
       }
     }
@@ -724,6 +730,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                  : "memory");
   }
   TraceSmem::end(s_tr, TR_GEMM + p.epi);
+}
+
+// The kernels: the plain one takes the maps of the panel only, the split one
+// those of its remainder too.
+template <bool kQ8>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
+              const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
+  gemm_tc_body<kQ8, false>(tmW, tmX64, tmX16, tmX64, tmX16, p);
+}
+template <bool kQ8>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_gemm_tc_split(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmX64,
+                    const __grid_constant__ CUtensorMap tmX16,
+                    const __grid_constant__ CUtensorMap tmX64lo,
+                    const __grid_constant__ CUtensorMap tmX16lo, const TcParams p) {
+  gemm_tc_body<kQ8, true>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -805,21 +829,25 @@ int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_byt
   return st;
 }
 
-template <bool kQ8>
+template <bool kQ8, bool kSplit>
 int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                 const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p0,
                 cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_gemm_tc<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAttr) != cudaSuccess)
+    const cudaError_t e =
+        kSplit ? cudaFuncSetAttribute(k_gemm_tc_split<kQ8>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr)
+               : cudaFuncSetAttribute(k_gemm_tc<kQ8>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr);
+    if (e != cudaSuccess)
       return 0;  // the launch below then fails and the caller reports it
     attr_set = true;
   }
   TcParams p = p0;
   int smem = 0;
   const int grid = p.P * p.groups;
-  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, p.split, &p.stage_bytes, &smem);
+  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, kSplit, &p.stage_bytes, &smem);
   // producer warps of single-piece blocks: up to 4, dividing the stage count
   p.prod_warps = 1;
   if (!kQ8) {
@@ -841,11 +869,19 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
         cs <= 8 && (size_t)kBM * (n_tot + 4) * 4 <= (size_t)p.stages * p.stage_bytes)
       p.cs = cs;
   }
-  if (p.cs)
-    launch_k_cluster(k_gemm_tc<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16, tmX64lo,
-                     tmX16lo, p);
-  else
-    launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
+  if (kSplit) {
+    if (p.cs)
+      launch_k_cluster(k_gemm_tc_split<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16,
+                       tmX64lo, tmX16lo, p);
+    else
+      launch_k(k_gemm_tc_split<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo,
+               tmX16lo, p);
+  } else {
+    if (p.cs)
+      launch_k_cluster(k_gemm_tc<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16, p);
+    else
+      launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
+  }
   return 1;
 }
 
@@ -879,14 +915,16 @@ __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __rest
 int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                    const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                    cudaStream_t s) {
-  return launch_impl<false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+  return p.split ? launch_impl<false, true>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
+                 : launch_impl<false, false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
 int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                       const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
                       cudaStream_t s) {
   // the W map is unused
-  return launch_impl<true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+  return p.split ? launch_impl<true, true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
+                 : launch_impl<true, false>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
 }
 
 namespace {
