@@ -36,6 +36,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct TcW {
   CUtensorMap tm;
   int m_tiles = 0, P = 1;  // row tiles, stream-K width
+  int kc = 1;              // short K: equal K splits of a tile (P = m_tiles * kc)
   int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
   __half* q8_scales = nullptr;
 };
@@ -83,6 +84,9 @@ int trace_release(const fs_handle* h) {
   g_trace_owner = nullptr;
   return ok ? FS_OK : FS_ERR_CUDA;
 }
+
+// Calls with at most this many lanes run short-K splits as separate blocks.
+constexpr int kSplitCallLanes = 64;
 
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
@@ -586,6 +590,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     auto setup = [&](const Mat& m, TcW* t) -> int {
       t->m_tiles = (m.N + 127) / 128;
       t->P = choose_width(t->m_tiles, m.Kp / 64, B, h->sms);
+      if (m.Kp / 64 < 32 && t->P % t->m_tiles == 0) t->kc = t->P / t->m_tiles;
       if (!tc_width_ok(t->m_tiles, m.Kp / 64, t->P))
         return h->fail(FS_ERR_ARG, "weight matrix too large for the tcgen05 GEMM");
       max_tiles = std::max(max_tiles, t->m_tiles);
@@ -755,6 +760,22 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.lanes_total = n; p.sms = h->sms;
     tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups);
     p.tmem_cols = tc_tmem_cols(p.lg);
+    p.kc = 1;
+    // A short-K matrix has kc K splits per tile. Small calls run them as
+    // kc blocks per tile (partial tiles summed in a thread-block cluster);
+    // larger calls give each block a whole tile with kc chunk accumulators
+    // summed in the same order (same bits, no partials leave the block).
+    if (T.kc > 1 && n > kSplitCallLanes) {
+      int lg = 0, groups = 0;
+      tc_lane_groups(n, T.m_tiles, h->sms, &lg, &groups);
+      if (tc_tmem_cols(T.kc * lg) <= 512) {
+        p.P = T.m_tiles; p.kc = T.kc; p.lg = lg; p.groups = groups;
+        p.tmem_cols = tc_tmem_cols(T.kc * lg);
+      }
+    }
+    // the cluster reduction pays where partial tiles are large or K short;
+    // long-K splits of small lane groups sum through the workspace
+    p.cs_off = (p.kb_total >= 32 && p.lg < 32) ? 1 : 0;
     p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
     p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
@@ -1443,7 +1464,7 @@ int fs_device_error(fs_handle* h, int32_t* code_out) {
 namespace {
 // tcgen05 GEMM of the test hooks with stream-K width P and its own workspace.
 int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, float* Y, int P,
-                 int reps, double* ms_out, cudaStream_t s, int cs_off = 0) {
+                 int reps, double* ms_out, cudaStream_t s, int cs_off = 0, int kc = 1) {
   using namespace fsk;
   CUtensorMap tw, tx, tx64;
   if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
@@ -1470,7 +1491,8 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
     p.m_tiles = m_tiles; p.P = P; p.kb_total = K / 64;
     p.lanes_total = B; p.sms = sms;
     tc_lane_groups(B, P, sms, &p.lg, &p.groups);
-    p.tmem_cols = tc_tmem_cols(p.lg);
+    p.tmem_cols = tc_tmem_cols(kc * p.lg);
+    p.kc = kc;
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
     p.cs_off = cs_off;
@@ -1521,7 +1543,7 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
                  float* Y, int32_t splits, int32_t path, void* stream) {
   using namespace fsk;
   if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
-      splits > K / 64 || splits > 8 || path < 0 || path > 2)
+      splits > K / 64 || splits > 8 || path < 0 || path > 3)
     return FS_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == 0) {
@@ -1536,8 +1558,17 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
   }
   // stream-K width m_tiles * splits: every block's range is the K split of
   // one tile, so the pieces are exactly the `splits` K splits
-  return gemm_tc_hook(W, N, K, X, B, Y, ((N + 127) / 128) * splits, 0, nullptr, s,
-                      path == 2 ? 1 : 0);
+  const int m_tiles = (N + 127) / 128;
+  if (path == 3) {  // whole tiles, `splits` chunk accumulators per tile
+    int lg = 0, groups = 0, sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FS_ERR_CUDA;
+    tc_lane_groups(B, m_tiles, sms, &lg, &groups);
+    if (tc_tmem_cols(splits * lg) > 512) return FS_ERR_ARG;
+    return gemm_tc_hook(W, N, K, X, B, Y, m_tiles, 0, nullptr, s, 0, splits);
+  }
+  return gemm_tc_hook(W, N, K, X, B, Y, m_tiles * splits, 0, nullptr, s, path == 2 ? 1 : 0);
 }
 
 int fs_gemm_bf16_width(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int32_t B,

@@ -424,6 +424,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   const int n_it = g1 - g0;  // >= 1 because P <= T
   const int t_first = g0 / kbt;
   const int n_pieces = (g1 - 1) / kbt - t_first + 1;
+  const int kc = p.P == p.m_tiles && p.kc > 1 ? p.kc : 1;  // K chunks of a whole tile
   const int S = p.stages;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
@@ -574,7 +575,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           tc_fence_after();
         }
         bool acc = false;
+        // whole-tile K chunks: accumulator j at columns j * n_tot
+        int chunk = 0, next_b = kc > 1 ? kbt / kc : INT_MAX;
+        uint32_t dacc = tmem;
         for (; ok && g0 + i < pe; ++i) {
+          if (kc > 1 && (g0 + i) - t_first * kbt == next_b) {
+            ++chunk;
+            next_b = ((chunk + 1) * kbt) / kc;
+            dacc = tmem + (uint32_t)(chunk * n_tot);
+            acc = false;
+          }
           const int s = i % S;
           const uint32_t ph = (uint32_t)(i / S) & 1u;
           if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
@@ -590,9 +600,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           const uint32_t b1 = b0 + (uint32_t)n_tot * 128;  // remainder panel
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+            mma_bf16(dacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (acc || kk > 0) ? 1u : 0u);
-            if (kSplit) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+            if (kSplit) mma_bf16(dacc, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
           }
           acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
@@ -635,7 +645,24 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       if (s_stop[q & 1]) break;
       const bool whole = pb == tb && pe == tb + kbt;
       const int slot = q == 0 ? 0 : 1;
-      for (int c0 = 0; c0 < n_tot; c0 += 32) {  // two 16-lane loads in flight
+      if (kc > 1) {  // whole tile in K chunks: sum the chunk accumulators in order
+        for (int cc = 0; cc < n_tot; cc += 16) {
+          float v[16];
+          uint32_t r[16];
+          tmem_ld16(trow + (uint32_t)cc, r);
+          tmem_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          for (int k = 1; k < kc; ++k) {
+            tmem_ld16(trow + (uint32_t)(k * n_tot + cc), r);
+            tmem_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+          }
+          emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
+        }
+      }
+      for (int c0 = 0; kc == 1 && c0 < n_tot; c0 += 32) {  // two 16-lane loads in flight
         uint32_t r[2][16];
         tmem_ld16(trow + (uint32_t)c0, r[0]);
         if (c0 + 16 < n_tot) tmem_ld16(trow + (uint32_t)(c0 + 16), r[1]);
