@@ -391,7 +391,14 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
 
 // kSplit: the panel has a remainder part (TcParams::split), two MMAs per
 // k-step; a compile-time switch so that the plain kernel carries none of it.
-template <bool kQ8, bool kSplit>
+// How a launch reduces K: plain (whole tiles, or stream-K ranges summed
+// through the workspace), cluster (the K splits of a tile are the blocks
+// of a thread-block cluster) or chunks (whole tiles with TcParams::kc chunk
+// accumulators). A compile-time switch, so that each kernel carries only
+// its own reduction.
+enum GemmMode { GM_PLAIN = 0, GM_CLUSTER = 1, GM_CHUNKS = 2 };
+
+template <bool kQ8, bool kSplit, int kMode>
 __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX64,
                                              const CUtensorMap& tmX16,
                                              const CUtensorMap& tmX64lo,
@@ -410,10 +417,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   // cluster reduction: the cs K splits of one (row tile, lane group) are
   // consecutive blocks, one cluster; otherwise the lane groups of one
   // stream-K range are consecutive (they share its weight tiles in L2)
-  const int cs_rank = p.cs ? (int)(blockIdx.x % p.cs) : 0;
-  const int cs_unit = p.cs ? (int)(blockIdx.x / p.cs) : 0;  // tile * groups + group
-  const int group = p.cs ? cs_unit % p.groups : (int)(blockIdx.x % p.groups);
-  const int cblk = p.cs ? (cs_unit / p.groups) * p.cs + cs_rank  // stream-K block
+  constexpr bool kCluster = kMode == GM_CLUSTER;
+  const int cs = kCluster ? p.cs : 0;
+  const int cs_rank = kCluster ? (int)(blockIdx.x % cs) : 0;
+  const int cs_unit = kCluster ? (int)(blockIdx.x / cs) : 0;  // tile * groups + group
+  const int group = kCluster ? cs_unit % p.groups : (int)(blockIdx.x % p.groups);
+  const int cblk = kCluster ? (cs_unit / p.groups) * cs + cs_rank  // stream-K block
                         : (int)(blockIdx.x / p.groups);
   const int lane0 = group * p.lg;
   const int lanes = min(p.lg, p.lanes_total - lane0);
@@ -424,7 +433,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   const int n_it = g1 - g0;  // >= 1 because P <= T
   const int t_first = g0 / kbt;
   const int n_pieces = (g1 - 1) / kbt - t_first + 1;
-  const int kc = p.P == p.m_tiles && p.kc > 1 ? p.kc : 1;  // K chunks of a whole tile
+  const int kc = kMode == GM_CHUNKS ? p.kc : 1;  // K chunks of a whole tile
   const int S = p.stages;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
@@ -676,7 +685,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
           if (whole) {
             emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
-          } else if (p.cs) {  // the partial tile stays in this block's ring
+          } else if (kCluster) {  // the partial tile stays in this block's ring
             float4* dst = reinterpret_cast<float4*>(
                 reinterpret_cast<float*>(smem) + row_local * (n_tot + 4) + cc);
 #pragma unroll
@@ -692,7 +701,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       }
       tc_fence_before();
       mbar_arrive(tempty);  // the accumulator may be overwritten by the next piece
-      if (!whole && !p.cs) {
+      if (!whole && !kCluster) {
         __threadfence();
         epi_bar();
         const TilePieces tp = tile_pieces(p, t);
@@ -709,7 +718,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   }
   tc_fence_before();
   __syncthreads();
-  if (p.cs) {
+  if (kCluster) {
     // Every thread of every block of the cluster passes both barriers,
     // whatever happened before (an aborted block still arrives), so no
     // block waits on another forever. After the first, every block's
@@ -720,13 +729,13 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
     cluster_sync();
     if (warp < 4) {
       int bad = 0;
-      for (int r = 0; r < p.cs; ++r) bad |= ld_dsmem_s32(dsmem_addr(smem_u32(&s_abort), r));
+      for (int r = 0; r < cs; ++r) bad |= ld_dsmem_s32(dsmem_addr(smem_u32(&s_abort), r));
       if (!bad) {
         const int row_local = warp * 32 + lane;
         const uint32_t mine = smem_u32(smem) + (uint32_t)(row_local * (n_tot + 4)) * 4u;
-        for (int c0 = cs_rank * 16; c0 < n_tot; c0 += p.cs * 16) {
+        for (int c0 = cs_rank * 16; c0 < n_tot; c0 += cs * 16) {
           float v[16];
-          for (int r = 0; r < p.cs; ++r) {
+          for (int r = 0; r < cs; ++r) {
             const uint32_t src = dsmem_addr(mine + (uint32_t)c0 * 4u, r);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -761,20 +770,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
 
 // The kernels: the plain one takes the maps of the panel only, the split one
 // those of its remainder too.
-template <bool kQ8>
+template <bool kQ8, int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
               const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
-  gemm_tc_body<kQ8, false>(tmW, tmX64, tmX16, tmX64, tmX16, p);
+  gemm_tc_body<kQ8, false, kMode>(tmW, tmX64, tmX16, tmX64, tmX16, p);
 }
-template <bool kQ8>
+template <bool kQ8, int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc_split(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX64,
                     const __grid_constant__ CUtensorMap tmX16,
                     const __grid_constant__ CUtensorMap tmX64lo,
                     const __grid_constant__ CUtensorMap tmX16lo, const TcParams p) {
-  gemm_tc_body<kQ8, true>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
+  gemm_tc_body<kQ8, true, kMode>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -856,21 +865,38 @@ int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_byt
   return st;
 }
 
+template <bool kQ8, bool kSplit, int kMode>
+cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmX64,
+                        const CUtensorMap& tmX16, const CUtensorMap& tmX64lo,
+                        const CUtensorMap& tmX16lo, const TcParams& p, int grid, int smem,
+                        cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        kSplit ? cudaFuncSetAttribute(k_gemm_tc_split<kQ8, kMode>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr)
+               : cudaFuncSetAttribute(k_gemm_tc<kQ8, kMode>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr);
+    if (e != cudaSuccess) return e;  // the caller's error check reports it
+    attr_set = true;
+  }
+  if (kSplit) {
+    if (kMode == GM_CLUSTER)
+      return launch_k_cluster(k_gemm_tc_split<kQ8, kMode>, grid, kThreads, smem, s, p.cs, tmW,
+                              tmX64, tmX16, tmX64lo, tmX16lo, p);
+    return launch_k(k_gemm_tc_split<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX64, tmX16,
+                    tmX64lo, tmX16lo, p);
+  }
+  if (kMode == GM_CLUSTER)
+    return launch_k_cluster(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, p.cs, tmW, tmX64,
+                            tmX16, p);
+  return launch_k(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
+}
+
 template <bool kQ8, bool kSplit>
 int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
                 const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p0,
                 cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        kSplit ? cudaFuncSetAttribute(k_gemm_tc_split<kQ8>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr)
-               : cudaFuncSetAttribute(k_gemm_tc<kQ8>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAttr);
-    if (e != cudaSuccess)
-      return 0;  // the launch below then fails and the caller reports it
-    attr_set = true;
-  }
   TcParams p = p0;
   int smem = 0;
   const int grid = p.P * p.groups;
@@ -892,23 +918,17 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
     const int n_tot = (p.lg + 15) & ~15;
     const int cs = p.P / p.m_tiles;
     if (tc_cluster_reduce() && !p.cs_off && p.epi != EPI_ARGMAX && p.P % p.m_tiles == 0 &&
-        cs >= 2 &&
-        cs <= 8 && (size_t)kBM * (n_tot + 4) * 4 <= (size_t)p.stages * p.stage_bytes)
+        cs >= 2 && cs <= 8 && (size_t)kBM * (n_tot + 4) * 4 <= (size_t)p.stages * p.stage_bytes)
       p.cs = cs;
   }
-  if (kSplit) {
-    if (p.cs)
-      launch_k_cluster(k_gemm_tc_split<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16,
-                       tmX64lo, tmX16lo, p);
-    else
-      launch_k(k_gemm_tc_split<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, tmX64lo,
-               tmX16lo, p);
-  } else {
-    if (p.cs)
-      launch_k_cluster(k_gemm_tc<kQ8>, grid, kThreads, smem, s, p.cs, tmW, tmX64, tmX16, p);
-    else
-      launch_k(k_gemm_tc<kQ8>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
-  }
+  const bool chunks = p.kc > 1 && p.P == p.m_tiles;
+  if (!chunks) p.kc = 1;
+  if (p.cs)
+    launch_mode<kQ8, kSplit, GM_CLUSTER>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
+  else if (chunks)
+    launch_mode<kQ8, kSplit, GM_CHUNKS>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
+  else
+    launch_mode<kQ8, kSplit, GM_PLAIN>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
   return 1;
 }
 
