@@ -657,16 +657,22 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       if (kc > 1) {  // whole tile in K chunks: sum the chunk accumulators in order
         for (int cc = 0; cc < n_tot; cc += 16) {
           float v[16];
-          uint32_t r[16];
-          tmem_ld16(trow + (uint32_t)cc, r);
+          uint32_t r[2][16];  // two chunks' loads in flight
+          tmem_ld16(trow + (uint32_t)cc, r[0]);
+          tmem_ld16(trow + (uint32_t)(n_tot + cc), r[1]);
           tmem_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          for (int k = 1; k < kc; ++k) {
-            tmem_ld16(trow + (uint32_t)(k * n_tot + cc), r);
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[0][j]) + __uint_as_float(r[1][j]);
+          for (int k = 2; k < kc; k += 2) {
+            tmem_ld16(trow + (uint32_t)(k * n_tot + cc), r[0]);
+            if (k + 1 < kc) tmem_ld16(trow + (uint32_t)((k + 1) * n_tot + cc), r[1]);
             tmem_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[0][j]);
+            if (k + 1 < kc) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[1][j]);
+            }
           }
           emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
         }
