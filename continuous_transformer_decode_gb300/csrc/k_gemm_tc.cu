@@ -439,7 +439,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S),
                  conv0 = smem_u32(bars + 2 * S), tfull = smem_u32(bars + 3 * S),
-                 tempty = smem_u32(bars + 3 * S + 1);
+                 tempty = smem_u32(bars + 3 * S + 1), tready = smem_u32(bars + 3 * S + 2);
   constexpr int kXOff = kQ8 ? kQ8XOff : kWTileBytes;
   const uint32_t ncols = p.tmem_cols;
 
@@ -458,21 +458,13 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
     }
     mbar_init(tfull, 1);     // the MMA issuer's commit at the end of a piece
     mbar_init(tempty, 128);  // every epilogue thread, after reading TMEM
+    mbar_init(tready, 1);    // the MMA warp, once it holds its TMEM columns
     mbar_init_fence();
     s_abort = 0;
     s_last = 0;
   }
-  if (warp == 5) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&s_tmem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  __syncthreads();  // barriers initialised
+  uint32_t tmem = 0;  // TMEM base, known to the MMA warp and (after tready) the epilogue
   // TMA producers. The copies one thread issues complete one after another
   // (about half a microsecond each, whatever their size), so copies are
   // spread over lanes: before the wait for the predecessor, one lane per
@@ -569,6 +561,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   if (warp == 4) {
     if (!warp_prod) produce(0, 1);
   } else if (warp == 5) {
+    // TMEM is taken only now, after the preceding kernel has finished (the
+    // wait above): a block brought in early by programmatic dependent launch
+    // holds no columns while it waits, so it never stalls the allocation of
+    // the running kernel's blocks, nor does its weight prefetch wait for one.
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tready);
+    tc_fence_after();
+    tmem = *(volatile uint32_t*)&s_tmem;
     if (lane == 0) {  // ---- MMA issuer: one TMEM accumulation per piece
       bool ok = true;
       int i = 0;
@@ -622,6 +628,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   } else {  // ---- warps 0-3: Q8_0 dequantisation of each piece, then its epilogue
     if (warp_prod && warp < npw) produce(warp, npw);
     const int row_local = warp * 32 + lane;
+    if (!mbar_wait(tready, 0)) {  // the MMA warp's columns
+      atomicExch(p.err, 7);
+      s_abort = 1;
+    }
+    tc_fence_after();
+    tmem = *(volatile uint32_t*)&s_tmem;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     int i = 0;
     for (int q = 0; q < n_pieces; ++q) {
@@ -863,11 +875,11 @@ int smem_budget() {
 }
 int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_bytes) {
   const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128 * (split ? 2 : 1);
-  const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 2);
+  const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 3);
   const int budget = smem_budget() - fixed;
   const int st = std::max(2, std::min(max_stages(), budget / sb));
   *stage_bytes = sb;
-  *smem_bytes = 1024 + st * sb + kXbufBytes + 8 * (3 * st + 2);
+  *smem_bytes = 1024 + st * sb + kXbufBytes + 8 * (3 * st + 3);
   return st;
 }
 
@@ -913,7 +925,7 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
     p.prod_warps = p.stages >= 4 ? 4 : p.stages;
     if (p.stages % p.prod_warps) {
       p.stages -= p.stages % p.prod_warps;
-      smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 2);
+      smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 3);
     }
   }
   // cluster reduction when every stream-K range is one of cs <= 8 equal K
