@@ -310,31 +310,42 @@ def run_ours(args, wl, ws, rank, local):
         timeline["records"] = int(appended)
         print(tr.table(timeline), file=sys.stderr)
 
-    # ---- B sweep on the same handle (device-timed, like `value`)
+    fs.fs_destroy(h)
+
+    # ---- B sweep, device-timed like `value`: each B on the workload's handle
+    # (its lane capacity) and, below it, on a handle sized to B (the lane
+    # capacity sets the GEMMs' K splits: a small handle splits short K)
     sweep = []
     if not args.no_sweep and "ctx" not in wl:
+        Wsw = gpu_weights(cfg, wl["wdtype"])
         for Bs in [b for b in (1, 4, 16, 64, 256, 512, 960) if b <= B]:
-            for k in range(B):
-                fs.fs_lane_reset(h, k)
-            ls = np.arange(Bs, dtype=np.int32)
-            ps_ = np.zeros(Bs, dtype=np.int32)
-            for t in range(prompt):
-                fs.fs_decode_step_batch(h, ls, ps_, prompts[:Bs, t])
-            tk_ = prompts[:Bs, -1].astype(np.int32).copy()
-            for _ in range(2):
-                fs.fs_decode_step_greedy(h, ls, ps_, tk_, dtok[:Bs])
-            torch.cuda.synchronize()
-            k_sw = 6
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            for _ in range(k_sw):
-                fs.fs_decode_step_greedy(h, ls, ps_, tk_, dtok[:Bs])
-            a1.record(stream)
-            torch.cuda.synchronize()
-            ms_sw = a0.elapsed_time(a1) / k_sw
-            sweep.append({"lanes": Bs, "ms_per_step": ms_sw, "tok_s": Bs / (ms_sw / 1e3),
-                          "positions": f"{prompt + 2}..{prompt + 2 + k_sw}"})
-    fs.fs_destroy(h)
+            for cap in sorted({B, Bs}, reverse=True):
+                hs, _, _ = make_handle(cfg, wl, cap, prompt + 12, W=Wsw)
+                try:
+                    fs.fs_set_stream(hs, stream)
+                    ls = np.arange(Bs, dtype=np.int32)
+                    ps_ = np.zeros(Bs, dtype=np.int32)
+                    for t in range(prompt):
+                        fs.fs_decode_step_batch(hs, ls, ps_, prompts[:Bs, t])
+                    tk_ = prompts[:Bs, -1].astype(np.int32).copy()
+                    for _ in range(2):
+                        fs.fs_decode_step_greedy(hs, ls, ps_, tk_, dtok[:Bs])
+                    torch.cuda.synchronize()
+                    k_sw = 6
+                    a0 = torch.cuda.Event(enable_timing=True)
+                    a1 = torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    for _ in range(k_sw):
+                        fs.fs_decode_step_greedy(hs, ls, ps_, tk_, dtok[:Bs])
+                    a1.record(stream)
+                    torch.cuda.synchronize()
+                finally:
+                    fs.fs_destroy(hs)
+                ms_sw = a0.elapsed_time(a1) / k_sw
+                sweep.append({"lanes": Bs, "handle_lanes": cap, "ms_per_step": ms_sw,
+                              "tok_s": Bs / (ms_sw / 1e3),
+                              "positions": f"{prompt + 2}..{prompt + 2 + k_sw}"})
+        del Wsw
 
     # ---- aggregate over ranks (max time)
     ms, e2e_s = max_over_ranks([ms, e2e_s], ws, "cuda")

@@ -36,7 +36,6 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct TcW {
   CUtensorMap tm;
   int m_tiles = 0, P = 1;  // row tiles, stream-K width
-  int kc = 1;              // short K: equal K splits of a tile (P = m_tiles * kc)
   int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
   __half* q8_scales = nullptr;
 };
@@ -85,8 +84,8 @@ int trace_release(const fs_handle* h) {
   return ok ? FS_OK : FS_ERR_CUDA;
 }
 
-// Calls with at most this many lanes run short-K splits as separate blocks.
-constexpr int kSplitCallLanes = 64;
+// Handles of at most this many lanes split short-K matrices.
+constexpr int kSplitHandleLanes = 64;
 
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
@@ -104,11 +103,13 @@ int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
     return m_tiles * std::max(1, std::min(kb_total, 2 * sms / m_tiles));
   const bool narrow = max_lanes <= 32;
   int s = narrow ? (13 * sms + 5 * m_tiles) / (10 * m_tiles) : (85 * sms) / (100 * m_tiles);
-  // short K (fewer than 32 k-blocks, e.g. a 576- or 1536-wide input): splits
-  // of at least 3 k-blocks, whose partial tiles sum inside a thread-block
-  // cluster; longer K: the splits the workspace reduction was timed with
-  const int cap = kb_total < 32 && tc_cluster_reduce() ? kb_total / 3
-                                                       : kb_total / (narrow ? 8 : 32);
+  // short K (fewer than 32 k-blocks, e.g. a 576- or 1536-wide input) on
+  // handles of at most 64 lanes: splits of at least 3 k-blocks, whose partial
+  // tiles sum inside a thread-block cluster; otherwise the splits the
+  // workspace reduction was timed with (none for short K)
+  const int cap = kb_total < 32 && max_lanes <= kSplitHandleLanes && tc_cluster_reduce()
+                      ? kb_total / 3
+                      : kb_total / (narrow ? 8 : 32);
   s = std::min(s, std::min(8, cap));
   return m_tiles * std::max(1, s);
 }
@@ -590,7 +591,6 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     auto setup = [&](const Mat& m, TcW* t) -> int {
       t->m_tiles = (m.N + 127) / 128;
       t->P = choose_width(t->m_tiles, m.Kp / 64, B, h->sms);
-      if (m.Kp / 64 < 32 && t->P % t->m_tiles == 0) t->kc = t->P / t->m_tiles;
       if (!tc_width_ok(t->m_tiles, m.Kp / 64, t->P))
         return h->fail(FS_ERR_ARG, "weight matrix too large for the tcgen05 GEMM");
       max_tiles = std::max(max_tiles, t->m_tiles);
@@ -760,19 +760,6 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.lanes_total = n; p.sms = h->sms;
     tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups);
     p.tmem_cols = tc_tmem_cols(p.lg);
-    p.kc = 1;
-    // A short-K matrix has kc K splits per tile. Small calls run them as
-    // kc blocks per tile (partial tiles summed in a thread-block cluster);
-    // larger calls give each block a whole tile with kc chunk accumulators
-    // summed in the same order (same bits, no partials leave the block).
-    if (T.kc > 1 && n > kSplitCallLanes) {
-      int lg = 0, groups = 0;
-      tc_lane_groups(n, T.m_tiles, h->sms, &lg, &groups);
-      if (tc_tmem_cols(T.kc * lg) <= 512) {
-        p.P = T.m_tiles; p.kc = T.kc; p.lg = lg; p.groups = groups;
-        p.tmem_cols = tc_tmem_cols(T.kc * lg);
-      }
-    }
     // the cluster reduction pays where partial tiles are large or K short;
     // long-K splits of small lane groups sum through the workspace
     p.cs_off = (p.kb_total >= 32 && p.lg < 32) ? 1 : 0;
@@ -1464,7 +1451,7 @@ int fs_device_error(fs_handle* h, int32_t* code_out) {
 namespace {
 // tcgen05 GEMM of the test hooks with stream-K width P and its own workspace.
 int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, float* Y, int P,
-                 int reps, double* ms_out, cudaStream_t s, int cs_off = 0, int kc = 1) {
+                 int reps, double* ms_out, cudaStream_t s, int cs_off = 0) {
   using namespace fsk;
   CUtensorMap tw, tx, tx64;
   if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
@@ -1491,8 +1478,7 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
     p.m_tiles = m_tiles; p.P = P; p.kb_total = K / 64;
     p.lanes_total = B; p.sms = sms;
     tc_lane_groups(B, P, sms, &p.lg, &p.groups);
-    p.tmem_cols = tc_tmem_cols(kc * p.lg);
-    p.kc = kc;
+    p.tmem_cols = tc_tmem_cols(p.lg);
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
     p.cs_off = cs_off;
@@ -1543,7 +1529,7 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
                  float* Y, int32_t splits, int32_t path, void* stream) {
   using namespace fsk;
   if (!W || !X || !Y || N < 1 || K < 64 || K % 64 || B < 1 || splits < 1 ||
-      splits > K / 64 || splits > 8 || path < 0 || path > 3)
+      splits > K / 64 || splits > 8 || path < 0 || path > 2)
     return FS_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == 0) {
@@ -1559,15 +1545,6 @@ int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X, int
   // stream-K width m_tiles * splits: every block's range is the K split of
   // one tile, so the pieces are exactly the `splits` K splits
   const int m_tiles = (N + 127) / 128;
-  if (path == 3) {  // whole tiles, `splits` chunk accumulators per tile
-    int lg = 0, groups = 0, sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return FS_ERR_CUDA;
-    tc_lane_groups(B, m_tiles, sms, &lg, &groups);
-    if (tc_tmem_cols(splits * lg) > 512) return FS_ERR_ARG;
-    return gemm_tc_hook(W, N, K, X, B, Y, m_tiles, 0, nullptr, s, 0, splits);
-  }
   return gemm_tc_hook(W, N, K, X, B, Y, m_tiles * splits, 0, nullptr, s, path == 2 ? 1 : 0);
 }
 

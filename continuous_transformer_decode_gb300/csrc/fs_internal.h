@@ -300,12 +300,6 @@ struct TcParams {
   // order of the workspace reduction, so the bits are the same)
   int cs;
   int cs_off;      // 1: never the cluster reduction (the caller's workspace serves)
-  // K chunks of a whole-tile block (P == m_tiles): its k-blocks form kc
-  // chunks with the boundaries of kc equal K splits (j * kb_total / kc),
-  // each accumulated in its own TMEM columns from zero and summed in chunk
-  // order by the epilogue: the same partial tiles, added in the same order,
-  // as the kc splits of P = m_tiles * kc blocks, so the same bits.
-  int kc;
 };
 // Per lane, the argmax over the tiles' (max, index) pairs of an EPI_ARGMAX
 // launch (lowest index on ties): tokens_out[b] for b < B.

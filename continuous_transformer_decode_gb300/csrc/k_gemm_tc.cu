@@ -392,11 +392,10 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
 // kSplit: the panel has a remainder part (TcParams::split), two MMAs per
 // k-step; a compile-time switch so that the plain kernel carries none of it.
 // How a launch reduces K: plain (whole tiles, or stream-K ranges summed
-// through the workspace), cluster (the K splits of a tile are the blocks
-// of a thread-block cluster) or chunks (whole tiles with TcParams::kc chunk
-// accumulators). A compile-time switch, so that each kernel carries only
-// its own reduction.
-enum GemmMode { GM_PLAIN = 0, GM_CLUSTER = 1, GM_CHUNKS = 2 };
+// through the workspace) or cluster (the K splits of a tile are the blocks
+// of a thread-block cluster). A compile-time switch, so that each kernel
+// carries only its own reduction.
+enum GemmMode { GM_PLAIN = 0, GM_CLUSTER = 1 };
 
 template <bool kQ8, bool kSplit, int kMode>
 __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX64,
@@ -433,7 +432,6 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   const int n_it = g1 - g0;  // >= 1 because P <= T
   const int t_first = g0 / kbt;
   const int n_pieces = (g1 - 1) / kbt - t_first + 1;
-  const int kc = kMode == GM_CHUNKS ? p.kc : 1;  // K chunks of a whole tile
   const int S = p.stages;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
@@ -590,16 +588,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           tc_fence_after();
         }
         bool acc = false;
-        // whole-tile K chunks: accumulator j at columns j * n_tot
-        int chunk = 0, next_b = kc > 1 ? kbt / kc : INT_MAX;
-        uint32_t dacc = tmem;
         for (; ok && g0 + i < pe; ++i) {
-          if (kc > 1 && (g0 + i) - t_first * kbt == next_b) {
-            ++chunk;
-            next_b = ((chunk + 1) * kbt) / kc;
-            dacc = tmem + (uint32_t)(chunk * n_tot);
-            acc = false;
-          }
           const int s = i % S;
           const uint32_t ph = (uint32_t)(i / S) & 1u;
           if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
@@ -615,9 +604,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           const uint32_t b1 = b0 + (uint32_t)n_tot * 128;  // remainder panel
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_bf16(dacc, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+            mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (acc || kk > 0) ? 1u : 0u);
-            if (kSplit) mma_bf16(dacc, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+            if (kSplit) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
           }
           acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
@@ -666,30 +655,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       if (s_stop[q & 1]) break;
       const bool whole = pb == tb && pe == tb + kbt;
       const int slot = q == 0 ? 0 : 1;
-      if (kc > 1) {  // whole tile in K chunks: sum the chunk accumulators in order
-        for (int cc = 0; cc < n_tot; cc += 16) {
-          float v[16];
-          uint32_t r[2][16];  // two chunks' loads in flight
-          tmem_ld16(trow + (uint32_t)cc, r[0]);
-          tmem_ld16(trow + (uint32_t)(n_tot + cc), r[1]);
-          tmem_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[0][j]) + __uint_as_float(r[1][j]);
-          for (int k = 2; k < kc; k += 2) {
-            tmem_ld16(trow + (uint32_t)(k * n_tot + cc), r[0]);
-            if (k + 1 < kc) tmem_ld16(trow + (uint32_t)((k + 1) * n_tot + cc), r[1]);
-            tmem_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[0][j]);
-            if (k + 1 < kc) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[1][j]);
-            }
-          }
-          emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
-        }
-      }
-      for (int c0 = 0; kc == 1 && c0 < n_tot; c0 += 32) {  // two 16-lane loads in flight
+      for (int c0 = 0; c0 < n_tot; c0 += 32) {  // two 16-lane loads in flight
         uint32_t r[2][16];
         tmem_ld16(trow + (uint32_t)c0, r[0]);
         if (c0 + 16 < n_tot) tmem_ld16(trow + (uint32_t)(c0 + 16), r[1]);
@@ -939,12 +905,8 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
         cs >= 2 && cs <= 8 && (size_t)kBM * (n_tot + 4) * 4 <= (size_t)p.stages * p.stage_bytes)
       p.cs = cs;
   }
-  const bool chunks = p.kc > 1 && p.P == p.m_tiles;
-  if (!chunks) p.kc = 1;
   if (p.cs)
     launch_mode<kQ8, kSplit, GM_CLUSTER>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
-  else if (chunks)
-    launch_mode<kQ8, kSplit, GM_CHUNKS>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
   else
     launch_mode<kQ8, kSplit, GM_PLAIN>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
   return 1;

@@ -372,11 +372,8 @@ int fs_selftest_bounded_wait(fs_handle* h, int32_t timeout_us, int32_t* code_out
  * 128-row tile (1 <= splits <= min(8, K/64)); the splits of a tile sum
  * through a thread-block cluster where the partial tile fits in shared
  * memory, else through the workspace; path 2 = the same with the workspace
- * reduction always; path 3 = one block per 128-row tile whose k-blocks
- * accumulate as the same `splits` chunks in separate tensor-memory columns,
- * summed in chunk order (FS_ERR_ARG when splits x lanes per group exceeds
- * 512 columns); path 0 = warp-GEMV kernel. Paths 1-3 give the same bits.
- * Allocates its own workspace; runs on
+ * reduction always; path 0 = warp-GEMV kernel. Paths 1 and 2 give the same
+ * bits. Allocates its own workspace; runs on
  * `stream` (NULL = default) and synchronises it. Errors: FS_ERR_ARG,
  * FS_ERR_OOM, FS_ERR_CUDA, FS_ERR_DEVICE (a bounded wait timed out). */
 int fs_gemm_bf16(const uint16_t* W, int32_t N, int32_t K, const uint16_t* X,
