@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <utility>
 
 namespace fsk {
@@ -309,11 +310,22 @@ int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_til
 // limit); a matrix with fewer stream-K blocks than SMs is spread over more
 // groups of at least 32 lanes to fill about two blocks per SM. Groups split
 // N only, so this may depend on the call's lane count.
+// FS_TC_LG_MIN (16..256, a tuning knob read once) is the smallest lane
+// group the fill rule may cut (default 32).
+inline int tc_lg_min() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_LG_MIN");
+    const int x = e ? atoi(e) : 32;
+    return std::max(16, std::min(256, x));
+  }();
+  return v;
+}
 inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups) {
   int g = (n + 255) / 256;
   if (P < sms) {
     const int fill = std::max(1, 2 * sms / P);
-    g = std::max(g, std::min(fill, std::max(1, (n + 31) / 32)));
+    const int m = tc_lg_min();
+    g = std::max(g, std::min(fill, std::max(1, (n + m - 1) / m)));
   }
   const int l = ((n + g - 1) / g + 15) / 16 * 16;
   *lg = l;
