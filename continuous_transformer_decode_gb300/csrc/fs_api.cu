@@ -758,7 +758,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     TcParams p{};
     p.m_tiles = T.m_tiles; p.P = T.P; p.kb_total = W.Kp / 64;
     p.lanes_total = n; p.sms = h->sms;
-    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups);
+    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, h->wtype == W_Q8 ? 32 : 16);
     p.tmem_cols = tc_tmem_cols(p.lg);
     // the cluster reduction pays where partial tiles are large or K short;
     // long-K splits of small lane groups sum through the workspace

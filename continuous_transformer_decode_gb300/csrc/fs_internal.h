@@ -310,21 +310,34 @@ int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_til
 // limit); a matrix with fewer stream-K blocks than SMs is spread over more
 // groups of at least 32 lanes to fill about two blocks per SM. Groups split
 // N only, so this may depend on the call's lane count.
-// FS_TC_LG_MIN (16..256, a tuning knob read once) is the smallest lane
-// group the fill rule may cut (default 32).
-inline int tc_lg_min() {
+// FS_TC_LG_MIN (16..256, a tuning knob read once) overrides the smallest
+// lane group the fill rule may cut (0: the caller's value).
+inline int tc_lg_min(int dflt) {
   static const int v = [] {
     const char* e = getenv("FS_TC_LG_MIN");
-    const int x = e ? atoi(e) : 32;
-    return std::max(16, std::min(256, x));
+    const int x = e ? atoi(e) : 0;
+    return x ? std::max(16, std::min(256, x)) : 0;
+  }();
+  return v ? v : dflt;
+}
+// FS_TC_LG_MAX (16..256, a tuning knob read once) caps the lanes of a group
+// (default 256, the MMA's N limit).
+inline int tc_lg_max() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_LG_MAX");
+    const int x = e ? atoi(e) : 256;
+    return std::max(16, std::min(256, x / 16 * 16));
   }();
   return v;
 }
-inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups) {
-  int g = (n + 255) / 256;
+// lg_min: the smallest group the fill rule may cut (16 for bf16 weights;
+// Q8_0 takes 32, as every group dequantises its weight tiles itself).
+inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups, int lg_min = 16) {
+  const int cap = tc_lg_max();
+  int g = (n + cap - 1) / cap;
   if (P < sms) {
     const int fill = std::max(1, 2 * sms / P);
-    const int m = tc_lg_min();
+    const int m = tc_lg_min(lg_min);
     g = std::max(g, std::min(fill, std::max(1, (n + m - 1) / m)));
   }
   const int l = ((n + g - 1) / g + 15) / 16 * 16;
