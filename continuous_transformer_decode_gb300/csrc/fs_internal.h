@@ -320,12 +320,15 @@ inline int tc_lg_min(int dflt) {
   }();
   return v ? v : dflt;
 }
-// FS_TC_LG_MAX (16..256, a tuning knob read once) caps the lanes of a group
-// (default 256, the MMA's N limit).
+// Lanes of a group are at most 128 (the MMA's N could take 256, but a
+// 256-lane group's stage holds 32 KB of panel next to 16 KB of weights, so
+// only two stages fit the ring: the LM heads of SmolLM2 at 256 lanes and of
+// its Q8_0 form at 960 lanes measured 40.3 -> 38.7 us and 216 -> 179 us).
+// FS_TC_LG_MAX (16..256) overrides it, a tuning knob read once.
 inline int tc_lg_max() {
   static const int v = [] {
     const char* e = getenv("FS_TC_LG_MAX");
-    const int x = e ? atoi(e) : 256;
+    const int x = e ? atoi(e) : 128;
     return std::max(16, std::min(256, x / 16 * 16));
   }();
   return v;
