@@ -34,7 +34,6 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // tcgen05 operand map and the fixed K split of one weight matrix.
 struct TcW {
-  CUtensorMap tm;
   int m_tiles = 0, P = 1;  // row tiles, stream-K width
   int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
   __half* q8_scales = nullptr;
@@ -130,13 +129,8 @@ struct fs_handle {
   Mat embed, head;
   TcW head_tc;
   bool use_tc = false;
-  // tensor maps of one activation panel (boxes of 16 and 64 lanes) and of
-  // its remainder part (act_split)
-  struct PanelMaps {
-    CUtensorMap m16, m64, lo16, lo64;
-  };
-  PanelMaps pm_h, pm_o, pm_a;
   int act_split = 0;
+  bool map_fail = false;  // a GEMM launch could not encode its tensor maps
   int64_t lo_h = 0, lo_o = 0, lo_a = 0;  // remainder offsets (elements; 0: none)
   float* ws = nullptr;
   int* counters = nullptr;
@@ -606,7 +600,8 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         FS_CK(h, cudaStreamSynchronize(h->stream));
         return FS_OK;
       }
-      if (tc_make_map(m.w, m.N, m.Kp, 128, &t->tm)) return h->fail(FS_ERR_CUDA, "tensor map");
+      CUtensorMap tm;  // the launches encode (and keep) their maps; this checks the shape
+      if (tc_make_map(m.w, m.N, m.Kp, 128, 1, &tm)) return h->fail(FS_ERR_CUDA, "tensor map");
       return FS_OK;
     };
     for (auto& L : h->layers) {
@@ -635,19 +630,13 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         h->release((void*)h->head.scales);
       }
     }
-    auto maps = [&](void* panel, int Kp, fs_handle::PanelMaps* m) {
-      const __nv_bfloat16* lo = static_cast<const __nv_bfloat16*>(panel) + (int64_t)B * Kp;
-      if (tc_make_map(panel, B, Kp, 16, &m->m16) || tc_make_map(panel, B, Kp, 64, &m->m64))
-        return 1;
-      if (!h->act_split) {
-        m->lo16 = m->m16;
-        m->lo64 = m->m64;
-        return 0;
-      }
-      return tc_make_map(lo, B, Kp, 16, &m->lo16) || tc_make_map(lo, B, Kp, 64, &m->lo64) ? 1 : 0;
+    auto maps = [&](const void* panel, int Kp, int64_t lo) {
+      CUtensorMap tm;
+      return tc_make_map(panel, B, Kp, 16, 1, &tm) ||
+             (lo && tc_make_map(static_cast<const __nv_bfloat16*>(panel) + lo, B, Kp, 16, 1, &tm));
     };
-    if (maps(h->hpanel, h->Kp_d, &h->pm_h) || maps(h->opanel, h->Kp_q, &h->pm_o) ||
-        maps(h->apanel, h->Kp_f, &h->pm_a))
+    if (maps(h->hpanel, h->Kp_d, h->lo_h) || maps(h->opanel, h->Kp_q, h->lo_o) ||
+        maps(h->apanel, h->Kp_f, h->lo_a))
       return h->fail(FS_ERR_CUDA, "panel tensor map");
     const size_t n_counters = (size_t)max_tiles * ((B + 15) / 16);
     if (h->alloc(&h->ws, std::max<size_t>(ws_elems, 1) * 4) != cudaSuccess ||
@@ -742,8 +731,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     return b;
   };
   // algorithmic bytes: weights once, activations in, outputs out
-  auto gemm = [&](const Mat& W, const TcW& T, const fs_handle::PanelMaps& pm, const void* X,
-                  int epi, float* of, void* ox, int ldo, int n_out) {
+  auto gemm = [&](const Mat& W, const TcW& T, const void* X, int64_t x_lo, int epi, float* of,
+                  void* ox, int ldo, int n_out) {
     double bytes = wbytes(W) + (double)n * W.K * xs;
     bytes += epi == EPI_ARGMAX ? (double)n * T.m_tiles * 8.0
              : epi == EPI_SWIGLU ? (double)n * n_out * xs
@@ -769,14 +758,12 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.am_val = h->am_val; p.am_idx = h->am_idx;
     p.split = h->act_split;
     p.lo_off = epi == EPI_SWIGLU ? h->lo_a : 0;
-    if (h->wtype == W_Q8)
-      h->launch(FS_PROF_GEMM, bytes, [&] {
-        return launch_gemm_tc_q8(pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
-      });
-    else
-      h->launch(FS_PROF_GEMM, bytes, [&] {
-        return launch_gemm_tc(T.tm, pm.m64, pm.m16, pm.lo64, pm.lo16, p, s);
-      });
+    const TcOperands o{W.w, W.N, X, d.max_lanes, W.Kp, x_lo};
+    h->launch(FS_PROF_GEMM, bytes, [&] {
+      const int r = h->wtype == W_Q8 ? launch_gemm_tc_q8(o, p, s) : launch_gemm_tc(o, p, s);
+      if (r < 0) h->map_fail = true;
+      return std::max(r, 0);
+    });
   };
   const double norm_bytes = (double)n * d.d_model * (4.0 * 3 + xs);
   // embedding gather + the first layer's input norm
@@ -791,7 +778,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
         return launch_rmsnorm(h->x, h->y, W.g_attn, n, d.d_model, d.rms_eps, h->hpanel,
                               h->xtype, h->Kp_d, h->lo_h, s);
       });
-    gemm(W.qkv, W.qkv_tc, h->pm_h, h->hpanel, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
+    gemm(W.qkv, W.qkv_tc, h->hpanel, h->lo_h, EPI_STORE, h->qkv, nullptr, h->Nqkv, h->Nqkv);
     // a chunked step first appends every row's k, v (rows of one lane at
     // consecutive positions see each other's keys); the MMA attention kernels
     // then only read, the other kernels give way to the three-kernel path
@@ -818,15 +805,15 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
                                      : launch_attention_tiled(ap, n, h->xtype, s);
                 });
     }
-    gemm(W.o, W.o_tc, h->pm_o, h->opanel, EPI_STORE, h->y, nullptr, d.d_model,
+    gemm(W.o, W.o_tc, h->opanel, h->lo_o, EPI_STORE, h->y, nullptr, d.d_model,
          d.d_model);
     h->launch(FS_PROF_OTHER, norm_bytes, [&] {
         return launch_rmsnorm(h->x, h->y, W.g_ffn, n, d.d_model, d.rms_eps, h->hpanel,
                               h->xtype, h->Kp_d, h->lo_h, s);
       });
-    gemm(W.gateup, W.gateup_tc, h->pm_h, h->hpanel, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
+    gemm(W.gateup, W.gateup_tc, h->hpanel, h->lo_h, EPI_SWIGLU, nullptr, h->apanel, h->Kp_f,
          d.d_ffn);
-    gemm(W.down, W.down_tc, h->pm_a, h->apanel, EPI_STORE, h->y, nullptr, d.d_model,
+    gemm(W.down, W.down_tc, h->apanel, h->lo_a, EPI_STORE, h->y, nullptr, d.d_model,
          d.d_model);
   }
   h->launch(FS_PROF_OTHER, norm_bytes, [&] {
@@ -834,14 +821,14 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
                             h->Kp_d, h->lo_h, s);
     });
   if (greedy && h->greedy_fused) {  // greedy tokens straight from the head's epilogue
-    gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_ARGMAX, nullptr, nullptr,
+    gemm(h->head, h->head_tc, h->hpanel, h->lo_h, EPI_ARGMAX, nullptr, nullptr,
          d.vocab, d.vocab);
     h->launch(FS_PROF_OTHER, (double)n * (h->head_tc.m_tiles * 8.0 + 4.0), [&] {
       return launch_argmax_tiles(h->am_val, h->am_idx, n, h->head_tc.m_tiles, greedy, s);
     });
     return;
   }
-  gemm(h->head, h->head_tc, h->pm_h, h->hpanel, EPI_STORE, out, nullptr, d.vocab, d.vocab);
+  gemm(h->head, h->head_tc, h->hpanel, h->lo_h, EPI_STORE, out, nullptr, d.vocab, d.vocab);
   if (greedy)
     h->launch(FS_PROF_OTHER, (double)n * d.vocab * 4.0, [&] {
       return launch_sample(out, n, d.vocab, h->d_zero_temps, h->d_zero_u64, h->d_zero_u64,
@@ -1053,9 +1040,14 @@ int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32
       const int64_t before = h->launches;
       cudaGraph_t g = nullptr;
       FS_CK(h, cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+      h->map_fail = false;
       enqueue_step(h, n, out, kv_read, chunked, greedy);
       cudaError_t e = cudaStreamEndCapture(h->stream, &g);
       if (e != cudaSuccess) return h->cuda_fail(e, "cudaStreamEndCapture");
+      if (h->map_fail) {
+        cudaGraphDestroy(g);
+        return h->fail(FS_ERR_CUDA, "GEMM tensor map encoding failed");
+      }
       fs_handle::Graph G;
       e = cudaGraphInstantiate(&G.exec, g, 0);
       cudaGraphDestroy(g);
@@ -1067,7 +1059,9 @@ int run_step(fs_handle* h, const int32_t* lanes, int32_t* positions, const int32
     FS_CK(h, cudaGraphLaunch(it->second.exec, h->stream));
     h->launches += it->second.kernels;
   } else {
+    h->map_fail = false;
     enqueue_step(h, n, out, kv_read, chunked, greedy);
+    if (h->map_fail) return h->fail(FS_ERR_CUDA, "GEMM tensor map encoding failed");
   }
   FS_CK(h, cudaGetLastError());
   if (greedy_out)
@@ -1453,10 +1447,7 @@ namespace {
 int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, float* Y, int P,
                  int reps, double* ms_out, cudaStream_t s, int cs_off = 0) {
   using namespace fsk;
-  CUtensorMap tw, tx, tx64;
-  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
-      tc_make_map(X, B, K, 64, &tx64))
-    return FS_ERR_CUDA;
+  const TcOperands o{W, N, X, B, K, 0};
   const int m_tiles = (N + 127) / 128;
   if (!tc_width_ok(m_tiles, K / 64, P)) return FS_ERR_ARG;
   int sms = 0, dev = 0;
@@ -1482,8 +1473,8 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
     p.epi = EPI_STORE; p.out_f32 = Y; p.ldo = N; p.n_out = N;
     p.ws = ws; p.counters = cnt; p.err = err;
     p.cs_off = cs_off;
-    launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
-    if (reps > 0 && ms_out) {
+    if (launch_gemm_tc(o, p, s) < 0) rc = FS_ERR_CUDA;
+    if (rc == FS_OK && reps > 0 && ms_out) {
       // each launch between two events, after a 256 MiB memset that evicts
       // the operands from L2 and keeps the GPU busy (clocks up)
       const size_t flush_bytes = (size_t)256 << 20;
@@ -1494,7 +1485,7 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
         for (int r = 0; r < reps; ++r) {
           cudaMemsetAsync(flush, r & 0xff, flush_bytes, s);
           cudaEventRecord(ev[2 * r], s);
-          launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
+          launch_gemm_tc(o, p, s);
           cudaEventRecord(ev[2 * r + 1], s);
         }
         double sum = 0.0;
@@ -1510,7 +1501,8 @@ int gemm_tc_hook(const uint16_t* W, int N, int K, const uint16_t* X, int B, floa
       for (auto& e : ev) cudaEventDestroy(e);
     }
     int herr = 0;
-    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
+    if (rc != FS_OK) {
+    } else if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
         cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
       rc = FS_ERR_CUDA;
     else if (herr)

@@ -275,6 +275,8 @@ struct TcParams {
   int tmem_cols;   // power of two >= max(32, lg)
   int sms;         // SMs of the device (stage budget: one or two blocks per SM)
   int stages, stage_bytes;  // set by the launcher
+  int kq;          // k-blocks per stage (set by the launcher)
+  int xh;          // panel rows per k-block of a stage: lg rounded up to 16 (set by the launcher)
   int prod_warps;  // TMA-issuing warps of single-piece blocks (set by the launcher)
   int epi;
   float* out_f32;
@@ -333,13 +335,23 @@ inline int tc_lg_max() {
   }();
   return v;
 }
+// Blocks per SM the fill rule aims at (FS_TC_FILL=1 or 2, a tuning knob
+// read once; default 2).
+inline int tc_fill_per_sm() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_FILL");
+    const int x = e ? atoi(e) : 2;
+    return std::max(1, std::min(2, x));
+  }();
+  return v;
+}
 // lg_min: the smallest group the fill rule may cut (16 for bf16 weights;
 // Q8_0 takes 32, as every group dequantises its weight tiles itself).
 inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups, int lg_min = 16) {
   const int cap = tc_lg_max();
   int g = (n + cap - 1) / cap;
   if (P < sms) {
-    const int fill = std::max(1, 2 * sms / P);
+    const int fill = std::max(1, tc_fill_per_sm() * sms / P);
     const int m = tc_lg_min(lg_min);
     g = std::max(g, std::min(fill, std::max(1, (n + m - 1) / m)));
   }
@@ -366,18 +378,27 @@ bool tc_available();
 // TcParams::cs); FS_TC_CLUSTER=0, a comparison knob read once, keeps the
 // workspace reduction everywhere.
 bool tc_cluster_reduce();
-int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out);
-// tmX64 / tmX16: maps of the activation panel with boxes of 64 / 16 rows.
-// tmX64lo / tmX16lo: the same boxes of the remainder panel (p.split = 1;
-// ignored otherwise).
-int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                   const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
-                   cudaStream_t s);
+// Tensor map of a bf16 [rows][Kp] matrix (Kp a multiple of 64) whose copies
+// bring kq consecutive 64-wide k-blocks of box_rows rows; 0 on success.
+int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, int kq, CUtensorMap* out);
+// Operands of one tcgen05 GEMM launch: bf16 weights w [w_rows][Kp] (unused
+// for Q8_0, whose tiles are in TcParams), the bf16 panel x [x_rows][Kp]
+// and, with TcParams::split, its remainder panel at x + x_lo elements. All
+// base addresses 16-byte aligned, Kp a multiple of 64.
+struct TcOperands {
+  const void* w;
+  int64_t w_rows;
+  const void* x;
+  int64_t x_rows;
+  int Kp;
+  int64_t x_lo;
+};
+// Launches the GEMM; returns the number of launches (1), or -1 when a tensor
+// map cannot be encoded (nothing launched).
+int launch_gemm_tc(const TcOperands& o, const TcParams& p, cudaStream_t s);
 // Same GEMM over Q8_0 tiles (p.q8_codes / p.q8_scales), dequantised to bf16
 // in shared memory inside the kernel.
-int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                      const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
-                      cudaStream_t s);
+int launch_gemm_tc_q8(const TcOperands& o, const TcParams& p, cudaStream_t s);
 // Row-major Q8_0 codes [N][Kp] / scales [N][Kp/32] -> the tiled layout above
 // (rows beyond N are zero).
 int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,

@@ -76,10 +76,6 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
   int* err = counters + m_tiles * groups;
   float* ws = reinterpret_cast<float*>(base + kCtrBytes);
 
-  CUtensorMap tw, tx, tx64;
-  if (tc_make_map(W, N, K, 128, &tw) || tc_make_map(X, B, K, 16, &tx) ||
-      tc_make_map(X, B, K, 64, &tx64))
-    return FS_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   // what must start at zero: the arrival counters and the error flag
   if (cudaMemsetAsync(counters, 0, ctr_bytes, s) != cudaSuccess) return FS_ERR_CUDA;
@@ -100,7 +96,8 @@ extern "C" int fs_gemm_bf16_noalloc(const uint16_t* W, int32_t N, int32_t K,
   p.counters = counters;
   p.err = err;
   p.cs_off = 1;  // K splits sum through the static workspace
-  launch_gemm_tc(tw, tx64, tx, tx64, tx, p, s);
+  const TcOperands o{W, N, X, B, K, 0};
+  if (launch_gemm_tc(o, p, s) < 0) return FS_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
     return FS_ERR_CUDA;
   int herr = 0;

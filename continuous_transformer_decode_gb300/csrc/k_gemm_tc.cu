@@ -36,6 +36,9 @@
 #include <algorithm>
 #include <climits>
 #include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "fs_internal.h"
 #include "tma_mbar.cuh"
@@ -50,7 +53,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;                 // bf16 elements per 128-byte row
 constexpr int kThreads = 192;
 constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kXBoxRows = 16;
 // Q8_0 stage: bf16 A tile | int8 codes (8 KB) | fp16 scales (512 B) | X tile
 constexpr int kQ8Codes = kBM * kBK;        // 8 KB
 constexpr int kQ8Scales = kBM * 2 * 2;     // 512 B
@@ -398,10 +400,8 @@ __device__ __forceinline__ void dequant_q8_tile(uint8_t* stage, int r) {
 enum GemmMode { GM_PLAIN = 0, GM_CLUSTER = 1 };
 
 template <bool kQ8, bool kSplit, int kMode>
-__device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX64,
-                                             const CUtensorMap& tmX16,
-                                             const CUtensorMap& tmX64lo,
-                                             const CUtensorMap& tmX16lo, const TcParams& p) {
+__device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUtensorMap& tmX,
+                                             const CUtensorMap& tmXlo, const TcParams& p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -428,27 +428,59 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   const int n_tot = (lanes + 15) & ~15;
   const int kbt = p.kb_total;
   const int T = p.m_tiles * kbt;
-  const int g0 = sk_lo(cblk, T, p.P), g1 = sk_lo(cblk + 1, T, p.P);
-  const int n_it = g1 - g0;  // >= 1 because P <= T
+  const int g0 = sk_lo(cblk, T, p.P), g1 = sk_lo(cblk + 1, T, p.P);  // g1 > g0: P <= T
   const int t_first = g0 / kbt;
   const int n_pieces = (g1 - 1) / kbt - t_first + 1;
+  // Stages: the range's k-blocks, piece by piece, in chunks of at most kq
+  // consecutive k-blocks of one row tile. A stage is one weight copy (a 3-D
+  // box of kq 128 x 64 tiles) and one panel copy per panel part (a box of
+  // kq tiles of xh lanes x 64), each tile in the 128-byte-swizzled K-major
+  // layout the MMA reads; copies past the range or the matrix are unused or
+  // zero-filled.
+  const int kq = p.kq, xh = p.xh;
+  int n_st = 0;
+  for (int q = 0; q < n_pieces; ++q) {
+    const int tb = (t_first + q) * kbt;
+    n_st += (min(g1, tb + kbt) - max(g0, tb) + kq - 1) / kq;
+  }
+  // first k-block and k-block count of stage i (0 <= i < n_st)
+  auto stage_at = [&](int i, int& g, int& cnt) {
+    if (kq == 1) {  // the stages are the range's k-blocks in order
+      g = g0 + i;
+      cnt = 1;
+      return;
+    }
+    if (n_pieces == 1) {
+      g = g0 + i * kq;
+      cnt = min(kq, g1 - g);
+      return;
+    }
+    int t = t_first, pb = g0;
+    for (;;) {
+      const int pe = min(g1, (t + 1) * kbt);
+      const int nch = (pe - pb + kq - 1) / kq;
+      if (i < nch) {
+        g = pb + i * kq;
+        cnt = min(kq, pe - g);
+        return;
+      }
+      i -= nch;
+      ++t;
+      pb = t * kbt;
+    }
+  };
   const int S = p.stages;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)S * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes + kXbufBytes);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S),
                  conv0 = smem_u32(bars + 2 * S), tfull = smem_u32(bars + 3 * S),
                  tempty = smem_u32(bars + 3 * S + 1), tready = smem_u32(bars + 3 * S + 2);
-  constexpr int kXOff = kQ8 ? kQ8XOff : kWTileBytes;
   const uint32_t ncols = p.tmem_cols;
 
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&tmW);
-    prefetch_tensormap(&tmX64);
-    prefetch_tensormap(&tmX16);
-    if (kSplit) {
-      prefetch_tensormap(&tmX64lo);
-      prefetch_tensormap(&tmX16lo);
-    }
+    if (!kQ8) prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmX);
+    if (kSplit) prefetch_tensormap(&tmXlo);
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -463,30 +495,28 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   }
   __syncthreads();  // barriers initialised
   uint32_t tmem = 0;  // TMEM base, known to the MMA warp and (after tready) the epilogue
-  // TMA producers. The copies one thread issues complete one after another
-  // (about half a microsecond each, whatever their size), so copies are
-  // spread over lanes: before the wait for the predecessor, one lane per
-  // stage issues that stage's weight tile; after it, one lane per panel box
-  // (lanes that issued no weight tile first); in the steady state lane 0
-  // issues the weight tile and lanes 1.. the panel boxes. A block holding a
-  // single piece (whole tile, or one K split of one) also lets its 4 epilogue
+  // TMA producers. Before the wait for the predecessor, one lane per stage
+  // issues that stage's weight copy; after it, one lane per panel copy (lanes
+  // that issued no weight copy first); in the steady state lane 0 issues the
+  // weight copy and lanes 1-2 the panel copies. A block holding a single
+  // piece (whole tile, or one K split of one) also lets its 4 epilogue
   // warps, idle until the accumulator is ready, take the stages congruent to
   // their index; otherwise warp 4 issues every stage (the epilogue warps then
   // drain pieces while it keeps the ring full).
   const int npw = p.prod_warps;  // divides S
   const bool warp_prod = !kQ8 && n_pieces == 1 && npw > 1;
-  const int nb64 = n_tot / 64;
-  const int nbox1 = nb64 + (n_tot - nb64 * 64) / kXBoxRows;  // boxes of one panel part
-  const int nbox = nbox1 * (kSplit ? 2 : 1);                  // panel boxes per stage
-  const uint32_t x_bytes = (uint32_t)n_tot * 128 * (kSplit ? 2 : 1);
-  // warp-collective: iterations first, first + step, ...
+  constexpr int nparts = kSplit ? 2 : 1;  // panel copies per stage
+  const uint32_t wpart = kQ8 ? (uint32_t)kQ8XOff : (uint32_t)(kq * kWTileBytes);
+  const uint32_t xpart = (uint32_t)(kq * xh * 128);  // one panel copy
+  const uint32_t x_bytes = xpart * nparts;
+  // warp-collective: stages first, first + step, ...
   auto produce = [&](int first, int step) {
-    int issued = -1;  // last iteration issued
-    auto load_w = [&](int i) {  // weight part of stage i (and its expect_tx)
+    int issued = -1;  // last stage issued
+    // g: the stage's first k-block (= m_tile * kb_total + kb)
+    auto load_w = [&](int i, int g) {  // weight part of stage i (and its expect_tx)
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-      const int g = g0 + i;  // = m_tile * kb_total + kb
-      if (kQ8) {
+      if (kQ8) {  // kq = 1
         mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales) + x_bytes);
         bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
                   full0 + 8 * s);
@@ -494,38 +524,36 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
                   kQ8Scales, full0 + 8 * s);
       } else {
         const int tile = g / kbt;
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)kWTileBytes + x_bytes);
-        tma_load_2d(st, &tmW, (g - tile * kbt) * kBK, tile * kBM, full0 + 8 * s);
+        mbar_expect_tx(full0 + 8 * s, wpart + x_bytes);
+        tma_load_3d(st, &tmW, 0, tile * kBM, g - tile * kbt, full0 + 8 * s);
       }
     };
-    auto load_x_box = [&](int i, int b) {  // panel box b of stage i
-      const int s = i % S;
-      const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-      const int x = ((g0 + i) % kbt) * kBK;
-      if (kSplit && b >= nbox1) {  // the remainder panel
-        const int bb = b - nbox1;
-        const int r = bb < nb64 ? bb * 64 : nb64 * 64 + (bb - nb64) * kXBoxRows;
-        tma_load_2d(st + kXOff + n_tot * 128 + r * 128, bb < nb64 ? &tmX64lo : &tmX16lo, x,
-                    lane0 + r, full0 + 8 * s);
-        return;
-      }
-      const int r = b < nb64 ? b * 64 : nb64 * 64 + (b - nb64) * kXBoxRows;
-      tma_load_2d(st + kXOff + r * 128, b < nb64 ? &tmX64 : &tmX16, x, lane0 + r, full0 + 8 * s);
+    auto load_x = [&](int i, int g, int part) {  // panel part (1: remainders) of stage i
+      const uint32_t st = smem_u32(smem + (size_t)(i % S) * p.stage_bytes) + wpart + part * xpart;
+      tma_load_3d(st, part ? &tmXlo : &tmX, 0, lane0, g % kbt, full0 + 8 * (i % S));
     };
     // Programmatic dependent launch: the weight tiles do not depend on the
-    // predecessor kernel, so they start before waiting for it; the panel is
-    // the predecessor's output.
-    const int pre = min(S, n_it);  // stages are empty at start: no wait needed
+    // predecessor kernel, so they are issued before waiting for it; the
+    // panel is the predecessor's output.
+    const int pre = min(S, n_st);  // stages are empty at start: no wait needed
     const int n_pre = pre > first ? (pre - first + step - 1) / step : 0;  // this warp's
-    for (int j = lane; j < n_pre; j += 32) load_w(first + j * step);
+    for (int j = lane; j < n_pre; j += 32) {
+      int g, cnt;
+      stage_at(first + j * step, g, cnt);
+      load_w(first + j * step, g);
+    }
     __syncwarp();
     pdl_wait();
     TraceSmem::ready(s_tr);
     pdl_trigger();
-    for (int c = (lane + 32 - n_pre % 32) % 32; c < n_pre * nbox; c += 32)
-      load_x_box(first + (c / nbox) * step, c % nbox);
+    for (int c = (lane + 32 - n_pre % 32) % 32; c < n_pre * nparts; c += 32) {
+      const int i = first + (c / nparts) * step;
+      int g, cnt;
+      stage_at(i, g, cnt);
+      load_x(i, g, c % nparts);
+    }
     if (n_pre > 0) issued = first + (n_pre - 1) * step;
-    for (int i = first + n_pre * step; i < n_it; i += step) {
+    for (int i = first + n_pre * step; i < n_st; i += step) {
       const int s = i % S;
       const uint32_t ph = (uint32_t)(i / S) & 1u;
       const bool ok = mbar_wait(empty0 + 8 * s, ph ^ 1u);
@@ -537,10 +565,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
         break;
       }
       if (__shfl_sync(0xffffffffu, *(volatile int*)&s_abort, 0)) break;
-      if (lane == 0) load_w(i);  // the expect_tx comes before any panel copy
+      int g, cnt;
+      stage_at(i, g, cnt);
+      if (lane == 0) load_w(i, g);  // the expect_tx comes before any panel copy
       __syncwarp();
-      if (lane >= 1)
-        for (int c = lane - 1; c < nbox; c += 31) load_x_box(i, c);
+      if (lane >= 1 && lane <= nparts) load_x(i, g, lane - 1);
       issued = i;
     }
     // drain: every copy issued here must have landed before the block exits
@@ -575,10 +604,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
     tmem = *(volatile uint32_t*)&s_tmem;
     if (lane == 0) {  // ---- MMA issuer: one TMEM accumulation per piece
       bool ok = true;
-      int i = 0;
+      int i = 0;  // stage
       const uint32_t idesc = idesc_bf16(kBM, n_tot);
       for (int q = 0; q < n_pieces && ok; ++q) {
-        const int pe = min(g1, (t_first + q + 1) * kbt);
+        const int tb = (t_first + q) * kbt;
+        const int pb = max(g0, tb), pe = min(g1, tb + kbt);
         if (q > 0) {  // the epilogue has read the previous piece out of TMEM
           if (!mbar_wait(tempty, (uint32_t)(q - 1) & 1u) || *(volatile int*)&s_abort) {
             atomicExch(p.err, 6);
@@ -588,7 +618,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           tc_fence_after();
         }
         bool acc = false;
-        for (; ok && g0 + i < pe; ++i) {
+        for (int g = pb; ok && g < pe; g += kq, ++i) {
+          const int cnt = min(kq, pe - g);
           const int s = i % S;
           const uint32_t ph = (uint32_t)(i / S) & 1u;
           if (!mbar_wait(full0 + 8 * s, ph) || (kQ8 && !mbar_wait(conv0 + 8 * s, ph)) ||
@@ -600,15 +631,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + (size_t)s * p.stage_bytes);
-          const uint32_t b0 = a0 + kXOff;
-          const uint32_t b1 = b0 + (uint32_t)n_tot * 128;  // remainder panel
+          const uint32_t b0 = a0 + wpart;
+          for (int j = 0; j < cnt; ++j) {
+            const uint32_t aj = a0 + (uint32_t)(j * kWTileBytes);
+            const uint32_t bj = b0 + (uint32_t)(j * xh * 128);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                     (acc || kk > 0) ? 1u : 0u);
-            if (kSplit) mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b1 + kk * 32), idesc, 1u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              mma_bf16(tmem, sw128_desc(aj + kk * 32), sw128_desc(bj + kk * 32), idesc,
+                       (acc || kk > 0) ? 1u : 0u);
+              if (kSplit)
+                mma_bf16(tmem, sw128_desc(aj + kk * 32), sw128_desc(bj + xpart + kk * 32), idesc,
+                         1u);
+            }
+            acc = true;
           }
-          acc = true;
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs finish
         }
         mma_commit(tfull);  // arrives when every MMA issued above has finished
@@ -752,22 +788,21 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
   TraceSmem::end(s_tr, TR_GEMM + p.epi);
 }
 
-// The kernels: the plain one takes the maps of the panel only, the split one
-// those of its remainder too.
+// The kernels: the plain one takes the map of the panel only, the split one
+// that of its remainder too (Q8_0 kernels get the panel map in place of the
+// unused weight map).
 template <bool kQ8, int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
-              const __grid_constant__ CUtensorMap tmX16, const TcParams p) {
-  gemm_tc_body<kQ8, false, kMode>(tmW, tmX64, tmX16, tmX64, tmX16, p);
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const TcParams p) {
+  gemm_tc_body<kQ8, false, kMode>(tmW, tmX, tmX, p);
 }
 template <bool kQ8, int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc_split(const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmX64,
-                    const __grid_constant__ CUtensorMap tmX16,
-                    const __grid_constant__ CUtensorMap tmX64lo,
-                    const __grid_constant__ CUtensorMap tmX16lo, const TcParams p) {
-  gemm_tc_body<kQ8, true, kMode>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p);
+                    const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmXlo, const TcParams p) {
+  gemm_tc_body<kQ8, true, kMode>(tmW, tmX, tmXlo, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -794,19 +829,45 @@ bool tc_available() {
   return true;
 }
 
-// 2-D bf16 map over [rows][Kp] (row stride Kp elements), box [box_rows][64],
-// 128-byte swizzle; reads beyond the rows return zeros.
-int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, CUtensorMap* out) {
+// bf16 map over [rows][Kp] (row stride Kp elements) seen as 3-D (64
+// elements, rows, Kp / 64 k-blocks), box (64, box_rows, kq): one copy
+// brings kq consecutive k-blocks of box_rows rows, each a [box_rows][64]
+// tile in the 128-byte-swizzled K-major layout. Reads beyond the rows or the
+// k-blocks return zeros. Encoded maps are kept (keyed by all arguments), so
+// a launch finds its maps without encoding them again.
+int tc_make_map(const void* base, int64_t rows, int Kp, int box_rows, int kq, CUtensorMap* out) {
   if (!tc_available()) return -1;
-  cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)Kp * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+  if (box_rows < 1 || box_rows > 256 || kq < 1 || kq > 256 || Kp % kBK) return -2;
+  struct Key {
+    const void* base;
+    int64_t rows;
+    int Kp, box_rows, kq;
+    bool operator<(const Key& o) const {
+      return std::tie(base, rows, Kp, box_rows, kq) <
+             std::tie(o.base, o.rows, o.Kp, o.box_rows, o.kq);
+    }
+  };
+  static std::mutex mu;
+  static std::map<Key, CUtensorMap> cache;
+  const Key key{base, rows, Kp, box_rows, kq};
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return 0;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(Kp / kBK)};
+  cuuint64_t strides[2] = {(cuuint64_t)Kp * 2, (cuuint64_t)kBK * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)kq};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : -2;
+  if (r != CUDA_SUCCESS) return -2;
+  if (cache.size() >= 4096) cache.clear();  // stale entries of freed buffers
+  cache.emplace(key, *out);
+  return 0;
 }
 
 namespace {
@@ -829,31 +890,70 @@ int max_stages() {
   }();
   return v;
 }
-// FS_TC_SMEM_KB (64..208, a tuning knob read once) sets the per-block shared
-// memory budget of the ring (default 112 KB: two blocks per SM).
-int smem_budget() {
-  static const int v = [] {
+// Per-block shared memory budget of the ring. A launch whose blocks fit on
+// the SMs one each takes most of an SM (FS_TC_SMEM_ALONE_KB, default 208
+// KB): more k-blocks per copy and more of the range in flight. A larger
+// launch keeps two blocks per SM (FS_TC_SMEM_KB, default 112 KB). Tuning
+// knobs (64..208), read once.
+int smem_budget(bool alone) {
+  static const int shared = [] {
     const char* e = getenv("FS_TC_SMEM_KB");
     const int x = e ? atoi(e) : 112;
     return std::max(64, std::min(208, x)) * 1024;
   }();
+  static const int single = [] {
+    const char* e = getenv("FS_TC_SMEM_ALONE_KB");
+    const int x = e ? atoi(e) : 208;
+    return std::max(64, std::min(208, x)) * 1024;
+  }();
+  return alone ? single : shared;
+}
+// k-blocks per stage (FS_TC_KQ=1..8 caps it, a tuning knob read once).
+int kq_max() {
+  static const int v = [] {
+    const char* e = getenv("FS_TC_KQ");
+    const int x = e ? atoi(e) : 8;
+    return std::max(1, std::min(8, x));
+  }();
   return v;
 }
-int tc_stages_for(int n_tot, bool q8, int split, int* stage_bytes, int* smem_bytes) {
-  const int sb = (q8 ? kQ8XOff : kWTileBytes) + n_tot * 128 * (split ? 2 : 1);
+// Stage layout for panel boxes of xh rows and kq k-blocks per stage: the
+// stage size, the stage count within the budget (at least 2) and the
+// dynamic shared memory of a block.
+int tc_stages_for(int xh, int kq, bool q8, int split, int budget_bytes, int* stage_bytes,
+                  int* smem_bytes) {
+  const int sb = (q8 ? kQ8XOff : kq * kWTileBytes) + kq * xh * 128 * (split ? 2 : 1);
   const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 3);
-  const int budget = smem_budget() - fixed;
+  const int budget = budget_bytes - fixed;
   const int st = std::max(2, std::min(max_stages(), budget / sb));
   *stage_bytes = sb;
   *smem_bytes = 1024 + st * sb + kXbufBytes + 8 * (3 * st + 3);
   return st;
 }
+// k-blocks per stage. A small matrix (under 32 MB of weight tiles) is
+// covered by one or two stages per block, where the number of copies sets
+// the time: as many k-blocks per stage as keep two stages within the budget
+// (at most kq_max()). A larger one streams from DRAM through several
+// refills of the ring, where the depth of the ring sets the time: at least
+// four stages, as few k-blocks per stage as that takes. Then the count is
+// evened out over the longest piece of a range so that its stages carry
+// equal counts (9 k-blocks: 5 + 4, not 8 + 1).
+int tc_choose_kq(const TcParams& p, int xh, bool q8, int split, int budget_bytes) {
+  if (q8) return 1;  // Q8_0 stages are dequantised one tile at a time
+  const int64_t T = (int64_t)p.m_tiles * p.kb_total;
+  const int longest = (int)std::min<int64_t>(p.kb_total, (T + p.P - 1) / p.P);
+  const int per_kb = kWTileBytes + xh * 128 * (split ? 2 : 1);
+  const int fixed = 1024 + kXbufBytes + 8 * (3 * kMaxStages + 3);
+  const int min_stages = T * kWTileBytes >= ((int64_t)32 << 20) ? 4 : 2;
+  int kq = std::min(kq_max(), std::min(longest, (budget_bytes - fixed) / (min_stages * per_kb)));
+  kq = std::max(1, kq);
+  const int chunks = (longest + kq - 1) / kq;
+  return (longest + chunks - 1) / chunks;
+}
 
 template <bool kQ8, bool kSplit, int kMode>
-cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmX64,
-                        const CUtensorMap& tmX16, const CUtensorMap& tmX64lo,
-                        const CUtensorMap& tmX16lo, const TcParams& p, int grid, int smem,
-                        cudaStream_t s) {
+cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmXlo,
+                        const TcParams& p, int grid, int smem, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
@@ -867,24 +967,23 @@ cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmX64,
   if (kSplit) {
     if (kMode == GM_CLUSTER)
       return launch_k_cluster(k_gemm_tc_split<kQ8, kMode>, grid, kThreads, smem, s, p.cs, tmW,
-                              tmX64, tmX16, tmX64lo, tmX16lo, p);
-    return launch_k(k_gemm_tc_split<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX64, tmX16,
-                    tmX64lo, tmX16lo, p);
+                              tmX, tmXlo, p);
+    return launch_k(k_gemm_tc_split<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX, tmXlo, p);
   }
   if (kMode == GM_CLUSTER)
-    return launch_k_cluster(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, p.cs, tmW, tmX64,
-                            tmX16, p);
-  return launch_k(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX64, tmX16, p);
+    return launch_k_cluster(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, p.cs, tmW, tmX, p);
+  return launch_k(k_gemm_tc<kQ8, kMode>, grid, kThreads, smem, s, tmW, tmX, p);
 }
 
 template <bool kQ8, bool kSplit>
-int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p0,
-                cudaStream_t s) {
+int launch_impl(const TcOperands& o, const TcParams& p0, cudaStream_t s) {
   TcParams p = p0;
   int smem = 0;
   const int grid = p.P * p.groups;
-  p.stages = tc_stages_for((p.lg + 15) & ~15, kQ8, kSplit, &p.stage_bytes, &smem);
+  p.xh = (p.lg + 15) & ~15;
+  const int budget = smem_budget(grid <= p.sms);
+  p.kq = tc_choose_kq(p, p.xh, kQ8, kSplit, budget);
+  p.stages = tc_stages_for(p.xh, p.kq, kQ8, kSplit, budget, &p.stage_bytes, &smem);
   // producer warps of single-piece blocks: up to 4, dividing the stage count
   p.prod_warps = 1;
   if (!kQ8) {
@@ -894,6 +993,14 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
       smem = 1024 + p.stages * p.stage_bytes + kXbufBytes + 8 * (3 * p.stages + 3);
     }
   }
+  CUtensorMap tw, tx, txlo;
+  if (tc_make_map(o.x, o.x_rows, o.Kp, p.xh, p.kq, &tx) ||
+      (kSplit && tc_make_map(static_cast<const __nv_bfloat16*>(o.x) + o.x_lo, o.x_rows, o.Kp,
+                             p.xh, p.kq, &txlo)) ||
+      (!kQ8 && tc_make_map(o.w, o.w_rows, o.Kp, kBM, p.kq, &tw)))
+    return -1;
+  if (!kSplit) txlo = tx;
+  if (kQ8) tw = tx;  // unused
   // cluster reduction when every stream-K range is one of cs <= 8 equal K
   // splits of a row tile and the partial tile (128 rows x (lanes + 4) f32)
   // fits in the ring; the argmax epilogue needs whole tiles anyway
@@ -906,9 +1013,9 @@ int launch_impl(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensor
       p.cs = cs;
   }
   if (p.cs)
-    launch_mode<kQ8, kSplit, GM_CLUSTER>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
+    launch_mode<kQ8, kSplit, GM_CLUSTER>(tw, tx, txlo, p, grid, smem, s);
   else
-    launch_mode<kQ8, kSplit, GM_PLAIN>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, grid, smem, s);
+    launch_mode<kQ8, kSplit, GM_PLAIN>(tw, tx, txlo, p, grid, smem, s);
   return 1;
 }
 
@@ -939,19 +1046,12 @@ __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __rest
 
 }  // namespace
 
-int launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                   const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
-                   cudaStream_t s) {
-  return p.split ? launch_impl<false, true>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
-                 : launch_impl<false, false>(tmW, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+int launch_gemm_tc(const TcOperands& o, const TcParams& p, cudaStream_t s) {
+  return p.split ? launch_impl<false, true>(o, p, s) : launch_impl<false, false>(o, p, s);
 }
 
-int launch_gemm_tc_q8(const CUtensorMap& tmX64, const CUtensorMap& tmX16,
-                      const CUtensorMap& tmX64lo, const CUtensorMap& tmX16lo, const TcParams& p,
-                      cudaStream_t s) {
-  // the W map is unused
-  return p.split ? launch_impl<true, true>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s)
-                 : launch_impl<true, false>(tmX64, tmX64, tmX16, tmX64lo, tmX16lo, p, s);
+int launch_gemm_tc_q8(const TcOperands& o, const TcParams& p, cudaStream_t s) {
+  return p.split ? launch_impl<true, true>(o, p, s) : launch_impl<true, false>(o, p, s);
 }
 
 namespace {

@@ -64,6 +64,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 3-D tiled load of the map's box at (x, y, z); same rules as tma_load_2d.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 // Brings a tensor map (a __grid_constant__ parameter) into the TMA unit's
 // descriptor cache ahead of the first copy that uses it.
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
