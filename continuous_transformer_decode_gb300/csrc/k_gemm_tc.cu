@@ -145,7 +145,10 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// z * sigmoid(z) with the fast exponential and division intrinsics (the
+// result is rounded to bf16, far coarser than their error); exp(-z)
+// overflowing to infinity gives -0.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Stream-K bookkeeping. The T = m_tiles * kb_total k-blocks of the matrix,
 // taken tile by tile, are cut into P contiguous ranges; block c of a lane
@@ -179,75 +182,85 @@ __device__ __forceinline__ TilePieces tile_pieces(const TcParams& p, int t) {
 }
 
 // Writes one 16-lane chunk of final values of this thread's row.
-// For SwiGLU the tile's rows 0-63 are gate rows and 64-127 the matching up
-// rows; the up half hands its values to the gate half through shared memory.
+// SwiGLU: the tile's rows 0-63 are gate rows and 64-127 the matching up
+// rows; the gate thread of a pair finishes lanes 0-7 and the up thread
+// lanes 8-15, each handing the other half of its values to its partner
+// through shared memory (xbuf: two 64 x 9 float arrays).
+// Argmax: per lane, (max, lowest row) over the tile's 128 rows. The chunk
+// goes through shared memory as order-preserving integer keys (abuf, two
+// alternating [16][136] arrays in the idle ring); 8 threads per lane then
+// scan 16 rows each in ascending order and combine with 3 shuffles.
 template <bool kSplit>
 __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int row_local,
                                            int lane0, int lanes, int c0, const float v[16],
-                                           float* xbuf) {
+                                           float* xbuf, uint32_t* abuf) {
   if (p.epi == EPI_SWIGLU) {
-    if (row_local >= 64) {
+    const bool up = row_local >= 64;
+    const int r = row_local & 63;
+    float* mine = xbuf + (up ? 64 * 9 : 0) + r * 9;
+    const float* theirs = xbuf + (up ? 0 : 64 * 9) + r * 9;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) xbuf[(row_local - 64) * 17 + j] = v[j];
-    }
+    for (int j = 0; j < 8; ++j) mine[j] = v[up ? j : 8 + j];
     epi_bar();
-    if (row_local < 64) {
-      const int f = m_tile * 64 + row_local;
-      if (f < p.n_out) {
+    const int f = m_tile * 64 + r;
+    if (f < p.n_out) {
+      __nv_bfloat16* o0 = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + c0) * p.ldo + f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = c0 + j;
-          if (b < lanes) {
-            const float a = silu(v[j]) * xbuf[row_local * 17 + j];
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_x) + (int64_t)(lane0 + b) * p.ldo + f;
-            const __nv_bfloat16 ah = __float2bfloat16_rn(a);
-            *o = ah;
-            if (kSplit && p.lo_off > 0) o[p.lo_off] = __float2bfloat16_rn(a - __bfloat162float(ah));
-          }
+      for (int j = 0; j < 8; ++j) {
+        const int jj = up ? 8 + j : j;  // lane of the chunk
+        if (c0 + jj < lanes) {
+          const float g = up ? theirs[j] : v[j];
+          const float u = up ? v[8 + j] : theirs[j];
+          const float a = silu(g) * u;
+          __nv_bfloat16* o = o0 + (int64_t)jj * p.ldo;
+          const __nv_bfloat16 ah = __float2bfloat16_rn(a);
+          *o = ah;
+          if (kSplit && p.lo_off > 0) o[p.lo_off] = __float2bfloat16_rn(a - __bfloat162float(ah));
         }
       }
     }
-    epi_bar();
+    epi_bar();  // xbuf is rewritten by the next chunk
     return;
   }
   if (p.epi == EPI_ARGMAX) {
-    // per lane: (max, lowest row) over the tile's 128 rows. In each warp, one
-    // integer max reduction over an order-preserving key of the value, then
-    // one min reduction over the rows that hold it; the 4 warps (rows in
-    // warp order) combine through shared memory, one barrier per chunk (two
-    // exchange buffers alternate between chunks)
-    const int t = row_local, w = t >> 5, l = t & 31;
-    const int row = m_tile * kBM + t;
-    const bool valid = row < p.n_out;
-    uint32_t* ek = reinterpret_cast<uint32_t*>(xbuf) + ((c0 >> 4) & 1) * 128;  // [4][16]
-    uint32_t* ei = ek + 64;                                                     // [4][16]
+    constexpr int kLd = 136;  // conflict-free for the writes and the scans
+    uint32_t* kb = abuf + ((c0 >> 4) & 1) * 16 * kLd;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const uint32_t u = __float_as_uint(v[j] + 0.0f);  // -0 as +0
-      const uint32_t key = valid ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t imin =
-          __reduce_min_sync(0xffffffffu, (valid && key == kmax) ? (uint32_t)row : 0xffffffffu);
-      if (l == j) {
-        ek[w * 16 + j] = kmax;
-        ei[w * 16 + j] = imin;
-      }
+      kb[j * kLd + row_local] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     }
     epi_bar();
-    if (t < 16 && c0 + t < lanes) {
-      uint32_t km = ek[t], im = ei[t];
+    const int jl = row_local >> 3, q = row_local & 7;
+    const int row0 = m_tile * kBM;
+    uint32_t bk = 0, br = 0xffffffffu;  // best key and its row (none yet)
 #pragma unroll
-      for (int ww = 1; ww < 4; ++ww)
-        if (ek[ww * 16 + t] > km) {  // later warps hold larger rows
-          km = ek[ww * 16 + t];
-          im = ei[ww * 16 + t];
-        }
-      const uint32_t u = (km & 0x80000000u) ? (km & 0x7fffffffu) : ~km;
-      const int64_t at = (int64_t)(lane0 + c0 + t) * p.m_tiles + m_tile;
-      p.am_val[at] = __uint_as_float(u);
-      p.am_idx[at] = (int)im;
+    for (int i = 0; i < 16; ++i) {
+      const int r = i * 8 + q;  // ascending: the first of equal keys is the lowest row
+      const uint32_t k = kb[jl * kLd + r];
+      if (row0 + r < p.n_out && (br == 0xffffffffu || k > bk)) {
+        bk = k;
+        br = (uint32_t)(row0 + r);
+      }
     }
-    return;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const uint32_t orow = __shfl_xor_sync(0xffffffffu, br, o);
+      if (orow != 0xffffffffu &&
+          (br == 0xffffffffu || ok > bk || (ok == bk && orow < br))) {
+        bk = ok;
+        br = orow;
+      }
+    }
+    if (q == 0 && c0 + jl < lanes) {
+      const uint32_t u = (bk & 0x80000000u) ? (bk & 0x7fffffffu) : ~bk;
+      const int64_t at = (int64_t)(lane0 + c0 + jl) * p.m_tiles + m_tile;
+      p.am_val[at] = __uint_as_float(u);
+      p.am_idx[at] = (int)br;
+    }
+    return;  // the next chunk writes the other array; the one after, past
+             // that chunk's barrier
   }
   const int row = m_tile * kBM + row_local;
   if (row >= p.n_out) return;
@@ -704,7 +717,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[h][j]);
           if (whole) {
-            emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf);
+            emit_chunk<kSplit>(p, t, row_local, lane0, lanes, cc, v, xbuf,
+                               reinterpret_cast<uint32_t*>(smem));
           } else if (kCluster) {  // the partial tile stays in this block's ring
             float4* dst = reinterpret_cast<float4*>(
                 reinterpret_cast<float*>(smem) + row_local * (n_tot + 4) + cc);
@@ -773,7 +787,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
               }
             }
           }
-          emit_chunk<kSplit>(p, t_first, row_local, lane0, lanes, c0, v, xbuf);
+          emit_chunk<kSplit>(p, t_first, row_local, lane0, lanes, c0, v, xbuf, nullptr);
         }
       }
     }
