@@ -268,7 +268,7 @@ __device__ __forceinline__ void emit_chunk(const TcParams& p, int m_tile, int ro
   if (p.epi == EPI_RESID) {
     float prev[16];  // every load of the chunk before any store
 #pragma unroll
-    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < lanes) ? o[(int64_t)j * p.ldo] : 0.0f;
+    for (int j = 0; j < 16; ++j) prev[j] = (c0 + j < lanes) ? __ldcg(o + (int64_t)j * p.ldo) : 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (c0 + j < lanes) o[(int64_t)j * p.ldo] = prev[j] + v[j];
@@ -366,10 +366,12 @@ __device__ void reduce_tile(const TcParams& p, int m_tile, const TilePieces& tp,
       if (b >= lanes) break;
       float* o = p.out_f32 + (int64_t)(lane0 + b) * p.ldo + row0;
       if (vec) {
+        if (p.epi == EPI_RESID) add4(v[u], __ldcg(reinterpret_cast<const float4*>(o)));
         *reinterpret_cast<float4*>(o) = v[u];
       } else {
         const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        for (int e = 0; e < 4 && row0 + e < p.n_out; ++e) o[e] = vv[e];
+        for (int e = 0; e < 4 && row0 + e < p.n_out; ++e)
+          o[e] = p.epi == EPI_RESID ? __ldcg(o + e) + vv[e] : vv[e];
       }
     }
   }

@@ -65,15 +65,19 @@ __global__ void __launch_bounds__(kNormRowThreads)
   tr.begin(g_trace);
   __shared__ float red[4];
   const int b = blockIdx.x;
-  // x was last written two or more kernels back (complete once this kernel
-  // runs: every kernel waits for its predecessor before letting its
-  // successor start), the gains never: both are read before the wait; r is
-  // the predecessor's output.
+  // The gains are never written: read before the wait. With r given, x was
+  // last written two or more kernels back (complete once this kernel runs:
+  // every kernel waits for its predecessor before letting its successor
+  // start) and is read before the wait too, r is the predecessor's output;
+  // without r, x itself is the predecessor's output (a projection that
+  // added into the residual stream) and is read after the wait.
   NormRow<MV> n;
-  n.load(x + (int64_t)b * d, g, d, threadIdx.x);
+  n.load_g(g, d, threadIdx.x);
+  if (r) n.load_x(x + (int64_t)b * d, d, threadIdx.x);
   pdl_wait();
   tr.ready();
   pdl_trigger();
+  if (!r) n.load_x(x + (int64_t)b * d, d, threadIdx.x);
   n.template finish<OT>(x + (int64_t)b * d, r ? r + (int64_t)b * d : nullptr, d, eps,
                out + (int64_t)b * ld_out, threadIdx.x, 1, red, lo_off);
   tr.end(TR_RMSNORM);

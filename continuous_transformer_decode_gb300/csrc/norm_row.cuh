@@ -18,9 +18,11 @@ constexpr int kNormRowThreads = 128;
 
 // The routine in two halves, so that what does not depend on the preceding
 // kernel (the row of x when it was written two or more kernels earlier, and
-// the gains) is loaded before waiting for it: load() reads x and g, finish()
-// adds y (the preceding kernel's output), normalises and stores. The
-// arithmetic is that of the one-piece routine below.
+// the gains) is loaded before waiting for it: load() reads x and g (or
+// load_g() the gains and, after the wait, load_x() a row of x that the
+// preceding kernel wrote), finish() adds y (the preceding kernel's output),
+// normalises and stores. The arithmetic is that of the one-piece routine
+// below.
 template <int MaxVec>
 struct NormRow {
   float4 v[MaxVec], gg[MaxVec];
@@ -36,6 +38,25 @@ struct NormRow {
         v[j] = *reinterpret_cast<const float4*>(x + 4 * c);
         gg[j] = *reinterpret_cast<const float4*>(g + 4 * c);
       }
+    }
+  }
+  __device__ __forceinline__ void load_g(const float* __restrict__ g, int d, int t) {
+    const int nvec = d >> 2;
+#pragma unroll
+    for (int j = 0; j < MaxVec; ++j) {
+      const int c = t + kNormRowThreads * j;
+      gg[j] = c < nvec ? *reinterpret_cast<const float4*>(g + 4 * c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  // through L2: the row may have been written by the preceding kernel
+  __device__ __forceinline__ void load_x(const float* x, int d, int t) {
+    const int nvec = d >> 2;
+#pragma unroll
+    for (int j = 0; j < MaxVec; ++j) {
+      const int c = t + kNormRowThreads * j;
+      v[j] = c < nvec ? __ldcg(reinterpret_cast<const float4*>(x + 4 * c))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   // `bar` is a named barrier id used by exactly the 128 participating
