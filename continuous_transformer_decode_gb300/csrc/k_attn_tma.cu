@@ -145,45 +145,74 @@ __device__ __forceinline__ void attn_tma_body(const CUtensorMap& tmK, const CUte
   const bool prefetch = !a.kv_written;  // else this step's rows come from the predecessor
   if (prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
+  // the rotation of position pos (constant tables): thread t rotates pairs
+  // i = t mod hd/2 of every head (kT is a multiple of hd/2)
+  static_assert(kT % kHalf == 0, "a thread's pairs share one rotation");
+  const int rp = tid % kHalf;
+  const float rc_i = a.rc[(int64_t)pos * kHalf + rp], rs_i = a.rs[(int64_t)pos * kHalf + rp];
   pdl_wait();  // the QKV projection's output is read below
   TraceSmem::ready(s_tr);
   pdl_trigger();
   if (!prefetch)
     for (int i = 0; i < min(R::kStages, n_tiles); ++i) issue(i);
 
-  // ---- rotated queries; the owner of pos also rotates k and appends k, v
+  // ---- rotated queries; the owner of pos also rotates k and appends k, v.
+  // Every load of the projection's row is issued before any use.
   const float* row = a.qkv + (int64_t)b * (H + 2 * Hkv) * HD;
-  const float* c = a.rc + (int64_t)pos * kHalf;
-  const float* sn = a.rs + (int64_t)pos * kHalf;
-  for (int idx = tid; idx < kG * kHalf; idx += kT) {
-    const int h = idx / kHalf, i = idx - h * kHalf;
-    float q0 = 0.0f, q1 = 0.0f;
-    if (h < G) {
-      const float x0 = row[(g * G + h) * HD + i], x1 = row[(g * G + h) * HD + i + kHalf];
-      rope_pair(x0, x1, c[i], sn[i], q0, q1);
-    }
-    qs[h * HD + i] = q0;
-    qs[h * HD + i + kHalf] = q1;
-  }
+  constexpr int kQIt = (kG * kHalf + kT - 1) / kT;
+  constexpr int kVIt = (HD + kT - 1) / kT;
   const bool append = owns_pos && !a.kv_written;
+  const float* kr = row + H * HD + g * HD;
+  const float* vr = row + (H + Hkv) * HD + g * HD;
+  float qx0[kQIt], qx1[kQIt], vx[kVIt];
+  float kx0 = 0.0f, kx1 = 0.0f;
+#pragma unroll
+  for (int it = 0; it < kQIt; ++it) {
+    const int idx = tid + it * kT, h = idx / kHalf;
+    qx0[it] = qx1[it] = 0.0f;
+    if (idx < kG * kHalf && h < G) {
+      qx0[it] = row[(g * G + h) * HD + rp];
+      qx1[it] = row[(g * G + h) * HD + rp + kHalf];
+    }
+  }
+  if (append && tid < kHalf) {
+    kx0 = kr[tid];
+    kx1 = kr[tid + kHalf];
+  }
+#pragma unroll
+  for (int it = 0; it < kVIt; ++it) {
+    const int i = tid + it * kT;
+    vx[it] = (append && i < HD) ? vr[i] : 0.0f;
+  }
+#pragma unroll
+  for (int it = 0; it < kQIt; ++it) {
+    const int idx = tid + it * kT, h = idx / kHalf;
+    if (idx < kG * kHalf) {
+      float q0 = 0.0f, q1 = 0.0f;
+      if (h < G) rope_pair(qx0[it], qx1[it], rc_i, rs_i, q0, q1);
+      qs[h * HD + rp] = q0;
+      qs[h * HD + rp + kHalf] = q1;
+    }
+  }
   if (append) {
-    const float* kr = row + H * HD + g * HD;
-    const float* vr = row + (H + Hkv) * HD + g * HD;
     const int pi = pos / ps, slot = pos - pi * ps;
     const int64_t off = (int64_t)a.layer * kv.layer_stride +
                         (((int64_t)ptrow[pi] * Hkv + g) * ps + slot) * HD;
-    for (int i = tid; i < kHalf; i += kT) {
-      const float x0 = kr[i], x1 = kr[i + kHalf];
+    if (tid < kHalf) {  // rp == tid
       float k0, k1;
-      rope_pair(x0, x1, c[i], sn[i], k0, k1);
-      Kg[off + i] = __float2bfloat16_rn(k0);
-      Kg[off + i + kHalf] = __float2bfloat16_rn(k1);
-      knew[i] = k0;
-      knew[i + kHalf] = k1;
+      rope_pair(kx0, kx1, rc_i, rs_i, k0, k1);
+      Kg[off + tid] = __float2bfloat16_rn(k0);
+      Kg[off + tid + kHalf] = __float2bfloat16_rn(k1);
+      knew[tid] = k0;
+      knew[tid + kHalf] = k1;
     }
-    for (int i = tid; i < HD; i += kT) {
-      Vg[off + i] = __float2bfloat16_rn(vr[i]);
-      vnew[i] = vr[i];
+#pragma unroll
+    for (int it = 0; it < kVIt; ++it) {
+      const int i = tid + it * kT;
+      if (i < HD) {
+        Vg[off + i] = __float2bfloat16_rn(vx[it]);
+        vnew[i] = vx[it];
+      }
     }
   }
   __syncthreads();
