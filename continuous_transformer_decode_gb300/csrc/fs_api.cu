@@ -68,6 +68,7 @@ const fs_handle* g_trace_owner = nullptr;
 bool trace_install_all(TraceBuf* b) {
   return trace_install_misc(b) && trace_install_gemm(b) && trace_install_gemv(b) &&
          trace_install_attn(b) && trace_install_attn_mma(b) && trace_install_attn_tma(b) &&
+         trace_install_attn_warp(b) &&
          trace_install_attn_tiled(b);
 }
 
@@ -163,6 +164,10 @@ struct fs_handle {
   bool attn_tiled = false;
   bool attn_mma = false;
   bool attn_tma = false;         // KV tiles by TMA (k_attn_tma.cu)
+  // one warp per (lane, KV head) on handles of <= 64 positions, for calls of
+  // at least attn_warp_rows rows (the cp.async kernel serves smaller calls)
+  bool attn_warp = false;
+  int attn_warp_rows = 0;
   CUtensorMap tm_kv_k, tm_kv_v;  // KV arenas as [rows][hd] bf16 for that kernel
 
   int32_t* d_args = nullptr;  // [7 * max_lanes + 1]
@@ -541,10 +546,12 @@ int create_impl(fs_handle* h, const fs_weights* W) {
   FS_CK(h, cudaMemset(h->d_zero_temps, 0, (size_t)B * 4));
   FS_CK(h, cudaMemset(h->d_zero_u64, 0, (size_t)B * 8));
   {
-    // FS_ATTN=mma (a comparison knob read at create) keeps the cp.async
-    // kernel on long-context handles; the two give the same bits
+    // FS_ATTN=mma / warp (comparison knobs read at create) keep the cp.async
+    // kernel on every handle / the one-warp kernel for every call of a
+    // short-context handle; the kernels give the same bits
     const char* e = getenv("FS_ATTN");
     const bool force_mma = e && std::string(e) == "mma";
+    const bool force_warp = e && std::string(e) == "warp";
     h->attn_mma = attn_mma_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, h->split_len,
                                     h->max_splits);
     // the TMA kernel's producer warp and barrier set-up pay off on long
@@ -558,6 +565,14 @@ int create_impl(fs_handle* h, const fs_weights* W) {
           attn_tma_make_map(h->kv.v, rows, d.head_dim, d.page_size, &h->tm_kv_v))
         h->attn_tma = false;  // arena too large for 32-bit rows: the cp.async kernel serves
     }
+    // lanes of at most 64 positions: one warp per (lane, KV head), the
+    // cp.async kernel's bits. It holds ten pairs an SM against the cp.async
+    // kernel's six of four warps each, so it pays once a call fills the SMs
+    // ten times over (SmolLM2 shape: 8.0 vs 5.8 us per layer at 256 lanes,
+    // faster at 960); smaller calls keep the cp.async kernel.
+    h->attn_warp = !force_mma && h->attn_mma &&
+                   attn_warp_supports(d.head_dim, h->G, d.kv_dtype == FS_DTYPE_F32, d.max_pos);
+    h->attn_warp_rows = force_warp ? 0 : (10 * h->sms + d.n_kv_heads - 1) / d.n_kv_heads;
     // f32 KV and head dims below 64: the tiled kernel
     h->attn_tiled = !h->attn_tma && !h->attn_mma &&
                     attn_tiled_supports(d.head_dim, h->G, d.page_size, h->split_len);
@@ -799,6 +814,8 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
       h->launch(FS_PROF_ATTN,
                 kv_read + (double)n * (h->Nqkv * 4.0 + h->Nq * xs + 2.0 * h->Nkv * kvs),
                 [&] {
+                  if (h->attn_warp && n >= h->attn_warp_rows)
+                    return launch_attention_warp(ap, n, h->xtype, s);
                   if (h->attn_tma)
                     return launch_attention_tma(h->tm_kv_k, h->tm_kv_v, ap, n, h->xtype, s);
                   return h->attn_mma ? launch_attention_mma(ap, n, h->xtype, s)
@@ -1413,6 +1430,7 @@ const char* fs_gemm_path(const fs_handle* h) {
 
 const char* fs_attention_path(const fs_handle* h) {
   if (!h) return "";
+  if (h->attn_warp) return "warp-mma";
   if (h->attn_tma) return "tma-mma";
   if (h->attn_mma) return "cp.async-mma";
   if (h->attn_tiled) return "tiled";

@@ -52,7 +52,7 @@ struct TraceBuf {
 // record tags
 enum TraceTag {
   TR_EMBED = 1, TR_RMSNORM = 2, TR_SAMPLE = 3, TR_ARGMAX = 4,
-  TR_ATTN_MMA = 5, TR_ATTN_TMA = 6, TR_ATTN_TILED = 7, TR_ATTN_FUSED = 8,
+  TR_ATTN_MMA = 5, TR_ATTN_TMA = 6, TR_ATTN_TILED = 7, TR_ATTN_WARP = 8,
   TR_ROPE_APPEND = 9, TR_GEMV = 10, TR_ATTN_PARTIAL = 11, TR_ATTN_COMBINE = 12,
   TR_GEMV_SWIGLU = 13,
   TR_GEMM = 16  // + the epilogue kind (Epi)
@@ -146,6 +146,7 @@ int trace_install_gemm(TraceBuf* p);
 int trace_install_gemv(TraceBuf* p);
 int trace_install_attn(TraceBuf* p);
 int trace_install_attn_mma(TraceBuf* p);
+int trace_install_attn_warp(TraceBuf* p);
 int trace_install_attn_tma(TraceBuf* p);
 int trace_install_attn_tiled(TraceBuf* p);
 
@@ -440,9 +441,14 @@ struct AttnParams {
   //    of one lane at consecutive positions, chunked prefill), so the kernel
   //    appends nothing and reads no KV before its predecessor has finished
   int kv_written;
+  int n_rows;        // panel rows of the step (set by the one-warp kernel's launcher)
 };
 bool attn_tiled_supports(int hd, int G, int page_size, int split_len);
 bool attn_mma_supports(int hd, int G, int kv_f32, int split_len, int max_splits);
+// One warp per (lane, KV head) for handles whose lanes hold at most 64
+// positions (k_attn_warp.cu): the bits of k_attn_mma.
+bool attn_warp_supports(int hd, int G, int kv_f32, int max_pos);
+int launch_attention_warp(const AttnParams& a, int B, int x_type, cudaStream_t s);
 // Same attention with the KV tiles fetched by TMA (k_attn_tma.cu): bf16 KV,
 // page_size a multiple of 8 that divides or is a multiple of 64.
 bool attn_tma_supports(int hd, int G, int kv_f32, int page_size, int split_len,

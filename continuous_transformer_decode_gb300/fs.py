@@ -244,7 +244,7 @@ def fs_lane_reset(h, lane: int) -> None:
 
 
 TRACE_TAGS = {1: "embed", 2: "rmsnorm", 3: "sample", 4: "argmax_tiles",
-              5: "attn_mma", 6: "attn_tma", 7: "attn_tiled", 8: "attn_fused",
+              5: "attn_mma", 6: "attn_tma", 7: "attn_tiled", 8: "attn_warp",
               9: "rope_append", 10: "gemv", 11: "attn_partial", 12: "attn_combine",
               13: "gemv_swiglu",
               16: "gemm_store", 17: "gemm_resid",

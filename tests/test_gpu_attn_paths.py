@@ -136,3 +136,75 @@ def test_tma_attention_long_splits(smol_l2):
     are 1, 2 and 3 splits."""
     cfg, Wb = smol_l2
     _check(cfg, Wb, 16, [300, 1100, 2100], with_oracle=True, max_lanes=128, max_pos=3100)
+
+
+def _check_warp(cfg, Wb, page_size, ctx, max_pos=64):
+    """The one-warp kernel (handles of at most 64 positions; FS_ATTN=warp
+    takes it for calls of any size) against the cp.async kernel, bit for
+    bit, and against the oracle."""
+    kv = _kv(cfg, ctx, seed=43)
+    rng = np.random.default_rng(7)
+    steps = min(3, max_pos - max(ctx))
+    toks = [[int(x) for x in rng.integers(0, cfg["V"], len(ctx))] for _ in range(steps)]
+    h_w = _handle(cfg, Wb, page_size, max_pos, force="warp", max_lanes=8)
+    h_m = _handle(cfg, Wb, page_size, max_pos, force="mma", max_lanes=8)
+    try:
+        assert fs.fs_attention_path(h_w) == "warp-mma"
+        assert fs.fs_attention_path(h_m) == "cp.async-mma"
+        got_w = _run_gpu(h_w, cfg, ctx, kv, toks)
+        got_m = _run_gpu(h_m, cfg, ctx, kv, toks)
+    finally:
+        fs.fs_destroy(h_w)
+        fs.fs_destroy(h_m)
+    assert np.array_equal(got_w.view(np.int32), got_m.view(np.int32))
+    ref = _run_oracle(cfg, Wb, ctx, kv, toks, max_pos)
+    U.compare_logits(got_w.reshape(-1, cfg["V"]), ref.reshape(-1, cfg["V"]),
+                     BF16_MAX_ABS, BF16_MIN_COS)
+
+
+@pytest.mark.parametrize("page_size", [8, 16, 64])
+def test_warp_attention_hd64(smol_l2, page_size):
+    """Contexts of 0 to 60 tokens: empty and partial 16-position chunks, a
+    lane whose position is the tile's last row."""
+    cfg, Wb = smol_l2
+    _check_warp(cfg, Wb, page_size, [0, 1, 15, 16, 37, 60])
+
+
+def test_warp_attention_hd128_mistral_shape():
+    cfg = synth.with_layers(synth.MODEL_M, 2)
+    Wb = synth.make_weights(cfg, seed=1, fmt="bf16")
+    _check_warp(cfg, Wb, 16, [3, 33, 61])
+
+
+def test_warp_attention_chunked_prefill(smol_l2):
+    """Chunked steps (every row's k, v appended before attention reads them)
+    on the one-warp and the cp.async kernels give the same bits."""
+    import torch
+    cfg, Wb = smol_l2
+    outs = []
+    for force in ("warp", "mma"):
+        h = _handle(cfg, Wb, 16, 64, force=force, max_lanes=8)
+        try:
+            pos = np.zeros(3, np.int32)
+            rows, lg = [], []
+            prompts = synth.make_prompts(3, [20, 9, 33], cfg["V"], seed=5)
+            # lane 0 takes 4 rows a step, lane 1 one, lane 2 three
+            p = np.zeros(3, np.int64)
+            while any(p[k] < len(prompts[k]) for k in range(3)):
+                lanes, poss, toks = [], [], []
+                for k, take in enumerate((4, 1, 3)):
+                    for _ in range(take):
+                        if p[k] < len(prompts[k]):
+                            lanes.append(k)
+                            poss.append(int(p[k]))
+                            toks.append(int(prompts[k][p[k]]))
+                            p[k] += 1
+                po = np.array([poss[i] for i in range(len(lanes))], np.int32)
+                buf = torch.empty((len(lanes), cfg["V"]), dtype=torch.float32, device="cuda")
+                fs.fs_step_batch_chunked(h, lanes, po, toks, logits_out=buf)
+                torch.cuda.synchronize()
+                lg.append(buf.cpu().numpy())
+            outs.append(np.concatenate(lg))
+        finally:
+            fs.fs_destroy(h)
+    assert np.array_equal(outs[0].view(np.int32), outs[1].view(np.int32))
