@@ -84,9 +84,6 @@ int trace_release(const fs_handle* h) {
   return ok ? FS_OK : FS_ERR_CUDA;
 }
 
-// Handles of at most this many lanes split short-K matrices.
-constexpr int kSplitHandleLanes = 64;
-
 int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   const int64_t T = (int64_t)m_tiles * kb_total;
   if (m_tiles >= sms) return m_tiles;
@@ -103,13 +100,14 @@ int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
     return m_tiles * std::max(1, std::min(kb_total, 2 * sms / m_tiles));
   const bool narrow = max_lanes <= 32;
   int s = narrow ? (13 * sms + 5 * m_tiles) / (10 * m_tiles) : (85 * sms) / (100 * m_tiles);
-  // short K (fewer than 32 k-blocks, e.g. a 576- or 1536-wide input) on
-  // handles of at most 64 lanes: splits of at least 3 k-blocks, whose partial
-  // tiles sum inside a thread-block cluster; otherwise the splits the
-  // workspace reduction was timed with (none for short K)
-  const int cap = kb_total < 32 && max_lanes <= kSplitHandleLanes && tc_cluster_reduce()
-                      ? kb_total / 3
-                      : kb_total / (narrow ? 8 : 32);
+  // short K (fewer than 32 k-blocks, e.g. a 576- or 1536-wide input): no
+  // splits, as the multi-k-block stages bring a whole tile's K in two or
+  // three copies and a cluster reduction would cost more (SmolLM2 bf16, ms
+  // per step on handles of 1 / 4 / 16 / 64 lanes: 0.929 / 0.968 / 1.000 /
+  // 1.175 with splits of 3 k-blocks, 0.887 / 0.886 / 0.903 / 0.921
+  // without); long K: splits of at least 32 k-blocks (8 on handles of at
+  // most 32 lanes)
+  const int cap = kb_total < 32 ? 1 : kb_total / (narrow ? 8 : 32);
   s = std::min(s, std::min(8, cap));
   return m_tiles * std::max(1, s);
 }
