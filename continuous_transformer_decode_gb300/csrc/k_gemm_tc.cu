@@ -8,7 +8,11 @@
 // Swap-AB: the weight tile is the M = 128 operand (rows of W), the lanes are
 // the N operand, so one 128-row weight tile serves every lane and small B
 // costs no weight re-reads. Operands are staged by TMA into 128-byte-swizzled
-// shared memory; the f32 accumulator lives in tensor memory (TMEM).
+// shared memory; the f32 accumulator lives in tensor memory (TMEM). A stage
+// holds several consecutive 64-wide k-blocks of one row tile, filled by one
+// 3-D weight copy and one 3-D panel copy: an SM's TMA copies complete one
+// after another, so their number, more than their bytes, sets a block's
+// time at the small sizes of a decode step.
 //
 // Block = 6 warps: warp 4 issues TMA loads, warp 5 owns TMEM and issues the
 // MMAs, warps 0-3 run the epilogue (warp w reads TMEM lanes 32w..32w+31,
