@@ -35,8 +35,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 // tcgen05 operand map and the fixed K split of one weight matrix.
 struct TcW {
   int m_tiles = 0, P = 1;  // row tiles, stream-K width
-  int8_t* q8_codes = nullptr;  // Q8_0 tiles (see launch_tile_q8)
-  __half* q8_scales = nullptr;
+  int8_t* q8_tiles = nullptr;  // Q8_0 tiles (see launch_tile_q8)
 };
 
 struct LayerW {
@@ -604,11 +603,10 @@ int create_impl(fs_handle* h, const fs_weights* W) {
       ws_elems = std::max(ws_elems, tc_ws_floats(t->P, B));
       if (h->wtype == W_Q8) {
         const size_t tiles = (size_t)t->m_tiles * (m.Kp / 64);
-        if (h->alloc(&t->q8_codes, tiles * 8192) != cudaSuccess ||
-            h->alloc(&t->q8_scales, tiles * 512) != cudaSuccess)
+        if (h->alloc(&t->q8_tiles, tiles * (8192 + 512)) != cudaSuccess)
           return h->fail(FS_ERR_OOM, "Q8_0 tile allocation failed");
-        h->launches += launch_tile_q8((const int8_t*)m.w, m.scales, m.N, m.Kp, t->q8_codes,
-                                      t->q8_scales, h->stream);
+        h->launches += launch_tile_q8((const int8_t*)m.w, m.scales, m.N, m.Kp, t->q8_tiles,
+                                      h->stream);
         FS_CK(h, cudaGetLastError());
         FS_CK(h, cudaStreamSynchronize(h->stream));
         return FS_OK;
@@ -767,7 +765,7 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.cs_off = (p.kb_total >= 32 && p.lg < 32) ? 1 : 0;
     p.epi = epi; p.out_f32 = of; p.out_x = ox; p.ldo = ldo; p.n_out = n_out;
     p.ws = h->ws; p.counters = h->counters; p.err = h->d_err_flag;
-    p.q8_codes = T.q8_codes; p.q8_scales = T.q8_scales;
+    p.q8_tiles = T.q8_tiles;
     p.am_val = h->am_val; p.am_idx = h->am_idx;
     p.split = h->act_split;
     p.lo_off = epi == EPI_SWIGLU ? h->lo_a : 0;

@@ -287,10 +287,9 @@ struct TcParams {
   float* ws;       // partial pieces [2][P][lanes_total][128] f32
   int* counters;   // [m_tiles * groups], zero between launches
   int* err;        // device-visible error flag
-  // Q8_0 weights in tiles: codes [m_tiles][kb][128][64] int8 and scales
-  // [m_tiles][kb][128][2] fp16 (one per 32 inputs)
-  const int8_t* q8_codes;
-  const __half* q8_scales;
+  // Q8_0 weights in tiles [m_tiles][kb], each its codes [128][64] int8 then
+  // its scales [128][2] fp16 (one per 32 inputs): 8704 bytes
+  const int8_t* q8_tiles;
   float* am_val;   // EPI_ARGMAX: [lanes_total][m_tiles] tile maxima
   int* am_idx;     //             and their row indices
   // 1: the panel has a remainder part (map tmX*lo): two MMAs per k-step,
@@ -397,13 +396,13 @@ struct TcOperands {
 // Launches the GEMM; returns the number of launches (1), or -1 when a tensor
 // map cannot be encoded (nothing launched).
 int launch_gemm_tc(const TcOperands& o, const TcParams& p, cudaStream_t s);
-// Same GEMM over Q8_0 tiles (p.q8_codes / p.q8_scales), dequantised to bf16
+// Same GEMM over Q8_0 tiles (p.q8_tiles), dequantised to bf16
 // in shared memory inside the kernel.
 int launch_gemm_tc_q8(const TcOperands& o, const TcParams& p, cudaStream_t s);
 // Row-major Q8_0 codes [N][Kp] / scales [N][Kp/32] -> the tiled layout above
 // (rows beyond N are zero).
-int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,
-                   __half* scales_t, cudaStream_t s);
+int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* tiles,
+                   cudaStream_t s);
 
 // x = E[tok]; if g is given also h = RMSNorm(x) * g (x_type panel).
 // lo_off (elements, bf16 panels only; 0: none): the row's rounding

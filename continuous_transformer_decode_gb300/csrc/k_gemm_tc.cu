@@ -61,6 +61,7 @@ constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kQ8Codes = kBM * kBK;        // 8 KB
 constexpr int kQ8Scales = kBM * 2 * 2;     // 512 B
 constexpr int kQ8XOff = 25 * 1024;         // 16 + 8 + 0.5 KB, 1 KB aligned
+constexpr int kQ8Tile = kQ8Codes + kQ8Scales;  // a tile in global memory: codes, then scales
 constexpr int kXbufBytes = 64 * 17 * 4 + 256;  // SwiGLU gate/up exchange, 8-byte aligned end
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -536,11 +537,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap& tmW, const CUten
       const int s = i % S;
       const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
       if (kQ8) {  // kq = 1
-        mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQ8Codes + kQ8Scales) + x_bytes);
-        bulk_load(st + kWTileBytes, p.q8_codes + (int64_t)g * kQ8Codes, kQ8Codes,
-                  full0 + 8 * s);
-        bulk_load(st + kWTileBytes + kQ8Codes, p.q8_scales + (int64_t)g * (kQ8Scales / 2),
-                  kQ8Scales, full0 + 8 * s);
+        // one copy: the tile's codes and, right after them, its scales
+        mbar_expect_tx(full0 + 8 * s, (uint32_t)kQ8Tile + x_bytes);
+        bulk_load(st + kWTileBytes, p.q8_tiles + (int64_t)g * kQ8Tile, kQ8Tile, full0 + 8 * s);
       } else {
         const int tile = g / kbt;
         mbar_expect_tx(full0 + 8 * s, wpart + x_bytes);
@@ -1040,15 +1039,14 @@ int launch_impl(const TcOperands& o, const TcParams& p0, cudaStream_t s) {
 }
 
 __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __restrict__ scales,
-                          int N, int Kp, int8_t* __restrict__ codes_t,
-                          __half* __restrict__ scales_t) {
+                          int N, int Kp, int8_t* __restrict__ tiles) {
   const int kb_total = Kp / kBK;
   const int64_t tile = blockIdx.x;  // (m_tile, kb)
   const int m_tile = (int)(tile / kb_total), kb = (int)(tile % kb_total);
   const int r = threadIdx.x;        // row in the tile (128 threads)
   const int row = m_tile * kBM + r;
-  int8_t* dst = codes_t + tile * kQ8Codes + r * kBK;
-  __half* sdst = scales_t + tile * (kQ8Scales / 2) + r * 2;
+  int8_t* dst = tiles + tile * kQ8Tile + r * kBK;
+  __half* sdst = reinterpret_cast<__half*>(tiles + tile * kQ8Tile + kQ8Codes) + r * 2;
   if (row < N) {
     const int8_t* src = codes + (int64_t)row * Kp + kb * kBK;
 #pragma unroll
@@ -1118,10 +1116,10 @@ int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_til
   return 1;
 }
 
-int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* codes_t,
-                   __half* scales_t, cudaStream_t s) {
+int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* tiles,
+                   cudaStream_t s) {
   const int m_tiles = (N + kBM - 1) / kBM;
-  k_tile_q8<<<m_tiles * (Kp / kBK), kBM, 0, s>>>(codes, scales, N, Kp, codes_t, scales_t);
+  k_tile_q8<<<m_tiles * (Kp / kBK), kBM, 0, s>>>(codes, scales, N, Kp, tiles);
   return 1;
 }
 
