@@ -255,6 +255,7 @@ def run_ours(args, wl, ws, rank, local):
     K, Wm = args.steps, args.warmup
     extra = Wm + 2 * K + 8 + args.trace  # warm-up, timed, end-to-end, traced steps
     h, ctx, wdt = make_handle(cfg, wl, B, extra)
+    gemm_path = fs.fs_gemm_path(h)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     fs.fs_set_stream(h, stream)
@@ -359,7 +360,10 @@ def run_ours(args, wl, ws, rank, local):
             "bound": "hbm", "achieved": None, "peak": peaks["hbm"], "unit": "GB/s",
             "frac": None, "traffic": None, "peak_source": peaks["src"],
             "launches_per_step": g_launches,
-            "algorithmic_bytes_per_launch": g_bytes / g_launches}
+            "algorithmic_bytes_per_launch": g_bytes / g_launches,
+            # tcgen05-q8_0+bf16: calls of many lane groups multiply bf16
+            # copies of the Q8_0 matrices (more bytes than the algorithmic ones)
+            "gemm_path": gemm_path}
     if timeline:
         share = sum(k["share"] or 0.0 for n, k in timeline["kernels"].items()
                     if n.startswith("gemm"))
@@ -417,6 +421,7 @@ def run_workloads(args, local):
         for B in Bs:
             t0 = time.perf_counter()
             h, ctx, wdt = make_handle(cfg, wl, B, warm + steps + 4, W=Wshared)
+            gemm_path = fs.fs_gemm_path(h)
             try:
                 fs.fs_set_stream(h, torch.cuda.current_stream())
                 lanes, pos, toks, _ = fill_lanes(h, cfg, wl, B, ctx)
@@ -429,6 +434,7 @@ def run_workloads(args, local):
             sr = step_roofline(cfg, wb, B, ctx_mean, peaks)
             tok_s = B / (ms / 1e3)
             out.append({"workload": name, "lanes": B, "ms_per_step": ms, "tok_s": tok_s,
+                        "gemm_path": gemm_path,
                         "activations": ("bf16 + bf16 remainder (act_split)"
                                         if wl.get("act_split") else "bf16"),
                         "context": (f"16-token prompts" if "ctx" not in wl else

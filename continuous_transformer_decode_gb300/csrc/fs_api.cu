@@ -36,6 +36,10 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct TcW {
   int m_tiles = 0, P = 1;  // row tiles, stream-K width
   int8_t* q8_tiles = nullptr;  // Q8_0 tiles (see launch_tile_q8)
+  // bf16 copy of a Q8_0 matrix, bf16(q * d) (see launch_dequant_q8_bf16):
+  // kept where the handle's lane capacity splits the matrix's Q8_0 GEMM into
+  // at least q8_copy_groups lane groups
+  __nv_bfloat16* q8_bf16 = nullptr;
 };
 
 struct LayerW {
@@ -128,6 +132,9 @@ struct fs_handle {
   TcW head_tc;
   bool use_tc = false;
   int act_split = 0;
+  // Q8_0: a GEMM call whose lane groups would number at least this many
+  // multiplies the matrix's bf16 copy instead (0: no copies)
+  int q8_copy_groups = 2;
   bool map_fail = false;  // a GEMM launch could not encode its tensor maps
   int64_t lo_h = 0, lo_o = 0, lo_a = 0;  // remainder offsets (elements; 0: none)
   float* ws = nullptr;
@@ -397,6 +404,10 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     h->act_split = d.act_split;
     const char* genv = getenv("FS_GRAPHS");
     h->graphs_on = !(genv && std::string(genv) == "0");
+    // FS_Q8_BF16_GROUPS (read at create): the lane-group count from which a
+    // Q8_0 GEMM runs on its bf16 copy; 0 keeps no copies (comparison knob)
+    const char* qenv = getenv("FS_Q8_BF16_GROUPS");
+    if (qenv) h->q8_copy_groups = std::max(0, atoi(qenv));
   }
 
   FS_CK(h, cudaStreamCreateWithFlags(&h->own_stream, cudaStreamDefault));
@@ -608,6 +619,23 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         h->launches += launch_tile_q8((const int8_t*)m.w, m.scales, m.N, m.Kp, t->q8_tiles,
                                       h->stream);
         FS_CK(h, cudaGetLastError());
+        // Every lane group of a Q8_0 GEMM dequantises each weight tile it
+        // multiplies, so a call of g groups converts the matrix g times.
+        // Where the lane capacity reaches q8_copy_groups groups the handle
+        // also keeps the matrix in bf16, converted once here: such calls
+        // stream 16 instead of 8.5 KB per tile and convert nothing.
+        int lg = 0, groups = 1;
+        tc_lane_groups(B, t->P, h->sms, &lg, &groups, 32);
+        if (h->q8_copy_groups > 0 && groups >= h->q8_copy_groups) {
+          if (h->alloc(&t->q8_bf16, (size_t)m.N * m.Kp * 2) != cudaSuccess)
+            return h->fail(FS_ERR_OOM, "Q8_0 bf16 copy allocation failed");
+          h->launches += launch_dequant_q8_bf16((const int8_t*)m.w, m.scales, m.N, m.Kp,
+                                                t->q8_bf16, h->stream);
+          FS_CK(h, cudaGetLastError());
+          CUtensorMap tm;
+          if (tc_make_map(t->q8_bf16, m.N, m.Kp, 128, 1, &tm))
+            return h->fail(FS_ERR_CUDA, "tensor map");
+        }
         FS_CK(h, cudaStreamSynchronize(h->stream));
         return FS_OK;
       }
@@ -758,7 +786,12 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     TcParams p{};
     p.m_tiles = T.m_tiles; p.P = T.P; p.kb_total = W.Kp / 64;
     p.lanes_total = n; p.sms = h->sms;
-    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, h->wtype == W_Q8 ? 32 : 16);
+    const bool q8 = h->wtype == W_Q8;
+    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, q8 ? 32 : 16);
+    // the bf16 copy serves the calls that would dequantise each tile in
+    // q8_copy_groups or more lane groups (same operand bits either way)
+    const bool q8_copy = q8 && T.q8_bf16 && p.groups >= h->q8_copy_groups;
+    if (q8_copy) tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, 16);
     p.tmem_cols = tc_tmem_cols(p.lg);
     // the cluster reduction pays where partial tiles are large or K short;
     // long-K splits of small lane groups sum through the workspace
@@ -769,9 +802,9 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.am_val = h->am_val; p.am_idx = h->am_idx;
     p.split = h->act_split;
     p.lo_off = epi == EPI_SWIGLU ? h->lo_a : 0;
-    const TcOperands o{W.w, W.N, X, d.max_lanes, W.Kp, x_lo};
+    const TcOperands o{q8_copy ? T.q8_bf16 : W.w, W.N, X, d.max_lanes, W.Kp, x_lo};
     h->launch(FS_PROF_GEMM, bytes, [&] {
-      const int r = h->wtype == W_Q8 ? launch_gemm_tc_q8(o, p, s) : launch_gemm_tc(o, p, s);
+      const int r = q8 && !q8_copy ? launch_gemm_tc_q8(o, p, s) : launch_gemm_tc(o, p, s);
       if (r < 0) h->map_fail = true;
       return std::max(r, 0);
     });
@@ -1421,7 +1454,11 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out) {
 const char* fs_gemm_path(const fs_handle* h) {
   if (!h) return "";
   if (!h->use_tc) return "warp-gemv";
-  return h->wtype == W_Q8 ? "tcgen05-q8_0" : "tcgen05";
+  if (h->wtype != W_Q8) return "tcgen05";
+  return h->head_tc.q8_bf16 || (!h->layers.empty() && (h->layers[0].qkv_tc.q8_bf16 ||
+                                                       h->layers[0].gateup_tc.q8_bf16))
+             ? "tcgen05-q8_0+bf16"
+             : "tcgen05-q8_0";
 }
 
 const char* fs_attention_path(const fs_handle* h) {

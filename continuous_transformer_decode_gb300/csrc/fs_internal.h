@@ -403,6 +403,10 @@ int launch_gemm_tc_q8(const TcOperands& o, const TcParams& p, cudaStream_t s);
 // (rows beyond N are zero).
 int launch_tile_q8(const int8_t* codes, const __half* scales, int N, int Kp, int8_t* tiles,
                    cudaStream_t s);
+// Row-major Q8_0 codes [N][Kp] / scales [N][Kp/32] -> bf16 [N][Kp] holding
+// bf16(q * d), the operand value the Q8_0 GEMM dequantises in shared memory.
+int launch_dequant_q8_bf16(const int8_t* codes, const __half* scales, int N, int Kp,
+                           __nv_bfloat16* out, cudaStream_t s);
 
 // x = E[tok]; if g is given also h = RMSNorm(x) * g (x_type panel).
 // lo_off (elements, bf16 panels only; 0: none): the row's rounding

@@ -1062,7 +1062,39 @@ __global__ void k_tile_q8(const int8_t* __restrict__ codes, const __half* __rest
   }
 }
 
+// bf16 copy of a Q8_0 matrix: out[row][k] = bf16(q * d), the value and the
+// rounding dequant_q8_tile gives the same weight inside the GEMM, so either
+// operand source feeds the MMAs the same bits. One thread per 8 inputs.
+__global__ void k_dequant_q8_bf16(const int8_t* __restrict__ codes,
+                                  const __half* __restrict__ scales, int64_t n8, int Kp,
+                                  __nv_bfloat16* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const int64_t e = i * 8;  // first of the thread's 8 inputs (row-major [N][Kp])
+  const int64_t row = e / Kp;
+  const int k = (int)(e % Kp);
+  const float d = __half2float(scales[row * (Kp / 32) + k / 32]);
+  const uint2 u = *reinterpret_cast<const uint2*>(codes + e);
+  const int8_t* q = reinterpret_cast<const int8_t*>(&u);
+  uint4 o;
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn((float)q[2 * j] * d, (float)q[2 * j + 1] * d);
+    ow[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  *reinterpret_cast<uint4*>(out + e) = o;
+}
+
 }  // namespace
+
+int launch_dequant_q8_bf16(const int8_t* codes, const __half* scales, int N, int Kp,
+                           __nv_bfloat16* out, cudaStream_t s) {
+  const int64_t n8 = (int64_t)N * Kp / 8;
+  if (n8 == 0) return 0;
+  k_dequant_q8_bf16<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(codes, scales, n8, Kp, out);
+  return 1;
+}
 
 int launch_gemm_tc(const TcOperands& o, const TcParams& p, cudaStream_t s) {
   return p.split ? launch_impl<false, true>(o, p, s) : launch_impl<false, false>(o, p, s);

@@ -2,6 +2,8 @@
 seeded inputs and collect per-(lane, step) logits."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import oracle.core as O
@@ -22,12 +24,22 @@ def quantize_weights(W: dict) -> dict:
 
 
 def make_gpu(cfg, W, wdtype, kvdtype=fs.FS_DTYPE_BF16, max_lanes=8,
-             max_pos=64, n_pages=None, page_size=16, act_split=0):
+             max_pos=64, n_pages=None, page_size=16, act_split=0, env=None):
+    """env: environment variables set while fs_create reads its knobs."""
     if n_pages is None:
         n_pages = max_lanes * (-(-max_pos // page_size))
     desc = fs.make_desc(cfg, wdtype, kvdtype, max_lanes, n_pages, max_pos,
                         page_size, act_split)
-    return fs.fs_create(desc, W)
+    old = {k: os.environ.get(k) for k in (env or {})}
+    try:
+        os.environ.update(env or {})
+        return fs.fs_create(desc, W)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
 
 def oracle_runs(model, prompts, n_steps, max_pos=64):

@@ -235,7 +235,9 @@ def test_smollm2_q8_full_depth_960_lane_handle(smol):
         feed[b] = seqs[i]
     h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=B, max_pos=32)
     try:
-        assert fs.fs_gemm_path(h) == "tcgen05-q8_0"
+        # 960 lanes cut every layer matrix into many lane groups: the handle
+        # keeps their bf16 copies (bf16(q * d)) and the steps multiply those
+        assert fs.fs_gemm_path(h) == "tcgen05-q8_0+bf16"
         got, pos = gpu_lockstep(h, feed, SAMPLE_960, V)
         worst = check_rows(got, ref)
         for i in range(len(SAMPLE_960)):
@@ -259,6 +261,16 @@ def test_smollm2_q8_full_depth_960_lane_handle(smol):
         for i, b in enumerate(SAMPLE_960):
             nxt[b] = int(np.argmax(ref[i, -1]))
         greedy_step_vs_oracle(h, mq, o_lanes, SAMPLE_960, nxt, B, V, pos, worst)
+    finally:
+        fs.fs_destroy(h)
+    # the same steps with every GEMM dequantising its Q8_0 tiles in shared
+    # memory: the same operand values, so the same bits at full depth
+    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=B, max_pos=32,
+                   env={"FS_Q8_BF16_GROUPS": "0"})
+    try:
+        assert fs.fs_gemm_path(h) == "tcgen05-q8_0"
+        got_tiles, _ = gpu_lockstep(h, feed, SAMPLE_960, V)
+        assert np.array_equal(got_tiles.view(np.uint32), got.view(np.uint32))
     finally:
         fs.fs_destroy(h)
 

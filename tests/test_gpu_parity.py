@@ -411,14 +411,19 @@ def test_mistral_shape_long_ragged_context_parity(mistral_l2):
         fs.fs_destroy(h)
 
 
-def test_smollm2_q8_tensor_core_path_batch_invariance(smol_l2):
+@pytest.mark.parametrize("copies", [True, False])
+def test_smollm2_q8_tensor_core_path_batch_invariance(smol_l2, copies):
     """Q8_0 weights on the tensor-core path: a lane's logits do not change
-    bits with the batch it runs in (B = 1, 5, 40)."""
+    bits with the batch it runs in (B = 1, 5, 40). With the handle's bf16
+    copies (copies=True), B = 1 and 5 dequantise the Q8_0 tiles inside the
+    GEMMs while B = 40 (two lane groups) multiplies the copies of the layer
+    matrices: the two operand sources give the same bits."""
     cfg, Wb, m = smol_l2
     Wq = U.quantize_weights(Wb)
-    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=40, max_pos=32)
+    h = U.make_gpu(cfg, Wq, fs.FS_DTYPE_Q8_0, max_lanes=40, max_pos=32,
+                   env=None if copies else {"FS_Q8_BF16_GROUPS": "0"})
     try:
-        assert fs.fs_gemm_path(h) == "tcgen05-q8_0"
+        assert fs.fs_gemm_path(h) == ("tcgen05-q8_0+bf16" if copies else "tcgen05-q8_0")
         seq = [int(t) for t in synth.make_prompts(1, 6, cfg["V"], seed=15)[0]]
         base = U.gpu_teacher_forced(h, cfg, [7], [seq], cfg["V"])[0]
         for B in (5, 40):
