@@ -308,9 +308,12 @@ struct TcParams {
 // launch (lowest index on ties): tokens_out[b] for b < B.
 int launch_argmax_tiles(const float* am_val, const int* am_idx, int B, int m_tiles,
                         int32_t* tokens_out, cudaStream_t s);
-// Lanes per group of one tcgen05 GEMM call: at most 256 (the MMA's N
-// limit); a matrix with fewer stream-K blocks than SMs is spread over more
-// groups of at least 32 lanes to fill about two blocks per SM. Groups split
+// Lanes per group of one tcgen05 GEMM call: at most tc_lg_max(); a matrix
+// with fewer stream-K blocks than SMs is spread over more groups to fill
+// about two blocks per SM, groups of at least lg_min lanes and of at least
+// n/16 (rounded up to 16: at most about 16 groups per row tile; SmolLM2 at
+// 960 lanes measured 1.70 ms per step with 64-lane groups against 1.84 with
+// 32 and 1.90 with 128; up to 256 lanes this leaves lg_min). Groups split
 // N only, so this may depend on the call's lane count.
 // FS_TC_LG_MIN (16..256, a tuning knob read once) overrides the smallest
 // lane group the fill rule may cut (0: the caller's value).
@@ -352,7 +355,7 @@ inline void tc_lane_groups(int n, int P, int sms, int* lg, int* groups, int lg_m
   int g = (n + cap - 1) / cap;
   if (P < sms) {
     const int fill = std::max(1, tc_fill_per_sm() * sms / P);
-    const int m = tc_lg_min(lg_min);
+    const int m = std::max(tc_lg_min(lg_min), (n + 255) / 256 * 16);
     g = std::max(g, std::min(fill, std::max(1, (n + m - 1) / m)));
   }
   const int l = ((n + g - 1) / g + 15) / 16 * 16;
