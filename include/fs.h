@@ -341,14 +341,14 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out);
 /* Name of the GEMM path serving the handle's weight matrices: "tcgen05"
  * (bf16 weights on the tensor cores), "tcgen05-q8_0" (Q8_0 weights,
  * dequantised to bf16 in shared memory inside the GEMM), "tcgen05-q8_0+bf16"
- * or "warp-gemv". A Q8_0 handle whose lane capacity cuts a matrix's GEMM into
- * two or more lane groups (each of which would dequantise every weight tile)
- * also keeps that matrix as bf16(q * d), converted once by fs_create (2 bytes
- * per weight on top of the Q8_0 tiles); calls of that many groups multiply
- * the copy, the same operand bits. The environment variable
- * FS_Q8_BF16_GROUPS, read by fs_create, sets that group count (default 2; 0
- * keeps no copies). FS_GEMM_PATH=gemv, also read by fs_create, selects the
- * warp-GEMV path for bf16 weights too (a comparison point). */
+ * or "warp-gemv" (f32 weights, d_ffn not a multiple of 64, or a device
+ * without tcgen05). A Q8_0 handle whose lane capacity cuts a matrix's GEMM
+ * into two or more lane groups (each of which would dequantise every weight
+ * tile) also keeps that matrix as bf16(q * d), converted once by fs_create
+ * (2 bytes per weight on top of the Q8_0 tiles); calls of that many groups
+ * multiply the copy, the same operand bits ("tcgen05-q8_0+bf16"). The
+ * environment variable FS_Q8_BF16_GROUPS, read by fs_create, sets that group
+ * count (default 2; 0 keeps no copies). */
 const char* fs_gemm_path(const fs_handle* h);
 
 /* Name of the decode-attention kernel serving the handle: "tma-mma" (KV
