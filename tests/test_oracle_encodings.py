@@ -44,7 +44,8 @@ def _f32_samples(n=40000, seed=0):
 
 def test_f32_to_f16_matches_numpy_rne():
     x = _f32_samples()
-    ref = x.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # the samples include values beyond fp16's range
+        ref = x.astype(np.float16).view(np.uint16)
     got = np.array([O.f32_to_f16(float(v)) for v in x], dtype=np.uint16)
     bad = np.nonzero(got != ref)[0]
     assert bad.size == 0, [(x[i], hex(got[i]), hex(ref[i])) for i in bad[:5]]
