@@ -114,6 +114,34 @@ int choose_width(int m_tiles, int kb_total, int max_lanes, int sms) {
   s = std::min(s, std::min(8, cap));
   return m_tiles * std::max(1, s);
 }
+
+// FS_Q8_BF16_GROUPS (read at create): the lane-group count from which a Q8_0
+// GEMM call multiplies the matrix's bf16 copy (default 2; 0: no copies).
+int q8_copy_groups_env() {
+  const char* e = getenv("FS_Q8_BF16_GROUPS");
+  return e ? std::max(0, atoi(e)) : 2;
+}
+
+// Every lane group of a Q8_0 GEMM dequantises each weight tile it
+// multiplies, so a call of g groups converts the matrix g times. A Q8_0
+// handle of B lanes keeps a bf16 copy of a matrix of stream-K width P when a
+// call of all B lanes would run copy_groups or more Q8_0 lane groups.
+bool q8_keeps_copy(int B, int P, int sms, int copy_groups) {
+  int lg = 0, groups = 1;
+  tc_lane_groups(B, P, sms, &lg, &groups, 32);
+  return copy_groups > 0 && groups >= copy_groups;
+}
+
+// Lane groups of one GEMM call of n lanes. Q8_0 groups take at least 32
+// lanes; a Q8_0 call that would run copy_groups or more of them multiplies
+// the matrix's bf16 copy when it has one (*use_copy) and is then grouped as a
+// bf16 call (the same operand bits either way).
+void gemm_call_groups(int n, int P, int sms, bool q8, bool has_copy, int copy_groups, int* lg,
+                      int* groups, bool* use_copy) {
+  tc_lane_groups(n, P, sms, lg, groups, q8 ? 32 : 16);
+  *use_copy = q8 && has_copy && *groups >= copy_groups;
+  if (*use_copy) tc_lane_groups(n, P, sms, lg, groups, 16);
+}
 }  // namespace
 
 struct fs_handle {
@@ -404,10 +432,7 @@ int create_impl(fs_handle* h, const fs_weights* W) {
     h->act_split = d.act_split;
     const char* genv = getenv("FS_GRAPHS");
     h->graphs_on = !(genv && std::string(genv) == "0");
-    // FS_Q8_BF16_GROUPS (read at create): the lane-group count from which a
-    // Q8_0 GEMM runs on its bf16 copy; 0 keeps no copies (comparison knob)
-    const char* qenv = getenv("FS_Q8_BF16_GROUPS");
-    if (qenv) h->q8_copy_groups = std::max(0, atoi(qenv));
+    h->q8_copy_groups = q8_copy_groups_env();
   }
 
   FS_CK(h, cudaStreamCreateWithFlags(&h->own_stream, cudaStreamDefault));
@@ -619,14 +644,10 @@ int create_impl(fs_handle* h, const fs_weights* W) {
         h->launches += launch_tile_q8((const int8_t*)m.w, m.scales, m.N, m.Kp, t->q8_tiles,
                                       h->stream);
         FS_CK(h, cudaGetLastError());
-        // Every lane group of a Q8_0 GEMM dequantises each weight tile it
-        // multiplies, so a call of g groups converts the matrix g times.
-        // Where the lane capacity reaches q8_copy_groups groups the handle
-        // also keeps the matrix in bf16, converted once here: such calls
-        // stream 16 instead of 8.5 KB per tile and convert nothing.
-        int lg = 0, groups = 1;
-        tc_lane_groups(B, t->P, h->sms, &lg, &groups, 32);
-        if (h->q8_copy_groups > 0 && groups >= h->q8_copy_groups) {
+        // where the lane capacity reaches q8_copy_groups lane groups the
+        // handle also keeps the matrix in bf16, converted once here: such
+        // calls stream 16 instead of 8.5 KB per tile and convert nothing
+        if (q8_keeps_copy(B, t->P, h->sms, h->q8_copy_groups)) {
           if (h->alloc(&t->q8_bf16, (size_t)m.N * m.Kp * 2) != cudaSuccess)
             return h->fail(FS_ERR_OOM, "Q8_0 bf16 copy allocation failed");
           h->launches += launch_dequant_q8_bf16((const int8_t*)m.w, m.scales, m.N, m.Kp,
@@ -787,11 +808,9 @@ void enqueue_step(fs_handle* h, int n, float* out, double kv_read, bool chunked,
     p.m_tiles = T.m_tiles; p.P = T.P; p.kb_total = W.Kp / 64;
     p.lanes_total = n; p.sms = h->sms;
     const bool q8 = h->wtype == W_Q8;
-    tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, q8 ? 32 : 16);
-    // the bf16 copy serves the calls that would dequantise each tile in
-    // q8_copy_groups or more lane groups (same operand bits either way)
-    const bool q8_copy = q8 && T.q8_bf16 && p.groups >= h->q8_copy_groups;
-    if (q8_copy) tc_lane_groups(n, T.P, h->sms, &p.lg, &p.groups, 16);
+    bool q8_copy = false;  // the bf16 copy serves this call
+    gemm_call_groups(n, T.P, h->sms, q8, T.q8_bf16 != nullptr, h->q8_copy_groups, &p.lg,
+                     &p.groups, &q8_copy);
     p.tmem_cols = tc_tmem_cols(p.lg);
     // the cluster reduction pays where partial tiles are large or K short;
     // long-K splits of small lane groups sum through the workspace
@@ -1459,6 +1478,34 @@ const char* fs_gemm_path(const fs_handle* h) {
                                                        h->layers[0].gateup_tc.q8_bf16))
              ? "tcgen05-q8_0+bf16"
              : "tcgen05-q8_0";
+}
+
+int fs_gemm_plan(int64_t n_rows, int64_t k_inputs, int max_lanes, int n, int sms,
+                 int weight_dtype, int32_t* out) {
+  if (!out || n_rows < 1 || k_inputs < 1 || k_inputs % 32 || max_lanes < 1 || n < 1 ||
+      n > max_lanes || sms < 1 || weight_dtype < FS_DTYPE_BF16 ||
+      weight_dtype > FS_DTYPE_Q8_0 || n_rows > ((int64_t)1 << 30) ||
+      k_inputs > ((int64_t)1 << 30))
+    return FS_ERR_ARG;
+  const int m_tiles = (int)((n_rows + 127) / 128);
+  const int kb_total = (int)(round_up(k_inputs, 64) / 64);
+  const int P = choose_width(m_tiles, kb_total, max_lanes, sms);
+  if (!tc_width_ok(m_tiles, kb_total, P)) return FS_ERR_ARG;
+  const bool q8 = weight_dtype == FS_DTYPE_Q8_0;
+  const int copy_groups = q8_copy_groups_env();
+  const bool kept = q8 && q8_keeps_copy(max_lanes, P, sms, copy_groups);
+  int lg = 0, groups = 1;
+  bool use_copy = false;
+  gemm_call_groups(n, P, sms, q8, kept, copy_groups, &lg, &groups, &use_copy);
+  out[0] = P;
+  out[1] = lg;
+  out[2] = groups;
+  out[3] = tc_tmem_cols(lg);
+  out[4] = kept ? 1 : 0;
+  out[5] = use_copy ? 1 : 0;
+  out[6] = m_tiles;
+  out[7] = kb_total;
+  return FS_OK;
 }
 
 const char* fs_attention_path(const fs_handle* h) {

@@ -124,6 +124,7 @@ def lib():
         "fs_profile_read": (C.c_int, [p, i32, p, p, p]),
         "fs_kernel_launches": (C.c_int, [p, p]),
         "fs_gemm_path": (C.c_char_p, [p]),
+        "fs_gemm_plan": (C.c_int, [i64, i64, i32, i32, i32, i32, p]),
         "fs_lane_capacity": (C.c_int, [p, p]),
         "fs_attention_path": (C.c_char_p, [p]),
         "fs_device_error": (C.c_int, [p, p]),
@@ -161,7 +162,7 @@ def exported_symbols() -> list:
             "fs_lane_reset", "fs_lane_clone", "fs_lane_evict", "fs_trace_enable", "fs_trace_read", "fs_selftest_bounded_wait", "fs_decode_step_batch", "fs_step_batch_chunked", "fs_decode_step_greedy", "fs_sample",
             "fs_lane_length", "fs_lane_pages", "fs_lane_export_kv",
             "fs_lane_import_kv", "fs_lane_fill_random_kv", "fs_quantize_q8_0",
-            "fs_kernel_launches", "fs_gemm_path", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
+            "fs_kernel_launches", "fs_gemm_path", "fs_gemm_plan", "fs_lane_capacity", "fs_attention_path", "fs_sample_device",
             "fs_profile_enable", "fs_profile_read", "fs_device_error",
             "fs_gemm_bf16", "fs_gemm_bf16_width", "fs_gemm_bf16_time", "fs_copy_logits", "fs_gemm_bf16_noalloc",
             "fs_sched_create", "fs_sched_create_model_free", "fs_sched_destroy",
@@ -416,6 +417,18 @@ def fs_kernel_launches(h) -> int:
 
 def fs_gemm_path(h) -> str:
     return lib().fs_gemm_path(h).decode()
+
+
+PLAN_KEYS = ("P", "lanes_per_group", "groups", "tmem_cols", "q8_copy_kept",
+             "q8_copy_used", "m_tiles", "k_blocks")
+
+
+def fs_gemm_plan(n_rows: int, k_inputs: int, max_lanes: int, n: int, sms: int,
+                 weight_dtype: int) -> dict:
+    """The tcgen05 GEMM's work split for one matrix and call (host only)."""
+    out = (C.c_int32 * 8)()
+    _check(None, lib().fs_gemm_plan(n_rows, k_inputs, max_lanes, n, sms, weight_dtype, out))
+    return dict(zip(PLAN_KEYS, [int(v) for v in out]))
 
 
 def fs_attention_path(h) -> str:

@@ -351,6 +351,25 @@ int fs_kernel_launches(const fs_handle* h, int64_t* count_out);
  * count (default 2; 0 keeps no copies). */
 const char* fs_gemm_path(const fs_handle* h);
 
+/* Work split of the tcgen05 GEMM for one weight matrix, as fs_create and the
+ * decode step choose it (host arithmetic only: no device, handle or CUDA call;
+ * a test and tuning hook). n_rows x k_inputs is the matrix (k_inputs a
+ * multiple of 32), max_lanes the handle's lane capacity, n the call's lanes
+ * (1 <= n <= max_lanes), sms the device's SM count, weight_dtype
+ * FS_DTYPE_BF16 or FS_DTYPE_Q8_0. Writes out[8] (host):
+ *   out[0] P, the stream-K width: blocks per lane group, a whole number of
+ *          K splits of every 128-row tile; fixed per handle, never dependent
+ *          on n (a lane's bits do not depend on its batch)
+ *   out[1] lanes per group (the MMA's N), out[2] lane groups,
+ *   out[3] TMEM columns a block allocates,
+ *   out[4] 1 when a Q8_0 handle keeps a bf16 copy of the matrix,
+ *   out[5] 1 when this call multiplies that copy,
+ *   out[6] 128-row tiles, out[7] 64-wide k-blocks.
+ * Reads the environment knobs fs_create reads for these choices.
+ * Errors: FS_ERR_ARG (sizes, dtype, or a matrix too large for the GEMM). */
+int fs_gemm_plan(int64_t n_rows, int64_t k_inputs, int max_lanes, int n, int sms,
+                 int weight_dtype, int32_t* out);
+
 /* Name of the decode-attention kernel serving the handle: "tma-mma" (KV
  * tiles by TMA, warp MMAs; bf16 KV, page_size a multiple of 8 that divides
  * or is a multiple of 64), "cp.async-mma" (KV tiles by cp.async, warp MMAs;
