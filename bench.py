@@ -497,6 +497,27 @@ def fs_path_name(cfg, wdt):
     return {0: "f32", 1: "bf16", 2: "q8_0"}[wdt] + " weights"
 
 
+def workload_config(args, wl, B, ws):
+    """The workload's `config` record, the same dict for both arms: the model
+    shape, lanes, context and what the step streams."""
+    from continuous_transformer_decode_gb300 import synth
+    cfg = model_cfg(wl["model"])
+    if args.layers:
+        cfg = synth.with_layers(cfg, args.layers)
+    wbytes = {"bf16": 2, "q8_0": 34 / 32}[wl["wdtype"]]
+    weight_mb = step_roofline(cfg, wbytes, 0, 0, _peaks())["bytes_per_step"] / 1e6
+    if "ctx" in wl:  # the lanes' context lengths: the draw make_handle makes
+        ctx = synth.make_context_lengths(B, *wl["ctx"], seed=3)
+        context = f"ctx U[{wl['ctx'][0]},{wl['ctx'][1]}] mean {float(np.mean(ctx)):.0f}"
+    else:
+        context = f"16-token prompts, positions 16..{16 + args.warmup + args.steps}"
+    return {"workload": args.workload, "model_shape": cfg["name"], "lanes": B,
+            "layers": cfg["L"], "d": cfg["d"], "vocab": cfg["V"], "context": context,
+            "l2": f"no flush: inputs larger than L2 ({weight_mb:.0f} MB of weights "
+                  "streamed per step vs 129 MB L2)",
+            "parallelism": f"replicas x{ws}"}
+
+
 class OracleArm:
     """The oracle as it stands, on this host's cores: StepBatch over a bounded
     number of the workload's lanes (up to 32), after seeding each lane with
@@ -736,7 +757,7 @@ def main():
                           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                           "dtype": "f32", "data": "synthetic",
-                          "config": {"workload": args.workload, "lanes": B},
+                          "config": workload_config(args, wl, B, ws),
                           "cpu_baseline": cb,
                           "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}))
@@ -759,9 +780,6 @@ def main():
     cb = None if args.no_cpu_baseline else cpu_baseline(wl, r["B"])
     cfg = r["cfg"]
     wbytes = {"bf16": 2, "q8_0": 34 / 32}[wl["wdtype"]]
-    n_par = cfg["V"] * cfg["d"] * (1 if cfg["tied"] else 2) + cfg["L"] * (
-        (cfg["H"] * cfg["hd"] * 2 + cfg["Hkv"] * cfg["hd"] * 2) * cfg["d"] + 3 * cfg["F"] * cfg["d"])
-    weight_mb = n_par * wbytes / 1e6
     peaks = _peaks()
     ctx_mean = float(np.mean(r["ctx"])) + args.warmup + args.steps / 2.0
     sr = step_roofline(cfg, wbytes, r["B"], ctx_mean, peaks)
@@ -770,14 +788,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl["wdtype"], "data": "synthetic (random N(0,0.02) weights, uniform prompts)",
-        "config": {"workload": args.workload, "model_shape": cfg["name"], "lanes": r["B"],
-                   "layers": cfg["L"], "d": cfg["d"], "vocab": cfg["V"],
-                   "context": (f"16-token prompts, positions 16..{16 + args.warmup + args.steps}"
-                               if "ctx" not in wl else
-                               f"ctx U[{wl['ctx'][0]},{wl['ctx'][1]}] mean {float(np.mean(r['ctx'])):.0f}"),
-                   "l2": f"no flush: inputs larger than L2 ({weight_mb:.0f} MB of weights "
-                         "streamed per step vs 129 MB L2)",
-                   "parallelism": f"replicas x{ws}"},
+        "config": workload_config(args, wl, r["B"], ws),
         "roofline": dict(r["roofline"], traffic=traffic_for("k_gemm_tc.cu", args.workload, r["B"])),
         "step_roofline": dict(sr, frac=r["value"] / ws / sr["tok_s_ceiling"], peak_source=peaks["src"]),
         "sweep": [dict(p, frac_of_step_roofline=p["tok_s"] / step_roofline(
